@@ -1,0 +1,241 @@
+/*
+ * csp.h — cascade attention over a shared-prefix paged KV cache (C ABI).
+ *
+ * The library (libcsp_gb300.so, built for sm_103a) exposes the steps of
+ * cascade attention as described on "vLLM Cascade Attention：用法、场景与原理解析"
+ * (beaiera.top):
+ *   - cascade_plan   : §八 Step 1-2 and §三 — the common-prefix planner and the
+ *                      use-cascade decision (host only);
+ *   - cascade_attn   : §一, §四 and §八 Step 5 — prefix phase (every query of the
+ *                      batch, non-causal, over the shared KV pages), suffix phase
+ *                      (each request, causal, over its own KV pages) and the LSE
+ *                      merge, in one call;
+ *   - paged_attn     : §五 and §十 — the standard (flat) path, each request over
+ *                      all of its KV pages, causal;
+ *   - merge_states   : §一 and §八 Step 5 (merge_attn_states) — the LSE merge of
+ *                      two partial results.
+ * Running-set semantics follow "fix(v1/kv_cache): resolve async KV transfer bug
+ * in cascade attention #23485": the planner sees exactly the rows passed in, which
+ * must be the requests that are running.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * Layouts (row-major, contiguous, no padding between rows):
+ *   q        bf16  [total_q, num_q_heads, head_dim]   queries of all requests, request
+ *                                                    r owning rows cu_seqlens_q[r] ..
+ *                                                    cu_seqlens_q[r+1]-1
+ *   k_cache, v_cache
+ *            bf16  [num_blocks, block_size, num_kv_heads, head_dim]
+ *   block_table int32 [num_reqs, bt_row_stride]      physical block of each logical
+ *                                                    page; only the first
+ *                                                    cdiv(seqused_k[r], block_size)
+ *                                                    entries of row r are read
+ *   cu_seqlens_q int32 [num_reqs + 1], cu_seqlens_q[0] = 0, nondecreasing
+ *   seqused_k    int32 [num_reqs]  KV length of each request, including this step's
+ *                                  query tokens (queries are the last q_len positions)
+ *   out      bf16  [total_q, num_q_heads, head_dim]
+ *   lse      fp32  [total_q, num_q_heads]  natural log of sum_j exp(scale * q.k_j)
+ * Query head h reads KV head h / (num_q_heads / num_kv_heads).  Query i of request r
+ * sits at absolute position seqused_k[r] - q_len_r + i and sees keys at positions
+ * <= its own (bottom-right causal alignment).
+ *
+ * Supported shapes: head_dim 64 or 128; block_size 16; num_q_heads a multiple of
+ * num_kv_heads with a group size (num_q_heads / num_kv_heads) of 1, 2, 4, 8 or 16.
+ * Anything else returns CSP_ERR_UNSUPPORTED without launching.
+ *
+ * Ownership: every pointer is owned by the caller.  The library allocates nothing,
+ * frees nothing and keeps no pointer after a call returns.  Device pointers must
+ * stay valid until the work queued on `stream` has finished.
+ *
+ * Asynchrony: device entry points queue kernels on `stream` (a cudaStream_t; NULL
+ * is the legacy default stream) and return without synchronising.
+ *
+ * Errors: a negative return value means nothing was launched (argument errors), or
+ * that a launch failed (CSP_ERR_CUDA, with the CUDA error kept for
+ * csp_last_cuda_error()).  No C++ exception crosses the ABI.  Kernels never trap:
+ * a wait inside a kernel that runs out of time writes CSP_ERR_TIMEOUT into the
+ * workspace status word (see csp_workspace_status) and the kernel returns.
+ *
+ * Thread safety: calls may be made from several host threads at once on different
+ * workspaces.  Two calls that share a workspace must be ordered on one stream.
+ */
+#ifndef CSP_H_
+#define CSP_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define CSP_API __attribute__((visibility("default")))
+#else
+#define CSP_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  CSP_OK = 0,
+  CSP_ERR_INVALID_ARG = -1,  /* null pointer, negative size, inconsistent shapes  */
+  CSP_ERR_UNSUPPORTED = -2,  /* head_dim / block_size / group size not built       */
+  CSP_ERR_WORKSPACE = -3,    /* workspace missing, too small or misaligned          */
+  CSP_ERR_CUDA = -4,         /* a CUDA call or launch failed                        */
+  CSP_ERR_TIMEOUT = -6       /* device-side: a bounded wait inside a kernel gave up */
+} csp_status;
+
+/* cascade_plan modes. */
+enum {
+  CSP_MODE_AUTO = 0,            /* the GB300 cost model decides                        */
+  CSP_MODE_FORCE_CASCADE = 1,   /* use cascade whenever common_prefix_len > 0          */
+  CSP_MODE_FORCE_FLAT = 2,      /* never use cascade                                   */
+  CSP_MODE_PAGE_THRESHOLDS = 3  /* the pages' rule only: prefix >= 256 and batch >= 8  */
+};
+
+/* Element type of the partial results given to merge_states. */
+enum { CSP_DTYPE_BF16 = 0, CSP_DTYPE_F32 = 1 };
+
+/*
+ * cascade_plan — common prefix of the running batch and the use-cascade decision.
+ * Host pointers only; no device work.
+ *
+ * Follows §八 Step 1 (longest run, from block 0, of physical block ids shared by
+ * every row), §八 Step 2 (common_prefix_len = blocks * block_size, capped to
+ * min(num_computed_tokens), floored to a multiple of block_size; the cap keeps the
+ * non-causal prefix phase from seeing a later token, §四), and §三 (no cascade for
+ * a prefix under 256 tokens or fewer than 8 requests).  Row r takes part only with
+ * its first cdiv(seq_lens[r], block_size) entries; the scan stops at the first
+ * mismatch.
+ *
+ *   block_table          int32 [num_reqs, bt_row_stride]  host
+ *   seq_lens             int32 [num_reqs]  host, KV length incl. this step's queries
+ *   num_computed_tokens  int32 [num_reqs]  host, seq_lens minus this step's queries
+ *   num_q_heads, num_kv_heads, head_dim   shape of the attention (cost model input)
+ *   num_sms              SM count for the cost model (<= 0: 148)
+ *   mode                 CSP_MODE_*
+ *   common_prefix_len_out  receives the capped, floored prefix length (tokens)
+ *   use_cascade_out        receives 1 to take cascade_attn, 0 for paged_attn
+ * num_reqs == 0 gives 0 / 0.  Returns CSP_OK or CSP_ERR_INVALID_ARG.
+ */
+CSP_API int cascade_plan(const int32_t* block_table, int64_t bt_row_stride, int32_t num_reqs,
+                 const int32_t* seq_lens, const int32_t* num_computed_tokens,
+                 int32_t block_size, int32_t num_q_heads, int32_t num_kv_heads,
+                 int32_t head_dim, int32_t num_sms, int32_t mode,
+                 int32_t* common_prefix_len_out, int32_t* use_cascade_out);
+
+/*
+ * csp_workspace_size — bytes of device workspace that cascade_attn (with this
+ * common_prefix_len) or paged_attn (common_prefix_len = 0) needs for this batch
+ * shape on the current device.  All arguments are host integers, the same as the
+ * attention call will get.  The workspace holds the split partial results and a
+ * status word; it must be 256-byte aligned and zero-filled before its first use.
+ * Returns CSP_OK and writes *bytes_out, or CSP_ERR_INVALID_ARG / CSP_ERR_CUDA.
+ */
+CSP_API int csp_workspace_size(int32_t num_reqs, int32_t total_q, int32_t max_seqlen_q,
+                       int32_t max_seqlen_k, int32_t common_prefix_len, int32_t num_q_heads,
+                       int32_t num_kv_heads, int32_t head_dim, size_t* bytes_out);
+
+/*
+ * cascade_attn — cascade attention for one batch (§八 Step 5).
+ *
+ * Prefix phase: all total_q queries, as one sequence, attend without a causal mask
+ * to KV positions [0, common_prefix_len), read through row 0 of block_table (the
+ * rows share these pages; that is what the planner established).  Suffix phase:
+ * request r attends causally to KV positions [common_prefix_len, seqused_k[r]),
+ * read through its own row starting at page common_prefix_len / block_size.  The
+ * two partial results are merged by LSE rescaling into out (bf16) and lse.
+ *
+ *   q, k_cache, v_cache, block_table, cu_seqlens_q, seqused_k, out  device pointers,
+ *                        layouts as above
+ *   num_blocks           first dimension of k_cache / v_cache
+ *   num_reqs, total_q    host copies of the batch size and cu_seqlens_q[num_reqs]
+ *   max_seqlen_q         host: max over r of the query count of request r
+ *   max_seqlen_k         host: max over r of seqused_k[r]
+ *   common_prefix_len    multiple of block_size, and at most min over r of
+ *                        (seqused_k[r] - q_len_r) — cascade_plan gives such a value;
+ *                        0 computes the standard result
+ *   softmax_scale        multiplies q.k before the softmax
+ *   lse                  device pointer or NULL (not written)
+ *   workspace            device, >= csp_workspace_size(...) bytes, 256-byte aligned
+ *   stream               cudaStream_t
+ * Results equal paged_attn's up to rounding (the pages state the two are
+ * mathematically the same, §一).
+ */
+CSP_API int cascade_attn(const void* q, const void* k_cache, const void* v_cache, int32_t num_blocks,
+                 const int32_t* block_table, int64_t bt_row_stride, const int32_t* cu_seqlens_q,
+                 const int32_t* seqused_k, int32_t num_reqs, int32_t total_q,
+                 int32_t max_seqlen_q, int32_t max_seqlen_k, int32_t common_prefix_len,
+                 int32_t block_size, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                 float softmax_scale, void* out, float* lse, void* workspace,
+                 size_t workspace_bytes, void* stream);
+
+/*
+ * cascade_attn_timed — cascade_attn plus four CUDA events recorded on `stream`
+ * between its kernels, for timing each phase: phase_events[0] before the
+ * prefix-phase kernel, [1] after it, [2] after the suffix-phase kernel, [3] after
+ * the merge kernel.  phase_events is a host array of four cudaEvent_t created by
+ * the caller (with timing enabled).  Arguments and results are otherwise those of
+ * cascade_attn; with common_prefix_len == 0, events [0] and [1] mark the same point.
+ */
+CSP_API int cascade_attn_timed(const void* q, const void* k_cache, const void* v_cache,
+                               int32_t num_blocks, const int32_t* block_table,
+                               int64_t bt_row_stride, const int32_t* cu_seqlens_q,
+                               const int32_t* seqused_k, int32_t num_reqs, int32_t total_q,
+                               int32_t max_seqlen_q, int32_t max_seqlen_k,
+                               int32_t common_prefix_len, int32_t block_size,
+                               int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                               float softmax_scale, void* out, float* lse, void* workspace,
+                               size_t workspace_bytes, void* stream,
+                               void* const* phase_events);
+
+/*
+ * paged_attn — the standard path (§五, §十): request r attends causally to all of
+ * its KV positions [0, seqused_k[r]) through its own block_table row.  Arguments
+ * as for cascade_attn, without common_prefix_len.
+ */
+CSP_API int paged_attn(const void* q, const void* k_cache, const void* v_cache, int32_t num_blocks,
+               const int32_t* block_table, int64_t bt_row_stride, const int32_t* cu_seqlens_q,
+               const int32_t* seqused_k, int32_t num_reqs, int32_t total_q, int32_t max_seqlen_q,
+               int32_t max_seqlen_k, int32_t block_size, int32_t num_q_heads,
+               int32_t num_kv_heads, int32_t head_dim, float softmax_scale, void* out,
+               float* lse, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * merge_states — LSE merge of two partial attention results over disjoint key sets
+ * (merge_attn_states, §一 and §八 Step 5):
+ *   m = max(l1, l2); out = (e^(l1-m) o1 + e^(l2-m) o2) / (e^(l1-m) + e^(l2-m));
+ *   out_lse = m + ln(e^(l1-m) + e^(l2-m)).
+ * Rows where both lse are -inf give out = 0 and out_lse = -inf.
+ *
+ *   out          device bf16 [num_tokens, num_heads, head_dim]
+ *   out_lse      device fp32 [num_tokens, num_heads] or NULL
+ *   prefix_out, suffix_out   device, [num_tokens, num_heads, head_dim] of partial_dtype
+ *   prefix_lse, suffix_lse   device fp32 [num_tokens, num_heads], natural log
+ *   partial_dtype            CSP_DTYPE_BF16 or CSP_DTYPE_F32
+ * head_dim must be a multiple of 8 and at most 512.
+ */
+CSP_API int merge_states(void* out, float* out_lse, const void* prefix_out, const float* prefix_lse,
+                 const void* suffix_out, const float* suffix_lse, int32_t num_tokens,
+                 int32_t num_heads, int32_t head_dim, int32_t partial_dtype, void* stream);
+
+/*
+ * csp_workspace_status — copies the workspace status word to the host (a blocking
+ * copy on `stream`).  0 means no kernel reported a problem since the workspace was
+ * zero-filled; CSP_ERR_TIMEOUT means a bounded wait gave up.  Writes *status_out.
+ */
+CSP_API int csp_workspace_status(const void* workspace, void* stream, int32_t* status_out);
+
+/* Human-readable name of a csp_status value (static string). */
+CSP_API const char* csp_status_string(int status);
+
+/* The CUDA error code behind the last CSP_ERR_CUDA returned on this host thread. */
+CSP_API int csp_last_cuda_error(void);
+
+/* ABI version: (major << 16) | minor. */
+CSP_API int csp_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CSP_H_ */

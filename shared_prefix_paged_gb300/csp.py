@@ -1,0 +1,224 @@
+"""ctypes binding of libcsp_gb300.so (include/csp.h).
+
+Argument marshalling only: every step of the computation runs in the library's
+CUDA kernels (or, for ``cascade_plan``, its host C code).  PyTorch supplies device
+memory and the current stream.  If the library cannot be loaded the first call
+raises; there is no fallback of any kind.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional
+
+import numpy as np
+
+from . import build as _build
+
+CSP_OK = 0
+CSP_ERR_INVALID_ARG = -1
+CSP_ERR_UNSUPPORTED = -2
+CSP_ERR_WORKSPACE = -3
+CSP_ERR_CUDA = -4
+CSP_ERR_TIMEOUT = -6
+
+MODE_AUTO, MODE_FORCE_CASCADE, MODE_FORCE_FLAT, MODE_PAGE_THRESHOLDS = 0, 1, 2, 3
+DTYPE_BF16, DTYPE_F32 = 0, 1
+
+# every symbol include/csp.h declares
+EXPORTS = ("cascade_plan", "csp_workspace_size", "cascade_attn", "cascade_attn_timed",
+           "paged_attn", "merge_states", "csp_workspace_status", "csp_status_string",
+           "csp_last_cuda_error", "csp_version")
+
+_lock = threading.Lock()
+_lib: Optional[ctypes.CDLL] = None
+
+
+class CspError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        lib = _lib
+        name = lib.csp_status_string(status).decode() if lib else str(status)
+        extra = ""
+        if status == CSP_ERR_CUDA and lib:
+            extra = f" (cudaError {lib.csp_last_cuda_error()})"
+        super().__init__(f"{what} failed: {name}{extra}")
+        self.status = status
+
+
+def library_path() -> str:
+    return _build.lib_path()
+
+
+def load(build_if_missing: bool = True) -> ctypes.CDLL:
+    """Open the library (building it first if it is missing or stale and nvcc exists)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = library_path()
+        if build_if_missing and (not os.path.exists(path) or _build.is_stale()):
+            _build.build()
+        if not os.path.exists(path):
+            raise RuntimeError(f"CUDA library missing: {path} (run the build first)")
+        lib = ctypes.CDLL(path)
+        p, i32, i64, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
+        lib.cascade_plan.argtypes = [p, i64, i32, p, p, i32, i32, i32, i32, i32, i32, p, p]
+        lib.csp_workspace_size.argtypes = [i32, i32, i32, i32, i32, i32, i32, i32, p]
+        attn = [p, p, p, i32, p, i64, p, p, i32, i32, i32, i32]
+        tail = [i32, i32, i32, i32, ctypes.c_float, p, p, p, sz, p]
+        lib.cascade_attn.argtypes = attn + [i32] + tail
+        lib.cascade_attn_timed.argtypes = attn + [i32] + tail + [p]
+        lib.paged_attn.argtypes = attn + tail
+        lib.merge_states.argtypes = [p, p, p, p, p, p, i32, i32, i32, i32, p]
+        lib.csp_workspace_status.argtypes = [p, p, p]
+        lib.csp_status_string.argtypes = [ctypes.c_int]
+        lib.csp_status_string.restype = ctypes.c_char_p
+        for name in ("cascade_plan", "csp_workspace_size", "cascade_attn", "cascade_attn_timed",
+                     "paged_attn",
+                     "merge_states", "csp_workspace_status", "csp_last_cuda_error",
+                     "csp_version"):
+            getattr(lib, name).restype = ctypes.c_int
+        _lib = lib
+        return lib
+
+
+def _check(status: int, what: str) -> None:
+    if status != CSP_OK:
+        raise CspError(status, what)
+
+
+def _host_i32(a) -> np.ndarray:
+    if hasattr(a, "detach"):
+        a = a.detach().cpu().numpy()
+    return np.ascontiguousarray(np.asarray(a, dtype=np.int32))
+
+
+def cascade_plan(block_table, seq_lens, num_computed_tokens, *, block_size=16, num_q_heads=32,
+                 num_kv_heads=8, head_dim=128, num_sms=0, mode=MODE_AUTO):
+    """(common_prefix_len, use_cascade) for host arrays (numpy or CPU tensors)."""
+    lib = load()
+    bt = _host_i32(block_table)
+    sl = _host_i32(seq_lens)
+    nc = _host_i32(num_computed_tokens)
+    n = int(sl.shape[0])
+    stride = int(bt.shape[1]) if bt.ndim == 2 else 0
+    cpl = ctypes.c_int32(0)
+    use = ctypes.c_int32(0)
+    _check(lib.cascade_plan(bt.ctypes.data if bt.size else None, stride, n,
+                            sl.ctypes.data if n else None, nc.ctypes.data if n else None,
+                            block_size, num_q_heads, num_kv_heads, head_dim, num_sms, mode,
+                            ctypes.byref(cpl), ctypes.byref(use)), "cascade_plan")
+    return int(cpl.value), bool(use.value)
+
+
+def workspace_size(num_reqs, total_q, max_seqlen_q, max_seqlen_k, common_prefix_len,
+                   num_q_heads, num_kv_heads, head_dim) -> int:
+    lib = load()
+    out = ctypes.c_size_t(0)
+    _check(lib.csp_workspace_size(num_reqs, total_q, max_seqlen_q, max_seqlen_k,
+                                  common_prefix_len, num_q_heads, num_kv_heads, head_dim,
+                                  ctypes.byref(out)), "csp_workspace_size")
+    return int(out.value)
+
+
+def _stream_ptr(stream, device):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else None
+
+
+def alloc_workspace(nbytes: int, device):
+    """Zero-filled, 256-byte-aligned device workspace (torch allocations are)."""
+    import torch
+    return torch.zeros(max(nbytes, 256), dtype=torch.uint8, device=device)
+
+
+def _attn(fn_name, q, k_cache, v_cache, block_table, cu_seqlens_q, seqused_k, *, max_seqlen_q,
+          max_seqlen_k, softmax_scale, common_prefix_len=None, out=None, lse=None,
+          workspace=None, stream=None, phase_events=None):
+    import torch
+    lib = load()
+    total_q, hq, d = q.shape
+    num_blocks, bs, hkv, _ = k_cache.shape
+    n = int(seqused_k.shape[0])
+    cpl = 0 if common_prefix_len is None else int(common_prefix_len)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((total_q, hq), dtype=torch.float32, device=q.device)
+    need = workspace_size(n, total_q, max_seqlen_q, max_seqlen_k, cpl, hq, hkv, d)
+    if workspace is None or workspace.numel() < need:
+        workspace = alloc_workspace(need, q.device)
+    args = [_ptr(q), _ptr(k_cache), _ptr(v_cache), num_blocks, _ptr(block_table),
+            int(block_table.stride(0)), _ptr(cu_seqlens_q), _ptr(seqused_k), n, total_q,
+            int(max_seqlen_q), int(max_seqlen_k)]
+    if fn_name == "cascade_attn":
+        args.append(cpl)
+    args += [bs, hq, hkv, d, float(softmax_scale), _ptr(out), _ptr(lse), _ptr(workspace),
+             workspace.numel(), _stream_ptr(stream, q.device)]
+    if phase_events is not None:
+        fn_name = "cascade_attn_timed"
+        handles = (ctypes.c_void_p * 4)(*[ev.cuda_event for ev in phase_events])
+        args.append(ctypes.cast(handles, ctypes.c_void_p))
+    _check(getattr(lib, fn_name)(*args), fn_name)
+    return out, lse
+
+
+def cascade_attn(q, k_cache, v_cache, block_table, cu_seqlens_q, seqused_k, *, max_seqlen_q,
+                 max_seqlen_k, common_prefix_len, softmax_scale, out=None, lse=None,
+                 workspace=None, stream=None, phase_events=None):
+    """Cascade attention (prefix phase + suffix phase + LSE merge) on device tensors.
+
+    phase_events: optional four torch.cuda.Event(enable_timing=True); when given, the
+    call goes through cascade_attn_timed and records them between the kernels.
+    """
+    return _attn("cascade_attn", q, k_cache, v_cache, block_table, cu_seqlens_q, seqused_k,
+                 max_seqlen_q=max_seqlen_q, max_seqlen_k=max_seqlen_k,
+                 softmax_scale=softmax_scale, common_prefix_len=common_prefix_len, out=out,
+                 lse=lse, workspace=workspace, stream=stream, phase_events=phase_events)
+
+
+def paged_attn(q, k_cache, v_cache, block_table, cu_seqlens_q, seqused_k, *, max_seqlen_q,
+               max_seqlen_k, softmax_scale, out=None, lse=None, workspace=None, stream=None):
+    """Standard (flat) paged attention on device tensors."""
+    return _attn("paged_attn", q, k_cache, v_cache, block_table, cu_seqlens_q, seqused_k,
+                 max_seqlen_q=max_seqlen_q, max_seqlen_k=max_seqlen_k,
+                 softmax_scale=softmax_scale, out=out, lse=lse, workspace=workspace,
+                 stream=stream)
+
+
+def merge_states(prefix_out, prefix_lse, suffix_out, suffix_lse, *, out=None, out_lse=None,
+                 stream=None):
+    """LSE merge of two partials ([T, H, D] bf16 or fp32, LSE fp32 [T, H], natural log)."""
+    import torch
+    lib = load()
+    t, h, d = prefix_out.shape
+    if out is None:
+        out = torch.empty((t, h, d), dtype=torch.bfloat16, device=prefix_out.device)
+    if out_lse is None:
+        out_lse = torch.empty((t, h), dtype=torch.float32, device=prefix_out.device)
+    dt = DTYPE_F32 if prefix_out.dtype == torch.float32 else DTYPE_BF16
+    assert suffix_out.dtype == prefix_out.dtype
+    _check(lib.merge_states(_ptr(out), _ptr(out_lse), _ptr(prefix_out), _ptr(prefix_lse),
+                            _ptr(suffix_out), _ptr(suffix_lse), t, h, d, dt,
+                            _stream_ptr(stream, prefix_out.device)), "merge_states")
+    return out, out_lse
+
+
+def workspace_status(workspace, stream=None) -> int:
+    lib = load()
+    st = ctypes.c_int32(0)
+    _check(lib.csp_workspace_status(_ptr(workspace), _stream_ptr(stream, workspace.device),
+                                    ctypes.byref(st)), "csp_workspace_status")
+    return int(st.value)
+
+
+def version() -> int:
+    return load().csp_version()

@@ -1,0 +1,443 @@
+// api.cu — the C ABI declared in include/csp.h: argument checks, the common-prefix
+// planner, the launch plan (tiles, key splits, workspace partition), TMA tensor-map
+// encoding and the launch sequence.  Everything here runs on the host.
+#include <atomic>
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+#include "csp.h"
+#include "kernels.cuh"
+
+namespace {
+
+thread_local int g_last_cuda_error = 0;
+
+int cuda_fail(cudaError_t e) {
+  g_last_cuda_error = static_cast<int>(e);
+  return CSP_ERR_CUDA;
+}
+
+constexpr int kPage = 16;
+constexpr size_t kHeaderBytes = 256;  // status word + reserved
+constexpr int kMaxSplits = 32;
+
+size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+int64_t cdiv64(int64_t a, int64_t b) { return (a + b - 1) / b; }
+int cdiv(int a, int b) { return (a + b - 1) / b; }
+
+int device_sm_count(int* sms) {
+  static std::atomic<int> cache[64];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (dev >= 0 && dev < 64) {
+    int v = cache[dev].load(std::memory_order_relaxed);
+    if (v > 0) {
+      *sms = v;
+      return CSP_OK;
+    }
+  }
+  int n = 0;
+  e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (dev >= 0 && dev < 64) cache[dev].store(n, std::memory_order_relaxed);
+  *sms = n;
+  return CSP_OK;
+}
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = []() -> EncodeTiledFn {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return nullptr;
+    return reinterpret_cast<EncodeTiledFn>(p);
+  }();
+  return fn;
+}
+
+// 3-D bf16 tensor map with a 128-byte swizzle: dims innermost first, strides of dims
+// 1 and 2 in bytes, box in elements.
+int make_map_3d(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1, uint64_t d2,
+                uint64_t s1, uint64_t s2, uint32_t b0, uint32_t b1, uint32_t b2) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return cuda_fail(cudaErrorNotSupported);
+  const cuuint64_t dims[3] = {d0, d1, d2};
+  const cuuint64_t strides[2] = {s1, s2};
+  const cuuint32_t box[3] = {b0, b1, b2};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return cuda_fail(cudaErrorInvalidValue);
+  return CSP_OK;
+}
+
+bool supported_group(int g) { return g == 1 || g == 2 || g == 4 || g == 8 || g == 16; }
+
+int check_shape(int num_reqs, int total_q, int max_q, int max_k, int Hq, int Hkv, int D, int bs) {
+  if (num_reqs < 0 || total_q < 0 || max_q < 0 || max_k < 0 || Hq <= 0 || Hkv <= 0)
+    return CSP_ERR_INVALID_ARG;
+  if (Hq % Hkv != 0) return CSP_ERR_INVALID_ARG;
+  if (!supported_group(Hq / Hkv)) return CSP_ERR_UNSUPPORTED;
+  if (D != 64 && D != 128) return CSP_ERR_UNSUPPORTED;
+  if (bs != kPage) return CSP_ERR_UNSUPPORTED;
+  return CSP_OK;
+}
+
+// How one attention call is cut into CTAs and where its partials live.
+struct LaunchPlan {
+  int group = 1;
+  // prefix phase (tcgen05)
+  int p_m_tiles = 0, p_splits = 0, p_tiles_per_split = 0;
+  // paged phase (suffix or standard path)
+  bool decode = true;
+  int s_row_tiles = 1, s_splits = 1, s_split_keys = 64;
+  bool direct = false;  // paged kernel writes the final output itself
+  int n_parts = 0;
+  size_t off_part_o = 0, off_part_lse = 0, bytes = 0;
+};
+
+void make_plan(int num_reqs, int total_q, int max_q, int max_k, int cpl, int Hq, int Hkv, int D,
+               int sms, LaunchPlan* P) {
+  LaunchPlan p;
+  p.group = Hq / Hkv;
+  if (cpl > 0) {
+    const int rows = total_q * p.group;
+    p.p_m_tiles = cdiv(rows, 128);
+    const int key_tiles = cdiv(cpl, 128);
+    const int base = p.p_m_tiles * Hkv;
+    // choose the split count by waves x per-CTA length (+1 tile of fixed cost)
+    int best_s = 1;
+    int64_t best_cost = -1;
+    for (int s = 1; s <= std::min(key_tiles, kMaxSplits); ++s) {
+      const int tps = cdiv(key_tiles, s);
+      const int s_eff = cdiv(key_tiles, tps);
+      const int64_t ctas = static_cast<int64_t>(base) * s_eff;
+      const int64_t cost = cdiv64(ctas, sms) * (tps + 1);
+      if (best_cost < 0 || cost < best_cost) {
+        best_cost = cost;
+        best_s = s_eff;
+      }
+    }
+    p.p_tiles_per_split = cdiv(key_tiles, best_s);
+    p.p_splits = cdiv(key_tiles, p.p_tiles_per_split);
+  }
+  p.decode = static_cast<int64_t>(max_q) * p.group <= 16;
+  const int rows_per_cta = p.decode ? 16 : 64;
+  p.s_row_tiles = std::max(1, cdiv(max_q * p.group, rows_per_cta));
+  const int max_len = std::max(0, max_k - cpl);
+  const int key_tiles = std::max(1, cdiv(max_len, 64));
+  const int64_t units = static_cast<int64_t>(num_reqs) * p.s_row_tiles * Hkv;
+  int s = units > 0 ? static_cast<int>(std::min<int64_t>(cdiv64(2LL * sms, units), kMaxSplits)) : 1;
+  s = std::max(1, std::min(s, key_tiles));
+  p.s_split_keys = cdiv(key_tiles, s) * 64;
+  p.s_splits = std::max(1, cdiv(std::max(max_len, 1), p.s_split_keys));
+  p.direct = (cpl == 0 && p.s_splits == 1);
+  p.n_parts = p.direct ? 0 : p.p_splits + p.s_splits;
+  const size_t rows_total = static_cast<size_t>(total_q) * Hq;
+  p.off_part_o = kHeaderBytes;
+  p.off_part_lse = p.off_part_o + align256(static_cast<size_t>(p.n_parts) * rows_total * D * 4);
+  p.bytes = p.off_part_lse + align256(static_cast<size_t>(p.n_parts) * rows_total * 4);
+  *P = p;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+// Shared body of cascade_attn (cpl > 0) and paged_attn (cpl == 0).
+int attention_call(const void* q, const void* k_cache, const void* v_cache, int32_t num_blocks,
+                   const int32_t* block_table, int64_t bt_row_stride,
+                   const int32_t* cu_seqlens_q, const int32_t* seqused_k, int32_t num_reqs,
+                   int32_t total_q, int32_t max_seqlen_q, int32_t max_seqlen_k, int32_t cpl,
+                   int32_t block_size, int32_t Hq, int32_t Hkv, int32_t D, float scale,
+                   void* out, float* lse, void* workspace, size_t workspace_bytes,
+                   void* stream_ptr, void* const* events = nullptr) {
+  int st = check_shape(num_reqs, total_q, max_seqlen_q, max_seqlen_k, Hq, Hkv, D, block_size);
+  if (st != CSP_OK) return st;
+  if (cpl < 0 || cpl % block_size != 0 || cpl > max_seqlen_k) return CSP_ERR_INVALID_ARG;
+  if (!(scale > 0.f) || !std::isfinite(scale)) return CSP_ERR_INVALID_ARG;
+  if (num_blocks <= 0 || static_cast<int64_t>(num_blocks) * block_size > INT32_MAX)
+    return CSP_ERR_INVALID_ARG;
+  if (total_q == 0 || num_reqs == 0) return CSP_OK;
+  if (!q || !k_cache || !v_cache || !block_table || !cu_seqlens_q || !seqused_k || !out)
+    return CSP_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out))
+    return CSP_ERR_INVALID_ARG;
+  if (bt_row_stride < cdiv(max_seqlen_k, block_size)) return CSP_ERR_INVALID_ARG;
+  int sms = 0;
+  if ((st = device_sm_count(&sms)) != CSP_OK) return st;
+  LaunchPlan P;
+  make_plan(num_reqs, total_q, max_seqlen_q, max_seqlen_k, cpl, Hq, Hkv, D, sms, &P);
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255) != 0 ||
+      workspace_bytes < P.bytes)
+    return CSP_ERR_WORKSPACE;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  int* status = reinterpret_cast<int*>(ws);
+  float* part_o = reinterpret_cast<float*>(ws + P.off_part_o);
+  float* part_lse = reinterpret_cast<float*>(ws + P.off_part_lse);
+  const float scale_log2 = scale * 1.4426950408889634f;
+  cudaError_t e;
+  auto mark = [&](int i) -> cudaError_t {
+    return events ? cudaEventRecord(static_cast<cudaEvent_t>(events[i]), stream) : cudaSuccess;
+  };
+  if ((e = mark(0)) != cudaSuccess) return cuda_fail(e);
+
+  if (cpl > 0) {
+    CUtensorMap tm_q, tm_k, tm_v;
+    const uint64_t row_b = static_cast<uint64_t>(D) * 2;
+    if ((st = make_map_3d(&tm_q, q, D, Hq, total_q, row_b, row_b * Hq, 64, P.group,
+                          128 / P.group)) != CSP_OK)
+      return st;
+    const uint64_t ntok = static_cast<uint64_t>(num_blocks) * block_size;
+    if ((st = make_map_3d(&tm_k, k_cache, D, Hkv, ntok, row_b, row_b * Hkv, 64, 1, kPage)) !=
+        CSP_OK)
+      return st;
+    if ((st = make_map_3d(&tm_v, v_cache, D, Hkv, ntok, row_b, row_b * Hkv, 64, 1, kPage)) !=
+        CSP_OK)
+      return st;
+    csp::PrefixArgs pa;
+    pa.block_table = block_table;
+    pa.total_q = total_q;
+    pa.num_q_heads = Hq;
+    pa.num_kv_heads = Hkv;
+    pa.group = P.group;
+    pa.cpl = cpl;
+    pa.m_tiles = P.p_m_tiles;
+    pa.n_splits = P.p_splits;
+    pa.tiles_per_split = P.p_tiles_per_split;
+    pa.scale_log2 = scale_log2;
+    pa.part_o = part_o;
+    pa.part_lse = part_lse;
+    pa.status = status;
+    if ((e = csp::launch_prefix(D, tm_q, tm_k, tm_v, pa, stream)) != cudaSuccess)
+      return cuda_fail(e);
+  }
+  if ((e = mark(1)) != cudaSuccess) return cuda_fail(e);
+
+  csp::PagedArgs ga;
+  ga.q = static_cast<const __nv_bfloat16*>(q);
+  ga.k = static_cast<const __nv_bfloat16*>(k_cache);
+  ga.v = static_cast<const __nv_bfloat16*>(v_cache);
+  ga.block_table = block_table;
+  ga.bt_stride = bt_row_stride;
+  ga.cu_seqlens_q = cu_seqlens_q;
+  ga.seq_lens = seqused_k;
+  ga.num_reqs = num_reqs;
+  ga.total_q = total_q;
+  ga.num_q_heads = Hq;
+  ga.num_kv_heads = Hkv;
+  ga.group = P.group;
+  ga.key_start = cpl;
+  ga.split_keys = P.s_split_keys;
+  ga.n_splits = P.s_splits;
+  ga.row_tiles = P.s_row_tiles;
+  ga.scale_log2 = scale_log2;
+  ga.part_o = P.direct ? nullptr : part_o;
+  ga.part_lse = P.direct ? nullptr : part_lse;
+  ga.part_slot0 = P.p_splits;
+  ga.out = static_cast<__nv_bfloat16*>(out);
+  ga.lse = lse;
+  if ((e = csp::launch_paged(D, P.decode, ga, stream)) != cudaSuccess) return cuda_fail(e);
+  if ((e = mark(2)) != cudaSuccess) return cuda_fail(e);
+
+  if (!P.direct) {
+    csp::CombineArgs ca;
+    ca.part_o = part_o;
+    ca.part_lse = part_lse;
+    ca.n_parts = P.n_parts;
+    ca.rows = total_q * Hq;
+    ca.out = static_cast<__nv_bfloat16*>(out);
+    ca.lse = lse;
+    if ((e = csp::launch_combine(D, ca, stream)) != cudaSuccess) return cuda_fail(e);
+  }
+  if ((e = mark(3)) != cudaSuccess) return cuda_fail(e);
+  return CSP_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int cascade_plan(const int32_t* block_table, int64_t bt_row_stride, int32_t num_reqs,
+                 const int32_t* seq_lens, const int32_t* num_computed_tokens,
+                 int32_t block_size, int32_t num_q_heads, int32_t num_kv_heads,
+                 int32_t head_dim, int32_t num_sms, int32_t mode,
+                 int32_t* common_prefix_len_out, int32_t* use_cascade_out) {
+  if (!common_prefix_len_out || !use_cascade_out || num_reqs < 0 || block_size <= 0)
+    return CSP_ERR_INVALID_ARG;
+  if (mode < CSP_MODE_AUTO || mode > CSP_MODE_PAGE_THRESHOLDS) return CSP_ERR_INVALID_ARG;
+  *common_prefix_len_out = 0;
+  *use_cascade_out = 0;
+  if (num_reqs == 0) return CSP_OK;
+  if (!block_table || !seq_lens || !num_computed_tokens) return CSP_ERR_INVALID_ARG;
+  // §八 Step 1: rows take part with their first cdiv(seq_len, bs) entries only
+  int64_t shortest = INT64_MAX;
+  int32_t min_computed = INT32_MAX;
+  for (int r = 0; r < num_reqs; ++r) {
+    if (seq_lens[r] < 0 || num_computed_tokens[r] < 0 || num_computed_tokens[r] > seq_lens[r])
+      return CSP_ERR_INVALID_ARG;
+    const int64_t used = cdiv64(seq_lens[r], block_size);
+    if (used > bt_row_stride) return CSP_ERR_INVALID_ARG;
+    shortest = std::min(shortest, used);
+    min_computed = std::min(min_computed, num_computed_tokens[r]);
+  }
+  int64_t ncpb = 0;
+  for (; ncpb < shortest; ++ncpb) {
+    const int32_t id = block_table[ncpb];
+    bool same = true;
+    for (int r = 1; r < num_reqs && same; ++r)
+      same = block_table[static_cast<int64_t>(r) * bt_row_stride + ncpb] == id;
+    if (!same) break;
+  }
+  // §八 Step 2: blocks to tokens, cap to min(num_computed_tokens), floor to block_size
+  int64_t cpl = ncpb * block_size;
+  cpl = std::min<int64_t>(cpl, min_computed);
+  cpl = (cpl / block_size) * block_size;
+  *common_prefix_len_out = static_cast<int32_t>(cpl);
+
+  // §三: never for a prefix under 256 tokens or a batch under 8 requests
+  const bool thresholds = cpl >= 256 && num_reqs >= 8;
+  int use = 0;
+  switch (mode) {
+    case CSP_MODE_FORCE_CASCADE:
+      use = cpl > 0;
+      break;
+    case CSP_MODE_FORCE_FLAT:
+      use = 0;
+      break;
+    case CSP_MODE_PAGE_THRESHOLDS:
+      use = thresholds;
+      break;
+    default: {
+      // GB300 rule: on top of the thresholds, cascade must cut the KV bytes the
+      // standard path streams by at least 1.5x (prefix read once instead of N times).
+      int64_t flat_tokens = 0, casc_tokens = cpl;
+      for (int r = 0; r < num_reqs; ++r) {
+        flat_tokens += seq_lens[r];
+        casc_tokens += seq_lens[r] - cpl;
+      }
+      (void)num_q_heads;
+      (void)num_kv_heads;
+      (void)head_dim;
+      (void)num_sms;
+      use = thresholds && casc_tokens > 0 && 2 * flat_tokens >= 3 * casc_tokens;
+      break;
+    }
+  }
+  *use_cascade_out = use;
+  return CSP_OK;
+}
+
+int csp_workspace_size(int32_t num_reqs, int32_t total_q, int32_t max_seqlen_q,
+                       int32_t max_seqlen_k, int32_t common_prefix_len, int32_t num_q_heads,
+                       int32_t num_kv_heads, int32_t head_dim, size_t* bytes_out) {
+  if (!bytes_out) return CSP_ERR_INVALID_ARG;
+  int st = check_shape(num_reqs, total_q, max_seqlen_q, max_seqlen_k, num_q_heads, num_kv_heads,
+                       head_dim, kPage);
+  if (st != CSP_OK) return st;
+  if (common_prefix_len < 0 || common_prefix_len % kPage != 0) return CSP_ERR_INVALID_ARG;
+  int sms = 0;
+  if ((st = device_sm_count(&sms)) != CSP_OK) return st;
+  LaunchPlan P;
+  make_plan(num_reqs, total_q, max_seqlen_q, max_seqlen_k, common_prefix_len, num_q_heads,
+            num_kv_heads, head_dim, sms, &P);
+  *bytes_out = P.bytes;
+  return CSP_OK;
+}
+
+int cascade_attn(const void* q, const void* k_cache, const void* v_cache, int32_t num_blocks,
+                 const int32_t* block_table, int64_t bt_row_stride, const int32_t* cu_seqlens_q,
+                 const int32_t* seqused_k, int32_t num_reqs, int32_t total_q,
+                 int32_t max_seqlen_q, int32_t max_seqlen_k, int32_t common_prefix_len,
+                 int32_t block_size, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                 float softmax_scale, void* out, float* lse, void* workspace,
+                 size_t workspace_bytes, void* stream) {
+  return attention_call(q, k_cache, v_cache, num_blocks, block_table, bt_row_stride, cu_seqlens_q,
+                        seqused_k, num_reqs, total_q, max_seqlen_q, max_seqlen_k,
+                        common_prefix_len, block_size, num_q_heads, num_kv_heads, head_dim,
+                        softmax_scale, out, lse, workspace, workspace_bytes, stream);
+}
+
+int cascade_attn_timed(const void* q, const void* k_cache, const void* v_cache,
+                       int32_t num_blocks, const int32_t* block_table, int64_t bt_row_stride,
+                       const int32_t* cu_seqlens_q, const int32_t* seqused_k, int32_t num_reqs,
+                       int32_t total_q, int32_t max_seqlen_q, int32_t max_seqlen_k,
+                       int32_t common_prefix_len, int32_t block_size, int32_t num_q_heads,
+                       int32_t num_kv_heads, int32_t head_dim, float softmax_scale, void* out,
+                       float* lse, void* workspace, size_t workspace_bytes, void* stream,
+                       void* const* phase_events) {
+  if (!phase_events) return CSP_ERR_INVALID_ARG;
+  for (int i = 0; i < 4; ++i)
+    if (!phase_events[i]) return CSP_ERR_INVALID_ARG;
+  return attention_call(q, k_cache, v_cache, num_blocks, block_table, bt_row_stride, cu_seqlens_q,
+                        seqused_k, num_reqs, total_q, max_seqlen_q, max_seqlen_k,
+                        common_prefix_len, block_size, num_q_heads, num_kv_heads, head_dim,
+                        softmax_scale, out, lse, workspace, workspace_bytes, stream,
+                        phase_events);
+}
+
+int paged_attn(const void* q, const void* k_cache, const void* v_cache, int32_t num_blocks,
+               const int32_t* block_table, int64_t bt_row_stride, const int32_t* cu_seqlens_q,
+               const int32_t* seqused_k, int32_t num_reqs, int32_t total_q, int32_t max_seqlen_q,
+               int32_t max_seqlen_k, int32_t block_size, int32_t num_q_heads,
+               int32_t num_kv_heads, int32_t head_dim, float softmax_scale, void* out,
+               float* lse, void* workspace, size_t workspace_bytes, void* stream) {
+  return attention_call(q, k_cache, v_cache, num_blocks, block_table, bt_row_stride, cu_seqlens_q,
+                        seqused_k, num_reqs, total_q, max_seqlen_q, max_seqlen_k, 0, block_size,
+                        num_q_heads, num_kv_heads, head_dim, softmax_scale, out, lse, workspace,
+                        workspace_bytes, stream);
+}
+
+int merge_states(void* out, float* out_lse, const void* prefix_out, const float* prefix_lse,
+                 const void* suffix_out, const float* suffix_lse, int32_t num_tokens,
+                 int32_t num_heads, int32_t head_dim, int32_t partial_dtype, void* stream) {
+  if (num_tokens < 0 || num_heads <= 0 || head_dim <= 0 || head_dim % 8 != 0 || head_dim > 512)
+    return CSP_ERR_INVALID_ARG;
+  if (partial_dtype != CSP_DTYPE_BF16 && partial_dtype != CSP_DTYPE_F32)
+    return CSP_ERR_INVALID_ARG;
+  if (num_tokens == 0) return CSP_OK;
+  if (!out || !prefix_out || !prefix_lse || !suffix_out || !suffix_lse)
+    return CSP_ERR_INVALID_ARG;
+  if (!aligned16(out) || !aligned16(prefix_out) || !aligned16(suffix_out))
+    return CSP_ERR_INVALID_ARG;
+  cudaError_t e = csp::launch_merge_states(
+      static_cast<__nv_bfloat16*>(out), out_lse, prefix_out, prefix_lse, suffix_out, suffix_lse,
+      num_tokens * num_heads, head_dim, partial_dtype == CSP_DTYPE_F32,
+      static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? CSP_OK : cuda_fail(e);
+}
+
+int csp_workspace_status(const void* workspace, void* stream, int32_t* status_out) {
+  if (!workspace || !status_out) return CSP_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemcpyAsync(status_out, workspace, sizeof(int32_t), cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  return e == cudaSuccess ? CSP_OK : cuda_fail(e);
+}
+
+const char* csp_status_string(int status) {
+  switch (status) {
+    case CSP_OK: return "CSP_OK";
+    case CSP_ERR_INVALID_ARG: return "CSP_ERR_INVALID_ARG";
+    case CSP_ERR_UNSUPPORTED: return "CSP_ERR_UNSUPPORTED";
+    case CSP_ERR_WORKSPACE: return "CSP_ERR_WORKSPACE";
+    case CSP_ERR_CUDA: return "CSP_ERR_CUDA";
+    case CSP_ERR_TIMEOUT: return "CSP_ERR_TIMEOUT";
+    default: return "CSP_ERR_UNKNOWN";
+  }
+}
+
+int csp_last_cuda_error(void) { return g_last_cuda_error; }
+
+int csp_version(void) { return (1 << 16) | 0; }
+
+}  // extern "C"

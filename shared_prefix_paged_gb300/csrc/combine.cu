@@ -1,0 +1,152 @@
+// combine.cu — LSE merging of partial attention results.
+//
+// "vLLM Cascade Attention：用法、场景与原理解析" §一 and §八 Step 5 (merge_attn_states):
+// partial results over disjoint key sets combine by log-sum-exp rescaling,
+//   m = max_p l_p,  w_p = e^(l_p - m),  out = sum_p w_p o_p / sum_p w_p,
+//   lse = m + ln(sum_p w_p).
+// §九 (FlashDecoding) uses the same rescaling to merge the splits of one key range,
+// so a single n-way pass merges the prefix splits, the suffix splits and the final
+// prefix/suffix pair at once.
+//
+// Both kernels are elementwise and HBM-bound: one warp (combine) or D/8 threads
+// (merge_states) per output row, 16-byte vector loads and stores, fp32 math.
+#include "common.cuh"
+#include "kernels.cuh"
+
+namespace csp {
+namespace {
+
+constexpr float kLn2 = 0.69314718055994531f;
+constexpr float kLog2e = 1.4426950408889634f;
+
+// Partials: o [n_parts][rows][D] fp32 (normalised), lse [n_parts][rows] log2 domain.
+template <int D>
+__global__ void __launch_bounds__(256) combine_kernel(const CombineArgs a) {
+  constexpr int kPer = D / 32;  // features per lane
+  const int row = blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= a.rows) return;
+  float m = -INFINITY;
+  for (int p = lane; p < a.n_parts; p += 32)
+    m = fmaxf(m, __ldg(a.part_lse + static_cast<int64_t>(p) * a.rows + row));
+#pragma unroll
+  for (int s = 16; s > 0; s >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, s));
+  float acc[kPer];
+#pragma unroll
+  for (int e = 0; e < kPer; ++e) acc[e] = 0.f;
+  float wsum = 0.f;
+  if (m != -INFINITY) {
+    for (int p = 0; p < a.n_parts; ++p) {
+      const float lp = __ldg(a.part_lse + static_cast<int64_t>(p) * a.rows + row);
+      if (lp == -INFINITY) continue;  // empty split: weight 0, its o is never read
+      const float w = exp2f(lp - m);
+      wsum += w;
+      const float* src = a.part_o + (static_cast<int64_t>(p) * a.rows + row) * D + lane * kPer;
+      if constexpr (kPer == 4) {
+        const float4 v = __ldg(reinterpret_cast<const float4*>(src));
+        acc[0] += w * v.x;
+        acc[1] += w * v.y;
+        acc[2] += w * v.z;
+        acc[3] += w * v.w;
+      } else {
+        const float2 v = __ldg(reinterpret_cast<const float2*>(src));
+        acc[0] += w * v.x;
+        acc[1] += w * v.y;
+      }
+    }
+  }
+  const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+  __nv_bfloat16* dst = a.out + static_cast<int64_t>(row) * D + lane * kPer;
+  if constexpr (kPer == 4) {
+    *reinterpret_cast<uint2*>(dst) =
+        make_uint2(pack_bf16x2(acc[0] * inv, acc[1] * inv), pack_bf16x2(acc[2] * inv, acc[3] * inv));
+  } else {
+    *reinterpret_cast<uint32_t*>(dst) = pack_bf16x2(acc[0] * inv, acc[1] * inv);
+  }
+  if (lane == 0 && a.lse != nullptr)
+    a.lse[row] = wsum > 0.f ? (m + log2f(wsum)) * kLn2 : -INFINITY;
+}
+
+// Two partials with natural-log LSEs (the merge_states entry point).  Each thread
+// handles 8 features of one row.
+template <bool kF32>
+__global__ void __launch_bounds__(256)
+    merge_states_kernel(__nv_bfloat16* __restrict__ out, float* __restrict__ out_lse,
+                        const void* __restrict__ o1, const float* __restrict__ l1,
+                        const void* __restrict__ o2, const float* __restrict__ l2, int rows,
+                        int head_dim) {
+  const int chunks = head_dim / 8;
+  const int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (idx >= static_cast<int64_t>(rows) * chunks) return;
+  const int row = static_cast<int>(idx / chunks);
+  const int c = static_cast<int>(idx % chunks);
+  const float a = __ldg(l1 + row), b = __ldg(l2 + row);
+  const float m = fmaxf(a, b);
+  float w1 = 0.f, w2 = 0.f;
+  if (m != -INFINITY) {
+    w1 = exp2f((a - m) * kLog2e);
+    w2 = exp2f((b - m) * kLog2e);
+  }
+  const float ws = w1 + w2;
+  const float inv = ws > 0.f ? 1.f / ws : 0.f;
+  float x1[8], x2[8];
+  const int64_t off = static_cast<int64_t>(row) * head_dim + c * 8;
+  if constexpr (kF32) {
+    const float4* p1 = reinterpret_cast<const float4*>(static_cast<const float*>(o1) + off);
+    const float4* p2 = reinterpret_cast<const float4*>(static_cast<const float*>(o2) + off);
+    const float4 u0 = __ldg(p1), u1 = __ldg(p1 + 1), v0 = __ldg(p2), v1 = __ldg(p2 + 1);
+    x1[0] = u0.x; x1[1] = u0.y; x1[2] = u0.z; x1[3] = u0.w;
+    x1[4] = u1.x; x1[5] = u1.y; x1[6] = u1.z; x1[7] = u1.w;
+    x2[0] = v0.x; x2[1] = v0.y; x2[2] = v0.z; x2[3] = v0.w;
+    x2[4] = v1.x; x2[5] = v1.y; x2[6] = v1.z; x2[7] = v1.w;
+  } else {
+    const uint4 u = __ldg(reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(o1) + off));
+    const uint4 v = __ldg(reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(o2) + off));
+    const __nv_bfloat162* pu = reinterpret_cast<const __nv_bfloat162*>(&u);
+    const __nv_bfloat162* pv = reinterpret_cast<const __nv_bfloat162*>(&v);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float2 fu = __bfloat1622float2(pu[e]);
+      const float2 fv = __bfloat1622float2(pv[e]);
+      x1[2 * e] = fu.x; x1[2 * e + 1] = fu.y;
+      x2[2 * e] = fv.x; x2[2 * e + 1] = fv.y;
+    }
+  }
+  uint32_t w[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    // an empty side (lse = -inf, weight 0) contributes nothing, whatever its values
+    const float y0 = (w1 > 0.f ? w1 * x1[2 * e] : 0.f) + (w2 > 0.f ? w2 * x2[2 * e] : 0.f);
+    const float y1 = (w1 > 0.f ? w1 * x1[2 * e + 1] : 0.f) + (w2 > 0.f ? w2 * x2[2 * e + 1] : 0.f);
+    w[e] = pack_bf16x2(y0 * inv, y1 * inv);
+  }
+  *reinterpret_cast<uint4*>(out + off) = make_uint4(w[0], w[1], w[2], w[3]);
+  if (c == 0 && out_lse != nullptr) out_lse[row] = ws > 0.f ? m + logf(ws) : -INFINITY;
+}
+
+}  // namespace
+
+cudaError_t launch_combine(int head_dim, const CombineArgs& a, cudaStream_t stream) {
+  const int grid = (a.rows + 7) / 8;
+  if (grid == 0) return cudaSuccess;
+  if (head_dim == 64)
+    combine_kernel<64><<<grid, 256, 0, stream>>>(a);
+  else
+    combine_kernel<128><<<grid, 256, 0, stream>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_merge_states(__nv_bfloat16* out, float* out_lse, const void* o1,
+                                const float* l1, const void* o2, const float* l2, int rows,
+                                int head_dim, bool f32_partials, cudaStream_t stream) {
+  const int64_t threads = static_cast<int64_t>(rows) * (head_dim / 8);
+  if (threads == 0) return cudaSuccess;
+  const int grid = static_cast<int>((threads + 255) / 256);
+  if (f32_partials)
+    merge_states_kernel<true><<<grid, 256, 0, stream>>>(out, out_lse, o1, l1, o2, l2, rows, head_dim);
+  else
+    merge_states_kernel<false><<<grid, 256, 0, stream>>>(out, out_lse, o1, l1, o2, l2, rows, head_dim);
+  return cudaGetLastError();
+}
+
+}  // namespace csp

@@ -1,0 +1,374 @@
+// paged_attn.cu — causal attention of each request over a range of its own KV
+// pages: the suffix phase of cascade attention (keys [cpl, seq_len), "vLLM Cascade
+// Attention：用法、场景与原理解析" §八 Step 5 Phase 2) and the standard path (keys
+// [0, seq_len), §五 and §十).
+//
+// This work streams each request's private pages from HBM once and does little
+// arithmetic per byte, so the design aims at bandwidth:
+//  * one CTA per (request, KV head, row tile, key split); the rows are the request's
+//    (query, head-in-group) pairs of that KV head, so all GQA heads of a KV head
+//    share each page load;
+//  * pages are fetched with 16-byte cp.async (coalesced: 16 threads per 256-byte
+//    page row) into an XOR-swizzled shared tile of 64 keys, three stages deep;
+//    keys past the range are zero-filled and never read from the block table;
+//  * QK^T and PV run on warp-level bf16 MMA (m16n8k16) fed by ldmatrix; the online
+//    softmax keeps its row max / sum with warp shuffles inside each 4-lane row group;
+//  * decode rows (<= 16 per request and KV head): the four warps split the keys
+//    of every tile and merge (max, sum, O) through shared memory at the end;
+//    prefill rows: each warp owns 16 rows of a 64-row tile;
+//  * split-KV (FlashDecoding, §九) over long ranges: each split writes a normalised
+//    fp32 partial + log2-sum-exp for the combine kernel; a single split of the
+//    standard path writes bf16 output and the natural-log LSE directly.
+#include "common.cuh"
+#include "kernels.cuh"
+
+namespace csp {
+namespace {
+
+constexpr int kTileKeys = 64;
+constexpr int kPage = 16;
+constexpr int kThreads = 128;
+constexpr int kStages = 3;
+
+template <int D>
+__device__ __forceinline__ uint32_t swz(int row, int chunk) {
+  // byte offset of 16-byte chunk `chunk` of row `row` in a [rows][D] bf16 tile
+  return static_cast<uint32_t>(row * (D * 2) + ((chunk ^ (row & 7)) << 4));
+}
+
+template <int D, bool kDecode>
+struct PagedLayout {
+  static constexpr int kRows = kDecode ? 16 : 64;
+  static constexpr int kQBytes = kRows * D * 2;
+  static constexpr int kKVBytes = kTileKeys * D * 2;
+  static constexpr int kQ = 0;
+  static constexpr int kK = kQ + kQBytes;
+  static constexpr int kV = kK + kStages * kKVBytes;
+  static constexpr int kEnd = kV + kStages * kKVBytes;
+  // decode merge scratch (reuses the K/V stages after the last tile)
+  static constexpr int kMergeBytes = 4 * 16 * D * 4 + 2 * 4 * 16 * 4;
+  static_assert(!kDecode || kMergeBytes <= 2 * kStages * kKVBytes, "merge scratch");
+};
+
+template <int D, bool kDecode>
+__global__ void __launch_bounds__(kThreads)
+    paged_attn_kernel(const PagedArgs a) {
+  using L = PagedLayout<D, kDecode>;
+  constexpr int kChunks = D / 8;               // 16-byte chunks per row
+  constexpr int kWarpKeys = kDecode ? 16 : 64; // keys of a tile each warp handles
+  constexpr int kNT = kWarpKeys / 8;           // S n-tiles per warp
+  constexpr int kDT = D / 8;                   // O n-tiles
+
+  extern __shared__ __align__(128) uint8_t smem[];
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  const int r = blockIdx.x / a.row_tiles;
+  const int rt = blockIdx.x % a.row_tiles;
+  const int g = blockIdx.y;
+  const int split = blockIdx.z;
+  const int q0 = __ldg(a.cu_seqlens_q + r);
+  const int q_len = __ldg(a.cu_seqlens_q + r + 1) - q0;
+  const int seq = __ldg(a.seq_lens + r);
+  const int rows_total = q_len * a.group;
+  const int row0 = rt * L::kRows;
+  if (row0 >= rows_total) return;
+  const int rows_here = min(L::kRows, rows_total - row0);
+
+  // key range of this split, clipped by the causal limit of the tile's last row
+  const int last_query = (row0 + rows_here - 1) / a.group;
+  const int kbeg = a.key_start + split * a.split_keys;
+  int kend = min(kbeg + a.split_keys, seq);
+  kend = min(kend, seq - q_len + last_query + 1);
+  const int n_tiles = kend > kbeg ? (kend - kbeg + kTileKeys - 1) / kTileKeys : 0;
+
+  const int64_t kv_tok_stride = static_cast<int64_t>(a.num_kv_heads) * D;
+  const int32_t* bt_row = a.block_table + static_cast<int64_t>(r) * a.bt_stride;
+  const uint32_t sbase = smem_u32(smem);
+
+  auto load_tile = [&](int ti, int stage) {
+    const int kt0 = kbeg + ti * kTileKeys;
+    uint8_t* sk = smem + L::kK + stage * L::kKVBytes;
+    uint8_t* sv = smem + L::kV + stage * L::kKVBytes;
+#pragma unroll
+    for (int x = threadIdx.x; x < kTileKeys * kChunks; x += kThreads) {
+      const int key = x / kChunks, c = x % kChunks;
+      const int kabs = kt0 + key;
+      const bool ok = kabs < kend;
+      int64_t off = 0;
+      if (ok) {
+        const int blk = __ldg(bt_row + kabs / kPage);
+        off = ((static_cast<int64_t>(blk) * kPage + kabs % kPage) * a.num_kv_heads + g) * D +
+              c * 8;
+      }
+      cp_async_16(sk + swz<D>(key, c), a.k + off, ok ? 16u : 0u);
+      cp_async_16(sv + swz<D>(key, c), a.v + off, ok ? 16u : 0u);
+    }
+  };
+
+  // Q rows of this tile: packed row rho = query * group + head-in-group
+#pragma unroll
+  for (int x = threadIdx.x; x < L::kRows * kChunks; x += kThreads) {
+    const int row = x / kChunks, c = x % kChunks;
+    const int rho = row0 + row;
+    const bool ok = rho < rows_total;
+    int64_t off = 0;
+    if (ok) {
+      const int qi = rho / a.group, j = rho % a.group;
+      off = (static_cast<int64_t>(q0 + qi) * a.num_q_heads + g * a.group + j) * D + c * 8;
+    }
+    cp_async_16(smem + L::kQ + swz<D>(row, c), a.q + off, ok ? 16u : 0u);
+  }
+#pragma unroll
+  for (int st = 0; st < kStages - 1; ++st) {
+    if (st < n_tiles) load_tile(st, st);
+    cp_async_commit();
+  }
+
+  // per-warp state: rows rbase .. rbase+15 (thread rows lane/4 and lane/4 + 8)
+  const int rbase = kDecode ? 0 : warp * 16;
+  const int kw0 = kDecode ? warp * 16 : 0;
+  float o[kDT][4];
+#pragma unroll
+  for (int i = 0; i < kDT; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+  float m_run[2] = {-INFINITY, -INFINITY};
+  float l_run[2] = {0.f, 0.f};
+  int pos[2];
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int rho = row0 + rbase + (lane >> 2) + 8 * h;
+    pos[h] = rho < rows_total ? seq - q_len + rho / a.group : -1;  // -1: padding row
+  }
+  uint32_t qa[D / 16][4];
+  const bool warp_live = kDecode || (row0 + rbase < rows_total);
+
+  for (int ti = 0; ti < n_tiles; ++ti) {
+    cp_async_wait<kStages - 2>();
+    __syncthreads();
+    if (ti + kStages - 1 < n_tiles) load_tile(ti + kStages - 1, (ti + kStages - 1) % kStages);
+    cp_async_commit();
+    if (ti == 0) {
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const int row = rbase + (lane & 7) + ((lane >> 3) & 1) * 8;
+        const int c = kk * 2 + (lane >> 4);
+        ldmatrix_x4(sbase + L::kQ + swz<D>(row, c), qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3]);
+      }
+    }
+    if (!warp_live) continue;
+    const int stage = ti % kStages;
+    const uint32_t sk = sbase + L::kK + stage * L::kKVBytes;
+    const uint32_t sv = sbase + L::kV + stage * L::kKVBytes;
+    const int kt0 = kbeg + ti * kTileKeys;
+
+    // S = Q K^T for this warp's keys
+    float sacc[kNT][4];
+#pragma unroll
+    for (int i = 0; i < kNT; ++i) sacc[i][0] = sacc[i][1] = sacc[i][2] = sacc[i][3] = 0.f;
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk) {
+#pragma unroll
+      for (int np = 0; np < kNT / 2; ++np) {
+        const int key = kw0 + np * 16 + (lane & 7) + (lane >> 4) * 8;
+        const int c = kk * 2 + ((lane >> 3) & 1);
+        uint32_t b0, b1, b2, b3;
+        ldmatrix_x4(sk + swz<D>(key, c), b0, b1, b2, b3);
+        mma_bf16_16816(sacc[2 * np], qa[kk], b0, b1);
+        mma_bf16_16816(sacc[2 * np + 1], qa[kk], b2, b3);
+      }
+    }
+    // mask, online softmax (base 2)
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      float mx = -INFINITY;
+#pragma unroll
+      for (int nt = 0; nt < kNT; ++nt) {
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int kabs = kt0 + kw0 + nt * 8 + (lane & 3) * 2 + e;
+          float& sref = sacc[nt][2 * h + e];
+          sref = (kabs < kend && kabs <= pos[h]) ? sref * a.scale_log2 : -INFINITY;
+          mx = fmaxf(mx, sref);
+        }
+      }
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+      const float m_new = fmaxf(m_run[h], mx);
+      const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
+      const float alpha = exp2f(m_run[h] - m_use);
+      float sum = 0.f;
+#pragma unroll
+      for (int nt = 0; nt < kNT; ++nt) {
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          float& sref = sacc[nt][2 * h + e];
+          sref = exp2f(sref - m_use);
+          sum += sref;
+        }
+      }
+      l_run[h] = l_run[h] * alpha + sum;
+      m_run[h] = m_new;
+#pragma unroll
+      for (int dt = 0; dt < kDT; ++dt) {
+        o[dt][2 * h] *= alpha;
+        o[dt][2 * h + 1] *= alpha;
+      }
+    }
+    // O += P V
+#pragma unroll
+    for (int kk = 0; kk < kWarpKeys / 16; ++kk) {
+      uint32_t pa[4];
+      pa[0] = pack_bf16x2(sacc[2 * kk][0], sacc[2 * kk][1]);
+      pa[1] = pack_bf16x2(sacc[2 * kk][2], sacc[2 * kk][3]);
+      pa[2] = pack_bf16x2(sacc[2 * kk + 1][0], sacc[2 * kk + 1][1]);
+      pa[3] = pack_bf16x2(sacc[2 * kk + 1][2], sacc[2 * kk + 1][3]);
+#pragma unroll
+      for (int dp = 0; dp < kDT / 2; ++dp) {
+        const int key = kw0 + kk * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
+        const int c = dp * 2 + (lane >> 4);
+        uint32_t b0, b1, b2, b3;
+        ldmatrix_x4_trans(sv + swz<D>(key, c), b0, b1, b2, b3);
+        mma_bf16_16816(o[2 * dp], pa, b0, b1);
+        mma_bf16_16816(o[2 * dp + 1], pa, b2, b3);
+      }
+    }
+  }
+  cp_async_wait<0>();
+
+  // row sums across the 4 lanes of each row group
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    l_run[h] += __shfl_xor_sync(0xffffffffu, l_run[h], 1);
+    l_run[h] += __shfl_xor_sync(0xffffffffu, l_run[h], 2);
+  }
+
+  if constexpr (kDecode) {
+    // merge the four warps' (m, l, O) of the same 16 rows
+    __syncthreads();
+    float* s_o = reinterpret_cast<float*>(smem + L::kK);   // [4][16][D]
+    float* s_m = s_o + 4 * 16 * D;                          // [4][16]
+    float* s_l = s_m + 4 * 16;                              // [4][16]
+    if ((lane & 3) == 0) {
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        s_m[warp * 16 + (lane >> 2) + 8 * h] = m_run[h];
+        s_l[warp * 16 + (lane >> 2) + 8 * h] = l_run[h];
+      }
+    }
+    __syncthreads();
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int rr = (lane >> 2) + 8 * h;
+      float mg = -INFINITY;
+#pragma unroll
+      for (int w = 0; w < 4; ++w) mg = fmaxf(mg, s_m[w * 16 + rr]);
+      const float scale = (m_run[h] == -INFINITY) ? 0.f : exp2f(m_run[h] - mg);
+#pragma unroll
+      for (int dt = 0; dt < kDT; ++dt) {
+        const int d = dt * 8 + (lane & 3) * 2;
+        s_o[(warp * 16 + rr) * D + d] = o[dt][2 * h] * scale;
+        s_o[(warp * 16 + rr) * D + d + 1] = o[dt][2 * h + 1] * scale;
+      }
+    }
+    __syncthreads();
+    // all 128 threads: row rr = tid / 8, 8 threads per row, D / 8 columns each
+    const int rr = threadIdx.x >> 3;
+    const int rho = row0 + rr;
+    if (rho < rows_total) {
+      float mg = -INFINITY;
+#pragma unroll
+      for (int w = 0; w < 4; ++w) mg = fmaxf(mg, s_m[w * 16 + rr]);
+      float lsum = 0.f;
+#pragma unroll
+      for (int w = 0; w < 4; ++w) {
+        const float mw = s_m[w * 16 + rr];
+        lsum += (mw == -INFINITY) ? 0.f : s_l[w * 16 + rr] * exp2f(mw - mg);
+      }
+      const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+      const int qi = rho / a.group, j = rho % a.group;
+      const int64_t orow = static_cast<int64_t>(q0 + qi) * a.num_q_heads + g * a.group + j;
+      const int c0 = (threadIdx.x & 7) * (D / 8);
+      float acc[D / 8];
+#pragma unroll
+      for (int e = 0; e < D / 8; ++e) {
+        acc[e] = 0.f;
+#pragma unroll
+        for (int w = 0; w < 4; ++w) acc[e] += s_o[(w * 16 + rr) * D + c0 + e];
+        acc[e] *= inv;
+      }
+      const float lse2 = lsum > 0.f ? mg + log2f(lsum) : -INFINITY;
+      if (a.part_o != nullptr) {
+        const int64_t prow = static_cast<int64_t>(a.part_slot0 + split) * a.total_q *
+                                 a.num_q_heads + orow;
+        float* dst = a.part_o + prow * D + c0;
+#pragma unroll
+        for (int e = 0; e < D / 8; e += 4)
+          *reinterpret_cast<float4*>(dst + e) = make_float4(acc[e], acc[e + 1], acc[e + 2], acc[e + 3]);
+        if ((threadIdx.x & 7) == 0) a.part_lse[prow] = lse2;
+      } else {
+        __nv_bfloat16* dst = a.out + orow * D + c0;
+#pragma unroll
+        for (int e = 0; e < D / 8; e += 8) {
+          uint4 w = make_uint4(pack_bf16x2(acc[e], acc[e + 1]), pack_bf16x2(acc[e + 2], acc[e + 3]),
+                               pack_bf16x2(acc[e + 4], acc[e + 5]),
+                               pack_bf16x2(acc[e + 6], acc[e + 7]));
+          *reinterpret_cast<uint4*>(dst + e) = w;
+        }
+        if ((threadIdx.x & 7) == 0 && a.lse != nullptr)
+          a.lse[orow] = lse2 * 0.69314718055994531f;
+      }
+    }
+  } else {
+    if (!warp_live) return;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int rho = row0 + rbase + (lane >> 2) + 8 * h;
+      if (rho >= rows_total) continue;
+      const int qi = rho / a.group, j = rho % a.group;
+      const int64_t orow = static_cast<int64_t>(q0 + qi) * a.num_q_heads + g * a.group + j;
+      const float inv = l_run[h] > 0.f ? 1.f / l_run[h] : 0.f;
+      const float lse2 = l_run[h] > 0.f ? m_run[h] + log2f(l_run[h]) : -INFINITY;
+      if (a.part_o != nullptr) {
+        const int64_t prow = static_cast<int64_t>(a.part_slot0 + split) * a.total_q *
+                                 a.num_q_heads + orow;
+        float* dst = a.part_o + prow * D;
+#pragma unroll
+        for (int dt = 0; dt < kDT; ++dt) {
+          const int d = dt * 8 + (lane & 3) * 2;
+          *reinterpret_cast<float2*>(dst + d) = make_float2(o[dt][2 * h] * inv, o[dt][2 * h + 1] * inv);
+        }
+        if ((lane & 3) == 0) a.part_lse[prow] = lse2;
+      } else {
+        __nv_bfloat16* dst = a.out + orow * D;
+#pragma unroll
+        for (int dt = 0; dt < kDT; ++dt) {
+          const int d = dt * 8 + (lane & 3) * 2;
+          *reinterpret_cast<uint32_t*>(dst + d) = pack_bf16x2(o[dt][2 * h] * inv, o[dt][2 * h + 1] * inv);
+        }
+        if ((lane & 3) == 0 && a.lse != nullptr) a.lse[orow] = lse2 * 0.69314718055994531f;
+      }
+    }
+  }
+}
+
+template <int D, bool kDecode>
+cudaError_t launch_paged_t(const PagedArgs& a, cudaStream_t stream) {
+  using L = PagedLayout<D, kDecode>;
+  const int smem = L::kEnd;
+  cudaError_t e = cudaFuncSetAttribute(paged_attn_kernel<D, kDecode>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  dim3 grid(a.num_reqs * a.row_tiles, a.num_kv_heads, a.n_splits);
+  paged_attn_kernel<D, kDecode><<<grid, kThreads, smem, stream>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_paged(int head_dim, bool decode, const PagedArgs& a, cudaStream_t stream) {
+  if (head_dim == 64)
+    return decode ? launch_paged_t<64, true>(a, stream) : launch_paged_t<64, false>(a, stream);
+  return decode ? launch_paged_t<128, true>(a, stream) : launch_paged_t<128, false>(a, stream);
+}
+
+}  // namespace csp

@@ -1,0 +1,84 @@
+"""C-ABI checks that need no GPU: the library builds and loads, it exports every
+function include/csp.h declares, and the host-side planner matches the planner
+oracle exactly (it runs no device code)."""
+
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+from oracle import planner
+from shared_prefix_paged_gb300 import csp, workloads
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared_symbols():
+    with open(os.path.join(ROOT, "include", "csp.h"), encoding="utf-8") as f:
+        text = f.read()
+    return sorted(set(re.findall(r"CSP_API\s+[\w\s\*]+?\b(\w+)\s*\(", text)))
+
+
+def test_header_declares_the_binding_exports():
+    assert _declared_symbols() == sorted(csp.EXPORTS)
+
+
+def test_library_loads_and_exports_every_declared_symbol():
+    lib = csp.load()
+    for name in _declared_symbols():
+        assert hasattr(lib, name), name
+        assert ctypes.cast(getattr(lib, name), ctypes.c_void_p).value
+    assert lib.csp_version() >> 16 == 1
+    assert lib.csp_status_string(csp.CSP_ERR_WORKSPACE) == b"CSP_ERR_WORKSPACE"
+
+
+def test_planner_worked_example():
+    # "vLLM Cascade Attention：用法、场景与原理解析" §四, block_size 1
+    bt = np.array([[0, 1, 2, 3, 4, 5], [0, 1, 2, 3, 4, 6]], np.int32)
+    cpl, use = csp.cascade_plan(bt, [6, 6], [3, 4], block_size=1,
+                                mode=csp.MODE_PAGE_THRESHOLDS)
+    assert (cpl, use) == (3, False)
+
+
+@pytest.mark.parametrize("bs", [1, 4, 16])
+def test_planner_matches_oracle_on_random_tables(bs):
+    rng = np.random.default_rng(100 + bs)
+    for _ in range(300):
+        n = int(rng.integers(1, 12))
+        common = int(rng.integers(0, 40))
+        seq = rng.integers(1, 40 * bs, size=n)
+        width = int(-(-seq.max() // bs)) + 3
+        table = rng.integers(0, 3, size=(n, width)).astype(np.int32)
+        common = min(common, width)
+        table[:, :common] = rng.integers(0, 1000, size=common)[None, :]
+        nc = np.array([int(rng.integers(0, s + 1)) for s in seq], np.int32)
+        want = planner.plan(table, seq, nc, bs)
+        got = csp.cascade_plan(table, seq, nc, block_size=bs, mode=csp.MODE_PAGE_THRESHOLDS)
+        assert got == want, (table, seq, nc)
+
+
+@pytest.mark.parametrize("name", ["tiny", "decode", "chunked", "chunked_cap"])
+def test_planner_matches_oracle_on_generated_batches(name):
+    b = workloads.by_name(name)
+    want = planner.plan(b.block_table, b.seq_lens, b.num_computed_tokens, b.block_size)
+    got = csp.cascade_plan(b.block_table, b.seq_lens, b.num_computed_tokens,
+                           block_size=b.block_size, mode=csp.MODE_PAGE_THRESHOLDS)
+    assert got == want
+
+
+def test_planner_modes_and_errors():
+    b = workloads.decode_batch(n=8, p=512, s=32)
+    args = (b.block_table, b.seq_lens, b.num_computed_tokens)
+    assert csp.cascade_plan(*args, mode=csp.MODE_FORCE_FLAT) == (512, False)
+    assert csp.cascade_plan(*args, mode=csp.MODE_FORCE_CASCADE) == (512, True)
+    assert csp.cascade_plan(*args, mode=csp.MODE_AUTO) == (512, True)
+    assert csp.cascade_plan(np.zeros((0, 4), np.int32), [], []) == (0, False)
+    with pytest.raises(csp.CspError) as e:
+        csp.cascade_plan(b.block_table, b.seq_lens, b.seq_lens + 1)   # computed > seq_len
+    assert e.value.status == csp.CSP_ERR_INVALID_ARG
+    with pytest.raises(csp.CspError):
+        csp.cascade_plan(b.block_table[:, :3], b.seq_lens, b.num_computed_tokens)  # row too short
+    with pytest.raises(csp.CspError):
+        csp.cascade_plan(*args, mode=9)
