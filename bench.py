@@ -1,0 +1,676 @@
+#!/usr/bin/env python
+"""Benchmark: cascade attention over a shared-prefix paged KV cache on GB300.
+
+Workload (default): the decode batch of "vLLM Cascade Attention：用法、场景与原理解析"
+§五 — N=64 requests sharing a P=4096-token prefix, each with S=128 private tokens
+(the last one is the single query), 32 query heads, 8 KV heads, head_dim 128, bf16,
+block size 16, shuffled physical blocks.  Synthetic N(0,1) data, seeded.
+
+One step = the host planner (cascade_plan on the block table) + the device path it
+picks (cascade_attn here: prefix kernel, suffix kernel, merge kernel) for one batch.
+Inputs stay resident in HBM; L2 is kept cold by rotating over several copies of the
+KV cache and queries (more bytes than 2x L2 touched between reuses).  Device steps
+are replayed from a CUDA graph of one round of copies; the planner runs on the host
+every step while the GPU executes.
+
+Prints one JSON line (rank 0).  ``--impl reference`` times the CPU oracle instead
+(bounded row samples of the same batch).  Under torchrun every rank runs its own
+batch (weak scaling, no collective on the data path); value = all ranks' queries /
+the slowest rank's time.
+"""
+
+from __future__ import annotations
+
+import argparse
+import ctypes
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "attn queries/s + HBM GB/s (% of roofline), decode N=64 P=4096 S=128"
+UNIT = "queries/s"
+L2_BYTES = 129 * 1024 * 1024
+KERNEL_SOURCES = {
+    "prefix_attn_kernel": ["prefix_attn.cu", "common.cuh"],
+    "paged_attn_kernel": ["paged_attn.cu", "common.cuh"],
+    "combine_kernel": ["combine.cu", "common.cuh"],
+}
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=200)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="decode",
+                    help="decode (N=64 P=4096 S=128), tiny, chunked, long")
+    ap.add_argument("--copies", type=int, default=0, help="input copies (0: enough for 2x L2)")
+    ap.add_argument("--quick", action="store_true",
+                    help="device timing only (no e2e, flat comparison or CPU baseline)")
+    ap.add_argument("--sweep", action="store_true",
+                    help="N x P decode sweep: cascade vs flat at every point, one line each")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    return ap.parse_args(argv)
+
+
+# ----------------------------------------------------------------- distributed --
+class Dist:
+    """Rank bookkeeping; a process group only when launched with WORLD_SIZE > 1."""
+
+    def __init__(self, backend=None):
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+        self.pg = None
+        if self.world > 1:
+            import torch.distributed as dist
+            dist.init_process_group(backend=backend or "nccl")
+            self.pg = dist
+
+    def barrier(self):
+        if self.pg is not None:
+            self.pg.barrier()
+
+    def max(self, x: float) -> float:
+        return self._reduce(x, "max")
+
+    def sum(self, x: float) -> float:
+        return self._reduce(x, "sum")
+
+    def _reduce(self, x, op):
+        if self.pg is None:
+            return float(x)
+        import torch
+        dev = "cuda" if self.pg.get_backend() == "nccl" else "cpu"
+        t = torch.tensor([float(x)], dtype=torch.float64, device=dev)
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX if op == "max" else self.pg.ReduceOp.SUM)
+        return float(t.item())
+
+    def close(self):
+        if self.pg is not None:
+            self.pg.destroy_process_group()
+
+
+def aggregate(dist: Dist, queries_local: float, elapsed_s_local: float):
+    """Whole-job throughput: every rank's queries over the slowest rank's time."""
+    total = dist.sum(queries_local)
+    slowest = dist.max(elapsed_s_local)
+    return total / slowest if slowest > 0 else 0.0, slowest
+
+
+# ---------------------------------------------------------------------- clocks --
+class ClockSampler:
+    """nvidia-smi samples (every 200 ms) kept with their wall-clock timestamps."""
+
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        self.lines = []
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-i", str(gpu_index), "-lms", "200"], stdout=subprocess.PIPE,
+                stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0: float, t1: float) -> dict:
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        inside = [l for (t, l) in self.lines if t0 <= t <= t1 + 0.25]
+        window = "timed region"
+        if not inside:  # region shorter than one sample period: nearest samples
+            near = sorted(self.lines, key=lambda x: min(abs(x[0] - t0), abs(x[0] - t1)))
+            inside = [l for (_, l) in near[:3]]
+            window = "nearest samples (timed region shorter than the 200 ms period)"
+        sm, smax, power, reasons = [], [], [], set()
+        for l in inside:
+            parts = [p.strip() for p in l.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+                power.append(float(parts[3]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
+                    "window": "no samples"}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "power_w_max": max(power) if power else None, "reasons": sorted(reasons),
+                "samples": len(sm), "window": window}
+
+
+# ------------------------------------------------------------------- workloads --
+def make_batch(name: str, rank: int):
+    from shared_prefix_paged_gb300 import workloads
+    if name == "decode":
+        return workloads.decode_batch(seed=1002 + 7919 * rank)
+    if name == "tiny":
+        return workloads.tiny_decode(seed=1001 + 7919 * rank)
+    if name == "chunked":
+        return workloads.chunked_prefill(seed=1003 + 7919 * rank)
+    if name == "long":
+        return workloads.long_prefix(seed=1004 + 7919 * rank)
+    raise SystemExit(f"unknown workload {name}")
+
+
+def kernel_source_sha(kernel: str) -> str:
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES[kernel]:
+        with open(os.path.join(ROOT, "shared_prefix_paged_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def committed_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if the kernel is unchanged."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    try:
+        with open(path, encoding="utf-8") as f:
+            table = json.load(f)
+    except (OSError, ValueError):
+        return None
+    e = table.get(f"{kernel}@{workload}")
+    if not e or e.get("source_sha") != kernel_source_sha(kernel):
+        return None
+    return e.get("bytes_per_launch")
+
+
+class DeviceRun:
+    """Device copies of one batch and the CUDA graphs that replay its steps."""
+
+    def __init__(self, b, copies: int, device):
+        import torch
+        from shared_prefix_paged_gb300 import csp
+        self.b, self.dev, self.R = b, device, copies
+        self.q = [b.q.to(device) for _ in range(copies)]
+        self.k = [b.k_cache.to(device) for _ in range(copies)]
+        self.v = [b.v_cache.to(device) for _ in range(copies)]
+        self.bt = torch.from_numpy(b.block_table).to(device)
+        self.cu = torch.from_numpy(b.cu_seqlens_q).to(device)
+        self.sl = torch.from_numpy(b.seq_lens).to(device)
+        self.out = [torch.empty_like(self.q[0]) for _ in range(copies)]
+        self.lse = [torch.empty((b.total_q, b.num_q_heads), dtype=torch.float32, device=device)
+                    for _ in range(copies)]
+        lib = csp.load()
+        # host planner with pre-made ctypes arguments
+        self._bt_h = np.ascontiguousarray(b.block_table, dtype=np.int32)
+        self._sl_h = np.ascontiguousarray(b.seq_lens, dtype=np.int32)
+        self._nc_h = np.ascontiguousarray(b.num_computed_tokens, dtype=np.int32)
+        self._cpl = ctypes.c_int32(0)
+        self._use = ctypes.c_int32(0)
+        self._plan_fn = lib.cascade_plan
+        self._plan_args = (ctypes.c_void_p(self._bt_h.ctypes.data), self._bt_h.shape[1],
+                           b.num_reqs, ctypes.c_void_p(self._sl_h.ctypes.data),
+                           ctypes.c_void_p(self._nc_h.ctypes.data), b.block_size,
+                           b.num_q_heads, b.num_kv_heads, b.head_dim, 0, csp.MODE_AUTO,
+                           ctypes.byref(self._cpl), ctypes.byref(self._use))
+        self.plan()
+        self.cpl, self.use_cascade = int(self._cpl.value), bool(self._use.value)
+        need = max(csp.workspace_size(b.num_reqs, b.total_q, b.max_seqlen_q, b.max_seqlen_k,
+                                      c, b.num_q_heads, b.num_kv_heads, b.head_dim)
+                   for c in (0, self.cpl))
+        self.ws = csp.alloc_workspace(need, device)
+
+    def plan(self):
+        st = self._plan_fn(*self._plan_args)
+        if st != 0:
+            raise RuntimeError(f"cascade_plan failed: {st}")
+
+    def step(self, i: int, path: str, events=None):
+        from shared_prefix_paged_gb300 import csp
+        b = self.b
+        common = dict(max_seqlen_q=b.max_seqlen_q, max_seqlen_k=b.max_seqlen_k,
+                      softmax_scale=b.scale, out=self.out[i], lse=self.lse[i], workspace=self.ws)
+        if path == "cascade":
+            csp.cascade_attn(self.q[i], self.k[i], self.v[i], self.bt, self.cu, self.sl,
+                             common_prefix_len=self.cpl, phase_events=events, **common)
+        else:
+            csp.paged_attn(self.q[i], self.k[i], self.v[i], self.bt, self.cu, self.sl, **common)
+
+    def graph(self, path: str, n_steps: int, events=None):
+        import torch
+        s = torch.cuda.Stream(self.dev)
+        s.wait_stream(torch.cuda.current_stream(self.dev))
+        with torch.cuda.stream(s):
+            for i in range(n_steps):
+                self.step(i % self.R, path, events[i] if events else None)
+        torch.cuda.current_stream(self.dev).wait_stream(s)
+        torch.cuda.synchronize(self.dev)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for i in range(n_steps):
+                self.step(i % self.R, path, events[i] if events else None)
+        return g
+
+
+def time_graph_steps(run: DeviceRun, path: str, steps: int, warmup: int, dist: Dist,
+                     with_planner=True, clocks=None):
+    """Replay `steps` device steps from graphs; returns (elapsed_s, host_s, t0, t1)."""
+    import torch
+    R = run.R
+    g = run.graph(path, R)
+    tail = steps % R
+    g_tail = run.graph(path, tail) if tail else None
+    for _ in range(max(1, math.ceil(warmup / R))):
+        g.replay()
+    torch.cuda.synchronize(run.dev)
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    dist.barrier()
+    torch.cuda.synchronize(run.dev)
+    t0 = time.time()
+    h0 = time.perf_counter()
+    start.record()
+    for _ in range(steps // R):
+        if with_planner:
+            for _ in range(R):
+                run.plan()
+        g.replay()
+    if g_tail is not None:
+        if with_planner:
+            for _ in range(tail):
+                run.plan()
+        g_tail.replay()
+    end.record()
+    h1 = time.perf_counter()
+    torch.cuda.synchronize(run.dev)
+    t1 = time.time()
+    dist.barrier()
+    return start.elapsed_time(end) / 1e3, h1 - h0, t0, t1
+
+
+def phase_times(run: DeviceRun, rounds: int = 16, batches: int = 3):
+    """Average device time of each kernel of a cascade step, from CUDA events recorded
+    by cascade_attn_timed between its kernels on the launching stream.  A GPU sleep
+    queued first lets the host enqueue every step before the GPU reaches them, so the
+    steps run back to back with no host gaps inside the event intervals."""
+    import torch
+    R = run.R
+    n_steps = R * rounds
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(n_steps)]
+    for evs in events:       # torch creates the CUDA event on its first record
+        for ev in evs:
+            ev.record()
+    for i in range(R):       # warm
+        run.step(i, "cascade")
+    torch.cuda.synchronize(run.dev)
+    acc = np.zeros(3)
+    n = 0
+    for _ in range(batches):
+        torch.cuda._sleep(50_000_000)   # ~25 ms of GPU time while the host enqueues
+        for i in range(n_steps):
+            run.step(i % R, "cascade", events[i])
+        torch.cuda.synchronize(run.dev)
+        for ev in events:
+            acc += [ev[0].elapsed_time(ev[1]), ev[1].elapsed_time(ev[2]),
+                    ev[2].elapsed_time(ev[3])]
+            n += 1
+    ms = acc / n
+    return {"prefix_attn_kernel": ms[0] * 1e3, "paged_attn_kernel": ms[1] * 1e3,
+            "combine_kernel": ms[2] * 1e3, "launches_averaged": n}
+
+
+def e2e_steps(run: DeviceRun, steps: int):
+    """Public-API steps from pinned host buffers: H2D of q and the batch metadata, host
+    planner, cascade_attn, D2H of out and lse, then the host waits for the result."""
+    import torch
+    from shared_prefix_paged_gb300 import csp
+    b = run.b
+    q_h = b.q.pin_memory()
+    bt_h = torch.from_numpy(b.block_table).pin_memory()
+    cu_h = torch.from_numpy(b.cu_seqlens_q).pin_memory()
+    sl_h = torch.from_numpy(b.seq_lens).pin_memory()
+    out_h = torch.empty(b.q.shape, dtype=torch.bfloat16).pin_memory()
+    lse_h = torch.empty((b.total_q, b.num_q_heads), dtype=torch.float32).pin_memory()
+    q_d = torch.empty_like(run.q[0])
+    bt_d, cu_d, sl_d = torch.empty_like(run.bt), torch.empty_like(run.cu), torch.empty_like(run.sl)
+    out_d, lse_d = run.out[0], run.lse[0]
+    h2d = sum(t.numel() * t.element_size() for t in (q_h, bt_h, cu_h, sl_h))
+    d2h = out_h.numel() * 2 + lse_h.numel() * 4
+    stream = torch.cuda.current_stream(run.dev)
+
+    def one(i):
+        q_d.copy_(q_h, non_blocking=True)
+        bt_d.copy_(bt_h, non_blocking=True)
+        cu_d.copy_(cu_h, non_blocking=True)
+        sl_d.copy_(sl_h, non_blocking=True)
+        cpl, use = csp.cascade_plan(b.block_table, b.seq_lens, b.num_computed_tokens,
+                                    block_size=b.block_size, num_q_heads=b.num_q_heads,
+                                    num_kv_heads=b.num_kv_heads, head_dim=b.head_dim)
+        kw = dict(max_seqlen_q=b.max_seqlen_q, max_seqlen_k=b.max_seqlen_k,
+                  softmax_scale=b.scale, out=out_d, lse=lse_d, workspace=run.ws)
+        if use:
+            csp.cascade_attn(q_d, run.k[i], run.v[i], bt_d, cu_d, sl_d, common_prefix_len=cpl,
+                             **kw)
+        else:
+            csp.paged_attn(q_d, run.k[i], run.v[i], bt_d, cu_d, sl_d, **kw)
+        out_h.copy_(out_d, non_blocking=True)
+        lse_h.copy_(lse_d, non_blocking=True)
+        stream.synchronize()
+
+    for i in range(5):
+        one(i % run.R)
+    t0 = time.perf_counter()
+    for s in range(steps):
+        one(s % run.R)
+    el = time.perf_counter() - t0
+    return b.total_q * steps / el, h2d, d2h, steps
+
+
+def cpu_oracle_rate(b, seconds: float, rng_seed=0):
+    """The oracle as it stands on this host's cores: rows (token, head) sampled from the
+    batch, as many as fill about `seconds`; returns (queries/s, threads, rows)."""
+    import oracle
+    threads = os.cpu_count() or 1
+    rng = np.random.default_rng(rng_seed)
+    total = b.total_q * b.num_q_heads
+
+    def run_rows(n):
+        flat = rng.choice(total, size=min(n, total), replace=n > total)
+        rows = np.stack([flat // b.num_q_heads, flat % b.num_q_heads], 1).astype(np.int32)
+        t0 = time.perf_counter()
+        oracle.attention(b.q, b.k_cache, b.v_cache, b.block_table, b.cu_seqlens_q, b.seq_lens,
+                         b.scale, rows=rows, n_threads=threads)
+        return time.perf_counter() - t0
+
+    n = max(threads, 16)
+    el = run_rows(n)
+    # grow the sample until one run fills about `seconds` (thread start-up dominates
+    # small probes, so estimate from the previous run each time)
+    while el < 0.7 * seconds and n < 400 * total:
+        n = int(min(400 * total, max(2 * n, n * seconds / max(el, 1e-6))))
+        el = run_rows(n)
+    return (n / b.num_q_heads) / el, threads, n
+
+
+def roofline_entry(kernel, us, b, run, peaks, workload, n_parts):
+    """Algorithmic bytes (and flops) per launch of a kernel of the cascade step."""
+    from shared_prefix_paged_gb300 import accounting
+    rows = b.total_q * b.num_q_heads
+    kvtok = accounting.kv_bytes_per_token(b.num_kv_heads, b.head_dim)
+    q_bytes = rows * b.head_dim * 2
+    partial = rows * (b.head_dim + 1) * 4
+    cpl = run.cpl
+    if kernel == "prefix_attn_kernel":
+        bytes_ = cpl * kvtok + q_bytes + partial
+        flops = accounting.prefix_flops(b.total_q, b.num_q_heads, b.head_dim, cpl)
+    elif kernel == "paged_attn_kernel":
+        bytes_ = int((b.seq_lens.astype(np.int64) - cpl).sum()) * kvtok + q_bytes + partial
+        flops = None
+    else:
+        bytes_ = n_parts * partial + rows * (b.head_dim * 2 + 4)
+        flops = None
+    gbs = bytes_ / (us * 1e-6) / 1e9
+    hbm_frac = gbs / peaks["hbm_gbs"]
+    entry = {"kernel": kernel, "bound": "hbm", "achieved": round(gbs, 1),
+             "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": round(hbm_frac, 4),
+             "peak_source": "measured (MEASURED_PEAKS.json hbm_gbs)",
+             "algorithmic_bytes_per_launch": int(bytes_), "us_per_launch": round(us, 3),
+             "traffic": committed_traffic(kernel, workload)}
+    if flops:
+        tf = flops / (us * 1e-6) / 1e12
+        tfrac = tf / peaks["bf16_tflops"]
+        entry["tensor"] = {"achieved": round(tf, 1), "peak": peaks["bf16_tflops"],
+                           "unit": "TFLOP/s", "frac": round(tfrac, 4),
+                           "flops_per_launch": int(flops)}
+        if tfrac > hbm_frac:
+            entry.update(bound="tensor", achieved=round(tf, 1), peak=peaks["bf16_tflops"],
+                         unit="TFLOP/s", frac=round(tfrac, 4),
+                         peak_source="measured (MEASURED_PEAKS.json bf16_tflops, burst)")
+    return entry
+
+
+def load_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json"), encoding="utf-8") as f:
+            p = json.load(f)
+        return {"hbm_gbs": float(p["hbm_gbs"]), "bf16_tflops": float(p["bf16_tflops"]),
+                "source": "measured"}
+    except (OSError, KeyError, ValueError):
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "source": "fallback"}
+
+
+def default_copies(b):
+    """Copies of q and the KV pool so that > 2x L2 is touched between reuses of one."""
+    per_copy = (b.k_cache.numel() + b.v_cache.numel() + b.q.numel()) * 2
+    return int(min(8, max(2, math.ceil(2 * L2_BYTES / max(per_copy, 1)) + 1)))
+
+
+# ------------------------------------------------------------------------ arms --
+def run_ours(args, dist: Dist):
+    import torch
+    from shared_prefix_paged_gb300 import accounting, csp
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU")
+    torch.cuda.set_device(dist.local_rank)
+    device = torch.device("cuda", dist.local_rank)
+    csp.load()
+    b = make_batch(args.workload, dist.rank)
+    R = args.copies or default_copies(b)
+    run = DeviceRun(b, R, device)
+    path = "cascade" if run.use_cascade else "flat"
+    peaks = load_peaks()
+    K, W = args.steps, max(3, args.warmup)
+
+    clocks = ClockSampler(dist.local_rank) if dist.rank == 0 else None
+    time.sleep(0.5 if clocks else 0.0)
+    elapsed, host_s, t0, t1 = time_graph_steps(run, path, K, W, dist)
+    if clocks:
+        clocks.stop()
+    qps, slowest = aggregate(dist, b.total_q * K, elapsed)
+    us_call = elapsed / K * 1e6
+    min_bytes = accounting.cascade_min_bytes(b, run.cpl if path == "cascade" else 0)
+    kv_bytes = (accounting.cascade_kv_tokens(b.seq_lens, run.cpl) if path == "cascade"
+                else accounting.flat_kv_tokens(b.seq_lens)) * accounting.kv_bytes_per_token(
+                    b.num_kv_heads, b.head_dim)
+    result = {
+        "metric": METRIC, "value": round(qps, 1), "unit": UNIT, "n_gpus": dist.world,
+        "steps": K, "warmup": W, "ms_per_step": round(slowest / K * 1e3, 6),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) bf16 Q/K/V, shuffled physical blocks)",
+        "config": {
+            "workload": b.name, "num_reqs": b.num_reqs, "total_q": b.total_q,
+            "common_prefix_len": run.cpl, "q_heads": b.num_q_heads, "kv_heads": b.num_kv_heads,
+            "head_dim": b.head_dim, "block_size": b.block_size, "path": path,
+            "l2": f"inputs larger than L2: {R} rotating copies of q and the KV cache",
+            "step": "host cascade_plan + device path replayed from a CUDA graph of "
+                    f"{R} steps", "parallelism": f"replicas x{dist.world}"},
+        "us_per_call": round(us_call, 3),
+        "kv_gbs": round(kv_bytes / (us_call * 1e-6) / 1e9, 1),
+        "min_bytes_per_call": int(min_bytes),
+        "hbm_frac_of_measured": round(min_bytes / (us_call * 1e-6) / 1e9 / peaks["hbm_gbs"], 4),
+        "hbm_frac_of_8tbs": round(min_bytes / (us_call * 1e-6) / 1e9 / 8000.0, 4),
+        "host_s_in_timed_region": round(host_s, 4),
+        "gpu_launches": K * (3 if path == "cascade" else 1),
+    }
+    if clocks:
+        result["clocks"] = clocks.summary(t0, t1)
+
+    if path == "cascade":
+        ph = phase_times(run)
+        kernels = ["prefix_attn_kernel", "paged_attn_kernel", "combine_kernel"]
+        # partial count, for the combine's algorithmic bytes: prefix + suffix splits
+        n_parts = _n_parts(b, run.cpl)
+        entries = {k: roofline_entry(k, ph[k], b, run, peaks, b.name, n_parts) for k in kernels}
+        dominant = max(kernels, key=lambda k: ph[k])
+        result["roofline"] = entries[dominant]
+        result["phases_us"] = {k: round(ph[k], 3) for k in kernels}
+        result["phases_roofline"] = {k: {kk: entries[k][kk] for kk in
+                                         ("bound", "achieved", "unit", "frac")}
+                                     for k in kernels}
+        result["phase_launches_averaged"] = ph["launches_averaged"]
+
+    if not args.quick:
+        # the standard (flat) path on the same batch, for the cascade speedup
+        fe, _, _, _ = time_graph_steps(run, "flat", max(R, min(K, 2000)), W, dist,
+                                       with_planner=False)
+        flat_us = fe / max(R, min(K, 2000)) * 1e6
+        result["flat"] = {"us_per_call": round(flat_us, 3),
+                          "speedup_cascade_over_flat": round(flat_us / us_call, 3),
+                          "kv_bytes": int(accounting.flat_kv_tokens(b.seq_lens) *
+                                          accounting.kv_bytes_per_token(b.num_kv_heads,
+                                                                        b.head_dim))}
+        e_qps, h2d, d2h, e_steps = e2e_steps(run, min(K, 3000))
+        e_total, _ = aggregate(dist, e_qps, 1.0)
+        result["e2e"] = {"value": round(e_total, 1), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                         "d2h_bytes_per_step": d2h, "steps": e_steps,
+                         "note": "pinned host q + block table + cu_seqlens + seq_lens in, "
+                                 "out + lse back, host waits each step; KV cache resident"}
+        if dist.rank == 0 and dist.world == 1:
+            rate, threads, rows = cpu_oracle_rate(b, args.cpu_seconds)
+            result["cpu_baseline"] = {"value": round(rate, 3), "unit": UNIT, "cores": threads,
+                                      "kind": "oracle",
+                                      "sample": f"{rows} random (token, head) rows of the "
+                                                f"same batch, fp64 C oracle, {threads} threads"}
+    return result
+
+
+def _n_parts(b, cpl):
+    """Partial slots the combine reads, from the workspace size of the call."""
+    from shared_prefix_paged_gb300 import csp
+    need = csp.workspace_size(b.num_reqs, b.total_q, b.max_seqlen_q, b.max_seqlen_k, cpl,
+                              b.num_q_heads, b.num_kv_heads, b.head_dim)
+    rows = b.total_q * b.num_q_heads
+    per = rows * (b.head_dim + 1) * 4
+    return max(1, round((need - 256) / per))
+
+
+def run_reference(args, dist: Dist):
+    """The CPU oracle as the reference arm: each step a bounded row sample."""
+    import oracle
+    b = make_batch(args.workload, 0)
+    threads = os.cpu_count() or 1
+    K, W = args.steps, max(3, args.warmup)
+    total = b.total_q * b.num_q_heads
+    rng = np.random.default_rng(0)
+
+    def sample(n):
+        flat = rng.choice(total, size=n, replace=n > total)
+        return np.stack([flat // b.num_q_heads, flat % b.num_q_heads], 1).astype(np.int32)
+
+    n = max(threads, 16)
+    while True:   # per-row cost at a sample size where thread start-up is amortised
+        t0 = time.perf_counter()
+        oracle.attention(b.q, b.k_cache, b.v_cache, b.block_table, b.cu_seqlens_q, b.seq_lens,
+                         b.scale, rows=sample(n), n_threads=threads)
+        el = time.perf_counter() - t0
+        if el > 1.0 or n >= total:
+            break
+        n = min(total, 4 * n)
+    per_row = el / n
+    budget = 120.0  # seconds for the whole run
+    rows_per_step = int(max(1, min(total, budget / (K + W) / max(per_row, 1e-9))))
+    for _ in range(W):
+        oracle.attention(b.q, b.k_cache, b.v_cache, b.block_table, b.cu_seqlens_q,
+                         b.seq_lens, b.scale, rows=sample(rows_per_step), n_threads=threads)
+    t0 = time.perf_counter()
+    for _ in range(K):
+        oracle.attention(b.q, b.k_cache, b.v_cache, b.block_table, b.cu_seqlens_q,
+                         b.seq_lens, b.scale, rows=sample(rows_per_step), n_threads=threads)
+    el = time.perf_counter() - t0
+    qps = rows_per_step * K / b.num_q_heads / el
+    sample_desc = (f"{rows_per_step} random (token, head) rows per step of the same batch, "
+                   f"fp64 C oracle, {threads} threads")
+    return {"impl": "reference", "metric": METRIC, "value": round(qps, 3), "unit": UNIT,
+            "n_gpus": dist.world, "steps": K, "warmup": W,
+            "ms_per_step": round(el / K * 1e3, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": b.name, "num_reqs": b.num_reqs, "total_q": b.total_q,
+                       "q_heads": b.num_q_heads, "kv_heads": b.num_kv_heads,
+                       "head_dim": b.head_dim, "block_size": b.block_size},
+            "cpu_baseline": {"value": round(qps, 3), "unit": UNIT, "cores": threads,
+                             "kind": "oracle", "sample": sample_desc},
+            "e2e": {"value": round(qps, 3), "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+
+
+def run_sweep(args, dist: Dist):
+    """Cascade vs flat at every point of the N x P decode grid (S=128)."""
+    import torch
+    from shared_prefix_paged_gb300 import accounting, csp, workloads
+    torch.cuda.set_device(dist.local_rank)
+    device = torch.device("cuda", dist.local_rank)
+    for n in workloads.SWEEP_N:
+        for p in workloads.SWEEP_P:
+            b = workloads.sweep_point(n, p)
+            R = args.copies or default_copies(b)
+            run = DeviceRun(b, R, device)
+            steps = max(R, min(args.steps, 600))
+            pc, _ = csp.cascade_plan(b.block_table, b.seq_lens, b.num_computed_tokens,
+                                     mode=csp.MODE_PAGE_THRESHOLDS)
+            ce, _, _, _ = time_graph_steps(run, "cascade", steps, args.warmup, dist, False)
+            fe, _, _, _ = time_graph_steps(run, "flat", steps, args.warmup, dist, False)
+            line = {"sweep": True, "N": n, "P": p, "S": 128, "cpl": run.cpl,
+                    "cascade_us": round(ce / steps * 1e6, 3), "flat_us": round(fe / steps * 1e6, 3),
+                    "speedup": round(fe / ce, 3),
+                    "auto_pick": "cascade" if run.use_cascade else "flat",
+                    "pages_rule_pick": "cascade" if pc >= 256 and n >= 8 else "flat",
+                    "kv_ratio": round(accounting.flat_kv_tokens(b.seq_lens) /
+                                      accounting.cascade_kv_tokens(b.seq_lens, run.cpl), 2)}
+            if dist.rank == 0:
+                print(json.dumps(line), flush=True)
+            del run
+            torch.cuda.empty_cache()
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        # rank 0 alone runs the CPU oracle; other ranks exit without work
+        if int(os.environ.get("RANK", "0")) != 0:
+            return 0
+        os.environ["WORLD_SIZE"] = "1"
+        print(json.dumps(run_reference(args, Dist())), flush=True)
+        return 0
+    dist = Dist()
+    try:
+        if args.sweep:
+            run_sweep(args, dist)
+            return 0
+        res = run_ours(args, dist)
+        if dist.rank == 0:
+            print(json.dumps(res), flush=True)
+        return 0
+    finally:
+        dist.close()
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -165,6 +165,8 @@ def _attn(fn_name, q, k_cache, v_cache, block_table, cu_seqlens_q, seqused_k, *,
              workspace.numel(), _stream_ptr(stream, q.device)]
     if phase_events is not None:
         fn_name = "cascade_attn_timed"
+        if len(phase_events) != 4 or any(ev.cuda_event == 0 for ev in phase_events):
+            raise ValueError("phase_events: four created CUDA events (record each once first)")
         handles = (ctypes.c_void_p * 4)(*[ev.cuda_event for ev in phase_events])
         args.append(ctypes.cast(handles, ctypes.c_void_p))
     _check(getattr(lib, fn_name)(*args), fn_name)

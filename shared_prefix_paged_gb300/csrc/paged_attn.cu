@@ -355,8 +355,8 @@ template <int D, bool kDecode>
 cudaError_t launch_paged_t(const PagedArgs& a, cudaStream_t stream) {
   using L = PagedLayout<D, kDecode>;
   const int smem = L::kEnd;
-  cudaError_t e = cudaFuncSetAttribute(paged_attn_kernel<D, kDecode>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  static std::atomic<uint64_t> attr_done{0};
+  cudaError_t e = set_smem_once(paged_attn_kernel<D, kDecode>, smem, attr_done);
   if (e != cudaSuccess) return e;
   dim3 grid(a.num_reqs * a.row_tiles, a.num_kv_heads, a.n_splits);
   paged_attn_kernel<D, kDecode><<<grid, kThreads, smem, stream>>>(a);

@@ -298,8 +298,8 @@ static cudaError_t launch_prefix_d(const CUtensorMap& tm_q, const CUtensorMap& t
                                    const CUtensorMap& tm_v, const PrefixArgs& a,
                                    cudaStream_t stream) {
   const int smem = Layout<D>::kDynamic;
-  cudaError_t e = cudaFuncSetAttribute(prefix_attn_kernel<D>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  static std::atomic<uint64_t> attr_done{0};
+  cudaError_t e = set_smem_once(prefix_attn_kernel<D>, smem, attr_done);
   if (e != cudaSuccess) return e;
   const int grid = a.m_tiles * a.n_splits * a.num_kv_heads;
   prefix_attn_kernel<D><<<grid, kThreads, smem, stream>>>(tm_q, tm_k, tm_v, a);
