@@ -189,6 +189,37 @@ CSP_API int cascade_attn_timed(const void* q, const void* k_cache, const void* v
                                void* const* phase_events);
 
 /*
+ * cascade_attn_noalloc — cascade_attn for callers that cannot allocate device memory.
+ * The pages have no counterpart: this is a deployment convenience of this library.
+ *
+ * Who needs it: code that runs attention where cudaMalloc is off limits, such as an
+ * engine that hands out all device memory from its own pool up front, a plugin
+ * inside a framework that owns every allocation, or a latency-critical loop where an
+ * allocation could synchronise the device.  Such a caller passes inputs and outputs
+ * exactly as for cascade_attn, but no workspace: the library uses a fixed 16 MiB
+ * array of its own device memory instead (reserved on each GPU where the library's
+ * device code is loaded, and held until the process exits).  Nothing is allocated
+ * or freed by this call.
+ *
+ * The first call on a device looks up that array's device address (once per device,
+ * with the device current); make that first call before any stream capture.  Every
+ * call on a device shares the one array: calls that can run at the same time on the
+ * GPU (different streams, no ordering between them) race and corrupt each other's
+ * results; order them on one stream.  The array keeps the previous call's contents;
+ * each call clears the status word at its start itself.  A batch whose workspace
+ * (csp_workspace_size) exceeds 16 MiB is rejected with CSP_ERR_WORKSPACE before
+ * anything is launched.  Other arguments, layouts and errors: as for cascade_attn.
+ */
+CSP_API int cascade_attn_noalloc(const void* q, const void* k_cache, const void* v_cache,
+                                 int32_t num_blocks, const int32_t* block_table,
+                                 int64_t bt_row_stride, const int32_t* cu_seqlens_q,
+                                 const int32_t* seqused_k, int32_t num_reqs, int32_t total_q,
+                                 int32_t max_seqlen_q, int32_t max_seqlen_k,
+                                 int32_t common_prefix_len, int32_t block_size,
+                                 int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                                 float softmax_scale, void* out, float* lse, void* stream);
+
+/*
  * paged_attn — the standard path (§五, §十): request r attends causally to all of
  * its KV positions [0, seqused_k[r]) through its own block_table row.  Arguments
  * as for cascade_attn, without common_prefix_len.

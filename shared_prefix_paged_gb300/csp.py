@@ -30,7 +30,7 @@ DTYPE_BF16, DTYPE_F32 = 0, 1
 # every symbol include/csp.h declares
 EXPORTS = ("cascade_plan", "csp_workspace_size", "cascade_attn", "cascade_attn_timed",
            "paged_attn", "merge_states", "csp_workspace_status", "csp_status_string",
-           "csp_last_cuda_error", "csp_version")
+           "csp_last_cuda_error", "csp_version", "cascade_attn_noalloc")
 
 _lock = threading.Lock()
 _lib: Optional[ctypes.CDLL] = None
