@@ -7,7 +7,8 @@ Workload (default): the decode batch of "vLLM Cascade Attentionï¼šç”¨æ³•ã€åœºæ™
 block size 16, shuffled physical blocks.  Synthetic N(0,1) data, seeded.
 
 One step = the host planner (cascade_plan on the block table) + the device path it
-picks (cascade_attn here: prefix kernel, suffix kernel, merge kernel) for one batch.
+picks (cascade_attn here: a prefix kernel and a suffix kernel that run concurrently
+and finish the LSE merge themselves) for one batch.
 Inputs stay resident in HBM; L2 is kept cold by rotating over several copies of the
 KV cache and queries (more bytes than 2x L2 touched between reuses).  Device steps
 are replayed from a CUDA graph of one round of copies; the planner runs on the host
@@ -44,10 +45,10 @@ METRIC = "attn queries/s + HBM GB/s (% of roofline), decode N=64 P=4096 S=128"
 UNIT = "queries/s"
 L2_BYTES = 129 * 1024 * 1024
 KERNEL_SOURCES = {
-    "prefix_attn_kernel": ["prefix_attn.cu", "common.cuh"],
-    "paged_attn_kernel": ["paged_attn.cu", "common.cuh"],
-    "combine_kernel": ["combine.cu", "common.cuh"],
+    "prefix_attn_kernel": ["prefix_attn.cu", "common.cuh", "merge.cuh"],
+    "paged_attn_kernel": ["paged_attn.cu", "common.cuh", "merge.cuh"],
 }
+KERNELS = list(KERNEL_SOURCES)
 
 
 def parse_args(argv=None):
@@ -317,7 +318,8 @@ def time_graph_steps(run: DeviceRun, path: str, steps: int, warmup: int, dist: D
 
 def phase_times(run: DeviceRun, rounds: int = 16, batches: int = 3):
     """Average device time of each kernel of a cascade step, from CUDA events recorded
-    by cascade_attn_timed between its kernels on the launching stream.  A GPU sleep
+    by cascade_attn_timed between its kernels on the launching stream (with events
+    between them the two kernels run back to back instead of overlapping).  A GPU sleep
     queued first lets the host enqueue every step before the GPU reaches them, so the
     steps run back to back with no host gaps inside the event intervals."""
     import torch
@@ -330,7 +332,7 @@ def phase_times(run: DeviceRun, rounds: int = 16, batches: int = 3):
     for i in range(R):       # warm
         run.step(i, "cascade")
     torch.cuda.synchronize(run.dev)
-    acc = np.zeros(3)
+    acc = np.zeros(2)
     n = 0
     for _ in range(batches):
         torch.cuda._sleep(50_000_000)   # ~25 ms of GPU time while the host enqueues
@@ -338,12 +340,11 @@ def phase_times(run: DeviceRun, rounds: int = 16, batches: int = 3):
             run.step(i % R, "cascade", events[i])
         torch.cuda.synchronize(run.dev)
         for ev in events:
-            acc += [ev[0].elapsed_time(ev[1]), ev[1].elapsed_time(ev[2]),
-                    ev[2].elapsed_time(ev[3])]
+            acc += [ev[0].elapsed_time(ev[1]), ev[1].elapsed_time(ev[2])]
             n += 1
     ms = acc / n
     return {"prefix_attn_kernel": ms[0] * 1e3, "paged_attn_kernel": ms[1] * 1e3,
-            "combine_kernel": ms[2] * 1e3, "launches_averaged": n}
+            "launches_averaged": n}
 
 
 def e2e_steps(run: DeviceRun, steps: int):
@@ -402,7 +403,7 @@ def cpu_oracle_rate(b, seconds: float, rng_seed=0):
     total = b.total_q * b.num_q_heads
 
     def run_rows(n):
-        flat = rng.choice(total, size=min(n, total), replace=n > total)
+        flat = rng.choice(total, size=n, replace=n > total)
         rows = np.stack([flat // b.num_q_heads, flat % b.num_q_heads], 1).astype(np.int32)
         t0 = time.perf_counter()
         oracle.attention(b.q, b.k_cache, b.v_cache, b.block_table, b.cu_seqlens_q, b.seq_lens,
@@ -419,28 +420,27 @@ def cpu_oracle_rate(b, seconds: float, rng_seed=0):
     return (n / b.num_q_heads) / el, threads, n
 
 
-def roofline_entry(kernel, us, b, run, peaks, workload, n_parts):
+def roofline_entry(kernel, us, b, run, peaks, workload):
     """Algorithmic bytes (and flops) per launch of a kernel of the cascade step."""
     from shared_prefix_paged_gb300 import accounting
     rows = b.total_q * b.num_q_heads
     kvtok = accounting.kv_bytes_per_token(b.num_kv_heads, b.head_dim)
     q_bytes = rows * b.head_dim * 2
-    partial = rows * (b.head_dim + 1) * 4
     cpl = run.cpl
     if kernel == "prefix_attn_kernel":
-        bytes_ = cpl * kvtok + q_bytes + partial
+        # prefix KV once, q, and one partial per row (bf16 O, fp32 LSE)
+        bytes_ = cpl * kvtok + q_bytes + rows * (b.head_dim * 2 + 4)
         flops = accounting.prefix_flops(b.total_q, b.num_q_heads, b.head_dim, cpl)
-    elif kernel == "paged_attn_kernel":
-        bytes_ = int((b.seq_lens.astype(np.int64) - cpl).sum()) * kvtok + q_bytes + partial
-        flops = None
     else:
-        bytes_ = n_parts * partial + rows * (b.head_dim * 2 + 4)
+        # each request's KV after the prefix, q, and the final bf16 output + LSE
+        bytes_ = (int((b.seq_lens.astype(np.int64) - cpl).sum()) * kvtok + q_bytes +
+                  rows * (b.head_dim * 2 + 4))
         flops = None
     gbs = bytes_ / (us * 1e-6) / 1e9
     hbm_frac = gbs / peaks["hbm_gbs"]
     entry = {"kernel": kernel, "bound": "hbm", "achieved": round(gbs, 1),
              "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": round(hbm_frac, 4),
-             "peak_source": "measured (MEASURED_PEAKS.json hbm_gbs)",
+             "peak_source": f"{peaks['source']} (MEASURED_PEAKS.json hbm_gbs)",
              "algorithmic_bytes_per_launch": int(bytes_), "us_per_launch": round(us, 3),
              "traffic": committed_traffic(kernel, workload)}
     if flops:
@@ -452,7 +452,8 @@ def roofline_entry(kernel, us, b, run, peaks, workload, n_parts):
         if tfrac > hbm_frac:
             entry.update(bound="tensor", achieved=round(tf, 1), peak=peaks["bf16_tflops"],
                          unit="TFLOP/s", frac=round(tfrac, 4),
-                         peak_source="measured (MEASURED_PEAKS.json bf16_tflops, burst)")
+                         peak_source=f"{peaks['source']} (MEASURED_PEAKS.json bf16_tflops, "
+                                     "burst)")
     return entry
 
 
@@ -517,23 +518,20 @@ def run_ours(args, dist: Dist):
         "hbm_frac_of_measured": round(min_bytes / (us_call * 1e-6) / 1e9 / peaks["hbm_gbs"], 4),
         "hbm_frac_of_8tbs": round(min_bytes / (us_call * 1e-6) / 1e9 / 8000.0, 4),
         "host_s_in_timed_region": round(host_s, 4),
-        "gpu_launches": K * (3 if path == "cascade" else 1),
+        "gpu_launches": K * (2 if path == "cascade" else 1),
     }
     if clocks:
         result["clocks"] = clocks.summary(t0, t1)
 
     if path == "cascade":
         ph = phase_times(run)
-        kernels = ["prefix_attn_kernel", "paged_attn_kernel", "combine_kernel"]
-        # partial count, for the combine's algorithmic bytes: prefix + suffix splits
-        n_parts = _n_parts(b, run.cpl)
-        entries = {k: roofline_entry(k, ph[k], b, run, peaks, b.name, n_parts) for k in kernels}
-        dominant = max(kernels, key=lambda k: ph[k])
+        entries = {k: roofline_entry(k, ph[k], b, run, peaks, b.name) for k in KERNELS}
+        dominant = max(KERNELS, key=lambda k: ph[k])
         result["roofline"] = entries[dominant]
-        result["phases_us"] = {k: round(ph[k], 3) for k in kernels}
+        result["phases_us"] = {k: round(ph[k], 3) for k in KERNELS}
         result["phases_roofline"] = {k: {kk: entries[k][kk] for kk in
                                          ("bound", "achieved", "unit", "frac")}
-                                     for k in kernels}
+                                     for k in KERNELS}
         result["phase_launches_averaged"] = ph["launches_averaged"]
 
     if not args.quick:
@@ -559,16 +557,6 @@ def run_ours(args, dist: Dist):
                                       "sample": f"{rows} random (token, head) rows of the "
                                                 f"same batch, fp64 C oracle, {threads} threads"}
     return result
-
-
-def _n_parts(b, cpl):
-    """Partial slots the combine reads, from the workspace size of the call."""
-    from shared_prefix_paged_gb300 import csp
-    need = csp.workspace_size(b.num_reqs, b.total_q, b.max_seqlen_q, b.max_seqlen_k, cpl,
-                              b.num_q_heads, b.num_kv_heads, b.head_dim)
-    rows = b.total_q * b.num_q_heads
-    per = rows * (b.head_dim + 1) * 4
-    return max(1, round((need - 256) / per))
 
 
 def run_reference(args, dist: Dist):

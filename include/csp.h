@@ -127,8 +127,10 @@ CSP_API int cascade_plan(const int32_t* block_table, int64_t bt_row_stride, int3
  * csp_workspace_size — bytes of device workspace that cascade_attn (with this
  * common_prefix_len) or paged_attn (common_prefix_len = 0) needs for this batch
  * shape on the current device.  All arguments are host integers, the same as the
- * attention call will get.  The workspace holds the split partial results and a
- * status word; it must be 256-byte aligned and zero-filled before its first use.
+ * attention call will get.  The workspace holds a status word, one counter per
+ * (query token, KV head) and the split partial results; it must be 256-byte aligned
+ * and zero-filled before its first use (for the status word: each call clears its
+ * counters itself, so one workspace may serve batches of different shapes).
  * Returns CSP_OK and writes *bytes_out, or CSP_ERR_INVALID_ARG / CSP_ERR_CUDA.
  */
 CSP_API int csp_workspace_size(int32_t num_reqs, int32_t total_q, int32_t max_seqlen_q,
@@ -172,9 +174,12 @@ CSP_API int cascade_attn(const void* q, const void* k_cache, const void* v_cache
 /*
  * cascade_attn_timed — cascade_attn plus four CUDA events recorded on `stream`
  * between its kernels, for timing each phase: phase_events[0] before the
- * prefix-phase kernel, [1] after it, [2] after the suffix-phase kernel, [3] after
- * the merge kernel.  phase_events is a host array of four cudaEvent_t created by
- * the caller (with timing enabled).  Arguments and results are otherwise those of
+ * prefix-phase kernel, [1] after it, [2] after the suffix-phase kernel (whose CTAs
+ * finish the LSE merge), [3] at the end of the call (the same point as [2]).
+ * phase_events is a host array of four cudaEvent_t created by the caller (with
+ * timing enabled).  With events between them, the two kernels run one after the
+ * other instead of overlapping, so the per-phase times add up to more than a
+ * cascade_attn call takes.  Arguments and results are otherwise those of
  * cascade_attn; with common_prefix_len == 0, events [0] and [1] mark the same point.
  */
 CSP_API int cascade_attn_timed(const void* q, const void* k_cache, const void* v_cache,

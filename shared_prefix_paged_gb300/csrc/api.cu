@@ -20,7 +20,7 @@ int cuda_fail(cudaError_t e) {
 
 constexpr int kPage = 16;
 constexpr size_t kHeaderBytes = 256;  // status word + reserved
-constexpr int kMaxSplits = 32;
+constexpr int kMaxSplits = 32;  // suffix splits; with the prefix's slots at most 32 partials per row
 
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 int64_t cdiv64(int64_t a, int64_t b) { return (a + b - 1) / b; }
@@ -96,14 +96,14 @@ int check_shape(int num_reqs, int total_q, int max_q, int max_k, int Hq, int Hkv
 // How one attention call is cut into CTAs and where its partials live.
 struct LaunchPlan {
   int group = 1;
-  // prefix phase (tcgen05)
-  int p_m_tiles = 0, p_splits = 0, p_tiles_per_split = 0;
+  // prefix phase (tcgen05): 256-row units x key ranges, one slot per range
+  int p_pairs = 0, p_splits = 0, p_tiles_per_split = 0, p_slots = 0;
   // paged phase (suffix or standard path)
   bool decode = true;
   int s_row_tiles = 1, s_splits = 1, s_split_keys = 64;
   bool direct = false;  // paged kernel writes the final output itself
-  int n_parts = 0;
-  size_t off_part_o = 0, off_part_lse = 0, bytes = 0;
+  int n_parts = 0;      // partial results per row group
+  size_t off_counters = 0, off_part_o = 0, off_part_lse = 0, bytes = 0;
 };
 
 void make_plan(int num_reqs, int total_q, int max_q, int max_k, int cpl, int Hq, int Hkv, int D,
@@ -112,24 +112,23 @@ void make_plan(int num_reqs, int total_q, int max_q, int max_k, int cpl, int Hq,
   p.group = Hq / Hkv;
   if (cpl > 0) {
     const int rows = total_q * p.group;
-    p.p_m_tiles = cdiv(rows, 128);
-    const int key_tiles = cdiv(cpl, 128);
-    const int base = p.p_m_tiles * Hkv;
-    // choose the split count by waves x per-CTA length (+1 tile of fixed cost)
-    int best_s = 1;
+    p.p_pairs = cdiv(rows, 256);
+    const int key_tiles = cdiv(cpl, 64);
+    const int base = p.p_pairs * Hkv;
+    // key ranges by waves x per-CTA length (+3 tiles of fixed cost: set-up, the
+    // partial write-out and the row-group merge); a prefix CTA takes a whole SM
     int64_t best_cost = -1;
-    for (int s = 1; s <= std::min(key_tiles, kMaxSplits); ++s) {
-      const int tps = cdiv(key_tiles, s);
-      const int s_eff = cdiv(key_tiles, tps);
-      const int64_t ctas = static_cast<int64_t>(base) * s_eff;
-      const int64_t cost = cdiv64(ctas, sms) * (tps + 1);
+    for (int s = 1; s <= 16; s *= 2) {
+      if (s > 1 && s > key_tiles) break;
+      const int64_t ctas = static_cast<int64_t>(base) * s;
+      const int64_t cost = cdiv64(ctas, sms) * (cdiv(key_tiles, s) + 3);
       if (best_cost < 0 || cost < best_cost) {
         best_cost = cost;
-        best_s = s_eff;
+        p.p_splits = s;
       }
     }
-    p.p_tiles_per_split = cdiv(key_tiles, best_s);
-    p.p_splits = cdiv(key_tiles, p.p_tiles_per_split);
+    p.p_tiles_per_split = cdiv(key_tiles, p.p_splits);
+    p.p_slots = p.p_splits;
   }
   p.decode = static_cast<int64_t>(max_q) * p.group <= 16;
   const int rows_per_cta = p.decode ? 16 : 64;
@@ -137,15 +136,17 @@ void make_plan(int num_reqs, int total_q, int max_q, int max_k, int cpl, int Hq,
   const int max_len = std::max(0, max_k - cpl);
   const int key_tiles = std::max(1, cdiv(max_len, 64));
   const int64_t units = static_cast<int64_t>(num_reqs) * p.s_row_tiles * Hkv;
-  int s = units > 0 ? static_cast<int>(std::min<int64_t>(cdiv64(2LL * sms, units), kMaxSplits)) : 1;
+  const int max_s = std::min(kMaxSplits, 32 - p.p_slots);
+  int s = units > 0 ? static_cast<int>(std::min<int64_t>(cdiv64(2LL * sms, units), max_s)) : 1;
   s = std::max(1, std::min(s, key_tiles));
   p.s_split_keys = cdiv(key_tiles, s) * 64;
   p.s_splits = std::max(1, cdiv(std::max(max_len, 1), p.s_split_keys));
   p.direct = (cpl == 0 && p.s_splits == 1);
-  p.n_parts = p.direct ? 0 : p.p_splits + p.s_splits;
+  p.n_parts = p.direct ? 0 : p.p_slots + p.s_splits;
   const size_t rows_total = static_cast<size_t>(total_q) * Hq;
-  p.off_part_o = kHeaderBytes;
-  p.off_part_lse = p.off_part_o + align256(static_cast<size_t>(p.n_parts) * rows_total * D * 4);
+  p.off_counters = kHeaderBytes;
+  p.off_part_o = p.off_counters + align256(static_cast<size_t>(total_q) * Hkv * 4);
+  p.off_part_lse = p.off_part_o + align256(static_cast<size_t>(p.n_parts) * rows_total * D * 2);
   p.bytes = p.off_part_lse + align256(static_cast<size_t>(p.n_parts) * rows_total * 4);
   *P = p;
 }
@@ -182,7 +183,8 @@ int attention_call(const void* q, const void* k_cache, const void* v_cache, int3
   cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   int* status = reinterpret_cast<int*>(ws);
-  float* part_o = reinterpret_cast<float*>(ws + P.off_part_o);
+  int* counters = reinterpret_cast<int*>(ws + P.off_counters);
+  __nv_bfloat16* part_o = reinterpret_cast<__nv_bfloat16*>(ws + P.off_part_o);
   float* part_lse = reinterpret_cast<float*>(ws + P.off_part_lse);
   const float scale_log2 = scale * 1.4426950408889634f;
   cudaError_t e;
@@ -190,6 +192,12 @@ int attention_call(const void* q, const void* k_cache, const void* v_cache, int3
     return events ? cudaEventRecord(static_cast<cudaEvent_t>(events[i]), stream) : cudaSuccess;
   };
   if ((e = mark(0)) != cudaSuccess) return cuda_fail(e);
+  // row-group counters start at zero in every call, whatever the workspace held
+  // (only several suffix splits count themselves)
+  if (P.n_parts > 0 && P.s_splits > 1 &&
+      (e = cudaMemsetAsync(counters, 0, static_cast<size_t>(total_q) * Hkv * sizeof(int32_t),
+                           stream)) != cudaSuccess)
+    return cuda_fail(e);
 
   if (cpl > 0) {
     CUtensorMap tm_q, tm_k, tm_v;
@@ -211,7 +219,7 @@ int attention_call(const void* q, const void* k_cache, const void* v_cache, int3
     pa.num_kv_heads = Hkv;
     pa.group = P.group;
     pa.cpl = cpl;
-    pa.m_tiles = P.p_m_tiles;
+    pa.pairs = P.p_pairs;
     pa.n_splits = P.p_splits;
     pa.tiles_per_split = P.p_tiles_per_split;
     pa.scale_log2 = scale_log2;
@@ -243,22 +251,17 @@ int attention_call(const void* q, const void* k_cache, const void* v_cache, int3
   ga.scale_log2 = scale_log2;
   ga.part_o = P.direct ? nullptr : part_o;
   ga.part_lse = P.direct ? nullptr : part_lse;
-  ga.part_slot0 = P.p_splits;
+  ga.n_prefix = P.p_slots;
+  ga.counters = counters;
   ga.out = static_cast<__nv_bfloat16*>(out);
   ga.lse = lse;
-  if ((e = csp::launch_paged(D, P.decode, ga, stream)) != cudaSuccess) return cuda_fail(e);
+  // concurrent with the prefix kernel (programmatic dependent launch) unless phase
+  // events sit between the two
+  const bool overlap = cpl > 0 && events == nullptr;
+  if ((e = csp::launch_paged(D, P.decode, ga, overlap, stream)) != cudaSuccess)
+    return cuda_fail(e);
   if ((e = mark(2)) != cudaSuccess) return cuda_fail(e);
 
-  if (!P.direct) {
-    csp::CombineArgs ca;
-    ca.part_o = part_o;
-    ca.part_lse = part_lse;
-    ca.n_parts = P.n_parts;
-    ca.rows = total_q * Hq;
-    ca.out = static_cast<__nv_bfloat16*>(out);
-    ca.lse = lse;
-    if ((e = csp::launch_combine(D, ca, stream)) != cudaSuccess) return cuda_fail(e);
-  }
   if ((e = mark(3)) != cudaSuccess) return cuda_fail(e);
   return CSP_OK;
 }

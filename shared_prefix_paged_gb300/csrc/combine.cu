@@ -1,71 +1,19 @@
-// combine.cu — LSE merging of partial attention results.
+// combine.cu — the merge_states entry point's kernel: LSE merge of two partials.
 //
 // "vLLM Cascade Attention：用法、场景与原理解析" §一 and §八 Step 5 (merge_attn_states):
 // partial results over disjoint key sets combine by log-sum-exp rescaling,
-//   m = max_p l_p,  w_p = e^(l_p - m),  out = sum_p w_p o_p / sum_p w_p,
-//   lse = m + ln(sum_p w_p).
-// §九 (FlashDecoding) uses the same rescaling to merge the splits of one key range,
-// so a single n-way pass merges the prefix splits, the suffix splits and the final
-// prefix/suffix pair at once.
-//
-// Both kernels are elementwise and HBM-bound: one warp (combine) or D/8 threads
-// (merge_states) per output row, 16-byte vector loads and stores, fp32 math.
+//   m = max(l1, l2),  w_i = e^(l_i - m),  out = (w1 o1 + w2 o2) / (w1 + w2),
+//   lse = m + ln(w1 + w2).
+// Elementwise and HBM-bound: D/8 threads per output row, 16-byte vector loads and
+// stores, fp32 math.  (Inside cascade_attn the same merge runs in the attention
+// kernels themselves, see merge.cuh.)
 #include "common.cuh"
 #include "kernels.cuh"
 
 namespace csp {
 namespace {
 
-constexpr float kLn2 = 0.69314718055994531f;
 constexpr float kLog2e = 1.4426950408889634f;
-
-// Partials: o [n_parts][rows][D] fp32 (normalised), lse [n_parts][rows] log2 domain.
-template <int D>
-__global__ void __launch_bounds__(256) combine_kernel(const CombineArgs a) {
-  constexpr int kPer = D / 32;  // features per lane
-  const int row = blockIdx.x * 8 + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
-  if (row >= a.rows) return;
-  float m = -INFINITY;
-  for (int p = lane; p < a.n_parts; p += 32)
-    m = fmaxf(m, __ldg(a.part_lse + static_cast<int64_t>(p) * a.rows + row));
-#pragma unroll
-  for (int s = 16; s > 0; s >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, s));
-  float acc[kPer];
-#pragma unroll
-  for (int e = 0; e < kPer; ++e) acc[e] = 0.f;
-  float wsum = 0.f;
-  if (m != -INFINITY) {
-    for (int p = 0; p < a.n_parts; ++p) {
-      const float lp = __ldg(a.part_lse + static_cast<int64_t>(p) * a.rows + row);
-      if (lp == -INFINITY) continue;  // empty split: weight 0, its o is never read
-      const float w = exp2f(lp - m);
-      wsum += w;
-      const float* src = a.part_o + (static_cast<int64_t>(p) * a.rows + row) * D + lane * kPer;
-      if constexpr (kPer == 4) {
-        const float4 v = __ldg(reinterpret_cast<const float4*>(src));
-        acc[0] += w * v.x;
-        acc[1] += w * v.y;
-        acc[2] += w * v.z;
-        acc[3] += w * v.w;
-      } else {
-        const float2 v = __ldg(reinterpret_cast<const float2*>(src));
-        acc[0] += w * v.x;
-        acc[1] += w * v.y;
-      }
-    }
-  }
-  const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
-  __nv_bfloat16* dst = a.out + static_cast<int64_t>(row) * D + lane * kPer;
-  if constexpr (kPer == 4) {
-    *reinterpret_cast<uint2*>(dst) =
-        make_uint2(pack_bf16x2(acc[0] * inv, acc[1] * inv), pack_bf16x2(acc[2] * inv, acc[3] * inv));
-  } else {
-    *reinterpret_cast<uint32_t*>(dst) = pack_bf16x2(acc[0] * inv, acc[1] * inv);
-  }
-  if (lane == 0 && a.lse != nullptr)
-    a.lse[row] = wsum > 0.f ? (m + log2f(wsum)) * kLn2 : -INFINITY;
-}
 
 // Two partials with natural-log LSEs (the merge_states entry point).  Each thread
 // handles 8 features of one row.
@@ -125,16 +73,6 @@ __global__ void __launch_bounds__(256)
 }
 
 }  // namespace
-
-cudaError_t launch_combine(int head_dim, const CombineArgs& a, cudaStream_t stream) {
-  const int grid = (a.rows + 7) / 8;
-  if (grid == 0) return cudaSuccess;
-  if (head_dim == 64)
-    combine_kernel<64><<<grid, 256, 0, stream>>>(a);
-  else
-    combine_kernel<128><<<grid, 256, 0, stream>>>(a);
-  return cudaGetLastError();
-}
 
 cudaError_t launch_merge_states(__nv_bfloat16* out, float* out_lse, const void* o1,
                                 const float* l1, const void* o2, const float* l2, int rows,

@@ -11,9 +11,10 @@ namespace csp {
 
 // Prefix phase ("vLLM Cascade Attention：用法、场景与原理解析" §八 Step 5, Phase 1):
 // every query row of the batch against KV positions [0, cpl) of block_table row 0,
-// no causal mask.  Rows are (token, head-in-group) pairs of one KV head packed into
-// 128-row tiles; each CTA takes one tile, one KV head and a range of 128-key tiles
-// and writes a normalised fp32 partial and its log2-sum-exp.
+// no causal mask.  Rows are (token, head-in-group) pairs of one KV head; a CTA owns
+// 256 of them (two 128-row M tiles).  The prefix's 64-key tiles are cut into
+// n_splits ranges, one CTA and one workspace slot each; the suffix kernel merges
+// those slots with its own partials (merge.cuh).
 struct PrefixArgs {
   const int32_t* block_table;  // row 0: the shared pages
   int total_q;
@@ -21,12 +22,12 @@ struct PrefixArgs {
   int num_kv_heads;
   int group;             // num_q_heads / num_kv_heads
   int cpl;               // common prefix length, multiple of 16
-  int m_tiles;           // ceil(total_q * group / 128)
-  int n_splits;          // key splits per (tile, KV head)
-  int tiles_per_split;   // 128-key tiles per split
+  int pairs;             // ceil(total_q * group / 256): 256-row units per KV head
+  int n_splits;          // key ranges per (unit, KV head)
+  int tiles_per_split;   // 64-key tiles per range
   float scale_log2;      // softmax_scale * log2(e)
-  float* part_o;         // [n_splits][total_q][num_q_heads][D]
-  float* part_lse;       // [n_splits][total_q][num_q_heads], log2 domain
+  __nv_bfloat16* part_o; // [n_parts][total_q][num_q_heads][D], normalised; slots [0, n_splits)
+  float* part_lse;       // [n_parts][total_q][num_q_heads], log2 domain
   int* status;           // workspace status word
 };
 
@@ -50,30 +51,21 @@ struct PagedArgs {
   int n_splits;
   int row_tiles;         // CTAs along the packed rows of one request
   float scale_log2;
-  float* part_o;         // partial mode: [slots][total_q][Hq][D] (slot = part_slot0 + split)
-  float* part_lse;       //               [slots][total_q][Hq], log2 domain
-  int part_slot0;
-  __nv_bfloat16* out;    // direct mode (part_o == nullptr): final output
-  float* lse;            //               natural-log LSE or nullptr
-};
-
-// Combine n_parts partial results per row into the final bf16 output and LSE.
-struct CombineArgs {
-  const float* part_o;
-  const float* part_lse;
-  int n_parts;
-  int rows;              // total_q * num_q_heads
-  __nv_bfloat16* out;
-  float* lse;            // natural log, or nullptr
+  __nv_bfloat16* part_o; // partial mode: [n_prefix + n_splits][total_q][Hq][D] (own slot: n_prefix + split)
+  float* part_lse;       //               [n_prefix + n_splits][total_q][Hq], log2 domain
+  int n_prefix;          //               prefix slots before the suffix ones (0: none)
+  int* counters;         //               row-group counters (merge.cuh)
+  __nv_bfloat16* out;    // final output: direct mode (part_o == nullptr) or last contributor
+  float* lse;            // natural-log LSE or nullptr
 };
 
 cudaError_t launch_prefix(int head_dim, const CUtensorMap& tm_q, const CUtensorMap& tm_k,
                           const CUtensorMap& tm_v, const PrefixArgs& a, cudaStream_t stream);
-size_t prefix_smem_bytes(int head_dim);
 
-cudaError_t launch_paged(int head_dim, bool decode, const PagedArgs& a, cudaStream_t stream);
-
-cudaError_t launch_combine(int head_dim, const CombineArgs& a, cudaStream_t stream);
+// after_prefix: launched right behind this call's prefix kernel on the same stream
+// (programmatic dependent launch, so it runs concurrently with it).
+cudaError_t launch_paged(int head_dim, bool decode, const PagedArgs& a, bool after_prefix,
+                         cudaStream_t stream);
 
 cudaError_t launch_merge_states(__nv_bfloat16* out, float* out_lse, const void* o1,
                                 const float* l1, const void* o2, const float* l2, int rows,

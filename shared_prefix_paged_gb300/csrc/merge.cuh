@@ -1,0 +1,125 @@
+// merge.cuh — in-kernel LSE merge of the partial results of a row group.
+//
+// A row group is one query token and one KV head: the `group` query heads that read
+// that KV head.  The prefix phase leaves one partial per key range in workspace
+// slots [0, n_prefix); every key split of the suffix phase (or of the standard
+// path) leaves one in the slots after them.  A partial is the normalised output in
+// bf16 plus its log2-sum-exp in fp32.  The suffix kernel waits for the prefix grid
+// (programmatic dependent launch) before it merges, and its splits count themselves
+// in the group's counter: the last one merges every slot ("vLLM Cascade Attention：
+// 用法、场景与原理解析" §一 and §八 Step 5, merge_attn_states: out = sum_p e^(l_p - m)
+// o_p / sum_p e^(l_p - m), lse = m + ln sum_p e^(l_p - m)) and writes bf16 out and
+// the natural-log LSE.  The host clears the counters before each call.
+#pragma once
+
+#include "common.cuh"
+
+namespace csp {
+
+// Most partial results one row group can have (one lane each in the merge).
+constexpr int kMaxParts = 32;
+
+struct MergeArgs {
+  const __nv_bfloat16* part_o;  // [n_parts][rows][D], normalised
+  const float* part_lse;        // [n_parts][rows], log2 domain; -inf: empty
+  int* counters;                // [total_q * num_kv_heads], zero at the start of the call
+  int n_parts;                  // slots merged per row (<= kMaxParts)
+  int n_count;                  // contributors counted per row group (suffix splits)
+  int rows;                     // total_q * num_q_heads
+  int num_q_heads;
+  int num_kv_heads;
+  int group;
+  __nv_bfloat16* out;           // [total_q][num_q_heads][D]
+  float* lse;                   // [total_q][num_q_heads] natural log, or nullptr
+};
+
+// Add 1 with acquire-release semantics at GPU scope: the partial results this CTA
+// wrote before (ordered by a CTA barrier) are published, and those the other
+// contributors published become visible to this CTA.
+__device__ __forceinline__ int atomic_add_acq_rel_gpu(int* p, int v) {
+  int old;
+  asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v)
+               : "memory");
+  return old;
+}
+
+__device__ __forceinline__ float4 load_bf16x4_cg(const __nv_bfloat16* p) {
+  const uint2 u = __ldcg(reinterpret_cast<const uint2*>(p));
+  const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.x));
+  const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.y));
+  return make_float4(a.x, a.y, b.x, b.y);
+}
+
+__device__ __forceinline__ void store_bf16x4(__nv_bfloat16* p, float4 v) {
+  *reinterpret_cast<uint2*>(p) = make_uint2(pack_bf16x2(v.x, v.y), pack_bf16x2(v.z, v.w));
+}
+
+// Merge one output row with one warp.  Slots [0, n_parts) come from the workspace;
+// `own` / `own_lse` (when own_lse is not -inf or has_own is set) is one more partial
+// held in registers, features [4 lane, 4 lane + 4).  Lane p holds slot p's weight,
+// then lane c accumulates features [4c, 4c+4) over all partials.
+template <int D>
+__device__ __forceinline__ void merge_row_warp(const MergeArgs& m, int64_t row, int lane,
+                                               bool has_own, float4 own, float own_lse) {
+  const float lp = lane < m.n_parts
+                       ? __ldcg(m.part_lse + static_cast<int64_t>(lane) * m.rows + row)
+                       : -INFINITY;
+  float mx = fmaxf(lp, has_own ? own_lse : -INFINITY);
+#pragma unroll
+  for (int s = 16; s > 0; s >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, s));
+  const float w = (mx == -INFINITY || lp == -INFINITY) ? 0.f : fast_exp2(lp - mx);
+  const float w_own =
+      (!has_own || mx == -INFINITY || own_lse == -INFINITY) ? 0.f : fast_exp2(own_lse - mx);
+  float wsum = w;
+#pragma unroll
+  for (int s = 16; s > 0; s >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, s);
+  wsum += w_own;
+  const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (w_own != 0.f) {
+    acc = make_float4(w_own * own.x, w_own * own.y, w_own * own.z, w_own * own.w);
+  }
+#pragma unroll 4
+  for (int p = 0; p < m.n_parts; ++p) {
+    const float wp = __shfl_sync(0xffffffffu, w, p);
+    if (lane < D / 4 && wp != 0.f) {
+      const float4 o = load_bf16x4_cg(m.part_o + (static_cast<int64_t>(p) * m.rows + row) * D +
+                                      lane * 4);
+      acc.x += wp * o.x;
+      acc.y += wp * o.y;
+      acc.z += wp * o.z;
+      acc.w += wp * o.w;
+    }
+  }
+  if (lane < D / 4)
+    store_bf16x4(m.out + row * D + lane * 4,
+                 make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv));
+  if (lane == 0 && m.lse != nullptr)
+    m.lse[row] = wsum > 0.f ? (mx + log2f(wsum)) * 0.69314718055994531f : -INFINITY;
+}
+
+// Called by every thread of the CTA (it contains __syncthreads) after the CTA wrote
+// its partial rows for tokens [t_first, t_first + n_tokens) of KV head g.
+// s_last: shared scratch of at least n_tokens ints.
+template <int D>
+__device__ __forceinline__ void count_and_merge(const MergeArgs& m, int t_first, int n_tokens,
+                                                int g, int* s_last) {
+  const int tid = threadIdx.x;
+  const int nthr = blockDim.x;
+  __syncthreads();  // every partial row of this CTA is written
+  for (int i = tid; i < n_tokens; i += nthr) {
+    int* c = m.counters + static_cast<int64_t>(t_first + i) * m.num_kv_heads + g;
+    s_last[i] = atomic_add_acq_rel_gpu(c, 1) == m.n_count - 1;
+  }
+  __syncthreads();
+  const int warp = tid >> 5, lane = tid & 31, nwarps = nthr >> 5;
+  for (int k = warp; k < n_tokens * m.group; k += nwarps) {
+    const int i = k / m.group;
+    if (!s_last[i]) continue;
+    const int64_t row = static_cast<int64_t>(t_first + i) * m.num_q_heads + g * m.group +
+                        k % m.group;
+    merge_row_warp<D>(m, row, lane, false, make_float4(0.f, 0.f, 0.f, 0.f), -INFINITY);
+  }
+}
+
+}  // namespace csp

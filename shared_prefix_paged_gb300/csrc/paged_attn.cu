@@ -17,10 +17,13 @@
 //    of every tile and merge (max, sum, O) through shared memory at the end;
 //    prefill rows: each warp owns 16 rows of a 64-row tile;
 //  * split-KV (FlashDecoding, §九) over long ranges: each split writes a normalised
-//    fp32 partial + log2-sum-exp for the combine kernel; a single split of the
-//    standard path writes bf16 output and the natural-log LSE directly.
+//    bf16 partial + log2-sum-exp and the last split of a row group merges them with
+//    the prefix phase's partials (merge.cuh); a single split merges its own result
+//    in registers; the standard path with one split writes bf16 output and the
+//    natural-log LSE directly.
 #include "common.cuh"
 #include "kernels.cuh"
+#include "merge.cuh"
 
 namespace csp {
 namespace {
@@ -28,7 +31,6 @@ namespace {
 constexpr int kTileKeys = 64;
 constexpr int kPage = 16;
 constexpr int kThreads = 128;
-constexpr int kStages = 3;
 
 template <int D>
 __device__ __forceinline__ uint32_t swz(int row, int chunk) {
@@ -38,15 +40,21 @@ __device__ __forceinline__ uint32_t swz(int row, int chunk) {
 
 template <int D, bool kDecode>
 struct PagedLayout {
+  // decode CTAs keep two 64-key tiles in flight (68 KB for D=128), so three fit on
+  // an SM, or one beside a prefix-phase CTA; prefill CTAs keep three
+  static constexpr int kStages = kDecode ? 2 : 3;
   static constexpr int kRows = kDecode ? 16 : 64;
   static constexpr int kQBytes = kRows * D * 2;
   static constexpr int kKVBytes = kTileKeys * D * 2;
   static constexpr int kQ = 0;
   static constexpr int kK = kQ + kQBytes;
   static constexpr int kV = kK + kStages * kKVBytes;
-  static constexpr int kEnd = kV + kStages * kKVBytes;
-  // decode merge scratch (reuses the K/V stages after the last tile)
-  static constexpr int kMergeBytes = 4 * 16 * D * 4 + 2 * 4 * 16 * 4;
+  static constexpr int kLast = kV + kStages * kKVBytes;   // int [64] row-group flags
+  static constexpr int kEnd = kLast + 64 * 4;
+  // decode merge scratch (reuses the K/V stages after the last tile): per warp 16
+  // rows of D floats with a padded stride, then per-warp max and sum
+  static constexpr int kORow = D + 8;
+  static constexpr int kMergeBytes = 4 * 16 * kORow * 4 + 2 * 4 * 16 * 4;
   static_assert(!kDecode || kMergeBytes <= 2 * kStages * kKVBytes, "merge scratch");
 };
 
@@ -54,6 +62,7 @@ template <int D, bool kDecode>
 __global__ void __launch_bounds__(kThreads)
     paged_attn_kernel(const PagedArgs a) {
   using L = PagedLayout<D, kDecode>;
+  constexpr int kStages = L::kStages;
   constexpr int kChunks = D / 8;               // 16-byte chunks per row
   constexpr int kWarpKeys = kDecode ? 16 : 64; // keys of a tile each warp handles
   constexpr int kNT = kWarpKeys / 8;           // S n-tiles per warp
@@ -82,7 +91,6 @@ __global__ void __launch_bounds__(kThreads)
   kend = min(kend, seq - q_len + last_query + 1);
   const int n_tiles = kend > kbeg ? (kend - kbeg + kTileKeys - 1) / kTileKeys : 0;
 
-  const int64_t kv_tok_stride = static_cast<int64_t>(a.num_kv_heads) * D;
   const int32_t* bt_row = a.block_table + static_cast<int64_t>(r) * a.bt_stride;
   const uint32_t sbase = smem_u32(smem);
 
@@ -119,8 +127,10 @@ __global__ void __launch_bounds__(kThreads)
     }
     cp_async_16(smem + L::kQ + swz<D>(row, c), a.q + off, ok ? 16u : 0u);
   }
+  // every stage in flight from the start; a stage is refilled right after its
+  // tile has been consumed
 #pragma unroll
-  for (int st = 0; st < kStages - 1; ++st) {
+  for (int st = 0; st < kStages; ++st) {
     if (st < n_tiles) load_tile(st, st);
     cp_async_commit();
   }
@@ -143,10 +153,8 @@ __global__ void __launch_bounds__(kThreads)
   const bool warp_live = kDecode || (row0 + rbase < rows_total);
 
   for (int ti = 0; ti < n_tiles; ++ti) {
-    cp_async_wait<kStages - 2>();
+    cp_async_wait<kStages - 1>();  // groups 0..ti (tile ti, and Q with tile 0) landed
     __syncthreads();
-    if (ti + kStages - 1 < n_tiles) load_tile(ti + kStages - 1, (ti + kStages - 1) % kStages);
-    cp_async_commit();
     if (ti == 0) {
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
@@ -155,7 +163,7 @@ __global__ void __launch_bounds__(kThreads)
         ldmatrix_x4(sbase + L::kQ + swz<D>(row, c), qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3]);
       }
     }
-    if (!warp_live) continue;
+    if (warp_live) {
     const int stage = ti % kStages;
     const uint32_t sk = sbase + L::kK + stage * L::kKVBytes;
     const uint32_t sv = sbase + L::kV + stage * L::kKVBytes;
@@ -232,6 +240,10 @@ __global__ void __launch_bounds__(kThreads)
         mma_bf16_16816(o[2 * dp + 1], pa, b2, b3);
       }
     }
+    }  // warp_live
+    __syncthreads();  // every warp is done with this stage
+    if (ti + kStages < n_tiles) load_tile(ti + kStages, ti % kStages);
+    cp_async_commit();
   }
   cp_async_wait<0>();
 
@@ -241,12 +253,29 @@ __global__ void __launch_bounds__(kThreads)
     l_run[h] += __shfl_xor_sync(0xffffffffu, l_run[h], 1);
     l_run[h] += __shfl_xor_sync(0xffffffffu, l_run[h], 2);
   }
+  const bool partial = a.part_o != nullptr;
+  constexpr float kLn2 = 0.69314718055994531f;
+  MergeArgs m;
+  m.part_o = a.part_o;
+  m.part_lse = a.part_lse;
+  m.counters = a.counters;
+  m.n_parts = a.n_prefix + a.n_splits;
+  m.n_count = a.n_splits;
+  m.rows = a.total_q * a.num_q_heads;
+  m.num_q_heads = a.num_q_heads;
+  m.num_kv_heads = a.num_kv_heads;
+  m.group = a.group;
+  m.out = a.out;
+  m.lse = a.lse;
+  // one suffix split: this CTA merges its rows itself, in registers, with the prefix
+  // slots; several splits: write a partial and let the last split merge
+  const bool merge_in_place = partial && a.n_splits == 1;
 
   if constexpr (kDecode) {
-    // merge the four warps' (m, l, O) of the same 16 rows
+    // merge the four warps' (m, l, O) of the same 16 rows through shared memory
     __syncthreads();
-    float* s_o = reinterpret_cast<float*>(smem + L::kK);   // [4][16][D]
-    float* s_m = s_o + 4 * 16 * D;                          // [4][16]
+    float* s_o = reinterpret_cast<float*>(smem + L::kK);   // [4][16][kORow]
+    float* s_m = s_o + 4 * 16 * L::kORow;                   // [4][16]
     float* s_l = s_m + 4 * 16;                              // [4][16]
     if ((lane & 3) == 0) {
 #pragma unroll
@@ -262,19 +291,22 @@ __global__ void __launch_bounds__(kThreads)
       float mg = -INFINITY;
 #pragma unroll
       for (int w = 0; w < 4; ++w) mg = fmaxf(mg, s_m[w * 16 + rr]);
-      const float scale = (m_run[h] == -INFINITY) ? 0.f : exp2f(m_run[h] - mg);
+      const float sc = (m_run[h] == -INFINITY) ? 0.f : exp2f(m_run[h] - mg);
+      float* dst = s_o + (warp * 16 + rr) * L::kORow;
 #pragma unroll
       for (int dt = 0; dt < kDT; ++dt) {
         const int d = dt * 8 + (lane & 3) * 2;
-        s_o[(warp * 16 + rr) * D + d] = o[dt][2 * h] * scale;
-        s_o[(warp * 16 + rr) * D + d + 1] = o[dt][2 * h + 1] * scale;
+        *reinterpret_cast<float2*>(dst + d) = make_float2(o[dt][2 * h] * sc, o[dt][2 * h + 1] * sc);
       }
     }
     __syncthreads();
-    // all 128 threads: row rr = tid / 8, 8 threads per row, D / 8 columns each
-    const int rr = threadIdx.x >> 3;
-    const int rho = row0 + rr;
-    if (rho < rows_total) {
+    // the prefix grid's partials are read below: wait for it (a no-op when this
+    // kernel was not launched behind it)
+    if (merge_in_place) grid_dependency_wait();
+    // warp w finalises rows w, w+4, w+8, w+12; lane c owns features [4c, 4c+4)
+    for (int rr = warp; rr < 16; rr += 4) {
+      const int rho = row0 + rr;
+      if (rho >= rows_total) break;
       float mg = -INFINITY;
 #pragma unroll
       for (int w = 0; w < 4; ++w) mg = fmaxf(mg, s_m[w * 16 + rr]);
@@ -285,90 +317,115 @@ __global__ void __launch_bounds__(kThreads)
         lsum += (mw == -INFINITY) ? 0.f : s_l[w * 16 + rr] * exp2f(mw - mg);
       }
       const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+      const float lse2 = lsum > 0.f ? mg + log2f(lsum) : -INFINITY;
       const int qi = rho / a.group, j = rho % a.group;
       const int64_t orow = static_cast<int64_t>(q0 + qi) * a.num_q_heads + g * a.group + j;
-      const int c0 = (threadIdx.x & 7) * (D / 8);
-      float acc[D / 8];
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (lane < D / 4) {
 #pragma unroll
-      for (int e = 0; e < D / 8; ++e) {
-        acc[e] = 0.f;
-#pragma unroll
-        for (int w = 0; w < 4; ++w) acc[e] += s_o[(w * 16 + rr) * D + c0 + e];
-        acc[e] *= inv;
-      }
-      const float lse2 = lsum > 0.f ? mg + log2f(lsum) : -INFINITY;
-      if (a.part_o != nullptr) {
-        const int64_t prow = static_cast<int64_t>(a.part_slot0 + split) * a.total_q *
-                                 a.num_q_heads + orow;
-        float* dst = a.part_o + prow * D + c0;
-#pragma unroll
-        for (int e = 0; e < D / 8; e += 4)
-          *reinterpret_cast<float4*>(dst + e) = make_float4(acc[e], acc[e + 1], acc[e + 2], acc[e + 3]);
-        if ((threadIdx.x & 7) == 0) a.part_lse[prow] = lse2;
-      } else {
-        __nv_bfloat16* dst = a.out + orow * D + c0;
-#pragma unroll
-        for (int e = 0; e < D / 8; e += 8) {
-          uint4 w = make_uint4(pack_bf16x2(acc[e], acc[e + 1]), pack_bf16x2(acc[e + 2], acc[e + 3]),
-                               pack_bf16x2(acc[e + 4], acc[e + 5]),
-                               pack_bf16x2(acc[e + 6], acc[e + 7]));
-          *reinterpret_cast<uint4*>(dst + e) = w;
+        for (int w = 0; w < 4; ++w) {
+          const float4 v = *reinterpret_cast<const float4*>(s_o + (w * 16 + rr) * L::kORow + lane * 4);
+          acc.x += v.x;
+          acc.y += v.y;
+          acc.z += v.z;
+          acc.w += v.w;
         }
-        if ((threadIdx.x & 7) == 0 && a.lse != nullptr)
-          a.lse[orow] = lse2 * 0.69314718055994531f;
+        acc = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+      }
+      if (merge_in_place) {
+        merge_row_warp<D>(m, orow, lane, true, acc, lse2);
+      } else if (partial) {
+        const int64_t prow = static_cast<int64_t>(a.n_prefix + split) * a.total_q *
+                                 a.num_q_heads + orow;
+        if (lane < D / 4) store_bf16x4(a.part_o + prow * D + lane * 4, acc);
+        if (lane == 0) a.part_lse[prow] = lse2;
+      } else {
+        if (lane < D / 4) store_bf16x4(a.out + orow * D + lane * 4, acc);
+        if (lane == 0 && a.lse != nullptr) a.lse[orow] = lse2 * kLn2;
       }
     }
   } else {
-    if (!warp_live) return;
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       const int rho = row0 + rbase + (lane >> 2) + 8 * h;
-      if (rho >= rows_total) continue;
+      if (!warp_live || rho >= rows_total) continue;
       const int qi = rho / a.group, j = rho % a.group;
       const int64_t orow = static_cast<int64_t>(q0 + qi) * a.num_q_heads + g * a.group + j;
       const float inv = l_run[h] > 0.f ? 1.f / l_run[h] : 0.f;
       const float lse2 = l_run[h] > 0.f ? m_run[h] + log2f(l_run[h]) : -INFINITY;
-      if (a.part_o != nullptr) {
-        const int64_t prow = static_cast<int64_t>(a.part_slot0 + split) * a.total_q *
+      __nv_bfloat16* dst;
+      if (partial) {
+        const int64_t prow = static_cast<int64_t>(a.n_prefix + split) * a.total_q *
                                  a.num_q_heads + orow;
-        float* dst = a.part_o + prow * D;
-#pragma unroll
-        for (int dt = 0; dt < kDT; ++dt) {
-          const int d = dt * 8 + (lane & 3) * 2;
-          *reinterpret_cast<float2*>(dst + d) = make_float2(o[dt][2 * h] * inv, o[dt][2 * h + 1] * inv);
-        }
+        dst = a.part_o + prow * D;
         if ((lane & 3) == 0) a.part_lse[prow] = lse2;
       } else {
-        __nv_bfloat16* dst = a.out + orow * D;
-#pragma unroll
-        for (int dt = 0; dt < kDT; ++dt) {
-          const int d = dt * 8 + (lane & 3) * 2;
-          *reinterpret_cast<uint32_t*>(dst + d) = pack_bf16x2(o[dt][2 * h] * inv, o[dt][2 * h + 1] * inv);
-        }
-        if ((lane & 3) == 0 && a.lse != nullptr) a.lse[orow] = lse2 * 0.69314718055994531f;
+        dst = a.out + orow * D;
+        if ((lane & 3) == 0 && a.lse != nullptr) a.lse[orow] = lse2 * kLn2;
       }
+#pragma unroll
+      for (int dt = 0; dt < kDT; ++dt) {
+        const int d = dt * 8 + (lane & 3) * 2;
+        *reinterpret_cast<uint32_t*>(dst + d) = pack_bf16x2(o[dt][2 * h] * inv, o[dt][2 * h + 1] * inv);
+      }
+    }
+  }
+
+  if (partial && !(kDecode && merge_in_place)) {
+    const int tok_first = row0 / a.group;
+    const int n_tok = (row0 + rows_here - 1) / a.group - tok_first + 1;
+    grid_dependency_wait();  // prefix partials are complete and visible
+    if (merge_in_place) {
+      // one split: this CTA is the only suffix contributor of its rows (its own
+      // partial is in slot n_prefix, written above)
+      MergeArgs mm = m;
+      mm.n_count = 1;
+      __syncthreads();
+      __threadfence_block();
+      for (int k = warp; k < n_tok * a.group; k += kThreads / 32) {
+        const int64_t row = static_cast<int64_t>(q0 + tok_first + k / a.group) * a.num_q_heads +
+                            g * a.group + k % a.group;
+        merge_row_warp<D>(mm, row, lane, false, make_float4(0.f, 0.f, 0.f, 0.f), -INFINITY);
+      }
+    } else {
+      if constexpr (kDecode) __syncthreads();  // merge scratch no longer needed below
+      count_and_merge<D>(m, q0 + tok_first, n_tok, g, reinterpret_cast<int*>(smem + L::kLast));
     }
   }
 }
 
 template <int D, bool kDecode>
-cudaError_t launch_paged_t(const PagedArgs& a, cudaStream_t stream) {
+cudaError_t launch_paged_t(const PagedArgs& a, bool after_prefix, cudaStream_t stream) {
   using L = PagedLayout<D, kDecode>;
   const int smem = L::kEnd;
   static std::atomic<uint64_t> attr_done{0};
   cudaError_t e = set_smem_once(paged_attn_kernel<D, kDecode>, smem, attr_done);
   if (e != cudaSuccess) return e;
-  dim3 grid(a.num_reqs * a.row_tiles, a.num_kv_heads, a.n_splits);
-  paged_attn_kernel<D, kDecode><<<grid, kThreads, smem, stream>>>(a);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.num_reqs * a.row_tiles, a.num_kv_heads, a.n_splits);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  // Right after the prefix kernel of the same call: start while it runs.  The two
+  // meet only through the row-group counters (atomics + fences), so this kernel
+  // never waits on the prefix grid.
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = after_prefix ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, paged_attn_kernel<D, kDecode>, a);
 }
 
 }  // namespace
 
-cudaError_t launch_paged(int head_dim, bool decode, const PagedArgs& a, cudaStream_t stream) {
+cudaError_t launch_paged(int head_dim, bool decode, const PagedArgs& a, bool after_prefix,
+                         cudaStream_t stream) {
   if (head_dim == 64)
-    return decode ? launch_paged_t<64, true>(a, stream) : launch_paged_t<64, false>(a, stream);
-  return decode ? launch_paged_t<128, true>(a, stream) : launch_paged_t<128, false>(a, stream);
+    return decode ? launch_paged_t<64, true>(a, after_prefix, stream)
+                  : launch_paged_t<64, false>(a, after_prefix, stream);
+  return decode ? launch_paged_t<128, true>(a, after_prefix, stream)
+                : launch_paged_t<128, false>(a, after_prefix, stream);
 }
 
 }  // namespace csp

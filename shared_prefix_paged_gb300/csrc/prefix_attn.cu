@@ -2,63 +2,75 @@
 //
 // "vLLM Cascade Attention：用法、场景与原理解析" §五 and §十: the prefix phase treats
 // every query of the batch as one sequence (cu_seqlens_q = [0, total_q]) so that one
-// load of a shared KV page serves a whole tile of queries, and §八 Step 5 Phase 1:
+// load of a shared KV page serves a whole tile of queries; §八 Step 5 Phase 1:
 // non-causal attention over KV [0, common_prefix_len) read through block_table[:1].
 //
 // GB300 design (not the FlashAttention tiling the page describes):
-//  * M tile = 128 packed rows (token, head-in-group) of ONE KV head, so the GQA
-//    heads that share a KV head share every K/V tile;
-//  * K and V pages (16 tokens x 64 features per box, 128-byte swizzle) are staged
-//    into shared memory by TMA, 8 pages per 128-key tile, double buffered;
-//  * S = Q K^T and O += P V run as tcgen05.mma (M=128, N=128 or D, K=16 steps) with
-//    fp32 accumulators in TMEM (S: columns 0-127, O: columns 128-255);
-//  * four softmax warps own one TMEM lane (row) per thread: they read S with
-//    tcgen05.ld, apply the online softmax in base 2, rescale O in TMEM only when the
-//    running max grows by more than 2^8, and write P (bf16) into shared memory in
-//    the 128-byte-swizzled K-major layout the PV MMA reads;
-//  * warp 4 is the TMA producer; thread 0 issues the MMAs.
-//  * the prefix length is split across CTAs for occupancy; each CTA writes a
-//    normalised fp32 partial and its log2-sum-exp, merged by the combine kernel.
+//  * a CTA owns 256 packed rows (token, head-in-group) of ONE KV head as two 128-row
+//    M tiles, so every K/V byte staged into shared memory serves 256 query rows and
+//    all the GQA heads of that KV head;
+//  * K and V pages (16 tokens x 64 features per box, 128-byte swizzle) are staged by
+//    TMA into a 3-deep ring of 64-key tiles;
+//  * per M tile, S = Q K^T (M=128, N=64) goes into one of two TMEM buffers, so the
+//    tensor core computes S(i+1) while the softmax works on S(i); P (bf16) is
+//    written back into the S buffer and used from TMEM as the A operand of
+//    O += P V (N = D).  The two M tiles use all 512 TMEM columns;
+//  * two softmax warpgroups (one per M tile) own one TMEM lane (row) per thread:
+//    online softmax in base 2 on the special-function unit, O rescaled in TMEM only
+//    when the running max grows by more than 2^8; warp 8 issues the MMAs, warp 9
+//    the TMA loads;
+//  * the prefix is cut into n_splits key ranges, one CTA each; a CTA stages its
+//    normalised rows (bf16) through shared memory and writes them, coalesced, into
+//    workspace slot `split`; the suffix kernel, which waits for this grid before it
+//    merges, combines them with its own partials (merge.cuh).
 #include "common.cuh"
 #include "kernels.cuh"
+#include "merge.cuh"
 
 namespace csp {
 namespace {
 
-constexpr int kRowsM = 128;     // packed rows per CTA
-constexpr int kKeysN = 128;     // keys per tile
-constexpr int kPage = 16;       // tokens per KV page
+constexpr int kRowsM = 128;    // rows per M tile
+constexpr int kRowsCta = 256;  // two M tiles
+constexpr int kKeysN = 64;     // keys per tile
+constexpr int kPage = 16;      // tokens per KV page
 constexpr int kPagesPerTile = kKeysN / kPage;
-constexpr int kHalfBytes = 128 * 128;   // 128 rows x 64 bf16 (one swizzle-128 column block)
-constexpr int kThreads = 160;           // 4 softmax warps + 1 producer warp
+constexpr int kStages = 3;
+constexpr int kThreads = 320;  // 2 softmax warpgroups, MMA warp, TMA warp
+constexpr int kWarpMma = 8;
+constexpr int kWarpTma = 9;
 
 template <int D>
 struct Layout {
   static constexpr int kHalves = D / 64;
-  static constexpr int kTileBytes = kHalves * kHalfBytes;   // Q tile, or one K / V tile
-  static constexpr int kQ = 0;
-  static constexpr int kK0 = kQ + kTileBytes;
-  static constexpr int kV0 = kK0 + 2 * kTileBytes;
-  static constexpr int kP = kV0 + 2 * kTileBytes;
-  static constexpr int kBar = kP + 2 * kHalfBytes;
-  static constexpr int kEnd = kBar + 128;
-  static constexpr int kDynamic = kEnd + 1024;   // slack to align the base to 1024 bytes
+  static constexpr int kQHalf = kRowsM * 128;           // 128 rows x 64 bf16
+  static constexpr int kKVHalf = kKeysN * 128;          // 64 keys x 64 bf16
+  static constexpr int kQTile = kHalves * kQHalf;       // one M tile of Q
+  static constexpr int kKVBytes = kHalves * kKVHalf;    // one K (or V) tile
+  static constexpr int kQ = 0;                          // [2 M tiles][halves]
+  static constexpr int kK0 = kQ + 2 * kQTile;
+  static constexpr int kV0 = kK0 + kStages * kKVBytes;
+  static constexpr int kRing = kV0 + kStages * kKVBytes;
+  // after the main loop, [0, kRing) stages the CTA's 256 normalised rows:
+  // [row][D + 8] bf16 (the padding spreads the rows one warp writes over all banks)
+  static constexpr int kStageRow = D + 8;
+  static_assert(kRowsCta * kStageRow * 2 <= kRing, "staging buffer fits Q + ring");
+  static constexpr int kLse = kRing;                    // float [256]
+  static constexpr int kBar = kLse + kRowsCta * 4;      // mbarriers + slot + flag
+  static constexpr int kEnd = kBar + 256;
+  static constexpr int kDynamic = kEnd + 1024;          // slack to align the base to 1024
 };
 
-__device__ __forceinline__ void named_bar_sync(int id, int n) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
-}
-
-// Barrier over the 128 softmax threads that also ORs a predicate across them.
-__device__ __forceinline__ bool softmax_bar_any(bool pred) {
+// Barrier over one softmax warpgroup (id 1 or 2, 128 threads) that ORs a predicate.
+__device__ __forceinline__ bool wg_bar_any(int id, bool pred) {
   uint32_t r;
   asm volatile(
       "{\n\t.reg .pred p, q;\n\t"
-      "setp.ne.u32 p, %1, 0;\n\t"
-      "bar.red.or.pred q, 1, 128, p;\n\t"
+      "setp.ne.u32 p, %2, 0;\n\t"
+      "bar.red.or.pred q, %1, 128, p;\n\t"
       "selp.u32 %0, 1, 0, q;\n\t}"
       : "=r"(r)
-      : "r"(static_cast<uint32_t>(pred))
+      : "r"(id), "r"(static_cast<uint32_t>(pred))
       : "memory");
   return r != 0;
 }
@@ -72,140 +84,198 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  uint8_t* sQ = smem + L::kQ;
-  uint8_t* sP = smem + L::kP;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBar);
   uint64_t* bar_q = bars + 0;
-  uint64_t* bar_kv = bars + 1;    // [2] tile loaded
-  uint64_t* bar_free = bars + 3;  // [2] PV of the tile in this stage finished
-  uint64_t* bar_s = bars + 5;     // S of the current tile ready in TMEM
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 6);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 7);
+  uint64_t* kv_full = bars + 1;   // [3]
+  uint64_t* kv_empty = bars + 4;  // [3]
+  uint64_t* s_full = bars + 7;    // [2 tiles][2 buffers]
+  uint64_t* p_full = bars + 11;   // [2 tiles][2 buffers]
+  uint64_t* o_done = bars + 15;   // [2 tiles]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 17);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 18);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int mt = blockIdx.x % a.m_tiles;
-  const int rest = blockIdx.x / a.m_tiles;
-  const int split = rest % a.n_splits;
-  const int kvh = rest / a.n_splits;
+  const int split = blockIdx.x % a.n_splits;
+  const int pair = (blockIdx.x / a.n_splits) % a.pairs;
+  const int kvh = blockIdx.x / (a.n_splits * a.pairs);
   const int key_tiles = (a.cpl + kKeysN - 1) / kKeysN;
-  const int t_first = split * a.tiles_per_split;
+  const int t_first = min(split * a.tiles_per_split, key_tiles);
   const int t_last = min(t_first + a.tiles_per_split, key_tiles);
   const int ntiles = t_last - t_first;
+  const int rows_total = a.total_q * a.group;                 // packed rows of this KV head
+  const bool has_m1 = pair * kRowsCta + kRowsM < rows_total;  // second M tile has rows
 
   if (threadIdx.x == 0) {
     mbar_init(bar_q, 1);
-    mbar_init(&bar_kv[0], 1);
-    mbar_init(&bar_kv[1], 1);
-    mbar_init(&bar_free[0], 1);
-    mbar_init(&bar_free[1], 1);
-    mbar_init(bar_s, 1);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&kv_full[s], 1);
+      mbar_init(&kv_empty[s], 1);
+    }
+    for (int b = 0; b < 4; ++b) {
+      mbar_init(&s_full[b], 1);
+      mbar_init(&p_full[b], 128);
+    }
+    mbar_init(&o_done[0], 1);
+    mbar_init(&o_done[1], 1);
     *abort_flag = 0;
     fence_mbarrier_init();
   }
-  if (warp == 0) tmem_alloc(tmem_slot, 256);
+  if (warp == kWarpMma) tmem_alloc(tmem_slot, 512);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // the suffix kernel (launched as a programmatic dependent) may start now; it reads
+  // this grid's partials only after waiting for the grid to complete
+  grid_launch_dependents();
 
-  if (warp == 4) {
-    // ------------------------------------------------------------ producer --
-    if (lane == 0) {
+  if (warp == kWarpTma) {
+    // ------------------------------------------------------------ TMA producer --
+    if (lane == 0 && ntiles > 0) {  // an empty key range loads nothing at all
       prefetch_tensormap(&tm_q);
       prefetch_tensormap(&tm_k);
       prefetch_tensormap(&tm_v);
-      mbar_arrive_expect_tx(bar_q, L::kTileBytes);
+      const int mts = has_m1 ? 2 : 1;
+      mbar_arrive_expect_tx(bar_q, mts * L::kQTile);
+      for (int m = 0; m < mts; ++m)
 #pragma unroll
-      for (int h = 0; h < L::kHalves; ++h)
-        tma_load_3d(sQ + h * kHalfBytes, &tm_q, bar_q, h * 64, kvh * a.group,
-                    mt * (kRowsM / a.group));
+        for (int h = 0; h < L::kHalves; ++h)
+          tma_load_3d(smem + L::kQ + m * L::kQTile + h * L::kQHalf, &tm_q, bar_q, h * 64,
+                      kvh * a.group, (pair * kRowsCta + m * kRowsM) / a.group);
     }
     for (int i = 0; i < ntiles; ++i) {
-      const int s = i & 1;
+      const int st = i % kStages;
       const int tile = t_first + i;
       const int valid_pages = min(kPagesPerTile, (a.cpl - tile * kKeysN) / kPage);
       int blk = 0;
       if (lane < kPagesPerTile) {
         // pages past the prefix re-read the tile's first page; their keys are masked
-        const int page = tile * kPagesPerTile + (lane < valid_pages ? lane : 0);
-        blk = __ldg(a.block_table + page);
+        blk = __ldg(a.block_table + tile * kPagesPerTile + (lane < valid_pages ? lane : 0));
       }
-      if (i >= 2 && !mbar_wait(&bar_free[s], ((i >> 1) - 1) & 1, abort_flag, a.status)) break;
-      if (lane == 0) mbar_arrive_expect_tx(&bar_kv[s], 2 * L::kTileBytes);
+      if (i >= kStages) {
+        bool ok = true;  // lane 0 waits; the decision is the same for the whole warp
+        if (lane == 0)
+          ok = mbar_wait(&kv_empty[st], ((i / kStages) - 1) & 1, abort_flag, a.status);
+        if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+      }
+      if (lane == 0) mbar_arrive_expect_tx(&kv_full[st], 2 * L::kKVBytes);
       __syncwarp();
       if (lane < kPagesPerTile) {
-        uint8_t* dk = smem + L::kK0 + s * L::kTileBytes + lane * (kPage * 128);
-        uint8_t* dv = smem + L::kV0 + s * L::kTileBytes + lane * (kPage * 128);
+        uint8_t* dk = smem + L::kK0 + st * L::kKVBytes + lane * (kPage * 128);
+        uint8_t* dv = smem + L::kV0 + st * L::kKVBytes + lane * (kPage * 128);
 #pragma unroll
         for (int h = 0; h < L::kHalves; ++h) {
-          tma_load_3d(dk + h * kHalfBytes, &tm_k, &bar_kv[s], h * 64, kvh, blk * kPage);
-          tma_load_3d(dv + h * kHalfBytes, &tm_v, &bar_kv[s], h * 64, kvh, blk * kPage);
+          tma_load_3d(dk + h * L::kKVHalf, &tm_k, &kv_full[st], h * 64, kvh, blk * kPage);
+          tma_load_3d(dv + h * L::kKVHalf, &tm_v, &kv_full[st], h * 64, kvh, blk * kPage);
         }
       }
     }
-  } else {
-    // ------------------------------------------------- softmax + MMA issue --
-    const int row = threadIdx.x;  // TMEM lane == packed row within the tile
-    const uint32_t t_warp = tmem + (static_cast<uint32_t>(warp * 32) << 16);
-    const uint32_t tS = t_warp;
-    const uint32_t tO = t_warp + 128;
-    constexpr uint32_t kIdS = umma_idesc_bf16(128, kKeysN, 0, 0);
-    constexpr uint32_t kIdO = umma_idesc_bf16(128, D, 0, 1);
-    const uint32_t q_addr = smem_u32(sQ);
-    const uint32_t p_addr = smem_u32(sP);
-    float m_run = -INFINITY;  // running max, log2 domain
-    float l_run = 0.f;
-    bool failed = false;
-
-    for (int i = 0; i < ntiles; ++i) {
-      const int s = i & 1;
-      const int tile = t_first + i;
-      if (threadIdx.x == 0) {
-        bool ok = (i > 0) || mbar_wait(bar_q, 0, abort_flag, a.status);
-        ok = ok && mbar_wait(&bar_kv[s], (i >> 1) & 1, abort_flag, a.status);
-        if (ok) {
-          tc_fence_after();
-          const uint32_t k_addr = smem_u32(smem + L::kK0 + s * L::kTileBytes);
+  } else if (warp == kWarpMma) {
+    // ------------------------------------------------------------- MMA issuer --
+    if (lane == 0 && ntiles > 0) {
+      constexpr uint32_t kIdS = umma_idesc_bf16(128, kKeysN, 0, 0);
+      constexpr uint32_t kIdO = umma_idesc_bf16(128, D, 0, 1);
+      const int mts = has_m1 ? 2 : 1;
+      auto issue_s = [&](int i) {
+        const uint32_t k_addr = smem_u32(smem + L::kK0 + (i % kStages) * L::kKVBytes);
+        for (int m = 0; m < mts; ++m) {
+          const uint32_t q_addr = smem_u32(smem + L::kQ + m * L::kQTile);
+          const uint32_t d = tmem + m * 256 + (i & 1) * kKeysN;
 #pragma unroll
           for (int k = 0; k < D / 16; ++k) {
-            const uint32_t off = (k >> 2) * kHalfBytes + (k & 3) * 32;
-            umma_bf16(tmem, umma_desc_sw128(q_addr + off, 16, 1024),
-                      umma_desc_sw128(k_addr + off, 16, 1024), kIdS, k > 0 ? 1u : 0u);
+            const uint32_t qo = (k >> 2) * L::kQHalf + (k & 3) * 32;
+            const uint32_t ko = (k >> 2) * L::kKVHalf + (k & 3) * 32;
+            umma_bf16(d, umma_desc_sw128(q_addr + qo, 16, 1024),
+                      umma_desc_sw128(k_addr + ko, 16, 1024), kIdS, k > 0 ? 1u : 0u);
           }
-          umma_commit(bar_s);
+          umma_commit(&s_full[m * 2 + (i & 1)]);
         }
+      };
+      bool ok = mbar_wait(bar_q, 0, abort_flag, a.status) &&
+                mbar_wait(&kv_full[0], 0, abort_flag, a.status);
+      if (ok) {
+        tc_fence_after();
+        issue_s(0);
       }
-      const bool ok = mbar_wait(bar_s, i & 1, abort_flag, a.status);
-      if (softmax_bar_any(!ok)) {
+      for (int i = 0; ok && i < ntiles; ++i) {
+        if (i + 1 < ntiles) {
+          ok = mbar_wait(&kv_full[(i + 1) % kStages], ((i + 1) / kStages) & 1, abort_flag,
+                         a.status);
+          if (!ok) break;
+          tc_fence_after();
+          issue_s(i + 1);  // S buffers (i+1)&1 were last read by PV(i-1), issued earlier
+        }
+        const uint32_t v_addr = smem_u32(smem + L::kV0 + (i % kStages) * L::kKVBytes);
+        for (int m = 0; ok && m < mts; ++m) {
+          ok = mbar_wait(&p_full[m * 2 + (i & 1)], (i >> 1) & 1, abort_flag, a.status);
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t p_tmem = tmem + m * 256 + (i & 1) * kKeysN;
+#pragma unroll
+          for (int kk = 0; kk < kKeysN / 16; ++kk)
+            umma_bf16_tmem_a(tmem + m * 256 + 2 * kKeysN, p_tmem + kk * 8,
+                             umma_desc_sw128(v_addr + kk * 16 * 128, L::kKVHalf, 1024), kIdO,
+                             (i > 0 || kk > 0) ? 1u : 0u);
+          umma_commit(&o_done[m]);
+        }
+        if (ok) umma_commit(&kv_empty[i % kStages]);
+      }
+    }
+    __syncwarp();
+  }
+
+  // --------------------------------------------------------------- softmax --
+  const int wg = warp >> 2;            // softmax warpgroup = M tile (warps 0-7)
+  const int row = threadIdx.x & 127;   // TMEM lane == row within the M tile
+  const uint32_t t_lane = tmem + wg * 256 + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+  const uint32_t tO = t_lane + 2 * kKeysN;
+  float m_run = -INFINITY;  // running max, log2 domain
+  float l_run = 0.f;
+  bool have = false;
+  const bool softmax_warp = warp < 8 && (wg == 0 || has_m1);
+  if (softmax_warp) {
+    bool failed = false;
+    for (int i = 0; i < ntiles; ++i) {
+      const int tile = t_first + i;
+      const bool ok = mbar_wait(&s_full[wg * 2 + (i & 1)], (i >> 1) & 1, abort_flag, a.status);
+      if (wg_bar_any(1 + wg, !ok)) {
         failed = true;
         break;
       }
       tc_fence_after();
-
       float sv[kKeysN];
-      tmem_ld128_sync(tS, sv);
-
-      const int valid = min(kKeysN, a.cpl - tile * kKeysN);
-      float mx = -INFINITY;
+      tmem_ld64_sync(t_lane + (i & 1) * kKeysN, sv);
+      const int valid = a.cpl - tile * kKeysN;
+      if (valid < kKeysN) {  // only the prefix's last tile can be partial
 #pragma unroll
-      for (int j = 0; j < kKeysN; ++j) {
-        sv[j] = (j < valid) ? sv[j] * a.scale_log2 : -INFINITY;
-        mx = fmaxf(mx, sv[j]);
+        for (int j = 0; j < kKeysN; ++j)
+          if (j >= valid) sv[j] = -INFINITY;
       }
-      // Rescale only when the running max grows by more than 2^8 (always on the
-      // first tile, where m_run is -inf); otherwise keep the stale max: P <= 256.
+      // row max of the raw scores as a tree (scale > 0 keeps the order)
+      float mx8[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) mx8[j] = sv[j];
+#pragma unroll
+      for (int j = 8; j < kKeysN; ++j) mx8[j & 7] = fmaxf(mx8[j & 7], sv[j]);
+      const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]))) *
+                       a.scale_log2;
+      // rescale only when the running max grows by more than 2^8 (always on the
+      // first tile, where m_run is -inf); otherwise keep the stale max: P <= 256
       const float m_new = fmaxf(m_run, mx);
       const bool grow = (m_new - m_run) > 8.f;
       float alpha = 1.f;
       if (grow) {
-        alpha = exp2f(m_run - m_new);
+        alpha = fast_exp2(m_run - m_new);
         l_run *= alpha;
         m_run = m_new;
       }
-      // tcgen05.ld / st are warp-collective: the whole warp rescales if any lane grew.
-      // O of the earlier tiles is complete here (bar_s covers every earlier MMA).
       if (i > 0 && __any_sync(0xffffffffu, grow)) {
+        // O must hold PV(i-1) before it is rescaled (the phase is unambiguous: PV(i)
+        // cannot complete before this thread has written P(i))
+        mbar_wait(&o_done[wg], (i - 1) & 1, abort_flag, a.status);
+        tc_fence_after();
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
           float o[32];
@@ -214,97 +284,112 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int j = 0; j < 32; ++j) o[j] *= alpha;
           tmem_st32(tO + c * 32, o);
         }
-        tmem_wait_st();
       }
-
-      // P = exp2(s - m), bf16, into the swizzled K-major P tile (two 64-key halves)
-      float sum = 0.f;
+      // p = 2^(s * scale * log2(e) - m): one FFMA and one ex2 per score
+      uint32_t pw[kKeysN / 2];
+      float sum4[4] = {0.f, 0.f, 0.f, 0.f};
+      const float neg_m = -m_run;
 #pragma unroll
-      for (int c = 0; c < kKeysN / 8; ++c) {
-        uint32_t w[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float p0 = exp2f(sv[c * 8 + 2 * e] - m_run);
-          const float p1 = exp2f(sv[c * 8 + 2 * e + 1] - m_run);
-          sum += p0 + p1;
-          w[e] = pack_bf16x2(p0, p1);
-        }
-        const int half = c >> 3, chunk = c & 7;
-        uint8_t* dst = sP + half * kHalfBytes + row * 128 + ((chunk ^ (row & 7)) << 4);
-        *reinterpret_cast<uint4*>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
+      for (int j = 0; j < kKeysN / 2; ++j) {
+        const float p0 = fast_exp2(fmaf(sv[2 * j], a.scale_log2, neg_m));
+        const float p1 = fast_exp2(fmaf(sv[2 * j + 1], a.scale_log2, neg_m));
+        sum4[j & 3] += p0 + p1;
+        pw[j] = pack_bf16x2(p0, p1);
       }
-      l_run += sum;
-      fence_proxy_async_smem();
+      l_run += (sum4[0] + sum4[1]) + (sum4[2] + sum4[3]);
+      tmem_st32_u(t_lane + (i & 1) * kKeysN, pw);
+      tmem_wait_st();
       tc_fence_before();
-      named_bar_sync(1, 128);
-      if (threadIdx.x == 0) {
-        tc_fence_after();
-        const uint32_t v_addr = smem_u32(smem + L::kV0 + s * L::kTileBytes);
-#pragma unroll
-        for (int k = 0; k < kKeysN / 16; ++k) {
-          const uint32_t aoff = (k >> 2) * kHalfBytes + (k & 3) * 32;
-          umma_bf16(tmem + 128, umma_desc_sw128(p_addr + aoff, 16, 1024),
-                    umma_desc_sw128(v_addr + k * 16 * 128, kHalfBytes, 1024), kIdO,
-                    (i > 0 || k > 0) ? 1u : 0u);
-        }
-        umma_commit(&bar_free[s]);
-      }
-    }
-
-    if (!failed && ntiles > 0) {
-      const int last = ntiles - 1;
-      const bool ok = mbar_wait(&bar_free[last & 1], (last >> 1) & 1, abort_flag, a.status);
-      failed = softmax_bar_any(!ok);
+      mbar_arrive(&p_full[wg * 2 + (i & 1)]);
     }
     if (!failed && ntiles > 0) {
-      tc_fence_after();
-      const int packed = mt * kRowsM + row;
-      const int t = packed / a.group;
-      const int h = kvh * a.group + packed % a.group;
-      const bool live = t < a.total_q;
-      const float inv_l = 1.f / l_run;
-      const size_t prow = (static_cast<size_t>(split) * a.total_q + t) * a.num_q_heads + h;
-      float* dst = a.part_o + prow * D;
-#pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        float o[32];
-        tmem_ld32_sync(tO + c * 32, o);
-        if (live) {
-#pragma unroll
-          for (int j = 0; j < 32; j += 4)
-            *reinterpret_cast<float4*>(dst + c * 32 + j) =
-                make_float4(o[j] * inv_l, o[j + 1] * inv_l, o[j + 2] * inv_l, o[j + 3] * inv_l);
-        }
-      }
-      if (live) a.part_lse[prow] = m_run + log2f(l_run);
+      const bool ok = mbar_wait(&o_done[wg], (ntiles - 1) & 1, abort_flag, a.status);
+      have = !wg_bar_any(1 + wg, !ok);
     }
     tc_fence_before();
   }
+
+  // ----------------------------------------- this split's partial -> slot --
+  // every MMA of the CTA is complete once both warpgroups saw their last o_done
+  // (or have nothing to do): Q and the ring become the staging buffer
   __syncthreads();
-  if (warp == 0) {
+  __nv_bfloat16* stage = reinterpret_cast<__nv_bfloat16*>(smem);
+  if (softmax_warp) {
     tc_fence_after();
-    tmem_dealloc(tmem, 256);
+    const float inv_l = have ? 1.f / l_run : 0.f;
+    __nv_bfloat16* dst = stage + (wg * kRowsM + row) * L::kStageRow;
+#pragma unroll
+    for (int c = 0; c < D / 32; ++c) {
+      float o[32];
+      tmem_ld32_sync(tO + c * 32, o);
+#pragma unroll
+      for (int j = 0; j < 32; j += 8)
+        *reinterpret_cast<uint4*>(dst + c * 32 + j) =
+            make_uint4(pack_bf16x2(o[j] * inv_l, o[j + 1] * inv_l),
+                       pack_bf16x2(o[j + 2] * inv_l, o[j + 3] * inv_l),
+                       pack_bf16x2(o[j + 4] * inv_l, o[j + 5] * inv_l),
+                       pack_bf16x2(o[j + 6] * inv_l, o[j + 7] * inv_l));
+    }
+  }
+  // a row with no key in this range (or no query) gets -inf: weight 0 in the merge
+  float* s_lse = reinterpret_cast<float*>(smem + L::kLse);
+  if (warp < 8) s_lse[wg * kRowsM + row] = (softmax_warp && have) ? m_run + log2f(l_run)
+                                                                  : -INFINITY;
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kWarpMma) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+  // coalesced copy-out: a warp writes whole rows (D/8 lanes x 16 bytes each)
+  {
+    constexpr int kChunks = D / 8;
+    const int gshift = __ffs(a.group) - 1;  // group is a power of two
+    for (int it = threadIdx.x; it < kRowsCta * kChunks; it += kThreads) {
+      const int r = it / kChunks;
+      const int c = it % kChunks;
+      const int packed = pair * kRowsCta + r;
+      const int t = packed >> gshift;
+      if (t >= a.total_q) continue;
+      const int64_t prow = (static_cast<int64_t>(split) * a.total_q + t) * a.num_q_heads +
+                           kvh * a.group + (packed & (a.group - 1));
+      *reinterpret_cast<uint4*>(a.part_o + prow * D + c * 8) =
+          *reinterpret_cast<const uint4*>(stage + r * L::kStageRow + c * 8);
+      if (c == 0) a.part_lse[prow] = s_lse[r];
+    }
   }
 }
 
-}  // namespace
-
-size_t prefix_smem_bytes(int head_dim) {
-  return head_dim == 64 ? Layout<64>::kDynamic : Layout<128>::kDynamic;
+template <int D>
+cudaLaunchConfig_t prefix_config(const PrefixArgs& a, cudaStream_t stream,
+                                 cudaLaunchAttribute* attr) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.n_splits * a.pairs * a.num_kv_heads);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = Layout<D>::kDynamic;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 0;
+  return cfg;
 }
 
 template <int D>
-static cudaError_t launch_prefix_d(const CUtensorMap& tm_q, const CUtensorMap& tm_k,
-                                   const CUtensorMap& tm_v, const PrefixArgs& a,
-                                   cudaStream_t stream) {
-  const int smem = Layout<D>::kDynamic;
+cudaError_t prepare() {
   static std::atomic<uint64_t> attr_done{0};
-  cudaError_t e = set_smem_once(prefix_attn_kernel<D>, smem, attr_done);
-  if (e != cudaSuccess) return e;
-  const int grid = a.m_tiles * a.n_splits * a.num_kv_heads;
-  prefix_attn_kernel<D><<<grid, kThreads, smem, stream>>>(tm_q, tm_k, tm_v, a);
-  return cudaGetLastError();
+  return set_smem_once(prefix_attn_kernel<D>, Layout<D>::kDynamic, attr_done);
 }
+
+template <int D>
+cudaError_t launch_prefix_d(const CUtensorMap& tm_q, const CUtensorMap& tm_k,
+                            const CUtensorMap& tm_v, const PrefixArgs& a, cudaStream_t stream) {
+  cudaError_t e = prepare<D>();
+  if (e != cudaSuccess) return e;
+  cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t cfg = prefix_config<D>(a, stream, attr);
+  return cudaLaunchKernelEx(&cfg, prefix_attn_kernel<D>, tm_q, tm_k, tm_v, a);
+}
+
+}  // namespace
 
 cudaError_t launch_prefix(int head_dim, const CUtensorMap& tm_q, const CUtensorMap& tm_k,
                           const CUtensorMap& tm_v, const PrefixArgs& a, cudaStream_t stream) {
