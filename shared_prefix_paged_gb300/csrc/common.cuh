@@ -344,10 +344,12 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) 
 
 // ---------------------------------------------------- cp.async / ldmatrix --
 // 16-byte async copy global -> shared; src_bytes = 0 zero-fills without reading.
+// No memory clobber: ordinary loads (the block-table lookups that give the source
+// addresses) may be scheduled ahead of earlier copies.  The copied data is only
+// read after cp_async_wait, which does carry the clobber.
 __device__ __forceinline__ void cp_async_16(void* smem_dst, const void* gsrc, uint32_t src_bytes) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(smem_dst)),
-               "l"(gsrc), "r"(src_bytes)
-               : "memory");
+               "l"(gsrc), "r"(src_bytes));
 }
 __device__ __forceinline__ void cp_async_commit() {
   asm volatile("cp.async.commit_group;" ::: "memory");

@@ -77,23 +77,35 @@ __device__ __forceinline__ void merge_row_warp(const MergeArgs& m, int64_t row, 
   const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   if (w_own != 0.f) {
-    acc = make_float4(w_own * own.x, w_own * own.y, w_own * own.z, w_own * own.w);
+    const float wo = w_own * inv;
+    acc = make_float4(wo * own.x, wo * own.y, wo * own.z, wo * own.w);
   }
-#pragma unroll 4
-  for (int p = 0; p < m.n_parts; ++p) {
-    const float wp = __shfl_sync(0xffffffffu, w, p);
-    if (lane < D / 4 && wp != 0.f) {
-      const float4 o = load_bf16x4_cg(m.part_o + (static_cast<int64_t>(p) * m.rows + row) * D +
-                                      lane * 4);
-      acc.x += wp * o.x;
-      acc.y += wp * o.y;
-      acc.z += wp * o.z;
-      acc.w += wp * o.w;
+  // eight slots at a time: their loads are independent and go out together; an
+  // empty slot (weight 0) is skipped by a select, so whatever it holds never mixes in
+  const __nv_bfloat16* base = m.part_o + row * D + lane * 4;
+  const int64_t slot_stride = static_cast<int64_t>(m.rows) * D;
+  for (int p0 = 0; p0 < m.n_parts; p0 += 8) {
+    float4 o[8];
+    float wp[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int p = p0 + j;
+      wp[j] = __shfl_sync(0xffffffffu, w, p & 31) * inv;
+      if (p >= m.n_parts) wp[j] = 0.f;
+      o[j] = (p < m.n_parts && lane < D / 4) ? load_bf16x4_cg(base + p * slot_stride)
+                                             : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      if (wp[j] != 0.f) {
+        acc.x = fmaf(wp[j], o[j].x, acc.x);
+        acc.y = fmaf(wp[j], o[j].y, acc.y);
+        acc.z = fmaf(wp[j], o[j].z, acc.z);
+        acc.w = fmaf(wp[j], o[j].w, acc.w);
+      }
     }
   }
-  if (lane < D / 4)
-    store_bf16x4(m.out + row * D + lane * 4,
-                 make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv));
+  if (lane < D / 4) store_bf16x4(m.out + row * D + lane * 4, acc);
   if (lane == 0 && m.lse != nullptr)
     m.lse[row] = wsum > 0.f ? (mx + log2f(wsum)) * 0.69314718055994531f : -INFINITY;
 }

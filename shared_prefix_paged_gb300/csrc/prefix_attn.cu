@@ -10,7 +10,7 @@
 //    M tiles, so every K/V byte staged into shared memory serves 256 query rows and
 //    all the GQA heads of that KV head;
 //  * K and V pages (16 tokens x 64 features per box, 128-byte swizzle) are staged by
-//    TMA into a 3-deep ring of 64-key tiles;
+//    TMA into a 4-deep ring of 64-key tiles;
 //  * per M tile, S = Q K^T (M=128, N=64) goes into one of two TMEM buffers, so the
 //    tensor core computes S(i+1) while the softmax works on S(i); P (bf16) is
 //    written back into the S buffer and used from TMEM as the A operand of
@@ -35,7 +35,7 @@ constexpr int kRowsCta = 256;  // two M tiles
 constexpr int kKeysN = 64;     // keys per tile
 constexpr int kPage = 16;      // tokens per KV page
 constexpr int kPagesPerTile = kKeysN / kPage;
-constexpr int kStages = 3;
+constexpr int kStages = 4;
 constexpr int kThreads = 320;  // 2 softmax warpgroups, MMA warp, TMA warp
 constexpr int kWarpMma = 8;
 constexpr int kWarpTma = 9;
@@ -86,13 +86,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBar);
   uint64_t* bar_q = bars + 0;
-  uint64_t* kv_full = bars + 1;   // [3]
-  uint64_t* kv_empty = bars + 4;  // [3]
-  uint64_t* s_full = bars + 7;    // [2 tiles][2 buffers]
-  uint64_t* p_full = bars + 11;   // [2 tiles][2 buffers]
-  uint64_t* o_done = bars + 15;   // [2 tiles]
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 17);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 18);
+  uint64_t* kv_full = bars + 1;   // [kStages]
+  uint64_t* kv_empty = bars + 1 + kStages;  // [kStages]
+  uint64_t* s_full = bars + 1 + 2 * kStages;    // [2 tiles][2 buffers]
+  uint64_t* p_full = bars + 5 + 2 * kStages;    // [2 tiles][2 buffers]
+  uint64_t* o_done = bars + 9 + 2 * kStages;    // [2 tiles]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 11 + 2 * kStages);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 12 + 2 * kStages);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -144,15 +144,19 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_load_3d(smem + L::kQ + m * L::kQTile + h * L::kQHalf, &tm_q, bar_q, h * 64,
                       kvh * a.group, (pair * kRowsCta + m * kRowsM) / a.group);
     }
+    // block id of page `lane` of tile t; pages past the prefix re-read the tile's
+    // first page (their keys are masked)
+    auto page_id = [&](int t) {
+      const int valid_pages = min(kPagesPerTile, (a.cpl - t * kKeysN) / kPage);
+      return lane < kPagesPerTile
+                 ? __ldg(a.block_table + t * kPagesPerTile + (lane < valid_pages ? lane : 0))
+                 : 0;
+    };
+    int blk_next = ntiles > 0 ? page_id(t_first) : 0;
     for (int i = 0; i < ntiles; ++i) {
       const int st = i % kStages;
-      const int tile = t_first + i;
-      const int valid_pages = min(kPagesPerTile, (a.cpl - tile * kKeysN) / kPage);
-      int blk = 0;
-      if (lane < kPagesPerTile) {
-        // pages past the prefix re-read the tile's first page; their keys are masked
-        blk = __ldg(a.block_table + tile * kPagesPerTile + (lane < valid_pages ? lane : 0));
-      }
+      const int blk = blk_next;
+      if (i + 1 < ntiles) blk_next = page_id(t_first + i + 1);  // in flight meanwhile
       if (i >= kStages) {
         bool ok = true;  // lane 0 waits; the decision is the same for the whole warp
         if (lane == 0)
