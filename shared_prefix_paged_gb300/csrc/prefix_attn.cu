@@ -90,9 +90,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* kv_empty = bars + 1 + kStages;  // [kStages]
   uint64_t* s_full = bars + 1 + 2 * kStages;    // [2 tiles][2 buffers]
   uint64_t* p_full = bars + 5 + 2 * kStages;    // [2 tiles][2 buffers]
-  uint64_t* o_done = bars + 9 + 2 * kStages;    // [2 tiles]
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 11 + 2 * kStages);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 12 + 2 * kStages);
+  uint64_t* o_done = bars + 9 + 2 * kStages;    // [2 tiles] every PV
+  uint64_t* o_last = bars + 11 + 2 * kStages;   // [2 tiles] the last PV
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 13 + 2 * kStages);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 14 + 2 * kStages);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -116,8 +117,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&s_full[b], 1);
       mbar_init(&p_full[b], 128);
     }
-    mbar_init(&o_done[0], 1);
-    mbar_init(&o_done[1], 1);
+    for (int m = 0; m < 2; ++m) {
+      mbar_init(&o_done[m], 1);
+      mbar_init(&o_last[m], 1);
+    }
     *abort_flag = 0;
     fence_mbarrier_init();
   }
@@ -222,6 +225,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                              umma_desc_sw128(v_addr + kk * 16 * 128, L::kKVHalf, 1024), kIdO,
                              (i > 0 || kk > 0) ? 1u : 0u);
           umma_commit(&o_done[m]);
+          if (i == ntiles - 1) umma_commit(&o_last[m]);
         }
         if (ok) umma_commit(&kv_empty[i % kStages]);
       }
@@ -307,7 +311,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_arrive(&p_full[wg * 2 + (i & 1)]);
     }
     if (!failed && ntiles > 0) {
-      const bool ok = mbar_wait(&o_done[wg], (ntiles - 1) & 1, abort_flag, a.status);
+      // o_done's parity alone cannot tell PV(ntiles-1) from PV(ntiles-2), which may
+      // still be running: o_last completes once, after every PV of the range
+      const bool ok = mbar_wait(&o_last[wg], 0, abort_flag, a.status);
       have = !wg_bar_any(1 + wg, !ok);
     }
     tc_fence_before();
