@@ -127,15 +127,40 @@ CSP_API int cascade_plan(const int32_t* block_table, int64_t bt_row_stride, int3
  * csp_workspace_size — bytes of device workspace that cascade_attn (with this
  * common_prefix_len) or paged_attn (common_prefix_len = 0) needs for this batch
  * shape on the current device.  All arguments are host integers, the same as the
- * attention call will get.  The workspace holds a status word, one counter per
- * (query token, KV head) and the split partial results; it must be 256-byte aligned
- * and zero-filled before its first use (for the status word: each call clears its
- * counters itself, so one workspace may serve batches of different shapes).
+ * attention call will get.  The workspace holds a status word, the counters of the
+ * single-kernel schedule, one counter per (query token, KV head) and the split
+ * partial results; it must be 256-byte aligned and zero-filled before its first use
+ * (each call leaves its counters at zero or clears them itself, so one workspace may
+ * serve batches of different shapes).  After a call reported CSP_ERR_TIMEOUT, zero
+ * the workspace again before reusing it.
  * Returns CSP_OK and writes *bytes_out, or CSP_ERR_INVALID_ARG / CSP_ERR_CUDA.
  */
 CSP_API int csp_workspace_size(int32_t num_reqs, int32_t total_q, int32_t max_seqlen_q,
                        int32_t max_seqlen_k, int32_t common_prefix_len, int32_t num_q_heads,
                        int32_t num_kv_heads, int32_t head_dim, size_t* bytes_out);
+
+/* csp_cascade_schedule results. */
+enum { CSP_SCHEDULE_TWO_KERNELS = 0, CSP_SCHEDULE_SINGLE = 1 };
+
+/*
+ * csp_cascade_schedule — which kernels cascade_attn launches for a batch of this
+ * shape on the current device.  Host integers, the same as the attention call will
+ * get (common_prefix_len > 0).
+ *   CSP_SCHEDULE_TWO_KERNELS : a prefix-phase kernel, then a paged kernel for the
+ *                              suffix phase whose CTAs also merge (any batch);
+ *   CSP_SCHEDULE_SINGLE      : one cooperative kernel of one CTA per SM, for batches
+ *                              where every request has at most 16 / (num_q_heads /
+ *                              num_kv_heads) query tokens: some CTAs run ranges of the
+ *                              prefix phase while the others stream the suffix
+ *                              phase, then every CTA merges a share of the rows.
+ * Writes *schedule_out and, when prefix_splits_out is not NULL, the number of key
+ * ranges the prefix phase is cut into (one workspace slot each).  Returns CSP_OK,
+ * CSP_ERR_INVALID_ARG, CSP_ERR_UNSUPPORTED or CSP_ERR_CUDA.
+ */
+CSP_API int csp_cascade_schedule(int32_t num_reqs, int32_t total_q, int32_t max_seqlen_q,
+                                 int32_t max_seqlen_k, int32_t common_prefix_len,
+                                 int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                                 int32_t* schedule_out, int32_t* prefix_splits_out);
 
 /*
  * cascade_attn — cascade attention for one batch (§八 Step 5).
@@ -173,14 +198,16 @@ CSP_API int cascade_attn(const void* q, const void* k_cache, const void* v_cache
 
 /*
  * cascade_attn_timed — cascade_attn plus four CUDA events recorded on `stream`
- * between its kernels, for timing each phase: phase_events[0] before the
- * prefix-phase kernel, [1] after it, [2] after the suffix-phase kernel (whose CTAs
- * finish the LSE merge), [3] at the end of the call (the same point as [2]).
- * phase_events is a host array of four cudaEvent_t created by the caller (with
- * timing enabled).  With events between them, the two kernels run one after the
- * other instead of overlapping, so the per-phase times add up to more than a
- * cascade_attn call takes.  Arguments and results are otherwise those of
- * cascade_attn; with common_prefix_len == 0, events [0] and [1] mark the same point.
+ * between its kernels, for timing each phase.  Two-kernel schedule:
+ * phase_events[0] before the prefix-phase kernel, [1] after it, [2] after the
+ * suffix-phase kernel (whose CTAs finish the LSE merge), [3] at the end of the call
+ * (the same point as [2]); with events between them, the two kernels run one after
+ * the other instead of overlapping, so the per-phase times add up to more than a
+ * cascade_attn call takes; with common_prefix_len == 0, events [0] and [1] mark the
+ * same point.  Single-kernel schedule (csp_cascade_schedule): [0] before the kernel,
+ * [1], [2] and [3] after it.  phase_events is a host array of four cudaEvent_t
+ * created by the caller (with timing enabled).  Arguments and results are otherwise
+ * those of cascade_attn.
  */
 CSP_API int cascade_attn_timed(const void* q, const void* k_cache, const void* v_cache,
                                int32_t num_blocks, const int32_t* block_table,

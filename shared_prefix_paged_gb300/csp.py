@@ -25,12 +25,14 @@ CSP_ERR_CUDA = -4
 CSP_ERR_TIMEOUT = -6
 
 MODE_AUTO, MODE_FORCE_CASCADE, MODE_FORCE_FLAT, MODE_PAGE_THRESHOLDS = 0, 1, 2, 3
+SCHEDULE_TWO_KERNELS, SCHEDULE_SINGLE = 0, 1
 DTYPE_BF16, DTYPE_F32 = 0, 1
 
 # every symbol include/csp.h declares
 EXPORTS = ("cascade_plan", "csp_workspace_size", "cascade_attn", "cascade_attn_timed",
            "paged_attn", "merge_states", "csp_workspace_status", "csp_status_string",
-           "csp_last_cuda_error", "csp_version", "cascade_attn_noalloc")
+           "csp_last_cuda_error", "csp_version", "cascade_attn_noalloc",
+           "csp_cascade_schedule")
 
 _lock = threading.Lock()
 _lib: Optional[ctypes.CDLL] = None
@@ -66,6 +68,7 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         p, i32, i64, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
         lib.cascade_plan.argtypes = [p, i64, i32, p, p, i32, i32, i32, i32, i32, i32, p, p]
         lib.csp_workspace_size.argtypes = [i32, i32, i32, i32, i32, i32, i32, i32, p]
+        lib.csp_cascade_schedule.argtypes = [i32, i32, i32, i32, i32, i32, i32, i32, p, p]
         attn = [p, p, p, i32, p, i64, p, p, i32, i32, i32, i32]
         tail = [i32, i32, i32, i32, ctypes.c_float, p, p, p, sz, p]
         lib.cascade_attn.argtypes = attn + [i32] + tail
@@ -78,7 +81,7 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         for name in ("cascade_plan", "csp_workspace_size", "cascade_attn", "cascade_attn_timed",
                      "paged_attn",
                      "merge_states", "csp_workspace_status", "csp_last_cuda_error",
-                     "csp_version"):
+                     "csp_version", "csp_cascade_schedule"):
             getattr(lib, name).restype = ctypes.c_int
         _lib = lib
         return lib
@@ -121,6 +124,20 @@ def workspace_size(num_reqs, total_q, max_seqlen_q, max_seqlen_k, common_prefix_
                                   common_prefix_len, num_q_heads, num_kv_heads, head_dim,
                                   ctypes.byref(out)), "csp_workspace_size")
     return int(out.value)
+
+
+def cascade_schedule(num_reqs, total_q, max_seqlen_q, max_seqlen_k, common_prefix_len,
+                     num_q_heads, num_kv_heads, head_dim):
+    """(schedule, prefix key ranges) that cascade_attn uses for this batch shape on the
+    current device: SCHEDULE_TWO_KERNELS or SCHEDULE_SINGLE."""
+    lib = load()
+    sched = ctypes.c_int32(0)
+    splits = ctypes.c_int32(0)
+    _check(lib.csp_cascade_schedule(num_reqs, total_q, max_seqlen_q, max_seqlen_k,
+                                    common_prefix_len, num_q_heads, num_kv_heads, head_dim,
+                                    ctypes.byref(sched), ctypes.byref(splits)),
+           "csp_cascade_schedule")
+    return int(sched.value), int(splits.value)
 
 
 def _stream_ptr(stream, device):

@@ -1,6 +1,7 @@
 // api.cu — the C ABI declared in include/csp.h: argument checks, the common-prefix
 // planner, the launch plan (tiles, key splits, workspace partition), TMA tensor-map
 // encoding and the launch sequence.  Everything here runs on the host.
+#include <algorithm>
 #include <atomic>
 #include <cmath>
 #include <cstring>
@@ -8,6 +9,7 @@
 
 #include "csp.h"
 #include "kernels.cuh"
+#include "merge.cuh"
 
 namespace {
 
@@ -19,7 +21,16 @@ int cuda_fail(cudaError_t e) {
 }
 
 constexpr int kPage = 16;
-constexpr size_t kHeaderBytes = 256;  // status word + reserved
+// Workspace header: [0] status word; [64] unit counter, [128] barrier count and
+// [192] barrier generation of the single-kernel decode schedule (that kernel leaves
+// the first two at zero when it exits).
+constexpr size_t kHeaderBytes = 256;
+constexpr size_t kOffWorkCounter = 64;
+constexpr size_t kOffBarCount = 128;
+constexpr size_t kOffBarGen = 192;
+// Most packed rows (query, head-in-group) per request and KV head that the decode
+// schedule takes: one warp-level MMA tile.
+constexpr int kDecodeRows = 16;
 constexpr int kMaxSplits = 32;  // suffix splits; with the prefix's slots at most 32 partials per row
 
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
@@ -104,6 +115,10 @@ struct LaunchPlan {
   bool direct = false;  // paged kernel writes the final output itself
   int n_parts = 0;      // partial results per row group
   size_t off_counters = 0, off_part_o = 0, off_part_lse = 0, bytes = 0;
+  // single-kernel decode schedule (decode_cascade.cu)
+  bool single = false;
+  int d_splits = 0, d_prefix_ctas = 0, d_grid = 0;
+  size_t d_off_o = 0, d_off_lse = 0;
 };
 
 void make_plan(int num_reqs, int total_q, int max_q, int max_k, int cpl, int Hq, int Hkv, int D,
@@ -148,6 +163,31 @@ void make_plan(int num_reqs, int total_q, int max_q, int max_k, int cpl, int Hq,
   p.off_part_o = p.off_counters + align256(static_cast<size_t>(total_q) * Hkv * 4);
   p.off_part_lse = p.off_part_o + align256(static_cast<size_t>(p.n_parts) * rows_total * D * 2);
   p.bytes = p.off_part_lse + align256(static_cast<size_t>(p.n_parts) * rows_total * 4);
+
+  // Decode-like batches (a request's rows of one KV head fit one 16-row MMA tile):
+  // one cooperative kernel, prefix ranges on some SMs while the others stream the
+  // suffix units.  The prefix gets enough ranges to end within about the time the
+  // whole call needs to stream its bytes: with ~0.75 us per 64-key tile of 256 rows
+  // and ~2.5 us of fixed cost per range, against the call's K/V bytes at ~5.5 TB/s
+  // (prefix once, every request's suffix at its longest).
+  const int d_base = p.p_pairs * Hkv;
+  if (cpl > 0 && static_cast<int64_t>(max_q) * p.group <= kDecodeRows && d_base <= sms) {
+    const int key_tiles = cdiv(cpl, 64);
+    const double tok_bytes = 4.0 * Hkv * D;
+    const double call_us =
+        (static_cast<double>(cpl) + static_cast<double>(num_reqs) * max_len) * tok_bytes / 5.5e6;
+    const double pair_rows = std::min(256.0, static_cast<double>(total_q) * p.group);
+    const double tile_us = 0.75 * std::max(0.5, pair_rows / 256.0);
+    int s = static_cast<int>(std::ceil(key_tiles * tile_us / std::max(1.0, call_us - 2.5)));
+    s = std::max(1, std::min({s, key_tiles, csp::kDecodeMaxParts - 1, sms / d_base}));
+    p.single = true;
+    p.d_splits = s;
+    p.d_prefix_ctas = d_base * s;
+    p.d_grid = sms;
+    p.d_off_o = kHeaderBytes;
+    p.d_off_lse = p.d_off_o + align256(static_cast<size_t>(s + 1) * rows_total * D * 2);
+    p.bytes = std::max(p.bytes, p.d_off_lse + align256(static_cast<size_t>(s + 1) * rows_total * 4));
+  }
   *P = p;
 }
 
@@ -191,6 +231,57 @@ int attention_call(const void* q, const void* k_cache, const void* v_cache, int3
   auto mark = [&](int i) -> cudaError_t {
     return events ? cudaEventRecord(static_cast<cudaEvent_t>(events[i]), stream) : cudaSuccess;
   };
+  if (P.single) {
+    CUtensorMap tm_q, tm_k, tm_v;
+    const uint64_t row_b = static_cast<uint64_t>(D) * 2;
+    const uint64_t ntok = static_cast<uint64_t>(num_blocks) * block_size;
+    if ((st = make_map_3d(&tm_q, q, D, Hq, total_q, row_b, row_b * Hq, 64, P.group,
+                          128 / P.group)) != CSP_OK ||
+        (st = make_map_3d(&tm_k, k_cache, D, Hkv, ntok, row_b, row_b * Hkv, 64, 1, kPage)) !=
+            CSP_OK ||
+        (st = make_map_3d(&tm_v, v_cache, D, Hkv, ntok, row_b, row_b * Hkv, 64, 1, kPage)) !=
+            CSP_OK)
+      return st;
+    csp::DecodeArgs da;
+    csp::PrefixArgs& pa = da.pre;
+    pa.k = static_cast<const __nv_bfloat16*>(k_cache);
+    pa.v = static_cast<const __nv_bfloat16*>(v_cache);
+    pa.block_table = block_table;
+    pa.total_q = total_q;
+    pa.num_q_heads = Hq;
+    pa.num_kv_heads = Hkv;
+    pa.group = P.group;
+    pa.cpl = cpl;
+    pa.pairs = P.p_pairs;
+    pa.n_splits = P.d_splits;
+    pa.tiles_per_split = 0;  // ranges come from key_tiles and n_splits
+    pa.scale_log2 = scale_log2;
+    pa.part_o = reinterpret_cast<__nv_bfloat16*>(ws + P.d_off_o);
+    pa.part_lse = reinterpret_cast<float*>(ws + P.d_off_lse);
+    pa.status = status;
+    da.q = static_cast<const __nv_bfloat16*>(q);
+    da.k = static_cast<const __nv_bfloat16*>(k_cache);
+    da.v = static_cast<const __nv_bfloat16*>(v_cache);
+    da.block_table = block_table;
+    da.bt_stride = bt_row_stride;
+    da.cu_seqlens_q = cu_seqlens_q;
+    da.seq_lens = seqused_k;
+    da.num_reqs = num_reqs;
+    da.prefix_ctas = P.d_prefix_ctas;
+    da.key_tiles = cdiv(cpl, 64);
+    da.work_counter = reinterpret_cast<int*>(ws + kOffWorkCounter);
+    da.bar_count = reinterpret_cast<int*>(ws + kOffBarCount);
+    da.bar_gen = reinterpret_cast<unsigned*>(ws + kOffBarGen);
+    da.out = static_cast<__nv_bfloat16*>(out);
+    da.lse = lse;
+    // phase events: [0] before the kernel, [1..3] after it
+    if ((e = mark(0)) != cudaSuccess) return cuda_fail(e);
+    if ((e = csp::launch_decode(D, tm_q, tm_k, tm_v, da, P.d_grid, stream)) != cudaSuccess)
+      return cuda_fail(e);
+    for (int i = 1; i < 4; ++i)
+      if ((e = mark(i)) != cudaSuccess) return cuda_fail(e);
+    return CSP_OK;
+  }
   if ((e = mark(0)) != cudaSuccess) return cuda_fail(e);
   // row-group counters start at zero in every call, whatever the workspace held
   // (only several suffix splits count themselves)
@@ -213,6 +304,8 @@ int attention_call(const void* q, const void* k_cache, const void* v_cache, int3
         CSP_OK)
       return st;
     csp::PrefixArgs pa;
+    pa.k = static_cast<const __nv_bfloat16*>(k_cache);
+    pa.v = static_cast<const __nv_bfloat16*>(v_cache);
     pa.block_table = block_table;
     pa.total_q = total_q;
     pa.num_q_heads = Hq;
@@ -441,6 +534,27 @@ const char* csp_status_string(int status) {
 
 int csp_last_cuda_error(void) { return g_last_cuda_error; }
 
-int csp_version(void) { return (1 << 16) | 0; }
+int csp_version(void) { return (1 << 16) | 1; }
+
+int csp_cascade_schedule(int32_t num_reqs, int32_t total_q, int32_t max_seqlen_q,
+                         int32_t max_seqlen_k, int32_t common_prefix_len, int32_t num_q_heads,
+                         int32_t num_kv_heads, int32_t head_dim, int32_t* schedule_out,
+                         int32_t* prefix_splits_out) {
+  if (!schedule_out) return CSP_ERR_INVALID_ARG;
+  int st = check_shape(num_reqs, total_q, max_seqlen_q, max_seqlen_k, num_q_heads, num_kv_heads,
+                       head_dim, kPage);
+  if (st != CSP_OK) return st;
+  if (common_prefix_len <= 0 || common_prefix_len % kPage != 0 ||
+      common_prefix_len > max_seqlen_k)
+    return CSP_ERR_INVALID_ARG;
+  int sms = 0;
+  if ((st = device_sm_count(&sms)) != CSP_OK) return st;
+  LaunchPlan P;
+  make_plan(num_reqs, total_q, max_seqlen_q, max_seqlen_k, common_prefix_len, num_q_heads,
+            num_kv_heads, head_dim, sms, &P);
+  *schedule_out = P.single ? CSP_SCHEDULE_SINGLE : CSP_SCHEDULE_TWO_KERNELS;
+  if (prefix_splits_out) *prefix_splits_out = P.single ? P.d_splits : P.p_splits;
+  return CSP_OK;
+}
 
 }  // extern "C"

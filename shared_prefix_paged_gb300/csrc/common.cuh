@@ -393,6 +393,20 @@ __device__ __forceinline__ void cp_async_16(void* smem_dst, const void* gsrc, ui
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(smem_dst)),
                "l"(gsrc), "r"(src_bytes));
 }
+// The same with the shared-memory destination as a 32-bit shared address.
+__device__ __forceinline__ void cp_async_16_u32(uint32_t smem_dst, const void* gsrc,
+                                                uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_dst), "l"(gsrc),
+               "r"(src_bytes));
+}
+
+// Arrive on `bar` once every cp.async this thread has issued so far has landed (the
+// barrier's expected count is not raised: init it with one arrival per thread).
+__device__ __forceinline__ void cp_async_mbar_arrive(uint64_t* bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar))
+               : "memory");
+}
+
 __device__ __forceinline__ void cp_async_commit() {
   asm volatile("cp.async.commit_group;" ::: "memory");
 }

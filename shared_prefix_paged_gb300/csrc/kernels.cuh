@@ -16,6 +16,8 @@ namespace csp {
 // n_splits ranges, one CTA and one workspace slot each; the suffix kernel merges
 // those slots with its own partials (merge.cuh).
 struct PrefixArgs {
+  const __nv_bfloat16* k;      // K cache [num_blocks][16][num_kv_heads][D]
+  const __nv_bfloat16* v;      // V cache, same layout
   const int32_t* block_table;  // row 0: the shared pages
   int total_q;
   int num_q_heads;
@@ -58,6 +60,39 @@ struct PagedArgs {
   __nv_bfloat16* out;    // final output: direct mode (part_o == nullptr) or last contributor
   float* lse;            // natural-log LSE or nullptr
 };
+
+// Single-kernel cascade step for decode-like batches (decode_cascade.cu): at most 16
+// packed rows (query, head-in-group) per request and KV head.  CTAs [0, prefix_ctas)
+// run one prefix range each (pre.n_splits ranges per (KV head, 256-row block), range
+// s = 64-key tiles [s*key_tiles/n_splits, (s+1)*key_tiles/n_splits), slot s); then
+// every CTA takes suffix units (request, KV head) from work_counter and writes them
+// into slot pre.n_splits; after a grid-wide barrier every CTA merges a share of rows
+// (at most kDecodeMaxParts partial results per row: the prefix ranges + the suffix).
+constexpr int kDecodeMaxParts = 16;
+
+struct DecodeArgs {
+  PrefixArgs pre;            // prefix phase; part_o / part_lse hold n_splits + 1 slots
+  const __nv_bfloat16* q;    // [total_q][num_q_heads][D]
+  const __nv_bfloat16* k;    // [num_blocks][16][num_kv_heads][D]
+  const __nv_bfloat16* v;
+  const int32_t* block_table;
+  int64_t bt_stride;
+  const int32_t* cu_seqlens_q;
+  const int32_t* seq_lens;
+  int num_reqs;
+  int prefix_ctas;           // num_kv_heads * pre.pairs * pre.n_splits (<= grid)
+  int key_tiles;             // ceil(cpl / 64)
+  int* work_counter;         // zero at launch; the kernel leaves it zero
+  int* bar_count;            // zero at launch; the kernel leaves it zero
+  unsigned* bar_gen;         // any value; advanced by one per call
+  __nv_bfloat16* out;
+  float* lse;                // natural-log LSE or nullptr
+};
+
+// grid <= the number of co-resident CTAs (one per SM); launched cooperatively.
+cudaError_t launch_decode(int head_dim, const CUtensorMap& tm_q, const CUtensorMap& tm_k,
+                          const CUtensorMap& tm_v, const DecodeArgs& a, int grid,
+                          cudaStream_t stream);
 
 cudaError_t launch_prefix(int head_dim, const CUtensorMap& tm_q, const CUtensorMap& tm_k,
                           const CUtensorMap& tm_v, const PrefixArgs& a, cudaStream_t stream);

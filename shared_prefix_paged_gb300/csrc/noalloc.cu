@@ -60,12 +60,12 @@ extern "C" int cascade_attn_noalloc(const void* q, const void* k_cache, const vo
   if (need > kScratchBytes) return CSP_ERR_WORKSPACE;  // batch too large for the array
   void* scratch = nullptr;
   if ((st = scratch_address(&scratch)) != CSP_OK) return st;
-  // The array keeps whatever the previous call left in it.  Only the status word at
-  // its start must read zero when a call begins; every partial result the merge
-  // reads is written earlier in the same call.
+  // The array keeps whatever the previous call left in it.  Only its 256-byte header
+  // (the status word and the counters of the single-kernel schedule) must read zero
+  // when a call begins; every partial result the merge reads is written earlier in
+  // the same call.
   if (total_q > 0 && num_reqs > 0 &&
-      cudaMemsetAsync(scratch, 0, sizeof(int32_t), static_cast<cudaStream_t>(stream)) !=
-          cudaSuccess)
+      cudaMemsetAsync(scratch, 0, 256, static_cast<cudaStream_t>(stream)) != cudaSuccess)
     return CSP_ERR_CUDA;
   return cascade_attn(q, k_cache, v_cache, num_blocks, block_table, bt_row_stride,
                       cu_seqlens_q, seqused_k, num_reqs, total_q, max_seqlen_q, max_seqlen_k,

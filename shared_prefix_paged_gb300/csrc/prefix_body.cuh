@@ -1,0 +1,439 @@
+// prefix_body.cuh — one CTA's share of the prefix phase of cascade attention, on
+// tcgen05 tensor cores.  Used by the standalone prefix kernel (prefix_attn.cu) and
+// by the single-kernel decode schedule (decode_cascade.cu).
+//
+// "vLLM Cascade Attention：用法、场景与原理解析" §五 and §十: the prefix phase treats
+// every query of the batch as one sequence (cu_seqlens_q = [0, total_q]) so that one
+// load of a shared KV page serves a whole tile of queries; §八 Step 5 Phase 1:
+// non-causal attention over KV [0, common_prefix_len) read through block_table[:1].
+//
+// GB300 design (not the FlashAttention tiling the page describes):
+//  * a CTA owns 256 packed rows (token, head-in-group) of ONE KV head as two 128-row
+//    M tiles, so every K/V byte staged into shared memory serves 256 query rows and
+//    all the GQA heads of that KV head;
+//  * K and V pages (16 tokens x 64 features per box, 128-byte swizzle) are staged by
+//    TMA into a 4-deep ring of 64-key tiles;
+//  * per M tile, S = Q K^T (M=128, N=64) goes into one of two TMEM buffers, so the
+//    tensor core computes S(i+1) while the softmax works on S(i); P (bf16) is
+//    written back into the S buffer and used from TMEM as the A operand of
+//    O += P V (N = D).  The two M tiles use all 512 TMEM columns;
+//  * two softmax warpgroups (one per M tile) own one TMEM lane (row) per thread:
+//    online softmax in base 2 on the special-function unit, O rescaled in TMEM only
+//    when the running max grows by more than 2^8; warp 8 issues the MMAs, warp 9
+//    the TMA loads;
+//  * a CTA covers one range of the prefix's key tiles and stages its normalised rows
+//    (bf16) through shared memory, then writes them, coalesced, into workspace slot
+//    `split`, with the log2-sum-exp of each row beside them; a later merge
+//    (merge.cuh) combines the slots with the suffix phase's partials.
+#pragma once
+
+#include "common.cuh"
+#include "kernels.cuh"
+
+namespace csp {
+namespace prefix {
+
+constexpr int kRowsM = 128;    // rows per M tile
+constexpr int kRowsCta = 256;  // two M tiles
+constexpr int kKeysN = 64;     // keys per tile
+constexpr int kPage = 16;      // tokens per KV page
+constexpr int kPagesPerTile = kKeysN / kPage;
+constexpr int kStages = 4;
+constexpr int kThreads = 320;  // 2 softmax warpgroups, MMA warp, TMA warp
+constexpr int kWarpMma = 8;
+constexpr int kWarpTma = 9;
+constexpr int kLoaders = 256;  // warps 0-7 load K/V
+template <int D>
+struct Layout {
+  static constexpr int kHalves = D / 64;
+  static constexpr int kQHalf = kRowsM * 128;           // 128 rows x 64 bf16
+  static constexpr int kKVHalf = kKeysN * 128;          // 64 keys x 64 bf16
+  static constexpr int kQTile = kHalves * kQHalf;       // one M tile of Q
+  static constexpr int kKVBytes = kHalves * kKVHalf;    // one K (or V) tile
+  static constexpr int kQ = 0;                          // [2 M tiles][halves]
+  static constexpr int kK0 = kQ + 2 * kQTile;
+  static constexpr int kV0 = kK0 + kStages * kKVBytes;
+  static constexpr int kRing = kV0 + kStages * kKVBytes;
+  // after the main loop, [0, kRing) stages the CTA's 256 normalised rows:
+  // [row][D + 8] bf16 (the padding spreads the rows one warp writes over all banks)
+  static constexpr int kStageRow = D + 8;
+  static_assert(kRowsCta * kStageRow * 2 <= kRing, "staging buffer fits Q + ring");
+  static constexpr int kLse = kRing;                    // float [256]
+  static constexpr int kData = kLse + kRowsCta * 4;     // end of the data area
+};
+
+// Bytes of the caller's barrier area: 15 mbarriers, the TMEM slot and the abort flag.
+constexpr int kBarBytes = 256;
+
+// Barrier over one softmax warpgroup (id 1 or 2, 128 threads) that ORs a predicate.
+__device__ __forceinline__ bool wg_bar_any(int id, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %2, 0;\n\t"
+      "bar.red.or.pred q, %1, 128, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(id), "r"(static_cast<uint32_t>(pred))
+      : "memory");
+  return r != 0;
+}
+
+// One CTA's share of the prefix phase: packed rows [256 pair, 256 pair + 256) of KV
+// head kvh against the prefix's 64-key tiles [t_first, t_last); the normalised
+// partial goes to workspace slot `split`.  Called by every thread of a 320-thread CTA.
+// smem: 1024-byte aligned, Layout<D>::kRing + 1 KB bytes (Q, the K/V ring, then the
+// staging buffer and the row LSEs); bars: kBarBytes for the mbarriers, the TMEM slot
+// and the abort flag.  Allocates and frees all 512 TMEM columns.  Ends with every
+// global store of the partial issued; the caller syncs before reusing smem.
+template <int D>
+__device__ __forceinline__ void prefix_range(const CUtensorMap* tm_q_p,
+                                             const CUtensorMap* tm_k_p,
+                                             const CUtensorMap* tm_v_p, const PrefixArgs& a,
+                                             int kvh, int pair, int split, int t_first,
+                                             int t_last, uint8_t* smem, uint64_t* bars) {
+  using L = Layout<D>;
+  const CUtensorMap& tm_q = *tm_q_p;
+  const CUtensorMap& tm_k = *tm_k_p;
+  const CUtensorMap& tm_v = *tm_v_p;
+  uint64_t* bar_q = bars + 0;
+  uint64_t* kv_full = bars + 1;   // [kStages]
+  uint64_t* kv_empty = bars + 1 + kStages;  // [kStages]
+  uint64_t* s_full = bars + 1 + 2 * kStages;    // [2 tiles][2 buffers]
+  uint64_t* p_full = bars + 5 + 2 * kStages;    // [2 tiles][2 buffers]
+  uint64_t* o_done = bars + 9 + 2 * kStages;    // [2 tiles] every PV
+  uint64_t* o_last = bars + 11 + 2 * kStages;   // [2 tiles] the last PV
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 13 + 2 * kStages);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 14 + 2 * kStages);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int ntiles = t_last - t_first;
+  // The CTAs of the other KV heads read the same pages (other rows of them): each
+  // head starts at its own point of the range, so at any time the CTAs of one range
+  // read different pages rather than all hitting the same ones together.
+  const int rot = ntiles > 0 ? (kvh * ntiles) / a.num_kv_heads : 0;
+  auto tile_of = [&](int i) {
+    const int r = i + rot;
+    return t_first + (r >= ntiles ? r - ntiles : r);
+  };
+  const int rows_total = a.total_q * a.group;                 // packed rows of this KV head
+  const bool has_m1 = pair * kRowsCta + kRowsM < rows_total;  // second M tile has rows
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar_q, 1);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&kv_full[s], kLoaders);  // one cp.async arrival per loader thread
+      mbar_init(&kv_empty[s], 1);
+    }
+    for (int b = 0; b < 4; ++b) {
+      mbar_init(&s_full[b], 1);
+      mbar_init(&p_full[b], 128);
+    }
+    for (int m = 0; m < 2; ++m) {
+      mbar_init(&o_done[m], 1);
+      mbar_init(&o_last[m], 1);
+    }
+    *abort_flag = 0;
+    fence_mbarrier_init();
+  }
+  if (warp == kWarpMma) tmem_alloc(tmem_slot, 512);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == kWarpTma) {
+    // ------------------------------------------------------- Q by TMA (once) --
+    if (lane == 0 && ntiles > 0) {  // an empty key range loads nothing at all
+      prefetch_tensormap(&tm_q);
+      const int mts = has_m1 ? 2 : 1;
+      mbar_arrive_expect_tx(bar_q, mts * L::kQTile);
+      for (int m = 0; m < mts; ++m)
+#pragma unroll
+        for (int h = 0; h < L::kHalves; ++h)
+          tma_load_3d(smem + L::kQ + m * L::kQTile + h * L::kQHalf, &tm_q, bar_q, h * 64,
+                      kvh * a.group, (pair * kRowsCta + m * kRowsM) / a.group);
+    }
+  } else if (warp == kWarpMma) {
+    // ------------------------------------------------------------- MMA issuer --
+    if (lane == 0 && ntiles > 0) {
+      constexpr uint32_t kIdS = umma_idesc_bf16(128, kKeysN, 0, 0);
+      constexpr uint32_t kIdO = umma_idesc_bf16(128, D, 0, 1);
+      const int mts = has_m1 ? 2 : 1;
+      auto issue_s = [&](int i) {
+        const uint32_t k_addr = smem_u32(smem + L::kK0 + (i % kStages) * L::kKVBytes);
+        for (int m = 0; m < mts; ++m) {
+          const uint32_t q_addr = smem_u32(smem + L::kQ + m * L::kQTile);
+          const uint32_t d = tmem + m * 256 + (i & 1) * kKeysN;
+#pragma unroll
+          for (int k = 0; k < D / 16; ++k) {
+            const uint32_t qo = (k >> 2) * L::kQHalf + (k & 3) * 32;
+            const uint32_t ko = (k >> 2) * L::kKVHalf + (k & 3) * 32;
+            umma_bf16(d, umma_desc_sw128(q_addr + qo, 16, 1024),
+                      umma_desc_sw128(k_addr + ko, 16, 1024), kIdS, k > 0 ? 1u : 0u);
+          }
+          umma_commit(&s_full[m * 2 + (i & 1)]);
+        }
+      };
+      // Event loop: S(j) as soon as its K tile is in (and PV(j-2), the last reader of
+      // its TMEM buffer, has been issued); PV(m, j) as soon as warpgroup m's P(j) is;
+      // stage j goes back to the producer once both PV(j) are issued.  Whichever is
+      // ready first goes first, so neither a late tile nor a slow warpgroup holds up
+      // the other work.
+      bool ok = mbar_wait(bar_q, 0, abort_flag, a.status);
+      int next_s = 0, next_pv = 0, pv_m = 0;
+      unsigned long long t0 = 0;
+      while (ok && next_pv < ntiles) {
+        bool progressed = false;
+        if (next_s < ntiles && next_s <= next_pv + 1 &&
+            mbar_test_wait(&kv_full[next_s % kStages], (next_s / kStages) & 1)) {
+          // the tile was written by cp.async (generic proxy); the MMAs read it through
+          // the async proxy
+          fence_proxy_async_smem();
+          tc_fence_after();
+          issue_s(next_s);
+          ++next_s;
+          progressed = true;
+        }
+        if (next_pv < next_s &&
+            mbar_test_wait(&p_full[pv_m * 2 + (next_pv & 1)], (next_pv >> 1) & 1)) {
+          tc_fence_after();
+          const int i = next_pv, m = pv_m;
+          const uint32_t v_addr = smem_u32(smem + L::kV0 + (i % kStages) * L::kKVBytes);
+          const uint32_t p_tmem = tmem + m * 256 + (i & 1) * kKeysN;
+#pragma unroll
+          for (int kk = 0; kk < kKeysN / 16; ++kk)
+            umma_bf16_tmem_a(tmem + m * 256 + 2 * kKeysN, p_tmem + kk * 8,
+                             umma_desc_sw128(v_addr + kk * 16 * 128, L::kKVHalf, 1024), kIdO,
+                             (i > 0 || kk > 0) ? 1u : 0u);
+          umma_commit(&o_done[m]);
+          if (i == ntiles - 1) umma_commit(&o_last[m]);
+          if (++pv_m == mts) {
+            umma_commit(&kv_empty[i % kStages]);
+            pv_m = 0;
+            ++next_pv;
+          }
+          progressed = true;
+        }
+        if (progressed) {
+          t0 = 0;
+        } else if (*abort_flag) {
+          ok = false;
+        } else {
+          // bounded: nothing became ready for kWaitLimitNs
+          const unsigned long long now = global_timer_ns();
+          if (t0 == 0) {
+            t0 = now;
+          } else if (now - t0 > kWaitLimitNs) {
+            *abort_flag = 1;
+            if (a.status) atomicCAS(a.status, 0, kErrTimeout);
+            ok = false;
+          }
+        }
+      }
+    }
+    __syncwarp();
+  }
+
+  // --------------------------------------------------------------- softmax --
+  const int wg = warp >> 2;            // softmax warpgroup = M tile (warps 0-7)
+  const int row = threadIdx.x & 127;   // TMEM lane == row within the M tile
+  const uint32_t t_lane = tmem + wg * 256 + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+  const uint32_t tO = t_lane + 2 * kKeysN;
+  float m_run = -INFINITY;  // running max, log2 domain
+  float l_run = 0.f;
+  bool have = false;
+  const bool softmax_warp = warp < 8 && (wg == 0 || has_m1);
+  if (warp < 8) {
+    // ---- K/V loads: the 256 threads of warps 0-7 issue 16-byte cp.async into the
+    // 128-byte-swizzled stages (the layout the MMA descriptors expect); each thread's
+    // arrival on the stage's full barrier fires once its copies have landed.  Tile
+    // i + kStages - 1 goes into the stage of tile i - 1 as soon as PV(i - 1) is done.
+    constexpr int kChunks = D / 8;
+    constexpr int kPer = kKeysN * kChunks / kLoaders;
+    const int lt = threadIdx.x;  // loader thread
+    // Block ids of the range's pages, 32 at a time (eight tiles; lane l holds page
+    // l % 4 of tile l / 4 of the window), read a window ahead of use.  Keys past the
+    // prefix are zero-filled without a read.
+    constexpr int kIdTiles = 32 / kPagesPerTile;
+    const int npages = a.cpl / kPage;
+    auto load_ids = [&](int i_base) {
+      const int i = i_base + lane / kPagesPerTile;
+      const int page = tile_of(i) * kPagesPerTile + (lane & (kPagesPerTile - 1));
+      return i < ntiles && page < npages ? __ldg(a.block_table + page) : 0;
+    };
+    int ids_cur = ntiles > 0 ? load_ids(0) : 0;
+    int ids_nxt = ntiles > kIdTiles ? load_ids(kIdTiles) : 0;
+    const uint32_t k_ring = smem_u32(smem + L::kK0);
+    const uint32_t v_ring = smem_u32(smem + L::kV0);
+    auto issue_tile = [&](int j) {  // tiles are issued in order 0, 1, 2, ...
+      if (j > 0 && j % kIdTiles == 0) {
+        ids_cur = ids_nxt;
+        ids_nxt = j + kIdTiles < ntiles ? load_ids(j + kIdTiles) : 0;
+      }
+      const int st = j % kStages;
+      const int key0 = tile_of(j) * kKeysN;
+      const int w0 = (j % kIdTiles) * kPagesPerTile;
+      int blk[kPagesPerTile];
+#pragma unroll
+      for (int q = 0; q < kPagesPerTile; ++q) blk[q] = __shfl_sync(0xffffffffu, ids_cur, w0 + q);
+#pragma unroll
+      for (int q = 0; q < kPer; ++q) {
+        const int x = lt + kLoaders * q;
+        const int key = x / kChunks, c = x % kChunks;
+        const int pq = key >> 4;
+        const int b = pq == 0 ? blk[0] : pq == 1 ? blk[1] : pq == 2 ? blk[2] : blk[3];
+        const bool in = key0 + key < a.cpl;
+        const int64_t off =
+            ((static_cast<int64_t>(b) * kPage + (key & 15)) * a.num_kv_heads + kvh) * D + c * 8;
+        const uint32_t o = static_cast<uint32_t>(st * L::kKVBytes + (c >> 3) * L::kKVHalf +
+                                                 key * 128 + (((c & 7) ^ (key & 7)) << 4));
+        cp_async_16_u32(k_ring + o, in ? a.k + off : a.k, in ? 16u : 0u);
+        cp_async_16_u32(v_ring + o, in ? a.v + off : a.v, in ? 16u : 0u);
+      }
+      cp_async_mbar_arrive(&kv_full[st]);
+    };
+    for (int j = 0; j < ntiles && j < kStages; ++j) issue_tile(j);
+
+    bool failed = false;
+    for (int i = 0; i < ntiles; ++i) {
+      if (i >= 1 && i + kStages - 1 < ntiles) {
+        const bool ok = mbar_wait(&kv_empty[(i - 1) % kStages], ((i - 1) / kStages) & 1,
+                                  abort_flag, a.status);
+        if (wg_bar_any(1 + wg, !ok)) {
+          failed = true;
+          break;
+        }
+        issue_tile(i + kStages - 1);
+      }
+      if (!softmax_warp) continue;
+      const int tile = tile_of(i);
+      const bool ok = mbar_wait(&s_full[wg * 2 + (i & 1)], (i >> 1) & 1, abort_flag, a.status);
+      if (wg_bar_any(1 + wg, !ok)) {
+        failed = true;
+        break;
+      }
+      tc_fence_after();
+      float sv[kKeysN];
+      tmem_ld64_sync(t_lane + (i & 1) * kKeysN, sv);
+      const int valid = a.cpl - tile * kKeysN;
+      if (valid < kKeysN) {  // only the prefix's last tile can be partial
+#pragma unroll
+        for (int j = 0; j < kKeysN; ++j)
+          if (j >= valid) sv[j] = -INFINITY;
+      }
+      // row max of the raw scores as a tree (scale > 0 keeps the order)
+      float mx8[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) mx8[j] = sv[j];
+#pragma unroll
+      for (int j = 8; j < kKeysN; ++j) mx8[j & 7] = fmaxf(mx8[j & 7], sv[j]);
+      const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]))) *
+                       a.scale_log2;
+      // rescale only when the running max grows by more than 2^8 (always on the
+      // first tile, where m_run is -inf); otherwise keep the stale max: P <= 256
+      const float m_new = fmaxf(m_run, mx);
+      const bool grow = (m_new - m_run) > 8.f;
+      float alpha = 1.f;
+      if (grow) {
+        alpha = fast_exp2(m_run - m_new);
+        l_run *= alpha;
+        m_run = m_new;
+      }
+      if (i > 0 && __any_sync(0xffffffffu, grow)) {
+        // O must hold PV(i-1) before it is rescaled (the phase is unambiguous: PV(i)
+        // cannot complete before this thread has written P(i))
+        mbar_wait(&o_done[wg], (i - 1) & 1, abort_flag, a.status);
+        tc_fence_after();
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          float o[32];
+          tmem_ld32_sync(tO + c * 32, o);
+#pragma unroll
+          for (int j = 0; j < 32; ++j) o[j] *= alpha;
+          tmem_st32(tO + c * 32, o);
+        }
+      }
+      // p = 2^(s * scale * log2(e) - m): one FFMA and one ex2 per score
+      uint32_t pw[kKeysN / 2];
+      float sum4[4] = {0.f, 0.f, 0.f, 0.f};
+      const float neg_m = -m_run;
+#pragma unroll
+      for (int j = 0; j < kKeysN / 2; ++j) {
+        const float p0 = fast_exp2(fmaf(sv[2 * j], a.scale_log2, neg_m));
+        const float p1 = fast_exp2(fmaf(sv[2 * j + 1], a.scale_log2, neg_m));
+        sum4[j & 3] += p0 + p1;
+        pw[j] = pack_bf16x2(p0, p1);
+      }
+      l_run += (sum4[0] + sum4[1]) + (sum4[2] + sum4[3]);
+      tmem_st32_u(t_lane + (i & 1) * kKeysN, pw);
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(&p_full[wg * 2 + (i & 1)]);
+    }
+    if (softmax_warp && !failed && ntiles > 0) {
+      // o_done's parity alone cannot tell PV(ntiles-1) from PV(ntiles-2), which may
+      // still be running: o_last completes once, after every PV of the range
+      const bool ok = mbar_wait(&o_last[wg], 0, abort_flag, a.status);
+      have = !wg_bar_any(1 + wg, !ok);
+    }
+    cp_async_wait<0>();  // nothing of this thread's still lands in the ring below
+    tc_fence_before();
+  }
+
+  // ----------------------------------------- this split's partial -> slot --
+  // every MMA of the CTA is complete once both warpgroups saw their last o_done
+  // (or have nothing to do): Q and the ring become the staging buffer
+  __syncthreads();
+  __nv_bfloat16* stage = reinterpret_cast<__nv_bfloat16*>(smem);
+  if (softmax_warp) {
+    tc_fence_after();
+    const float inv_l = have ? 1.f / l_run : 0.f;
+    __nv_bfloat16* dst = stage + (wg * kRowsM + row) * L::kStageRow;
+#pragma unroll
+    for (int c = 0; c < D / 32; ++c) {
+      float o[32];
+      tmem_ld32_sync(tO + c * 32, o);
+#pragma unroll
+      for (int j = 0; j < 32; j += 8)
+        *reinterpret_cast<uint4*>(dst + c * 32 + j) =
+            make_uint4(pack_bf16x2(o[j] * inv_l, o[j + 1] * inv_l),
+                       pack_bf16x2(o[j + 2] * inv_l, o[j + 3] * inv_l),
+                       pack_bf16x2(o[j + 4] * inv_l, o[j + 5] * inv_l),
+                       pack_bf16x2(o[j + 6] * inv_l, o[j + 7] * inv_l));
+    }
+  }
+  // a row with no key in this range (or no query) gets -inf: weight 0 in the merge
+  float* s_lse = reinterpret_cast<float*>(smem + L::kLse);
+  if (warp < 8) s_lse[wg * kRowsM + row] = (softmax_warp && have) ? m_run + log2f(l_run)
+                                                                  : -INFINITY;
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kWarpMma) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+  // coalesced copy-out: a warp writes whole rows (D/8 lanes x 16 bytes each)
+  {
+    constexpr int kChunks = D / 8;
+    const int gshift = __ffs(a.group) - 1;  // group is a power of two
+    for (int it = threadIdx.x; it < kRowsCta * kChunks; it += kThreads) {
+      const int r = it / kChunks;
+      const int c = it % kChunks;
+      const int packed = pair * kRowsCta + r;
+      const int t = packed >> gshift;
+      if (t >= a.total_q) continue;
+      const int64_t prow = (static_cast<int64_t>(split) * a.total_q + t) * a.num_q_heads +
+                           kvh * a.group + (packed & (a.group - 1));
+      *reinterpret_cast<uint4*>(a.part_o + prow * D + c * 8) =
+          *reinterpret_cast<const uint4*>(stage + r * L::kStageRow + c * 8);
+      if (c == 0) a.part_lse[prow] = s_lse[r];
+    }
+  }
+}
+
+
+}  // namespace prefix
+}  // namespace csp
