@@ -165,21 +165,32 @@ void make_plan(int num_reqs, int total_q, int max_q, int max_k, int cpl, int Hq,
   p.bytes = p.off_part_lse + align256(static_cast<size_t>(p.n_parts) * rows_total * 4);
 
   // Decode-like batches (a request's rows of one KV head fit one 16-row MMA tile):
-  // one cooperative kernel, prefix ranges on some SMs while the others stream the
-  // suffix units.  The prefix gets enough ranges to end within about the time the
-  // whole call needs to stream its bytes: with ~0.75 us per 64-key tile of 256 rows
-  // and ~2.5 us of fixed cost per range, against the call's K/V bytes at ~5.5 TB/s
-  // (prefix once, every request's suffix at its longest).
+  // one cooperative kernel; d_base * s CTAs run the prefix ranges while the other
+  // CTAs stream the suffix.  s balances the two roles by a measured cost model: a
+  // prefix CTA takes ~4.5 us of fixed cost plus ~0.95 us per 64-key tile of 256 rows
+  // (the tensor core and softmax pace it); a suffix CTA takes ~4 us plus its share of
+  // the suffix K/V bytes at ~40 GB/s (every request's suffix counted at its longest).
+  // At least 16 CTAs are left for the suffix.
   const int d_base = p.p_pairs * Hkv;
-  if (cpl > 0 && static_cast<int64_t>(max_q) * p.group <= kDecodeRows && d_base <= sms) {
+  if (cpl > 0 && static_cast<int64_t>(max_q) * p.group <= kDecodeRows && d_base + 16 <= sms) {
     const int key_tiles = cdiv(cpl, 64);
-    const double tok_bytes = 4.0 * Hkv * D;
-    const double call_us =
-        (static_cast<double>(cpl) + static_cast<double>(num_reqs) * max_len) * tok_bytes / 5.5e6;
+    const double suffix_bytes =
+        static_cast<double>(num_reqs) * max_len * 4.0 * Hkv * D;   // K and V, bf16
     const double pair_rows = std::min(256.0, static_cast<double>(total_q) * p.group);
-    const double tile_us = 0.75 * std::max(0.5, pair_rows / 256.0);
-    int s = static_cast<int>(std::ceil(key_tiles * tile_us / std::max(1.0, call_us - 2.5)));
-    s = std::max(1, std::min({s, key_tiles, csp::kDecodeMaxParts - 1, sms / d_base}));
+    const double tile_us = 0.95 * std::max(0.5, pair_rows / 256.0);
+    const int s_max = std::max(1, std::min({key_tiles, csp::kDecodeMaxParts - 1,
+                                            (sms - 16) / d_base}));
+    int s = 1;
+    double best = -1.0;
+    for (int c = 1; c <= s_max; ++c) {
+      const double pre_us = 4.5 + cdiv(key_tiles, c) * tile_us;
+      const double suf_us = 4.0 + suffix_bytes / ((sms - d_base * c) * 40e3);
+      const double t = std::max(pre_us, suf_us);
+      if (best < 0.0 || t < best) {
+        best = t;
+        s = c;
+      }
+    }
     p.single = true;
     p.d_splits = s;
     p.d_prefix_ctas = d_base * s;

@@ -2,7 +2,7 @@
 // mbarrier waits, TMA tensor loads, tcgen05 (TMEM alloc / MMA / ld / st), cp.async,
 // ldmatrix and the warp-level mma.sync used by the HBM-bound kernels.
 //
-// Every wait on an mbarrier is bounded by wall-clock time (%globaltimer).  A wait
+// Every wait on an mbarrier is bounded (about a second of SM clock cycles).  A wait
 // that runs out writes CSP_ERR_TIMEOUT into the status word of the workspace,
 // raises the CTA's abort flag, and returns false; kernels then skip their
 // remaining work and tear down normally.  Nothing here traps.
@@ -20,6 +20,8 @@ namespace csp {
 constexpr int kErrTimeout = -6;
 // Upper bound of any single wait inside a kernel (nanoseconds).
 constexpr unsigned long long kWaitLimitNs = 1000000000ull;
+// The same bound in SM clock cycles (about one second at 2 GHz).
+constexpr long long kWaitLimitCycles = 2000000000ll;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -82,20 +84,36 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 }
 
 // Bounded wait for the phase with the given parity to complete.  `abort` is the
-// CTA's shared abort flag; `status` the workspace status word (may be null).
+// CTA's shared abort flag; `status` the workspace status word (may be null).  The
+// bound is counted in SM clock cycles (kWaitLimitCycles, about a second at the SM's
+// clock): the cycle counter is cheap to read, and the abort flag and the bound are
+// checked only every 64 polls, so a waiting thread sees the phase complete promptly.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
                                           int* status) {
   if (mbar_try_wait(bar, parity)) return true;
-  const unsigned long long t0 = global_timer_ns();
-  while (true) {
-    if (*abort) return false;
+  const long long c0 = clock64();
+  for (unsigned n = 1;; ++n) {
     if (mbar_try_wait(bar, parity)) return true;
-    if (global_timer_ns() - t0 > kWaitLimitNs) {
-      *abort = 1;
-      if (status) atomicCAS(status, 0, kErrTimeout);
-      return false;
+    if ((n & 63u) == 0) {
+      if (*abort) return false;
+      if (clock64() - c0 > kWaitLimitCycles) {
+        *abort = 1;
+        if (status) atomicCAS(status, 0, kErrTimeout);
+        return false;
+      }
     }
   }
+}
+
+// mbar_wait for a whole (converged) warp: lane 0 polls, the other lanes wait at the
+// warp barrier, so a waiting warp puts one poll stream on the shared-memory pipe
+// instead of 32 (the pipe also feeds the tensor core's operand reads).  The result is
+// the same for every lane.
+__device__ __forceinline__ bool warp_mbar_wait(uint64_t* bar, uint32_t parity,
+                                               volatile int* abort, int* status) {
+  bool ok = true;
+  if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity, abort, status);
+  return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
 }
 
 // --------------------------------------------------------------------- TMA --

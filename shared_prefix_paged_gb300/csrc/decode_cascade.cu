@@ -10,18 +10,18 @@
 // SM (a cooperative launch, so every CTA is resident):
 //  * CTAs [0, prefix_ctas) each run one range of the prefix on tcgen05 tensor cores
 //    (prefix_range, prefix_body.cuh) and write a partial into slot `split`;
-//  * every CTA (the prefix CTAs once their range is done) then streams suffix units
-//    — one per (request, KV head), all its rows (at most 16 packed (query,
-//    head-in-group) rows) in one warp-level MMA tile — taken from a counter in the
-//    workspace, so the prefix's compute and the suffix's HBM streaming overlap on
-//    different SMs and the work evens out by itself;
+//  * the other CTAs stream the suffix units — one per (request, KV head), all its
+//    rows (at most 16 packed (query, head-in-group) rows) in one warp-level MMA tile —
+//    split evenly between them, so the prefix's compute and the suffix's HBM streaming
+//    overlap on different SMs (the host picks the number of prefix ranges so that the
+//    two roles end together);
 //  * a grid-wide barrier, then every CTA merges a share of the rows: prefix slots
 //    plus the suffix slot, by LSE rescaling, into bf16 out and the natural-log LSE.
 //
 // Suffix streaming within a CTA: two groups of four warps (warps 0-3 and 4-7), each
-// an independent multistage pipeline over its own units.  Lane g of warp 8 takes
-// units for group g from the counter, resolves their request metadata and first
-// block ids, and queues them in shared memory.  A group loads its stages itself with
+// an independent multistage pipeline over its own units.  Lane g of warp 8 walks the
+// units of group g, resolves their request metadata and first block ids ahead of
+// use, and queues them in shared memory.  A group loads its stages itself with
 // 16-byte cp.async (128 threads issuing: on GB300 this path keeps more bytes in flight
 // per SM than TMA page boxes do) into 128-byte-swizzled 64-key stages, two stages
 // ahead of the one it computes; the first stage of a unit also carries its Q rows.
@@ -67,11 +67,7 @@ struct SLayout {
   static constexpr int kQ = kHalves * kQHalf;
   static constexpr int kStage = 2 * kKV + kQ;    // K, V, then Q
   static constexpr int kRing = 221184;           // bytes of stages (216 KB)
-  // at most kQueue stages per group: the load side runs at most kGroupStages - 1 tiles
-  // (so at most kQueue - 1 units) ahead of the unit being computed, whose queue slot
-  // is still taken
-  static constexpr int kGroupStages =
-      kRing / kStage / kGroups > kQueue ? kQueue : kRing / kStage / kGroups;
+  static constexpr int kGroupStages = kRing / kStage / kGroups > 4 ? 4 : kRing / kStage / kGroups;
   static constexpr int kGroupBytes = kGroupStages * kStage;
   // the data area serves both roles: the prefix's Q + ring + staging, or the stages
   static constexpr int kPrefixData = prefix::Layout<D>::kData;
@@ -83,8 +79,8 @@ struct SLayout {
   static constexpr int kDynamic = kSuffixBars + kSuffixBarBytes + 1024;  // + align slack
   static_assert(kGroupStages >= 3, "two stages in flight ahead of the computed one");
   static_assert(kStage % 1024 == 0 && (2 * kKV) % 1024 == 0, "swizzled stage alignment");
-  static_assert(2 * kGroups * kQueue * 8 +
-                        kGroups * kQueue * static_cast<int>(sizeof(UnitDesc)) + 16 <=
+  static_assert(2 * kGroups * kQueue * 8 + kGroups * kGroupStages * 8 +
+                        kGroups * kQueue * static_cast<int>(sizeof(UnitDesc)) + 32 <=
                     kSuffixBarBytes,
                 "suffix barrier area");
   static_assert(kDynamic <= 227 * 1024, "one CTA per SM");
@@ -113,26 +109,31 @@ __device__ __forceinline__ void group_sync(int g) {
 }
 
 // ----------------------------------------------------------------- scheduler --
-// Lane g of warp 8 for streaming group g (the two lanes run independently).  Takes a
-// unit from the workspace counter as soon as one of the group's queue slots is free
-// (a slot stays taken until the group has finished that unit), reads its request's
-// query range and length and the block ids of its first two tiles, and posts it.
-// The block ids are read before the request's length is known: entries past the
-// request's pages (up to the row stride) are read but never used.  Units without
-// query rows are skipped.  Ends with an end marker.
-__device__ __forceinline__ void schedule_lane(const DecodeArgs& a, uint64_t* q_full,
+// Lane g of warp 8 for streaming group g (the two lanes run independently).  The
+// suffix units are split evenly over the CTAs that run no prefix range: CTA c of those
+// takes units [c*U/n, (c+1)*U/n), its group g every other one of them starting at g.
+// As soon as one of the group's queue slots is free (a slot stays taken until the
+// group has finished that unit), the lane reads the next unit's request query range
+// and length and the block ids of its first two tiles, and posts it.  The block ids
+// are read before the request's length is known: entries past the request's pages (up
+// to the row stride) are read but never used.  Units without query rows are skipped.
+// Ends with an end marker.
+__device__ __forceinline__ void schedule_lane(const DecodeArgs& a, int g, uint64_t* q_full,
                                               uint64_t* q_empty, UnitDesc* queue,
                                               volatile int* abort_flag) {
   const PrefixArgs& p = a.pre;
   const int n_units = a.num_reqs * p.num_kv_heads;
   const int page0 = p.cpl / kPage;
-  for (int n = 0;;) {
+  const int n_ctas = static_cast<int>(gridDim.x) - a.prefix_ctas;
+  const int c = static_cast<int>(blockIdx.x) - a.prefix_ctas;
+  const int u_end = c >= 0 ? static_cast<int>((static_cast<int64_t>(c) + 1) * n_units / n_ctas) : 0;
+  int u = c >= 0 ? static_cast<int>(static_cast<int64_t>(c) * n_units / n_ctas) + g : u_end;
+  for (int n = 0;; u += kGroups) {
     const int slot = n % kQueue;
     if (n >= kQueue && !mbar_wait(&q_empty[slot], ((n / kQueue) - 1) & 1, abort_flag, p.status))
       return;
-    const int u = atomicAdd(a.work_counter, 1);
     UnitDesc& d = queue[slot];
-    if (u >= n_units) {
+    if (u >= u_end) {
       d.ntiles = -1;
       mbar_arrive(&q_full[slot]);
       return;
@@ -172,7 +173,9 @@ __device__ __forceinline__ void schedule_lane(const DecodeArgs& a, uint64_t* q_f
 template <int D>
 __device__ __forceinline__ void stream_group(const DecodeArgs& a, int g, uint8_t* gsmem,
                                              uint64_t* q_full, uint64_t* q_empty,
-                                             const UnitDesc* queue, volatile int* abort_flag) {
+                                             const UnitDesc* queue, uint64_t* st_full,
+                                             volatile int* ready_flag,
+                                             volatile int* abort_flag) {
   using L = SLayout<D>;
   constexpr int kS = L::kGroupStages;
   constexpr int kChunks = D / 8;          // 16-byte chunks per row
@@ -181,7 +184,6 @@ __device__ __forceinline__ void stream_group(const DecodeArgs& a, int g, uint8_t
   constexpr int kDT = D / 8;              // O n-tiles (8 features each)
   constexpr int kORow = D + 4;            // merge scratch row stride (floats)
   static_assert(4 * kRows * kORow * 4 + 2 * 4 * kRows * 4 <= L::kStage, "merge scratch");
-  static_assert(kS <= kQueue, "the load side never needs a slot the computed unit holds");
   const PrefixArgs& p = a.pre;
   const int tid = threadIdx.x & 127;
   const int lane = threadIdx.x & 31;
@@ -204,10 +206,18 @@ __device__ __forceinline__ void stream_group(const DecodeArgs& a, int g, uint8_t
       dst[q] = pp < npages ? __ldg(l_bt + pp) : 0;
     }
   };
-  auto issue = [&]() {
-    if (!l_end && ok && lt == 0) {
+  // Issue the next tile if its unit's descriptor is there: `must` waits for it (the
+  // group has nothing else to do), otherwise `ready` says whether it was posted.  The
+  // tile's loads arrive on the stage's barrier once they have landed.
+  auto issue = [&](bool must, bool ready) -> bool {
+    if (l_end || !ok) return false;
+    if (lt == 0) {
       // start of unit lu: its descriptor (posted by the scheduler lane)
-      ok = mbar_wait(&q_full[lu % kQueue], (lu / kQueue) & 1, abort_flag, p.status);
+      if (must) {
+        ok = warp_mbar_wait(&q_full[lu % kQueue], (lu / kQueue) & 1, abort_flag, p.status);
+      } else if (!ready) {
+        return false;
+      }
       if (ok) {
         const UnitDesc& d = queue[lu % kQueue];
         if (d.ntiles < 0) {
@@ -259,6 +269,7 @@ __device__ __forceinline__ void stream_group(const DecodeArgs& a, int g, uint8_t
                           in ? 16u : 0u);
         }
       }
+      cp_async_mbar_arrive(&st_full[issued % kS]);
       ++issued;
       if (++lt == l_nt) {
         ++lu;
@@ -271,8 +282,9 @@ __device__ __forceinline__ void stream_group(const DecodeArgs& a, int g, uint8_t
         }
         if (lt + 2 < l_nt) far_ids(lt + 2, npages, ids2);
       }
+      return true;
     }
-    cp_async_commit();  // one group per call, empty past the end
+    return false;
   };
 
   // ---- compute side: tile ct of unit cu; per-unit state in registers
@@ -284,13 +296,29 @@ __device__ __forceinline__ void stream_group(const DecodeArgs& a, int g, uint8_t
   uint32_t qa[D / 16][4];
   const int kw0 = wi * 16;  // this warp's keys within a stage
 
-  for (int s = 0; s < kS - 1; ++s) issue();
-  for (int item = 0; ok && item < issued; ++item) {
-    cp_async_wait<kS - 2>();
-    group_sync(g);  // the tile's chunks from every thread have landed; the stage of
-                    // item - 1 is no longer read by anyone
-    issue();
-    if (!ok) break;
+  // Thread 0 of the group looks (without waiting) whether the next unit is posted; the
+  // group sync publishes its answer, so every thread takes the same branch.
+  // (two flags, alternating by tile, so the next answer never overwrites one a slow
+  // warp has yet to read)
+  auto probe_next = [&](int item) {
+    if (tid == 0)
+      ready_flag[item & 1] = (l_end || lt != 0) ? 1
+                                       : (mbar_test_wait(&q_full[lu % kQueue], (lu / kQueue) & 1)
+                                              ? 1 : 0);
+  };
+  issue(true, false);
+  for (int s = 1; s < kS - 1; ++s) issue(false, false);
+  for (int item = 0; ok; ++item) {
+    if (item == issued) {
+      // nothing loaded is left to compute: wait for the next unit (or the end)
+      issue(true, false);
+      if (!ok || item == issued) break;
+    }
+    probe_next(item);
+    group_sync(g);  // the stage of tile item - 1 is no longer read by anyone: refill it
+    issue(false, ready_flag[item & 1] != 0);
+    // this tile's chunks from every thread have landed
+    if (!(ok = warp_mbar_wait(&st_full[item % kS], (item / kS) & 1, abort_flag, p.status))) break;
     const uint32_t kb = gbase + (item % kS) * L::kStage;
     const uint32_t vb = kb + L::kKV;
     if (ct == 0) {
@@ -551,27 +579,32 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   // ---- role 2: suffix units from the shared counter, two streaming groups
   {
+    constexpr int kS = L::kGroupStages;
     uint64_t* q_full = reinterpret_cast<uint64_t*>(smem + L::kSuffixBars);  // [2][kQueue]
     uint64_t* q_empty = q_full + kGroups * kQueue;                           // [2][kQueue]
-    UnitDesc* queue = reinterpret_cast<UnitDesc*>(q_empty + kGroups * kQueue);
+    uint64_t* st_full = q_empty + kGroups * kQueue;                          // [2][kS]
+    UnitDesc* queue = reinterpret_cast<UnitDesc*>(st_full + kGroups * kS);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(queue + kGroups * kQueue);
+    volatile int* ready_flag = abort_flag + 1;                               // [2][2]
     if (threadIdx.x == 0) {
       for (int i = 0; i < kGroups * kQueue; ++i) {
         mbar_init(&q_full[i], 1);
         mbar_init(&q_empty[i], 1);
       }
+      for (int i = 0; i < kGroups * kS; ++i) mbar_init(&st_full[i], 128);  // group threads
       *abort_flag = 0;
       fence_mbarrier_init();
     }
     __syncthreads();
     if (warp == kWarpScheduler) {
       if (lane < kGroups)
-        schedule_lane(a, q_full + lane * kQueue, q_empty + lane * kQueue, queue + lane * kQueue,
-                      abort_flag);
+        schedule_lane(a, lane, q_full + lane * kQueue, q_empty + lane * kQueue,
+                      queue + lane * kQueue, abort_flag);
     } else if (warp < 4 * kGroups) {
       const int g = warp >> 2;
       stream_group<D>(a, g, smem + g * L::kGroupBytes, q_full + g * kQueue,
-                      q_empty + g * kQueue, queue + g * kQueue, abort_flag);
+                      q_empty + g * kQueue, queue + g * kQueue, st_full + g * kS,
+                      ready_flag + 2 * g, abort_flag);
     }
   }
 

@@ -124,7 +124,7 @@ __device__ __forceinline__ void prefix_range(const CUtensorMap* tm_q_p,
     mbar_init(bar_q, 1);
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&kv_full[s], kLoaders);  // one cp.async arrival per loader thread
-      mbar_init(&kv_empty[s], 1);
+      mbar_init(&kv_empty[s], has_m1 ? 2 : 1);  // one commit per M tile's issuer
     }
     for (int b = 0; b < 4; ++b) {
       mbar_init(&s_full[b], 1);
@@ -155,86 +155,84 @@ __device__ __forceinline__ void prefix_range(const CUtensorMap* tm_q_p,
           tma_load_3d(smem + L::kQ + m * L::kQTile + h * L::kQHalf, &tm_q, bar_q, h * 64,
                       kvh * a.group, (pair * kRowsCta + m * kRowsM) / a.group);
     }
-  } else if (warp == kWarpMma) {
-    // ------------------------------------------------------------- MMA issuer --
-    if (lane == 0 && ntiles > 0) {
-      constexpr uint32_t kIdS = umma_idesc_bf16(128, kKeysN, 0, 0);
-      constexpr uint32_t kIdO = umma_idesc_bf16(128, D, 0, 1);
-      const int mts = has_m1 ? 2 : 1;
-      auto issue_s = [&](int i) {
-        const uint32_t k_addr = smem_u32(smem + L::kK0 + (i % kStages) * L::kKVBytes);
-        for (int m = 0; m < mts; ++m) {
-          const uint32_t q_addr = smem_u32(smem + L::kQ + m * L::kQTile);
-          const uint32_t d = tmem + m * 256 + (i & 1) * kKeysN;
+  }
+  // ------------------------------------------------- MMA issuers, one per M tile --
+  // Warp 8 issues for M tile 0, warp 9 (once Q is on its way) for M tile 1.  An MMA
+  // issue is held until the tensor pipe takes it, so a single issuer stuck behind one
+  // M tile's S could not issue the other tile's ready PV; with one issuer each, each
+  // warpgroup's S -> softmax -> PV chain advances on its own.
+  // Event loop: S(j) as soon as its K tile is in (and PV(j-2), the last reader of its
+  // TMEM buffer, has been issued); PV(j) as soon as this warpgroup's P(j) is.  Stage j
+  // goes back to the loaders once every M tile's PV(j) is done (kv_empty counts one
+  // commit per issuer).
+  if ((warp == kWarpMma || (warp == kWarpTma && has_m1)) && lane == 0 && ntiles > 0) {
+    const int m = warp == kWarpMma ? 0 : 1;
+    constexpr uint32_t kIdS = umma_idesc_bf16(128, kKeysN, 0, 0);
+    constexpr uint32_t kIdO = umma_idesc_bf16(128, D, 0, 1);
+    const uint32_t q_addr = smem_u32(smem + L::kQ + m * L::kQTile);
+    const uint32_t tm = tmem + m * 256;
+    auto issue_s = [&](int i) {
+      const uint32_t k_addr = smem_u32(smem + L::kK0 + (i % kStages) * L::kKVBytes);
+      const uint32_t d = tm + (i & 1) * kKeysN;
 #pragma unroll
-          for (int k = 0; k < D / 16; ++k) {
-            const uint32_t qo = (k >> 2) * L::kQHalf + (k & 3) * 32;
-            const uint32_t ko = (k >> 2) * L::kKVHalf + (k & 3) * 32;
-            umma_bf16(d, umma_desc_sw128(q_addr + qo, 16, 1024),
-                      umma_desc_sw128(k_addr + ko, 16, 1024), kIdS, k > 0 ? 1u : 0u);
-          }
-          umma_commit(&s_full[m * 2 + (i & 1)]);
-        }
-      };
-      // Event loop: S(j) as soon as its K tile is in (and PV(j-2), the last reader of
-      // its TMEM buffer, has been issued); PV(m, j) as soon as warpgroup m's P(j) is;
-      // stage j goes back to the producer once both PV(j) are issued.  Whichever is
-      // ready first goes first, so neither a late tile nor a slow warpgroup holds up
-      // the other work.
-      bool ok = mbar_wait(bar_q, 0, abort_flag, a.status);
-      int next_s = 0, next_pv = 0, pv_m = 0;
-      unsigned long long t0 = 0;
-      while (ok && next_pv < ntiles) {
-        bool progressed = false;
-        if (next_s < ntiles && next_s <= next_pv + 1 &&
-            mbar_test_wait(&kv_full[next_s % kStages], (next_s / kStages) & 1)) {
-          // the tile was written by cp.async (generic proxy); the MMAs read it through
-          // the async proxy
-          fence_proxy_async_smem();
-          tc_fence_after();
-          issue_s(next_s);
-          ++next_s;
-          progressed = true;
-        }
-        if (next_pv < next_s &&
-            mbar_test_wait(&p_full[pv_m * 2 + (next_pv & 1)], (next_pv >> 1) & 1)) {
-          tc_fence_after();
-          const int i = next_pv, m = pv_m;
-          const uint32_t v_addr = smem_u32(smem + L::kV0 + (i % kStages) * L::kKVBytes);
-          const uint32_t p_tmem = tmem + m * 256 + (i & 1) * kKeysN;
+      for (int k = 0; k < D / 16; ++k) {
+        const uint32_t qo = (k >> 2) * L::kQHalf + (k & 3) * 32;
+        const uint32_t ko = (k >> 2) * L::kKVHalf + (k & 3) * 32;
+        umma_bf16(d, umma_desc_sw128(q_addr + qo, 16, 1024),
+                  umma_desc_sw128(k_addr + ko, 16, 1024), kIdS, k > 0 ? 1u : 0u);
+      }
+      umma_commit(&s_full[m * 2 + (i & 1)]);
+    };
+    bool ok = mbar_wait(bar_q, 0, abort_flag, a.status);
+    int next_s = 0, next_pv = 0;
+    unsigned idle = 0;
+    long long c0 = 0;
+    while (ok && next_pv < ntiles) {
+      bool progressed = false;
+      if (next_s < ntiles && next_s <= next_pv + 1 &&
+          mbar_test_wait(&kv_full[next_s % kStages], (next_s / kStages) & 1)) {
+        // the tile was written by cp.async (generic proxy); the MMAs read it through
+        // the async proxy
+        fence_proxy_async_smem();
+        tc_fence_after();
+        issue_s(next_s);
+        ++next_s;
+        progressed = true;
+      }
+      if (next_pv < next_s &&
+          mbar_test_wait(&p_full[m * 2 + (next_pv & 1)], (next_pv >> 1) & 1)) {
+        tc_fence_after();
+        const int i = next_pv;
+        const uint32_t v_addr = smem_u32(smem + L::kV0 + (i % kStages) * L::kKVBytes);
+        const uint32_t p_tmem = tm + (i & 1) * kKeysN;
 #pragma unroll
-          for (int kk = 0; kk < kKeysN / 16; ++kk)
-            umma_bf16_tmem_a(tmem + m * 256 + 2 * kKeysN, p_tmem + kk * 8,
-                             umma_desc_sw128(v_addr + kk * 16 * 128, L::kKVHalf, 1024), kIdO,
-                             (i > 0 || kk > 0) ? 1u : 0u);
-          umma_commit(&o_done[m]);
-          if (i == ntiles - 1) umma_commit(&o_last[m]);
-          if (++pv_m == mts) {
-            umma_commit(&kv_empty[i % kStages]);
-            pv_m = 0;
-            ++next_pv;
-          }
-          progressed = true;
-        }
-        if (progressed) {
-          t0 = 0;
-        } else if (*abort_flag) {
+        for (int kk = 0; kk < kKeysN / 16; ++kk)
+          umma_bf16_tmem_a(tm + 2 * kKeysN, p_tmem + kk * 8,
+                           umma_desc_sw128(v_addr + kk * 16 * 128, L::kKVHalf, 1024), kIdO,
+                           (i > 0 || kk > 0) ? 1u : 0u);
+        umma_commit(&o_done[m]);
+        if (i == ntiles - 1) umma_commit(&o_last[m]);
+        umma_commit(&kv_empty[i % kStages]);
+        ++next_pv;
+        progressed = true;
+      }
+      if (progressed) {
+        idle = 0;
+      } else if ((++idle & 63u) == 0) {
+        // bounded: nothing became ready for kWaitLimitCycles
+        if (*abort_flag) {
           ok = false;
-        } else {
-          // bounded: nothing became ready for kWaitLimitNs
-          const unsigned long long now = global_timer_ns();
-          if (t0 == 0) {
-            t0 = now;
-          } else if (now - t0 > kWaitLimitNs) {
-            *abort_flag = 1;
-            if (a.status) atomicCAS(a.status, 0, kErrTimeout);
-            ok = false;
-          }
+        } else if (idle == 64) {
+          c0 = clock64();
+        } else if (clock64() - c0 > kWaitLimitCycles) {
+          *abort_flag = 1;
+          if (a.status) atomicCAS(a.status, 0, kErrTimeout);
+          ok = false;
         }
       }
     }
-    __syncwarp();
   }
+  if (warp >= 8) __syncwarp();
 
   // --------------------------------------------------------------- softmax --
   const int wg = warp >> 2;            // softmax warpgroup = M tile (warps 0-7)
@@ -299,8 +297,8 @@ __device__ __forceinline__ void prefix_range(const CUtensorMap* tm_q_p,
     bool failed = false;
     for (int i = 0; i < ntiles; ++i) {
       if (i >= 1 && i + kStages - 1 < ntiles) {
-        const bool ok = mbar_wait(&kv_empty[(i - 1) % kStages], ((i - 1) / kStages) & 1,
-                                  abort_flag, a.status);
+        const bool ok = warp_mbar_wait(&kv_empty[(i - 1) % kStages], ((i - 1) / kStages) & 1,
+                                       abort_flag, a.status);
         if (wg_bar_any(1 + wg, !ok)) {
           failed = true;
           break;
@@ -309,7 +307,8 @@ __device__ __forceinline__ void prefix_range(const CUtensorMap* tm_q_p,
       }
       if (!softmax_warp) continue;
       const int tile = tile_of(i);
-      const bool ok = mbar_wait(&s_full[wg * 2 + (i & 1)], (i >> 1) & 1, abort_flag, a.status);
+      const bool ok =
+          warp_mbar_wait(&s_full[wg * 2 + (i & 1)], (i >> 1) & 1, abort_flag, a.status);
       if (wg_bar_any(1 + wg, !ok)) {
         failed = true;
         break;
@@ -345,7 +344,7 @@ __device__ __forceinline__ void prefix_range(const CUtensorMap* tm_q_p,
       if (i > 0 && __any_sync(0xffffffffu, grow)) {
         // O must hold PV(i-1) before it is rescaled (the phase is unambiguous: PV(i)
         // cannot complete before this thread has written P(i))
-        mbar_wait(&o_done[wg], (i - 1) & 1, abort_flag, a.status);
+        warp_mbar_wait(&o_done[wg], (i - 1) & 1, abort_flag, a.status);
         tc_fence_after();
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
@@ -376,7 +375,7 @@ __device__ __forceinline__ void prefix_range(const CUtensorMap* tm_q_p,
     if (softmax_warp && !failed && ntiles > 0) {
       // o_done's parity alone cannot tell PV(ntiles-1) from PV(ntiles-2), which may
       // still be running: o_last completes once, after every PV of the range
-      const bool ok = mbar_wait(&o_last[wg], 0, abort_flag, a.status);
+      const bool ok = warp_mbar_wait(&o_last[wg], 0, abort_flag, a.status);
       have = !wg_bar_any(1 + wg, !ok);
     }
     cp_async_wait<0>();  // nothing of this thread's still lands in the ring below
