@@ -45,10 +45,11 @@ METRIC = "attn queries/s + HBM GB/s (% of roofline), decode N=64 P=4096 S=128"
 UNIT = "queries/s"
 L2_BYTES = 129 * 1024 * 1024
 KERNEL_SOURCES = {
-    "prefix_attn_kernel": ["prefix_attn.cu", "common.cuh", "merge.cuh"],
+    "decode_cascade_kernel": ["decode_cascade.cu", "prefix_body.cuh", "common.cuh"],
+    "prefix_attn_kernel": ["prefix_attn.cu", "prefix_body.cuh", "common.cuh", "merge.cuh"],
     "paged_attn_kernel": ["paged_attn.cu", "common.cuh", "merge.cuh"],
 }
-KERNELS = list(KERNEL_SOURCES)
+TWO_KERNELS = ["prefix_attn_kernel", "paged_attn_kernel"]
 
 
 def parse_args(argv=None):
@@ -247,6 +248,10 @@ class DeviceRun:
                                       c, b.num_q_heads, b.num_kv_heads, b.head_dim)
                    for c in (0, self.cpl))
         self.ws = csp.alloc_workspace(need, device)
+        self.schedule, self.prefix_ranges = csp.cascade_schedule(
+            b.num_reqs, b.total_q, b.max_seqlen_q, b.max_seqlen_k, self.cpl, b.num_q_heads,
+            b.num_kv_heads, b.head_dim) if self.use_cascade else (csp.SCHEDULE_TWO_KERNELS, 0)
+        self.single = self.schedule == csp.SCHEDULE_SINGLE
 
     def plan(self):
         st = self._plan_fn(*self._plan_args)
@@ -343,6 +348,9 @@ def phase_times(run: DeviceRun, rounds: int = 16, batches: int = 3):
             acc += [ev[0].elapsed_time(ev[1]), ev[1].elapsed_time(ev[2])]
             n += 1
     ms = acc / n
+    if run.single:
+        # one kernel: events 0 and 1 bracket it, event 2 follows immediately
+        return {"decode_cascade_kernel": ms[0] * 1e3, "launches_averaged": n}
     return {"prefix_attn_kernel": ms[0] * 1e3, "paged_attn_kernel": ms[1] * 1e3,
             "launches_averaged": n}
 
@@ -427,7 +435,11 @@ def roofline_entry(kernel, us, b, run, peaks, workload):
     kvtok = accounting.kv_bytes_per_token(b.num_kv_heads, b.head_dim)
     q_bytes = rows * b.head_dim * 2
     cpl = run.cpl
-    if kernel == "prefix_attn_kernel":
+    if kernel == "decode_cascade_kernel":
+        # the whole step in one launch: KV once, q read, out + lse written
+        bytes_ = accounting.cascade_min_bytes(b, cpl)
+        flops = None
+    elif kernel == "prefix_attn_kernel":
         # prefix KV once, q, and one partial per row (bf16 O, fp32 LSE)
         bytes_ = cpl * kvtok + q_bytes + rows * (b.head_dim * 2 + 4)
         flops = accounting.prefix_flops(b.total_q, b.num_q_heads, b.head_dim, cpl)
@@ -509,6 +521,8 @@ def run_ours(args, dist: Dist):
             "workload": b.name, "num_reqs": b.num_reqs, "total_q": b.total_q,
             "common_prefix_len": run.cpl, "q_heads": b.num_q_heads, "kv_heads": b.num_kv_heads,
             "head_dim": b.head_dim, "block_size": b.block_size, "path": path,
+            "schedule": ("single kernel" if run.single else "prefix + suffix kernels")
+                        if path == "cascade" else "flat", "prefix_ranges": run.prefix_ranges,
             "l2": f"inputs larger than L2: {R} rotating copies of q and the KV cache",
             "step": "host cascade_plan + device path replayed from a CUDA graph of "
                     f"{R} steps", "parallelism": f"replicas x{dist.world}"},
@@ -518,20 +532,21 @@ def run_ours(args, dist: Dist):
         "hbm_frac_of_measured": round(min_bytes / (us_call * 1e-6) / 1e9 / peaks["hbm_gbs"], 4),
         "hbm_frac_of_8tbs": round(min_bytes / (us_call * 1e-6) / 1e9 / 8000.0, 4),
         "host_s_in_timed_region": round(host_s, 4),
-        "gpu_launches": K * (2 if path == "cascade" else 1),
+        "gpu_launches": K * (2 if path == "cascade" and not run.single else 1),
     }
     if clocks:
         result["clocks"] = clocks.summary(t0, t1)
 
     if path == "cascade":
         ph = phase_times(run)
-        entries = {k: roofline_entry(k, ph[k], b, run, peaks, b.name) for k in KERNELS}
-        dominant = max(KERNELS, key=lambda k: ph[k])
+        kernels = ["decode_cascade_kernel"] if run.single else TWO_KERNELS
+        entries = {k: roofline_entry(k, ph[k], b, run, peaks, b.name) for k in kernels}
+        dominant = max(kernels, key=lambda k: ph[k])
         result["roofline"] = entries[dominant]
-        result["phases_us"] = {k: round(ph[k], 3) for k in KERNELS}
+        result["phases_us"] = {k: round(ph[k], 3) for k in kernels}
         result["phases_roofline"] = {k: {kk: entries[k][kk] for kk in
                                          ("bound", "achieved", "unit", "frac")}
-                                     for k in KERNELS}
+                                     for k in kernels}
         result["phase_launches_averaged"] = ph["launches_averaged"]
 
     if not args.quick:
