@@ -21,13 +21,12 @@ int cuda_fail(cudaError_t e) {
 }
 
 constexpr int kPage = 16;
-// Workspace header: [0] status word; [64] unit counter, [128] barrier count and
-// [192] barrier generation of the single-kernel decode schedule (that kernel leaves
-// the first two at zero when it exits).
+// Workspace header: [0] status word; counters of the single-kernel decode schedule,
+// which that kernel leaves at zero when it exits: [64] written prefix ranges, [128]
+// finished CTAs.
 constexpr size_t kHeaderBytes = 256;
-constexpr size_t kOffWorkCounter = 64;
-constexpr size_t kOffBarCount = 128;
-constexpr size_t kOffBarGen = 192;
+constexpr size_t kOffPrefixDone = 64;
+constexpr size_t kOffExitCount = 128;
 // Most packed rows (query, head-in-group) per request and KV head that the decode
 // schedule takes: one warp-level MMA tile.
 constexpr int kDecodeRows = 16;
@@ -117,7 +116,7 @@ struct LaunchPlan {
   size_t off_counters = 0, off_part_o = 0, off_part_lse = 0, bytes = 0;
   // single-kernel decode schedule (decode_cascade.cu)
   bool single = false;
-  int d_splits = 0, d_prefix_ctas = 0, d_grid = 0;
+  int d_splits = 0, d_prefix_ctas = 0, d_prefix_units = 0, d_grid = 0;
   size_t d_off_o = 0, d_off_lse = 0;
 };
 
@@ -165,39 +164,55 @@ void make_plan(int num_reqs, int total_q, int max_q, int max_k, int cpl, int Hq,
   p.bytes = p.off_part_lse + align256(static_cast<size_t>(p.n_parts) * rows_total * 4);
 
   // Decode-like batches (a request's rows of one KV head fit one 16-row MMA tile):
-  // one cooperative kernel; d_base * s CTAs run the prefix ranges while the other
-  // CTAs stream the suffix.  s balances the two roles by a measured cost model: a
-  // prefix CTA takes ~4.5 us of fixed cost plus ~0.95 us per 64-key tile of 256 rows
-  // (the tensor core and softmax pace it); a suffix CTA takes ~4 us plus its share of
-  // the suffix K/V bytes at ~40 GB/s (every request's suffix counted at its longest).
-  // At least 16 CTAs are left for the suffix.
+  // one cooperative kernel.  d_base * s CTAs each run a prefix range and then stream
+  // k suffix units; the other CTAs stream the rest of the suffix units from the start.
+  // s and k come from a cost model measured on GB300 (per CTA, in us): ~3 until the
+  // first bytes land; a prefix 64-key tile at the CTA's load rate (~33 GB/s per SM) or
+  // ~1.1 per 256 rows (tensor core and softmax), whichever is slower; ~3 to write the
+  // range's partial; a suffix unit's K/V bytes (its longest request) at ~33 GB/s.
+  // Both kinds of CTA should finish together.
   const int d_base = p.p_pairs * Hkv;
-  if (cpl > 0 && static_cast<int64_t>(max_q) * p.group <= kDecodeRows && d_base + 16 <= sms) {
-    const int key_tiles = cdiv(cpl, 64);
-    const double suffix_bytes =
-        static_cast<double>(num_reqs) * max_len * 4.0 * Hkv * D;   // K and V, bf16
+  if (cpl > 0 && static_cast<int64_t>(max_q) * p.group <= kDecodeRows && d_base <= sms) {
+    const int pre_tiles = cdiv(cpl, 64);
+    const double kRate = 33e3;  // bytes per us per SM
     const double pair_rows = std::min(256.0, static_cast<double>(total_q) * p.group);
-    const double tile_us = 0.95 * std::max(0.5, pair_rows / 256.0);
-    const int s_max = std::max(1, std::min({key_tiles, csp::kDecodeMaxParts - 1,
-                                            (sms - 16) / d_base}));
-    int s = 1;
+    const double tile_us = std::max(64.0 * 4.0 * D / kRate, 1.1 * pair_rows / 256.0);
+    const double unit_us =
+        std::max(1, cdiv(max_len, 64)) * 64.0 * 4.0 * D / kRate;  // K and V, bf16
+    const int64_t units = static_cast<int64_t>(num_reqs) * Hkv;
+    const int s_max = std::max(1, std::min({pre_tiles, csp::kDecodeMaxParts - 1, sms / d_base}));
+    int s = 0, k = 0;
     double best = -1.0;
     for (int c = 1; c <= s_max; ++c) {
-      const double pre_us = 4.5 + cdiv(key_tiles, c) * tile_us;
-      const double suf_us = 4.0 + suffix_bytes / ((sms - d_base * c) * 40e3);
-      const double t = std::max(pre_us, suf_us);
-      if (best < 0.0 || t < best) {
-        best = t;
-        s = c;
+      const int64_t pc = static_cast<int64_t>(d_base) * c;  // prefix CTAs
+      const int64_t nc = sms - pc;                            // suffix-only CTAs
+      const double pre_us = 3.0 + cdiv(pre_tiles, c) * tile_us + 3.0;
+      const int64_t k_lo = nc > 0 ? 0 : cdiv64(units, pc);
+      for (int64_t kk = k_lo; kk <= cdiv64(units, pc); ++kk) {
+        const int64_t rest = std::max<int64_t>(0, units - pc * kk);
+        const int64_t per = nc > 0 ? cdiv64(rest, nc) : 0;
+        if (std::max(kk, per) > csp::kDecodeMaxUnitsPerCta) continue;
+        const double t = std::max(pre_us + kk * unit_us, 3.0 + per * unit_us);
+        if (best < 0.0 || t < best) {
+          best = t;
+          s = c;
+          k = static_cast<int>(kk);
+        }
+        if (per == 0) break;
       }
     }
-    p.single = true;
-    p.d_splits = s;
-    p.d_prefix_ctas = d_base * s;
-    p.d_grid = sms;
-    p.d_off_o = kHeaderBytes;
-    p.d_off_lse = p.d_off_o + align256(static_cast<size_t>(s + 1) * rows_total * D * 2);
-    p.bytes = std::max(p.bytes, p.d_off_lse + align256(static_cast<size_t>(s + 1) * rows_total * 4));
+    if (s > 0) {
+      p.single = true;
+      p.d_splits = s;
+      p.d_prefix_ctas = d_base * s;
+      p.d_prefix_units = k;
+      p.d_grid = sms;
+      // slots: [0, s) the prefix ranges, s the suffix
+      p.d_off_o = kHeaderBytes;
+      p.d_off_lse = p.d_off_o + align256(static_cast<size_t>(s + 1) * rows_total * D * 2);
+      p.bytes = std::max(p.bytes,
+                         p.d_off_lse + align256(static_cast<size_t>(s + 1) * rows_total * 4));
+    }
   }
   *P = p;
 }
@@ -279,10 +294,10 @@ int attention_call(const void* q, const void* k_cache, const void* v_cache, int3
     da.seq_lens = seqused_k;
     da.num_reqs = num_reqs;
     da.prefix_ctas = P.d_prefix_ctas;
+    da.prefix_units = P.d_prefix_units;
     da.key_tiles = cdiv(cpl, 64);
-    da.work_counter = reinterpret_cast<int*>(ws + kOffWorkCounter);
-    da.bar_count = reinterpret_cast<int*>(ws + kOffBarCount);
-    da.bar_gen = reinterpret_cast<unsigned*>(ws + kOffBarGen);
+    da.prefix_done = reinterpret_cast<int*>(ws + kOffPrefixDone);
+    da.exit_count = reinterpret_cast<int*>(ws + kOffExitCount);
     da.out = static_cast<__nv_bfloat16*>(out);
     da.lse = lse;
     // phase events: [0] before the kernel, [1..3] after it

@@ -18,6 +18,7 @@
 namespace csp {
 
 constexpr int kErrTimeout = -6;
+constexpr int kErrInternal = -7;  // a kernel's bookkeeping limit was exceeded (a bug)
 // Upper bound of any single wait inside a kernel (nanoseconds).
 constexpr unsigned long long kWaitLimitNs = 1000000000ull;
 // The same bound in SM clock cycles (about one second at 2 GHz).

@@ -6,30 +6,27 @@
 // §十: the prefix is read once for all queries instead of once per request.
 //
 // A decode batch moves far more suffix bytes than prefix bytes, while the prefix is
-// the only dense contraction.  So the SMs take roles inside one grid of one CTA per
-// SM (a cooperative launch, so every CTA is resident):
-//  * CTAs [0, prefix_ctas) each run one range of the prefix on tcgen05 tensor cores
-//    (prefix_range, prefix_body.cuh) and write a partial into slot `split`;
-//  * the other CTAs stream the suffix units — one per (request, KV head), all its
-//    rows (at most 16 packed (query, head-in-group) rows) in one warp-level MMA tile —
-//    split evenly between them, so the prefix's compute and the suffix's HBM streaming
-//    overlap on different SMs (the host picks the number of prefix ranges so that the
-//    two roles end together);
-//  * a grid-wide barrier, then every CTA merges a share of the rows: prefix slots
-//    plus the suffix slot, by LSE rescaling, into bf16 out and the natural-log LSE.
+// the only dense contraction.  On GB300 a single SM pulls only ~30-40 GB/s from HBM or
+// L2 through cp.async or page-sized TMA boxes, so the whole GPU's bandwidth is there
+// only while every SM streams.  So the SMs share the work inside one grid of one CTA
+// per SM (a cooperative launch, so every CTA is resident):
+//  * CTAs [0, prefix_ctas) each first run one range of the prefix on tcgen05 tensor
+//    cores (prefix_range, prefix_body.cuh), write a partial into slot `split` and
+//    count it in prefix_done; then, like every other CTA, they stream suffix units;
+//  * a suffix unit is one (request, KV head): all its rows (at most 16 packed
+//    (query, head-in-group) rows) in one warp-level MMA tile.  Each prefix CTA takes
+//    prefix_units of them, the other CTAs share the rest evenly; the host picks the
+//    number of prefix ranges and prefix_units so that every CTA ends together;
+//  * merge_attn_states without a grid-wide barrier: a CTA lists its finished units
+//    and, once prefix_done is complete, merges their rows (prefix slots plus the
+//    suffix slot, by LSE rescaling) into bf16 out and the natural-log LSE.
 //
-// Suffix streaming within a CTA: two groups of four warps (warps 0-3 and 4-7), each
-// an independent multistage pipeline over its own units.  Lane g of warp 8 walks the
-// units of group g, resolves their request metadata and first block ids ahead of
-// use, and queues them in shared memory.  A group loads its stages itself with
-// 16-byte cp.async (128 threads issuing: on GB300 this path keeps more bytes in flight
-// per SM than TMA page boxes do) into 128-byte-swizzled 64-key stages, two stages
-// ahead of the one it computes; the first stage of a unit also carries its Q rows.
-// Warp w of the group takes keys [16 w, 16 w + 16) of each stage: S = Q K^T and
-// O += P V on mma.sync m16n8k16 (bf16 in, fp32 accumulate) fed by ldmatrix, masked
-// by the request's causal limit (bottom-right alignment, §四), online softmax in
-// base 2; at the unit's end the four warps merge through shared memory and write the
-// normalised bf16 rows and their log2-sum-exp.
+// Suffix streaming within a CTA (stream_units): lane 0 of warp 8 walks the CTA's
+// units, resolves their request metadata and first block ids ahead of use, and queues
+// them in shared memory; warps 0-7 load two 64-key tiles of a unit at a time with
+// 16-byte cp.async into 128-byte-swizzled stages (on GB300 this path keeps more bytes
+// in flight per SM than TMA page boxes do), two such pairs ahead of the one they
+// compute, and each warp computes 16 keys of one tile on mma.sync.
 #include <type_traits>
 
 #include "merge.cuh"
@@ -43,20 +40,13 @@ constexpr int kKeys = 64;                   // keys per suffix stage
 constexpr int kPage = 16;
 constexpr int kTilePages = kKeys / kPage;
 constexpr int kRows = 16;                   // packed rows of a suffix unit (one M tile)
-constexpr int kGroups = 2;                  // streaming groups of four warps
-constexpr int kWarpScheduler = 8;           // lane g schedules for group g
-constexpr int kQueue = 4;                   // units resolved ahead, per group
-constexpr int kDescPages = 8;               // block ids resolved ahead: two 64-key tiles
+constexpr int kStreamWarps = 8;             // warps 0-7 stream the suffix
+constexpr int kStreamThreads = 32 * kStreamWarps;
+constexpr int kWarpScheduler = 8;           // produces the suffix items
+constexpr int kPend = kDecodeMaxUnitsPerCta;  // finished units awaiting their merge
+constexpr int kWarpWatcher = 9;             // lane 0 waits for every prefix range
 
 static_assert(kThreads == 320, "ten warps: 8 softmax/streaming, MMA/scheduler, TMA");
-
-// A suffix unit resolved by the scheduler: its request's metadata and the physical
-// blocks of its first two tiles.  ntiles < 0: no more units.
-struct UnitDesc {
-  int r, kvh, q0, q_len, seq_len, ntiles;
-  int pages[kDescPages];
-  int pad[2];
-};
 
 template <int D>
 struct SLayout {
@@ -66,22 +56,19 @@ struct SLayout {
   static constexpr int kQHalf = kRows * 128;
   static constexpr int kQ = kHalves * kQHalf;
   static constexpr int kStage = 2 * kKV + kQ;    // K, V, then Q
-  static constexpr int kRing = 221184;           // bytes of stages (216 KB)
-  static constexpr int kGroupStages = kRing / kStage / kGroups > 4 ? 4 : kRing / kStage / kGroups;
-  static constexpr int kGroupBytes = kGroupStages * kStage;
-  // the data area serves both roles: the prefix's Q + ring + staging, or the stages
+  static constexpr int kItem = 2 * kStage;       // two tiles of one unit
+  static constexpr int kRing = 221184;           // bytes of items (216 KB)
+  static constexpr int kSlots = kRing / kItem > 6 ? 6 : kRing / kItem;
+  // the data area serves both roles: the prefix's Q + ring + staging, or the items
   static constexpr int kPrefixData = prefix::Layout<D>::kData;
-  static constexpr int kData =
-      kGroups * kGroupBytes > kPrefixData ? kGroups * kGroupBytes : kPrefixData;
+  static constexpr int kData = kSlots * kItem > kPrefixData ? kSlots * kItem : kPrefixData;
   static constexpr int kPrefixBars = kData;                        // prefix::kBarBytes
   static constexpr int kSuffixBars = kPrefixBars + prefix::kBarBytes;
-  static constexpr int kSuffixBarBytes = 1024;
+  static constexpr int kSuffixBarBytes = 2048;
   static constexpr int kDynamic = kSuffixBars + kSuffixBarBytes + 1024;  // + align slack
-  static_assert(kGroupStages >= 3, "two stages in flight ahead of the computed one");
+  static_assert(kSlots >= 3, "two items in flight ahead of the computed one");
   static_assert(kStage % 1024 == 0 && (2 * kKV) % 1024 == 0, "swizzled stage alignment");
-  static_assert(2 * kGroups * kQueue * 8 + kGroups * kGroupStages * 8 +
-                        kGroups * kQueue * static_cast<int>(sizeof(UnitDesc)) + 32 <=
-                    kSuffixBarBytes,
+  static_assert(2 * kSlots * 8 + kSlots * 32 + 16 + kPend * 8 <= kSuffixBarBytes,
                 "suffix barrier area");
   static_assert(kDynamic <= 227 * 1024, "one CTA per SM");
 };
@@ -94,422 +81,67 @@ __device__ __forceinline__ uint32_t sw128(int row, int c) {
                                (((c & 7) ^ (row & 7)) << 4));
 }
 
-__device__ __forceinline__ unsigned ld_acquire_gpu_u32(const unsigned* p) {
-  unsigned v;
-  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+__device__ __forceinline__ int ld_acquire_gpu_s32(const int* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
   return v;
 }
 
-__device__ __forceinline__ void st_release_gpu_u32(unsigned* p, unsigned v) {
-  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+__device__ __forceinline__ void red_release_gpu_add(int* p, int v) {
+  asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
-__device__ __forceinline__ void group_sync(int g) {
-  asm volatile("bar.sync %0, 128;" ::"r"(1 + g) : "memory");
-}
-
-// ----------------------------------------------------------------- scheduler --
-// Lane g of warp 8 for streaming group g (the two lanes run independently).  The
-// suffix units are split evenly over the CTAs that run no prefix range: CTA c of those
-// takes units [c*U/n, (c+1)*U/n), its group g every other one of them starting at g.
-// As soon as one of the group's queue slots is free (a slot stays taken until the
-// group has finished that unit), the lane reads the next unit's request query range
-// and length and the block ids of its first two tiles, and posts it.  The block ids
-// are read before the request's length is known: entries past the request's pages (up
-// to the row stride) are read but never used.  Units without query rows are skipped.
-// Ends with an end marker.
-__device__ __forceinline__ void schedule_lane(const DecodeArgs& a, int g, uint64_t* q_full,
-                                              uint64_t* q_empty, UnitDesc* queue,
-                                              volatile int* abort_flag) {
-  const PrefixArgs& p = a.pre;
-  const int n_units = a.num_reqs * p.num_kv_heads;
-  const int page0 = p.cpl / kPage;
-  const int n_ctas = static_cast<int>(gridDim.x) - a.prefix_ctas;
-  const int c = static_cast<int>(blockIdx.x) - a.prefix_ctas;
-  const int u_end = c >= 0 ? static_cast<int>((static_cast<int64_t>(c) + 1) * n_units / n_ctas) : 0;
-  int u = c >= 0 ? static_cast<int>(static_cast<int64_t>(c) * n_units / n_ctas) + g : u_end;
-  for (int n = 0;; u += kGroups) {
-    const int slot = n % kQueue;
-    if (n >= kQueue && !mbar_wait(&q_empty[slot], ((n / kQueue) - 1) & 1, abort_flag, p.status))
-      return;
-    UnitDesc& d = queue[slot];
-    if (u >= u_end) {
-      d.ntiles = -1;
-      mbar_arrive(&q_full[slot]);
-      return;
-    }
-    const int r = u / p.num_kv_heads;
-    const int q0 = __ldg(a.cu_seqlens_q + r);
-    const int q_len = __ldg(a.cu_seqlens_q + r + 1) - q0;
-    const int seq_len = __ldg(a.seq_lens + r);
-    const int32_t* bt = a.block_table + static_cast<int64_t>(r) * a.bt_stride;
-    int pg[kDescPages];
-#pragma unroll
-    for (int j = 0; j < kDescPages; ++j)
-      pg[j] = __ldg(bt + min(static_cast<int64_t>(page0 + j), a.bt_stride - 1));
-    if (q_len <= 0) continue;  // no query rows: nothing to compute or write
-    const int nkeys = seq_len - p.cpl;
-    d.r = r;
-    d.kvh = u - r * p.num_kv_heads;
-    d.q0 = q0;
-    d.q_len = q_len;
-    d.seq_len = seq_len;
-    d.ntiles = nkeys > 0 ? (nkeys + kKeys - 1) / kKeys : 0;
-#pragma unroll
-    for (int j = 0; j < kDescPages; ++j) d.pages[j] = pg[j];
-    mbar_arrive(&q_full[slot]);
-    ++n;
-  }
-}
-
-// ------------------------------------------------------------------ streaming --
-// Streaming group g (warps 4g .. 4g+3, 128 threads) over the units its scheduler lane
-// posts.  A cp.async pipeline of kGroupStages stages: the group issues the tile
-// kGroupStages - 1 ahead of the one it computes (one commit group per tile), then
-// waits for the computed tile's group and syncs.  Thread t loads the 16-byte chunks
-// t, t + 128, ... of the tile's K and V (and, with a unit's first tile, of its Q
-// rows); keys past the request and padding rows are zero-filled without a read.
-// Returns after the end marker (or an abort).
-template <int D>
-__device__ __forceinline__ void stream_group(const DecodeArgs& a, int g, uint8_t* gsmem,
-                                             uint64_t* q_full, uint64_t* q_empty,
-                                             const UnitDesc* queue, uint64_t* st_full,
-                                             volatile int* ready_flag,
-                                             volatile int* abort_flag) {
-  using L = SLayout<D>;
-  constexpr int kS = L::kGroupStages;
-  constexpr int kChunks = D / 8;          // 16-byte chunks per row
-  constexpr int kPer = kKeys * kChunks / 128;   // K (and V) chunks per thread per tile
-  constexpr int kQPer = kRows * kChunks / 128;  // Q chunks per thread
-  constexpr int kDT = D / 8;              // O n-tiles (8 features each)
-  constexpr int kORow = D + 4;            // merge scratch row stride (floats)
-  static_assert(4 * kRows * kORow * 4 + 2 * 4 * kRows * 4 <= L::kStage, "merge scratch");
-  const PrefixArgs& p = a.pre;
-  const int tid = threadIdx.x & 127;
-  const int lane = threadIdx.x & 31;
-  const int wi = tid >> 5;
-  const uint32_t gbase = smem_u32(gsmem);
-  const int page0 = p.cpl / kPage;
-  const int hkv = p.num_kv_heads;
-  bool ok = true;
-
-  // ---- load side: next tile (unit lu, tile lt); block ids of tiles lt, lt+1, lt+2
-  int lu = 0, lt = 0, l_nt = 0;
-  bool l_end = false;
-  int issued = 0;
-  int ids0[kTilePages], ids1[kTilePages], ids2[kTilePages];
-  const int32_t* l_bt = a.block_table;
-  auto far_ids = [&](int tile, int npages, int (&dst)[kTilePages]) {
-#pragma unroll
-    for (int q = 0; q < kTilePages; ++q) {
-      const int pp = page0 + tile * kTilePages + q;
-      dst[q] = pp < npages ? __ldg(l_bt + pp) : 0;
-    }
-  };
-  // Issue the next tile if its unit's descriptor is there: `must` waits for it (the
-  // group has nothing else to do), otherwise `ready` says whether it was posted.  The
-  // tile's loads arrive on the stage's barrier once they have landed.
-  auto issue = [&](bool must, bool ready) -> bool {
-    if (l_end || !ok) return false;
-    if (lt == 0) {
-      // start of unit lu: its descriptor (posted by the scheduler lane)
-      if (must) {
-        ok = warp_mbar_wait(&q_full[lu % kQueue], (lu / kQueue) & 1, abort_flag, p.status);
-      } else if (!ready) {
-        return false;
-      }
-      if (ok) {
-        const UnitDesc& d = queue[lu % kQueue];
-        if (d.ntiles < 0) {
-          l_end = true;
-        } else {
-          l_nt = max(d.ntiles, 1);  // no suffix key: one all-masked (zero-filled) tile
-          l_bt = a.block_table + static_cast<int64_t>(d.r) * a.bt_stride;
-#pragma unroll
-          for (int q = 0; q < kTilePages; ++q) {
-            ids0[q] = d.pages[q];
-            ids1[q] = d.pages[kTilePages + q];
-          }
-          if (l_nt > 2) far_ids(2, (d.seq_len + kPage - 1) / kPage, ids2);
-        }
-      }
-    }
-    if (!l_end && ok) {
-      const UnitDesc& d = queue[lu % kQueue];
-      const int seq_len = d.seq_len, kvh = d.kvh;
-      const int npages = (seq_len + kPage - 1) / kPage;
-      const uint32_t sb = gbase + (issued % kS) * L::kStage;
-      const int key0 = p.cpl + lt * kKeys;
-#pragma unroll
-      for (int j = 0; j < kPer; ++j) {
-        const int x = tid + 128 * j;
-        const int key = x / kChunks, c = x % kChunks;
-        const int pq = key >> 4;
-        // pages past the request re-read the tile's first page (its keys are masked)
-        const int blk = page0 + lt * kTilePages + pq < npages ? ids0[pq] : ids0[0];
-        const bool in = key0 + key < seq_len;
-        const int64_t off =
-            ((static_cast<int64_t>(blk) * kPage + (key & 15)) * hkv + kvh) * D + c * 8;
-        cp_async_16_u32(sb + sw128<kKeys>(key, c), in ? a.k + off : a.k, in ? 16u : 0u);
-        cp_async_16_u32(sb + L::kKV + sw128<kKeys>(key, c), in ? a.v + off : a.v,
-                        in ? 16u : 0u);
-      }
-      if (lt == 0) {
-        const int rows = d.q_len * p.group;
-#pragma unroll
-        for (int j = 0; j < kQPer; ++j) {
-          const int x = tid + 128 * j;
-          const int row = x / kChunks, c = x % kChunks;
-          const bool in = row < rows;
-          const int qi = row / p.group, hj = row - qi * p.group;
-          const int64_t off =
-              (static_cast<int64_t>(d.q0 + qi) * p.num_q_heads + kvh * p.group + hj) * D +
-              c * 8;
-          cp_async_16_u32(sb + 2 * L::kKV + sw128<kRows>(row, c), in ? a.q + off : a.q,
-                          in ? 16u : 0u);
-        }
-      }
-      cp_async_mbar_arrive(&st_full[issued % kS]);
-      ++issued;
-      if (++lt == l_nt) {
-        ++lu;
-        lt = 0;
-      } else {
-#pragma unroll
-        for (int q = 0; q < kTilePages; ++q) {
-          ids0[q] = ids1[q];
-          ids1[q] = ids2[q];
-        }
-        if (lt + 2 < l_nt) far_ids(lt + 2, npages, ids2);
-      }
-      return true;
-    }
-    return false;
-  };
-
-  // ---- compute side: tile ct of unit cu; per-unit state in registers
-  int cu = 0, ct = 0, c_nt = 0;
-  int c_seq = 0, c_qlen = 0, c_q0 = 0, c_kvh = 0, rows_valid = 0;
-  int pos[2] = {-1, -1};
-  float o[kDT][4];
-  float m_run[2], l_run[2];
-  uint32_t qa[D / 16][4];
-  const int kw0 = wi * 16;  // this warp's keys within a stage
-
-  // Thread 0 of the group looks (without waiting) whether the next unit is posted; the
-  // group sync publishes its answer, so every thread takes the same branch.
-  // (two flags, alternating by tile, so the next answer never overwrites one a slow
-  // warp has yet to read)
-  auto probe_next = [&](int item) {
-    if (tid == 0)
-      ready_flag[item & 1] = (l_end || lt != 0) ? 1
-                                       : (mbar_test_wait(&q_full[lu % kQueue], (lu / kQueue) & 1)
-                                              ? 1 : 0);
-  };
-  issue(true, false);
-  for (int s = 1; s < kS - 1; ++s) issue(false, false);
-  for (int item = 0; ok; ++item) {
-    if (item == issued) {
-      // nothing loaded is left to compute: wait for the next unit (or the end)
-      issue(true, false);
-      if (!ok || item == issued) break;
-    }
-    probe_next(item);
-    group_sync(g);  // the stage of tile item - 1 is no longer read by anyone: refill it
-    issue(false, ready_flag[item & 1] != 0);
-    // this tile's chunks from every thread have landed
-    if (!(ok = warp_mbar_wait(&st_full[item % kS], (item / kS) & 1, abort_flag, p.status))) break;
-    const uint32_t kb = gbase + (item % kS) * L::kStage;
-    const uint32_t vb = kb + L::kKV;
-    if (ct == 0) {
-      const UnitDesc& d = queue[cu % kQueue];
-      c_nt = max(d.ntiles, 1);
-      c_seq = d.seq_len;
-      c_qlen = d.q_len;
-      c_q0 = d.q0;
-      c_kvh = d.kvh;
-      rows_valid = c_qlen * p.group;
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int rho = (lane >> 2) + 8 * h;
-        pos[h] = rho < rows_valid ? c_seq - c_qlen + rho / p.group : -1;
-        m_run[h] = -INFINITY;
-        l_run[h] = 0.f;
-      }
-#pragma unroll
-      for (int i = 0; i < kDT; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
-      const uint32_t qb = kb + 2 * L::kKV;
-#pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk) {
-        const int row = (lane & 7) + ((lane >> 3) & 1) * 8;
-        const int c = kk * 2 + (lane >> 4);
-        ldmatrix_x4(qb + sw128<kRows>(row, c), qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3]);
-      }
-    }
-    // S = Q K^T over this warp's 16 keys (two n-tiles of 8)
-    float sacc[2][4];
-#pragma unroll
-    for (int i = 0; i < 2; ++i) sacc[i][0] = sacc[i][1] = sacc[i][2] = sacc[i][3] = 0.f;
-#pragma unroll
-    for (int kk = 0; kk < D / 16; ++kk) {
-      const int key = kw0 + (lane & 7) + (lane >> 4) * 8;
-      const int c = kk * 2 + ((lane >> 3) & 1);
-      uint32_t b0, b1, b2, b3;
-      ldmatrix_x4(kb + sw128<kKeys>(key, c), b0, b1, b2, b3);
-      mma_bf16_16816(sacc[0], qa[kk], b0, b1);
-      mma_bf16_16816(sacc[1], qa[kk], b2, b3);
-    }
-    // mask (keys past the request, and the causal limit), online softmax in base 2
-    const int key0 = p.cpl + ct * kKeys + kw0;
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      float mx = -INFINITY;
-#pragma unroll
-      for (int nt = 0; nt < 2; ++nt) {
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const int kabs = key0 + nt * 8 + (lane & 3) * 2 + e;
-          float& sref = sacc[nt][2 * h + e];
-          sref = (kabs < c_seq && kabs <= pos[h]) ? sref * p.scale_log2 : -INFINITY;
-          mx = fmaxf(mx, sref);
-        }
-      }
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-      const float m_new = fmaxf(m_run[h], mx);
-      const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
-      const float alpha = fast_exp2(m_run[h] - m_use);
-      float sum = 0.f;
-#pragma unroll
-      for (int nt = 0; nt < 2; ++nt) {
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          float& sref = sacc[nt][2 * h + e];
-          sref = fast_exp2(sref - m_use);
-          sum += sref;
-        }
-      }
-      l_run[h] = l_run[h] * alpha + sum;
-      m_run[h] = m_new;
-#pragma unroll
-      for (int dt = 0; dt < kDT; ++dt) {
-        o[dt][2 * h] *= alpha;
-        o[dt][2 * h + 1] *= alpha;
-      }
-    }
-    // O += P V over the same 16 keys
-    uint32_t pa[4];
-    pa[0] = pack_bf16x2(sacc[0][0], sacc[0][1]);
-    pa[1] = pack_bf16x2(sacc[0][2], sacc[0][3]);
-    pa[2] = pack_bf16x2(sacc[1][0], sacc[1][1]);
-    pa[3] = pack_bf16x2(sacc[1][2], sacc[1][3]);
-#pragma unroll
-    for (int dp = 0; dp < kDT / 2; ++dp) {
-      const int key = kw0 + (lane & 7) + ((lane >> 3) & 1) * 8;
-      const int c = dp * 2 + (lane >> 4);
-      uint32_t b0, b1, b2, b3;
-      ldmatrix_x4_trans(vb + sw128<kKeys>(key, c), b0, b1, b2, b3);
-      mma_bf16_16816(o[2 * dp], pa, b0, b1);
-      mma_bf16_16816(o[2 * dp + 1], pa, b2, b3);
-    }
-    if (++ct < c_nt) continue;
-
-    // ---- the unit's last tile: the four warps' (max, sum, O) -> one normalised
-    // partial per row, through this stage's memory (nobody reads its K/V any more
-    // once the group has synced; the next write to it comes after the next sync)
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      l_run[h] += __shfl_xor_sync(0xffffffffu, l_run[h], 1);
-      l_run[h] += __shfl_xor_sync(0xffffffffu, l_run[h], 2);
-    }
-    group_sync(g);
-    float* s_o = reinterpret_cast<float*>(gsmem + (item % kS) * L::kStage);  // [4][16][kORow]
-    float* s_m = s_o + 4 * kRows * kORow;                                    // [4][16]
-    float* s_l = s_m + 4 * kRows;                                            // [4][16]
-    if ((lane & 3) == 0) {
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        s_m[wi * kRows + (lane >> 2) + 8 * h] = m_run[h];
-        s_l[wi * kRows + (lane >> 2) + 8 * h] = l_run[h];
-      }
-    }
-    group_sync(g);
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const int rr = (lane >> 2) + 8 * h;
-      if (rr >= rows_valid) continue;
-      float mg = -INFINITY;
-#pragma unroll
-      for (int w = 0; w < 4; ++w) mg = fmaxf(mg, s_m[w * kRows + rr]);
-      const float sc = (m_run[h] == -INFINITY) ? 0.f : fast_exp2(m_run[h] - mg);
-      float* dst = s_o + (wi * kRows + rr) * kORow;
-#pragma unroll
-      for (int dt = 0; dt < kDT; ++dt) {
-        const int d = dt * 8 + (lane & 3) * 2;
-        *reinterpret_cast<float2*>(dst + d) = make_float2(o[dt][2 * h] * sc, o[dt][2 * h + 1] * sc);
-      }
-    }
-    group_sync(g);
-    const int64_t slot_rows = static_cast<int64_t>(p.n_splits) * p.total_q * p.num_q_heads;
-    // warp wi finalises rows wi, wi + 4, ...; lane c owns features [4c, 4c + 4)
-    for (int rr = wi; rr < rows_valid; rr += 4) {
-      float mg = -INFINITY;
-#pragma unroll
-      for (int w = 0; w < 4; ++w) mg = fmaxf(mg, s_m[w * kRows + rr]);
-      float lsum = 0.f;
-#pragma unroll
-      for (int w = 0; w < 4; ++w) {
-        const float mw = s_m[w * kRows + rr];
-        lsum += (mw == -INFINITY) ? 0.f : s_l[w * kRows + rr] * fast_exp2(mw - mg);
-      }
-      const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
-      const int qi = rr / p.group, j = rr - qi * p.group;
-      const int64_t prow =
-          slot_rows + static_cast<int64_t>(c_q0 + qi) * p.num_q_heads + c_kvh * p.group + j;
-      if (lane < D / 4) {
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-        for (int w = 0; w < 4; ++w) {
-          const float4 v =
-              *reinterpret_cast<const float4*>(s_o + (w * kRows + rr) * kORow + lane * 4);
-          acc.x += v.x;
-          acc.y += v.y;
-          acc.z += v.z;
-          acc.w += v.w;
-        }
-        store_bf16x4(p.part_o + prow * D + lane * 4,
-                     make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv));
-      }
-      if (lane == 0) p.part_lse[prow] = lsum > 0.f ? mg + log2f(lsum) : -INFINITY;
-    }
-    // the unit is done: its queue slot goes back to the scheduler lane
-    if (tid == 0) mbar_arrive(&q_empty[cu % kQueue]);
-    ++cu;
-    ct = 0;
-  }
-  cp_async_wait<0>();
+// the eight streaming warps (named barrier 1)
+__device__ __forceinline__ void stream_sync() {
+  asm volatile("bar.sync 1, %0;" ::"r"(kStreamThreads) : "memory");
 }
 
 // -------------------------------------------------------------------- merge --
-// merge_attn_states for one output row with 16 lanes (a half warp): slots [0, n) of
-// the workspace, n <= kDecodeMaxParts.  Lane i holds the weight of slot i and
-// features [i*D/16, (i+1)*D/16).  Every slot's loads are issued before any is used,
-// so a row costs one round trip to L2.  An empty slot (lse -inf) gets weight 0 and
-// whatever it holds never mixes in.
+// Loads from L2 whose order the compiler keeps: every slot of a row is requested
+// before the first result is used, so a row costs one round trip.  A false `pred`
+// leaves the destination zero without a read.
+__device__ __forceinline__ void ld_cg_pred(uint4& v, const void* ptr, bool pred) {
+  v = make_uint4(0u, 0u, 0u, 0u);
+  asm volatile(
+      "{\n .reg .pred q;\n setp.ne.b32 q, %5, 0;\n"
+      " @q ld.global.cg.v4.u32 {%0, %1, %2, %3}, [%4];\n}\n"
+      : "+r"(v.x), "+r"(v.y), "+r"(v.z), "+r"(v.w)
+      : "l"(ptr), "r"(pred ? 1 : 0));
+}
+__device__ __forceinline__ void ld_cg_pred(uint2& v, const void* ptr, bool pred) {
+  v = make_uint2(0u, 0u);
+  asm volatile(
+      "{\n .reg .pred q;\n setp.ne.b32 q, %3, 0;\n @q ld.global.cg.v2.u32 {%0, %1}, [%2];\n}\n"
+      : "+r"(v.x), "+r"(v.y)
+      : "l"(ptr), "r"(pred ? 1 : 0));
+}
+__device__ __forceinline__ float ld_cg_pred_f32(const float* ptr, bool pred, float fill) {
+  float v = fill;
+  asm volatile(
+      "{\n .reg .pred q;\n setp.ne.b32 q, %2, 0;\n @q ld.global.cg.f32 %0, [%1];\n}\n"
+      : "+f"(v)
+      : "l"(ptr), "r"(pred ? 1 : 0));
+  return v;
+}
+
+// merge_attn_states for one row with 16 lanes (a half warp): workspace slots
+// [first, first + n), n <= 16, into dst_o (bf16) and *dst_lse (log2 domain, or the
+// natural-log LSE with `natural`); a null destination is not written.  Lane i holds the weight of
+// slot first + i and features [i*D/16, (i+1)*D/16).  An empty slot (lse -inf) gets
+// weight 0 and whatever it holds never mixes in.
 template <int D>
-__device__ __forceinline__ void merge_row_half(const DecodeArgs& a, int64_t row, int n,
-                                               int hl) {
+__device__ __forceinline__ void merge_slots(const PrefixArgs& p, int64_t row, int first,
+                                            int n, int hl, __nv_bfloat16* dst_o,
+                                            float* dst_lse, bool natural) {
   constexpr int kF = D / 16;  // features per lane: 8 (16 bytes) or 4 (8 bytes)
+  constexpr int kMax = 16;
   using Vec = typename std::conditional<kF == 8, uint4, uint2>::type;
-  static_assert(kDecodeMaxParts <= 16, "one slot weight per lane of a half warp");
-  const PrefixArgs& p = a.pre;
   const int64_t rows = static_cast<int64_t>(p.total_q) * p.num_q_heads;
-  const float lw = hl < n ? __ldcg(p.part_lse + hl * rows + row) : -INFINITY;
-  Vec v[kDecodeMaxParts];
-  const __nv_bfloat16* base = p.part_o + row * D + hl * kF;
+  Vec v[kMax];
+  const __nv_bfloat16* base = p.part_o + (first * rows + row) * D + hl * kF;
 #pragma unroll
-  for (int s = 0; s < kDecodeMaxParts; ++s)
-    if (s < n) v[s] = __ldcg(reinterpret_cast<const Vec*>(base + s * rows * D));
+  for (int s = 0; s < kMax; ++s) ld_cg_pred(v[s], base + s * rows * D, s < n);
+  const float lw = ld_cg_pred_f32(p.part_lse + (first + hl) * rows + row, hl < n, -INFINITY);
   const unsigned mask = 0xffffu << (threadIdx.x & 16);
   float mx = lw;
 #pragma unroll
@@ -523,7 +155,7 @@ __device__ __forceinline__ void merge_row_half(const DecodeArgs& a, int64_t row,
 #pragma unroll
   for (int f = 0; f < kF; ++f) acc[f] = 0.f;
 #pragma unroll
-  for (int s = 0; s < kDecodeMaxParts; ++s) {
+  for (int s = 0; s < kMax; ++s) {
     const float ws = __shfl_sync(mask, w, s, 16) * inv;
     if (s < n && ws != 0.f) {
       const uint32_t* u = reinterpret_cast<const uint32_t*>(&v[s]);
@@ -539,11 +171,398 @@ __device__ __forceinline__ void merge_row_half(const DecodeArgs& a, int64_t row,
   uint32_t* ou = reinterpret_cast<uint32_t*>(&o);
 #pragma unroll
   for (int f = 0; f < kF / 2; ++f) ou[f] = pack_bf16x2(acc[2 * f], acc[2 * f + 1]);
-  *reinterpret_cast<Vec*>(a.out + row * D + hl * kF) = o;
-  if (hl == 0 && a.lse != nullptr)
-    a.lse[row] = wsum > 0.f ? (mx + log2f(wsum)) * 0.69314718055994531f : -INFINITY;
+  if (dst_o != nullptr) *reinterpret_cast<Vec*>(dst_o + hl * kF) = o;
+  if (hl == 0 && dst_lse != nullptr) {
+    const float l2 = wsum > 0.f ? mx + log2f(wsum) : -INFINITY;
+    *dst_lse = natural ? l2 * 0.69314718055994531f : l2;
+  }
 }
 
+// ------------------------------------------------------------------ streaming --
+// The CTA's suffix units, two 64-key tiles of a unit at a time.  An "item" is a pair
+// of stages holding tiles t and t + 1 of one unit (the second left empty when the
+// unit has a single tile left); a unit's first item also carries its Q rows.  Items
+// go through a ring of kSlots in shared memory:
+//  * warp 8 produces them.  It walks the CTA's units (see unit_range), reads each
+//    request's query range, length and block ids (lane j the id of the item's page j,
+//    one item ahead), and fills a free slot: every lane issues one TMA page box
+//    (64 features x 16 tokens of one KV head) of the item's K or V, and the lanes copy
+//    the Q rows with 16-byte cp.async (rows past the unit's are zero-filled without a
+//    read).  A page past the request re-reads the item's first page (its keys are
+//    masked); the item's descriptor tells the consumers which unit and tiles it holds.
+//  * warps 0-7 consume them: warps 0-3 compute the item's first tile and warps 4-7 its
+//    second, warp w taking keys [16 (w % 4), 16 (w % 4) + 16): S = Q K^T and O += P V
+//    on mma.sync m16n8k16 (bf16 in, fp32 accumulate) fed by ldmatrix, masked by the
+//    request's causal limit (bottom-right alignment, §四), online softmax in base 2.
+//    V rows past the request are zeroed first (a TMA page holds whatever the cache
+//    has there).  At the unit's end the eight warps merge through the item's memory
+//    and write the normalised bf16 rows and their log2-sum-exp into the suffix slot;
+//    the unit then waits in `pend` for its rows' final merge.
+// Loads never hold up the computing warps: the producer alone waits for free slots.
+struct ItemDesc {
+  int q0, q_len, seq_len, kvh, ntiles, t0, pad0, pad1;  // ntiles < 0: no more items
+};
+
+// The CTA's units: a CTA that ran a prefix range takes the next prefix_units units in
+// CTA order after it; the remaining units are split evenly over the other CTAs (CTA c
+// of those n takes units [c*R/n, (c+1)*R/n) of the R left).
+__device__ __forceinline__ void unit_range(const DecodeArgs& a, int& u_begin, int& u_end) {
+  const int n_units = a.num_reqs * a.pre.num_kv_heads;
+  const int b = static_cast<int>(blockIdx.x);
+  const int64_t pre_units =
+      min(static_cast<int64_t>(a.prefix_ctas) * a.prefix_units, static_cast<int64_t>(n_units));
+  if (b < a.prefix_ctas) {
+    u_begin = static_cast<int>(min(static_cast<int64_t>(b) * a.prefix_units, pre_units));
+    u_end = static_cast<int>(min(static_cast<int64_t>(b + 1) * a.prefix_units, pre_units));
+  } else {
+    const int64_t rest = n_units - pre_units;
+    const int n_ctas = static_cast<int>(gridDim.x) - a.prefix_ctas;
+    const int c = b - a.prefix_ctas;
+    u_begin = static_cast<int>(pre_units + c * rest / n_ctas);
+    u_end = static_cast<int>(pre_units + (c + 1) * rest / n_ctas);
+  }
+}
+
+template <int D>
+__device__ __forceinline__ void produce_items(const DecodeArgs& a, const CUtensorMap* tm_k,
+                                              const CUtensorMap* tm_v, uint8_t* ring,
+                                              uint64_t* st_full, uint64_t* st_empty,
+                                              ItemDesc* idesc, volatile int* abort_flag) {
+  using L = SLayout<D>;
+  constexpr int kS = L::kSlots;
+  constexpr int kChunks = D / 8;
+  constexpr int kBoxesPerTile = kTilePages * 2 * L::kHalves;  // pages x {K, V} x halves
+  static_assert(2 * kBoxesPerTile <= 32, "one box per lane");
+  const PrefixArgs& p = a.pre;
+  const int lane = threadIdx.x & 31;
+  const int page0 = p.cpl / kPage;
+  const int hkv = p.num_kv_heads;
+  int u, u_end;
+  unit_range(a, u, u_end);
+  // the unit being produced and the next one's metadata (read one unit ahead)
+  int item = 0;
+  // next unit's raw metadata: lanes 0-2 hold cu_seqlens_q[r], cu_seqlens_q[r+1],
+  // seq_lens[r]; lanes 0-7 also the block ids of its first eight pages
+  auto fetch = [&](int uu, int& meta, int& id) {
+    meta = 0;
+    id = 0;
+    if (uu >= u_end) return;
+    const int r = uu / hkv;
+    const int32_t* bt = a.block_table + static_cast<int64_t>(r) * a.bt_stride;
+    if (lane == 0) meta = __ldg(a.cu_seqlens_q + r);
+    if (lane == 1) meta = __ldg(a.cu_seqlens_q + r + 1);
+    if (lane == 2) meta = __ldg(a.seq_lens + r);
+    // read before the request's length is known: entries past its pages (up to the
+    // row stride) are read but never used
+    if (lane < 2 * kTilePages) id = __ldg(bt + min(static_cast<int64_t>(page0 + lane), a.bt_stride - 1));
+  };
+  int n_meta, n_id;
+  fetch(u, n_meta, n_id);
+  bool ok = true;
+  for (; ok; ++u) {
+    // ---- unit u (or the end): its metadata, and the next unit's on its way
+    int q0 = 0, q_len = 0, seq_len = 0, ids = 0;
+    const bool end = u >= u_end;
+    if (!end) {
+      q0 = __shfl_sync(0xffffffffu, n_meta, 0);
+      q_len = __shfl_sync(0xffffffffu, n_meta, 1) - q0;
+      seq_len = __shfl_sync(0xffffffffu, n_meta, 2);
+      ids = n_id;
+      fetch(u + 1, n_meta, n_id);
+      if (q_len <= 0) continue;  // no query rows: nothing to compute or write
+    }
+    const int kvh = u - (u / hkv) * hkv;
+    const int nkeys = seq_len - p.cpl;
+    const int nt = end ? -1 : max(1, (nkeys + kKeys - 1) / kKeys);  // >= 1 all-masked tile
+    const int npages = (seq_len + kPage - 1) / kPage;
+    const int32_t* bt = a.block_table + static_cast<int64_t>(end ? 0 : u / hkv) * a.bt_stride;
+    for (int t0 = 0; end ? t0 == 0 : t0 < nt; t0 += 2) {
+      const int slot = item % kS;
+      if (item >= kS &&
+          !(ok = warp_mbar_wait(&st_empty[slot], ((item / kS) - 1) & 1, abort_flag, p.status)))
+        break;
+      const int tiles = end ? 0 : min(2, nt - t0);
+      if (lane == 0) {
+        ItemDesc& d = idesc[slot];
+        d.q0 = q0;
+        d.q_len = q_len;
+        d.seq_len = seq_len;
+        d.kvh = kvh;
+        d.ntiles = nt;
+        d.t0 = t0;
+        mbar_arrive_expect_tx(&st_full[slot], static_cast<uint32_t>(tiles * 2 * L::kKV));
+      }
+      __syncwarp();
+      // block ids of the item's pages: lane j holds page page0 + 4 t0 + j; the next
+      // item's are read now, one item ahead
+      int nxt = 0;
+      if (t0 + 2 < nt && lane < 2 * kTilePages) {
+        const int pp = page0 + (t0 + 2) * kTilePages + lane;
+        nxt = pp < npages ? __ldg(bt + pp) : 0;
+      }
+      {
+        const int h = lane / kBoxesPerTile, rem = lane % kBoxesPerTile;
+        const int q = rem / (2 * L::kHalves), kv = (rem / L::kHalves) & 1, hf = rem % L::kHalves;
+        const int pq = (h * kTilePages + q) & (2 * kTilePages - 1);
+        const int id_q = __shfl_sync(0xffffffffu, ids, pq);
+        const int id_0 = __shfl_sync(0xffffffffu, ids, 0);
+        const int page = page0 + t0 * kTilePages + pq;
+        const int blk = page < npages ? id_q : id_0;
+        if (lane < tiles * kBoxesPerTile) {
+          uint8_t* dst = ring + slot * L::kItem + h * L::kStage + kv * L::kKV +
+                         hf * L::kKVHalf + q * (kPage * 128);
+          tma_load_3d(dst, kv ? tm_v : tm_k, &st_full[slot], hf * 64, kvh, blk * kPage);
+        }
+      }
+      if (t0 == 0 && !end) {
+        const uint32_t qb = smem_u32(ring + slot * L::kItem + 2 * L::kKV);
+        const int rows = q_len * p.group;
+        for (int x = lane; x < kRows * kChunks; x += 32) {
+          const int row = x / kChunks, c = x % kChunks;
+          const bool in = row < rows;
+          const int qi = row / p.group, hj = row - qi * p.group;
+          const int64_t off =
+              (static_cast<int64_t>(q0 + qi) * p.num_q_heads + kvh * p.group + hj) * D + c * 8;
+          cp_async_16_u32(qb + sw128<kRows>(row, c), in ? a.q + off : a.q, in ? 16u : 0u);
+        }
+      }
+      cp_async_mbar_arrive(&st_full[slot]);
+      ++item;
+      ids = nxt;
+    }
+    if (end) break;
+  }
+  cp_async_wait<0>();
+}
+
+template <int D>
+__device__ __forceinline__ void consume_items(const DecodeArgs& a, uint8_t* ring,
+                                              uint64_t* st_full, uint64_t* st_empty,
+                                              const ItemDesc* idesc, int2* pend,
+                                              volatile int* n_pend, volatile int* abort_flag) {
+  using L = SLayout<D>;
+  constexpr int kS = L::kSlots;
+  constexpr int kChunks = D / 8;          // 16-byte chunks per row
+  constexpr int kDT = D / 8;              // O n-tiles (8 features each)
+  constexpr int kORow = D + 4;            // merge scratch row (floats)
+  static_assert(kStreamWarps * kRows * kORow * 4 + 2 * kStreamWarps * kRows * 4 <= L::kItem,
+                "merge scratch fits one item");
+  const PrefixArgs& p = a.pre;
+  const int tid = threadIdx.x;  // 0 .. 255
+  const int lane = tid & 31;
+  const int wi = tid >> 5;      // 0 .. 7
+  const int half = wi >> 2;     // which tile of the item this warp computes
+  const int kw0 = (wi & 3) * 16;  // this warp's keys within its tile
+  const uint32_t rbase = smem_u32(ring);
+
+  int c_nt = 0, c_seq = 0, c_qlen = 0, c_q0 = 0, c_kvh = 0, rows_valid = 0;
+  int pos[2] = {-1, -1};
+  float o[kDT][4];
+  float m_run[2], l_run[2];
+  uint32_t qa[D / 16][4];
+  for (int item = 0;; ++item) {
+    const int slot = item % kS;
+    const uint32_t par = (item / kS) & 1;
+    if (!warp_mbar_wait(&st_full[slot], par, abort_flag, p.status)) break;
+    // every lane observes the completed phase (the TMA bytes are visible to it)
+    mbar_test_wait(&st_full[slot], par);
+    const ItemDesc d = idesc[slot];
+    if (d.ntiles < 0) break;
+    const uint32_t ib = rbase + slot * L::kItem;
+    const int t0 = d.t0;
+    if (t0 == 0) {
+      c_nt = d.ntiles;
+      c_seq = d.seq_len;
+      c_qlen = d.q_len;
+      c_q0 = d.q0;
+      c_kvh = d.kvh;
+      rows_valid = c_qlen * p.group;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int rho = (lane >> 2) + 8 * h;
+        pos[h] = rho < rows_valid ? c_seq - c_qlen + rho / p.group : -1;
+        m_run[h] = -INFINITY;
+        l_run[h] = 0.f;
+      }
+#pragma unroll
+      for (int i = 0; i < kDT; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+      const uint32_t qb = ib + 2 * L::kKV;
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const int row = (lane & 7) + ((lane >> 3) & 1) * 8;
+        const int c = kk * 2 + (lane >> 4);
+        ldmatrix_x4(qb + sw128<kRows>(row, c), qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3]);
+      }
+    }
+    if (t0 + half < c_nt) {
+      const uint32_t kb = ib + half * L::kStage;
+      const uint32_t vb = kb + L::kKV;
+      const int key0 = p.cpl + (t0 + half) * kKeys + kw0;
+      if (key0 + 16 > c_seq) {
+        // this warp's keys past the request: zero their V rows (P is 0 there, but the
+        // page may hold anything)
+        for (int x = lane; x < 16 * kChunks; x += 32) {
+          const int k = x / kChunks, c = x % kChunks;
+          if (key0 + k >= c_seq)
+            asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(
+                             vb + sw128<kKeys>(kw0 + k, c)), "r"(0u)
+                         : "memory");
+        }
+        __syncwarp();
+      }
+      // S = Q K^T over this warp's 16 keys (two n-tiles of 8)
+      float sacc[2][4];
+#pragma unroll
+      for (int i = 0; i < 2; ++i) sacc[i][0] = sacc[i][1] = sacc[i][2] = sacc[i][3] = 0.f;
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const int key = kw0 + (lane & 7) + (lane >> 4) * 8;
+        const int c = kk * 2 + ((lane >> 3) & 1);
+        uint32_t b0, b1, b2, b3;
+        ldmatrix_x4(kb + sw128<kKeys>(key, c), b0, b1, b2, b3);
+        mma_bf16_16816(sacc[0], qa[kk], b0, b1);
+        mma_bf16_16816(sacc[1], qa[kk], b2, b3);
+      }
+      // mask (keys past the request, and the causal limit), online softmax in base 2
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        float mx = -INFINITY;
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int kabs = key0 + nt * 8 + (lane & 3) * 2 + e;
+            float& sref = sacc[nt][2 * h + e];
+            sref = (kabs < c_seq && kabs <= pos[h]) ? sref * p.scale_log2 : -INFINITY;
+            mx = fmaxf(mx, sref);
+          }
+        }
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+        const float m_new = fmaxf(m_run[h], mx);
+        const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
+        const float alpha = fast_exp2(m_run[h] - m_use);
+        float sum = 0.f;
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            float& sref = sacc[nt][2 * h + e];
+            sref = fast_exp2(sref - m_use);
+            sum += sref;
+          }
+        }
+        l_run[h] = l_run[h] * alpha + sum;
+        m_run[h] = m_new;
+#pragma unroll
+        for (int dt = 0; dt < kDT; ++dt) {
+          o[dt][2 * h] *= alpha;
+          o[dt][2 * h + 1] *= alpha;
+        }
+      }
+      // O += P V over the same 16 keys
+      uint32_t pa[4];
+      pa[0] = pack_bf16x2(sacc[0][0], sacc[0][1]);
+      pa[1] = pack_bf16x2(sacc[0][2], sacc[0][3]);
+      pa[2] = pack_bf16x2(sacc[1][0], sacc[1][1]);
+      pa[3] = pack_bf16x2(sacc[1][2], sacc[1][3]);
+#pragma unroll
+      for (int dp = 0; dp < kDT / 2; ++dp) {
+        const int key = kw0 + (lane & 7) + ((lane >> 3) & 1) * 8;
+        const int c = dp * 2 + (lane >> 4);
+        uint32_t b0, b1, b2, b3;
+        ldmatrix_x4_trans(vb + sw128<kKeys>(key, c), b0, b1, b2, b3);
+        mma_bf16_16816(o[2 * dp], pa, b0, b1);
+        mma_bf16_16816(o[2 * dp + 1], pa, b2, b3);
+      }
+    }
+    if (t0 + 2 >= c_nt) {
+      // ---- the unit's last item: the eight warps' (max, sum, O) -> one normalised
+      // partial per row, through this item's memory
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        l_run[h] += __shfl_xor_sync(0xffffffffu, l_run[h], 1);
+        l_run[h] += __shfl_xor_sync(0xffffffffu, l_run[h], 2);
+      }
+      stream_sync();  // every warp is done reading this item's K/V
+      float* s_o = reinterpret_cast<float*>(ring + slot * L::kItem);  // [8][16][kORow]
+      float* s_m = s_o + kStreamWarps * kRows * kORow;                // [8][16]
+      float* s_l = s_m + kStreamWarps * kRows;                        // [8][16]
+      if ((lane & 3) == 0) {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          s_m[wi * kRows + (lane >> 2) + 8 * h] = m_run[h];
+          s_l[wi * kRows + (lane >> 2) + 8 * h] = l_run[h];
+        }
+      }
+      stream_sync();
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int rr = (lane >> 2) + 8 * h;
+        if (rr >= rows_valid) continue;
+        float mg = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < kStreamWarps; ++w) mg = fmaxf(mg, s_m[w * kRows + rr]);
+        const float sc = (m_run[h] == -INFINITY) ? 0.f : fast_exp2(m_run[h] - mg);
+        float* dst = s_o + (wi * kRows + rr) * kORow;
+#pragma unroll
+        for (int dt = 0; dt < kDT; ++dt) {
+          const int dd = dt * 8 + (lane & 3) * 2;
+          *reinterpret_cast<float2*>(dst + dd) =
+              make_float2(o[dt][2 * h] * sc, o[dt][2 * h + 1] * sc);
+        }
+      }
+      stream_sync();
+      const int64_t slot_rows = static_cast<int64_t>(p.n_splits) * p.total_q * p.num_q_heads;
+      // warp wi finalises rows wi and wi + 8; lane c owns features [4c, 4c + 4)
+      for (int rr = wi; rr < rows_valid; rr += kStreamWarps) {
+        float mg = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < kStreamWarps; ++w) mg = fmaxf(mg, s_m[w * kRows + rr]);
+        float lsum = 0.f;
+#pragma unroll
+        for (int w = 0; w < kStreamWarps; ++w) {
+          const float mw = s_m[w * kRows + rr];
+          lsum += (mw == -INFINITY) ? 0.f : s_l[w * kRows + rr] * fast_exp2(mw - mg);
+        }
+        const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+        const int qi = rr / p.group, j = rr - qi * p.group;
+        const int64_t prow =
+            slot_rows + static_cast<int64_t>(c_q0 + qi) * p.num_q_heads + c_kvh * p.group + j;
+        if (lane < D / 4) {
+          float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+          for (int w = 0; w < kStreamWarps; ++w) {
+            const float4 v =
+                *reinterpret_cast<const float4*>(s_o + (w * kRows + rr) * kORow + lane * 4);
+            acc.x += v.x;
+            acc.y += v.y;
+            acc.z += v.z;
+            acc.w += v.w;
+          }
+          store_bf16x4(p.part_o + prow * D + lane * 4,
+                       make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv));
+        }
+        if (lane == 0) p.part_lse[prow] = lsum > 0.f ? mg + log2f(lsum) : -INFINITY;
+      }
+      // the unit waits for its merge at the end of the kernel
+      if (tid == 0) {
+        const int n = *n_pend;
+        if (n < kPend) {
+          pend[n] = make_int2(c_q0, (c_kvh << 8) | rows_valid);
+          *n_pend = n + 1;
+        } else {
+          atomicCAS(p.status, 0, kErrInternal);  // the host keeps units per CTA <= kPend
+        }
+      }
+    }
+    // the item goes back to the producer (its TMA will overwrite what this warp
+    // wrote through the generic proxy)
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&st_empty[slot]);
+  }
+}
 
 // ------------------------------------------------------------------ the kernel --
 template <int D>
@@ -558,8 +577,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   const PrefixArgs& p = a.pre;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  // generation of the grid barrier at the end (read now, off the critical path)
-  const unsigned g0 = threadIdx.x == 0 ? ld_acquire_gpu_u32(a.bar_gen) : 0u;
 
   // ---- role 1: one range of the prefix phase (tcgen05)
   if (static_cast<int>(blockIdx.x) < a.prefix_ctas) {
@@ -577,69 +594,109 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
   }
 
-  // ---- role 2: suffix units from the shared counter, two streaming groups
+  // ---- role 2: the suffix units, produced by warp 8 and computed by warps 0-7
+  constexpr int kS = L::kSlots;
+  uint64_t* st_full = reinterpret_cast<uint64_t*>(smem + L::kSuffixBars);  // [kS]
+  uint64_t* st_empty = st_full + kS;                                        // [kS]
+  ItemDesc* idesc = reinterpret_cast<ItemDesc*>(st_empty + kS);              // [kS]
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(idesc + kS);
+  volatile int* n_pend = abort_flag + 1;
+  volatile int* prefix_ready = abort_flag + 2;
+  int2* pend = reinterpret_cast<int2*>(const_cast<int*>(abort_flag + 4));    // [kPend]
   {
-    constexpr int kS = L::kGroupStages;
-    uint64_t* q_full = reinterpret_cast<uint64_t*>(smem + L::kSuffixBars);  // [2][kQueue]
-    uint64_t* q_empty = q_full + kGroups * kQueue;                           // [2][kQueue]
-    uint64_t* st_full = q_empty + kGroups * kQueue;                          // [2][kS]
-    UnitDesc* queue = reinterpret_cast<UnitDesc*>(st_full + kGroups * kS);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(queue + kGroups * kQueue);
-    volatile int* ready_flag = abort_flag + 1;                               // [2][2]
+    int u_begin, u_end;
+    unit_range(a, u_begin, u_end);
     if (threadIdx.x == 0) {
-      for (int i = 0; i < kGroups * kQueue; ++i) {
-        mbar_init(&q_full[i], 1);
-        mbar_init(&q_empty[i], 1);
+      for (int i = 0; i < kS; ++i) {
+        mbar_init(&st_full[i], 1 + 32);  // the producer's expect_tx + its lanes' copies
+        mbar_init(&st_empty[i], kStreamWarps);
       }
-      for (int i = 0; i < kGroups * kS; ++i) mbar_init(&st_full[i], 128);  // group threads
       *abort_flag = 0;
+      *n_pend = 0;
+      *prefix_ready = 0;
       fence_mbarrier_init();
     }
     __syncthreads();
-    if (warp == kWarpScheduler) {
-      if (lane < kGroups)
-        schedule_lane(a, lane, q_full + lane * kQueue, q_empty + lane * kQueue,
-                      queue + lane * kQueue, abort_flag);
-    } else if (warp < 4 * kGroups) {
-      const int g = warp >> 2;
-      stream_group<D>(a, g, smem + g * L::kGroupBytes, q_full + g * kQueue,
-                      q_empty + g * kQueue, queue + g * kQueue, st_full + g * kS,
-                      ready_flag + 2 * g, abort_flag);
+    if (warp == kWarpWatcher) {
+      // lane 0: wait until every prefix range is written, then post it for the merge
+      // (2: it never was, within the time limit, or the streaming gave up)
+      if (lane == 0 && static_cast<int>(blockIdx.x) < a.prefix_ctas) {
+        // this CTA's range is written (every thread's stores precede the CTA barriers
+        // since): count it, off the streaming warps' path
+        __threadfence();
+        red_release_gpu_add(a.prefix_done, 1);
+      }
+      if (lane == 0 && u_begin < u_end) {
+        int st = 1;
+        const long long c0 = clock64();
+        while (ld_acquire_gpu_s32(a.prefix_done) < a.prefix_ctas) {
+          if (*abort_flag) {
+            st = 2;
+            break;
+          }
+          if (clock64() - c0 > kWaitLimitCycles) {
+            if (p.status) atomicCAS(p.status, 0, kErrTimeout);
+            st = 2;
+            break;
+          }
+          __nanosleep(128);
+        }
+        __threadfence_block();
+        *prefix_ready = st;
+      }
+    } else if (warp == kWarpScheduler) {
+      produce_items<D>(a, &tm_k, &tm_v, smem, st_full, st_empty, idesc, abort_flag);
+    } else {
+      consume_items<D>(a, smem, st_full, st_empty, idesc, pend, n_pend, abort_flag);
     }
   }
 
-  // ---- grid-wide barrier: every partial of the call is written.  The arrival is one
-  // acquire-release add (the CTA barrier before it makes every thread's partial
-  // stores part of what it releases); the last CTA advances the generation, which the
-  // others read at their start (no CTA can advance it before every CTA has arrived).
+  // ---- merge_attn_states for the rows of this CTA's units, once every prefix range
+  // is written.  The rows of the list are numbered in order; pass k gives row
+  // 2 * (warp + 10 k) + h to half warp h of each warp (both halves in step, so a warp
+  // never runs two merges one after the other).
   __syncthreads();
-  if (threadIdx.x == 0) {
-    const int old = atomic_add_acq_rel_gpu(a.bar_count, 1);
-    if (old == static_cast<int>(gridDim.x) - 1) {
-      st_release_gpu_u32(a.bar_gen, g0 + 1u);
-      // nothing reads these again in this call: zero for the next one
-      *a.bar_count = 0;
-      *a.work_counter = 0;
-    } else {
-      const unsigned long long t0 = global_timer_ns();
-      while (ld_acquire_gpu_u32(a.bar_gen) == g0) {
-        if (global_timer_ns() - t0 > kWaitLimitNs) {
-          atomicCAS(p.status, 0, kErrTimeout);
-          break;
+  {
+    const int n_all = *n_pend;
+    if (n_all > 0 && *prefix_ready == 1) {
+      __threadfence_block();
+      constexpr int kWarps = kThreads / 32;
+      int total = 0;
+      for (int e = 0; e < n_all; ++e) total += pend[e].y & 255;
+      const int h = lane >> 4;
+      for (int base = 2 * warp; base < total; base += 2 * kWarps) {
+        // find row base + h: entry e, row rr within it
+        int want = base + h, e = 0, q0 = 0, kvh = 0, rr = -1;
+        for (; e < n_all; ++e) {
+          const int2 en = pend[e];
+          const int rows = en.y & 255;
+          if (want < rows) {
+            q0 = en.x;
+            kvh = en.y >> 8;
+            rr = want;
+            break;
+          }
+          want -= rows;
         }
-        __nanosleep(64);
+        const int qi = rr >= 0 ? rr / p.group : 0, j = rr >= 0 ? rr - qi * p.group : 0;
+        const int64_t row = static_cast<int64_t>(q0 + qi) * p.num_q_heads + kvh * p.group + j;
+        // a half warp past the last row loads nothing and writes nothing
+        merge_slots<D>(p, row, 0, rr >= 0 ? p.n_splits + 1 : 0, lane & 15,
+                       rr >= 0 ? a.out + row * D : nullptr,
+                       (rr >= 0 && a.lse != nullptr) ? a.lse + row : nullptr, true);
       }
     }
   }
-  __syncthreads();
 
-  // ---- merge_attn_states: prefix slots [0, n_splits) and the suffix slot n_splits
-  {
-    const int rows = p.total_q * p.num_q_heads;
-    const int halves = kThreads / 16;
-    for (int row = blockIdx.x * halves + (threadIdx.x >> 4); row < rows;
-         row += gridDim.x * halves)
-      merge_row_half<D>(a, row, p.n_splits + 1, threadIdx.x & 15);
+  // ---- the last CTA to finish zeroes the counters for the next call (every CTA's
+  // reads of prefix_done precede its count)
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    if (atomicAdd(a.exit_count, 1) == static_cast<int>(gridDim.x) - 1) {
+      *a.prefix_done = 0;
+      *a.exit_count = 0;
+    }
   }
 }
 
@@ -656,7 +713,7 @@ cudaError_t launch_decode_d(const CUtensorMap& tm_q, const CUtensorMap& tm_k,
   cfg.dynamicSmemBytes = SLayout<D>::kDynamic;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
-  // every CTA must be resident: the grid-wide barrier waits for all of them
+  // every CTA must be resident: suffix CTAs wait for the prefix CTAs' results
   attr[0].id = cudaLaunchAttributeCooperative;
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;

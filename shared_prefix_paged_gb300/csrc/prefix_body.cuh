@@ -101,8 +101,7 @@ __device__ __forceinline__ void prefix_range(const CUtensorMap* tm_q_p,
   uint64_t* kv_empty = bars + 1 + kStages;  // [kStages]
   uint64_t* s_full = bars + 1 + 2 * kStages;    // [2 tiles][2 buffers]
   uint64_t* p_full = bars + 5 + 2 * kStages;    // [2 tiles][2 buffers]
-  uint64_t* o_done = bars + 9 + 2 * kStages;    // [2 tiles] every PV
-  uint64_t* o_last = bars + 11 + 2 * kStages;   // [2 tiles] the last PV
+  uint64_t* o_last = bars + 11 + 2 * kStages;   // [2 tiles] the last PV (9, 10 unused)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 13 + 2 * kStages);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 14 + 2 * kStages);
 
@@ -130,10 +129,7 @@ __device__ __forceinline__ void prefix_range(const CUtensorMap* tm_q_p,
       mbar_init(&s_full[b], 1);
       mbar_init(&p_full[b], 128);
     }
-    for (int m = 0; m < 2; ++m) {
-      mbar_init(&o_done[m], 1);
-      mbar_init(&o_last[m], 1);
-    }
+    for (int m = 0; m < 2; ++m) mbar_init(&o_last[m], 1);
     *abort_flag = 0;
     fence_mbarrier_init();
   }
@@ -210,7 +206,6 @@ __device__ __forceinline__ void prefix_range(const CUtensorMap* tm_q_p,
           umma_bf16_tmem_a(tm + 2 * kKeysN, p_tmem + kk * 8,
                            umma_desc_sw128(v_addr + kk * 16 * 128, L::kKVHalf, 1024), kIdO,
                            (i > 0 || kk > 0) ? 1u : 0u);
-        umma_commit(&o_done[m]);
         if (i == ntiles - 1) umma_commit(&o_last[m]);
         umma_commit(&kv_empty[i % kStages]);
         ++next_pv;
@@ -247,7 +242,8 @@ __device__ __forceinline__ void prefix_range(const CUtensorMap* tm_q_p,
     // ---- K/V loads: the 256 threads of warps 0-7 issue 16-byte cp.async into the
     // 128-byte-swizzled stages (the layout the MMA descriptors expect); each thread's
     // arrival on the stage's full barrier fires once its copies have landed.  Tile
-    // i + kStages - 1 goes into the stage of tile i - 1 as soon as PV(i - 1) is done.
+    // i + kStages - 1 goes into the stage of tile i - 1 once PV(i - 1) is done and
+    // the thread's warp has handed P(i) over.
     constexpr int kChunks = D / 8;
     constexpr int kPer = kKeysN * kChunks / kLoaders;
     const int lt = threadIdx.x;  // loader thread
@@ -294,25 +290,13 @@ __device__ __forceinline__ void prefix_range(const CUtensorMap* tm_q_p,
     };
     for (int j = 0; j < ntiles && j < kStages; ++j) issue_tile(j);
 
-    bool failed = false;
-    for (int i = 0; i < ntiles; ++i) {
-      if (i >= 1 && i + kStages - 1 < ntiles) {
-        const bool ok = warp_mbar_wait(&kv_empty[(i - 1) % kStages], ((i - 1) / kStages) & 1,
-                                       abort_flag, a.status);
-        if (wg_bar_any(1 + wg, !ok)) {
-          failed = true;
-          break;
-        }
-        issue_tile(i + kStages - 1);
-      }
-      if (!softmax_warp) continue;
+    // one tile of the online softmax: S(i) from TMEM -> P(i) back into TMEM (bf16)
+    auto softmax_tile = [&](int i) -> bool {
       const int tile = tile_of(i);
+
       const bool ok =
           warp_mbar_wait(&s_full[wg * 2 + (i & 1)], (i >> 1) & 1, abort_flag, a.status);
-      if (wg_bar_any(1 + wg, !ok)) {
-        failed = true;
-        break;
-      }
+      if (wg_bar_any(1 + wg, !ok)) return false;
       tc_fence_after();
       float sv[kKeysN];
       tmem_ld64_sync(t_lane + (i & 1) * kKeysN, sv);
@@ -342,9 +326,12 @@ __device__ __forceinline__ void prefix_range(const CUtensorMap* tm_q_p,
         m_run = m_new;
       }
       if (i > 0 && __any_sync(0xffffffffu, grow)) {
-        // O must hold PV(i-1) before it is rescaled (the phase is unambiguous: PV(i)
-        // cannot complete before this thread has written P(i))
-        warp_mbar_wait(&o_done[wg], (i - 1) & 1, abort_flag, a.status);
+        // O must hold PV(i-1) before it is rescaled.  Stage (i-1) % kStages is freed
+        // once every M tile's PV(i-1) is done; its phase is unambiguous: the stage's
+        // previous tile (i-1-kStages) was freed before tile i-1 was loaded into it,
+        // and its next tile's PV cannot complete before this thread writes P(i).
+        warp_mbar_wait(&kv_empty[(i - 1) % kStages], ((i - 1) / kStages) & 1, abort_flag,
+                       a.status);
         tc_fence_after();
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
@@ -371,10 +358,30 @@ __device__ __forceinline__ void prefix_range(const CUtensorMap* tm_q_p,
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(&p_full[wg * 2 + (i & 1)]);
+      return true;
+    };
+
+    bool failed = false;
+    for (int i = 0; i < ntiles; ++i) {
+      if (softmax_warp) {
+        if (!softmax_tile(i)) {
+          failed = true;
+          break;
+        }
+      }
+      // refill after the softmax, so that waiting for PV(i - 1) never delays S(i)
+      if (i >= 1 && i + kStages - 1 < ntiles) {
+        const bool ok = warp_mbar_wait(&kv_empty[(i - 1) % kStages], ((i - 1) / kStages) & 1,
+                                       abort_flag, a.status);
+        if (wg_bar_any(1 + wg, !ok)) {
+          failed = true;
+          break;
+        }
+        issue_tile(i + kStages - 1);
+      }
     }
     if (softmax_warp && !failed && ntiles > 0) {
-      // o_done's parity alone cannot tell PV(ntiles-1) from PV(ntiles-2), which may
-      // still be running: o_last completes once, after every PV of the range
+      // o_last completes once, after every PV of the range
       const bool ok = warp_mbar_wait(&o_last[wg], 0, abort_flag, a.status);
       have = !wg_bar_any(1 + wg, !ok);
     }
@@ -383,7 +390,7 @@ __device__ __forceinline__ void prefix_range(const CUtensorMap* tm_q_p,
   }
 
   // ----------------------------------------- this split's partial -> slot --
-  // every MMA of the CTA is complete once both warpgroups saw their last o_done
+  // every MMA of the CTA is complete once both warpgroups saw their o_last
   // (or have nothing to do): Q and the ring become the staging buffer
   __syncthreads();
   __nv_bfloat16* stage = reinterpret_cast<__nv_bfloat16*>(smem);
