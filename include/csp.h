@@ -81,9 +81,7 @@ typedef enum {
   CSP_ERR_UNSUPPORTED = -2,  /* head_dim / block_size / group size not built       */
   CSP_ERR_WORKSPACE = -3,    /* workspace missing, too small or misaligned          */
   CSP_ERR_CUDA = -4,         /* a CUDA call or launch failed                        */
-  CSP_ERR_TIMEOUT = -6,      /* device-side: a bounded wait inside a kernel gave up */
-  CSP_ERR_INTERNAL = -7      /* device-side: a kernel's bookkeeping limit was
-                                exceeded (a bug in the planner, never the input)    */
+  CSP_ERR_TIMEOUT = -6       /* device-side: a bounded wait inside a kernel gave up */
 } csp_status;
 
 /* cascade_plan modes. */

@@ -23,7 +23,6 @@ CSP_ERR_UNSUPPORTED = -2
 CSP_ERR_WORKSPACE = -3
 CSP_ERR_CUDA = -4
 CSP_ERR_TIMEOUT = -6
-CSP_ERR_INTERNAL = -7
 
 MODE_AUTO, MODE_FORCE_CASCADE, MODE_FORCE_FLAT, MODE_PAGE_THRESHOLDS = 0, 1, 2, 3
 SCHEDULE_TWO_KERNELS, SCHEDULE_SINGLE = 0, 1

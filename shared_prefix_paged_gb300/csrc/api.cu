@@ -21,12 +21,11 @@ int cuda_fail(cudaError_t e) {
 }
 
 constexpr int kPage = 16;
-// Workspace header: [0] status word; counters of the single-kernel decode schedule,
-// which that kernel leaves at zero when it exits: [64] written prefix ranges, [128]
-// finished CTAs.
+// Workspace header: [0] status word; the grid barrier of the single-kernel decode
+// schedule: [64] its count (that kernel leaves it at zero) and [128] its generation.
 constexpr size_t kHeaderBytes = 256;
-constexpr size_t kOffPrefixDone = 64;
-constexpr size_t kOffExitCount = 128;
+constexpr size_t kOffBarCount = 64;
+constexpr size_t kOffBarGen = 128;
 // Most packed rows (query, head-in-group) per request and KV head that the decode
 // schedule takes: one warp-level MMA tile.
 constexpr int kDecodeRows = 16;
@@ -165,20 +164,21 @@ void make_plan(int num_reqs, int total_q, int max_q, int max_k, int cpl, int Hq,
 
   // Decode-like batches (a request's rows of one KV head fit one 16-row MMA tile):
   // one cooperative kernel.  d_base * s CTAs each run a prefix range and then stream
-  // k suffix units; the other CTAs stream the rest of the suffix units from the start.
-  // s and k come from a cost model measured on GB300 (per CTA, in us): ~3 until the
-  // first bytes land; a prefix 64-key tile at the CTA's load rate (~33 GB/s per SM) or
-  // ~1.1 per 256 rows (tensor core and softmax), whichever is slower; ~3 to write the
-  // range's partial; a suffix unit's K/V bytes (its longest request) at ~33 GB/s.
-  // Both kinds of CTA should finish together.
+  // k suffix units; the other CTAs stream the rest of the suffix units from the
+  // start.  s and k come from a cost model measured on
+  // GB300 (per CTA, in us): a CTA moves ~31 GB/s of K/V (the per-SM copy rate); the
+  // prefix's first tile lands at ~3.5 and the
+  // suffix's first item at ~5.3; a prefix 64-key tile takes its bytes' time or ~1.1
+  // per 256 rows (tensor core and softmax), whichever is longer; writing a range's
+  // partial takes ~2.5.  Both kinds of CTA should finish together.
   const int d_base = p.p_pairs * Hkv;
   if (cpl > 0 && static_cast<int64_t>(max_q) * p.group <= kDecodeRows && d_base <= sms) {
     const int pre_tiles = cdiv(cpl, 64);
-    const double kRate = 33e3;  // bytes per us per SM
+    const double kRate = 31e3;  // bytes per us per SM
     const double pair_rows = std::min(256.0, static_cast<double>(total_q) * p.group);
     const double tile_us = std::max(64.0 * 4.0 * D / kRate, 1.1 * pair_rows / 256.0);
     const double unit_us =
-        std::max(1, cdiv(max_len, 64)) * 64.0 * 4.0 * D / kRate;  // K and V, bf16
+        (std::max(1, cdiv(max_len, 64)) * 64.0 * 4.0 * D + max_q * p.group * D * 2.0) / kRate;
     const int64_t units = static_cast<int64_t>(num_reqs) * Hkv;
     const int s_max = std::max(1, std::min({pre_tiles, csp::kDecodeMaxParts - 1, sms / d_base}));
     int s = 0, k = 0;
@@ -186,13 +186,14 @@ void make_plan(int num_reqs, int total_q, int max_q, int max_k, int cpl, int Hq,
     for (int c = 1; c <= s_max; ++c) {
       const int64_t pc = static_cast<int64_t>(d_base) * c;  // prefix CTAs
       const int64_t nc = sms - pc;                            // suffix-only CTAs
-      const double pre_us = 3.0 + cdiv(pre_tiles, c) * tile_us + 3.0;
+      const double pre_us = 3.5 + cdiv(pre_tiles, c) * tile_us + 2.5;
       const int64_t k_lo = nc > 0 ? 0 : cdiv64(units, pc);
       for (int64_t kk = k_lo; kk <= cdiv64(units, pc); ++kk) {
         const int64_t rest = std::max<int64_t>(0, units - pc * kk);
         const int64_t per = nc > 0 ? cdiv64(rest, nc) : 0;
-        if (std::max(kk, per) > csp::kDecodeMaxUnitsPerCta) continue;
-        const double t = std::max(pre_us + kk * unit_us, 3.0 + per * unit_us);
+        // a prefix CTA's first suffix item lands ~3.5 after its range is written
+        const double t =
+            std::max(pre_us + (kk > 0 ? 3.5 : 0.0) + kk * unit_us, 5.3 + per * unit_us);
         if (best < 0.0 || t < best) {
           best = t;
           s = c;
@@ -210,8 +211,9 @@ void make_plan(int num_reqs, int total_q, int max_q, int max_k, int cpl, int Hq,
       // slots: [0, s) the prefix ranges, s the suffix
       p.d_off_o = kHeaderBytes;
       p.d_off_lse = p.d_off_o + align256(static_cast<size_t>(s + 1) * rows_total * D * 2);
-      p.bytes = std::max(p.bytes,
-                         p.d_off_lse + align256(static_cast<size_t>(s + 1) * rows_total * 4));
+      // (+256: the merge reads each slot's LSE run rounded out to 16 bytes)
+      p.bytes = std::max(p.bytes, p.d_off_lse +
+                                      align256(static_cast<size_t>(s + 1) * rows_total * 4) + 256);
     }
   }
   *P = p;
@@ -296,8 +298,8 @@ int attention_call(const void* q, const void* k_cache, const void* v_cache, int3
     da.prefix_ctas = P.d_prefix_ctas;
     da.prefix_units = P.d_prefix_units;
     da.key_tiles = cdiv(cpl, 64);
-    da.prefix_done = reinterpret_cast<int*>(ws + kOffPrefixDone);
-    da.exit_count = reinterpret_cast<int*>(ws + kOffExitCount);
+    da.bar_count = reinterpret_cast<int*>(ws + kOffBarCount);
+    da.bar_gen = reinterpret_cast<unsigned*>(ws + kOffBarGen);
     da.out = static_cast<__nv_bfloat16*>(out);
     da.lse = lse;
     // phase events: [0] before the kernel, [1..3] after it

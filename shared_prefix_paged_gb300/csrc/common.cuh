@@ -18,7 +18,6 @@
 namespace csp {
 
 constexpr int kErrTimeout = -6;
-constexpr int kErrInternal = -7;  // a kernel's bookkeeping limit was exceeded (a bug)
 // Upper bound of any single wait inside a kernel (nanoseconds).
 constexpr unsigned long long kWaitLimitNs = 1000000000ull;
 // The same bound in SM clock cycles (about one second at 2 GHz).
@@ -125,6 +124,16 @@ __device__ __forceinline__ void tma_load_3d(void* smem_dst, const CUtensorMap* m
       "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
       " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_u32(smem_dst)),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+
+// 1-D bulk copy global -> shared, completion counted on `bar`: both addresses 16-byte
+// aligned, `bytes` a multiple of 16.
+__device__ __forceinline__ void bulk_load(void* smem_dst, const void* src, uint32_t bytes,
+                                          uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+      ::"r"(smem_u32(smem_dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar))
       : "memory");
 }
 

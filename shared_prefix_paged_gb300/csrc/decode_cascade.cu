@@ -11,22 +11,19 @@
 // only while every SM streams.  So the SMs share the work inside one grid of one CTA
 // per SM (a cooperative launch, so every CTA is resident):
 //  * CTAs [0, prefix_ctas) each first run one range of the prefix on tcgen05 tensor
-//    cores (prefix_range, prefix_body.cuh), write a partial into slot `split` and
-//    count it in prefix_done; then, like every other CTA, they stream suffix units;
+//    cores (prefix_range, prefix_body.cuh) and write a partial into slot `split`;
+//    then, like every other CTA, they stream suffix units;
 //  * a suffix unit is one (request, KV head): all its rows (at most 16 packed
 //    (query, head-in-group) rows) in one warp-level MMA tile.  Each prefix CTA takes
 //    prefix_units of them, the other CTAs share the rest evenly; the host picks the
 //    number of prefix ranges and prefix_units so that every CTA ends together;
-//  * merge_attn_states without a grid-wide barrier: a CTA lists its finished units
-//    and, once prefix_done is complete, merges their rows (prefix slots plus the
-//    suffix slot, by LSE rescaling) into bf16 out and the natural-log LSE.
+//  * a grid-wide barrier, then every CTA merges an equal share of the rows (prefix
+//    slots plus the suffix slot, by LSE rescaling) into bf16 out and the natural-log
+//    LSE: one round trip to L2 per row, spread over every SM.
 //
-// Suffix streaming within a CTA (stream_units): lane 0 of warp 8 walks the CTA's
-// units, resolves their request metadata and first block ids ahead of use, and queues
-// them in shared memory; warps 0-7 load two 64-key tiles of a unit at a time with
-// 16-byte cp.async into 128-byte-swizzled stages (on GB300 this path keeps more bytes
-// in flight per SM than TMA page boxes do), two such pairs ahead of the one they
-// compute, and each warp computes 16 keys of one tile on mma.sync.
+// Suffix streaming within a CTA: warp 8 produces ring items (two 64-key tiles of a
+// unit, loaded by TMA) and warps 0-7 compute them on mma.sync (see produce_items and
+// consume_items).
 #include <type_traits>
 
 #include "merge.cuh"
@@ -43,8 +40,9 @@ constexpr int kRows = 16;                   // packed rows of a suffix unit (one
 constexpr int kStreamWarps = 8;             // warps 0-7 stream the suffix
 constexpr int kStreamThreads = 32 * kStreamWarps;
 constexpr int kWarpScheduler = 8;           // produces the suffix items
-constexpr int kPend = kDecodeMaxUnitsPerCta;  // finished units awaiting their merge
-constexpr int kWarpWatcher = 9;             // lane 0 waits for every prefix range
+constexpr int kMergeBarOff = 512;           // merge barrier within the suffix barrier area
+constexpr int kMergeBytes = 200 * 1024;     // shared memory the staged merge may use
+constexpr int kChunkRows = 256;             // most rows merged per chunk
 
 static_assert(kThreads == 320, "ten warps: 8 softmax/streaming, MMA/scheduler, TMA");
 
@@ -64,12 +62,11 @@ struct SLayout {
   static constexpr int kData = kSlots * kItem > kPrefixData ? kSlots * kItem : kPrefixData;
   static constexpr int kPrefixBars = kData;                        // prefix::kBarBytes
   static constexpr int kSuffixBars = kPrefixBars + prefix::kBarBytes;
-  static constexpr int kSuffixBarBytes = 2048;
+  static constexpr int kSuffixBarBytes = 1024;
   static constexpr int kDynamic = kSuffixBars + kSuffixBarBytes + 1024;  // + align slack
   static_assert(kSlots >= 3, "two items in flight ahead of the computed one");
   static_assert(kStage % 1024 == 0 && (2 * kKV) % 1024 == 0, "swizzled stage alignment");
-  static_assert(2 * kSlots * 8 + kSlots * 32 + 16 + kPend * 8 <= kSuffixBarBytes,
-                "suffix barrier area");
+  static_assert(2 * kSlots * 8 + kSlots * 32 + 16 <= kSuffixBarBytes, "suffix barrier area");
   static_assert(kDynamic <= 227 * 1024, "one CTA per SM");
 };
 
@@ -81,101 +78,19 @@ __device__ __forceinline__ uint32_t sw128(int row, int c) {
                                (((c & 7) ^ (row & 7)) << 4));
 }
 
-__device__ __forceinline__ int ld_acquire_gpu_s32(const int* p) {
-  int v;
-  asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+__device__ __forceinline__ unsigned ld_acquire_gpu_u32(const unsigned* p) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
   return v;
 }
 
-__device__ __forceinline__ void red_release_gpu_add(int* p, int v) {
-  asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+__device__ __forceinline__ void st_release_gpu_u32(unsigned* p, unsigned v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
 // the eight streaming warps (named barrier 1)
 __device__ __forceinline__ void stream_sync() {
   asm volatile("bar.sync 1, %0;" ::"r"(kStreamThreads) : "memory");
-}
-
-// -------------------------------------------------------------------- merge --
-// Loads from L2 whose order the compiler keeps: every slot of a row is requested
-// before the first result is used, so a row costs one round trip.  A false `pred`
-// leaves the destination zero without a read.
-__device__ __forceinline__ void ld_cg_pred(uint4& v, const void* ptr, bool pred) {
-  v = make_uint4(0u, 0u, 0u, 0u);
-  asm volatile(
-      "{\n .reg .pred q;\n setp.ne.b32 q, %5, 0;\n"
-      " @q ld.global.cg.v4.u32 {%0, %1, %2, %3}, [%4];\n}\n"
-      : "+r"(v.x), "+r"(v.y), "+r"(v.z), "+r"(v.w)
-      : "l"(ptr), "r"(pred ? 1 : 0));
-}
-__device__ __forceinline__ void ld_cg_pred(uint2& v, const void* ptr, bool pred) {
-  v = make_uint2(0u, 0u);
-  asm volatile(
-      "{\n .reg .pred q;\n setp.ne.b32 q, %3, 0;\n @q ld.global.cg.v2.u32 {%0, %1}, [%2];\n}\n"
-      : "+r"(v.x), "+r"(v.y)
-      : "l"(ptr), "r"(pred ? 1 : 0));
-}
-__device__ __forceinline__ float ld_cg_pred_f32(const float* ptr, bool pred, float fill) {
-  float v = fill;
-  asm volatile(
-      "{\n .reg .pred q;\n setp.ne.b32 q, %2, 0;\n @q ld.global.cg.f32 %0, [%1];\n}\n"
-      : "+f"(v)
-      : "l"(ptr), "r"(pred ? 1 : 0));
-  return v;
-}
-
-// merge_attn_states for one row with 16 lanes (a half warp): workspace slots
-// [first, first + n), n <= 16, into dst_o (bf16) and *dst_lse (log2 domain, or the
-// natural-log LSE with `natural`); a null destination is not written.  Lane i holds the weight of
-// slot first + i and features [i*D/16, (i+1)*D/16).  An empty slot (lse -inf) gets
-// weight 0 and whatever it holds never mixes in.
-template <int D>
-__device__ __forceinline__ void merge_slots(const PrefixArgs& p, int64_t row, int first,
-                                            int n, int hl, __nv_bfloat16* dst_o,
-                                            float* dst_lse, bool natural) {
-  constexpr int kF = D / 16;  // features per lane: 8 (16 bytes) or 4 (8 bytes)
-  constexpr int kMax = 16;
-  using Vec = typename std::conditional<kF == 8, uint4, uint2>::type;
-  const int64_t rows = static_cast<int64_t>(p.total_q) * p.num_q_heads;
-  Vec v[kMax];
-  const __nv_bfloat16* base = p.part_o + (first * rows + row) * D + hl * kF;
-#pragma unroll
-  for (int s = 0; s < kMax; ++s) ld_cg_pred(v[s], base + s * rows * D, s < n);
-  const float lw = ld_cg_pred_f32(p.part_lse + (first + hl) * rows + row, hl < n, -INFINITY);
-  const unsigned mask = 0xffffu << (threadIdx.x & 16);
-  float mx = lw;
-#pragma unroll
-  for (int o = 8; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(mask, mx, o, 16));
-  const float w = (mx == -INFINITY || lw == -INFINITY) ? 0.f : fast_exp2(lw - mx);
-  float wsum = w;
-#pragma unroll
-  for (int o = 8; o > 0; o >>= 1) wsum += __shfl_xor_sync(mask, wsum, o, 16);
-  const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
-  float acc[kF];
-#pragma unroll
-  for (int f = 0; f < kF; ++f) acc[f] = 0.f;
-#pragma unroll
-  for (int s = 0; s < kMax; ++s) {
-    const float ws = __shfl_sync(mask, w, s, 16) * inv;
-    if (s < n && ws != 0.f) {
-      const uint32_t* u = reinterpret_cast<const uint32_t*>(&v[s]);
-#pragma unroll
-      for (int f = 0; f < kF / 2; ++f) {
-        const float2 x = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u[f]));
-        acc[2 * f] = fmaf(ws, x.x, acc[2 * f]);
-        acc[2 * f + 1] = fmaf(ws, x.y, acc[2 * f + 1]);
-      }
-    }
-  }
-  Vec o;
-  uint32_t* ou = reinterpret_cast<uint32_t*>(&o);
-#pragma unroll
-  for (int f = 0; f < kF / 2; ++f) ou[f] = pack_bf16x2(acc[2 * f], acc[2 * f + 1]);
-  if (dst_o != nullptr) *reinterpret_cast<Vec*>(dst_o + hl * kF) = o;
-  if (hl == 0 && dst_lse != nullptr) {
-    const float l2 = wsum > 0.f ? mx + log2f(wsum) : -INFINITY;
-    *dst_lse = natural ? l2 * 0.69314718055994531f : l2;
-  }
 }
 
 // ------------------------------------------------------------------ streaming --
@@ -196,8 +111,7 @@ __device__ __forceinline__ void merge_slots(const PrefixArgs& p, int64_t row, in
 //    request's causal limit (bottom-right alignment, §四), online softmax in base 2.
 //    V rows past the request are zeroed first (a TMA page holds whatever the cache
 //    has there).  At the unit's end the eight warps merge through the item's memory
-//    and write the normalised bf16 rows and their log2-sum-exp into the suffix slot;
-//    the unit then waits in `pend` for its rows' final merge.
+//    and write the normalised bf16 rows and their log2-sum-exp into the suffix slot.
 // Loads never hold up the computing warps: the producer alone waits for free slots.
 struct ItemDesc {
   int q0, q_len, seq_len, kvh, ntiles, t0, pad0, pad1;  // ntiles < 0: no more items
@@ -338,8 +252,7 @@ __device__ __forceinline__ void produce_items(const DecodeArgs& a, const CUtenso
 template <int D>
 __device__ __forceinline__ void consume_items(const DecodeArgs& a, uint8_t* ring,
                                               uint64_t* st_full, uint64_t* st_empty,
-                                              const ItemDesc* idesc, int2* pend,
-                                              volatile int* n_pend, volatile int* abort_flag) {
+                                              const ItemDesc* idesc, volatile int* abort_flag) {
   using L = SLayout<D>;
   constexpr int kS = L::kSlots;
   constexpr int kChunks = D / 8;          // 16-byte chunks per row
@@ -545,22 +458,107 @@ __device__ __forceinline__ void consume_items(const DecodeArgs& a, uint8_t* ring
         }
         if (lane == 0) p.part_lse[prow] = lsum > 0.f ? mg + log2f(lsum) : -INFINITY;
       }
-      // the unit waits for its merge at the end of the kernel
-      if (tid == 0) {
-        const int n = *n_pend;
-        if (n < kPend) {
-          pend[n] = make_int2(c_q0, (c_kvh << 8) | rows_valid);
-          *n_pend = n + 1;
-        } else {
-          atomicCAS(p.status, 0, kErrInternal);  // the host keeps units per CTA <= kPend
-        }
-      }
     }
     // the item goes back to the producer (its TMA will overwrite what this warp
     // wrote through the generic proxy)
     fence_proxy_async_smem();
     __syncwarp();
     if (lane == 0) mbar_arrive(&st_empty[slot]);
+  }
+}
+
+// ------------------------------------------------------------ staged merge --
+// merge_attn_states for rows [b R / G, (b + 1) R / G) of CTA b, in chunks of up to
+// kChunkRows rows: thread 0 copies each slot's chunk of bf16 rows (contiguous, 16-byte
+// aligned) and of LSEs (the run rounded out to 16-byte boundaries; the workspace has
+// room past its end) into shared memory with bulk async copies completing on `bar`;
+// then half a warp merges each row (lane i: the weight of slot i and features
+// [i*D/16, (i+1)*D/16)).  An empty slot (lse -inf) gets weight 0.
+template <int D>
+__device__ __forceinline__ void merge_rows_staged(const DecodeArgs& a, uint8_t* smem,
+                                                  uint64_t* bar, volatile int* abort_flag) {
+  constexpr int kF = D / 16;
+  using Vec = typename std::conditional<kF == 8, uint4, uint2>::type;
+  const PrefixArgs& p = a.pre;
+  const int n = p.n_splits + 1;  // slots
+  const int64_t rows = static_cast<int64_t>(p.total_q) * p.num_q_heads;
+  const int64_t r0 = static_cast<int64_t>(blockIdx.x) * rows / gridDim.x;
+  const int64_t r1 = static_cast<int64_t>(blockIdx.x + 1) * rows / gridDim.x;
+  // rows per chunk: n slots of bf16 rows plus n LSE runs (each up to 8 floats longer)
+  const int chunk = min(kChunkRows, (kMergeBytes / n - 64) / (D * 2 + 4));
+  const int o_bytes_row = D * 2;
+  const int lse_stride = (chunk + 6 + 3) & ~3;  // floats per slot's LSE run
+  __nv_bfloat16* s_o = reinterpret_cast<__nv_bfloat16*>(smem);
+  float* s_l = reinterpret_cast<float*>(smem + static_cast<size_t>(n) * chunk * o_bytes_row);
+  const int hw = threadIdx.x >> 4, hl = threadIdx.x & 15;
+  const unsigned mask = 0xffffu << (threadIdx.x & 16);
+  uint32_t phase = 0;
+  for (int64_t c0 = r0; c0 < r1; c0 += chunk, phase ^= 1u) {
+    const int m = static_cast<int>(min(static_cast<int64_t>(chunk), r1 - c0));
+    if (threadIdx.x == 0) {
+      const uint32_t ob = static_cast<uint32_t>(m) * o_bytes_row;
+      uint32_t total = 0;
+      for (int s = 0; s < n; ++s) {
+        const int64_t g = s * rows + c0;  // the run's first LSE, 16-byte aligned both ends
+        total += ob + static_cast<uint32_t>(((g + m + 3) & ~int64_t{3}) - (g & ~int64_t{3})) * 4;
+      }
+      mbar_arrive_expect_tx(bar, total);
+      // the partials were written by other CTAs through the generic proxy; the copies
+      // read them through the async proxy
+      asm volatile("fence.proxy.async.global;" ::: "memory");
+      for (int s = 0; s < n; ++s) {
+        const int64_t g = s * rows + c0;
+        const int64_t g0 = g & ~int64_t{3}, g1 = (g + m + 3) & ~int64_t{3};
+        bulk_load(s_o + static_cast<size_t>(s) * chunk * D, p.part_o + g * D, ob, bar);
+        bulk_load(s_l + s * lse_stride, p.part_lse + g0, static_cast<uint32_t>(g1 - g0) * 4, bar);
+      }
+    }
+    const bool ok = mbar_wait(bar, phase, abort_flag, p.status);
+    // lane hl's slot: where the chunk's first row sits in that slot's LSE run
+    const int lo = static_cast<int>((hl * rows + c0) & 3);
+    // both halves of a warp in step
+    for (int base = 2 * (hw >> 1); base < m; base += kThreads / 16) {
+      const int i = base + (hw & 1);
+      const bool in = ok && i < m;
+      const float lw = (in && hl < n) ? s_l[hl * lse_stride + lo + i] : -INFINITY;
+      float mx = lw;
+#pragma unroll
+      for (int o = 8; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(mask, mx, o, 16));
+      const float w = (mx == -INFINITY || lw == -INFINITY) ? 0.f : fast_exp2(lw - mx);
+      float wsum = w;
+#pragma unroll
+      for (int o = 8; o > 0; o >>= 1) wsum += __shfl_xor_sync(mask, wsum, o, 16);
+      const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+      float acc[kF];
+#pragma unroll
+      for (int f = 0; f < kF; ++f) acc[f] = 0.f;
+      for (int s = 0; s < n; ++s) {
+        const float ws = __shfl_sync(mask, w, s, 16) * inv;
+        if (in && ws != 0.f) {
+          const Vec v = *reinterpret_cast<const Vec*>(s_o + (static_cast<size_t>(s) * chunk + i) * D +
+                                                     hl * kF);
+          const uint32_t* u = reinterpret_cast<const uint32_t*>(&v);
+#pragma unroll
+          for (int f = 0; f < kF / 2; ++f) {
+            const float2 x = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u[f]));
+            acc[2 * f] = fmaf(ws, x.x, acc[2 * f]);
+            acc[2 * f + 1] = fmaf(ws, x.y, acc[2 * f + 1]);
+          }
+        }
+      }
+      if (in) {
+        const int64_t row = c0 + i;
+        Vec o;
+        uint32_t* ou = reinterpret_cast<uint32_t*>(&o);
+#pragma unroll
+        for (int f = 0; f < kF / 2; ++f) ou[f] = pack_bf16x2(acc[2 * f], acc[2 * f + 1]);
+        *reinterpret_cast<Vec*>(a.out + row * D + hl * kF) = o;
+        if (hl == 0 && a.lse != nullptr)
+          a.lse[row] = wsum > 0.f ? (mx + log2f(wsum)) * 0.69314718055994531f : -INFINITY;
+      }
+    }
+    // the next chunk's copies overwrite what was read here
+    __syncthreads();
   }
 }
 
@@ -577,6 +575,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const PrefixArgs& p = a.pre;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  // generation of the grid barrier at the end (read now, off the critical path)
+  const unsigned g0 = threadIdx.x == 0 ? ld_acquire_gpu_u32(a.bar_gen) : 0u;
 
   // ---- role 1: one range of the prefix phase (tcgen05)
   if (static_cast<int>(blockIdx.x) < a.prefix_ctas) {
@@ -600,104 +600,58 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* st_empty = st_full + kS;                                        // [kS]
   ItemDesc* idesc = reinterpret_cast<ItemDesc*>(st_empty + kS);              // [kS]
   volatile int* abort_flag = reinterpret_cast<volatile int*>(idesc + kS);
-  volatile int* n_pend = abort_flag + 1;
-  volatile int* prefix_ready = abort_flag + 2;
-  int2* pend = reinterpret_cast<int2*>(const_cast<int*>(abort_flag + 4));    // [kPend]
-  {
-    int u_begin, u_end;
-    unit_range(a, u_begin, u_end);
-    if (threadIdx.x == 0) {
-      for (int i = 0; i < kS; ++i) {
-        mbar_init(&st_full[i], 1 + 32);  // the producer's expect_tx + its lanes' copies
-        mbar_init(&st_empty[i], kStreamWarps);
-      }
-      *abort_flag = 0;
-      *n_pend = 0;
-      *prefix_ready = 0;
-      fence_mbarrier_init();
+  uint64_t* merge_bar = reinterpret_cast<uint64_t*>(smem + L::kSuffixBars + kMergeBarOff);
+  int u_begin, u_end;
+  unit_range(a, u_begin, u_end);
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kS; ++i) {
+      mbar_init(&st_full[i], 1 + 32);  // the producer's expect_tx + its lanes' copies
+      mbar_init(&st_empty[i], kStreamWarps);
     }
-    __syncthreads();
-    if (warp == kWarpWatcher) {
-      // lane 0: wait until every prefix range is written, then post it for the merge
-      // (2: it never was, within the time limit, or the streaming gave up)
-      if (lane == 0 && static_cast<int>(blockIdx.x) < a.prefix_ctas) {
-        // this CTA's range is written (every thread's stores precede the CTA barriers
-        // since): count it, off the streaming warps' path
-        __threadfence();
-        red_release_gpu_add(a.prefix_done, 1);
-      }
-      if (lane == 0 && u_begin < u_end) {
-        int st = 1;
-        const long long c0 = clock64();
-        while (ld_acquire_gpu_s32(a.prefix_done) < a.prefix_ctas) {
-          if (*abort_flag) {
-            st = 2;
-            break;
-          }
-          if (clock64() - c0 > kWaitLimitCycles) {
-            if (p.status) atomicCAS(p.status, 0, kErrTimeout);
-            st = 2;
-            break;
-          }
-          __nanosleep(128);
-        }
-        __threadfence_block();
-        *prefix_ready = st;
-      }
-    } else if (warp == kWarpScheduler) {
-      produce_items<D>(a, &tm_k, &tm_v, smem, st_full, st_empty, idesc, abort_flag);
-    } else {
-      consume_items<D>(a, smem, st_full, st_empty, idesc, pend, n_pend, abort_flag);
-    }
+    mbar_init(merge_bar, 1);
+    *abort_flag = 0;
+    fence_mbarrier_init();
   }
-
-  // ---- merge_attn_states for the rows of this CTA's units, once every prefix range
-  // is written.  The rows of the list are numbered in order; pass k gives row
-  // 2 * (warp + 10 k) + h to half warp h of each warp (both halves in step, so a warp
-  // never runs two merges one after the other).
   __syncthreads();
-  {
-    const int n_all = *n_pend;
-    if (n_all > 0 && *prefix_ready == 1) {
-      __threadfence_block();
-      constexpr int kWarps = kThreads / 32;
-      int total = 0;
-      for (int e = 0; e < n_all; ++e) total += pend[e].y & 255;
-      const int h = lane >> 4;
-      for (int base = 2 * warp; base < total; base += 2 * kWarps) {
-        // find row base + h: entry e, row rr within it
-        int want = base + h, e = 0, q0 = 0, kvh = 0, rr = -1;
-        for (; e < n_all; ++e) {
-          const int2 en = pend[e];
-          const int rows = en.y & 255;
-          if (want < rows) {
-            q0 = en.x;
-            kvh = en.y >> 8;
-            rr = want;
-            break;
-          }
-          want -= rows;
-        }
-        const int qi = rr >= 0 ? rr / p.group : 0, j = rr >= 0 ? rr - qi * p.group : 0;
-        const int64_t row = static_cast<int64_t>(q0 + qi) * p.num_q_heads + kvh * p.group + j;
-        // a half warp past the last row loads nothing and writes nothing
-        merge_slots<D>(p, row, 0, rr >= 0 ? p.n_splits + 1 : 0, lane & 15,
-                       rr >= 0 ? a.out + row * D : nullptr,
-                       (rr >= 0 && a.lse != nullptr) ? a.lse + row : nullptr, true);
-      }
+  if (u_begin < u_end) {  // (a prefix CTA may have none)
+    if (warp == kWarpScheduler) {
+      produce_items<D>(a, &tm_k, &tm_v, smem, st_full, st_empty, idesc, abort_flag);
+    } else if (warp < kStreamWarps) {
+      consume_items<D>(a, smem, st_full, st_empty, idesc, abort_flag);
     }
   }
+  // the bulk copies of the merge below overwrite what was written here through the
+  // generic proxy
+  fence_proxy_async_smem();
 
-  // ---- the last CTA to finish zeroes the counters for the next call (every CTA's
-  // reads of prefix_done precede its count)
+  // ---- grid-wide barrier: every partial of the call is written.  The arrival is one
+  // acquire-release add (the CTA barrier before it makes every thread's partial
+  // stores part of what it releases); the last CTA zeroes the count and advances the
+  // generation, which the others read at their start (no CTA can advance it before
+  // every CTA has arrived).
   __syncthreads();
   if (threadIdx.x == 0) {
-    __threadfence();
-    if (atomicAdd(a.exit_count, 1) == static_cast<int>(gridDim.x) - 1) {
-      *a.prefix_done = 0;
-      *a.exit_count = 0;
+    const int old = atomic_add_acq_rel_gpu(a.bar_count, 1);
+    if (old == static_cast<int>(gridDim.x) - 1) {
+      *a.bar_count = 0;
+      st_release_gpu_u32(a.bar_gen, g0 + 1u);
+    } else {
+      const long long c0 = clock64();
+      unsigned spins = 0;
+      while (ld_acquire_gpu_u32(a.bar_gen) == g0) {
+        if ((++spins & 255u) == 0 && clock64() - c0 > kWaitLimitCycles) {
+          if (p.status) atomicCAS(p.status, 0, kErrTimeout);
+          break;
+        }
+      }
     }
   }
+  __syncthreads();
+
+  // ---- merge_attn_states: CTA b takes rows [b R / G, (b + 1) R / G) of the R rows,
+  // which are contiguous in every slot: one bulk copy per slot brings a chunk of them
+  // (and their LSEs) into shared memory, then half a warp merges each row
+  merge_rows_staged<D>(a, smem, merge_bar, abort_flag);
 }
 
 template <int D>

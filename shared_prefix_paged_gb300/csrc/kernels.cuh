@@ -64,16 +64,13 @@ struct PagedArgs {
 // Single-kernel cascade step for decode-like batches (decode_cascade.cu): at most 16
 // packed rows (query, head-in-group) per request and KV head.  CTAs [0, prefix_ctas)
 // run one prefix range each (pre.n_splits ranges per (KV head, 256-row block), range
-// s = 64-key tiles [s*key_tiles/n_splits, (s+1)*key_tiles/n_splits), slot s), count
-// themselves in prefix_done, then stream prefix_units suffix units each; the other
-// CTAs share the remaining suffix units (request, KV head).  Suffix partials go to slot
-// pre.n_splits; a CTA merges the rows of its own units from slots [0, n_splits] once
-// prefix_done reaches prefix_ctas.  The last CTA to finish zeroes the counters.
+// s = 64-key tiles [s*key_tiles/n_splits, (s+1)*key_tiles/n_splits), slot s), then
+// stream prefix_units suffix units; the other CTAs share the remaining suffix units
+// (request, KV head).  Suffix partials go to slot n_splits.  After a grid-wide barrier
+// every CTA merges an equal share of the rows from slots [0, n_splits].
 // Most partial results per row (the prefix ranges + the suffix): one merge reads at
 // most 16 slots.
 constexpr int kDecodeMaxParts = 16;
-// Most suffix units (request, KV head) one CTA of that kernel streams.
-constexpr int kDecodeMaxUnitsPerCta = 128;
 
 struct DecodeArgs {
   PrefixArgs pre;            // prefix phase; part_o / part_lse hold n_splits + 1 slots
@@ -88,8 +85,8 @@ struct DecodeArgs {
   int prefix_ctas;           // num_kv_heads * pre.pairs * pre.n_splits (<= grid)
   int prefix_units;          // suffix units each prefix CTA streams after its range
   int key_tiles;             // ceil(cpl / 64)
-  int* prefix_done;          // prefix ranges written; zero at launch, left zero
-  int* exit_count;           // CTAs finished; zero at launch, left zero
+  int* bar_count;            // zero at launch; the kernel leaves it zero
+  unsigned* bar_gen;         // any value; advanced by one per call
   __nv_bfloat16* out;
   float* lse;                // natural-log LSE or nullptr
 };
