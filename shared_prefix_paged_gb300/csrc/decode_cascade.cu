@@ -469,58 +469,64 @@ __device__ __forceinline__ void consume_items(const DecodeArgs& a, uint8_t* ring
 
 // ------------------------------------------------------------ staged merge --
 // merge_attn_states for rows [b R / G, (b + 1) R / G) of CTA b, in chunks of up to
-// kChunkRows rows: thread 0 copies each slot's chunk of bf16 rows (contiguous, 16-byte
-// aligned) and of LSEs (the run rounded out to 16-byte boundaries; the workspace has
-// room past its end) into shared memory with bulk async copies completing on `bar`;
-// then half a warp merges each row (lane i: the weight of slot i and features
-// [i*D/16, (i+1)*D/16)).  An empty slot (lse -inf) gets weight 0.
+// kChunkRows rows.  A chunk's bf16 rows are contiguous (and 16-byte aligned) in every
+// slot: lane s of warp 0 brings slot s's with one bulk async copy into shared memory,
+// completing on `bar`, while each half warp loads the LSEs of its row from L2 (lane i:
+// slot i).  Then half a warp merges each row (lane i also holds features
+// [i*D/16, (i+1)*D/16) of every slot).  An empty slot (lse -inf) gets weight 0.
 template <int D>
 __device__ __forceinline__ void merge_rows_staged(const DecodeArgs& a, uint8_t* smem,
                                                   uint64_t* bar, volatile int* abort_flag) {
   constexpr int kF = D / 16;
+  constexpr int kMax = 16;
   using Vec = typename std::conditional<kF == 8, uint4, uint2>::type;
   const PrefixArgs& p = a.pre;
   const int n = p.n_splits + 1;  // slots
   const int64_t rows = static_cast<int64_t>(p.total_q) * p.num_q_heads;
-  const int64_t r0 = static_cast<int64_t>(blockIdx.x) * rows / gridDim.x;
-  const int64_t r1 = static_cast<int64_t>(blockIdx.x + 1) * rows / gridDim.x;
-  // rows per chunk: n slots of bf16 rows plus n LSE runs (each up to 8 floats longer)
-  const int chunk = min(kChunkRows, (kMergeBytes / n - 64) / (D * 2 + 4));
-  const int o_bytes_row = D * 2;
-  const int lse_stride = (chunk + 6 + 3) & ~3;  // floats per slot's LSE run
-  __nv_bfloat16* s_o = reinterpret_cast<__nv_bfloat16*>(smem);
-  float* s_l = reinterpret_cast<float*>(smem + static_cast<size_t>(n) * chunk * o_bytes_row);
+  // (32-bit products while they fit: a 64-bit division costs hundreds of cycles)
+  const int64_t r0 = rows * gridDim.x < (int64_t{1} << 31)
+                         ? static_cast<int64_t>(static_cast<uint32_t>(blockIdx.x * rows) / gridDim.x)
+                         : static_cast<int64_t>(blockIdx.x) * rows / gridDim.x;
+  const int64_t r1 = rows * gridDim.x < (int64_t{1} << 31)
+                         ? static_cast<int64_t>(static_cast<uint32_t>((blockIdx.x + 1) * rows) /
+                                                gridDim.x)
+                         : static_cast<int64_t>(blockIdx.x + 1) * rows / gridDim.x;
+  const int chunk = min(kChunkRows, kMergeBytes / (n * D * 2));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int hw = threadIdx.x >> 4, hl = threadIdx.x & 15;
   const unsigned mask = 0xffffu << (threadIdx.x & 16);
+  __nv_bfloat16* s_o = reinterpret_cast<__nv_bfloat16*>(smem);
   uint32_t phase = 0;
   for (int64_t c0 = r0; c0 < r1; c0 += chunk, phase ^= 1u) {
     const int m = static_cast<int>(min(static_cast<int64_t>(chunk), r1 - c0));
-    if (threadIdx.x == 0) {
-      const uint32_t ob = static_cast<uint32_t>(m) * o_bytes_row;
-      uint32_t total = 0;
-      for (int s = 0; s < n; ++s) {
-        const int64_t g = s * rows + c0;  // the run's first LSE, 16-byte aligned both ends
-        total += ob + static_cast<uint32_t>(((g + m + 3) & ~int64_t{3}) - (g & ~int64_t{3})) * 4;
-      }
-      mbar_arrive_expect_tx(bar, total);
-      // the partials were written by other CTAs through the generic proxy; the copies
-      // read them through the async proxy
-      asm volatile("fence.proxy.async.global;" ::: "memory");
-      for (int s = 0; s < n; ++s) {
-        const int64_t g = s * rows + c0;
-        const int64_t g0 = g & ~int64_t{3}, g1 = (g + m + 3) & ~int64_t{3};
-        bulk_load(s_o + static_cast<size_t>(s) * chunk * D, p.part_o + g * D, ob, bar);
-        bulk_load(s_l + s * lse_stride, p.part_lse + g0, static_cast<uint32_t>(g1 - g0) * 4, bar);
+    if (warp == 0) {
+      if (lane == 0) mbar_arrive_expect_tx(bar, static_cast<uint32_t>(n * m * D * 2));
+      __syncwarp();
+      if (lane < n) {
+        // the partials were written by other CTAs through the generic proxy; the copy
+        // reads them through the async proxy
+        asm volatile("fence.proxy.async.global;" ::: "memory");
+        bulk_load(s_o + static_cast<size_t>(lane) * chunk * D, p.part_o + (lane * rows + c0) * D,
+                  static_cast<uint32_t>(m * D * 2), bar);
       }
     }
+    // both halves of a warp in step: pass k takes rows 2 (warp + 10 k) + {0, 1}
+    int i = 2 * (hw >> 1) + (hw & 1);
+    float lw = (i < m && hl < n) ? __ldcg(p.part_lse + hl * rows + c0 + i) : -INFINITY;
     const bool ok = mbar_wait(bar, phase, abort_flag, p.status);
-    // lane hl's slot: where the chunk's first row sits in that slot's LSE run
-    const int lo = static_cast<int>((hl * rows + c0) & 3);
-    // both halves of a warp in step
     for (int base = 2 * (hw >> 1); base < m; base += kThreads / 16) {
-      const int i = base + (hw & 1);
       const bool in = ok && i < m;
-      const float lw = (in && hl < n) ? s_l[hl * lse_stride + lo + i] : -INFINITY;
+      const int i_next = i + kThreads / 16;
+      // the next pass's LSEs are on their way while this row is merged
+      const float lw_next =
+          (i_next < m && hl < n) ? __ldcg(p.part_lse + hl * rows + c0 + i_next) : -INFINITY;
+      Vec v[kMax];
+#pragma unroll
+      for (int s = 0; s < kMax; ++s) {
+        if (in && s < n)
+          v[s] = *reinterpret_cast<const Vec*>(s_o + (static_cast<size_t>(s) * chunk + i) * D + hl * kF);
+      }
+      if (!in) lw = -INFINITY;
       float mx = lw;
 #pragma unroll
       for (int o = 8; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(mask, mx, o, 16));
@@ -532,12 +538,11 @@ __device__ __forceinline__ void merge_rows_staged(const DecodeArgs& a, uint8_t* 
       float acc[kF];
 #pragma unroll
       for (int f = 0; f < kF; ++f) acc[f] = 0.f;
-      for (int s = 0; s < n; ++s) {
+#pragma unroll
+      for (int s = 0; s < kMax; ++s) {
         const float ws = __shfl_sync(mask, w, s, 16) * inv;
-        if (in && ws != 0.f) {
-          const Vec v = *reinterpret_cast<const Vec*>(s_o + (static_cast<size_t>(s) * chunk + i) * D +
-                                                     hl * kF);
-          const uint32_t* u = reinterpret_cast<const uint32_t*>(&v);
+        if (s < n && ws != 0.f) {
+          const uint32_t* u = reinterpret_cast<const uint32_t*>(&v[s]);
 #pragma unroll
           for (int f = 0; f < kF / 2; ++f) {
             const float2 x = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u[f]));
@@ -556,6 +561,8 @@ __device__ __forceinline__ void merge_rows_staged(const DecodeArgs& a, uint8_t* 
         if (hl == 0 && a.lse != nullptr)
           a.lse[row] = wsum > 0.f ? (mx + log2f(wsum)) * 0.69314718055994531f : -INFINITY;
       }
+      i = i_next;
+      lw = lw_next;
     }
     // the next chunk's copies overwrite what was read here
     __syncthreads();
@@ -577,6 +584,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int lane = threadIdx.x & 31;
   // generation of the grid barrier at the end (read now, off the critical path)
   const unsigned g0 = threadIdx.x == 0 ? ld_acquire_gpu_u32(a.bar_gen) : 0u;
+  // the first TMA through each map would otherwise wait for its descriptor
+  if (threadIdx.x == 32 * kWarpScheduler) {
+    prefetch_tensormap(&tm_k);
+    prefetch_tensormap(&tm_v);
+    prefetch_tensormap(&tm_q);
+  }
 
   // ---- role 1: one range of the prefix phase (tcgen05)
   if (static_cast<int>(blockIdx.x) < a.prefix_ctas) {
