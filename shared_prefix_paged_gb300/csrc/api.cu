@@ -26,6 +26,10 @@ constexpr int kPage = 16;
 constexpr size_t kHeaderBytes = 256;
 constexpr size_t kOffBarCount = 64;
 constexpr size_t kOffBarGen = 128;
+// Shared memory the decode schedule's merge stages its bf16 rows in.
+constexpr size_t kMergeSmemBytes = 192 * 1024;
+// LSE box of a merge chunk: the chunk's rows, rounded out to 16-byte boundaries.
+int merge_lse_box(int rows) { return (rows + 3 + 3) & ~3; }
 // Most packed rows (query, head-in-group) per request and KV head that the decode
 // schedule takes: one warp-level MMA tile.
 constexpr int kDecodeRows = 16;
@@ -90,6 +94,20 @@ int make_map_3d(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1, ui
   return CSP_OK;
 }
 
+// Plain (unswizzled) tiled map of `rank` dims: the decode schedule's merge reads its
+// workspace slots through these.
+int make_map_plain(CUtensorMap* map, CUtensorMapDataType type, uint32_t rank, const void* base,
+                   const cuuint64_t* dims, const cuuint64_t* strides, const cuuint32_t* box) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return cuda_fail(cudaErrorNotSupported);
+  const cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(map, type, rank, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return cuda_fail(cudaErrorInvalidValue);
+  return CSP_OK;
+}
+
 bool supported_group(int g) { return g == 1 || g == 2 || g == 4 || g == 8 || g == 16; }
 
 int check_shape(int num_reqs, int total_q, int max_q, int max_k, int Hq, int Hkv, int D, int bs) {
@@ -115,7 +133,8 @@ struct LaunchPlan {
   size_t off_counters = 0, off_part_o = 0, off_part_lse = 0, bytes = 0;
   // single-kernel decode schedule (decode_cascade.cu)
   bool single = false;
-  int d_splits = 0, d_prefix_ctas = 0, d_prefix_units = 0, d_grid = 0;
+  int d_splits = 0, d_prefix_ctas = 0, d_prefix_units = 0, d_grid = 0, d_merge_rows = 0;
+  int64_t d_lse_stride = 0;
   size_t d_off_o = 0, d_off_lse = 0;
 };
 
@@ -208,12 +227,19 @@ void make_plan(int num_reqs, int total_q, int max_q, int max_k, int cpl, int Hq,
       p.d_prefix_ctas = d_base * s;
       p.d_prefix_units = k;
       p.d_grid = sms;
-      // slots: [0, s) the prefix ranges, s the suffix
+      // slots: [0, s) the prefix ranges, s the suffix; an LSE slot is padded to a
+      // multiple of four rows (the merge's tensor map wants 16-byte strides)
+      p.d_lse_stride = (static_cast<int64_t>(rows_total) + 3) & ~int64_t{3};
+      // rows per merge chunk: a CTA's share, within the box limit and the shared
+      // memory the merge stages them in
+      p.d_merge_rows = static_cast<int>(std::min<int64_t>(
+          {cdiv64(static_cast<int64_t>(rows_total), sms), 252,
+           static_cast<int64_t>(kMergeSmemBytes / (static_cast<size_t>(s + 1) * D * 2))}));
+      p.d_merge_rows = std::max(p.d_merge_rows, 1);
       p.d_off_o = kHeaderBytes;
       p.d_off_lse = p.d_off_o + align256(static_cast<size_t>(s + 1) * rows_total * D * 2);
-      // (+256: the merge reads each slot's LSE run rounded out to 16 bytes)
-      p.bytes = std::max(p.bytes, p.d_off_lse +
-                                      align256(static_cast<size_t>(s + 1) * rows_total * 4) + 256);
+      p.bytes = std::max(p.bytes, p.d_off_lse + align256(static_cast<size_t>(s + 1) *
+                                                         p.d_lse_stride * 4));
     }
   }
   *P = p;
@@ -286,7 +312,27 @@ int attention_call(const void* q, const void* k_cache, const void* v_cache, int3
     pa.scale_log2 = scale_log2;
     pa.part_o = reinterpret_cast<__nv_bfloat16*>(ws + P.d_off_o);
     pa.part_lse = reinterpret_cast<float*>(ws + P.d_off_lse);
+    pa.lse_stride = P.d_lse_stride;
     pa.status = status;
+    // the merge's views of the slots: bf16 rows [slot][row][D] and LSEs [slot][row]
+    CUtensorMap tm_po, tm_pl;
+    {
+      const uint64_t n_slots = static_cast<uint64_t>(P.d_splits) + 1;
+      const uint64_t rows = static_cast<uint64_t>(total_q) * Hq;
+      const cuuint64_t od[3] = {static_cast<cuuint64_t>(D), rows, n_slots};
+      const cuuint64_t os[2] = {row_b, rows * row_b};
+      const cuuint32_t ob[3] = {static_cast<cuuint32_t>(D), static_cast<cuuint32_t>(P.d_merge_rows),
+                                static_cast<cuuint32_t>(n_slots)};
+      const cuuint64_t ld[2] = {static_cast<cuuint64_t>(P.d_lse_stride), n_slots};
+      const cuuint64_t ls[1] = {static_cast<cuuint64_t>(P.d_lse_stride) * 4};
+      const cuuint32_t lb[2] = {static_cast<cuuint32_t>(merge_lse_box(P.d_merge_rows)),
+                                static_cast<cuuint32_t>(n_slots)};
+      if ((st = make_map_plain(&tm_po, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, pa.part_o, od, os,
+                               ob)) != CSP_OK ||
+          (st = make_map_plain(&tm_pl, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, pa.part_lse, ld, ls,
+                               lb)) != CSP_OK)
+        return st;
+    }
     da.q = static_cast<const __nv_bfloat16*>(q);
     da.k = static_cast<const __nv_bfloat16*>(k_cache);
     da.v = static_cast<const __nv_bfloat16*>(v_cache);
@@ -297,6 +343,7 @@ int attention_call(const void* q, const void* k_cache, const void* v_cache, int3
     da.num_reqs = num_reqs;
     da.prefix_ctas = P.d_prefix_ctas;
     da.prefix_units = P.d_prefix_units;
+    da.merge_rows = P.d_merge_rows;
     da.key_tiles = cdiv(cpl, 64);
     da.bar_count = reinterpret_cast<int*>(ws + kOffBarCount);
     da.bar_gen = reinterpret_cast<unsigned*>(ws + kOffBarGen);
@@ -304,7 +351,8 @@ int attention_call(const void* q, const void* k_cache, const void* v_cache, int3
     da.lse = lse;
     // phase events: [0] before the kernel, [1..3] after it
     if ((e = mark(0)) != cudaSuccess) return cuda_fail(e);
-    if ((e = csp::launch_decode(D, tm_q, tm_k, tm_v, da, P.d_grid, stream)) != cudaSuccess)
+    if ((e = csp::launch_decode(D, tm_q, tm_k, tm_v, tm_po, tm_pl, da, P.d_grid, stream)) !=
+        cudaSuccess)
       return cuda_fail(e);
     for (int i = 1; i < 4; ++i)
       if ((e = mark(i)) != cudaSuccess) return cuda_fail(e);
@@ -346,6 +394,7 @@ int attention_call(const void* q, const void* k_cache, const void* v_cache, int3
     pa.scale_log2 = scale_log2;
     pa.part_o = part_o;
     pa.part_lse = part_lse;
+    pa.lse_stride = static_cast<int64_t>(total_q) * Hq;
     pa.status = status;
     if ((e = csp::launch_prefix(D, tm_q, tm_k, tm_v, pa, stream)) != cudaSuccess)
       return cuda_fail(e);

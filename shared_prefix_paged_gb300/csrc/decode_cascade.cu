@@ -41,8 +41,6 @@ constexpr int kStreamWarps = 8;             // warps 0-7 stream the suffix
 constexpr int kStreamThreads = 32 * kStreamWarps;
 constexpr int kWarpScheduler = 8;           // produces the suffix items
 constexpr int kMergeBarOff = 512;           // merge barrier within the suffix barrier area
-constexpr int kMergeBytes = 200 * 1024;     // shared memory the staged merge may use
-constexpr int kChunkRows = 256;             // most rows merged per chunk
 
 static_assert(kThreads == 320, "ten warps: 8 softmax/streaming, MMA/scheduler, TMA");
 
@@ -440,8 +438,8 @@ __device__ __forceinline__ void consume_items(const DecodeArgs& a, uint8_t* ring
         }
         const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
         const int qi = rr / p.group, j = rr - qi * p.group;
-        const int64_t prow =
-            slot_rows + static_cast<int64_t>(c_q0 + qi) * p.num_q_heads + c_kvh * p.group + j;
+        const int64_t row = static_cast<int64_t>(c_q0 + qi) * p.num_q_heads + c_kvh * p.group + j;
+        const int64_t prow = slot_rows + row;
         if (lane < D / 4) {
           float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
@@ -456,7 +454,8 @@ __device__ __forceinline__ void consume_items(const DecodeArgs& a, uint8_t* ring
           store_bf16x4(p.part_o + prow * D + lane * 4,
                        make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv));
         }
-        if (lane == 0) p.part_lse[prow] = lsum > 0.f ? mg + log2f(lsum) : -INFINITY;
+        if (lane == 0)
+          p.part_lse[p.n_splits * p.lse_stride + row] = lsum > 0.f ? mg + log2f(lsum) : -INFINITY;
       }
     }
     // the item goes back to the producer (its TMA will overwrite what this warp
@@ -468,65 +467,63 @@ __device__ __forceinline__ void consume_items(const DecodeArgs& a, uint8_t* ring
 }
 
 // ------------------------------------------------------------ staged merge --
-// merge_attn_states for rows [b R / G, (b + 1) R / G) of CTA b, in chunks of up to
-// kChunkRows rows.  A chunk's bf16 rows are contiguous (and 16-byte aligned) in every
-// slot: lane s of warp 0 brings slot s's with one bulk async copy into shared memory,
-// completing on `bar`, while each half warp loads the LSEs of its row from L2 (lane i:
-// slot i).  Then half a warp merges each row (lane i also holds features
-// [i*D/16, (i+1)*D/16) of every slot).  An empty slot (lse -inf) gets weight 0.
+// merge_attn_states for rows [b R / G, (b + 1) R / G) of CTA b, in chunks of
+// a.merge_rows rows.  Thread 0 brings a chunk of every slot with two TMA tensor
+// copies completing on `bar`: the bf16 rows ([slot][row][D], tm_po) and the LSEs
+// ([slot][row], tm_pl, the run starting at the 16-byte boundary at or before the
+// chunk); rows past the workspace's arrive zero-filled and are not merged.  Then half
+// a warp merges each row: lane i holds the weight of slot i and features
+// [i*D/16, (i+1)*D/16) of every slot.  An empty slot (lse -inf) gets weight 0.
 template <int D>
-__device__ __forceinline__ void merge_rows_staged(const DecodeArgs& a, uint8_t* smem,
+__device__ __forceinline__ void merge_rows_staged(const DecodeArgs& a, const CUtensorMap* tm_po,
+                                                  const CUtensorMap* tm_pl, uint8_t* smem,
                                                   uint64_t* bar, volatile int* abort_flag) {
   constexpr int kF = D / 16;
   constexpr int kMax = 16;
   using Vec = typename std::conditional<kF == 8, uint4, uint2>::type;
   const PrefixArgs& p = a.pre;
   const int n = p.n_splits + 1;  // slots
+  const int chunk = a.merge_rows;
+  const int lbox = (chunk + 6) & ~3;  // LSEs per slot in a chunk's copy
   const int64_t rows = static_cast<int64_t>(p.total_q) * p.num_q_heads;
   // (32-bit products while they fit: a 64-bit division costs hundreds of cycles)
-  const int64_t r0 = rows * gridDim.x < (int64_t{1} << 31)
-                         ? static_cast<int64_t>(static_cast<uint32_t>(blockIdx.x * rows) / gridDim.x)
-                         : static_cast<int64_t>(blockIdx.x) * rows / gridDim.x;
-  const int64_t r1 = rows * gridDim.x < (int64_t{1} << 31)
-                         ? static_cast<int64_t>(static_cast<uint32_t>((blockIdx.x + 1) * rows) /
-                                                gridDim.x)
-                         : static_cast<int64_t>(blockIdx.x + 1) * rows / gridDim.x;
-  const int chunk = min(kChunkRows, kMergeBytes / (n * D * 2));
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const bool small = rows * gridDim.x < (int64_t{1} << 31);
+  const int64_t r0 = small ? static_cast<int64_t>(static_cast<uint32_t>(blockIdx.x * rows) / gridDim.x)
+                           : static_cast<int64_t>(blockIdx.x) * rows / gridDim.x;
+  const int64_t r1 = small ? static_cast<int64_t>(static_cast<uint32_t>((blockIdx.x + 1) * rows) /
+                                                  gridDim.x)
+                           : static_cast<int64_t>(blockIdx.x + 1) * rows / gridDim.x;
   const int hw = threadIdx.x >> 4, hl = threadIdx.x & 15;
-  const unsigned mask = 0xffffu << (threadIdx.x & 16);
-  __nv_bfloat16* s_o = reinterpret_cast<__nv_bfloat16*>(smem);
+  // the two halves of a warp run in step: whole-warp shuffles in 16-lane segments
+  const unsigned mask = 0xffffffffu;
+  __nv_bfloat16* s_o = reinterpret_cast<__nv_bfloat16*>(smem);  // [n][chunk][D]
+  float* s_l = reinterpret_cast<float*>(smem + static_cast<size_t>(n) * chunk * D * 2);  // [n][lbox]
   uint32_t phase = 0;
   for (int64_t c0 = r0; c0 < r1; c0 += chunk, phase ^= 1u) {
     const int m = static_cast<int>(min(static_cast<int64_t>(chunk), r1 - c0));
-    if (warp == 0) {
-      if (lane == 0) mbar_arrive_expect_tx(bar, static_cast<uint32_t>(n * m * D * 2));
-      __syncwarp();
-      if (lane < n) {
-        // the partials were written by other CTAs through the generic proxy; the copy
-        // reads them through the async proxy
-        asm volatile("fence.proxy.async.global;" ::: "memory");
-        bulk_load(s_o + static_cast<size_t>(lane) * chunk * D, p.part_o + (lane * rows + c0) * D,
-                  static_cast<uint32_t>(m * D * 2), bar);
-      }
+    const int l0 = static_cast<int>(c0 & ~int64_t{3});  // the LSE run's first row
+    if (threadIdx.x == 0) {
+      mbar_arrive_expect_tx(bar, static_cast<uint32_t>(n * chunk * D * 2 + n * lbox * 4));
+      // the partials were written by other CTAs through the generic proxy; the copies
+      // read them through the async proxy
+      asm volatile("fence.proxy.async.global;" ::: "memory");
+      tma_load_3d(s_o, tm_po, bar, 0, static_cast<int>(c0), 0);
+      tma_load_2d(s_l, tm_pl, bar, l0, 0);
     }
-    // both halves of a warp in step: pass k takes rows 2 (warp + 10 k) + {0, 1}
-    int i = 2 * (hw >> 1) + (hw & 1);
-    float lw = (i < m && hl < n) ? __ldcg(p.part_lse + hl * rows + c0 + i) : -INFINITY;
     const bool ok = mbar_wait(bar, phase, abort_flag, p.status);
+    const int lo = static_cast<int>(c0) - l0;
+    // pass k takes rows 2 (warp + 10 k) + {0, 1}
     for (int base = 2 * (hw >> 1); base < m; base += kThreads / 16) {
+      const int i = base + (hw & 1);
       const bool in = ok && i < m;
-      const int i_next = i + kThreads / 16;
-      // the next pass's LSEs are on their way while this row is merged
-      const float lw_next =
-          (i_next < m && hl < n) ? __ldcg(p.part_lse + hl * rows + c0 + i_next) : -INFINITY;
       Vec v[kMax];
 #pragma unroll
       for (int s = 0; s < kMax; ++s) {
         if (in && s < n)
-          v[s] = *reinterpret_cast<const Vec*>(s_o + (static_cast<size_t>(s) * chunk + i) * D + hl * kF);
+          v[s] = *reinterpret_cast<const Vec*>(s_o + (static_cast<size_t>(s) * chunk + i) * D +
+                                               hl * kF);
       }
-      if (!in) lw = -INFINITY;
+      const float lw = (in && hl < n) ? s_l[hl * lbox + lo + i] : -INFINITY;
       float mx = lw;
 #pragma unroll
       for (int o = 8; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(mask, mx, o, 16));
@@ -535,19 +532,22 @@ __device__ __forceinline__ void merge_rows_staged(const DecodeArgs& a, uint8_t* 
 #pragma unroll
       for (int o = 8; o > 0; o >>= 1) wsum += __shfl_xor_sync(mask, wsum, o, 16);
       const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+      // every slot's weight first (independent shuffles), then the sums
+      float wsv[kMax];
+#pragma unroll
+      for (int s = 0; s < kMax; ++s) wsv[s] = __shfl_sync(mask, w, s, 16) * inv;
       float acc[kF];
 #pragma unroll
       for (int f = 0; f < kF; ++f) acc[f] = 0.f;
 #pragma unroll
       for (int s = 0; s < kMax; ++s) {
-        const float ws = __shfl_sync(mask, w, s, 16) * inv;
-        if (s < n && ws != 0.f) {
+        if (s < n && wsv[s] != 0.f) {
           const uint32_t* u = reinterpret_cast<const uint32_t*>(&v[s]);
 #pragma unroll
           for (int f = 0; f < kF / 2; ++f) {
             const float2 x = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u[f]));
-            acc[2 * f] = fmaf(ws, x.x, acc[2 * f]);
-            acc[2 * f + 1] = fmaf(ws, x.y, acc[2 * f + 1]);
+            acc[2 * f] = fmaf(wsv[s], x.x, acc[2 * f]);
+            acc[2 * f + 1] = fmaf(wsv[s], x.y, acc[2 * f + 1]);
           }
         }
       }
@@ -561,8 +561,6 @@ __device__ __forceinline__ void merge_rows_staged(const DecodeArgs& a, uint8_t* 
         if (hl == 0 && a.lse != nullptr)
           a.lse[row] = wsum > 0.f ? (mx + log2f(wsum)) * 0.69314718055994531f : -INFINITY;
       }
-      i = i_next;
-      lw = lw_next;
     }
     // the next chunk's copies overwrite what was read here
     __syncthreads();
@@ -574,7 +572,9 @@ template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_cascade_kernel(const __grid_constant__ CUtensorMap tm_q,
                           const __grid_constant__ CUtensorMap tm_k,
-                          const __grid_constant__ CUtensorMap tm_v, const DecodeArgs a) {
+                          const __grid_constant__ CUtensorMap tm_v,
+                          const __grid_constant__ CUtensorMap tm_po,
+                          const __grid_constant__ CUtensorMap tm_pl, const DecodeArgs a) {
   using L = SLayout<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -589,6 +589,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefetch_tensormap(&tm_k);
     prefetch_tensormap(&tm_v);
     prefetch_tensormap(&tm_q);
+    prefetch_tensormap(&tm_po);
+    prefetch_tensormap(&tm_pl);
   }
 
   // ---- role 1: one range of the prefix phase (tcgen05)
@@ -664,12 +666,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   // ---- merge_attn_states: CTA b takes rows [b R / G, (b + 1) R / G) of the R rows,
   // which are contiguous in every slot: one bulk copy per slot brings a chunk of them
   // (and their LSEs) into shared memory, then half a warp merges each row
-  merge_rows_staged<D>(a, smem, merge_bar, abort_flag);
+  merge_rows_staged<D>(a, &tm_po, &tm_pl, smem, merge_bar, abort_flag);
 }
 
 template <int D>
 cudaError_t launch_decode_d(const CUtensorMap& tm_q, const CUtensorMap& tm_k,
-                            const CUtensorMap& tm_v, const DecodeArgs& a, int grid,
+                            const CUtensorMap& tm_v, const CUtensorMap& tm_po,
+                            const CUtensorMap& tm_pl, const DecodeArgs& a, int grid,
                             cudaStream_t stream) {
   static std::atomic<uint64_t> attr_done{0};
   cudaError_t e = set_smem_once(decode_cascade_kernel<D>, SLayout<D>::kDynamic, attr_done);
@@ -680,21 +683,22 @@ cudaError_t launch_decode_d(const CUtensorMap& tm_q, const CUtensorMap& tm_k,
   cfg.dynamicSmemBytes = SLayout<D>::kDynamic;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
-  // every CTA must be resident: suffix CTAs wait for the prefix CTAs' results
+  // every CTA must be resident: the grid-wide barrier waits for all of them
   attr[0].id = cudaLaunchAttributeCooperative;
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, decode_cascade_kernel<D>, tm_q, tm_k, tm_v, a);
+  return cudaLaunchKernelEx(&cfg, decode_cascade_kernel<D>, tm_q, tm_k, tm_v, tm_po, tm_pl, a);
 }
 
 }  // namespace
 
 cudaError_t launch_decode(int head_dim, const CUtensorMap& tm_q, const CUtensorMap& tm_k,
-                          const CUtensorMap& tm_v, const DecodeArgs& a, int grid,
+                          const CUtensorMap& tm_v, const CUtensorMap& tm_po,
+                          const CUtensorMap& tm_pl, const DecodeArgs& a, int grid,
                           cudaStream_t stream) {
-  if (head_dim == 64) return launch_decode_d<64>(tm_q, tm_k, tm_v, a, grid, stream);
-  return launch_decode_d<128>(tm_q, tm_k, tm_v, a, grid, stream);
+  if (head_dim == 64) return launch_decode_d<64>(tm_q, tm_k, tm_v, tm_po, tm_pl, a, grid, stream);
+  return launch_decode_d<128>(tm_q, tm_k, tm_v, tm_po, tm_pl, a, grid, stream);
 }
 
 }  // namespace csp

@@ -29,7 +29,8 @@ struct PrefixArgs {
   int tiles_per_split;   // 64-key tiles per range
   float scale_log2;      // softmax_scale * log2(e)
   __nv_bfloat16* part_o; // [n_parts][total_q][num_q_heads][D], normalised; slots [0, n_splits)
-  float* part_lse;       // [n_parts][total_q][num_q_heads], log2 domain
+  float* part_lse;       // [n_parts][lse_stride], log2 domain (row t * num_q_heads + h)
+  int64_t lse_stride;    // floats per LSE slot, >= total_q * num_q_heads
   int* status;           // workspace status word
 };
 
@@ -84,6 +85,7 @@ struct DecodeArgs {
   int num_reqs;
   int prefix_ctas;           // num_kv_heads * pre.pairs * pre.n_splits (<= grid)
   int prefix_units;          // suffix units each prefix CTA streams after its range
+  int merge_rows;            // rows per merge chunk (the merge tensor maps' box)
   int key_tiles;             // ceil(cpl / 64)
   int* bar_count;            // zero at launch; the kernel leaves it zero
   unsigned* bar_gen;         // any value; advanced by one per call
@@ -92,8 +94,12 @@ struct DecodeArgs {
 };
 
 // grid <= the number of co-resident CTAs (one per SM); launched cooperatively.
+// tm_po / tm_pl: the workspace slots as bf16 [n_splits + 1][rows][D] and fp32
+// [n_splits + 1][pre.lse_stride], boxes of merge_rows rows (and of
+// (merge_rows + 6) & ~3 LSEs).
 cudaError_t launch_decode(int head_dim, const CUtensorMap& tm_q, const CUtensorMap& tm_k,
-                          const CUtensorMap& tm_v, const DecodeArgs& a, int grid,
+                          const CUtensorMap& tm_v, const CUtensorMap& tm_po,
+                          const CUtensorMap& tm_pl, const DecodeArgs& a, int grid,
                           cudaStream_t stream);
 
 cudaError_t launch_prefix(int head_dim, const CUtensorMap& tm_q, const CUtensorMap& tm_k,

@@ -431,11 +431,12 @@ __device__ __forceinline__ void prefix_range(const CUtensorMap* tm_q_p,
       const int packed = pair * kRowsCta + r;
       const int t = packed >> gshift;
       if (t >= a.total_q) continue;
-      const int64_t prow = (static_cast<int64_t>(split) * a.total_q + t) * a.num_q_heads +
-                           kvh * a.group + (packed & (a.group - 1));
+      const int64_t row = static_cast<int64_t>(t) * a.num_q_heads + kvh * a.group +
+                          (packed & (a.group - 1));
+      const int64_t prow = static_cast<int64_t>(split) * a.total_q * a.num_q_heads + row;
       *reinterpret_cast<uint4*>(a.part_o + prow * D + c * 8) =
           *reinterpret_cast<const uint4*>(stage + r * L::kStageRow + c * 8);
-      if (c == 0) a.part_lse[prow] = s_lse[r];
+      if (c == 0) a.part_lse[split * a.lse_stride + row] = s_lse[r];
     }
   }
 }
