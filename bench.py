@@ -45,7 +45,8 @@ METRIC = "attn queries/s + HBM GB/s (% of roofline), decode N=64 P=4096 S=128"
 UNIT = "queries/s"
 L2_BYTES = 129 * 1024 * 1024
 KERNEL_SOURCES = {
-    "decode_cascade_kernel": ["decode_cascade.cu", "prefix_body.cuh", "common.cuh"],
+    "decode_cascade_kernel": ["decode_cascade.cu", "prefix_body.cuh", "common.cuh", "merge.cuh",
+                              "kernels.cuh"],
     "prefix_attn_kernel": ["prefix_attn.cu", "prefix_body.cuh", "common.cuh", "merge.cuh"],
     "paged_attn_kernel": ["paged_attn.cu", "common.cuh", "merge.cuh"],
 }
@@ -540,6 +541,12 @@ def run_ours(args, dist: Dist):
     if path == "cascade":
         ph = phase_times(run)
         kernels = ["decode_cascade_kernel"] if run.single else TWO_KERNELS
+        if run.single:
+            # one launch per step: the launch's average duration over the timed region
+            # is the region's event time / K (an isolated launch, timed with events
+            # right around it, also carries the launch gap)
+            result["isolated_launch_us"] = round(ph["decode_cascade_kernel"], 3)
+            ph["decode_cascade_kernel"] = us_call
         entries = {k: roofline_entry(k, ph[k], b, run, peaks, b.name) for k in kernels}
         dominant = max(kernels, key=lambda k: ph[k])
         result["roofline"] = entries[dominant]
