@@ -29,7 +29,10 @@
  *   block_table int32 [num_reqs, bt_row_stride]      physical block of each logical
  *                                                    page; only the first
  *                                                    cdiv(seqused_k[r], block_size)
- *                                                    entries of row r are read
+ *                                                    entries of row r are used (the
+ *                                                    decode schedule may read entries
+ *                                                    past them, within the row's
+ *                                                    bt_row_stride, and ignores them)
  *   cu_seqlens_q int32 [num_reqs + 1], cu_seqlens_q[0] = 0, nondecreasing
  *   seqused_k    int32 [num_reqs]  KV length of each request, including this step's
  *                                  query tokens (queries are the last q_len positions)
