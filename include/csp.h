@@ -130,9 +130,10 @@ CSP_API int cascade_plan(const int32_t* block_table, int64_t bt_row_stride, int3
  * csp_workspace_size — bytes of device workspace that cascade_attn (with this
  * common_prefix_len) or paged_attn (common_prefix_len = 0) needs for this batch
  * shape on the current device.  All arguments are host integers, the same as the
- * attention call will get.  The workspace holds a status word, the counters of the
- * single-kernel schedule, one counter per (query token, KV head) and the split
- * partial results; it must be 256-byte aligned and zero-filled before its first use
+ * attention call will get.  The workspace holds a status word, the counters and the
+ * call counter of the single-kernel schedule, one word per (query token, KV head) and
+ * the split partial results; it must be 256-byte aligned and zero-filled before its
+ * first use, and is not to be modified between calls except for zeroing it all again
  * (each call leaves its counters at zero or clears them itself, so one workspace may
  * serve batches of different shapes).  After a call reported CSP_ERR_TIMEOUT, zero
  * the workspace again before reusing it.

@@ -472,8 +472,9 @@ __device__ __forceinline__ void consume_items(const DecodeArgs& a, uint8_t* ring
 // copies completing on `bar`: the bf16 rows ([slot][row][D], tm_po) and the LSEs
 // ([slot][row], tm_pl, the run starting at the 16-byte boundary at or before the
 // chunk); rows past the workspace's arrive zero-filled and are not merged.  Then half
-// a warp merges each row: lane i holds the weight of slot i and features
-// [i*D/16, (i+1)*D/16) of every slot.  An empty slot (lse -inf) gets weight 0.
+// a warp merges each row: every lane computes the slots' weights from their LSEs and
+// sums features [i*D/16, (i+1)*D/16) of every slot.  An empty slot (lse -inf) gets
+// weight 0.
 template <int D>
 __device__ __forceinline__ void merge_rows_staged(const DecodeArgs& a, const CUtensorMap* tm_po,
                                                   const CUtensorMap* tm_pl, uint8_t* smem,
@@ -494,8 +495,6 @@ __device__ __forceinline__ void merge_rows_staged(const DecodeArgs& a, const CUt
                                                   gridDim.x)
                            : static_cast<int64_t>(blockIdx.x + 1) * rows / gridDim.x;
   const int hw = threadIdx.x >> 4, hl = threadIdx.x & 15;
-  // the two halves of a warp run in step: whole-warp shuffles in 16-lane segments
-  const unsigned mask = 0xffffffffu;
   __nv_bfloat16* s_o = reinterpret_cast<__nv_bfloat16*>(smem);  // [n][chunk][D]
   float* s_l = reinterpret_cast<float*>(smem + static_cast<size_t>(n) * chunk * D * 2);  // [n][lbox]
   uint32_t phase = 0;
@@ -523,31 +522,34 @@ __device__ __forceinline__ void merge_rows_staged(const DecodeArgs& a, const CUt
           v[s] = *reinterpret_cast<const Vec*>(s_o + (static_cast<size_t>(s) * chunk + i) * D +
                                                hl * kF);
       }
-      const float lw = (in && hl < n) ? s_l[hl * lbox + lo + i] : -INFINITY;
-      float mx = lw;
+      // every lane reads all slots' LSEs (one broadcast each): weights without shuffles
+      float lsv[kMax];
+      float mx = -INFINITY;
 #pragma unroll
-      for (int o = 8; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(mask, mx, o, 16));
-      const float w = (mx == -INFINITY || lw == -INFINITY) ? 0.f : fast_exp2(lw - mx);
-      float wsum = w;
+      for (int s = 0; s < kMax; ++s) {
+        lsv[s] = (in && s < n) ? s_l[s * lbox + lo + i] : -INFINITY;
+        mx = fmaxf(mx, lsv[s]);
+      }
+      float wsum = 0.f;
 #pragma unroll
-      for (int o = 8; o > 0; o >>= 1) wsum += __shfl_xor_sync(mask, wsum, o, 16);
+      for (int s = 0; s < kMax; ++s) {
+        lsv[s] = (mx == -INFINITY || lsv[s] == -INFINITY) ? 0.f : fast_exp2(lsv[s] - mx);
+        wsum += lsv[s];
+      }
       const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
-      // every slot's weight first (independent shuffles), then the sums
-      float wsv[kMax];
-#pragma unroll
-      for (int s = 0; s < kMax; ++s) wsv[s] = __shfl_sync(mask, w, s, 16) * inv;
       float acc[kF];
 #pragma unroll
       for (int f = 0; f < kF; ++f) acc[f] = 0.f;
 #pragma unroll
       for (int s = 0; s < kMax; ++s) {
-        if (s < n && wsv[s] != 0.f) {
+        const float ws = lsv[s] * inv;
+        if (s < n && ws != 0.f) {
           const uint32_t* u = reinterpret_cast<const uint32_t*>(&v[s]);
 #pragma unroll
           for (int f = 0; f < kF / 2; ++f) {
             const float2 x = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u[f]));
-            acc[2 * f] = fmaf(wsv[s], x.x, acc[2 * f]);
-            acc[2 * f + 1] = fmaf(wsv[s], x.y, acc[2 * f + 1]);
+            acc[2 * f] = fmaf(ws, x.x, acc[2 * f]);
+            acc[2 * f + 1] = fmaf(ws, x.y, acc[2 * f + 1]);
           }
         }
       }
