@@ -2,12 +2,13 @@
 
 cascade_attn runs batches whose requests have at most 16 packed rows (query, head in
 group) per KV head as one cooperative kernel: some CTAs run ranges of the prefix phase
-on tcgen05 while the others stream suffix units taken from a counter in the workspace,
-then every CTA merges a share of the rows after a grid-wide barrier.  These cases
+on tcgen05 while the others stream suffix units (request, KV head) through a
+producer warp's TMA ring, then every CTA merges a share of the rows after a grid-wide
+barrier.  These cases
 exercise that kernel's own logic against the oracle: causal suffix rows of several
 queries, group sizes at the 16-row limit, D 64, suffixes of many tiles, a request
 without queries, the fallback to two kernels, and one workspace reused across calls
-of different shapes (its counters must come back to zero after each call).
+of different shapes (its barrier count must come back to zero after each call).
 """
 
 import pytest
