@@ -480,7 +480,6 @@ __device__ __forceinline__ void merge_rows_staged(const DecodeArgs& a, const CUt
                                                   const CUtensorMap* tm_pl, uint8_t* smem,
                                                   uint64_t* bar, volatile int* abort_flag) {
   constexpr int kF = D / 16;
-  constexpr int kMax = 16;
   using Vec = typename std::conditional<kF == 8, uint4, uint2>::type;
   const PrefixArgs& p = a.pre;
   const int n = p.n_splits + 1;  // slots
@@ -515,44 +514,47 @@ __device__ __forceinline__ void merge_rows_staged(const DecodeArgs& a, const CUt
     for (int base = 2 * (hw >> 1); base < m; base += kThreads / 16) {
       const int i = base + (hw & 1);
       const bool in = ok && i < m;
-      Vec v[kMax];
-#pragma unroll
-      for (int s = 0; s < kMax; ++s) {
-        if (in && s < n)
-          v[s] = *reinterpret_cast<const Vec*>(s_o + (static_cast<size_t>(s) * chunk + i) * D +
-                                               hl * kF);
-      }
-      // every lane reads all slots' LSEs (one broadcast each): weights without shuffles
-      float lsv[kMax];
+      // the slots' weights from their LSEs (every lane reads them all: one broadcast
+      // each), then the weighted sum, four slots at a time up to the slot count
       float mx = -INFINITY;
+      for (int s0 = 0; s0 < n; s0 += 4) {
 #pragma unroll
-      for (int s = 0; s < kMax; ++s) {
-        lsv[s] = (in && s < n) ? s_l[s * lbox + lo + i] : -INFINITY;
-        mx = fmaxf(mx, lsv[s]);
+        for (int k = 0; k < 4; ++k)
+          if (in && s0 + k < n) mx = fmaxf(mx, s_l[(s0 + k) * lbox + lo + i]);
       }
       float wsum = 0.f;
-#pragma unroll
-      for (int s = 0; s < kMax; ++s) {
-        lsv[s] = (mx == -INFINITY || lsv[s] == -INFINITY) ? 0.f : fast_exp2(lsv[s] - mx);
-        wsum += lsv[s];
-      }
-      const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
       float acc[kF];
 #pragma unroll
       for (int f = 0; f < kF; ++f) acc[f] = 0.f;
+      for (int s0 = 0; s0 < n; s0 += 4) {
+        float w[4];
+        Vec v[4];
 #pragma unroll
-      for (int s = 0; s < kMax; ++s) {
-        const float ws = lsv[s] * inv;
-        if (s < n && ws != 0.f) {
-          const uint32_t* u = reinterpret_cast<const uint32_t*>(&v[s]);
+        for (int k = 0; k < 4; ++k) {
+          const float l = (in && s0 + k < n) ? s_l[(s0 + k) * lbox + lo + i] : -INFINITY;
+          w[k] = (mx == -INFINITY || l == -INFINITY) ? 0.f : fast_exp2(l - mx);
+          wsum += w[k];
+          if (w[k] != 0.f)
+            v[k] = *reinterpret_cast<const Vec*>(
+                s_o + (static_cast<size_t>(s0 + k) * chunk + i) * D + hl * kF);
+        }
 #pragma unroll
-          for (int f = 0; f < kF / 2; ++f) {
-            const float2 x = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u[f]));
-            acc[2 * f] = fmaf(ws, x.x, acc[2 * f]);
-            acc[2 * f + 1] = fmaf(ws, x.y, acc[2 * f + 1]);
+        for (int k = 0; k < 4; ++k) {
+          if (w[k] != 0.f) {
+            const uint32_t* u = reinterpret_cast<const uint32_t*>(&v[k]);
+#pragma unroll
+            for (int f = 0; f < kF / 2; ++f) {
+              const float2 x =
+                  __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u[f]));
+              acc[2 * f] = fmaf(w[k], x.x, acc[2 * f]);
+              acc[2 * f + 1] = fmaf(w[k], x.y, acc[2 * f + 1]);
+            }
           }
         }
       }
+      const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+#pragma unroll
+      for (int f = 0; f < kF; ++f) acc[f] *= inv;
       if (in) {
         const int64_t row = c0 + i;
         Vec o;
