@@ -473,9 +473,9 @@ __device__ __forceinline__ void consume_items(const DecodeArgs& a, uint8_t* ring
 // ([slot][row], tm_pl, the run starting at the 16-byte boundary at or before the
 // chunk); rows past the workspace's arrive zero-filled and are not merged.  Then half
 // a warp merges each row: every lane computes the slots' weights from their LSEs and
-// sums features [i*D/16, (i+1)*D/16) of every slot.  An empty slot (lse -inf) gets
-// weight 0.
-template <int D>
+// sums features [i*D/16, (i+1)*D/16) of every slot, its loop unrolled to kSlots >= the
+// slot count.  An empty slot (lse -inf) gets weight 0.
+template <int D, int kSlots>
 __device__ __forceinline__ void merge_rows_staged(const DecodeArgs& a, const CUtensorMap* tm_po,
                                                   const CUtensorMap* tm_pl, uint8_t* smem,
                                                   uint64_t* bar, volatile int* abort_flag) {
@@ -514,42 +514,41 @@ __device__ __forceinline__ void merge_rows_staged(const DecodeArgs& a, const CUt
     for (int base = 2 * (hw >> 1); base < m; base += kThreads / 16) {
       const int i = base + (hw & 1);
       const bool in = ok && i < m;
-      // the slots' weights from their LSEs (every lane reads them all: one broadcast
-      // each), then the weighted sum, four slots at a time up to the slot count
-      float mx = -INFINITY;
-      for (int s0 = 0; s0 < n; s0 += 4) {
+      // every load first (slots past n read slot n - 1 and get weight 0; a partial is
+      // always finite), then the weights, then the sums: no load waits on another
+      float l[kSlots];
+      Vec v[kSlots];
 #pragma unroll
-        for (int k = 0; k < 4; ++k)
-          if (in && s0 + k < n) mx = fmaxf(mx, s_l[(s0 + k) * lbox + lo + i]);
+      for (int s = 0; s < kSlots; ++s) {
+        const int sc = min(s, n - 1);
+        l[s] = s_l[sc * lbox + lo + i];
+        v[s] = *reinterpret_cast<const Vec*>(s_o + (static_cast<size_t>(sc) * chunk + i) * D +
+                                             hl * kF);
       }
+      float mx = -INFINITY;
+#pragma unroll
+      for (int s = 0; s < kSlots; ++s) {
+        if (s >= n) l[s] = -INFINITY;
+        mx = fmaxf(mx, l[s]);
+      }
+      if (!in) mx = -INFINITY;
       float wsum = 0.f;
+#pragma unroll
+      for (int s = 0; s < kSlots; ++s) {
+        l[s] = (mx == -INFINITY || l[s] == -INFINITY) ? 0.f : fast_exp2(l[s] - mx);
+        wsum += l[s];
+      }
       float acc[kF];
 #pragma unroll
       for (int f = 0; f < kF; ++f) acc[f] = 0.f;
-      for (int s0 = 0; s0 < n; s0 += 4) {
-        float w[4];
-        Vec v[4];
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const float l = (in && s0 + k < n) ? s_l[(s0 + k) * lbox + lo + i] : -INFINITY;
-          w[k] = (mx == -INFINITY || l == -INFINITY) ? 0.f : fast_exp2(l - mx);
-          wsum += w[k];
-          if (w[k] != 0.f)
-            v[k] = *reinterpret_cast<const Vec*>(
-                s_o + (static_cast<size_t>(s0 + k) * chunk + i) * D + hl * kF);
-        }
+      for (int s = 0; s < kSlots; ++s) {
+        const uint32_t* u = reinterpret_cast<const uint32_t*>(&v[s]);
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          if (w[k] != 0.f) {
-            const uint32_t* u = reinterpret_cast<const uint32_t*>(&v[k]);
-#pragma unroll
-            for (int f = 0; f < kF / 2; ++f) {
-              const float2 x =
-                  __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u[f]));
-              acc[2 * f] = fmaf(w[k], x.x, acc[2 * f]);
-              acc[2 * f + 1] = fmaf(w[k], x.y, acc[2 * f + 1]);
-            }
-          }
+        for (int f = 0; f < kF / 2; ++f) {
+          const float2 x = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u[f]));
+          acc[2 * f] = fmaf(l[s], x.x, acc[2 * f]);
+          acc[2 * f + 1] = fmaf(l[s], x.y, acc[2 * f + 1]);
         }
       }
       const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
@@ -670,7 +669,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   // ---- merge_attn_states: CTA b takes rows [b R / G, (b + 1) R / G) of the R rows,
   // which are contiguous in every slot: one bulk copy per slot brings a chunk of them
   // (and their LSEs) into shared memory, then half a warp merges each row
-  merge_rows_staged<D>(a, &tm_po, &tm_pl, smem, merge_bar, abort_flag);
+  // (the slot loop is unrolled to a bound: 8 when it suffices)
+  if (p.n_splits + 1 <= 8)
+    merge_rows_staged<D, 8>(a, &tm_po, &tm_pl, smem, merge_bar, abort_flag);
+  else
+    merge_rows_staged<D, kDecodeMaxParts>(a, &tm_po, &tm_pl, smem, merge_bar, abort_flag);
 }
 
 template <int D>
