@@ -350,9 +350,20 @@ __device__ __forceinline__ void consume_items(const DecodeArgs& a, uint8_t* ring
         }
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-        const float m_new = fmaxf(m_run[h], mx);
-        const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
-        const float alpha = fast_exp2(m_run[h] - m_use);
+        // keep the running max unless it grows by more than 2^8 (always on the row's
+        // first unmasked keys, where it is -inf): then p = 2^(s - m) <= 256 and O and
+        // l need rescaling only now and then
+        if (mx > m_run[h] + 8.f) {
+          const float alpha = fast_exp2(m_run[h] - mx);
+          l_run[h] *= alpha;
+#pragma unroll
+          for (int dt = 0; dt < kDT; ++dt) {
+            o[dt][2 * h] *= alpha;
+            o[dt][2 * h + 1] *= alpha;
+          }
+          m_run[h] = mx;
+        }
+        const float m_use = (m_run[h] == -INFINITY) ? 0.f : m_run[h];
         float sum = 0.f;
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt) {
@@ -363,13 +374,7 @@ __device__ __forceinline__ void consume_items(const DecodeArgs& a, uint8_t* ring
             sum += sref;
           }
         }
-        l_run[h] = l_run[h] * alpha + sum;
-        m_run[h] = m_new;
-#pragma unroll
-        for (int dt = 0; dt < kDT; ++dt) {
-          o[dt][2 * h] *= alpha;
-          o[dt][2 * h + 1] *= alpha;
-        }
+        l_run[h] += sum;
       }
       // O += P V over the same 16 keys
       uint32_t pa[4];
@@ -399,6 +404,7 @@ __device__ __forceinline__ void consume_items(const DecodeArgs& a, uint8_t* ring
       float* s_o = reinterpret_cast<float*>(ring + slot * L::kItem);  // [8][16][kORow]
       float* s_m = s_o + kStreamWarps * kRows * kORow;                // [8][16]
       float* s_l = s_m + kStreamWarps * kRows;                        // [8][16]
+      // every warp's raw (max, sum, O) of its keys; the weights come in the final pass
       if ((lane & 3) == 0) {
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
@@ -406,35 +412,33 @@ __device__ __forceinline__ void consume_items(const DecodeArgs& a, uint8_t* ring
           s_l[wi * kRows + (lane >> 2) + 8 * h] = l_run[h];
         }
       }
-      stream_sync();
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         const int rr = (lane >> 2) + 8 * h;
         if (rr >= rows_valid) continue;
-        float mg = -INFINITY;
-#pragma unroll
-        for (int w = 0; w < kStreamWarps; ++w) mg = fmaxf(mg, s_m[w * kRows + rr]);
-        const float sc = (m_run[h] == -INFINITY) ? 0.f : fast_exp2(m_run[h] - mg);
         float* dst = s_o + (wi * kRows + rr) * kORow;
 #pragma unroll
         for (int dt = 0; dt < kDT; ++dt) {
           const int dd = dt * 8 + (lane & 3) * 2;
-          *reinterpret_cast<float2*>(dst + dd) =
-              make_float2(o[dt][2 * h] * sc, o[dt][2 * h + 1] * sc);
+          *reinterpret_cast<float2*>(dst + dd) = make_float2(o[dt][2 * h], o[dt][2 * h + 1]);
         }
       }
       stream_sync();
       const int64_t slot_rows = static_cast<int64_t>(p.n_splits) * p.total_q * p.num_q_heads;
       // warp wi finalises rows wi and wi + 8; lane c owns features [4c, 4c + 4)
       for (int rr = wi; rr < rows_valid; rr += kStreamWarps) {
+        float mw[kStreamWarps];
         float mg = -INFINITY;
 #pragma unroll
-        for (int w = 0; w < kStreamWarps; ++w) mg = fmaxf(mg, s_m[w * kRows + rr]);
+        for (int w = 0; w < kStreamWarps; ++w) {
+          mw[w] = s_m[w * kRows + rr];
+          mg = fmaxf(mg, mw[w]);
+        }
         float lsum = 0.f;
 #pragma unroll
         for (int w = 0; w < kStreamWarps; ++w) {
-          const float mw = s_m[w * kRows + rr];
-          lsum += (mw == -INFINITY) ? 0.f : s_l[w * kRows + rr] * fast_exp2(mw - mg);
+          mw[w] = (mw[w] == -INFINITY) ? 0.f : fast_exp2(mw[w] - mg);  // warp w's weight
+          lsum += s_l[w * kRows + rr] * mw[w];
         }
         const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
         const int qi = rr / p.group, j = rr - qi * p.group;
@@ -446,10 +450,10 @@ __device__ __forceinline__ void consume_items(const DecodeArgs& a, uint8_t* ring
           for (int w = 0; w < kStreamWarps; ++w) {
             const float4 v =
                 *reinterpret_cast<const float4*>(s_o + (w * kRows + rr) * kORow + lane * 4);
-            acc.x += v.x;
-            acc.y += v.y;
-            acc.z += v.z;
-            acc.w += v.w;
+            acc.x = fmaf(mw[w], v.x, acc.x);
+            acc.y = fmaf(mw[w], v.y, acc.y);
+            acc.z = fmaf(mw[w], v.z, acc.z);
+            acc.w = fmaf(mw[w], v.w, acc.w);
           }
           store_bf16x4(p.part_o + prow * D + lane * 4,
                        make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv));
