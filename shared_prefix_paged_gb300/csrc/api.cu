@@ -184,20 +184,23 @@ void make_plan(int num_reqs, int total_q, int max_q, int max_k, int cpl, int Hq,
   // Decode-like batches (a request's rows of one KV head fit one 16-row MMA tile):
   // one cooperative kernel.  d_base * s CTAs each run a prefix range and then stream
   // k suffix units; the other CTAs stream the rest of the suffix units from the
-  // start.  s and k come from a cost model measured on
-  // GB300 (per CTA, in us): a CTA moves ~31 GB/s of K/V (the per-SM copy rate); the
-  // prefix's first tile lands at ~3.5 and the
-  // suffix's first item at ~5.3; a prefix 64-key tile takes its bytes' time or ~1.1
-  // per 256 rows (tensor core and softmax), whichever is longer; writing a range's
-  // partial takes ~2.5.  Both kinds of CTA should finish together.
+  // start.  s and k come from a cost model measured on GB300 (per CTA, in us): the
+  // prefix's first tile lands at ~3.5; a prefix 64-key tile takes its bytes' time at
+  // ~31 GB/s (the per-SM copy rate) or ~1.22 per 256 rows (tensor core and softmax),
+  // whichever is longer; writing a range's partial takes ~3.4; the suffix's first
+  // item lands at ~5 and a suffix unit then takes its bytes' time at ~28.5 GB/s (the
+  // copies and the computing warps pace it together).  Both kinds of CTA should finish
+  // together.  The merge after them costs ~0.1 per slot its loop is unrolled to (8 up
+  // to 7 prefix ranges, 16 beyond); on a tie the fewer prefix ranges win.
   const int d_base = p.p_pairs * Hkv;
   if (cpl > 0 && static_cast<int64_t>(max_q) * p.group <= kDecodeRows && d_base <= sms) {
     const int pre_tiles = cdiv(cpl, 64);
-    const double kRate = 31e3;  // bytes per us per SM
+    const double kRate = 31e3, kUnitRate = 28.5e3;  // bytes per us per SM
     const double pair_rows = std::min(256.0, static_cast<double>(total_q) * p.group);
-    const double tile_us = std::max(64.0 * 4.0 * D / kRate, 1.1 * pair_rows / 256.0);
+    const double tile_us = std::max(64.0 * 4.0 * D / kRate, 1.22 * pair_rows / 256.0);
     const double unit_us =
-        (std::max(1, cdiv(max_len, 64)) * 64.0 * 4.0 * D + max_q * p.group * D * 2.0) / kRate;
+        (std::max(1, cdiv(max_len, 64)) * 64.0 * 4.0 * D + max_q * p.group * D * 2.0) /
+        kUnitRate;
     const int64_t units = static_cast<int64_t>(num_reqs) * Hkv;
     const int s_max = std::max(1, std::min({pre_tiles, csp::kDecodeMaxParts - 1, sms / d_base}));
     int s = 0, k = 0;
@@ -205,14 +208,15 @@ void make_plan(int num_reqs, int total_q, int max_q, int max_k, int cpl, int Hq,
     for (int c = 1; c <= s_max; ++c) {
       const int64_t pc = static_cast<int64_t>(d_base) * c;  // prefix CTAs
       const int64_t nc = sms - pc;                            // suffix-only CTAs
-      const double pre_us = 3.5 + cdiv(pre_tiles, c) * tile_us + 2.5;
+      const double pre_us = 3.5 + cdiv(pre_tiles, c) * tile_us + 3.4;
       const int64_t k_lo = nc > 0 ? 0 : cdiv64(units, pc);
       for (int64_t kk = k_lo; kk <= cdiv64(units, pc); ++kk) {
         const int64_t rest = std::max<int64_t>(0, units - pc * kk);
         const int64_t per = nc > 0 ? cdiv64(rest, nc) : 0;
         // a prefix CTA's first suffix item lands ~3.5 after its range is written
         const double t =
-            std::max(pre_us + (kk > 0 ? 3.5 : 0.0) + kk * unit_us, 5.3 + per * unit_us);
+            std::max(pre_us + (kk > 0 ? 3.5 : 0.0) + kk * unit_us, 5.0 + per * unit_us) +
+            (c + 1 <= 8 ? 0.8 : 1.6);
         if (best < 0.0 || t < best) {
           best = t;
           s = c;
