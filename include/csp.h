@@ -89,7 +89,8 @@ typedef enum {
 
 /* cascade_plan modes. */
 enum {
-  CSP_MODE_AUTO = 0,            /* the GB300 cost model decides                        */
+  CSP_MODE_AUTO = 0,            /* GB300 rule: cascade when it cuts the streamed KV
+                                   tokens by >= 1.8x (fitted to a measured sweep)     */
   CSP_MODE_FORCE_CASCADE = 1,   /* use cascade whenever common_prefix_len > 0          */
   CSP_MODE_FORCE_FLAT = 2,      /* never use cascade                                   */
   CSP_MODE_PAGE_THRESHOLDS = 3  /* the pages' rule only: prefix >= 256 and batch >= 8  */
@@ -199,6 +200,29 @@ CSP_API int cascade_attn(const void* q, const void* k_cache, const void* v_cache
                  int32_t block_size, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
                  float softmax_scale, void* out, float* lse, void* workspace,
                  size_t workspace_bytes, void* stream);
+
+/*
+ * cascade_attn_scheduled — cascade_attn with the schedule given by the caller instead
+ * of the cost model's (for tests and tuning; results are the same up to rounding):
+ *   schedule       CSP_SCHEDULE_TWO_KERNELS, or CSP_SCHEDULE_SINGLE where that kernel
+ *                  can run (a request's rows of one KV head fit 16 and the prefix's
+ *                  256-row blocks x KV heads fit the SMs; else CSP_ERR_UNSUPPORTED)
+ *   prefix_ranges  > 0: the single kernel's number of prefix key ranges (capped at 15,
+ *                  the prefix's 64-key tiles and the SMs' room); 0: the cost model's
+ * common_prefix_len must be > 0.  Other arguments, the workspace (csp_workspace_size
+ * covers every schedule and number of ranges) and the errors are cascade_attn's;
+ * CSP_ERR_INVALID_ARG for an unknown schedule or a negative prefix_ranges.
+ */
+CSP_API int cascade_attn_scheduled(const void* q, const void* k_cache, const void* v_cache,
+                                   int32_t num_blocks, const int32_t* block_table,
+                                   int64_t bt_row_stride, const int32_t* cu_seqlens_q,
+                                   const int32_t* seqused_k, int32_t num_reqs, int32_t total_q,
+                                   int32_t max_seqlen_q, int32_t max_seqlen_k,
+                                   int32_t common_prefix_len, int32_t block_size,
+                                   int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                                   float softmax_scale, void* out, float* lse, void* workspace,
+                                   size_t workspace_bytes, void* stream, int32_t schedule,
+                                   int32_t prefix_ranges);
 
 /*
  * cascade_attn_timed — cascade_attn plus four CUDA events recorded on `stream`

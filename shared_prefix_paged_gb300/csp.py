@@ -30,8 +30,8 @@ DTYPE_BF16, DTYPE_F32 = 0, 1
 
 # every symbol include/csp.h declares
 EXPORTS = ("cascade_plan", "csp_workspace_size", "cascade_attn", "cascade_attn_timed",
-           "paged_attn", "merge_states", "csp_workspace_status", "csp_status_string",
-           "csp_last_cuda_error", "csp_version", "cascade_attn_noalloc",
+           "cascade_attn_scheduled", "paged_attn", "merge_states", "csp_workspace_status",
+           "csp_status_string", "csp_last_cuda_error", "csp_version", "cascade_attn_noalloc",
            "csp_cascade_schedule")
 
 _lock = threading.Lock()
@@ -73,13 +73,14 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         tail = [i32, i32, i32, i32, ctypes.c_float, p, p, p, sz, p]
         lib.cascade_attn.argtypes = attn + [i32] + tail
         lib.cascade_attn_timed.argtypes = attn + [i32] + tail + [p]
+        lib.cascade_attn_scheduled.argtypes = attn + [i32] + tail + [i32, i32]
         lib.paged_attn.argtypes = attn + tail
         lib.merge_states.argtypes = [p, p, p, p, p, p, i32, i32, i32, i32, p]
         lib.csp_workspace_status.argtypes = [p, p, p]
         lib.csp_status_string.argtypes = [ctypes.c_int]
         lib.csp_status_string.restype = ctypes.c_char_p
         for name in ("cascade_plan", "csp_workspace_size", "cascade_attn", "cascade_attn_timed",
-                     "paged_attn",
+                     "cascade_attn_scheduled", "paged_attn",
                      "merge_states", "csp_workspace_status", "csp_last_cuda_error",
                      "csp_version", "csp_cascade_schedule"):
             getattr(lib, name).restype = ctypes.c_int
@@ -159,7 +160,7 @@ def alloc_workspace(nbytes: int, device):
 
 def _attn(fn_name, q, k_cache, v_cache, block_table, cu_seqlens_q, seqused_k, *, max_seqlen_q,
           max_seqlen_k, softmax_scale, common_prefix_len=None, out=None, lse=None,
-          workspace=None, stream=None, phase_events=None):
+          workspace=None, stream=None, phase_events=None, schedule=None, prefix_ranges=0):
     import torch
     lib = load()
     total_q, hq, d = q.shape
@@ -180,6 +181,11 @@ def _attn(fn_name, q, k_cache, v_cache, block_table, cu_seqlens_q, seqused_k, *,
         args.append(cpl)
     args += [bs, hq, hkv, d, float(softmax_scale), _ptr(out), _ptr(lse), _ptr(workspace),
              workspace.numel(), _stream_ptr(stream, q.device)]
+    if schedule is not None:
+        if phase_events is not None:
+            raise ValueError("schedule and phase_events do not combine")
+        fn_name = "cascade_attn_scheduled"
+        args += [int(schedule), int(prefix_ranges)]
     if phase_events is not None:
         fn_name = "cascade_attn_timed"
         if len(phase_events) != 4 or any(ev.cuda_event == 0 for ev in phase_events):
@@ -192,16 +198,21 @@ def _attn(fn_name, q, k_cache, v_cache, block_table, cu_seqlens_q, seqused_k, *,
 
 def cascade_attn(q, k_cache, v_cache, block_table, cu_seqlens_q, seqused_k, *, max_seqlen_q,
                  max_seqlen_k, common_prefix_len, softmax_scale, out=None, lse=None,
-                 workspace=None, stream=None, phase_events=None):
+                 workspace=None, stream=None, phase_events=None, schedule=None,
+                 prefix_ranges=0):
     """Cascade attention (prefix phase + suffix phase + LSE merge) on device tensors.
 
     phase_events: optional four torch.cuda.Event(enable_timing=True); when given, the
     call goes through cascade_attn_timed and records them between the kernels.
+    schedule: SCHEDULE_TWO_KERNELS or SCHEDULE_SINGLE to override the cost model
+    (cascade_attn_scheduled), with prefix_ranges > 0 fixing the single kernel's number
+    of prefix key ranges.
     """
     return _attn("cascade_attn", q, k_cache, v_cache, block_table, cu_seqlens_q, seqused_k,
                  max_seqlen_q=max_seqlen_q, max_seqlen_k=max_seqlen_k,
                  softmax_scale=softmax_scale, common_prefix_len=common_prefix_len, out=out,
-                 lse=lse, workspace=workspace, stream=stream, phase_events=phase_events)
+                 lse=lse, workspace=workspace, stream=stream, phase_events=phase_events,
+                 schedule=schedule, prefix_ranges=prefix_ranges)
 
 
 def paged_attn(q, k_cache, v_cache, block_table, cu_seqlens_q, seqused_k, *, max_seqlen_q,

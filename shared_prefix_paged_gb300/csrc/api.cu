@@ -138,8 +138,11 @@ struct LaunchPlan {
   size_t d_off_o = 0, d_off_lse = 0;
 };
 
+// sched_override: -1 (the cost model decides), CSP_SCHEDULE_TWO_KERNELS or
+// CSP_SCHEDULE_SINGLE (taken where the single kernel can run); ranges_override > 0
+// fixes the single kernel's number of prefix ranges.
 void make_plan(int num_reqs, int total_q, int max_q, int max_k, int cpl, int Hq, int Hkv, int D,
-               int sms, LaunchPlan* P) {
+               int sms, LaunchPlan* P, int sched_override = -1, int ranges_override = 0) {
   LaunchPlan p;
   p.group = Hq / Hkv;
   if (cpl > 0) {
@@ -191,7 +194,10 @@ void make_plan(int num_reqs, int total_q, int max_q, int max_k, int cpl, int Hq,
   // item lands at ~5 and a suffix unit then takes its bytes' time at ~28.5 GB/s (the
   // copies and the computing warps pace it together).  Both kinds of CTA should finish
   // together.  The merge after them costs ~0.1 per slot its loop is unrolled to (8 up
-  // to 7 prefix ranges, 16 beyond); on a tie the fewer prefix ranges win.
+  // to 7 prefix ranges, 16 beyond); on a tie the fewer prefix ranges win.  The single
+  // kernel is taken only if the same model does not expect the two-kernel schedule to
+  // be faster (a long prefix over many 256-row blocks leaves it too few SMs for one
+  // of the phases).
   const int d_base = p.p_pairs * Hkv;
   if (cpl > 0 && static_cast<int64_t>(max_q) * p.group <= kDecodeRows && d_base <= sms) {
     const int pre_tiles = cdiv(cpl, 64);
@@ -203,13 +209,14 @@ void make_plan(int num_reqs, int total_q, int max_q, int max_k, int cpl, int Hq,
         kUnitRate;
     const int64_t units = static_cast<int64_t>(num_reqs) * Hkv;
     const int s_max = std::max(1, std::min({pre_tiles, csp::kDecodeMaxParts - 1, sms / d_base}));
-    int s = 0, k = 0;
-    double best = -1.0;
-    for (int c = 1; c <= s_max; ++c) {
+    // best number of prefix units for c ranges (and the model's time for it)
+    auto best_k = [&](int c, double* t_out) {
       const int64_t pc = static_cast<int64_t>(d_base) * c;  // prefix CTAs
       const int64_t nc = sms - pc;                            // suffix-only CTAs
       const double pre_us = 3.5 + cdiv(pre_tiles, c) * tile_us + 3.4;
       const int64_t k_lo = nc > 0 ? 0 : cdiv64(units, pc);
+      double best_t = -1.0;
+      int kb = 0;
       for (int64_t kk = k_lo; kk <= cdiv64(units, pc); ++kk) {
         const int64_t rest = std::max<int64_t>(0, units - pc * kk);
         const int64_t per = nc > 0 ? cdiv64(rest, nc) : 0;
@@ -217,34 +224,59 @@ void make_plan(int num_reqs, int total_q, int max_q, int max_k, int cpl, int Hq,
         const double t =
             std::max(pre_us + (kk > 0 ? 3.5 : 0.0) + kk * unit_us, 5.0 + per * unit_us) +
             (c + 1 <= 8 ? 0.8 : 1.6);
-        if (best < 0.0 || t < best) {
-          best = t;
-          s = c;
-          k = static_cast<int>(kk);
+        if (best_t < 0.0 || t < best_t) {
+          best_t = t;
+          kb = static_cast<int>(kk);
         }
         if (per == 0) break;
       }
+      *t_out = best_t;
+      return kb;
+    };
+    int s = 1;
+    double best = -1.0;
+    for (int c = 1; c <= s_max; ++c) {
+      double t;
+      best_k(c, &t);
+      if (best < 0.0 || t < best) {
+        best = t;
+        s = c;
+      }
     }
-    if (s > 0) {
-      p.single = true;
-      p.d_splits = s;
-      p.d_prefix_ctas = d_base * s;
-      p.d_prefix_units = k;
-      p.d_grid = sms;
-      // slots: [0, s) the prefix ranges, s the suffix; an LSE slot is padded to a
-      // multiple of four rows (the merge's tensor map wants 16-byte strides)
-      p.d_lse_stride = (static_cast<int64_t>(rows_total) + 3) & ~int64_t{3};
-      // rows per merge chunk: a CTA's share, within the box limit and the shared
-      // memory the merge stages them in
-      p.d_merge_rows = static_cast<int>(std::min<int64_t>(
-          {cdiv64(static_cast<int64_t>(rows_total), sms), 252,
-           static_cast<int64_t>(kMergeSmemBytes / (static_cast<size_t>(s + 1) * D * 2))}));
-      p.d_merge_rows = std::max(p.d_merge_rows, 1);
-      p.d_off_o = kHeaderBytes;
-      p.d_off_lse = p.d_off_o + align256(static_cast<size_t>(s + 1) * rows_total * D * 2);
-      p.bytes = std::max(p.bytes, p.d_off_lse + align256(static_cast<size_t>(s + 1) *
-                                                         p.d_lse_stride * 4));
-    }
+    // the two-kernel schedule: its prefix kernel (p_splits ranges per block, in waves
+    // over the SMs), while the SMs it leaves free start the suffix, which every SM
+    // then streams
+    const double pre2_us = cdiv64(static_cast<int64_t>(d_base) * p.p_splits, sms) *
+                           (3.5 + p.p_tiles_per_split * tile_us + 3.4);
+    const int64_t free_sms = std::max<int64_t>(0, sms - static_cast<int64_t>(d_base) * p.p_splits);
+    const double two_us =
+        pre2_us + 5.0 +
+        std::max(0.0, static_cast<double>(units) * unit_us - free_sms * pre2_us) / sms;
+    p.single = sched_override == CSP_SCHEDULE_SINGLE ||
+               (sched_override < 0 && best <= two_us);
+    if (ranges_override > 0) s = std::min(ranges_override, s_max);
+    double t_s;
+    const int k = best_k(s, &t_s);
+    p.d_splits = s;
+    p.d_prefix_ctas = d_base * s;
+    p.d_prefix_units = k;
+    p.d_grid = sms;
+    // slots: [0, s) the prefix ranges, s the suffix; an LSE slot is padded to a
+    // multiple of four rows (the merge's tensor map wants 16-byte strides)
+    p.d_lse_stride = (static_cast<int64_t>(rows_total) + 3) & ~int64_t{3};
+    // rows per merge chunk: a CTA's share, within the box limit and the shared memory
+    // the merge stages them in
+    p.d_merge_rows = static_cast<int>(std::min<int64_t>(
+        {cdiv64(static_cast<int64_t>(rows_total), sms), 252,
+         static_cast<int64_t>(kMergeSmemBytes / (static_cast<size_t>(s + 1) * D * 2))}));
+    p.d_merge_rows = std::max(p.d_merge_rows, 1);
+    p.d_off_o = kHeaderBytes;
+    p.d_off_lse = p.d_off_o + align256(static_cast<size_t>(s + 1) * rows_total * D * 2);
+    // the workspace fits this schedule at any number of ranges (the most slots)
+    const size_t lse_max = static_cast<size_t>(s_max + 1) * p.d_lse_stride * 4;
+    p.bytes = std::max(p.bytes, kHeaderBytes +
+                                    align256(static_cast<size_t>(s_max + 1) * rows_total * D * 2) +
+                                    align256(lse_max));
   }
   *P = p;
 }
@@ -258,7 +290,8 @@ int attention_call(const void* q, const void* k_cache, const void* v_cache, int3
                    int32_t total_q, int32_t max_seqlen_q, int32_t max_seqlen_k, int32_t cpl,
                    int32_t block_size, int32_t Hq, int32_t Hkv, int32_t D, float scale,
                    void* out, float* lse, void* workspace, size_t workspace_bytes,
-                   void* stream_ptr, void* const* events = nullptr) {
+                   void* stream_ptr, void* const* events = nullptr, int sched_override = -1,
+                   int ranges_override = 0) {
   int st = check_shape(num_reqs, total_q, max_seqlen_q, max_seqlen_k, Hq, Hkv, D, block_size);
   if (st != CSP_OK) return st;
   if (cpl < 0 || cpl % block_size != 0 || cpl > max_seqlen_k) return CSP_ERR_INVALID_ARG;
@@ -274,7 +307,9 @@ int attention_call(const void* q, const void* k_cache, const void* v_cache, int3
   int sms = 0;
   if ((st = device_sm_count(&sms)) != CSP_OK) return st;
   LaunchPlan P;
-  make_plan(num_reqs, total_q, max_seqlen_q, max_seqlen_k, cpl, Hq, Hkv, D, sms, &P);
+  make_plan(num_reqs, total_q, max_seqlen_q, max_seqlen_k, cpl, Hq, Hkv, D, sms, &P,
+            sched_override, ranges_override);
+  if (sched_override == CSP_SCHEDULE_SINGLE && !P.single) return CSP_ERR_UNSUPPORTED;
   if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255) != 0 ||
       workspace_bytes < P.bytes)
     return CSP_ERR_WORKSPACE;
@@ -495,8 +530,11 @@ int cascade_plan(const int32_t* block_table, int64_t bt_row_stride, int32_t num_
       use = thresholds;
       break;
     default: {
-      // GB300 rule: on top of the thresholds, cascade must cut the KV bytes the
-      // standard path streams by at least 1.5x (prefix read once instead of N times).
+      // GB300 rule, fitted to a cascade-vs-flat sweep of N in {4..256} x P in
+      // {128..16384} (S = 128) on one GB300: cascade when it cuts the KV tokens the
+      // standard path streams by at least 1.8x (the prefix read once instead of N
+      // times).  On that grid it is never more than 5% slower than the better path;
+      // the pages' thresholds (prefix >= 256, batch >= 8) lost up to 2x at N = 4.
       int64_t flat_tokens = 0, casc_tokens = cpl;
       for (int r = 0; r < num_reqs; ++r) {
         flat_tokens += seq_lens[r];
@@ -506,7 +544,7 @@ int cascade_plan(const int32_t* block_table, int64_t bt_row_stride, int32_t num_
       (void)num_kv_heads;
       (void)head_dim;
       (void)num_sms;
-      use = thresholds && casc_tokens > 0 && 2 * flat_tokens >= 3 * casc_tokens;
+      use = cpl > 0 && casc_tokens > 0 && 5 * flat_tokens >= 9 * casc_tokens;
       break;
     }
   }
@@ -542,6 +580,25 @@ int cascade_attn(const void* q, const void* k_cache, const void* v_cache, int32_
                         seqused_k, num_reqs, total_q, max_seqlen_q, max_seqlen_k,
                         common_prefix_len, block_size, num_q_heads, num_kv_heads, head_dim,
                         softmax_scale, out, lse, workspace, workspace_bytes, stream);
+}
+
+int cascade_attn_scheduled(const void* q, const void* k_cache, const void* v_cache,
+                           int32_t num_blocks, const int32_t* block_table, int64_t bt_row_stride,
+                           const int32_t* cu_seqlens_q, const int32_t* seqused_k,
+                           int32_t num_reqs, int32_t total_q, int32_t max_seqlen_q,
+                           int32_t max_seqlen_k, int32_t common_prefix_len, int32_t block_size,
+                           int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                           float softmax_scale, void* out, float* lse, void* workspace,
+                           size_t workspace_bytes, void* stream, int32_t schedule,
+                           int32_t prefix_ranges) {
+  if (schedule != CSP_SCHEDULE_TWO_KERNELS && schedule != CSP_SCHEDULE_SINGLE)
+    return CSP_ERR_INVALID_ARG;
+  if (prefix_ranges < 0 || common_prefix_len <= 0) return CSP_ERR_INVALID_ARG;
+  return attention_call(q, k_cache, v_cache, num_blocks, block_table, bt_row_stride, cu_seqlens_q,
+                        seqused_k, num_reqs, total_q, max_seqlen_q, max_seqlen_k,
+                        common_prefix_len, block_size, num_q_heads, num_kv_heads, head_dim,
+                        softmax_scale, out, lse, workspace, workspace_bytes, stream, nullptr,
+                        schedule, prefix_ranges);
 }
 
 int cascade_attn_timed(const void* q, const void* k_cache, const void* v_cache,

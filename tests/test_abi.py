@@ -74,6 +74,15 @@ def test_planner_modes_and_errors():
     assert csp.cascade_plan(*args, mode=csp.MODE_FORCE_FLAT) == (512, False)
     assert csp.cascade_plan(*args, mode=csp.MODE_FORCE_CASCADE) == (512, True)
     assert csp.cascade_plan(*args, mode=csp.MODE_AUTO) == (512, True)
+    # the GB300 rule keeps cascade for a small batch over a long prefix (the pages'
+    # thresholds refuse N < 8) and refuses it where it would save too few bytes
+    small = workloads.decode_batch(n=4, p=4096, s=32)
+    sargs = (small.block_table, small.seq_lens, small.num_computed_tokens)
+    assert csp.cascade_plan(*sargs, mode=csp.MODE_PAGE_THRESHOLDS) == (4096, False)
+    assert csp.cascade_plan(*sargs, mode=csp.MODE_AUTO) == (4096, True)
+    short = workloads.decode_batch(n=16, p=64, s=128)   # 16*192 vs 64+16*128 tokens: 1.46x
+    rargs = (short.block_table, short.seq_lens, short.num_computed_tokens)
+    assert csp.cascade_plan(*rargs, mode=csp.MODE_AUTO) == (64, False)
     assert csp.cascade_plan(np.zeros((0, 4), np.int32), [], []) == (0, False)
     with pytest.raises(csp.CspError) as e:
         csp.cascade_plan(b.block_table, b.seq_lens, b.seq_lens + 1)   # computed > seq_len

@@ -42,21 +42,52 @@ CASES = [
 ]
 
 
+SINGLE = dict(schedule=csp.SCHEDULE_SINGLE)
+
+
 @pytest.mark.parametrize("case", CASES, ids=[f"case{c[0]}" for c in CASES])
 def test_single_kernel_all_rows(case):
+    # the schedule is forced: with few long suffixes the cost model would rather take
+    # the two-kernel schedule, but these shapes exercise the single kernel's own paths
     seed, seq, ql, shared, hq, hkv, d = case
     b = small(seed, seq, ql, shared, hq, hkv, d)
     dev = H.to_device(b)
     ref_o, ref_l = H.oracle_ref(b)
     cpl, _ = H.plan(b, mode=csp.MODE_FORCE_CASCADE)
     assert cpl > 0
-    sched, splits = schedule(b, cpl)
-    assert sched == csp.SCHEDULE_SINGLE and splits >= 1
-    out, lse = H.run_cascade(b, dev, cpl)
+    out, lse = H.run_cascade(b, dev, cpl, **SINGLE)
     H.compare(out, lse, ref_o, ref_l, what="single kernel")
     # a shorter prefix is as valid: more of each request's keys go to the suffix phase
-    out, lse = H.run_cascade(b, dev, 16)
+    out, lse = H.run_cascade(b, dev, 16, **SINGLE)
     H.compare(out, lse, ref_o, ref_l, what="single kernel cpl=16")
+    # other numbers of prefix ranges (one range; several, with prefix CTAs taking units)
+    for r in (1, 3):
+        out, lse = H.run_cascade(b, dev, cpl, prefix_ranges=r, **SINGLE)
+        H.compare(out, lse, ref_o, ref_l, what=f"single kernel, {r} prefix ranges")
+
+
+def test_forced_schedules_and_errors():
+    b = small(38, [300, 320, 350, 310], [4, 3, 1, 2], 288, 32, 8, 128)
+    dev = H.to_device(b)
+    ref_o, ref_l = H.oracle_ref(b)
+    cpl, _ = H.plan(b, mode=csp.MODE_FORCE_CASCADE)
+    out, lse = H.run_cascade(b, dev, cpl, schedule=csp.SCHEDULE_TWO_KERNELS)
+    H.compare(out, lse, ref_o, ref_l, what="forced two kernels")
+    with pytest.raises(csp.CspError) as e:
+        H.run_cascade(b, dev, cpl, schedule=7)
+    assert e.value.status == csp.CSP_ERR_INVALID_ARG
+    # 16 query tokens x group 4: 64 rows per request and KV head, past the 16-row tile
+    wide = small(39, [300, 310], [16, 16], 288, 32, 8, 128)
+    wdev = H.to_device(wide)
+    wcpl, _ = H.plan(wide, mode=csp.MODE_FORCE_CASCADE)
+    with pytest.raises(csp.CspError) as e:
+        H.run_cascade(wide, wdev, wcpl, **SINGLE)
+    assert e.value.status == csp.CSP_ERR_UNSUPPORTED
+
+
+def test_cost_model_picks_single_kernel_for_decode():
+    b = workloads.decode_batch()
+    assert schedule(b, 4096)[0] == csp.SCHEDULE_SINGLE
 
 
 def test_request_without_queries():
@@ -64,8 +95,7 @@ def test_request_without_queries():
     dev = H.to_device(b)
     ref_o, ref_l = H.oracle_ref(b)
     cpl, _ = H.plan(b, mode=csp.MODE_FORCE_CASCADE)
-    assert schedule(b, cpl)[0] == csp.SCHEDULE_SINGLE
-    out, lse = H.run_cascade(b, dev, cpl)
+    out, lse = H.run_cascade(b, dev, cpl, **SINGLE)
     H.compare(out, lse, ref_o, ref_l, what="empty request")
 
 
@@ -76,8 +106,7 @@ def test_last_block_with_one_m_tile():
     rows = H.sample_rows(b, 800, seed=1)
     ref_o, ref_l = H.oracle_ref(b, rows)
     cpl, _ = H.plan(b)
-    assert schedule(b, cpl)[0] == csp.SCHEDULE_SINGLE
-    out, lse = H.run_cascade(b, dev, cpl)
+    out, lse = H.run_cascade(b, dev, cpl, **SINGLE)
     H.compare(out, lse, ref_o, ref_l, rows, what="N=80")
 
 
