@@ -49,8 +49,9 @@ KERNEL_SOURCES = {
                               "kernels.cuh"],
     "prefix_attn_kernel": ["prefix_attn.cu", "prefix_body.cuh", "common.cuh", "merge.cuh"],
     "paged_attn_kernel": ["paged_attn.cu", "common.cuh", "merge.cuh"],
+    "paged_tc_kernel": ["paged_tc.cu", "prefix_body.cuh", "common.cuh", "merge.cuh",
+                        "kernels.cuh"],
 }
-TWO_KERNELS = ["prefix_attn_kernel", "paged_attn_kernel"]
 
 
 def parse_args(argv=None):
@@ -253,6 +254,11 @@ class DeviceRun:
             b.num_reqs, b.total_q, b.max_seqlen_q, b.max_seqlen_k, self.cpl, b.num_q_heads,
             b.num_kv_heads, b.head_dim) if self.use_cascade else (csp.SCHEDULE_TWO_KERNELS, 0)
         self.single = self.schedule == csp.SCHEDULE_SINGLE
+        # the suffix (or flat) kernel: tcgen05 once a request has more than 16 packed
+        # rows (query, head-in-group) per KV head, the warp-MMA kernel below that
+        self.suffix_kernel = ("paged_tc_kernel"
+                              if b.max_seqlen_q * (b.num_q_heads // b.num_kv_heads) > 16
+                              else "paged_attn_kernel")
 
     def plan(self):
         st = self._plan_fn(*self._plan_args)
@@ -352,7 +358,7 @@ def phase_times(run: DeviceRun, rounds: int = 16, batches: int = 3):
     if run.single:
         # one kernel: events 0 and 1 bracket it, event 2 follows immediately
         return {"decode_cascade_kernel": ms[0] * 1e3, "launches_averaged": n}
-    return {"prefix_attn_kernel": ms[0] * 1e3, "paged_attn_kernel": ms[1] * 1e3,
+    return {"prefix_attn_kernel": ms[0] * 1e3, run.suffix_kernel: ms[1] * 1e3,
             "launches_averaged": n}
 
 
@@ -540,7 +546,8 @@ def run_ours(args, dist: Dist):
 
     if path == "cascade":
         ph = phase_times(run)
-        kernels = ["decode_cascade_kernel"] if run.single else TWO_KERNELS
+        kernels = (["decode_cascade_kernel"] if run.single
+                   else ["prefix_attn_kernel", run.suffix_kernel])
         if run.single:
             # one launch per step: the launch's average duration over the timed region
             # is the region's event time / K (an isolated launch, timed with events

@@ -19,8 +19,8 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 INCLUDE = os.path.join(ROOT, "include")
 LIB_NAME = "libcsp_gb300.so"
-SOURCES = ["api.cu", "prefix_attn.cu", "paged_attn.cu", "decode_cascade.cu", "combine.cu",
-           "noalloc.cu"]
+SOURCES = ["api.cu", "prefix_attn.cu", "paged_attn.cu", "paged_tc.cu", "decode_cascade.cu",
+           "combine.cu", "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

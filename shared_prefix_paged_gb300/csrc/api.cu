@@ -127,6 +127,7 @@ struct LaunchPlan {
   int p_pairs = 0, p_splits = 0, p_tiles_per_split = 0, p_slots = 0;
   // paged phase (suffix or standard path)
   bool decode = true;
+  bool tc = false;      // many rows per (request, KV head): the tcgen05 kernel (paged_tc.cu)
   int s_row_tiles = 1, s_splits = 1, s_split_keys = 64;
   bool direct = false;  // paged kernel writes the final output itself
   int n_parts = 0;      // partial results per row group
@@ -166,13 +167,26 @@ void make_plan(int num_reqs, int total_q, int max_q, int max_k, int cpl, int Hq,
     p.p_slots = p.p_splits;
   }
   p.decode = static_cast<int64_t>(max_q) * p.group <= 16;
-  const int rows_per_cta = p.decode ? 16 : 64;
+  p.tc = !p.decode;
+  const int rows_per_cta = p.decode ? 16 : 256;
   p.s_row_tiles = std::max(1, cdiv(max_q * p.group, rows_per_cta));
   const int max_len = std::max(0, max_k - cpl);
   const int key_tiles = std::max(1, cdiv(max_len, 64));
   const int64_t units = static_cast<int64_t>(num_reqs) * p.s_row_tiles * Hkv;
   const int max_s = std::min(kMaxSplits, 32 - p.p_slots);
   int s = units > 0 ? static_cast<int>(std::min<int64_t>(cdiv64(2LL * sms, units), max_s)) : 1;
+  if (p.tc) {
+    // one CTA per SM: waves x (a split's tiles + ~5 tiles of fixed cost: the first
+    // tile's latency, the output and the merge)
+    int64_t best_cost = -1;
+    for (int c = 1; c <= std::min(max_s, key_tiles); ++c) {
+      const int64_t cost = cdiv64(units * c, sms) * (cdiv(key_tiles, c) + 5);
+      if (best_cost < 0 || cost < best_cost) {
+        best_cost = cost;
+        s = c;
+      }
+    }
+  }
   s = std::max(1, std::min(s, key_tiles));
   p.s_split_keys = cdiv(key_tiles, s) * 64;
   p.s_splits = std::max(1, cdiv(std::max(max_len, 1), p.s_split_keys));
@@ -464,11 +478,21 @@ int attention_call(const void* q, const void* k_cache, const void* v_cache, int3
   ga.counters = counters;
   ga.out = static_cast<__nv_bfloat16*>(out);
   ga.lse = lse;
+  ga.status = status;
   // concurrent with the prefix kernel (programmatic dependent launch) unless phase
   // events sit between the two
   const bool overlap = cpl > 0 && events == nullptr;
-  if ((e = csp::launch_paged(D, P.decode, ga, overlap, stream)) != cudaSuccess)
-    return cuda_fail(e);
+  if (P.tc) {
+    CUtensorMap tm_q;
+    const uint64_t row_b = static_cast<uint64_t>(D) * 2;
+    if ((st = make_map_3d(&tm_q, q, D, Hq, total_q, row_b, row_b * Hq, 64, P.group,
+                          128 / P.group)) != CSP_OK)
+      return st;
+    e = csp::launch_paged_tc(D, tm_q, ga, overlap, stream);
+  } else {
+    e = csp::launch_paged(D, P.decode, ga, overlap, stream);
+  }
+  if (e != cudaSuccess) return cuda_fail(e);
   if ((e = mark(2)) != cudaSuccess) return cuda_fail(e);
 
   if ((e = mark(3)) != cudaSuccess) return cuda_fail(e);

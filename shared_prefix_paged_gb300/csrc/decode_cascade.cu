@@ -608,7 +608,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int kvh = b / (p.n_splits * p.pairs);
     const int t_first = split * a.key_tiles / p.n_splits;
     const int t_last = (split + 1) * a.key_tiles / p.n_splits;
-    prefix::prefix_range<D>(&tm_q, &tm_k, &tm_v, p, kvh, pair, split, t_first, t_last, smem,
+    prefix::prefix_range<D>(&tm_q, &tm_k, &tm_v, p, prefix::prefix_geom(p, pair), kvh, split,
+                            t_first, t_last, smem,
                             reinterpret_cast<uint64_t*>(smem + L::kPrefixBars));
     // the staging buffer was read through the generic proxy and TMA wrote the stages;
     // the suffix role below rewrites the same memory

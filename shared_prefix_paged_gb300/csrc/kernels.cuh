@@ -60,6 +60,7 @@ struct PagedArgs {
   int* counters;         //               row-group counters (merge.cuh)
   __nv_bfloat16* out;    // final output: direct mode (part_o == nullptr) or last contributor
   float* lse;            // natural-log LSE or nullptr
+  int* status;           // workspace status word (bounded waits of the tcgen05 variant)
 };
 
 // Single-kernel cascade step for decode-like batches (decode_cascade.cu): at most 16
@@ -109,6 +110,13 @@ cudaError_t launch_prefix(int head_dim, const CUtensorMap& tm_q, const CUtensorM
 // (programmatic dependent launch, so it runs concurrently with it).
 cudaError_t launch_paged(int head_dim, bool decode, const PagedArgs& a, bool after_prefix,
                          cudaStream_t stream);
+
+// The same computation on tcgen05 for units of many rows (paged_tc.cu): one CTA per
+// (request, KV head, 256-row tile, key split); a.row_tiles counts 256-row tiles.
+// tm_q: q as bf16 [total_q][num_q_heads][D], boxes of 64 features x group heads x
+// 128 / group tokens.
+cudaError_t launch_paged_tc(int head_dim, const CUtensorMap& tm_q, const PagedArgs& a,
+                            bool after_prefix, cudaStream_t stream);
 
 cudaError_t launch_merge_states(__nv_bfloat16* out, float* out_lse, const void* o1,
                                 const float* l1, const void* o2, const float* l2, int rows,

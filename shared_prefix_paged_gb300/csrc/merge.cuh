@@ -134,4 +134,109 @@ __device__ __forceinline__ void count_and_merge(const MergeArgs& m, int t_first,
   }
 }
 
+// Block-wide merge of `n_rows` output rows, for a CTA that holds many rows of one
+// row space (paged_tc.cu).  Row i is output row row_of(i); skip(i) leaves it alone.
+// Slots [0, m.n_parts) come from the workspace; with `own` (bf16 rows at
+// own + i * own_stride, log2-sum-exp own_lse[i]) one more partial comes from shared
+// memory.  Every thread takes part and every load of a step is issued before its
+// results are used, so the step costs about one memory round trip rather than one per
+// row.  s_w: shared scratch of n_rows * (m.n_parts + 1) floats.  Called by every
+// thread of the CTA (contains __syncthreads).
+template <int D, typename RowOf, typename Skip>
+__device__ __forceinline__ void merge_rows_block(const MergeArgs& m, int n_rows, RowOf row_of,
+                                                 Skip skip, const __nv_bfloat16* own,
+                                                 int own_stride, const float* own_lse,
+                                                 float* s_w) {
+  const int tid = threadIdx.x, nthr = blockDim.x;
+  const int np = m.n_parts;
+  const int W = np + 1;
+  // weights of every partial of a row (normalised) and the row's final LSE
+  for (int i = tid; i < n_rows; i += nthr) {
+    if (skip(i)) continue;
+    const int64_t row = row_of(i);
+    float* w = s_w + i * W;
+    float mx = own ? own_lse[i] : -INFINITY;
+#pragma unroll 4
+    for (int p = 0; p < np; ++p) {
+      const float l = __ldcg(m.part_lse + static_cast<int64_t>(p) * m.rows + row);
+      w[p] = l;
+      mx = fmaxf(mx, l);
+    }
+    float wsum = 0.f;
+    for (int p = 0; p < np; ++p) {
+      const float e = (w[p] == -INFINITY || mx == -INFINITY) ? 0.f : fast_exp2(w[p] - mx);
+      w[p] = e;
+      wsum += e;
+    }
+    const float w_own =
+        (own && mx != -INFINITY && own_lse[i] != -INFINITY) ? fast_exp2(own_lse[i] - mx) : 0.f;
+    wsum += w_own;
+    const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+    for (int p = 0; p < np; ++p) w[p] *= inv;
+    w[np] = w_own * inv;
+    if (m.lse != nullptr)
+      m.lse[row] = wsum > 0.f ? (mx + log2f(wsum)) * 0.69314718055994531f : -INFINITY;
+  }
+  __syncthreads();
+  // the rows, 16 bytes (8 features) per item, eight items per thread in flight
+  constexpr int kC = D / 8;
+  const int n_items = n_rows * kC;
+  const int64_t slot_stride = static_cast<int64_t>(m.rows) * D;
+  for (int base = tid; base < n_items; base += 8 * nthr) {
+    float acc[8][8];
+    int64_t off[8];
+    int ri[8];
+    bool ok[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int it = base + j * nthr;
+      const int i = it / kC, c = it % kC;
+      ok[j] = it < n_items && !skip(i);
+      ri[j] = i;
+      off[j] = ok[j] ? row_of(i) * D + c * 8 : 0;
+      const float wo = ok[j] ? s_w[i * W + np] : 0.f;
+      if (own && wo != 0.f) {
+        const uint4 u = *reinterpret_cast<const uint4*>(own + i * own_stride + c * 8);
+        const uint32_t uu[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&uu[e]));
+          acc[j][2 * e] = wo * f.x;
+          acc[j][2 * e + 1] = wo * f.y;
+        }
+      } else {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc[j][e] = 0.f;
+      }
+    }
+    for (int p = 0; p < np; ++p) {
+      uint4 v[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        v[j] = ok[j] ? __ldcg(reinterpret_cast<const uint4*>(m.part_o + p * slot_stride + off[j]))
+                     : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const float wp = ok[j] ? s_w[ri[j] * W + p] : 0.f;
+        if (wp != 0.f) {  // an empty slot is never read into the sum
+          const uint32_t uu[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float2 f =
+                __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&uu[e]));
+            acc[j][2 * e] = fmaf(wp, f.x, acc[j][2 * e]);
+            acc[j][2 * e + 1] = fmaf(wp, f.y, acc[j][2 * e + 1]);
+          }
+        }
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      if (ok[j])
+        *reinterpret_cast<uint4*>(m.out + off[j]) =
+            make_uint4(pack_bf16x2(acc[j][0], acc[j][1]), pack_bf16x2(acc[j][2], acc[j][3]),
+                       pack_bf16x2(acc[j][4], acc[j][5]), pack_bf16x2(acc[j][6], acc[j][7]));
+  }
+}
+
 }  // namespace csp

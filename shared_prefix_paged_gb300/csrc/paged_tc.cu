@@ -1,0 +1,191 @@
+// paged_tc.cu — causal attention of each request over a range of its own KV pages,
+// on tcgen05 tensor cores, for requests with many query rows per KV head (prefill
+// and chunked prefill): the suffix phase of cascade attention (keys [cpl, seq_len),
+// "vLLM Cascade Attention：用法、场景与原理解析" §八 Step 5 Phase 2) and the standard
+// path (keys [0, seq_len), §五).
+//
+// A CTA owns up to 256 packed rows (query, head-in-group) of one request and one KV
+// head, and one key split.  Its main loop is the prefix phase's (prefix_body.cuh):
+// pages by 16-byte cp.async into a 4-deep ring of 64-key tiles, S = Q K^T and
+// O += P V on tcgen05 with TMEM accumulators, the online softmax one TMEM lane (row)
+// per thread.  Here each row also stops at its causal limit: query i of a request
+// with q_len queries and seq_len keys sees keys <= seq_len - q_len + i (bottom-right
+// alignment; the KV includes the new tokens).  The output step:
+//  * standard path with one split: bf16 out and the natural-log LSE directly;
+//  * one suffix split after the prefix phase: each row is merged in place with the
+//    prefix's slots (merge.cuh) once the prefix grid is complete;
+//  * several splits: each writes a partial slot and the last split of a row group
+//    merges every slot.
+#include "merge.cuh"
+#include "prefix_body.cuh"
+
+namespace csp {
+namespace {
+
+using prefix::Layout;
+using prefix::kRowsCta;
+using prefix::kThreads;
+
+// Dynamic shared memory: the data area, the barrier area, and slack to align the
+// base to 1024 bytes (128-byte swizzled tiles).
+template <int D>
+constexpr int kDynamic = Layout<D>::kData + prefix::kBarBytes + 1024;
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    paged_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const PagedArgs a) {
+  using L = Layout<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kData);
+
+  const int r = blockIdx.x / a.row_tiles;
+  const int rt = blockIdx.x % a.row_tiles;
+  const int g = blockIdx.y;
+  const int split = blockIdx.z;
+  const int q0 = __ldg(a.cu_seqlens_q + r);
+  const int q_len = __ldg(a.cu_seqlens_q + r + 1) - q0;
+  const int seq = __ldg(a.seq_lens + r);
+  const int rows_total = q_len * a.group;
+  const int prow0 = rt * kRowsCta;
+  if (prow0 >= rows_total) return;  // the request has fewer row tiles
+  const int rows_here = min(kRowsCta, rows_total - prow0);
+  const int gshift = __ffs(a.group) - 1;  // group is a power of two
+
+  // keys of this split, clipped by the causal limit of the CTA's last row
+  const int last_query = (prow0 + rows_here - 1) >> gshift;
+  const int kbeg = a.key_start + split * a.split_keys;
+  int kend = min(kbeg + a.split_keys, seq);
+  kend = min(kend, seq - q_len + last_query + 1);
+  const int ntiles = kend > kbeg ? (kend - kbeg + prefix::kKeysN - 1) / prefix::kKeysN : 0;
+
+  // what the main loop reads besides the geometry: sizes, scale, the status word
+  PrefixArgs pa;
+  pa.k = a.k;
+  pa.v = a.v;
+  pa.block_table = a.block_table;
+  pa.total_q = a.total_q;
+  pa.num_q_heads = a.num_q_heads;
+  pa.num_kv_heads = a.num_kv_heads;
+  pa.group = a.group;
+  pa.cpl = 0;
+  pa.pairs = 0;
+  pa.n_splits = 0;
+  pa.tiles_per_split = 0;
+  pa.scale_log2 = a.scale_log2;
+  pa.part_o = nullptr;
+  pa.part_lse = nullptr;
+  pa.lse_stride = 0;
+  pa.status = a.status;
+  prefix::RangeGeom geo;
+  geo.bt = a.block_table + static_cast<int64_t>(r) * a.bt_stride;
+  geo.key0 = kbeg;
+  geo.key_end = max(kend, kbeg);
+  geo.tok0 = q0;
+  geo.prow0 = prow0;
+  geo.rows_total = rows_total;
+  geo.causal_base = seq - q_len;
+  prefix::prefix_range<D, true>(&tm_q, &tm_q, &tm_q, pa, geo, g, split, 0, ntiles, smem, bars);
+
+  // 256 normalised rows (bf16) and their log2-sum-exp are staged and visible
+  const __nv_bfloat16* stage = reinterpret_cast<const __nv_bfloat16*>(smem);
+  const float* s_lse = reinterpret_cast<const float*>(smem + L::kLse);
+  constexpr int kChunks = D / 8;
+  constexpr float kLn2 = 0.69314718055994531f;
+  const bool partial = a.part_o != nullptr;
+  const bool merge_in_place = partial && a.n_splits == 1;
+  auto out_row = [&](int rr) {
+    const int rho = prow0 + rr;
+    return static_cast<int64_t>(q0 + (rho >> gshift)) * a.num_q_heads + g * a.group +
+           (rho & (a.group - 1));
+  };
+  if (!merge_in_place) {
+    // the final rows (standard path, one split) or this split's partial slot
+    for (int it = threadIdx.x; it < rows_here * kChunks; it += kThreads) {
+      const int rr = it / kChunks, c = it % kChunks;
+      const int64_t orow = out_row(rr);
+      const uint4 v = *reinterpret_cast<const uint4*>(stage + rr * L::kStageRow + c * 8);
+      if (partial) {
+        const int64_t prow =
+            static_cast<int64_t>(a.n_prefix + split) * a.total_q * a.num_q_heads + orow;
+        *reinterpret_cast<uint4*>(a.part_o + prow * D + c * 8) = v;
+        if (c == 0) a.part_lse[prow] = s_lse[rr];
+      } else {
+        *reinterpret_cast<uint4*>(a.out + orow * D + c * 8) = v;
+        if (c == 0 && a.lse != nullptr) a.lse[orow] = s_lse[rr] * kLn2;
+      }
+    }
+  }
+  if (!partial) return;
+
+  MergeArgs m;
+  m.part_o = a.part_o;
+  m.part_lse = a.part_lse;
+  m.counters = a.counters;
+  m.n_parts = a.n_prefix + a.n_splits;
+  m.n_count = a.n_splits;
+  m.rows = a.total_q * a.num_q_heads;
+  m.num_q_heads = a.num_q_heads;
+  m.num_kv_heads = a.num_kv_heads;
+  m.group = a.group;
+  m.out = a.out;
+  m.lse = a.lse;
+  // shared scratch past the staged rows: the last-split flags, then the weights
+  int* s_last = reinterpret_cast<int*>(smem + kRowsCta * L::kStageRow * 2);
+  float* s_w = reinterpret_cast<float*>(s_last + kRowsCta + 1);
+  grid_dependency_wait();  // the prefix grid's partials are complete and visible
+  if (merge_in_place) {
+    // this CTA is its rows' only suffix contributor: its staged rows join the prefix
+    // slots directly
+    m.n_parts = a.n_prefix;
+    merge_rows_block<D>(m, rows_here, out_row, [](int) { return false; }, stage, L::kStageRow,
+                        s_lse, s_w);
+  } else {
+    // count this split in the row groups (tokens) it touched; the last split of a
+    // group merges every slot of its rows
+    const int tok_first = prow0 >> gshift;
+    const int n_tok = ((prow0 + rows_here - 1) >> gshift) - tok_first + 1;
+    __syncthreads();  // every partial row of this CTA is written
+    for (int i = threadIdx.x; i < n_tok; i += kThreads) {
+      int* c = a.counters + static_cast<int64_t>(q0 + tok_first + i) * a.num_kv_heads + g;
+      s_last[i] = atomic_add_acq_rel_gpu(c, 1) == a.n_splits - 1;
+    }
+    __syncthreads();
+    merge_rows_block<D>(
+        m, rows_here, out_row,
+        [&](int rr) { return s_last[((prow0 + rr) >> gshift) - tok_first] == 0; }, nullptr, 0,
+        nullptr, s_w);
+  }
+}
+
+template <int D>
+cudaError_t launch_tc_t(const CUtensorMap& tm_q, const PagedArgs& a, bool after_prefix,
+                        cudaStream_t stream) {
+  static std::atomic<uint64_t> attr_done{0};
+  cudaError_t e = set_smem_once(paged_tc_kernel<D>, kDynamic<D>, attr_done);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.num_reqs * a.row_tiles, a.num_kv_heads, a.n_splits);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kDynamic<D>;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  // behind this call's prefix kernel: start on the SMs it leaves free; the merge
+  // waits for the prefix grid
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = after_prefix ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, paged_tc_kernel<D>, tm_q, a);
+}
+
+}  // namespace
+
+cudaError_t launch_paged_tc(int head_dim, const CUtensorMap& tm_q, const PagedArgs& a,
+                            bool after_prefix, cudaStream_t stream) {
+  if (head_dim == 64) return launch_tc_t<64>(tm_q, a, after_prefix, stream);
+  return launch_tc_t<128>(tm_q, a, after_prefix, stream);
+}
+
+}  // namespace csp

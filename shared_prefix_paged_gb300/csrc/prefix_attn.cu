@@ -34,8 +34,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int key_tiles = (a.cpl + prefix::kKeysN - 1) / prefix::kKeysN;
   const int t_first = min(split * a.tiles_per_split, key_tiles);
   const int t_last = min(t_first + a.tiles_per_split, key_tiles);
-  prefix::prefix_range<D>(&tm_q, &tm_k, &tm_v, a, kvh, pair, split, t_first, t_last, smem,
-                          bars);
+  prefix::prefix_range<D>(&tm_q, &tm_k, &tm_v, a, prefix::prefix_geom(a, pair), kvh, split,
+                          t_first, t_last, smem, bars);
 }
 
 template <int D>

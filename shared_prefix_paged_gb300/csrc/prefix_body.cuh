@@ -65,6 +65,33 @@ struct Layout {
 // Bytes of the caller's barrier area: 15 mbarriers, the TMEM slot and the abort flag.
 constexpr int kBarBytes = 256;
 
+// Where one CTA's rows and keys come from.  The prefix phase: the rows are every
+// query row of the batch, the keys [0, cpl) through block-table row 0, unmasked.  A
+// request's own range (paged_tc.cu): the rows are that request's, the keys
+// [key0, key_end) through its block-table row, and packed row rho sees keys up to
+// causal_base + rho / group (bottom-right causal alignment).
+struct RangeGeom {
+  const int32_t* bt;  // block-table row holding the range's pages
+  int key0;           // key position of tile 0, a multiple of the page size
+  int key_end;        // keys at or past it are neither loaded nor seen
+  int tok0;           // Q token of packed row 0
+  int prow0;          // the CTA's first packed row
+  int rows_total;     // packed rows that exist; rows past them are padding
+  int causal_base;    // kCausal: packed row rho sees keys <= causal_base + rho / group
+};
+
+__device__ __forceinline__ RangeGeom prefix_geom(const PrefixArgs& a, int pair) {
+  RangeGeom g;
+  g.bt = a.block_table;
+  g.key0 = 0;
+  g.key_end = a.cpl;
+  g.tok0 = 0;
+  g.prow0 = pair * 256;
+  g.rows_total = a.total_q * a.group;
+  g.causal_base = 0;
+  return g;
+}
+
 // Barrier over one softmax warpgroup (id 1 or 2, 128 threads) that ORs a predicate.
 __device__ __forceinline__ bool wg_bar_any(int id, bool pred) {
   uint32_t r;
@@ -86,12 +113,17 @@ __device__ __forceinline__ bool wg_bar_any(int id, bool pred) {
 // staging buffer and the row LSEs); bars: kBarBytes for the mbarriers, the TMEM slot
 // and the abort flag.  Allocates and frees all 512 TMEM columns.  Ends with every
 // global store of the partial issued; the caller syncs before reusing smem.
-template <int D>
+// With kCausal, rows and keys come from `geo` (a request's own range, causal mask)
+// and the CTA stops once its 256 normalised rows (bf16, [row][Layout::kStageRow] at
+// smem) and their log2-sum-exp (float [256] at smem + Layout::kLse; -inf for a row
+// that saw no key) are staged and visible to every thread: the caller writes them.
+template <int D, bool kCausal = false>
 __device__ __forceinline__ void prefix_range(const CUtensorMap* tm_q_p,
                                              const CUtensorMap* tm_k_p,
                                              const CUtensorMap* tm_v_p, const PrefixArgs& a,
-                                             int kvh, int pair, int split, int t_first,
-                                             int t_last, uint8_t* smem, uint64_t* bars) {
+                                             const RangeGeom& geo, int kvh, int split,
+                                             int t_first, int t_last, uint8_t* smem,
+                                             uint64_t* bars) {
   using L = Layout<D>;
   const CUtensorMap& tm_q = *tm_q_p;
   const CUtensorMap& tm_k = *tm_k_p;
@@ -111,13 +143,13 @@ __device__ __forceinline__ void prefix_range(const CUtensorMap* tm_q_p,
   // The CTAs of the other KV heads read the same pages (other rows of them): each
   // head starts at its own point of the range, so at any time the CTAs of one range
   // read different pages rather than all hitting the same ones together.
-  const int rot = ntiles > 0 ? (kvh * ntiles) / a.num_kv_heads : 0;
+  const int rot = (!kCausal && ntiles > 0) ? (kvh * ntiles) / a.num_kv_heads : 0;
   auto tile_of = [&](int i) {
     const int r = i + rot;
     return t_first + (r >= ntiles ? r - ntiles : r);
   };
-  const int rows_total = a.total_q * a.group;                 // packed rows of this KV head
-  const bool has_m1 = pair * kRowsCta + kRowsM < rows_total;  // second M tile has rows
+  const int rows_total = geo.rows_total;             // packed rows of this KV head
+  const bool has_m1 = geo.prow0 + kRowsM < rows_total;  // second M tile has rows
 
   if (threadIdx.x == 0) {
     mbar_init(bar_q, 1);
@@ -149,7 +181,7 @@ __device__ __forceinline__ void prefix_range(const CUtensorMap* tm_q_p,
 #pragma unroll
         for (int h = 0; h < L::kHalves; ++h)
           tma_load_3d(smem + L::kQ + m * L::kQTile + h * L::kQHalf, &tm_q, bar_q, h * 64,
-                      kvh * a.group, (pair * kRowsCta + m * kRowsM) / a.group);
+                      kvh * a.group, geo.tok0 + (geo.prow0 + m * kRowsM) / a.group);
     }
   }
   // ------------------------------------------------- MMA issuers, one per M tile --
@@ -249,13 +281,14 @@ __device__ __forceinline__ void prefix_range(const CUtensorMap* tm_q_p,
     const int lt = threadIdx.x;  // loader thread
     // Block ids of the range's pages, 32 at a time (eight tiles; lane l holds page
     // l % 4 of tile l / 4 of the window), read a window ahead of use.  Keys past the
-    // prefix are zero-filled without a read.
+    // range are zero-filled without a read.
     constexpr int kIdTiles = 32 / kPagesPerTile;
-    const int npages = a.cpl / kPage;
+    const int npages = (geo.key_end - geo.key0 + kPage - 1) / kPage;
+    const int32_t* bt_pages = geo.bt + geo.key0 / kPage;
     auto load_ids = [&](int i_base) {
       const int i = i_base + lane / kPagesPerTile;
       const int page = tile_of(i) * kPagesPerTile + (lane & (kPagesPerTile - 1));
-      return i < ntiles && page < npages ? __ldg(a.block_table + page) : 0;
+      return i < ntiles && page < npages ? __ldg(bt_pages + page) : 0;
     };
     int ids_cur = ntiles > 0 ? load_ids(0) : 0;
     int ids_nxt = ntiles > kIdTiles ? load_ids(kIdTiles) : 0;
@@ -267,7 +300,7 @@ __device__ __forceinline__ void prefix_range(const CUtensorMap* tm_q_p,
         ids_nxt = j + kIdTiles < ntiles ? load_ids(j + kIdTiles) : 0;
       }
       const int st = j % kStages;
-      const int key0 = tile_of(j) * kKeysN;
+      const int key0 = geo.key0 + tile_of(j) * kKeysN;
       const int w0 = (j % kIdTiles) * kPagesPerTile;
       int blk[kPagesPerTile];
 #pragma unroll
@@ -278,7 +311,7 @@ __device__ __forceinline__ void prefix_range(const CUtensorMap* tm_q_p,
         const int key = x / kChunks, c = x % kChunks;
         const int pq = key >> 4;
         const int b = pq == 0 ? blk[0] : pq == 1 ? blk[1] : pq == 2 ? blk[2] : blk[3];
-        const bool in = key0 + key < a.cpl;
+        const bool in = key0 + key < geo.key_end;
         const int64_t off =
             ((static_cast<int64_t>(b) * kPage + (key & 15)) * a.num_kv_heads + kvh) * D + c * 8;
         const uint32_t o = static_cast<uint32_t>(st * L::kKVBytes + (c >> 3) * L::kKVHalf +
@@ -289,6 +322,12 @@ __device__ __forceinline__ void prefix_range(const CUtensorMap* tm_q_p,
       cp_async_mbar_arrive(&kv_full[st]);
     };
     for (int j = 0; j < ntiles && j < kStages; ++j) issue_tile(j);
+    // the first key past this thread's row: the range's end, or its causal limit
+    int key_lim = geo.key_end;
+    if (kCausal) {
+      const int rho = geo.prow0 + wg * kRowsM + row;
+      key_lim = min(key_lim, geo.causal_base + rho / a.group + 1);
+    }
 
     // one tile of the online softmax: S(i) from TMEM -> P(i) back into TMEM (bf16)
     auto softmax_tile = [&](int i) -> bool {
@@ -300,8 +339,8 @@ __device__ __forceinline__ void prefix_range(const CUtensorMap* tm_q_p,
       tc_fence_after();
       float sv[kKeysN];
       tmem_ld64_sync(t_lane + (i & 1) * kKeysN, sv);
-      const int valid = a.cpl - tile * kKeysN;
-      if (valid < kKeysN) {  // only the prefix's last tile can be partial
+      const int valid = key_lim - (geo.key0 + tile * kKeysN);
+      if (valid < kKeysN) {  // the range's last tile, or past a causal limit
 #pragma unroll
         for (int j = 0; j < kKeysN; ++j)
           if (j >= valid) sv[j] = -INFINITY;
@@ -345,7 +384,8 @@ __device__ __forceinline__ void prefix_range(const CUtensorMap* tm_q_p,
       // p = 2^(s * scale * log2(e) - m): one FFMA and one ex2 per score
       uint32_t pw[kKeysN / 2];
       float sum4[4] = {0.f, 0.f, 0.f, 0.f};
-      const float neg_m = -m_run;
+      // a row whose keys so far are all masked keeps m_run = -inf: its p are 0
+      const float neg_m = (kCausal && m_run == -INFINITY) ? 0.f : -m_run;
 #pragma unroll
       for (int j = 0; j < kKeysN / 2; ++j) {
         const float p0 = fast_exp2(fmaf(sv[2 * j], a.scale_log2, neg_m));
@@ -396,12 +436,17 @@ __device__ __forceinline__ void prefix_range(const CUtensorMap* tm_q_p,
   __nv_bfloat16* stage = reinterpret_cast<__nv_bfloat16*>(smem);
   if (softmax_warp) {
     tc_fence_after();
-    const float inv_l = have ? 1.f / l_run : 0.f;
+    // a row that saw no key (l = 0) stages zeros
+    const float inv_l = (have && l_run > 0.f) ? 1.f / l_run : 0.f;
     __nv_bfloat16* dst = stage + (wg * kRowsM + row) * L::kStageRow;
 #pragma unroll
     for (int c = 0; c < D / 32; ++c) {
       float o[32];
       tmem_ld32_sync(tO + c * 32, o);
+      if (inv_l == 0.f) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) o[j] = 0.f;
+      }
 #pragma unroll
       for (int j = 0; j < 32; j += 8)
         *reinterpret_cast<uint4*>(dst + c * 32 + j) =
@@ -413,14 +458,16 @@ __device__ __forceinline__ void prefix_range(const CUtensorMap* tm_q_p,
   }
   // a row with no key in this range (or no query) gets -inf: weight 0 in the merge
   float* s_lse = reinterpret_cast<float*>(smem + L::kLse);
-  if (warp < 8) s_lse[wg * kRowsM + row] = (softmax_warp && have) ? m_run + log2f(l_run)
-                                                                  : -INFINITY;
+  if (warp < 8)
+    s_lse[wg * kRowsM + row] =
+        (softmax_warp && have && l_run > 0.f) ? m_run + log2f(l_run) : -INFINITY;
   tc_fence_before();
   __syncthreads();
   if (warp == kWarpMma) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
+  if constexpr (kCausal) return;  // the caller writes the staged rows
   // coalesced copy-out: a warp writes whole rows (D/8 lanes x 16 bytes each)
   {
     constexpr int kChunks = D / 8;
@@ -428,7 +475,7 @@ __device__ __forceinline__ void prefix_range(const CUtensorMap* tm_q_p,
     for (int it = threadIdx.x; it < kRowsCta * kChunks; it += kThreads) {
       const int r = it / kChunks;
       const int c = it % kChunks;
-      const int packed = pair * kRowsCta + r;
+      const int packed = geo.prow0 + r;
       const int t = packed >> gshift;
       if (t >= a.total_q) continue;
       const int64_t row = static_cast<int64_t>(t) * a.num_q_heads + kvh * a.group +

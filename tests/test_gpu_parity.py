@@ -34,6 +34,8 @@ SMALL_CASES = [
     (5, [400] * 6, [3] * 6, 384, 32, 2, 128),                     # group 16, 3 queries
     (6, [260, 390], [40, 2], 256, 16, 2, 64),                     # group 8, D 64, prefill rows
     (7, [1000] * 3, [1] * 3, 992, 8, 4, 128),                     # long prefix, short suffix
+    (8, [700, 420, 300], [100, 70, 1], 256, 16, 4, 128),          # two 256-row tiles
+    (9, [300, 200], [40, 33], 128, 4, 4, 64),                     # group 1, prefill rows
 ]
 
 
