@@ -94,6 +94,26 @@ int make_map_3d(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1, ui
   return CSP_OK;
 }
 
+// A K or V cache [blocks][16][Hkv][D] seen as 4-D {64 features, tokens, D / 64
+// feature halves, Hkv} (the halves and heads listed after the tokens), 128-byte
+// swizzle, boxes {64, 16, D / 64, 1}: one page of one KV head lands in shared memory
+// as [half][16 tokens][128 B], so 16 consecutive keys are consecutive swizzled rows.
+int make_map_kv_pages(CUtensorMap* map, const void* base, int D, int Hkv, uint64_t ntok) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return cuda_fail(cudaErrorNotSupported);
+  const cuuint64_t dims[4] = {64, ntok, static_cast<cuuint64_t>(D / 64),
+                              static_cast<cuuint64_t>(Hkv)};
+  const cuuint64_t strides[3] = {static_cast<cuuint64_t>(Hkv) * D * 2, 128,
+                                 static_cast<cuuint64_t>(D) * 2};
+  const cuuint32_t box[4] = {64, kPage, static_cast<cuuint32_t>(D / 64), 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims,
+                  strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return cuda_fail(cudaErrorInvalidValue);
+  return CSP_OK;
+}
+
 // Plain (unswizzled) tiled map of `rank` dims: the decode schedule's merge reads its
 // workspace slots through these.
 int make_map_plain(CUtensorMap* map, CUtensorMapDataType type, uint32_t rank, const void* base,
@@ -344,10 +364,8 @@ int attention_call(const void* q, const void* k_cache, const void* v_cache, int3
     const uint64_t ntok = static_cast<uint64_t>(num_blocks) * block_size;
     if ((st = make_map_3d(&tm_q, q, D, Hq, total_q, row_b, row_b * Hq, 64, P.group,
                           128 / P.group)) != CSP_OK ||
-        (st = make_map_3d(&tm_k, k_cache, D, Hkv, ntok, row_b, row_b * Hkv, 64, 1, kPage)) !=
-            CSP_OK ||
-        (st = make_map_3d(&tm_v, v_cache, D, Hkv, ntok, row_b, row_b * Hkv, 64, 1, kPage)) !=
-            CSP_OK)
+        (st = make_map_kv_pages(&tm_k, k_cache, D, Hkv, ntok)) != CSP_OK ||
+        (st = make_map_kv_pages(&tm_v, v_cache, D, Hkv, ntok)) != CSP_OK)
       return st;
     csp::DecodeArgs da;
     csp::PrefixArgs& pa = da.pre;

@@ -47,8 +47,7 @@ static_assert(kThreads == 320, "ten warps: 8 softmax/streaming, MMA/scheduler, T
 template <int D>
 struct SLayout {
   static constexpr int kHalves = D / 64;
-  static constexpr int kKVHalf = kKeys * 128;    // 64 keys x 64 features (128 B rows)
-  static constexpr int kKV = kHalves * kKVHalf;  // one K (or V) stage
+  static constexpr int kKV = kKeys * D * 2;  // one K (or V) stage: [page][half][16 keys][128 B]
   static constexpr int kQHalf = kRows * 128;
   static constexpr int kQ = kHalves * kQHalf;
   static constexpr int kStage = 2 * kKV + kQ;    // K, V, then Q
@@ -76,6 +75,14 @@ __device__ __forceinline__ uint32_t sw128(int row, int c) {
                                (((c & 7) ^ (row & 7)) << 4));
 }
 
+// The same for a K or V stage as the page boxes leave it: [page][half][16 keys][128 B]
+// (one box per page brings both feature halves), swizzled by the row's index.
+template <int D>
+__device__ __forceinline__ uint32_t kv_off(int key, int c) {
+  const int r = (key >> 4) * (16 * (D / 64)) + (c >> 3) * 16 + (key & 15);
+  return static_cast<uint32_t>(r * 128 + (((c & 7) ^ (r & 7)) << 4));
+}
+
 __device__ __forceinline__ unsigned ld_acquire_gpu_u32(const unsigned* p) {
   unsigned v;
   asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
@@ -98,8 +105,8 @@ __device__ __forceinline__ void stream_sync() {
 // go through a ring of kSlots in shared memory:
 //  * warp 8 produces them.  It walks the CTA's units (see unit_range), reads each
 //    request's query range, length and block ids (lane j the id of the item's page j,
-//    one item ahead), and fills a free slot: every lane issues one TMA page box
-//    (64 features x 16 tokens of one KV head) of the item's K or V, and the lanes copy
+//    one item ahead), and fills a free slot: lane j < 16 issues one TMA box of the
+//    item's K or V (one page of one KV head, both feature halves), and the lanes copy
 //    the Q rows with 16-byte cp.async (rows past the unit's are zero-filled without a
 //    read).  A page past the request re-reads the item's first page (its keys are
 //    masked); the item's descriptor tells the consumers which unit and tiles it holds.
@@ -143,7 +150,7 @@ __device__ __forceinline__ void produce_items(const DecodeArgs& a, const CUtenso
   using L = SLayout<D>;
   constexpr int kS = L::kSlots;
   constexpr int kChunks = D / 8;
-  constexpr int kBoxesPerTile = kTilePages * 2 * L::kHalves;  // pages x {K, V} x halves
+  constexpr int kBoxesPerTile = kTilePages * 2;  // pages x {K, V}, both feature halves each
   static_assert(2 * kBoxesPerTile <= 32, "one box per lane");
   const PrefixArgs& p = a.pre;
   const int lane = threadIdx.x & 31;
@@ -214,16 +221,15 @@ __device__ __forceinline__ void produce_items(const DecodeArgs& a, const CUtenso
       }
       {
         const int h = lane / kBoxesPerTile, rem = lane % kBoxesPerTile;
-        const int q = rem / (2 * L::kHalves), kv = (rem / L::kHalves) & 1, hf = rem % L::kHalves;
+        const int q = rem >> 1, kv = rem & 1;
         const int pq = (h * kTilePages + q) & (2 * kTilePages - 1);
         const int id_q = __shfl_sync(0xffffffffu, ids, pq);
         const int id_0 = __shfl_sync(0xffffffffu, ids, 0);
         const int page = page0 + t0 * kTilePages + pq;
         const int blk = page < npages ? id_q : id_0;
         if (lane < tiles * kBoxesPerTile) {
-          uint8_t* dst = ring + slot * L::kItem + h * L::kStage + kv * L::kKV +
-                         hf * L::kKVHalf + q * (kPage * 128);
-          tma_load_3d(dst, kv ? tm_v : tm_k, &st_full[slot], hf * 64, kvh, blk * kPage);
+          uint8_t* dst = ring + slot * L::kItem + h * L::kStage + kv * L::kKV + q * (kPage * D * 2);
+          tma_load_4d(dst, kv ? tm_v : tm_k, &st_full[slot], 0, blk * kPage, 0, kvh);
         }
       }
       if (t0 == 0 && !end) {
@@ -316,7 +322,7 @@ __device__ __forceinline__ void consume_items(const DecodeArgs& a, uint8_t* ring
           const int k = x / kChunks, c = x % kChunks;
           if (key0 + k >= c_seq)
             asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(
-                             vb + sw128<kKeys>(kw0 + k, c)), "r"(0u)
+                             vb + kv_off<D>(kw0 + k, c)), "r"(0u)
                          : "memory");
         }
         __syncwarp();
@@ -330,7 +336,7 @@ __device__ __forceinline__ void consume_items(const DecodeArgs& a, uint8_t* ring
         const int key = kw0 + (lane & 7) + (lane >> 4) * 8;
         const int c = kk * 2 + ((lane >> 3) & 1);
         uint32_t b0, b1, b2, b3;
-        ldmatrix_x4(kb + sw128<kKeys>(key, c), b0, b1, b2, b3);
+        ldmatrix_x4(kb + kv_off<D>(key, c), b0, b1, b2, b3);
         mma_bf16_16816(sacc[0], qa[kk], b0, b1);
         mma_bf16_16816(sacc[1], qa[kk], b2, b3);
       }
@@ -387,7 +393,7 @@ __device__ __forceinline__ void consume_items(const DecodeArgs& a, uint8_t* ring
         const int key = kw0 + (lane & 7) + ((lane >> 3) & 1) * 8;
         const int c = dp * 2 + (lane >> 4);
         uint32_t b0, b1, b2, b3;
-        ldmatrix_x4_trans(vb + sw128<kKeys>(key, c), b0, b1, b2, b3);
+        ldmatrix_x4_trans(vb + kv_off<D>(key, c), b0, b1, b2, b3);
         mma_bf16_16816(o[2 * dp], pa, b0, b1);
         mma_bf16_16816(o[2 * dp + 1], pa, b2, b3);
       }
