@@ -166,19 +166,31 @@ void make_plan(int num_reqs, int total_q, int max_q, int max_k, int cpl, int Hq,
                int sms, LaunchPlan* P, int sched_override = -1, int ranges_override = 0) {
   LaunchPlan p;
   p.group = Hq / Hkv;
+  p.decode = static_cast<int64_t>(max_q) * p.group <= 16;
+  p.tc = !p.decode;
+  const int max_len = std::max(0, max_k - cpl);
   if (cpl > 0) {
     const int rows = total_q * p.group;
     p.p_pairs = cdiv(rows, 256);
     const int key_tiles = cdiv(cpl, 64);
     const int base = p.p_pairs * Hkv;
-    // key ranges by waves x per-CTA length (+3 tiles of fixed cost: set-up, the
-    // partial write-out and the row-group merge); a prefix CTA takes a whole SM
-    int64_t best_cost = -1;
+    // Key ranges per (256-row block, KV head).  The suffix kernel runs on the SMs the
+    // prefix leaves free, so the call takes about max(the prefix's waves x a CTA's
+    // time, (prefix + suffix SM time) / SMs).  A prefix CTA costs its tiles plus ~3
+    // tiles of fixed cost (set-up, the partial write-out) at ~1.22 us each; the suffix
+    // streams half its longest range on average at ~32 GB/s per SM, plus ~5 us per CTA
+    // of the tcgen05 variant.  More ranges also mean more slots for the suffix to merge.
+    const double tile_us = 1.22;
+    const double suf_bytes = static_cast<double>(num_reqs) * Hkv * (0.5 * max_len + 64.0) * 4.0 * D;
+    const double suf_sm_us =
+        suf_bytes / 32e3 + (p.tc ? 5.0 * num_reqs * Hkv * cdiv(max_q * p.group, 256) : 0.0);
+    double best_cost = -1.0;
     for (int s = 1; s <= 16; s *= 2) {
       if (s > 1 && s > key_tiles) break;
       const int64_t ctas = static_cast<int64_t>(base) * s;
-      const int64_t cost = cdiv64(ctas, sms) * (cdiv(key_tiles, s) + 3);
-      if (best_cost < 0 || cost < best_cost) {
+      const double cta_us = (cdiv(key_tiles, s) + 3) * tile_us;
+      const double cost = std::max(cdiv64(ctas, sms) * cta_us, (ctas * cta_us + suf_sm_us) / sms);
+      if (best_cost < 0.0 || cost < best_cost) {
         best_cost = cost;
         p.p_splits = s;
       }
@@ -186,11 +198,8 @@ void make_plan(int num_reqs, int total_q, int max_q, int max_k, int cpl, int Hq,
     p.p_tiles_per_split = cdiv(key_tiles, p.p_splits);
     p.p_slots = p.p_splits;
   }
-  p.decode = static_cast<int64_t>(max_q) * p.group <= 16;
-  p.tc = !p.decode;
   const int rows_per_cta = p.decode ? 16 : 256;
   p.s_row_tiles = std::max(1, cdiv(max_q * p.group, rows_per_cta));
-  const int max_len = std::max(0, max_k - cpl);
   const int key_tiles = std::max(1, cdiv(max_len, 64));
   const int64_t units = static_cast<int64_t>(num_reqs) * p.s_row_tiles * Hkv;
   const int max_s = std::min(kMaxSplits, 32 - p.p_slots);

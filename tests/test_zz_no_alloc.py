@@ -64,7 +64,10 @@ def test_noalloc_matches_cascade_attn_on_consecutive_calls():
 
 def test_noalloc_rejects_a_batch_beyond_its_array():
     fn = _noalloc_fn()
-    b = workloads.chunked_prefill()              # ~1000 query tokens x 32 heads
+    # 64 requests x 64 new tokens x 32 heads: two partial slots of 131,072 rows
+    g = torch.Generator().manual_seed(77)
+    b = workloads.build_batch("wide", [320] * 64, [64] * 64, 256, num_q_heads=32,
+                              num_kv_heads=8, head_dim=128, gen=g)
     cpl, _ = H.plan(b)
     need = csp.workspace_size(b.num_reqs, b.total_q, b.max_seqlen_q, b.max_seqlen_k, cpl,
                               b.num_q_heads, b.num_kv_heads, b.head_dim)
