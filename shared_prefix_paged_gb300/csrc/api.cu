@@ -368,13 +368,15 @@ int attention_call(const void* q, const void* k_cache, const void* v_cache, int3
     return events ? cudaEventRecord(static_cast<cudaEvent_t>(events[i]), stream) : cudaSuccess;
   };
   if (P.single) {
-    CUtensorMap tm_q, tm_k, tm_v;
+    CUtensorMap tm_q, tm_k, tm_v, tm_kp;
     const uint64_t row_b = static_cast<uint64_t>(D) * 2;
     const uint64_t ntok = static_cast<uint64_t>(num_blocks) * block_size;
     if ((st = make_map_3d(&tm_q, q, D, Hq, total_q, row_b, row_b * Hq, 64, P.group,
                           128 / P.group)) != CSP_OK ||
         (st = make_map_kv_pages(&tm_k, k_cache, D, Hkv, ntok)) != CSP_OK ||
-        (st = make_map_kv_pages(&tm_v, v_cache, D, Hkv, ntok)) != CSP_OK)
+        (st = make_map_kv_pages(&tm_v, v_cache, D, Hkv, ntok)) != CSP_OK ||
+        (st = make_map_3d(&tm_kp, k_cache, D, Hkv, ntok, row_b, row_b * Hkv, 64, 1, kPage)) !=
+            CSP_OK)
       return st;
     csp::DecodeArgs da;
     csp::PrefixArgs& pa = da.pre;
@@ -431,7 +433,8 @@ int attention_call(const void* q, const void* k_cache, const void* v_cache, int3
     da.lse = lse;
     // phase events: [0] before the kernel, [1..3] after it
     if ((e = mark(0)) != cudaSuccess) return cuda_fail(e);
-    if ((e = csp::launch_decode(D, tm_q, tm_k, tm_v, tm_po, tm_pl, da, P.d_grid, stream)) !=
+    if ((e = csp::launch_decode(D, tm_q, tm_k, tm_v, tm_kp, tm_po, tm_pl, da, P.d_grid,
+                                stream)) !=
         cudaSuccess)
       return cuda_fail(e);
     for (int i = 1; i < 4; ++i)
@@ -456,9 +459,7 @@ int attention_call(const void* q, const void* k_cache, const void* v_cache, int3
     if ((st = make_map_3d(&tm_k, k_cache, D, Hkv, ntok, row_b, row_b * Hkv, 64, 1, kPage)) !=
         CSP_OK)
       return st;
-    if ((st = make_map_3d(&tm_v, v_cache, D, Hkv, ntok, row_b, row_b * Hkv, 64, 1, kPage)) !=
-        CSP_OK)
-      return st;
+    if ((st = make_map_kv_pages(&tm_v, v_cache, D, Hkv, ntok)) != CSP_OK) return st;
     csp::PrefixArgs pa;
     pa.k = static_cast<const __nv_bfloat16*>(k_cache);
     pa.v = static_cast<const __nv_bfloat16*>(v_cache);
@@ -510,12 +511,16 @@ int attention_call(const void* q, const void* k_cache, const void* v_cache, int3
   // events sit between the two
   const bool overlap = cpl > 0 && events == nullptr;
   if (P.tc) {
-    CUtensorMap tm_q;
+    CUtensorMap tm_q, tm_k, tm_v;
     const uint64_t row_b = static_cast<uint64_t>(D) * 2;
+    const uint64_t ntok = static_cast<uint64_t>(num_blocks) * block_size;
     if ((st = make_map_3d(&tm_q, q, D, Hq, total_q, row_b, row_b * Hq, 64, P.group,
-                          128 / P.group)) != CSP_OK)
+                          128 / P.group)) != CSP_OK ||
+        (st = make_map_3d(&tm_k, k_cache, D, Hkv, ntok, row_b, row_b * Hkv, 64, 1, kPage)) !=
+            CSP_OK ||
+        (st = make_map_kv_pages(&tm_v, v_cache, D, Hkv, ntok)) != CSP_OK)
       return st;
-    e = csp::launch_paged_tc(D, tm_q, ga, overlap, stream);
+    e = csp::launch_paged_tc(D, tm_q, tm_k, tm_v, ga, overlap, stream);
   } else {
     e = csp::launch_paged(D, P.decode, ga, overlap, stream);
   }

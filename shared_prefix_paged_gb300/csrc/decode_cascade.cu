@@ -32,7 +32,7 @@
 namespace csp {
 namespace {
 
-constexpr int kThreads = prefix::kThreads;  // 320: ten warps
+constexpr int kThreads = prefix::kThreads;  // 352: eleven warps
 constexpr int kKeys = 64;                   // keys per suffix stage
 constexpr int kPage = 16;
 constexpr int kTilePages = kKeys / kPage;
@@ -42,7 +42,7 @@ constexpr int kStreamThreads = 32 * kStreamWarps;
 constexpr int kWarpScheduler = 8;           // produces the suffix items
 constexpr int kMergeBarOff = 512;           // merge barrier within the suffix barrier area
 
-static_assert(kThreads == 320, "ten warps: 8 softmax/streaming, MMA/scheduler, TMA");
+static_assert(kThreads == 352, "eleven warps: 8 softmax/streaming, 2 MMA (one the scheduler), loader");
 
 template <int D>
 struct SLayout {
@@ -520,7 +520,7 @@ __device__ __forceinline__ void merge_rows_staged(const DecodeArgs& a, const CUt
     }
     const bool ok = mbar_wait(bar, phase, abort_flag, p.status);
     const int lo = static_cast<int>(c0) - l0;
-    // pass k takes rows 2 (warp + 10 k) + {0, 1}
+    // half-warp h takes rows h, h + kThreads / 16, ...
     for (int base = 2 * (hw >> 1); base < m; base += kThreads / 16) {
       const int i = base + (hw & 1);
       const bool in = ok && i < m;
@@ -586,6 +586,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     decode_cascade_kernel(const __grid_constant__ CUtensorMap tm_q,
                           const __grid_constant__ CUtensorMap tm_k,
                           const __grid_constant__ CUtensorMap tm_v,
+                          const __grid_constant__ CUtensorMap tm_kp,
                           const __grid_constant__ CUtensorMap tm_po,
                           const __grid_constant__ CUtensorMap tm_pl, const DecodeArgs a) {
   using L = SLayout<D>;
@@ -602,6 +603,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefetch_tensormap(&tm_k);
     prefetch_tensormap(&tm_v);
     prefetch_tensormap(&tm_q);
+    prefetch_tensormap(&tm_kp);
     prefetch_tensormap(&tm_po);
     prefetch_tensormap(&tm_pl);
   }
@@ -614,7 +616,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int kvh = b / (p.n_splits * p.pairs);
     const int t_first = split * a.key_tiles / p.n_splits;
     const int t_last = (split + 1) * a.key_tiles / p.n_splits;
-    prefix::prefix_range<D>(&tm_q, &tm_k, &tm_v, p, prefix::prefix_geom(p, pair), kvh, split,
+    prefix::prefix_range<D>(&tm_q, &tm_kp, &tm_v, p, prefix::prefix_geom(p, pair), kvh, split,
                             t_first, t_last, smem,
                             reinterpret_cast<uint64_t*>(smem + L::kPrefixBars));
     // the staging buffer was read through the generic proxy and TMA wrote the stages;
@@ -689,7 +691,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <int D>
 cudaError_t launch_decode_d(const CUtensorMap& tm_q, const CUtensorMap& tm_k,
-                            const CUtensorMap& tm_v, const CUtensorMap& tm_po,
+                            const CUtensorMap& tm_v, const CUtensorMap& tm_kp,
+                            const CUtensorMap& tm_po,
                             const CUtensorMap& tm_pl, const DecodeArgs& a, int grid,
                             cudaStream_t stream) {
   static std::atomic<uint64_t> attr_done{0};
@@ -706,17 +709,19 @@ cudaError_t launch_decode_d(const CUtensorMap& tm_q, const CUtensorMap& tm_k,
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, decode_cascade_kernel<D>, tm_q, tm_k, tm_v, tm_po, tm_pl, a);
+  return cudaLaunchKernelEx(&cfg, decode_cascade_kernel<D>, tm_q, tm_k, tm_v, tm_kp, tm_po,
+                            tm_pl, a);
 }
 
 }  // namespace
 
 cudaError_t launch_decode(int head_dim, const CUtensorMap& tm_q, const CUtensorMap& tm_k,
-                          const CUtensorMap& tm_v, const CUtensorMap& tm_po,
-                          const CUtensorMap& tm_pl, const DecodeArgs& a, int grid,
-                          cudaStream_t stream) {
-  if (head_dim == 64) return launch_decode_d<64>(tm_q, tm_k, tm_v, tm_po, tm_pl, a, grid, stream);
-  return launch_decode_d<128>(tm_q, tm_k, tm_v, tm_po, tm_pl, a, grid, stream);
+                          const CUtensorMap& tm_v, const CUtensorMap& tm_kp,
+                          const CUtensorMap& tm_po, const CUtensorMap& tm_pl,
+                          const DecodeArgs& a, int grid, cudaStream_t stream) {
+  if (head_dim == 64)
+    return launch_decode_d<64>(tm_q, tm_k, tm_v, tm_kp, tm_po, tm_pl, a, grid, stream);
+  return launch_decode_d<128>(tm_q, tm_k, tm_v, tm_kp, tm_po, tm_pl, a, grid, stream);
 }
 
 }  // namespace csp

@@ -98,8 +98,12 @@ struct DecodeArgs {
 // tm_po / tm_pl: the workspace slots as bf16 [n_splits + 1][rows][D] and fp32
 // [n_splits + 1][pre.lse_stride], boxes of merge_rows rows (and of
 // (merge_rows + 6) & ~3 LSEs).
+// tm_k / tm_v: the K / V cache as pages of one KV head with both feature halves
+// (boxes {64, 16, D / 64, 1} of {64, tokens, D / 64, Hkv}); tm_kp: K as {D, Hkv,
+// tokens} with boxes {64, 1, 16}, for the prefix ranges.
 cudaError_t launch_decode(int head_dim, const CUtensorMap& tm_q, const CUtensorMap& tm_k,
-                          const CUtensorMap& tm_v, const CUtensorMap& tm_po,
+                          const CUtensorMap& tm_v, const CUtensorMap& tm_kp,
+                          const CUtensorMap& tm_po,
                           const CUtensorMap& tm_pl, const DecodeArgs& a, int grid,
                           cudaStream_t stream);
 
@@ -114,9 +118,11 @@ cudaError_t launch_paged(int head_dim, bool decode, const PagedArgs& a, bool aft
 // The same computation on tcgen05 for units of many rows (paged_tc.cu): one CTA per
 // (request, KV head, 256-row tile, key split); a.row_tiles counts 256-row tiles.
 // tm_q: q as bf16 [total_q][num_q_heads][D], boxes of 64 features x group heads x
-// 128 / group tokens.
-cudaError_t launch_paged_tc(int head_dim, const CUtensorMap& tm_q, const PagedArgs& a,
-                            bool after_prefix, cudaStream_t stream);
+// 128 / group tokens; tm_k: K as {D, Hkv, tokens}, boxes {64, 1, 16}; tm_v: V as
+// {64, tokens, D / 64, Hkv}, boxes {64, 16, D / 64, 1}.
+cudaError_t launch_paged_tc(int head_dim, const CUtensorMap& tm_q, const CUtensorMap& tm_k,
+                            const CUtensorMap& tm_v, const PagedArgs& a, bool after_prefix,
+                            cudaStream_t stream);
 
 cudaError_t launch_merge_states(__nv_bfloat16* out, float* out_lse, const void* o1,
                                 const float* l1, const void* o2, const float* l2, int rows,

@@ -6,7 +6,7 @@
 //
 // A CTA owns up to 256 packed rows (query, head-in-group) of one request and one KV
 // head, and one key split.  Its main loop is the prefix phase's (prefix_body.cuh):
-// pages by 16-byte cp.async into a 4-deep ring of 64-key tiles, S = Q K^T and
+// pages by TMA into a 4-deep ring of 64-key tiles, S = Q K^T and
 // O += P V on tcgen05 with TMEM accumulators, the online softmax one TMEM lane (row)
 // per thread.  Here each row also stops at its causal limit: query i of a request
 // with q_len queries and seq_len keys sees keys <= seq_len - q_len + i (bottom-right
@@ -33,7 +33,9 @@ constexpr int kDynamic = Layout<D>::kData + prefix::kBarBytes + 1024;
 
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
-    paged_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const PagedArgs a) {
+    paged_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
+                    const __grid_constant__ CUtensorMap tm_k,
+                    const __grid_constant__ CUtensorMap tm_v, const PagedArgs a) {
   using L = Layout<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -86,7 +88,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   geo.prow0 = prow0;
   geo.rows_total = rows_total;
   geo.causal_base = seq - q_len;
-  prefix::prefix_range<D, true>(&tm_q, &tm_q, &tm_q, pa, geo, g, split, 0, ntiles, smem, bars);
+  prefix::prefix_range<D, true>(&tm_q, &tm_k, &tm_v, pa, geo, g, split, 0, ntiles, smem, bars);
 
   // 256 normalised rows (bf16) and their log2-sum-exp are staged and visible
   const __nv_bfloat16* stage = reinterpret_cast<const __nv_bfloat16*>(smem);
@@ -160,7 +162,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 template <int D>
-cudaError_t launch_tc_t(const CUtensorMap& tm_q, const PagedArgs& a, bool after_prefix,
+cudaError_t launch_tc_t(const CUtensorMap& tm_q, const CUtensorMap& tm_k,
+                        const CUtensorMap& tm_v, const PagedArgs& a, bool after_prefix,
                         cudaStream_t stream) {
   static std::atomic<uint64_t> attr_done{0};
   cudaError_t e = set_smem_once(paged_tc_kernel<D>, kDynamic<D>, attr_done);
@@ -177,15 +180,16 @@ cudaError_t launch_tc_t(const CUtensorMap& tm_q, const PagedArgs& a, bool after_
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = after_prefix ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, paged_tc_kernel<D>, tm_q, a);
+  return cudaLaunchKernelEx(&cfg, paged_tc_kernel<D>, tm_q, tm_k, tm_v, a);
 }
 
 }  // namespace
 
-cudaError_t launch_paged_tc(int head_dim, const CUtensorMap& tm_q, const PagedArgs& a,
-                            bool after_prefix, cudaStream_t stream) {
-  if (head_dim == 64) return launch_tc_t<64>(tm_q, a, after_prefix, stream);
-  return launch_tc_t<128>(tm_q, a, after_prefix, stream);
+cudaError_t launch_paged_tc(int head_dim, const CUtensorMap& tm_q, const CUtensorMap& tm_k,
+                            const CUtensorMap& tm_v, const PagedArgs& a, bool after_prefix,
+                            cudaStream_t stream) {
+  if (head_dim == 64) return launch_tc_t<64>(tm_q, tm_k, tm_v, a, after_prefix, stream);
+  return launch_tc_t<128>(tm_q, tm_k, tm_v, a, after_prefix, stream);
 }
 
 }  // namespace csp

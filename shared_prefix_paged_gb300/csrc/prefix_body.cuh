@@ -11,16 +11,18 @@
 //  * a CTA owns 256 packed rows (token, head-in-group) of ONE KV head as two 128-row
 //    M tiles, so every K/V byte staged into shared memory serves 256 query rows and
 //    all the GQA heads of that KV head;
-//  * K and V pages (16 tokens x 64 features per box, 128-byte swizzle) are staged by
-//    TMA into a 4-deep ring of 64-key tiles;
+//  * warp 10 stages K and V by TMA into a 4-deep ring of 64-key tiles (128-byte
+//    swizzle): K as [feature half][64 keys][128 B] (one box per page and half), V as
+//    [page][feature half][16 keys][128 B] (one box per page); it alone waits for free
+//    stages, so the softmax warps never issue copies;
 //  * per M tile, S = Q K^T (M=128, N=64) goes into one of two TMEM buffers, so the
 //    tensor core computes S(i+1) while the softmax works on S(i); P (bf16) is
 //    written back into the S buffer and used from TMEM as the A operand of
 //    O += P V (N = D).  The two M tiles use all 512 TMEM columns;
 //  * two softmax warpgroups (one per M tile) own one TMEM lane (row) per thread:
 //    online softmax in base 2 on the special-function unit, O rescaled in TMEM only
-//    when the running max grows by more than 2^8; warp 8 issues the MMAs, warp 9
-//    the TMA loads;
+//    when the running max grows by more than 2^8; warps 8 and 9 issue the MMAs (one
+//    per M tile), warp 9 also the Q load;
 //  * a CTA covers one range of the prefix's key tiles and stages its normalised rows
 //    (bf16) through shared memory, then writes them, coalesced, into workspace slot
 //    `split`, with the log2-sum-exp of each row beside them; a later merge
@@ -39,10 +41,10 @@ constexpr int kKeysN = 64;     // keys per tile
 constexpr int kPage = 16;      // tokens per KV page
 constexpr int kPagesPerTile = kKeysN / kPage;
 constexpr int kStages = 4;
-constexpr int kThreads = 320;  // 2 softmax warpgroups, MMA warp, TMA warp
+constexpr int kThreads = 352;  // 2 softmax warpgroups, two MMA issuers, the K/V loader
 constexpr int kWarpMma = 8;
-constexpr int kWarpTma = 9;
-constexpr int kLoaders = 256;  // warps 0-7 load K/V
+constexpr int kWarpTma = 9;    // Q by TMA, then the MMA issuer of M tile 1
+constexpr int kWarpLoad = 10;  // K and V by TMA
 template <int D>
 struct Layout {
   static constexpr int kHalves = D / 64;
@@ -50,6 +52,7 @@ struct Layout {
   static constexpr int kKVHalf = kKeysN * 128;          // 64 keys x 64 bf16
   static constexpr int kQTile = kHalves * kQHalf;       // one M tile of Q
   static constexpr int kKVBytes = kHalves * kKVHalf;    // one K (or V) tile
+  static constexpr int kVPage = kPage * D * 2;          // one page of V: both halves
   static constexpr int kQ = 0;                          // [2 M tiles][halves]
   static constexpr int kK0 = kQ + 2 * kQTile;
   static constexpr int kV0 = kK0 + kStages * kKVBytes;
@@ -117,6 +120,9 @@ __device__ __forceinline__ bool wg_bar_any(int id, bool pred) {
 // and the CTA stops once its 256 normalised rows (bf16, [row][Layout::kStageRow] at
 // smem) and their log2-sum-exp (float [256] at smem + Layout::kLse; -inf for a row
 // that saw no key) are staged and visible to every thread: the caller writes them.
+// tm_k: the K cache as {D, Hkv, tokens} with boxes {64, 1, 16} (one page, one half);
+// tm_v: the V cache as {64, tokens, D / 64, Hkv} with boxes {64, 16, D / 64, 1} (one
+// page, both halves); both with the 128-byte swizzle.
 template <int D, bool kCausal = false>
 __device__ __forceinline__ void prefix_range(const CUtensorMap* tm_q_p,
                                              const CUtensorMap* tm_k_p,
@@ -154,7 +160,7 @@ __device__ __forceinline__ void prefix_range(const CUtensorMap* tm_q_p,
   if (threadIdx.x == 0) {
     mbar_init(bar_q, 1);
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(&kv_full[s], kLoaders);  // one cp.async arrival per loader thread
+      mbar_init(&kv_full[s], 1);  // the loader's expect_tx; the TMA bytes complete it
       mbar_init(&kv_empty[s], has_m1 ? 2 : 1);  // one commit per M tile's issuer
     }
     for (int b = 0; b < 4; ++b) {
@@ -219,9 +225,6 @@ __device__ __forceinline__ void prefix_range(const CUtensorMap* tm_q_p,
       bool progressed = false;
       if (next_s < ntiles && next_s <= next_pv + 1 &&
           mbar_test_wait(&kv_full[next_s % kStages], (next_s / kStages) & 1)) {
-        // the tile was written by cp.async (generic proxy); the MMAs read it through
-        // the async proxy
-        fence_proxy_async_smem();
         tc_fence_after();
         issue_s(next_s);
         ++next_s;
@@ -234,9 +237,9 @@ __device__ __forceinline__ void prefix_range(const CUtensorMap* tm_q_p,
         const uint32_t v_addr = smem_u32(smem + L::kV0 + (i % kStages) * L::kKVBytes);
         const uint32_t p_tmem = tm + (i & 1) * kKeysN;
 #pragma unroll
-        for (int kk = 0; kk < kKeysN / 16; ++kk)
+        for (int kk = 0; kk < kKeysN / 16; ++kk)  // 16 keys = one page of V
           umma_bf16_tmem_a(tm + 2 * kKeysN, p_tmem + kk * 8,
-                           umma_desc_sw128(v_addr + kk * 16 * 128, L::kKVHalf, 1024), kIdO,
+                           umma_desc_sw128(v_addr + kk * L::kVPage, kPage * 128, 1024), kIdO,
                            (i > 0 || kk > 0) ? 1u : 0u);
         if (i == ntiles - 1) umma_commit(&o_last[m]);
         umma_commit(&kv_empty[i % kStages]);
@@ -259,6 +262,64 @@ __device__ __forceinline__ void prefix_range(const CUtensorMap* tm_q_p,
       }
     }
   }
+  // ------------------------------------------------------- K/V loader (TMA) --
+  // Tile j goes into stage j % kStages once PV(j - kStages) of every M tile is done.
+  // Lane l holds the block id of page l % 4 of tile l / 4 of a window of eight tiles,
+  // read a window ahead.  A page wholly past the range is loaded from an out-of-range
+  // token coordinate: TMA fills it with zeros (no NaN from a page the cache never
+  // wrote can reach O).
+  if (warp == kWarpLoad && ntiles > 0) {
+    constexpr int kIdTiles = 32 / kPagesPerTile;
+    constexpr int kKBoxes = kPagesPerTile * L::kHalves;
+    const int npages = (geo.key_end - geo.key0 + kPage - 1) / kPage;
+    const int32_t* bt_pages = geo.bt + geo.key0 / kPage;
+    auto load_ids = [&](int i_base) {
+      const int i = i_base + lane / kPagesPerTile;
+      const int page = tile_of(i) * kPagesPerTile + (lane & (kPagesPerTile - 1));
+      return i < ntiles && page < npages ? __ldg(bt_pages + page) : -1;
+    };
+    int ids_cur = load_ids(0);
+    int ids_nxt = ntiles > kIdTiles ? load_ids(kIdTiles) : -1;
+    int issued = 0;
+    for (int j = 0; j < ntiles; ++j) {
+      const int st = j % kStages;
+      if (j >= kStages &&
+          !warp_mbar_wait(&kv_empty[st], ((j / kStages) - 1) & 1, abort_flag, a.status))
+        break;
+      if (j > 0 && j % kIdTiles == 0) {
+        ids_cur = ids_nxt;
+        ids_nxt = j + kIdTiles < ntiles ? load_ids(j + kIdTiles) : -1;
+      }
+      if (lane == 0) mbar_arrive_expect_tx(&kv_full[st], 2 * L::kKVBytes);
+      __syncwarp();
+      // lanes [0, kKBoxes): K page lane / halves, half lane % halves; then one lane per
+      // page of V
+      const bool is_k = lane < kKBoxes;
+      const int q = is_k ? lane / L::kHalves : lane - kKBoxes;
+      const int blk = __shfl_sync(0xffffffffu, ids_cur, ((j % kIdTiles) * kPagesPerTile + q) & 31);
+      const int tok = blk >= 0 ? blk * kPage : -kPage;  // -16: a box of zeros
+      if (is_k) {
+        const int h = lane % L::kHalves;
+        tma_load_3d(smem + L::kK0 + st * L::kKVBytes + h * L::kKVHalf + q * (kPage * 128),
+                    &tm_k, &kv_full[st], h * 64, kvh, tok);
+      } else if (lane < kKBoxes + kPagesPerTile) {
+        tma_load_4d(smem + L::kV0 + st * L::kKVBytes + q * L::kVPage, &tm_v, &kv_full[st], 0,
+                    tok, 0, kvh);
+      }
+      issued = j + 1;
+    }
+    // after a failure the last tiles' copies may still be landing: they must land
+    // before this CTA's shared memory is reused or released (a bounded wait each)
+    if (lane == 0) {
+      for (int j = issued > kStages ? issued - kStages : 0; j < issued; ++j) {
+        const long long c0 = clock64();
+        while (!mbar_try_wait(&kv_full[j % kStages], (j / kStages) & 1) &&
+               clock64() - c0 < kWaitLimitCycles) {
+        }
+      }
+    }
+    __syncwarp();
+  }
   if (warp >= 8) __syncwarp();
 
   // --------------------------------------------------------------- softmax --
@@ -271,57 +332,6 @@ __device__ __forceinline__ void prefix_range(const CUtensorMap* tm_q_p,
   bool have = false;
   const bool softmax_warp = warp < 8 && (wg == 0 || has_m1);
   if (warp < 8) {
-    // ---- K/V loads: the 256 threads of warps 0-7 issue 16-byte cp.async into the
-    // 128-byte-swizzled stages (the layout the MMA descriptors expect); each thread's
-    // arrival on the stage's full barrier fires once its copies have landed.  Tile
-    // i + kStages - 1 goes into the stage of tile i - 1 once PV(i - 1) is done and
-    // the thread's warp has handed P(i) over.
-    constexpr int kChunks = D / 8;
-    constexpr int kPer = kKeysN * kChunks / kLoaders;
-    const int lt = threadIdx.x;  // loader thread
-    // Block ids of the range's pages, 32 at a time (eight tiles; lane l holds page
-    // l % 4 of tile l / 4 of the window), read a window ahead of use.  Keys past the
-    // range are zero-filled without a read.
-    constexpr int kIdTiles = 32 / kPagesPerTile;
-    const int npages = (geo.key_end - geo.key0 + kPage - 1) / kPage;
-    const int32_t* bt_pages = geo.bt + geo.key0 / kPage;
-    auto load_ids = [&](int i_base) {
-      const int i = i_base + lane / kPagesPerTile;
-      const int page = tile_of(i) * kPagesPerTile + (lane & (kPagesPerTile - 1));
-      return i < ntiles && page < npages ? __ldg(bt_pages + page) : 0;
-    };
-    int ids_cur = ntiles > 0 ? load_ids(0) : 0;
-    int ids_nxt = ntiles > kIdTiles ? load_ids(kIdTiles) : 0;
-    const uint32_t k_ring = smem_u32(smem + L::kK0);
-    const uint32_t v_ring = smem_u32(smem + L::kV0);
-    auto issue_tile = [&](int j) {  // tiles are issued in order 0, 1, 2, ...
-      if (j > 0 && j % kIdTiles == 0) {
-        ids_cur = ids_nxt;
-        ids_nxt = j + kIdTiles < ntiles ? load_ids(j + kIdTiles) : 0;
-      }
-      const int st = j % kStages;
-      const int key0 = geo.key0 + tile_of(j) * kKeysN;
-      const int w0 = (j % kIdTiles) * kPagesPerTile;
-      int blk[kPagesPerTile];
-#pragma unroll
-      for (int q = 0; q < kPagesPerTile; ++q) blk[q] = __shfl_sync(0xffffffffu, ids_cur, w0 + q);
-#pragma unroll
-      for (int q = 0; q < kPer; ++q) {
-        const int x = lt + kLoaders * q;
-        const int key = x / kChunks, c = x % kChunks;
-        const int pq = key >> 4;
-        const int b = pq == 0 ? blk[0] : pq == 1 ? blk[1] : pq == 2 ? blk[2] : blk[3];
-        const bool in = key0 + key < geo.key_end;
-        const int64_t off =
-            ((static_cast<int64_t>(b) * kPage + (key & 15)) * a.num_kv_heads + kvh) * D + c * 8;
-        const uint32_t o = static_cast<uint32_t>(st * L::kKVBytes + (c >> 3) * L::kKVHalf +
-                                                 key * 128 + (((c & 7) ^ (key & 7)) << 4));
-        cp_async_16_u32(k_ring + o, in ? a.k + off : a.k, in ? 16u : 0u);
-        cp_async_16_u32(v_ring + o, in ? a.v + off : a.v, in ? 16u : 0u);
-      }
-      cp_async_mbar_arrive(&kv_full[st]);
-    };
-    for (int j = 0; j < ntiles && j < kStages; ++j) issue_tile(j);
     // the first key past this thread's row: the range's end, or its causal limit
     int key_lim = geo.key_end;
     if (kCausal) {
@@ -409,23 +419,12 @@ __device__ __forceinline__ void prefix_range(const CUtensorMap* tm_q_p,
           break;
         }
       }
-      // refill after the softmax, so that waiting for PV(i - 1) never delays S(i)
-      if (i >= 1 && i + kStages - 1 < ntiles) {
-        const bool ok = warp_mbar_wait(&kv_empty[(i - 1) % kStages], ((i - 1) / kStages) & 1,
-                                       abort_flag, a.status);
-        if (wg_bar_any(1 + wg, !ok)) {
-          failed = true;
-          break;
-        }
-        issue_tile(i + kStages - 1);
-      }
     }
     if (softmax_warp && !failed && ntiles > 0) {
       // o_last completes once, after every PV of the range
       const bool ok = warp_mbar_wait(&o_last[wg], 0, abort_flag, a.status);
       have = !wg_bar_any(1 + wg, !ok);
     }
-    cp_async_wait<0>();  // nothing of this thread's still lands in the ring below
     tc_fence_before();
   }
 
