@@ -51,6 +51,7 @@ KERNEL_SOURCES = {
     "paged_attn_kernel": ["paged_attn.cu", "common.cuh", "merge.cuh"],
     "paged_tc_kernel": ["paged_tc.cu", "prefix_body.cuh", "common.cuh", "merge.cuh",
                         "kernels.cuh"],
+    "merge_slots_kernel": ["combine.cu", "merge.cuh", "common.cuh", "kernels.cuh"],
 }
 
 
@@ -259,6 +260,9 @@ class DeviceRun:
         self.suffix_kernel = ("paged_tc_kernel"
                               if b.max_seqlen_q * (b.num_q_heads // b.num_kv_heads) > 16
                               else "paged_attn_kernel")
+        # after a prefix phase the tcgen05 suffix leaves the merge to a third kernel
+        self.merge_after = (self.use_cascade and not self.single and self.cpl > 0 and
+                            self.suffix_kernel == "paged_tc_kernel")
 
     def plan(self):
         st = self._plan_fn(*self._plan_args)
@@ -344,7 +348,7 @@ def phase_times(run: DeviceRun, rounds: int = 16, batches: int = 3):
     for i in range(R):       # warm
         run.step(i, "cascade")
     torch.cuda.synchronize(run.dev)
-    acc = np.zeros(2)
+    acc = np.zeros(3)
     n = 0
     for _ in range(batches):
         torch.cuda._sleep(50_000_000)   # ~25 ms of GPU time while the host enqueues
@@ -352,14 +356,18 @@ def phase_times(run: DeviceRun, rounds: int = 16, batches: int = 3):
             run.step(i % R, "cascade", events[i])
         torch.cuda.synchronize(run.dev)
         for ev in events:
-            acc += [ev[0].elapsed_time(ev[1]), ev[1].elapsed_time(ev[2])]
+            acc += [ev[0].elapsed_time(ev[1]), ev[1].elapsed_time(ev[2]),
+                    ev[2].elapsed_time(ev[3])]
             n += 1
     ms = acc / n
     if run.single:
         # one kernel: events 0 and 1 bracket it, event 2 follows immediately
         return {"decode_cascade_kernel": ms[0] * 1e3, "launches_averaged": n}
-    return {"prefix_attn_kernel": ms[0] * 1e3, run.suffix_kernel: ms[1] * 1e3,
-            "launches_averaged": n}
+    out = {"prefix_attn_kernel": ms[0] * 1e3, run.suffix_kernel: ms[1] * 1e3}
+    if run.merge_after:
+        out["merge_slots_kernel"] = ms[2] * 1e3
+    out["launches_averaged"] = n
+    return out
 
 
 def e2e_steps(run: DeviceRun, steps: int):
@@ -445,6 +453,12 @@ def roofline_entry(kernel, us, b, run, peaks, workload):
     if kernel == "decode_cascade_kernel":
         # the whole step in one launch: KV once, q read, out + lse written
         bytes_ = accounting.cascade_min_bytes(b, cpl)
+        flops = None
+    elif kernel == "merge_slots_kernel":
+        # every row: its slots read (the prefix ranges and one suffix split), out + lse
+        # written
+        n_slots = run.prefix_ranges + 1
+        bytes_ = rows * (n_slots * (b.head_dim * 2 + 4) + b.head_dim * 2 + 4)
         flops = None
     elif kernel == "prefix_attn_kernel":
         # prefix KV once, q, and one partial per row (bf16 O, fp32 LSE)
@@ -539,7 +553,8 @@ def run_ours(args, dist: Dist):
         "hbm_frac_of_measured": round(min_bytes / (us_call * 1e-6) / 1e9 / peaks["hbm_gbs"], 4),
         "hbm_frac_of_8tbs": round(min_bytes / (us_call * 1e-6) / 1e9 / 8000.0, 4),
         "host_s_in_timed_region": round(host_s, 4),
-        "gpu_launches": K * (2 if path == "cascade" and not run.single else 1),
+        "gpu_launches": K * ((3 if run.merge_after else 2)
+                             if path == "cascade" and not run.single else 1),
     }
     if clocks:
         result["clocks"] = clocks.summary(t0, t1)
@@ -547,7 +562,8 @@ def run_ours(args, dist: Dist):
     if path == "cascade":
         ph = phase_times(run)
         kernels = (["decode_cascade_kernel"] if run.single
-                   else ["prefix_attn_kernel", run.suffix_kernel])
+                   else ["prefix_attn_kernel", run.suffix_kernel] +
+                   (["merge_slots_kernel"] if run.merge_after else []))
         if run.single:
             # one launch per step: the launch's average duration over the timed region
             # is the region's event time / K (an isolated launch, timed with events

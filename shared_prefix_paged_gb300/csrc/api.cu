@@ -442,9 +442,12 @@ int attention_call(const void* q, const void* k_cache, const void* v_cache, int3
     return CSP_OK;
   }
   if ((e = mark(0)) != cudaSuccess) return cuda_fail(e);
-  // row-group counters start at zero in every call, whatever the workspace held
-  // (only several suffix splits count themselves)
-  if (P.n_parts > 0 && P.s_splits > 1 &&
+  // After a prefix phase the tcgen05 suffix kernel writes its partials and a third
+  // kernel merges every row (the two phases never wait for each other); otherwise the
+  // suffix kernel merges, and several suffix splits count themselves in row-group
+  // counters that start at zero in every call, whatever the workspace held.
+  const bool merge_after = P.tc && cpl > 0;
+  if (P.n_parts > 0 && P.s_splits > 1 && !merge_after &&
       (e = cudaMemsetAsync(counters, 0, static_cast<size_t>(total_q) * Hkv * sizeof(int32_t),
                            stream)) != cudaSuccess)
     return cuda_fail(e);
@@ -507,6 +510,7 @@ int attention_call(const void* q, const void* k_cache, const void* v_cache, int3
   ga.out = static_cast<__nv_bfloat16*>(out);
   ga.lse = lse;
   ga.status = status;
+  if (merge_after) ga.counters = nullptr;
   // concurrent with the prefix kernel (programmatic dependent launch) unless phase
   // events sit between the two
   const bool overlap = cpl > 0 && events == nullptr;
@@ -526,7 +530,12 @@ int attention_call(const void* q, const void* k_cache, const void* v_cache, int3
   }
   if (e != cudaSuccess) return cuda_fail(e);
   if ((e = mark(2)) != cudaSuccess) return cuda_fail(e);
-
+  // in stream order (no programmatic launch): both phases' slots are complete
+  if (merge_after &&
+      (e = csp::launch_merge_slots(D, part_o, part_lse, P.n_parts,
+                                   static_cast<int64_t>(total_q) * Hq,
+                                   static_cast<__nv_bfloat16*>(out), lse, stream)) != cudaSuccess)
+    return cuda_fail(e);
   if ((e = mark(3)) != cudaSuccess) return cuda_fail(e);
   return CSP_OK;
 }

@@ -6,9 +6,11 @@
 //   lse = m + ln(w1 + w2).
 // Elementwise and HBM-bound: D/8 threads per output row, 16-byte vector loads and
 // stores, fp32 math.  (Inside cascade_attn the same merge runs in the attention
-// kernels themselves, see merge.cuh.)
+// kernels themselves, see merge.cuh, or, after a tcgen05 suffix phase, in
+// merge_slots_kernel below.)
 #include "common.cuh"
 #include "kernels.cuh"
+#include "merge.cuh"
 
 namespace csp {
 namespace {
@@ -72,7 +74,73 @@ __global__ void __launch_bounds__(256)
   if (c == 0 && out_lse != nullptr) out_lse[row] = ws > 0.f ? m + logf(ws) : -INFINITY;
 }
 
+// n slots per row (the cascade call's partials, log2 domain): one thread per 8
+// features of a row.  It reads the row's n LSEs (the row's other threads read the same
+// ones: one L1 line), then the slots' 16-byte pieces with non-zero weight, and writes
+// 16 bytes of out (the first thread of a row also the LSE).  An empty slot (lse -inf)
+// is never read into the sum.
+constexpr int kMergeThreads = 256;
+
+template <int D>
+__global__ void __launch_bounds__(kMergeThreads)
+    merge_slots_kernel(const MergeArgs m) {
+  constexpr int kC = D / 8;
+  const int64_t idx = static_cast<int64_t>(blockIdx.x) * kMergeThreads + threadIdx.x;
+  if (idx >= static_cast<int64_t>(m.rows) * kC) return;
+  const int64_t row = idx / kC;
+  const int c = static_cast<int>(idx % kC);
+  float mx = -INFINITY;
+#pragma unroll 4
+  for (int p = 0; p < m.n_parts; ++p)
+    mx = fmaxf(mx, __ldcg(m.part_lse + static_cast<int64_t>(p) * m.rows + row));
+  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  float wsum = 0.f;
+#pragma unroll 4
+  for (int p = 0; p < m.n_parts; ++p) {
+    const int64_t prow = static_cast<int64_t>(p) * m.rows + row;
+    const float lp = __ldcg(m.part_lse + prow);
+    const float w = (lp == -INFINITY || mx == -INFINITY) ? 0.f : fast_exp2(lp - mx);
+    if (w != 0.f) {
+      const uint4 u = __ldcg(reinterpret_cast<const uint4*>(m.part_o + prow * D + c * 8));
+      const uint32_t uu[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&uu[e]));
+        acc[2 * e] = fmaf(w, f.x, acc[2 * e]);
+        acc[2 * e + 1] = fmaf(w, f.y, acc[2 * e + 1]);
+      }
+      wsum += w;
+    }
+  }
+  const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+  *reinterpret_cast<uint4*>(m.out + row * D + c * 8) =
+      make_uint4(pack_bf16x2(acc[0] * inv, acc[1] * inv), pack_bf16x2(acc[2] * inv, acc[3] * inv),
+                 pack_bf16x2(acc[4] * inv, acc[5] * inv), pack_bf16x2(acc[6] * inv, acc[7] * inv));
+  if (c == 0 && m.lse != nullptr)
+    m.lse[row] = wsum > 0.f ? (mx + log2f(wsum)) * 0.69314718055994531f : -INFINITY;
+}
+
 }  // namespace
+
+cudaError_t launch_merge_slots(int head_dim, const __nv_bfloat16* part_o, const float* part_lse,
+                               int n_parts, int64_t rows, __nv_bfloat16* out, float* lse,
+                               cudaStream_t stream) {
+  if (rows <= 0) return cudaSuccess;
+  MergeArgs m = {};
+  m.part_o = part_o;
+  m.part_lse = part_lse;
+  m.n_parts = n_parts;
+  m.rows = static_cast<int>(rows);
+  m.out = out;
+  m.lse = lse;
+  const int64_t threads = rows * (head_dim / 8);
+  const unsigned grid = static_cast<unsigned>((threads + kMergeThreads - 1) / kMergeThreads);
+  if (head_dim == 64)
+    merge_slots_kernel<64><<<grid, kMergeThreads, 0, stream>>>(m);
+  else
+    merge_slots_kernel<128><<<grid, kMergeThreads, 0, stream>>>(m);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_merge_states(__nv_bfloat16* out, float* out_lse, const void* o1,
                                 const float* l1, const void* o2, const float* l2, int rows,

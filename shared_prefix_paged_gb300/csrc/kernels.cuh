@@ -57,7 +57,8 @@ struct PagedArgs {
   __nv_bfloat16* part_o; // partial mode: [n_prefix + n_splits][total_q][Hq][D] (own slot: n_prefix + split)
   float* part_lse;       //               [n_prefix + n_splits][total_q][Hq], log2 domain
   int n_prefix;          //               prefix slots before the suffix ones (0: none)
-  int* counters;         //               row-group counters (merge.cuh)
+  int* counters;         //               row-group counters (merge.cuh); the tcgen05 variant
+                         //               with none leaves every merge to merge_slots
   __nv_bfloat16* out;    // final output: direct mode (part_o == nullptr) or last contributor
   float* lse;            // natural-log LSE or nullptr
   int* status;           // workspace status word (bounded waits of the tcgen05 variant)
@@ -123,6 +124,13 @@ cudaError_t launch_paged(int head_dim, bool decode, const PagedArgs& a, bool aft
 cudaError_t launch_paged_tc(int head_dim, const CUtensorMap& tm_q, const CUtensorMap& tm_k,
                             const CUtensorMap& tm_v, const PagedArgs& a, bool after_prefix,
                             cudaStream_t stream);
+
+// merge_attn_states over n_parts slots of every row (rows = total_q * num_q_heads):
+// part_o [n_parts][rows][D] bf16 normalised, part_lse [n_parts][rows] log2 domain ->
+// bf16 out and the natural-log LSE (lse may be null).
+cudaError_t launch_merge_slots(int head_dim, const __nv_bfloat16* part_o, const float* part_lse,
+                               int n_parts, int64_t rows, __nv_bfloat16* out, float* lse,
+                               cudaStream_t stream);
 
 cudaError_t launch_merge_states(__nv_bfloat16* out, float* out_lse, const void* o1,
                                 const float* l1, const void* o2, const float* l2, int rows,

@@ -239,4 +239,23 @@ __device__ __forceinline__ void merge_rows_block(const MergeArgs& m, int n_rows,
   }
 }
 
+// After a CTA has written its partial rows: count it in the row groups (token
+// t_first + i, KV head g) for i in [0, n_tok); the group's m.n_count-th contributor
+// merges the group's rows of this CTA (row i of n_rows is output row row_of(i), of the
+// CTA's token tok_local(i)).  s_last: shared scratch of n_tok ints; s_w as for
+// merge_rows_block.  Called by every thread of the CTA.
+template <int D, typename RowOf, typename TokOf>
+__device__ __forceinline__ void count_and_merge_block(const MergeArgs& m, int t_first, int n_tok,
+                                                      int g, int n_rows, RowOf row_of,
+                                                      TokOf tok_local, int* s_last, float* s_w) {
+  __syncthreads();  // every partial row of this CTA is written
+  for (int i = threadIdx.x; i < n_tok; i += blockDim.x) {
+    int* c = m.counters + static_cast<int64_t>(t_first + i) * m.num_kv_heads + g;
+    s_last[i] = atomic_add_acq_rel_gpu(c, 1) == m.n_count - 1;
+  }
+  __syncthreads();
+  merge_rows_block<D>(m, n_rows, row_of, [&](int i) { return s_last[tok_local(i)] == 0; },
+                      nullptr, 0, nullptr, s_w);
+}
+
 }  // namespace csp

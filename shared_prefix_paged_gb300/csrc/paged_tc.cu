@@ -12,10 +12,12 @@
 // with q_len queries and seq_len keys sees keys <= seq_len - q_len + i (bottom-right
 // alignment; the KV includes the new tokens).  The output step:
 //  * standard path with one split: bf16 out and the natural-log LSE directly;
-//  * one suffix split after the prefix phase: each row is merged in place with the
-//    prefix's slots (merge.cuh) once the prefix grid is complete;
-//  * several splits: each writes a partial slot and the last split of a row group
-//    merges every slot.
+//  * after a prefix phase, each split writes its partial slot and a third kernel
+//    (merge_slots, combine.cu) merges every row once both phases are done, so the
+//    suffix never waits for the prefix grid;
+//  * standard path with several splits: each writes a partial slot and counts itself
+//    in its row groups (token, KV head); the last split of a group merges every slot
+//    of its rows (merge.cuh).
 #include "merge.cuh"
 #include "prefix_body.cuh"
 
@@ -96,31 +98,30 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr int kChunks = D / 8;
   constexpr float kLn2 = 0.69314718055994531f;
   const bool partial = a.part_o != nullptr;
-  const bool merge_in_place = partial && a.n_splits == 1;
   auto out_row = [&](int rr) {
     const int rho = prow0 + rr;
     return static_cast<int64_t>(q0 + (rho >> gshift)) * a.num_q_heads + g * a.group +
            (rho & (a.group - 1));
   };
-  if (!merge_in_place) {
-    // the final rows (standard path, one split) or this split's partial slot
-    for (int it = threadIdx.x; it < rows_here * kChunks; it += kThreads) {
-      const int rr = it / kChunks, c = it % kChunks;
-      const int64_t orow = out_row(rr);
-      const uint4 v = *reinterpret_cast<const uint4*>(stage + rr * L::kStageRow + c * 8);
-      if (partial) {
-        const int64_t prow =
-            static_cast<int64_t>(a.n_prefix + split) * a.total_q * a.num_q_heads + orow;
-        *reinterpret_cast<uint4*>(a.part_o + prow * D + c * 8) = v;
-        if (c == 0) a.part_lse[prow] = s_lse[rr];
-      } else {
-        *reinterpret_cast<uint4*>(a.out + orow * D + c * 8) = v;
-        if (c == 0 && a.lse != nullptr) a.lse[orow] = s_lse[rr] * kLn2;
-      }
+  // the final rows (standard path, one split) or this split's partial slot
+  for (int it = threadIdx.x; it < rows_here * kChunks; it += kThreads) {
+    const int rr = it / kChunks, c = it % kChunks;
+    const int64_t orow = out_row(rr);
+    const uint4 v = *reinterpret_cast<const uint4*>(stage + rr * L::kStageRow + c * 8);
+    if (partial) {
+      const int64_t prow =
+          static_cast<int64_t>(a.n_prefix + split) * a.total_q * a.num_q_heads + orow;
+      *reinterpret_cast<uint4*>(a.part_o + prow * D + c * 8) = v;
+      if (c == 0) a.part_lse[prow] = s_lse[rr];
+    } else {
+      *reinterpret_cast<uint4*>(a.out + orow * D + c * 8) = v;
+      if (c == 0 && a.lse != nullptr) a.lse[orow] = s_lse[rr] * kLn2;
     }
   }
-  if (!partial) return;
+  if (!partial || a.counters == nullptr) return;  // no counters: merge_slots follows
 
+  // count this split in the row groups (tokens) it covered; the last split of a group
+  // merges every slot of its rows
   MergeArgs m;
   m.part_o = a.part_o;
   m.part_lse = a.part_lse;
@@ -133,32 +134,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   m.group = a.group;
   m.out = a.out;
   m.lse = a.lse;
-  // shared scratch past the staged rows: the last-split flags, then the weights
+  // shared scratch past the staged rows: the last-contributor flags, then the weights
   int* s_last = reinterpret_cast<int*>(smem + kRowsCta * L::kStageRow * 2);
   float* s_w = reinterpret_cast<float*>(s_last + kRowsCta + 1);
-  grid_dependency_wait();  // the prefix grid's partials are complete and visible
-  if (merge_in_place) {
-    // this CTA is its rows' only suffix contributor: its staged rows join the prefix
-    // slots directly
-    m.n_parts = a.n_prefix;
-    merge_rows_block<D>(m, rows_here, out_row, [](int) { return false; }, stage, L::kStageRow,
-                        s_lse, s_w);
-  } else {
-    // count this split in the row groups (tokens) it touched; the last split of a
-    // group merges every slot of its rows
-    const int tok_first = prow0 >> gshift;
-    const int n_tok = ((prow0 + rows_here - 1) >> gshift) - tok_first + 1;
-    __syncthreads();  // every partial row of this CTA is written
-    for (int i = threadIdx.x; i < n_tok; i += kThreads) {
-      int* c = a.counters + static_cast<int64_t>(q0 + tok_first + i) * a.num_kv_heads + g;
-      s_last[i] = atomic_add_acq_rel_gpu(c, 1) == a.n_splits - 1;
-    }
-    __syncthreads();
-    merge_rows_block<D>(
-        m, rows_here, out_row,
-        [&](int rr) { return s_last[((prow0 + rr) >> gshift) - tok_first] == 0; }, nullptr, 0,
-        nullptr, s_w);
-  }
+  const int tok_first = prow0 >> gshift;
+  const int n_tok = ((prow0 + rows_here - 1) >> gshift) - tok_first + 1;
+  count_and_merge_block<D>(m, q0 + tok_first, n_tok, g, rows_here, out_row,
+                           [&](int rr) { return ((prow0 + rr) >> gshift) - tok_first; }, s_last,
+                           s_w);
 }
 
 template <int D>
