@@ -75,13 +75,14 @@ __global__ void __launch_bounds__(256)
 }
 
 // n slots per row (the cascade call's partials, log2 domain): one thread per 8
-// features of a row.  It reads the row's n LSEs (the row's other threads read the same
-// ones: one L1 line), then the slots' 16-byte pieces with non-zero weight, and writes
-// 16 bytes of out (the first thread of a row also the LSE).  An empty slot (lse -inf)
-// is never read into the sum.
+// features of a row.  It issues every slot's LSE and 16-byte piece at once (the slot
+// loop unrolled to kS >= n; the row's other threads read the same LSEs: one L1 line),
+// then weighs them and writes 16 bytes of out (the first thread of a row also the
+// LSE).  An empty slot (lse -inf) gets weight 0 and a select keeps whatever it holds
+// out of the sum.
 constexpr int kMergeThreads = 256;
 
-template <int D>
+template <int D, int kS>
 __global__ void __launch_bounds__(kMergeThreads)
     merge_slots_kernel(const MergeArgs m) {
   constexpr int kC = D / 8;
@@ -89,27 +90,29 @@ __global__ void __launch_bounds__(kMergeThreads)
   if (idx >= static_cast<int64_t>(m.rows) * kC) return;
   const int64_t row = idx / kC;
   const int c = static_cast<int>(idx % kC);
+  float l[kS];
+  uint4 u[kS];
+#pragma unroll
+  for (int s = 0; s < kS; ++s) {
+    const int64_t prow = static_cast<int64_t>(min(s, m.n_parts - 1)) * m.rows + row;
+    l[s] = s < m.n_parts ? __ldcg(m.part_lse + prow) : -INFINITY;
+    u[s] = __ldcg(reinterpret_cast<const uint4*>(m.part_o + prow * D + c * 8));
+  }
   float mx = -INFINITY;
-#pragma unroll 4
-  for (int p = 0; p < m.n_parts; ++p)
-    mx = fmaxf(mx, __ldcg(m.part_lse + static_cast<int64_t>(p) * m.rows + row));
+#pragma unroll
+  for (int s = 0; s < kS; ++s) mx = fmaxf(mx, l[s]);
   float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
   float wsum = 0.f;
-#pragma unroll 4
-  for (int p = 0; p < m.n_parts; ++p) {
-    const int64_t prow = static_cast<int64_t>(p) * m.rows + row;
-    const float lp = __ldcg(m.part_lse + prow);
-    const float w = (lp == -INFINITY || mx == -INFINITY) ? 0.f : fast_exp2(lp - mx);
-    if (w != 0.f) {
-      const uint4 u = __ldcg(reinterpret_cast<const uint4*>(m.part_o + prow * D + c * 8));
-      const uint32_t uu[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&uu[e]));
-        acc[2 * e] = fmaf(w, f.x, acc[2 * e]);
-        acc[2 * e + 1] = fmaf(w, f.y, acc[2 * e + 1]);
-      }
-      wsum += w;
+  for (int s = 0; s < kS; ++s) {
+    const float w = (l[s] == -INFINITY || mx == -INFINITY) ? 0.f : fast_exp2(l[s] - mx);
+    wsum += w;
+    const uint32_t uu[4] = {u[s].x, u[s].y, u[s].z, u[s].w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&uu[e]));
+      acc[2 * e] = w != 0.f ? fmaf(w, f.x, acc[2 * e]) : acc[2 * e];
+      acc[2 * e + 1] = w != 0.f ? fmaf(w, f.y, acc[2 * e + 1]) : acc[2 * e + 1];
     }
   }
   const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
@@ -118,6 +121,20 @@ __global__ void __launch_bounds__(kMergeThreads)
                  pack_bf16x2(acc[4] * inv, acc[5] * inv), pack_bf16x2(acc[6] * inv, acc[7] * inv));
   if (c == 0 && m.lse != nullptr)
     m.lse[row] = wsum > 0.f ? (mx + log2f(wsum)) * 0.69314718055994531f : -INFINITY;
+}
+
+template <int D>
+void launch_slots_d(const MergeArgs& m, unsigned grid, cudaStream_t stream) {
+  if (m.n_parts <= 2)
+    merge_slots_kernel<D, 2><<<grid, kMergeThreads, 0, stream>>>(m);
+  else if (m.n_parts <= 4)
+    merge_slots_kernel<D, 4><<<grid, kMergeThreads, 0, stream>>>(m);
+  else if (m.n_parts <= 8)
+    merge_slots_kernel<D, 8><<<grid, kMergeThreads, 0, stream>>>(m);
+  else if (m.n_parts <= 16)
+    merge_slots_kernel<D, 16><<<grid, kMergeThreads, 0, stream>>>(m);
+  else
+    merge_slots_kernel<D, kMaxParts><<<grid, kMergeThreads, 0, stream>>>(m);
 }
 
 }  // namespace
@@ -136,9 +153,9 @@ cudaError_t launch_merge_slots(int head_dim, const __nv_bfloat16* part_o, const 
   const int64_t threads = rows * (head_dim / 8);
   const unsigned grid = static_cast<unsigned>((threads + kMergeThreads - 1) / kMergeThreads);
   if (head_dim == 64)
-    merge_slots_kernel<64><<<grid, kMergeThreads, 0, stream>>>(m);
+    launch_slots_d<64>(m, grid, stream);
   else
-    merge_slots_kernel<128><<<grid, kMergeThreads, 0, stream>>>(m);
+    launch_slots_d<128>(m, grid, stream);
   return cudaGetLastError();
 }
 
