@@ -36,6 +36,7 @@ SMALL_CASES = [
     (7, [1000] * 3, [1] * 3, 992, 8, 4, 128),                     # long prefix, short suffix
     (8, [700, 420, 300], [100, 70, 1], 256, 16, 4, 128),          # two 256-row tiles
     (9, [300, 200], [40, 33], 128, 4, 4, 64),                     # group 1, prefill rows
+    (10, [4200, 4300], [40, 50], 4096, 16, 4, 128),               # prefill rows, many prefix ranges
 ]
 
 
