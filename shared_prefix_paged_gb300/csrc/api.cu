@@ -426,6 +426,9 @@ int attention_call(const void* q, const void* k_cache, const void* v_cache, int3
     da.prefix_ctas = P.d_prefix_ctas;
     da.prefix_units = P.d_prefix_units;
     da.merge_rows = P.d_merge_rows;
+    // every request's suffix within one item (two 64-key tiles): two groups of four
+    // warps take alternate units
+    da.unit_groups = max_seqlen_k - cpl <= 2 * 64 ? 2 : 1;
     da.key_tiles = cdiv(cpl, 64);
     da.bar_count = reinterpret_cast<int*>(ws + kOffBarCount);
     da.bar_gen = reinterpret_cast<unsigned*>(ws + kOffBarGen);

@@ -38,7 +38,6 @@ constexpr int kPage = 16;
 constexpr int kTilePages = kKeys / kPage;
 constexpr int kRows = 16;                   // packed rows of a suffix unit (one M tile)
 constexpr int kStreamWarps = 8;             // warps 0-7 stream the suffix
-constexpr int kStreamThreads = 32 * kStreamWarps;
 constexpr int kWarpScheduler = 8;           // produces the suffix items
 constexpr int kMergeBarOff = 512;           // merge barrier within the suffix barrier area
 
@@ -93,9 +92,10 @@ __device__ __forceinline__ void st_release_gpu_u32(unsigned* p, unsigned v) {
   asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
-// the eight streaming warps (named barrier 1)
-__device__ __forceinline__ void stream_sync() {
-  asm volatile("bar.sync 1, %0;" ::"r"(kStreamThreads) : "memory");
+// the streaming warps of one unit group: named barrier 1 + group, kWPU warps
+template <int kWPU>
+__device__ __forceinline__ void group_sync(int group) {
+  asm volatile("bar.sync %0, %1;" ::"r"(1 + group), "r"(kWPU * 32) : "memory");
 }
 
 // ------------------------------------------------------------------ streaming --
@@ -195,7 +195,8 @@ __device__ __forceinline__ void produce_items(const DecodeArgs& a, const CUtenso
     const int nt = end ? -1 : max(1, (nkeys + kKeys - 1) / kKeys);  // >= 1 all-masked tile
     const int npages = (seq_len + kPage - 1) / kPage;
     const int32_t* bt = a.block_table + static_cast<int64_t>(end ? 0 : u / hkv) * a.bt_stride;
-    for (int t0 = 0; end ? t0 == 0 : t0 < nt; t0 += 2) {
+    // the end: one marker per consumer group (each group reads every unit_groups-th item)
+    for (int t0 = 0; end ? t0 < 2 * a.unit_groups : t0 < nt; t0 += 2) {
       const int slot = item % kS;
       if (item >= kS &&
           !(ok = warp_mbar_wait(&st_empty[slot], ((item / kS) - 1) & 1, abort_flag, p.status)))
@@ -253,7 +254,11 @@ __device__ __forceinline__ void produce_items(const DecodeArgs& a, const CUtenso
   cp_async_wait<0>();
 }
 
-template <int D>
+// kG groups of 8 / kG streaming warps: group g takes items g, g + kG, g + 2 kG, ...
+// (kG = 2 only when every unit is a single item, so a unit never spans two groups).
+// Within a group, warp w' takes keys [w' * 16 kG, (w' + 1) * 16 kG) of the item's 128
+// (kG blocks of 16 keys in one of its two tiles).
+template <int D, int kG>
 __device__ __forceinline__ void consume_items(const DecodeArgs& a, uint8_t* ring,
                                               uint64_t* st_full, uint64_t* st_empty,
                                               const ItemDesc* idesc, volatile int* abort_flag) {
@@ -262,14 +267,18 @@ __device__ __forceinline__ void consume_items(const DecodeArgs& a, uint8_t* ring
   constexpr int kChunks = D / 8;          // 16-byte chunks per row
   constexpr int kDT = D / 8;              // O n-tiles (8 features each)
   constexpr int kORow = D + 4;            // merge scratch row (floats)
-  static_assert(kStreamWarps * kRows * kORow * 4 + 2 * kStreamWarps * kRows * 4 <= L::kItem,
+  constexpr int kWPU = kStreamWarps / kG; // warps per unit
+  constexpr int kB = kG;                  // 16-key blocks per warp
+  static_assert(kWPU * kRows * kORow * 4 + 2 * kWPU * kRows * 4 <= L::kItem,
                 "merge scratch fits one item");
   const PrefixArgs& p = a.pre;
   const int tid = threadIdx.x;  // 0 .. 255
   const int lane = tid & 31;
   const int wi = tid >> 5;      // 0 .. 7
-  const int half = wi >> 2;     // which tile of the item this warp computes
-  const int kw0 = (wi & 3) * 16;  // this warp's keys within its tile
+  const int grp = wi / kWPU;    // this warp's group
+  const int wg = wi % kWPU;     // its index within the group
+  const int half = (wg * 16 * kB) >> 6;      // which tile of the item this warp computes
+  const int kw0 = (wg * 16 * kB) & 63;       // its first key within that tile
   const uint32_t rbase = smem_u32(ring);
 
   int c_nt = 0, c_seq = 0, c_qlen = 0, c_q0 = 0, c_kvh = 0, rows_valid = 0;
@@ -277,7 +286,7 @@ __device__ __forceinline__ void consume_items(const DecodeArgs& a, uint8_t* ring
   float o[kDT][4];
   float m_run[2], l_run[2];
   uint32_t qa[D / 16][4];
-  for (int item = 0;; ++item) {
+  for (int item = grp;; item += kG) {
     const int slot = item % kS;
     const uint32_t par = (item / kS) & 1;
     if (!warp_mbar_wait(&st_full[slot], par, abort_flag, p.status)) break;
@@ -315,10 +324,10 @@ __device__ __forceinline__ void consume_items(const DecodeArgs& a, uint8_t* ring
       const uint32_t kb = ib + half * L::kStage;
       const uint32_t vb = kb + L::kKV;
       const int key0 = p.cpl + (t0 + half) * kKeys + kw0;
-      if (key0 + 16 > c_seq) {
+      if (key0 + 16 * kB > c_seq) {
         // this warp's keys past the request: zero their V rows (P is 0 there, but the
         // page may hold anything)
-        for (int x = lane; x < 16 * kChunks; x += 32) {
+        for (int x = lane; x < 16 * kB * kChunks; x += 32) {
           const int k = x / kChunks, c = x % kChunks;
           if (key0 + k >= c_seq)
             asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(
@@ -327,25 +336,28 @@ __device__ __forceinline__ void consume_items(const DecodeArgs& a, uint8_t* ring
         }
         __syncwarp();
       }
-      // S = Q K^T over this warp's 16 keys (two n-tiles of 8)
-      float sacc[2][4];
+      // S = Q K^T over this warp's keys (two n-tiles of 8 per 16-key block)
+      float sacc[2 * kB][4];
 #pragma unroll
-      for (int i = 0; i < 2; ++i) sacc[i][0] = sacc[i][1] = sacc[i][2] = sacc[i][3] = 0.f;
+      for (int i = 0; i < 2 * kB; ++i) sacc[i][0] = sacc[i][1] = sacc[i][2] = sacc[i][3] = 0.f;
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
-        const int key = kw0 + (lane & 7) + (lane >> 4) * 8;
-        const int c = kk * 2 + ((lane >> 3) & 1);
-        uint32_t b0, b1, b2, b3;
-        ldmatrix_x4(kb + kv_off<D>(key, c), b0, b1, b2, b3);
-        mma_bf16_16816(sacc[0], qa[kk], b0, b1);
-        mma_bf16_16816(sacc[1], qa[kk], b2, b3);
+#pragma unroll
+        for (int b = 0; b < kB; ++b) {
+          const int key = kw0 + 16 * b + (lane & 7) + (lane >> 4) * 8;
+          const int c = kk * 2 + ((lane >> 3) & 1);
+          uint32_t b0, b1, b2, b3;
+          ldmatrix_x4(kb + kv_off<D>(key, c), b0, b1, b2, b3);
+          mma_bf16_16816(sacc[2 * b], qa[kk], b0, b1);
+          mma_bf16_16816(sacc[2 * b + 1], qa[kk], b2, b3);
+        }
       }
       // mask (keys past the request, and the causal limit), online softmax in base 2
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         float mx = -INFINITY;
 #pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
+        for (int nt = 0; nt < 2 * kB; ++nt) {
 #pragma unroll
           for (int e = 0; e < 2; ++e) {
             const int kabs = key0 + nt * 8 + (lane & 3) * 2 + e;
@@ -372,7 +384,7 @@ __device__ __forceinline__ void consume_items(const DecodeArgs& a, uint8_t* ring
         const float m_use = (m_run[h] == -INFINITY) ? 0.f : m_run[h];
         float sum = 0.f;
 #pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
+        for (int nt = 0; nt < 2 * kB; ++nt) {
 #pragma unroll
           for (int e = 0; e < 2; ++e) {
             float& sref = sacc[nt][2 * h + e];
@@ -382,67 +394,70 @@ __device__ __forceinline__ void consume_items(const DecodeArgs& a, uint8_t* ring
         }
         l_run[h] += sum;
       }
-      // O += P V over the same 16 keys
-      uint32_t pa[4];
-      pa[0] = pack_bf16x2(sacc[0][0], sacc[0][1]);
-      pa[1] = pack_bf16x2(sacc[0][2], sacc[0][3]);
-      pa[2] = pack_bf16x2(sacc[1][0], sacc[1][1]);
-      pa[3] = pack_bf16x2(sacc[1][2], sacc[1][3]);
+      // O += P V over the same keys
 #pragma unroll
-      for (int dp = 0; dp < kDT / 2; ++dp) {
-        const int key = kw0 + (lane & 7) + ((lane >> 3) & 1) * 8;
-        const int c = dp * 2 + (lane >> 4);
-        uint32_t b0, b1, b2, b3;
-        ldmatrix_x4_trans(vb + kv_off<D>(key, c), b0, b1, b2, b3);
-        mma_bf16_16816(o[2 * dp], pa, b0, b1);
-        mma_bf16_16816(o[2 * dp + 1], pa, b2, b3);
+      for (int b = 0; b < kB; ++b) {
+        uint32_t pa[4];
+        pa[0] = pack_bf16x2(sacc[2 * b][0], sacc[2 * b][1]);
+        pa[1] = pack_bf16x2(sacc[2 * b][2], sacc[2 * b][3]);
+        pa[2] = pack_bf16x2(sacc[2 * b + 1][0], sacc[2 * b + 1][1]);
+        pa[3] = pack_bf16x2(sacc[2 * b + 1][2], sacc[2 * b + 1][3]);
+#pragma unroll
+        for (int dp = 0; dp < kDT / 2; ++dp) {
+          const int key = kw0 + 16 * b + (lane & 7) + ((lane >> 3) & 1) * 8;
+          const int c = dp * 2 + (lane >> 4);
+          uint32_t b0, b1, b2, b3;
+          ldmatrix_x4_trans(vb + kv_off<D>(key, c), b0, b1, b2, b3);
+          mma_bf16_16816(o[2 * dp], pa, b0, b1);
+          mma_bf16_16816(o[2 * dp + 1], pa, b2, b3);
+        }
       }
     }
     if (t0 + 2 >= c_nt) {
-      // ---- the unit's last item: the eight warps' (max, sum, O) -> one normalised
-      // partial per row, through this item's memory
+      // ---- the unit's last item: the group's warps' (max, sum, O) -> one normalised
+      // partial per row, through this item's memory (only this group reads the item)
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         l_run[h] += __shfl_xor_sync(0xffffffffu, l_run[h], 1);
         l_run[h] += __shfl_xor_sync(0xffffffffu, l_run[h], 2);
       }
-      stream_sync();  // every warp is done reading this item's K/V
-      float* s_o = reinterpret_cast<float*>(ring + slot * L::kItem);  // [8][16][kORow]
-      float* s_m = s_o + kStreamWarps * kRows * kORow;                // [8][16]
-      float* s_l = s_m + kStreamWarps * kRows;                        // [8][16]
+      group_sync<kWPU>(grp);  // every warp of the group is done reading this item's K/V
+      float* s_o = reinterpret_cast<float*>(ring + slot * L::kItem);  // [kWPU][16][kORow]
+      float* s_m = s_o + kWPU * kRows * kORow;                        // [kWPU][16]
+      float* s_l = s_m + kWPU * kRows;                                // [kWPU][16]
       // every warp's raw (max, sum, O) of its keys; the weights come in the final pass
       if ((lane & 3) == 0) {
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
-          s_m[wi * kRows + (lane >> 2) + 8 * h] = m_run[h];
-          s_l[wi * kRows + (lane >> 2) + 8 * h] = l_run[h];
+          s_m[wg * kRows + (lane >> 2) + 8 * h] = m_run[h];
+          s_l[wg * kRows + (lane >> 2) + 8 * h] = l_run[h];
         }
       }
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         const int rr = (lane >> 2) + 8 * h;
         if (rr >= rows_valid) continue;
-        float* dst = s_o + (wi * kRows + rr) * kORow;
+        float* dst = s_o + (wg * kRows + rr) * kORow;
 #pragma unroll
         for (int dt = 0; dt < kDT; ++dt) {
           const int dd = dt * 8 + (lane & 3) * 2;
           *reinterpret_cast<float2*>(dst + dd) = make_float2(o[dt][2 * h], o[dt][2 * h + 1]);
         }
       }
-      stream_sync();
+      group_sync<kWPU>(grp);
       const int64_t slot_rows = static_cast<int64_t>(p.n_splits) * p.total_q * p.num_q_heads;
-      // warp wi finalises rows wi and wi + 8; lane c owns features [4c, 4c + 4)
-      for (int rr = wi; rr < rows_valid; rr += kStreamWarps) {
-        float mw[kStreamWarps];
+      // warp w' finalises rows w', w' + kWPU, ...; lane c owns features [4c, 4c + 4)
+      for (int rr = wg; rr < rows_valid; rr += kWPU) {
+        float mw[kWPU];
         float mg = -INFINITY;
 #pragma unroll
-        for (int w = 0; w < kStreamWarps; ++w) {
+        for (int w = 0; w < kWPU; ++w) {
           mw[w] = s_m[w * kRows + rr];
           mg = fmaxf(mg, mw[w]);
         }
         float lsum = 0.f;
 #pragma unroll
-        for (int w = 0; w < kStreamWarps; ++w) {
+        for (int w = 0; w < kWPU; ++w) {
           mw[w] = (mw[w] == -INFINITY) ? 0.f : fast_exp2(mw[w] - mg);  // warp w's weight
           lsum += s_l[w * kRows + rr] * mw[w];
         }
@@ -453,7 +468,7 @@ __device__ __forceinline__ void consume_items(const DecodeArgs& a, uint8_t* ring
         if (lane < D / 4) {
           float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-          for (int w = 0; w < kStreamWarps; ++w) {
+          for (int w = 0; w < kWPU; ++w) {
             const float4 v =
                 *reinterpret_cast<const float4*>(s_o + (w * kRows + rr) * kORow + lane * 4);
             acc.x = fmaf(mw[w], v.x, acc.x);
@@ -637,7 +652,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < kS; ++i) {
       mbar_init(&st_full[i], 1 + 32);  // the producer's expect_tx + its lanes' copies
-      mbar_init(&st_empty[i], kStreamWarps);
+      mbar_init(&st_empty[i], kStreamWarps / a.unit_groups);  // the warps of one unit
     }
     mbar_init(merge_bar, 1);
     *abort_flag = 0;
@@ -648,7 +663,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == kWarpScheduler) {
       produce_items<D>(a, &tm_k, &tm_v, smem, st_full, st_empty, idesc, abort_flag);
     } else if (warp < kStreamWarps) {
-      consume_items<D>(a, smem, st_full, st_empty, idesc, abort_flag);
+      if (a.unit_groups == 2)
+        consume_items<D, 2>(a, smem, st_full, st_empty, idesc, abort_flag);
+      else
+        consume_items<D, 1>(a, smem, st_full, st_empty, idesc, abort_flag);
     }
   }
   // the bulk copies of the merge below overwrite what was written here through the

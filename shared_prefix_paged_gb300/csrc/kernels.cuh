@@ -88,6 +88,8 @@ struct DecodeArgs {
   int prefix_ctas;           // num_kv_heads * pre.pairs * pre.n_splits (<= grid)
   int prefix_units;          // suffix units each prefix CTA streams after its range
   int merge_rows;            // rows per merge chunk (the merge tensor maps' box)
+  int unit_groups;           // 2: every suffix unit is one item (<= 128 keys) and two groups
+                             // of four warps take alternate units; 1: all eight warps
   int key_tiles;             // ceil(cpl / 64)
   int* bar_count;            // zero at launch; the kernel leaves it zero
   unsigned* bar_gen;         // any value; advanced by one per call
