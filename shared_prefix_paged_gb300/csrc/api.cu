@@ -570,13 +570,16 @@ int cascade_plan(const int32_t* block_table, int64_t bt_row_stride, int32_t num_
     shortest = std::min(shortest, used);
     min_computed = std::min(min_computed, num_computed_tokens[r]);
   }
-  int64_t ncpb = 0;
-  for (; ncpb < shortest; ++ncpb) {
-    const int32_t id = block_table[ncpb];
-    bool same = true;
-    for (int r = 1; r < num_reqs && same; ++r)
-      same = block_table[static_cast<int64_t>(r) * bt_row_stride + ncpb] == id;
-    if (!same) break;
+  // the longest run shared by every row = the shortest of each row's run in common with
+  // row 0, each bounded by what is left; rows are scanned in memory order
+  int64_t ncpb = shortest;
+  for (int r = 1; r < num_reqs && ncpb > 0; ++r) {
+    const int32_t* row = block_table + static_cast<int64_t>(r) * bt_row_stride;
+    int64_t k = 0;
+    while (k + 16 <= ncpb && std::memcmp(row + k, block_table + k, 16 * sizeof(int32_t)) == 0)
+      k += 16;  // 64-byte blocks first (the common case is a long shared run)
+    while (k < ncpb && row[k] == block_table[k]) ++k;
+    ncpb = k;
   }
   // §八 Step 2: blocks to tokens, cap to min(num_computed_tokens), floor to block_size
   int64_t cpl = ncpb * block_size;
