@@ -171,9 +171,9 @@ def _attn(fn_name, q, k_cache, v_cache, block_table, cu_seqlens_q, seqused_k, *,
         out = torch.empty_like(q)
     if lse is None:
         lse = torch.empty((total_q, hq), dtype=torch.float32, device=q.device)
-    need = workspace_size(n, total_q, max_seqlen_q, max_seqlen_k, cpl, hq, hkv, d)
-    if workspace is None or workspace.numel() < need:
-        workspace = alloc_workspace(need, q.device)
+    if workspace is None:  # a caller's workspace is checked by the library itself
+        workspace = alloc_workspace(
+            workspace_size(n, total_q, max_seqlen_q, max_seqlen_k, cpl, hq, hkv, d), q.device)
     args = [_ptr(q), _ptr(k_cache), _ptr(v_cache), num_blocks, _ptr(block_table),
             int(block_table.stride(0)), _ptr(cu_seqlens_q), _ptr(seqused_k), n, total_q,
             int(max_seqlen_q), int(max_seqlen_k)]
@@ -202,6 +202,8 @@ def cascade_attn(q, k_cache, v_cache, block_table, cu_seqlens_q, seqused_k, *, m
                  prefix_ranges=0):
     """Cascade attention (prefix phase + suffix phase + LSE merge) on device tensors.
 
+    workspace: a uint8 device tensor of at least workspace_size(...) bytes (allocated
+    here when None); one that is too small raises (CSP_ERR_WORKSPACE).
     phase_events: optional four torch.cuda.Event(enable_timing=True); when given, the
     call goes through cascade_attn_timed and records them between the kernels.
     schedule: SCHEDULE_TWO_KERNELS or SCHEDULE_SINGLE to override the cost model
