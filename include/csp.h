@@ -152,7 +152,10 @@ enum { CSP_SCHEDULE_TWO_KERNELS = 0, CSP_SCHEDULE_SINGLE = 1 };
  * shape on the current device.  Host integers, the same as the attention call will
  * get (common_prefix_len > 0).
  *   CSP_SCHEDULE_TWO_KERNELS : a prefix-phase kernel, then a paged kernel for the
- *                              suffix phase whose CTAs also merge (any batch);
+ *                              suffix phase (any batch); where a request and KV head
+ *                              have at most 16 query rows (query tokens x heads in
+ *                              the group) the paged kernel's CTAs also merge, for
+ *                              more rows a third kernel merges every row after both;
  *   CSP_SCHEDULE_SINGLE      : one cooperative kernel of one CTA per SM, for batches
  *                              where every request has at most 16 / (num_q_heads /
  *                              num_kv_heads) query tokens: some CTAs run ranges of the
@@ -228,8 +231,10 @@ CSP_API int cascade_attn_scheduled(const void* q, const void* k_cache, const voi
  * cascade_attn_timed — cascade_attn plus four CUDA events recorded on `stream`
  * between its kernels, for timing each phase.  Two-kernel schedule:
  * phase_events[0] before the prefix-phase kernel, [1] after it, [2] after the
- * suffix-phase kernel (whose CTAs finish the LSE merge), [3] at the end of the call
- * (the same point as [2]); with events between them, the two kernels run one after
+ * suffix-phase kernel (whose CTAs finish the LSE merge, or which is followed by the
+ * merge kernel: see csp_cascade_schedule), [3] at the end of the call (after the merge
+ * kernel where there is one, else the same point as [2]); with events between them,
+ * the kernels run one after
  * the other instead of overlapping, so the per-phase times add up to more than a
  * cascade_attn call takes; with common_prefix_len == 0, events [0] and [1] mark the
  * same point.  Single-kernel schedule (csp_cascade_schedule): [0] before the kernel,
