@@ -529,7 +529,7 @@ int attention_call(const void* q, const void* k_cache, const void* v_cache, int3
       return st;
     e = csp::launch_paged_tc(D, tm_q, tm_k, tm_v, ga, overlap, stream);
   } else {
-    e = csp::launch_paged(D, P.decode, ga, overlap, stream);
+    e = csp::launch_paged(D, ga, overlap, stream);
   }
   if (e != cudaSuccess) return cuda_fail(e);
   if ((e = mark(2)) != cudaSuccess) return cuda_fail(e);

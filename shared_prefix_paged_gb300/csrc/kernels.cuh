@@ -115,7 +115,7 @@ cudaError_t launch_prefix(int head_dim, const CUtensorMap& tm_q, const CUtensorM
 
 // after_prefix: launched right behind this call's prefix kernel on the same stream
 // (programmatic dependent launch, so it runs concurrently with it).
-cudaError_t launch_paged(int head_dim, bool decode, const PagedArgs& a, bool after_prefix,
+cudaError_t launch_paged(int head_dim, const PagedArgs& a, bool after_prefix,
                          cudaStream_t stream);
 
 // The same computation on tcgen05 for units of many rows (paged_tc.cu): one CTA per

@@ -5,17 +5,18 @@
 //
 // This work streams each request's private pages from HBM once and does little
 // arithmetic per byte, so the design aims at bandwidth:
-//  * one CTA per (request, KV head, row tile, key split); the rows are the request's
+//  * for decode-shaped rows: at most 16 per request and KV head (query tokens x heads
+//    in the group); more rows take the tcgen05 variant (paged_tc.cu);
+//  * one CTA per (request, KV head, key split); its rows are the request's
 //    (query, head-in-group) pairs of that KV head, so all GQA heads of a KV head
 //    share each page load;
 //  * pages are fetched with 16-byte cp.async (coalesced: 16 threads per 256-byte
-//    page row) into an XOR-swizzled shared tile of 64 keys, three stages deep;
+//    page row) into an XOR-swizzled shared tile of 64 keys, two stages deep;
 //    keys past the range are zero-filled and never read from the block table;
 //  * QK^T and PV run on warp-level bf16 MMA (m16n8k16) fed by ldmatrix; the online
 //    softmax keeps its row max / sum with warp shuffles inside each 4-lane row group;
-//  * decode rows (<= 16 per request and KV head): the four warps split the keys
-//    of every tile and merge (max, sum, O) through shared memory at the end;
-//    prefill rows: each warp owns 16 rows of a 64-row tile;
+//  * the four warps split the keys of every tile and merge (max, sum, O) through
+//    shared memory at the end;
 //  * split-KV (FlashDecoding, §九) over long ranges: each split writes a normalised
 //    bf16 partial + log2-sum-exp and the last split of a row group merges them with
 //    the prefix phase's partials (merge.cuh); a single split merges its own result
@@ -38,12 +39,11 @@ __device__ __forceinline__ uint32_t swz(int row, int chunk) {
   return static_cast<uint32_t>(row * (D * 2) + ((chunk ^ (row & 7)) << 4));
 }
 
-template <int D, bool kDecode>
+template <int D>
 struct PagedLayout {
-  // decode CTAs keep two 64-key tiles in flight (68 KB for D=128), so three fit on
-  // an SM, or one beside a prefix-phase CTA; prefill CTAs keep three
-  static constexpr int kStages = kDecode ? 2 : 3;
-  static constexpr int kRows = kDecode ? 16 : 64;
+  // two 64-key tiles in flight (68 KB for D=128), so three CTAs fit on an SM
+  static constexpr int kStages = 2;
+  static constexpr int kRows = 16;
   static constexpr int kQBytes = kRows * D * 2;
   static constexpr int kKVBytes = kTileKeys * D * 2;
   static constexpr int kQ = 0;
@@ -55,16 +55,16 @@ struct PagedLayout {
   // rows of D floats with a padded stride, then per-warp max and sum
   static constexpr int kORow = D + 8;
   static constexpr int kMergeBytes = 4 * 16 * kORow * 4 + 2 * 4 * 16 * 4;
-  static_assert(!kDecode || kMergeBytes <= 2 * kStages * kKVBytes, "merge scratch");
+  static_assert(kMergeBytes <= 2 * kStages * kKVBytes, "merge scratch");
 };
 
-template <int D, bool kDecode>
+template <int D>
 __global__ void __launch_bounds__(kThreads)
     paged_attn_kernel(const PagedArgs a) {
-  using L = PagedLayout<D, kDecode>;
+  using L = PagedLayout<D>;
   constexpr int kStages = L::kStages;
   constexpr int kChunks = D / 8;               // 16-byte chunks per row
-  constexpr int kWarpKeys = kDecode ? 16 : 64; // keys of a tile each warp handles
+  constexpr int kWarpKeys = 16;                // keys of a tile each warp handles
   constexpr int kNT = kWarpKeys / 8;           // S n-tiles per warp
   constexpr int kDT = D / 8;                   // O n-tiles
 
@@ -135,9 +135,8 @@ __global__ void __launch_bounds__(kThreads)
     cp_async_commit();
   }
 
-  // per-warp state: rows rbase .. rbase+15 (thread rows lane/4 and lane/4 + 8)
-  const int rbase = kDecode ? 0 : warp * 16;
-  const int kw0 = kDecode ? warp * 16 : 0;
+  // per-warp state: all 16 rows (thread rows lane/4 and lane/4 + 8)
+  const int kw0 = warp * 16;
   float o[kDT][4];
 #pragma unroll
   for (int i = 0; i < kDT; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
@@ -146,11 +145,10 @@ __global__ void __launch_bounds__(kThreads)
   int pos[2];
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
-    const int rho = row0 + rbase + (lane >> 2) + 8 * h;
+    const int rho = row0 + (lane >> 2) + 8 * h;
     pos[h] = rho < rows_total ? seq - q_len + rho / a.group : -1;  // -1: padding row
   }
   uint32_t qa[D / 16][4];
-  const bool warp_live = kDecode || (row0 + rbase < rows_total);
 
   for (int ti = 0; ti < n_tiles; ++ti) {
     cp_async_wait<kStages - 1>();  // groups 0..ti (tile ti, and Q with tile 0) landed
@@ -158,12 +156,12 @@ __global__ void __launch_bounds__(kThreads)
     if (ti == 0) {
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
-        const int row = rbase + (lane & 7) + ((lane >> 3) & 1) * 8;
+        const int row = (lane & 7) + ((lane >> 3) & 1) * 8;
         const int c = kk * 2 + (lane >> 4);
         ldmatrix_x4(sbase + L::kQ + swz<D>(row, c), qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3]);
       }
     }
-    if (warp_live) {
+    {
     const int stage = ti % kStages;
     const uint32_t sk = sbase + L::kK + stage * L::kKVBytes;
     const uint32_t sv = sbase + L::kV + stage * L::kKVBytes;
@@ -240,7 +238,7 @@ __global__ void __launch_bounds__(kThreads)
         mma_bf16_16816(o[2 * dp + 1], pa, b2, b3);
       }
     }
-    }  // warp_live
+    }
     __syncthreads();  // every warp is done with this stage
     if (ti + kStages < n_tiles) load_tile(ti + kStages, ti % kStages);
     cp_async_commit();
@@ -271,7 +269,7 @@ __global__ void __launch_bounds__(kThreads)
   // slots; several splits: write a partial and let the last split merge
   const bool merge_in_place = partial && a.n_splits == 1;
 
-  if constexpr (kDecode) {
+  {
     // merge the four warps' (m, l, O) of the same 16 rows through shared memory
     __syncthreads();
     float* s_o = reinterpret_cast<float*>(smem + L::kK);   // [4][16][kORow]
@@ -344,62 +342,24 @@ __global__ void __launch_bounds__(kThreads)
         if (lane == 0 && a.lse != nullptr) a.lse[orow] = lse2 * kLn2;
       }
     }
-  } else {
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const int rho = row0 + rbase + (lane >> 2) + 8 * h;
-      if (!warp_live || rho >= rows_total) continue;
-      const int qi = rho / a.group, j = rho % a.group;
-      const int64_t orow = static_cast<int64_t>(q0 + qi) * a.num_q_heads + g * a.group + j;
-      const float inv = l_run[h] > 0.f ? 1.f / l_run[h] : 0.f;
-      const float lse2 = l_run[h] > 0.f ? m_run[h] + log2f(l_run[h]) : -INFINITY;
-      __nv_bfloat16* dst;
-      if (partial) {
-        const int64_t prow = static_cast<int64_t>(a.n_prefix + split) * a.total_q *
-                                 a.num_q_heads + orow;
-        dst = a.part_o + prow * D;
-        if ((lane & 3) == 0) a.part_lse[prow] = lse2;
-      } else {
-        dst = a.out + orow * D;
-        if ((lane & 3) == 0 && a.lse != nullptr) a.lse[orow] = lse2 * kLn2;
-      }
-#pragma unroll
-      for (int dt = 0; dt < kDT; ++dt) {
-        const int d = dt * 8 + (lane & 3) * 2;
-        *reinterpret_cast<uint32_t*>(dst + d) = pack_bf16x2(o[dt][2 * h] * inv, o[dt][2 * h + 1] * inv);
-      }
-    }
   }
 
-  if (partial && !(kDecode && merge_in_place)) {
+  if (partial && !merge_in_place) {
+    // several splits: count in the row groups; the last split merges every slot
     const int tok_first = row0 / a.group;
     const int n_tok = (row0 + rows_here - 1) / a.group - tok_first + 1;
     grid_dependency_wait();  // prefix partials are complete and visible
-    if (merge_in_place) {
-      // one split: this CTA is the only suffix contributor of its rows (its own
-      // partial is in slot n_prefix, written above)
-      MergeArgs mm = m;
-      mm.n_count = 1;
-      __syncthreads();
-      __threadfence_block();
-      for (int k = warp; k < n_tok * a.group; k += kThreads / 32) {
-        const int64_t row = static_cast<int64_t>(q0 + tok_first + k / a.group) * a.num_q_heads +
-                            g * a.group + k % a.group;
-        merge_row_warp<D>(mm, row, lane, false, make_float4(0.f, 0.f, 0.f, 0.f), -INFINITY);
-      }
-    } else {
-      if constexpr (kDecode) __syncthreads();  // merge scratch no longer needed below
-      count_and_merge<D>(m, q0 + tok_first, n_tok, g, reinterpret_cast<int*>(smem + L::kLast));
-    }
+    __syncthreads();         // merge scratch no longer needed below
+    count_and_merge<D>(m, q0 + tok_first, n_tok, g, reinterpret_cast<int*>(smem + L::kLast));
   }
 }
 
-template <int D, bool kDecode>
+template <int D>
 cudaError_t launch_paged_t(const PagedArgs& a, bool after_prefix, cudaStream_t stream) {
-  using L = PagedLayout<D, kDecode>;
+  using L = PagedLayout<D>;
   const int smem = L::kEnd;
   static std::atomic<uint64_t> attr_done{0};
-  cudaError_t e = set_smem_once(paged_attn_kernel<D, kDecode>, smem, attr_done);
+  cudaError_t e = set_smem_once(paged_attn_kernel<D>, smem, attr_done);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(a.num_reqs * a.row_tiles, a.num_kv_heads, a.n_splits);
@@ -407,25 +367,21 @@ cudaError_t launch_paged_t(const PagedArgs& a, bool after_prefix, cudaStream_t s
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
-  // Right after the prefix kernel of the same call: start while it runs.  The two
-  // meet only through the row-group counters (atomics + fences), so this kernel
-  // never waits on the prefix grid.
+  // Right after the prefix kernel of the same call: start while it runs; the merge
+  // with the prefix slots waits for the prefix grid (griddepcontrol.wait).
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = after_prefix ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, paged_attn_kernel<D, kDecode>, a);
+  return cudaLaunchKernelEx(&cfg, paged_attn_kernel<D>, a);
 }
 
 }  // namespace
 
-cudaError_t launch_paged(int head_dim, bool decode, const PagedArgs& a, bool after_prefix,
+cudaError_t launch_paged(int head_dim, const PagedArgs& a, bool after_prefix,
                          cudaStream_t stream) {
-  if (head_dim == 64)
-    return decode ? launch_paged_t<64, true>(a, after_prefix, stream)
-                  : launch_paged_t<64, false>(a, after_prefix, stream);
-  return decode ? launch_paged_t<128, true>(a, after_prefix, stream)
-                : launch_paged_t<128, false>(a, after_prefix, stream);
+  if (head_dim == 64) return launch_paged_t<64>(a, after_prefix, stream);
+  return launch_paged_t<128>(a, after_prefix, stream);
 }
 
 }  // namespace csp
