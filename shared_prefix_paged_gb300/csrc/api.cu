@@ -575,9 +575,13 @@ int cascade_plan(const int32_t* block_table, int64_t bt_row_stride, int32_t num_
   int64_t ncpb = shortest;
   for (int r = 1; r < num_reqs && ncpb > 0; ++r) {
     const int32_t* row = block_table + static_cast<int64_t>(r) * bt_row_stride;
+    // the common case: the whole run so far is shared (one memcmp); otherwise find the
+    // first difference, 64-byte blocks first
+    if (std::memcmp(row, block_table, static_cast<size_t>(ncpb) * sizeof(int32_t)) == 0)
+      continue;
     int64_t k = 0;
     while (k + 16 <= ncpb && std::memcmp(row + k, block_table + k, 16 * sizeof(int32_t)) == 0)
-      k += 16;  // 64-byte blocks first (the common case is a long shared run)
+      k += 16;
     while (k < ncpb && row[k] == block_table[k]) ++k;
     ncpb = k;
   }
