@@ -298,7 +298,13 @@ class DeviceRun:
 
 def time_graph_steps(run: DeviceRun, path: str, steps: int, warmup: int, dist: Dist,
                      with_planner=True, clocks=None):
-    """Replay `steps` device steps from graphs; returns (elapsed_s, host_s, t0, t1)."""
+    """Replay `steps` device steps from graphs; returns (elapsed_s, host_s, t0, t1).
+
+    With the planner, the host plans one graph's worth of steps ahead: the plans of the
+    first R steps run before the timed region, and after each replay is queued the host
+    plans the next R steps while the GPU runs it (the last round plans steps that never
+    run).  The timed region thus holds exactly `steps` planner calls and `steps` device
+    steps, and the GPU never waits for the host at its start."""
     import torch
     R = run.R
     g = run.graph(path, R)
@@ -309,21 +315,22 @@ def time_graph_steps(run: DeviceRun, path: str, steps: int, warmup: int, dist: D
     torch.cuda.synchronize(run.dev)
     start = torch.cuda.Event(enable_timing=True)
     end = torch.cuda.Event(enable_timing=True)
+    rounds = [R] * (steps // R) + ([tail] if tail else [])
+    if with_planner:
+        for _ in range(rounds[0]):       # the first round's plans
+            run.plan()
     dist.barrier()
     torch.cuda.synchronize(run.dev)
     t0 = time.time()
     h0 = time.perf_counter()
     start.record()
-    for _ in range(steps // R):
+    for k, n in enumerate(rounds):
+        (g if n == R else g_tail).replay()
         if with_planner:
-            for _ in range(R):
+            # the next round's plans (after the last round: as many as the first
+            # round's, which ran before the region, so every step has one)
+            for _ in range(rounds[k + 1] if k + 1 < len(rounds) else rounds[0]):
                 run.plan()
-        g.replay()
-    if g_tail is not None:
-        if with_planner:
-            for _ in range(tail):
-                run.plan()
-        g_tail.replay()
     end.record()
     h1 = time.perf_counter()
     torch.cuda.synchronize(run.dev)
@@ -371,50 +378,94 @@ def phase_times(run: DeviceRun, rounds: int = 16, batches: int = 3):
 
 
 def e2e_steps(run: DeviceRun, steps: int):
-    """Public-API steps from pinned host buffers: H2D of q and the batch metadata, host
-    planner, cascade_attn, D2H of out and lse, then the host waits for the result."""
+    """Public-API steps from pinned host memory: one H2D copy of the step's inputs (q,
+    block table, cu_seqlens, seq_lens packed in one pinned buffer), the host planner
+    (csp.Planner), the attention call (csp.PreparedCall), one D2H copy of out and lse
+    (adjacent in one device buffer), then the host waits for the result.  Returns the
+    rate, the bytes copied each way per step, the step count and the average time of
+    each part (host: perf_counter; device: CUDA events on the stream)."""
     import torch
     from shared_prefix_paged_gb300 import csp
     b = run.b
-    q_h = b.q.pin_memory()
-    bt_h = torch.from_numpy(b.block_table).pin_memory()
-    cu_h = torch.from_numpy(b.cu_seqlens_q).pin_memory()
-    sl_h = torch.from_numpy(b.seq_lens).pin_memory()
-    out_h = torch.empty(b.q.shape, dtype=torch.bfloat16).pin_memory()
-    lse_h = torch.empty((b.total_q, b.num_q_heads), dtype=torch.float32).pin_memory()
-    q_d = torch.empty_like(run.q[0])
-    bt_d, cu_d, sl_d = torch.empty_like(run.bt), torch.empty_like(run.cu), torch.empty_like(run.sl)
-    out_d, lse_d = run.out[0], run.lse[0]
-    h2d = sum(t.numel() * t.element_size() for t in (q_h, bt_h, cu_h, sl_h))
-    d2h = out_h.numel() * 2 + lse_h.numel() * 4
-    stream = torch.cuda.current_stream(run.dev)
+    dev = run.dev
+    parts = [("q", b.q.view(torch.int16).reshape(-1)),
+             ("bt", torch.from_numpy(np.ascontiguousarray(b.block_table)).reshape(-1)),
+             ("cu", torch.from_numpy(b.cu_seqlens_q)),
+             ("sl", torch.from_numpy(b.seq_lens))]
+    sizes = [t.numel() * t.element_size() for _, t in parts]
+    offs = np.cumsum([0] + [(n + 255) // 256 * 256 for n in sizes])
+    in_h = torch.empty(int(offs[-1]), dtype=torch.uint8).pin_memory()
+    for (name, t), o, n in zip(parts, offs, sizes):
+        in_h[o:o + n].copy_(t.contiguous().view(torch.uint8))
+    in_d = torch.empty(int(offs[-1]), dtype=torch.uint8, device=dev)
+    q_d = in_d[offs[0]:offs[0] + sizes[0]].view(torch.bfloat16).view(b.q.shape)
+    bt_d = in_d[offs[1]:offs[1] + sizes[1]].view(torch.int32).view(b.block_table.shape)
+    cu_d = in_d[offs[2]:offs[2] + sizes[2]].view(torch.int32)
+    sl_d = in_d[offs[3]:offs[3] + sizes[3]].view(torch.int32)
+    o_bytes = b.q.numel() * 2
+    l_bytes = b.total_q * b.num_q_heads * 4
+    res_d = torch.empty(o_bytes + l_bytes, dtype=torch.uint8, device=dev)
+    res_h = torch.empty(o_bytes + l_bytes, dtype=torch.uint8).pin_memory()
+    out_d = res_d[:o_bytes].view(torch.bfloat16).view(b.q.shape)
+    lse_d = res_d[o_bytes:].view(torch.float32).view(b.total_q, b.num_q_heads)
+    stream = torch.cuda.current_stream(dev)
+    planner = csp.Planner(b.block_table, b.seq_lens, b.num_computed_tokens,
+                          block_size=b.block_size, num_q_heads=b.num_q_heads,
+                          num_kv_heads=b.num_kv_heads, head_dim=b.head_dim)
+    calls = [csp.PreparedCall(q_d, run.k[i], run.v[i], bt_d, cu_d, sl_d,
+                              max_seqlen_q=b.max_seqlen_q, max_seqlen_k=b.max_seqlen_k,
+                              softmax_scale=b.scale, out=out_d, lse=lse_d, workspace=run.ws,
+                              stream=stream) for i in range(run.R)]
+    h2d = int(sum(sizes))
+    d2h = o_bytes + l_bytes
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+    acc = np.zeros(6)
 
-    def one(i):
-        q_d.copy_(q_h, non_blocking=True)
-        bt_d.copy_(bt_h, non_blocking=True)
-        cu_d.copy_(cu_h, non_blocking=True)
-        sl_d.copy_(sl_h, non_blocking=True)
-        cpl, use = csp.cascade_plan(b.block_table, b.seq_lens, b.num_computed_tokens,
-                                    block_size=b.block_size, num_q_heads=b.num_q_heads,
-                                    num_kv_heads=b.num_kv_heads, head_dim=b.head_dim)
-        kw = dict(max_seqlen_q=b.max_seqlen_q, max_seqlen_k=b.max_seqlen_k,
-                  softmax_scale=b.scale, out=out_d, lse=lse_d, workspace=run.ws)
-        if use:
-            csp.cascade_attn(q_d, run.k[i], run.v[i], bt_d, cu_d, sl_d, common_prefix_len=cpl,
-                             **kw)
-        else:
-            csp.paged_attn(q_d, run.k[i], run.v[i], bt_d, cu_d, sl_d, **kw)
-        out_h.copy_(out_d, non_blocking=True)
-        lse_h.copy_(lse_d, non_blocking=True)
+    def one(i, timed):
+        h0 = time.perf_counter()
+        if timed:
+            ev[0].record(stream)
+        in_d.copy_(in_h, non_blocking=True)
+        if timed:
+            ev[1].record(stream)
+        h1 = time.perf_counter()
+        cpl, use = planner()
+        h2 = time.perf_counter()
+        calls[i](cpl, use)
+        h3 = time.perf_counter()
+        if timed:
+            ev[2].record(stream)
+        res_h.copy_(res_d, non_blocking=True)
+        if timed:
+            ev[3].record(stream)
         stream.synchronize()
+        h4 = time.perf_counter()
+        return np.array([h1 - h0, h2 - h1, h3 - h2, h4 - h3, 0.0, 0.0])
 
     for i in range(5):
-        one(i % run.R)
+        one(i % run.R, False)
     t0 = time.perf_counter()
     for s in range(steps):
-        one(s % run.R)
+        one(s % run.R, False)
     el = time.perf_counter() - t0
-    return b.total_q * steps / el, h2d, d2h, steps
+    # the breakdown, from separate instrumented steps (events add host work)
+    n_bd = min(steps, 500)
+    dev_ms = np.zeros(3)
+    for s in range(n_bd):
+        acc += one(s % run.R, True)
+        dev_ms += [ev[0].elapsed_time(ev[1]), ev[1].elapsed_time(ev[2]),
+                   ev[2].elapsed_time(ev[3])]
+    acc /= n_bd
+    dev_ms /= n_bd
+    breakdown = {"host_h2d_issue_us": round(acc[0] * 1e6, 2),
+                 "host_planner_us": round(acc[1] * 1e6, 2),
+                 "host_attention_call_us": round(acc[2] * 1e6, 2),
+                 "host_d2h_issue_and_wait_us": round(acc[3] * 1e6, 2),
+                 "device_h2d_us": round(dev_ms[0] * 1e3, 2),
+                 "device_plan_to_kernel_end_us": round(dev_ms[1] * 1e3, 2),
+                 "device_d2h_us": round(dev_ms[2] * 1e3, 2),
+                 "step_us": round(el / steps * 1e6, 2)}
+    return b.total_q * steps / el, h2d, d2h, steps, breakdown
 
 
 def cpu_oracle_rate(b, seconds: float, rng_seed=0):
@@ -546,7 +597,8 @@ def run_ours(args, dist: Dist):
                         if path == "cascade" else "flat", "prefix_ranges": run.prefix_ranges,
             "l2": f"inputs larger than L2: {R} rotating copies of q and the KV cache",
             "step": "host cascade_plan + device path replayed from a CUDA graph of "
-                    f"{R} steps", "parallelism": f"replicas x{dist.world}"},
+                    f"{R} steps (the host plans the next {R} steps while the GPU runs "
+                    "these)", "parallelism": f"replicas x{dist.world}"},
         "us_per_call": round(us_call, 3),
         "kv_gbs": round(kv_bytes / (us_call * 1e-6) / 1e9, 1),
         "min_bytes_per_call": int(min_bytes),
@@ -589,12 +641,13 @@ def run_ours(args, dist: Dist):
                           "kv_bytes": int(accounting.flat_kv_tokens(b.seq_lens) *
                                           accounting.kv_bytes_per_token(b.num_kv_heads,
                                                                         b.head_dim))}
-        e_qps, h2d, d2h, e_steps = e2e_steps(run, min(K, 3000))
+        e_qps, h2d, d2h, e_steps, bd = e2e_steps(run, min(K, 3000))
         e_total, _ = aggregate(dist, e_qps, 1.0)
         result["e2e"] = {"value": round(e_total, 1), "unit": UNIT, "h2d_bytes_per_step": h2d,
-                         "d2h_bytes_per_step": d2h, "steps": e_steps,
-                         "note": "pinned host q + block table + cu_seqlens + seq_lens in, "
-                                 "out + lse back, host waits each step; KV cache resident"}
+                         "d2h_bytes_per_step": d2h, "steps": e_steps, "breakdown": bd,
+                         "note": "one pinned H2D copy of q + block table + cu_seqlens + "
+                                 "seq_lens, host planner, the attention call, one D2H copy "
+                                 "of out + lse, host waits each step; KV cache resident"}
         if dist.rank == 0 and dist.world == 1:
             rate, threads, rows = cpu_oracle_rate(b, args.cpu_seconds)
             result["cpu_baseline"] = {"value": round(rate, 3), "unit": UNIT, "cores": threads,

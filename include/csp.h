@@ -128,6 +128,35 @@ CSP_API int cascade_plan(const int32_t* block_table, int64_t bt_row_stride, int3
                  int32_t* common_prefix_len_out, int32_t* use_cascade_out);
 
 /*
+ * csp_validate_batch — optional host-side check of a batch before it is launched.
+ * Host pointers only; no device work.  The kernels read the block ids they are given
+ * without a bounds check (by TMA or 16-byte copies), so an id past the cache reads
+ * whatever memory lies there; a caller that cannot vouch for its tables runs this on
+ * the host copies first and launches only on CSP_OK.
+ *
+ * Checks, in this order: num_reqs >= 0, block_size > 0, num_blocks > 0; for every
+ * request r: 0 <= seq_lens[r] and cdiv(seq_lens[r], block_size) <= bt_row_stride;
+ * every block id a request uses (its first cdiv(seq_lens[r], block_size) entries —
+ * the same entries cascade_plan scans and the kernels read) lies in [0, num_blocks);
+ * if cu_seqlens_q is given: cu_seqlens_q[0] == 0 and
+ * 0 <= cu_seqlens_q[r+1] - cu_seqlens_q[r] <= seq_lens[r]; common_prefix_len is a
+ * multiple of block_size in [0, min_r seq_lens[r]] (0 for num_reqs == 0).
+ *
+ *   block_table   int32 [num_reqs, bt_row_stride]  host
+ *   seq_lens      int32 [num_reqs]  host
+ *   cu_seqlens_q  int32 [num_reqs + 1]  host, or NULL to skip the query checks
+ *   bad_index_out NULL, or receives the flat index (r * bt_row_stride + j) of the
+ *                 first out-of-range block id, or -1 when the first problem is not a
+ *                 block id (and -1 on CSP_OK)
+ * Returns CSP_OK or CSP_ERR_INVALID_ARG (the first problem found).
+ */
+CSP_API int csp_validate_batch(const int32_t* block_table, int64_t bt_row_stride,
+                               int32_t num_reqs, const int32_t* seq_lens,
+                               const int32_t* cu_seqlens_q, int32_t block_size,
+                               int32_t num_blocks, int32_t common_prefix_len,
+                               int64_t* bad_index_out);
+
+/*
  * csp_workspace_size — bytes of device workspace that cascade_attn (with this
  * common_prefix_len) or paged_attn (common_prefix_len = 0) needs for this batch
  * shape on the current device.  All arguments are host integers, the same as the
@@ -266,14 +295,19 @@ CSP_API int cascade_attn_timed(const void* q, const void* k_cache, const void* v
  * device code is loaded, and held until the process exits).  Nothing is allocated
  * or freed by this call.
  *
- * The first call on a device looks up that array's device address (once per device,
- * with the device current); make that first call before any stream capture.  Every
+ * The first call on a device looks up that array's device address (once per device
+ * and context, with the device current); make that first call before any stream
+ * capture.  A context that is destroyed and created again (cudaDeviceReset) gets a new
+ * array, whose address the next call looks up the same way.  Every
  * call on a device shares the one array: calls that can run at the same time on the
  * GPU (different streams, no ordering between them) race and corrupt each other's
  * results; order them on one stream.  The array keeps the previous call's contents;
  * each call clears the status word at its start itself.  A batch whose workspace
  * (csp_workspace_size) exceeds 16 MiB is rejected with CSP_ERR_WORKSPACE before
- * anything is launched.  Other arguments, layouts and errors: as for cascade_attn.
+ * anything is launched.  A bounded wait inside the kernels that gives up writes
+ * CSP_ERR_TIMEOUT into the array's status word, as for a caller's workspace: read it
+ * with csp_noalloc_status after the call and before the next one (each call clears
+ * it).  Other arguments, layouts and errors: as for cascade_attn.
  */
 CSP_API int cascade_attn_noalloc(const void* q, const void* k_cache, const void* v_cache,
                                  int32_t num_blocks, const int32_t* block_table,
@@ -283,6 +317,16 @@ CSP_API int cascade_attn_noalloc(const void* q, const void* k_cache, const void*
                                  int32_t common_prefix_len, int32_t block_size,
                                  int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
                                  float softmax_scale, void* out, float* lse, void* stream);
+
+/*
+ * csp_noalloc_status — the status word of the array cascade_attn_noalloc uses on the
+ * current device, copied to the host (a blocking copy on `stream`; order it after the
+ * call it checks).  0: the last call's kernels reported no problem; CSP_ERR_TIMEOUT: a
+ * bounded wait gave up and that call's out/lse are not valid.  Writes *status_out.
+ * No counterpart on the pages (it belongs to cascade_attn_noalloc).  Allocates
+ * nothing.
+ */
+CSP_API int csp_noalloc_status(void* stream, int32_t* status_out);
 
 /*
  * paged_attn — the standard path (§五, §十): request r attends causally to all of

@@ -32,7 +32,7 @@ DTYPE_BF16, DTYPE_F32 = 0, 1
 EXPORTS = ("cascade_plan", "csp_workspace_size", "cascade_attn", "cascade_attn_timed",
            "cascade_attn_scheduled", "paged_attn", "merge_states", "csp_workspace_status",
            "csp_status_string", "csp_last_cuda_error", "csp_version", "cascade_attn_noalloc",
-           "csp_cascade_schedule")
+           "csp_noalloc_status", "csp_cascade_schedule", "csp_validate_batch")
 
 _lock = threading.Lock()
 _lib: Optional[ctypes.CDLL] = None
@@ -77,12 +77,13 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         lib.paged_attn.argtypes = attn + tail
         lib.merge_states.argtypes = [p, p, p, p, p, p, i32, i32, i32, i32, p]
         lib.csp_workspace_status.argtypes = [p, p, p]
+        lib.csp_validate_batch.argtypes = [p, i64, i32, p, p, i32, i32, i32, p]
         lib.csp_status_string.argtypes = [ctypes.c_int]
         lib.csp_status_string.restype = ctypes.c_char_p
         for name in ("cascade_plan", "csp_workspace_size", "cascade_attn", "cascade_attn_timed",
                      "cascade_attn_scheduled", "paged_attn",
                      "merge_states", "csp_workspace_status", "csp_last_cuda_error",
-                     "csp_version", "csp_cascade_schedule"):
+                     "csp_version", "csp_cascade_schedule", "csp_validate_batch"):
             getattr(lib, name).restype = ctypes.c_int
         _lib = lib
         return lib
@@ -115,6 +116,82 @@ def cascade_plan(block_table, seq_lens, num_computed_tokens, *, block_size=16, n
                             block_size, num_q_heads, num_kv_heads, head_dim, num_sms, mode,
                             ctypes.byref(cpl), ctypes.byref(use)), "cascade_plan")
     return int(cpl.value), bool(use.value)
+
+
+def validate_batch(block_table, seq_lens, cu_seqlens_q=None, *, block_size=16, num_blocks,
+                   common_prefix_len=0):
+    """csp_validate_batch on host arrays: (status, flat index of the first out-of-range
+    block id or -1).  Raises nothing; CSP_OK means the batch may be launched."""
+    lib = load()
+    bt = _host_i32(block_table)
+    sl = _host_i32(seq_lens)
+    cu = None if cu_seqlens_q is None else _host_i32(cu_seqlens_q)
+    n = int(sl.shape[0])
+    stride = int(bt.shape[1]) if bt.ndim == 2 else 0
+    bad = ctypes.c_int64(0)
+    st = lib.csp_validate_batch(bt.ctypes.data if bt.size else None, stride, n,
+                                sl.ctypes.data if n else None,
+                                None if cu is None else cu.ctypes.data, int(block_size),
+                                int(num_blocks), int(common_prefix_len), ctypes.byref(bad))
+    return int(st), int(bad.value)
+
+
+class Planner:
+    """cascade_plan over fixed host arrays (numpy int32, kept alive here), with its
+    arguments marshalled once: each call passes the arrays' current contents, so a
+    caller that rewrites them in place between steps re-plans without re-marshalling."""
+
+    def __init__(self, block_table, seq_lens, num_computed_tokens, *, block_size=16,
+                 num_q_heads=32, num_kv_heads=8, head_dim=128, num_sms=0, mode=MODE_AUTO):
+        self._lib = load()
+        self.block_table = _host_i32(block_table)
+        self.seq_lens = _host_i32(seq_lens)
+        self.num_computed_tokens = _host_i32(num_computed_tokens)
+        self._cpl = ctypes.c_int32(0)
+        self._use = ctypes.c_int32(0)
+        n = int(self.seq_lens.shape[0])
+        bt = self.block_table
+        self._args = (bt.ctypes.data if bt.size else None,
+                      int(bt.shape[1]) if bt.ndim == 2 else 0, n,
+                      self.seq_lens.ctypes.data if n else None,
+                      self.num_computed_tokens.ctypes.data if n else None, block_size,
+                      num_q_heads, num_kv_heads, head_dim, num_sms, mode,
+                      ctypes.byref(self._cpl), ctypes.byref(self._use))
+
+    def __call__(self):
+        """(common_prefix_len, use_cascade) for the arrays' current contents."""
+        _check(self._lib.cascade_plan(*self._args), "cascade_plan")
+        return self._cpl.value, self._use.value != 0
+
+
+class PreparedCall:
+    """One attention call (cascade_attn or paged_attn) on fixed device tensors, its
+    arguments marshalled once.  Calling it launches on `stream` with the step's prefix
+    length: the tensors' current contents are the step's inputs and outputs."""
+
+    def __init__(self, q, k_cache, v_cache, block_table, cu_seqlens_q, seqused_k, *,
+                 max_seqlen_q, max_seqlen_k, softmax_scale, out, lse, workspace, stream=None):
+        self._lib = load()
+        total_q, hq, d = q.shape
+        num_blocks, bs, hkv, _ = k_cache.shape
+        n = int(seqused_k.shape[0])
+        self._keep = (q, k_cache, v_cache, block_table, cu_seqlens_q, seqused_k, out, lse,
+                      workspace)
+        self._head = [_ptr(q), _ptr(k_cache), _ptr(v_cache), num_blocks, _ptr(block_table),
+                      int(block_table.stride(0)), _ptr(cu_seqlens_q), _ptr(seqused_k), n,
+                      total_q, int(max_seqlen_q), int(max_seqlen_k)]
+        self._tail = [bs, hq, hkv, d, ctypes.c_float(float(softmax_scale)), _ptr(out),
+                      _ptr(lse), _ptr(workspace), workspace.numel(),
+                      _stream_ptr(stream, q.device)]
+        self._cascade = self._lib.cascade_attn
+        self._paged = self._lib.paged_attn
+
+    def __call__(self, common_prefix_len: int, use_cascade: bool = True) -> None:
+        if use_cascade:
+            st = self._cascade(*self._head, int(common_prefix_len), *self._tail)
+            _check(st, "cascade_attn")
+        else:
+            _check(self._paged(*self._head, *self._tail), "paged_attn")
 
 
 def workspace_size(num_reqs, total_q, max_seqlen_q, max_seqlen_k, common_prefix_len,
@@ -160,13 +237,20 @@ def alloc_workspace(nbytes: int, device):
 
 def _attn(fn_name, q, k_cache, v_cache, block_table, cu_seqlens_q, seqused_k, *, max_seqlen_q,
           max_seqlen_k, softmax_scale, common_prefix_len=None, out=None, lse=None,
-          workspace=None, stream=None, phase_events=None, schedule=None, prefix_ranges=0):
+          workspace=None, stream=None, phase_events=None, schedule=None, prefix_ranges=0,
+          validate=None):
     import torch
     lib = load()
     total_q, hq, d = q.shape
     num_blocks, bs, hkv, _ = k_cache.shape
     n = int(seqused_k.shape[0])
     cpl = 0 if common_prefix_len is None else int(common_prefix_len)
+    if validate is not None:
+        # opt-in: host copies (block_table, seq_lens, cu_seqlens_q) checked by the
+        # library before anything is launched
+        st, bad = validate_batch(*validate, block_size=bs, num_blocks=num_blocks,
+                                 common_prefix_len=cpl)
+        _check(st, f"csp_validate_batch (first bad block-table index {bad})")
     if out is None:
         out = torch.empty_like(q)
     if lse is None:
@@ -199,9 +283,12 @@ def _attn(fn_name, q, k_cache, v_cache, block_table, cu_seqlens_q, seqused_k, *,
 def cascade_attn(q, k_cache, v_cache, block_table, cu_seqlens_q, seqused_k, *, max_seqlen_q,
                  max_seqlen_k, common_prefix_len, softmax_scale, out=None, lse=None,
                  workspace=None, stream=None, phase_events=None, schedule=None,
-                 prefix_ranges=0):
+                 prefix_ranges=0, validate=None):
     """Cascade attention (prefix phase + suffix phase + LSE merge) on device tensors.
 
+    validate: optional host copies (block_table, seq_lens, cu_seqlens_q) that the
+    library checks (csp_validate_batch) before launching; a bad batch raises
+    CspError(CSP_ERR_INVALID_ARG) and nothing runs on the device.
     workspace: a uint8 device tensor of at least workspace_size(...) bytes (allocated
     here when None); one that is too small raises (CSP_ERR_WORKSPACE).
     phase_events: optional four torch.cuda.Event(enable_timing=True); when given, the
@@ -214,16 +301,18 @@ def cascade_attn(q, k_cache, v_cache, block_table, cu_seqlens_q, seqused_k, *, m
                  max_seqlen_q=max_seqlen_q, max_seqlen_k=max_seqlen_k,
                  softmax_scale=softmax_scale, common_prefix_len=common_prefix_len, out=out,
                  lse=lse, workspace=workspace, stream=stream, phase_events=phase_events,
-                 schedule=schedule, prefix_ranges=prefix_ranges)
+                 schedule=schedule, prefix_ranges=prefix_ranges, validate=validate)
 
 
 def paged_attn(q, k_cache, v_cache, block_table, cu_seqlens_q, seqused_k, *, max_seqlen_q,
-               max_seqlen_k, softmax_scale, out=None, lse=None, workspace=None, stream=None):
-    """Standard (flat) paged attention on device tensors."""
+               max_seqlen_k, softmax_scale, out=None, lse=None, workspace=None, stream=None,
+               validate=None):
+    """Standard (flat) paged attention on device tensors (validate: as for
+    cascade_attn)."""
     return _attn("paged_attn", q, k_cache, v_cache, block_table, cu_seqlens_q, seqused_k,
                  max_seqlen_q=max_seqlen_q, max_seqlen_k=max_seqlen_k,
                  softmax_scale=softmax_scale, out=out, lse=lse, workspace=workspace,
-                 stream=stream)
+                 stream=stream, validate=validate)
 
 
 def merge_states(prefix_out, prefix_lse, suffix_out, suffix_lse, *, out=None, out_lse=None,

@@ -1,6 +1,7 @@
 // api.cu — the C ABI declared in include/csp.h: argument checks, the common-prefix
 // planner, the launch plan (tiles, key splits, workspace partition), TMA tensor-map
 // encoding and the launch sequence.  Everything here runs on the host.
+#include <climits>
 #include <algorithm>
 #include <atomic>
 #include <cmath>
@@ -608,8 +609,8 @@ int cascade_plan(const int32_t* block_table, int64_t bt_row_stride, int32_t num_
       // GB300 rule, fitted to a cascade-vs-flat sweep of N in {4..256} x P in
       // {128..16384} (S = 128) on one GB300: cascade when it cuts the KV tokens the
       // standard path streams by at least 1.8x (the prefix read once instead of N
-      // times).  On that grid it is never more than 5% slower than the better path;
-      // the pages' thresholds (prefix >= 256, batch >= 8) lost up to 2x at N = 4.
+      // times).  On that grid it was never more than 2% slower than the better path;
+      // the pages' thresholds (prefix >= 256, batch >= 8) lost up to 2.2x at N = 4.
       int64_t flat_tokens = 0, casc_tokens = cpl;
       for (int r = 0; r < num_reqs; ++r) {
         flat_tokens += seq_lens[r];
@@ -624,6 +625,40 @@ int cascade_plan(const int32_t* block_table, int64_t bt_row_stride, int32_t num_
     }
   }
   *use_cascade_out = use;
+  return CSP_OK;
+}
+
+int csp_validate_batch(const int32_t* block_table, int64_t bt_row_stride, int32_t num_reqs,
+                       const int32_t* seq_lens, const int32_t* cu_seqlens_q,
+                       int32_t block_size, int32_t num_blocks, int32_t common_prefix_len,
+                       int64_t* bad_index_out) {
+  if (bad_index_out) *bad_index_out = -1;
+  if (num_reqs < 0 || block_size <= 0 || num_blocks <= 0 || bt_row_stride < 0)
+    return CSP_ERR_INVALID_ARG;
+  if (num_reqs > 0 && (!block_table || !seq_lens)) return CSP_ERR_INVALID_ARG;
+  int32_t min_len = num_reqs > 0 ? INT32_MAX : 0;
+  for (int32_t r = 0; r < num_reqs; ++r) {
+    const int32_t len = seq_lens[r];
+    if (len < 0) return CSP_ERR_INVALID_ARG;
+    min_len = len < min_len ? len : min_len;
+    const int64_t pages = (static_cast<int64_t>(len) + block_size - 1) / block_size;
+    if (pages > bt_row_stride) return CSP_ERR_INVALID_ARG;
+    const int32_t* row = block_table + static_cast<int64_t>(r) * bt_row_stride;
+    for (int64_t j = 0; j < pages; ++j) {
+      if (row[j] < 0 || row[j] >= num_blocks) {
+        if (bad_index_out) *bad_index_out = static_cast<int64_t>(r) * bt_row_stride + j;
+        return CSP_ERR_INVALID_ARG;
+      }
+    }
+    if (cu_seqlens_q) {
+      if (r == 0 && cu_seqlens_q[0] != 0) return CSP_ERR_INVALID_ARG;
+      const int64_t ql = static_cast<int64_t>(cu_seqlens_q[r + 1]) - cu_seqlens_q[r];
+      if (ql < 0 || ql > len) return CSP_ERR_INVALID_ARG;
+    }
+  }
+  if (common_prefix_len < 0 || common_prefix_len % block_size != 0 ||
+      common_prefix_len > min_len)
+    return CSP_ERR_INVALID_ARG;
   return CSP_OK;
 }
 

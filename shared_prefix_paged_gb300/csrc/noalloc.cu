@@ -8,6 +8,8 @@
 // cascade_attn needs for its split partial results.  This entry point gives them
 // one: a fixed array in the library's own device memory, reserved when the library's
 // device code is loaded on a GPU and held until the process exits.
+#include <cuda.h>
+
 #include <mutex>
 
 #include "csp.h"
@@ -22,23 +24,63 @@ static __device__ __align__(256) unsigned char csp_noalloc_scratch[kScratchBytes
 namespace {
 
 std::mutex g_setup_mutex;
-void* g_scratch_addr[64] = {};
+
+// The array's device address on one device, valid for the context it was looked up
+// in: a context torn down and created again (cudaDeviceReset, for one) reloads the
+// library's device code, and the array with it, at another address.
+struct ScratchEntry {
+  unsigned long long ctx_id;
+  void* addr;
+};
+ScratchEntry g_scratch[64] = {};
+
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long*);
+
+// Identity of the calling thread's current context (0 if it cannot be read).
+unsigned long long current_context_id() {
+  static CtxGetCurrentFn get_current = nullptr;
+  static CtxGetIdFn get_id = nullptr;
+  static bool looked_up = false;
+  if (!looked_up) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<CtxGetCurrentFn>(p);
+    p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<CtxGetIdFn>(p);
+    looked_up = true;
+  }
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (get_current && get_id && get_current(&ctx) == CUDA_SUCCESS && ctx != nullptr &&
+      get_id(ctx, &id) == CUDA_SUCCESS)
+    return id;
+  return 0;
+}
 
 // Device address of the array on the current device.  The symbol's name in host
-// code only stands in for it; the real address comes from the runtime, once per
-// device, with that device current.
+// code only stands in for it; the real address comes from the runtime, with that
+// device current, once per device and context.
 int scratch_address(void** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return CSP_ERR_CUDA;
   if (dev < 0 || dev >= 64) return CSP_ERR_UNSUPPORTED;
   std::lock_guard<std::mutex> lock(g_setup_mutex);
-  if (g_scratch_addr[dev] == nullptr) {
+  const unsigned long long ctx = current_context_id();
+  ScratchEntry& e = g_scratch[dev];
+  if (e.addr == nullptr || ctx == 0 || e.ctx_id != ctx) {
+    // (this lookup also makes the device's primary context current if none is)
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, csp_noalloc_scratch) != cudaSuccess || p == nullptr)
       return CSP_ERR_CUDA;
-    g_scratch_addr[dev] = p;
+    e.addr = p;
+    e.ctx_id = ctx != 0 ? ctx : current_context_id();
   }
-  *out = g_scratch_addr[dev];
+  *out = e.addr;
   return CSP_OK;
 }
 
@@ -71,4 +113,13 @@ extern "C" int cascade_attn_noalloc(const void* q, const void* k_cache, const vo
                       cu_seqlens_q, seqused_k, num_reqs, total_q, max_seqlen_q, max_seqlen_k,
                       common_prefix_len, block_size, num_q_heads, num_kv_heads, head_dim,
                       softmax_scale, out, lse, scratch, kScratchBytes, stream);
+}
+
+extern "C" int csp_noalloc_status(void* stream, int32_t* status_out) {
+  if (!status_out) return CSP_ERR_INVALID_ARG;
+  void* scratch = nullptr;
+  int st = scratch_address(&scratch);
+  if (st != CSP_OK) return st;
+  // the status word is the array's first 4 bytes (the workspace header's)
+  return csp_workspace_status(scratch, stream, status_out);
 }

@@ -3,15 +3,26 @@ the C-ABI paths, and compare with the oracle at the stated tolerances."""
 
 from __future__ import annotations
 
+import json
+import os
+
 import numpy as np
 import torch
 
 import oracle
 from shared_prefix_paged_gb300 import csp
 
-# bf16 output: max-abs error <= 2e-2; fp32 LSE: |error| <= 1e-3 * max(1, |lse|)
+# bf16 output: max-abs error <= 2e-2; fp32 LSE: |error| <= 1e-3 * max(1, |lse|).  The
+# LSE bound is relative with a floor of 1: |lse| can sit near 0 (a row whose scores sum
+# to about 1), where a purely relative bound would demand more than fp32 accumulation
+# of the sum gives.
 OUT_TOL = 2e-2
 LSE_REL = 1e-3
+
+# When set, every comparison appends one JSON line (case, max-abs out error, worst
+# LSE error as a fraction of its bound) to this file: the margins left under the
+# tolerances are then measured, not argued.
+_LOG = os.environ.get("CSP_PARITY_LOG")
 
 
 def to_device(b, device="cuda"):
@@ -67,5 +78,9 @@ def compare(out, lse, ref_o, ref_l, rows=None, what=""):
     lerr = np.abs(l - ref_l)
     bound = LSE_REL * np.maximum(1.0, np.abs(ref_l))
     worst = float((lerr / bound).max(initial=0.0))
+    if _LOG:
+        with open(_LOG, "a") as f:
+            f.write(json.dumps({"case": what, "out_err": err, "lse_frac": worst,
+                                "rows": int(o.shape[0])}) + "\n")
     assert worst <= 1.0, f"{what}: lse error {worst:.2f}x the bound"
     return err

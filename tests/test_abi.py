@@ -91,3 +91,58 @@ def test_planner_modes_and_errors():
         csp.cascade_plan(b.block_table[:, :3], b.seq_lens, b.num_computed_tokens)  # row too short
     with pytest.raises(csp.CspError):
         csp.cascade_plan(*args, mode=9)
+
+
+def test_validate_batch_accepts_generated_batches():
+    for name in ("tiny", "decode", "chunked", "chunked_cap"):
+        b = workloads.by_name(name)
+        cpl, _ = csp.cascade_plan(b.block_table, b.seq_lens, b.num_computed_tokens,
+                                  block_size=b.block_size)
+        assert csp.validate_batch(b.block_table, b.seq_lens, b.cu_seqlens_q,
+                                  block_size=b.block_size, num_blocks=b.num_blocks,
+                                  common_prefix_len=cpl) == (csp.CSP_OK, -1)
+
+
+def test_validate_batch_rejects_bad_tables():
+    b = workloads.tiny_decode()
+    bt = b.block_table.copy()
+    w = bt.shape[1]
+    ok = dict(block_size=16, num_blocks=b.num_blocks)
+    # an id past the cache in a used entry: rejected, its flat index reported
+    used = (int(b.seq_lens[3]) + 15) // 16
+    bt[3, used - 1] = b.num_blocks
+    assert csp.validate_batch(bt, b.seq_lens, b.cu_seqlens_q, **ok) == \
+        (csp.CSP_ERR_INVALID_ARG, 3 * w + used - 1)
+    bt[3, used - 1] = -1
+    assert csp.validate_batch(bt, b.seq_lens, **ok)[0] == csp.CSP_ERR_INVALID_ARG
+    # the same id past the row's used entries is never read: accepted
+    bt = b.block_table.copy()
+    if used < w:
+        bt[3, used] = 10 ** 6
+        assert csp.validate_batch(bt, b.seq_lens, **ok)[0] == csp.CSP_OK
+    # lengths and queries
+    sl = b.seq_lens.copy()
+    sl[0] = -1
+    assert csp.validate_batch(b.block_table, sl, **ok) == (csp.CSP_ERR_INVALID_ARG, -1)
+    sl = b.seq_lens.copy()
+    sl[0] = 16 * w + 1                                   # more pages than the row holds
+    assert csp.validate_batch(b.block_table, sl, **ok)[0] == csp.CSP_ERR_INVALID_ARG
+    cu = b.cu_seqlens_q.copy()
+    cu[2] = cu[1] - 1                                    # negative query count
+    assert csp.validate_batch(b.block_table, b.seq_lens, cu, **ok)[0] == \
+        csp.CSP_ERR_INVALID_ARG
+    cu = b.cu_seqlens_q.copy()
+    cu[0] = 1
+    assert csp.validate_batch(b.block_table, b.seq_lens, cu, **ok)[0] == \
+        csp.CSP_ERR_INVALID_ARG
+    # the prefix length: a multiple of the block size, at most the shortest request
+    assert csp.validate_batch(b.block_table, b.seq_lens, common_prefix_len=250,
+                              **ok)[0] == csp.CSP_ERR_INVALID_ARG
+    assert csp.validate_batch(b.block_table, b.seq_lens,
+                              common_prefix_len=16 * ((int(b.seq_lens.min()) + 16) // 16),
+                              **ok)[0] == csp.CSP_ERR_INVALID_ARG
+    assert csp.validate_batch(b.block_table, b.seq_lens, common_prefix_len=256,
+                              **ok) == (csp.CSP_OK, -1)
+    assert csp.validate_batch(np.zeros((0, 4), np.int32), [], **ok) == (csp.CSP_OK, -1)
+    assert csp.validate_batch(b.block_table, b.seq_lens, block_size=16,
+                              num_blocks=0)[0] == csp.CSP_ERR_INVALID_ARG

@@ -105,15 +105,23 @@ def test_batch_size_sweep(n):
     H.compare(out, lse, ref_o, ref_l, rows, what=f"N={n} paged")
 
 
-@pytest.mark.parametrize("p", [128, 256, 1024, 4096, 16384])
-def test_sweep_column(p):
-    b = workloads.sweep_point(64, p)
+GRID = [(n, p) for n in workloads.SWEEP_N for p in workloads.SWEEP_P]
+
+
+@pytest.mark.parametrize("n,p", GRID, ids=[f"N{n}_P{p}" for n, p in GRID])
+def test_sweep_grid(n, p):
+    """Every point of the heuristic-sweep grid (S = 128), cascade and flat, against the
+    oracle on sampled rows (the first and last row always among them)."""
+    b = workloads.sweep_point(n, p)
     dev = H.to_device(b)
-    rows = H.sample_rows(b, 300, seed=p)
+    rows = H.sample_rows(b, 200, seed=n * 100003 + p)
     ref_o, ref_l = H.oracle_ref(b, rows)
     cpl, _ = H.plan(b)
+    assert cpl == (p if n > 1 else ((p + 128 - 1) // 16) * 16)
     out, lse = H.run_cascade(b, dev, cpl)
-    H.compare(out, lse, ref_o, ref_l, rows, what=f"P={p} cascade")
+    H.compare(out, lse, ref_o, ref_l, rows, what=f"sweep N={n} P={p} cascade")
+    out, lse = H.run_paged(b, dev)
+    H.compare(out, lse, ref_o, ref_l, rows, what=f"sweep N={n} P={p} flat")
 
 
 def test_request_without_queries():
@@ -189,3 +197,23 @@ def test_status_word_stays_clear():
     for _ in range(3):
         H.run_cascade(b, dev, cpl, workspace=ws)
     assert csp.workspace_status(ws) == 0
+
+
+def test_validated_call_with_a_bad_block_id_launches_nothing():
+    b = workloads.tiny_decode()
+    dev = H.to_device(b)
+    cpl, _ = H.plan(b)
+    bad = b.block_table.copy()
+    bad[5, (int(b.seq_lens[5]) - 1) // 16] = b.num_blocks + 7   # past the cache
+    out = torch.zeros_like(dev["q"])
+    lse = torch.zeros((b.total_q, b.num_q_heads), device="cuda")
+    for fn in (lambda **kw: H.run_cascade(b, dev, cpl, **kw), lambda **kw: H.run_paged(b, dev, **kw)):
+        with pytest.raises(csp.CspError) as e:
+            fn(out=out, lse=lse, validate=(bad, b.seq_lens, b.cu_seqlens_q))
+        assert e.value.status == csp.CSP_ERR_INVALID_ARG
+        torch.cuda.synchronize()
+        assert out.abs().max().item() == 0.0 and lse.abs().max().item() == 0.0
+    # the good tables pass the same check and the call runs
+    ref_o, ref_l = H.oracle_ref(b)
+    o2, l2 = H.run_cascade(b, dev, cpl, validate=(b.block_table, b.seq_lens, b.cu_seqlens_q))
+    H.compare(o2, l2, ref_o, ref_l, what="validated cascade")

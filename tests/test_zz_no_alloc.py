@@ -32,6 +32,16 @@ def _noalloc_fn():
     return fn
 
 
+def _status():
+    lib = csp.load()
+    fn = lib.csp_noalloc_status
+    fn.argtypes = [ctypes.c_void_p, ctypes.POINTER(ctypes.c_int32)]
+    fn.restype = ctypes.c_int
+    st = ctypes.c_int32(-999)
+    assert fn(torch.cuda.current_stream().cuda_stream, ctypes.byref(st)) == csp.CSP_OK
+    return st.value
+
+
 def _call(fn, b, d, cpl, out, lse):
     stream = torch.cuda.current_stream().cuda_stream
     return fn(d["q"].data_ptr(), d["k"].data_ptr(), d["v"].data_ptr(), b.num_blocks,
@@ -53,6 +63,7 @@ def _check_against_cascade_attn(fn, b):
         out = torch.full_like(d["q"], float("nan"))
         lse = torch.full((b.total_q, b.num_q_heads), float("nan"), device="cuda")
         assert _call(fn, b, d, cpl, out, lse) == csp.CSP_OK
+        assert _status() == 0                        # no bounded wait gave up
         H.compare(out, lse, ref_out, ref_lse, what="noalloc vs cascade_attn")
 
 
