@@ -71,6 +71,9 @@ def _load(mutant: int = 0) -> ctypes.CDLL:
         lib.oracle_attention_rows.argtypes = [p, p, p, i32, i32, p, i64, p, p, i32, i32, i32, i32,
                                               f64, i32, i32, p, p, i64, p, p, i32]
         lib.oracle_attention_rows.restype = ctypes.c_int
+        lib.oracle_attention_sinks.argtypes = [p, p, p, i32, i32, p, i64, p, p, i32, i32, i32,
+                                               i32, f64, p, p, p, i64, p, p, i32]
+        lib.oracle_attention_sinks.restype = ctypes.c_int
         lib.oracle_merge_states.argtypes = [p, p, p, p, i64, i32, p, p]
         lib.oracle_merge_states.restype = None
         lib.oracle_mutant_id.restype = ctypes.c_int
@@ -99,14 +102,16 @@ def _ptr(a: np.ndarray):
 
 
 def attention(q, k_cache, v_cache, block_table, cu_seqlens_q, seq_lens, scale, *,
-              mode=FULL, cpl=0, rows=None, n_threads=None, mutant=0):
+              mode=FULL, cpl=0, rows=None, n_threads=None, mutant=0, sinks=None):
     """Oracle attention.
 
     q: bf16 [total_q, Hq, D]; k_cache / v_cache: bf16 [num_blocks, bs, Hkv, D];
     block_table int32 [N, W]; cu_seqlens_q int32 [N+1]; seq_lens int32 [N].
     rows: None for every (token, head) row, or an int array [n, 2] of
-    (token, head) pairs.  Returns (out float64 [n_rows, D] or [total_q, Hq, D],
-    lse float64 [n_rows] or [total_q, Hq]).
+    (token, head) pairs.  sinks: None, or one logit per query head (float [Hq],
+    natural log, -inf for none) for the standard path with attention sinks.
+    Returns (out float64 [n_rows, D] or [total_q, Hq, D], lse float64 [n_rows] or
+    [total_q, Hq]).
     """
     lib = _load(mutant)
     qb, kb, vb = _bits(q), _bits(k_cache), _bits(v_cache)
@@ -121,7 +126,29 @@ def attention(q, k_cache, v_cache, block_table, cu_seqlens_q, seq_lens, scale, *
     assert int(cu[-1]) == total_q
     if n_threads is None:
         n_threads = os.cpu_count() or 1
-    if rows is None:
+    if sinks is not None:
+        assert mode == FULL, "sinks belong to the standard path"
+        sk = np.ascontiguousarray(np.asarray(sinks, dtype=np.float64).reshape(-1))
+        assert sk.shape[0] == Hq
+        if rows is None:
+            out = np.empty((total_q, Hq, D), np.float64)
+            lse = np.empty((total_q, Hq), np.float64)
+            st = lib.oracle_attention_sinks(_ptr(qb), _ptr(kb), _ptr(vb), num_blocks, bs,
+                                            _ptr(bt), bt.shape[1], _ptr(cu), _ptr(sl), N, Hq,
+                                            Hkv, D, float(scale), _ptr(sk), None, None, 0,
+                                            _ptr(out), _ptr(lse), int(n_threads))
+        else:
+            rows = np.ascontiguousarray(np.asarray(rows, dtype=np.int32).reshape(-1, 2))
+            rt = np.ascontiguousarray(rows[:, 0])
+            rh = np.ascontiguousarray(rows[:, 1])
+            n = rows.shape[0]
+            out = np.empty((n, D), np.float64)
+            lse = np.empty((n,), np.float64)
+            st = lib.oracle_attention_sinks(_ptr(qb), _ptr(kb), _ptr(vb), num_blocks, bs,
+                                            _ptr(bt), bt.shape[1], _ptr(cu), _ptr(sl), N, Hq,
+                                            Hkv, D, float(scale), _ptr(sk), _ptr(rt), _ptr(rh),
+                                            n, _ptr(out), _ptr(lse), int(n_threads))
+    elif rows is None:
         out = np.empty((total_q, Hq, D), np.float64)
         lse = np.empty((total_q, Hq), np.float64)
         st = lib.oracle_attention(_ptr(qb), _ptr(kb), _ptr(vb), num_blocks, bs, _ptr(bt),

@@ -30,6 +30,15 @@
  * phase), SUFFIX = [cpl, p] (the suffix phase).  Key j of request r lives in
  * physical block block_table[r][j / block_size], slot j % block_size.
  *
+ * Attention sinks (§九 "Attention Sinks": a mechanism that always lets attention
+ * put weight on a token outside the request's keys; every backend takes an optional
+ * `sinks` argument).  Read as one logit s_h per query head, in natural-log units and
+ * not multiplied by the scale, that joins the softmax of every row of head h as one
+ * more key whose value row is zero.  Standard path only (a phase partial has none):
+ *     m   = max(max_j s_j, s_h),   l = sum_j exp(s_j - m) + exp(s_h - m)
+ *     out = sum_j exp(s_j - m) v_j / l,   lse = m + ln(l)
+ * s_h = -inf is the standard path exactly.
+ *
  * Every floating-point step is IEEE double; bf16 inputs are widened exactly.
  * Sums run in key / feature index order.  No blocking, no fusion, no reordering.
  * An empty key range gives out = 0 and lse = -inf.
@@ -73,6 +82,7 @@ typedef struct {
   double scale;
   int32_t mode;
   int32_t cpl;
+  const double* sinks; /* [Hq] or NULL: no sinks (standard path only) */
 } oracle_problem;
 
 static double bf16_bits_to_double(uint16_t bits) {
@@ -135,9 +145,11 @@ static int attend_row(const oracle_problem* P, int32_t t, int32_t h, double* out
 #endif
   }
   const int D = P->D;
+  /* the sink logit of this row's head (standard path only); -inf: none */
+  const double sink = (P->sinks && P->mode == ORACLE_FULL) ? P->sinks[h] : -INFINITY;
   if (hi <= lo) {
     for (int d = 0; d < D; ++d) out[d] = 0.0;
-    *lse = -INFINITY;
+    *lse = sink;
     return 0;
   }
   const uint16_t* qrow = P->q + ((int64_t)t * P->Hq + h) * D;
@@ -160,8 +172,14 @@ static int attend_row(const oracle_problem* P, int32_t t, int32_t h, double* out
 #endif
     if (s[j - lo] > m) m = s[j - lo];
   }
+  if (sink > m) m = sink;
   double l = 0.0;
   for (int32_t j = lo; j < hi; ++j) l += exp(s[j - lo] - m);
+#if ORACLE_MUTANT == 8
+  l += exp(m - sink); /* planted: the sink's exponent with its sign flipped */
+#else
+  if (sink != -INFINITY) l += exp(sink - m);
+#endif
   for (int d = 0; d < D; ++d) {
     double acc = 0.0;
     for (int32_t j = lo; j < hi; ++j) {
@@ -260,9 +278,23 @@ int oracle_attention(const uint16_t* q, const uint16_t* k, const uint16_t* v, in
                      double* out, double* lse, int32_t n_threads) {
   oracle_problem P = {q,           k,        v,    num_blocks, block_size, block_table, bt_stride,
                       cu_seqlens_q, seq_lens, num_reqs, Hq,  Hkv,        D,           scale,
-                      mode,        cpl};
+                      mode,        cpl,      NULL};
   int64_t total_q = cu_seqlens_q[num_reqs];
   return run_rows(&P, NULL, NULL, total_q * Hq, out, lse, n_threads);
+}
+
+/* oracle_attention_sinks: the standard path with per-head sinks (sinks [Hq]). */
+int oracle_attention_sinks(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                           int32_t num_blocks, int32_t block_size, const int32_t* block_table,
+                           int64_t bt_stride, const int32_t* cu_seqlens_q, const int32_t* seq_lens,
+                           int32_t num_reqs, int32_t Hq, int32_t Hkv, int32_t D, double scale,
+                           const double* sinks, const int32_t* row_token, const int32_t* row_head,
+                           int64_t n_rows, double* out, double* lse, int32_t n_threads) {
+  oracle_problem P = {q,           k,        v,    num_blocks, block_size, block_table, bt_stride,
+                      cu_seqlens_q, seq_lens, num_reqs, Hq,  Hkv,        D,           scale,
+                      ORACLE_FULL, 0,       sinks};
+  if (row_token) return run_rows(&P, row_token, row_head, n_rows, out, lse, n_threads);
+  return run_rows(&P, NULL, NULL, (int64_t)cu_seqlens_q[num_reqs] * Hq, out, lse, n_threads);
 }
 
 /* oracle_attention_rows: only the listed (token, head) rows, for sampled checks. */
@@ -275,7 +307,7 @@ int oracle_attention_rows(const uint16_t* q, const uint16_t* k, const uint16_t* 
                           int32_t n_threads) {
   oracle_problem P = {q,           k,        v,    num_blocks, block_size, block_table, bt_stride,
                       cu_seqlens_q, seq_lens, num_reqs, Hq,  Hkv,        D,           scale,
-                      mode,        cpl};
+                      mode,        cpl,      NULL};
   return run_rows(&P, row_token, row_head, n_rows, out, lse, n_threads);
 }
 

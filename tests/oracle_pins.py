@@ -265,5 +265,72 @@ def pin_page_invariance(mutant=0):
     return fails
 
 
+def library_reference_sinks(paged, dense, sinks):
+    """Dense attention with one more key per head: the sink logit s_h as an extra score
+    column whose value row is zero, through scipy logsumexp / softmax."""
+    Hq, Hkv, D = dense["Hq"], dense["Hkv"], dense["D"]
+    group = Hq // Hkv
+    scale = paged["scale"]
+    outs, lses = [], []
+    for qq, kk, vv in zip(dense["q"], dense["k"], dense["v"]):
+        ql, s = qq.shape[0], kk.shape[0]
+        qf, kf, vf = qq.double().numpy(), kk.double().numpy(), vv.double().numpy()
+        pos = s - ql + np.arange(ql)
+        mask = np.arange(s)[None, :] <= pos[:, None]                      # [ql, s]
+        o = np.zeros((ql, Hq, D))
+        l = np.zeros((ql, Hq))
+        for h in range(Hq):
+            gi = h // group
+            S = np.where(mask, scale * (qf[:, h, :] @ kf[:, gi, :].T), -np.inf)
+            S = np.concatenate([S, np.full((ql, 1), sinks[h])], axis=1)   # the sink column
+            Vx = np.concatenate([vf[:, gi, :], np.zeros((1, D))], axis=0)  # its zero value
+            l[:, h] = scipy.special.logsumexp(S, axis=1)
+            o[:, h, :] = scipy.special.softmax(S, axis=1) @ Vx
+        outs.append(o)
+        lses.append(l)
+    return np.concatenate(outs, 0), np.concatenate(lses, 0)
+
+
+def pin_sinks(mutant=0):
+    """Attention sinks: equal to dense library attention with the sink as one more
+    score column of zero value; -inf sinks give the standard path bit for bit; one key
+    and one sink in closed form; the merge of the standard path with an (O = 0,
+    lse = s_h) partial."""
+    fails = []
+    rng = np.random.default_rng(41)
+    for seed, sl, ql, Hq, Hkv, D, bs, sh in CASES:
+        paged, dense = dense_problem(seed, sl, ql, Hq=Hq, Hkv=Hkv, D=D, bs=bs, shared_tokens=sh)
+        sinks = rng.standard_normal(Hq) * 3.0
+        sinks[0] = -np.inf
+        ref_o, ref_l = library_reference_sinks(paged, dense, sinks)
+        o, l = _run(paged, mutant, sinks=sinks)
+        fails += _close(o, ref_o, 1e-10, f"case{seed} sinks out")
+        fails += _close(l, ref_l, 1e-10, f"case{seed} sinks lse")
+        # -inf everywhere: the standard path exactly
+        so, sl_ = _run(paged, mutant, sinks=np.full(Hq, -np.inf))
+        po, pl = _run(paged, mutant)
+        fails += _close(so, po, 0.0, f"case{seed} -inf sinks out")
+        fails += _close(sl_, pl, 0.0, f"case{seed} -inf sinks lse")
+        # the sink as one more partial of the LSE merge
+        t = l.shape[0]
+        mo, ml = oracle.merge_states(po, pl, np.zeros_like(po),
+                                     np.broadcast_to(sinks, pl.shape).copy(), mutant=mutant)
+        fails += _close(mo, o, 1e-12, f"case{seed} sinks merge out")
+        fails += _close(ml, l, 1e-12, f"case{seed} sinks merge lse")
+    # one key x and one sink s: out = v e^x / (e^x + e^s), lse = ln(e^x + e^s)
+    paged, dense = dense_problem(42, [1], [1], Hq=2, Hkv=1, D=16, bs=16)
+    sinks = np.array([0.75, -2.5])
+    o, l = _run(paged, mutant, sinks=sinks)
+    v0 = dense["v"][0][0, 0].double().numpy()
+    k0 = dense["k"][0][0, 0].double().numpy()
+    for h in range(2):
+        x = paged["scale"] * float(np.dot(dense["q"][0][0, h].double().numpy(), k0))
+        w = 1.0 / (1.0 + math.exp(sinks[h] - x))
+        fails += _close(o[0, h], v0 * w, 1e-14, "one key + sink out")
+        fails += _close(l[0, h], x + math.log1p(math.exp(sinks[h] - x)), 1e-14,
+                        "one key + sink lse")
+    return fails
+
+
 ALL_PINS = [pin_dense_library, pin_partials_library, pin_closed_forms, pin_merge_identity,
-            pin_page_invariance]
+            pin_page_invariance, pin_sinks]
