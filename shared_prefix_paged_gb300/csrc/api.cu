@@ -97,19 +97,16 @@ int make_map_3d(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1, ui
 
 // A K or V cache [blocks][16][Hkv][D] seen as 4-D {64 features, tokens, D / 64
 // feature halves, Hkv} (the halves and heads listed after the tokens), 128-byte
-// swizzle, boxes {64, 16, D / 64, heads}: one page of `heads` KV heads lands in shared
-// memory as [head][half][16 tokens][128 B], so 16 consecutive keys of one head are
-// consecutive swizzled rows.
-int make_map_kv_pages(CUtensorMap* map, const void* base, int D, int Hkv, uint64_t ntok,
-                      int heads) {
+// swizzle, boxes {64, 16, D / 64, 1}: one page of one KV head lands in shared memory
+// as [half][16 tokens][128 B], so 16 consecutive keys are consecutive swizzled rows.
+int make_map_kv_pages(CUtensorMap* map, const void* base, int D, int Hkv, uint64_t ntok) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return cuda_fail(cudaErrorNotSupported);
   const cuuint64_t dims[4] = {64, ntok, static_cast<cuuint64_t>(D / 64),
                               static_cast<cuuint64_t>(Hkv)};
   const cuuint64_t strides[3] = {static_cast<cuuint64_t>(Hkv) * D * 2, 128,
                                  static_cast<cuuint64_t>(D) * 2};
-  const cuuint32_t box[4] = {64, kPage, static_cast<cuuint32_t>(D / 64),
-                             static_cast<cuuint32_t>(heads)};
+  const cuuint32_t box[4] = {64, kPage, static_cast<cuuint32_t>(D / 64), 1};
   const cuuint32_t estr[4] = {1, 1, 1, 1};
   CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims,
                   strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -159,57 +156,9 @@ struct LaunchPlan {
   // single-kernel decode schedule (decode_cascade.cu)
   bool single = false;
   int d_splits = 0, d_prefix_ctas = 0, d_prefix_units = 0, d_grid = 0, d_merge_rows = 0;
-  int d_units_per_req = 0, d_unit_pages = 0, d_item_pages = 0, d_page_bytes = 0;
-  int d_item_bytes = 0, d_ring_slots = 0, d_q_off = 0, d_suffix_slots = 0;
   int64_t d_lse_stride = 0;
   size_t d_off_o = 0, d_off_lse = 0;
 };
-
-// The single-kernel schedule's unit partition (the host copy of unit_range_of and
-// cta_of_unit in decode_cascade.cu): n_units units, the first pc CTAs hold k units
-// each after their prefix range, the other grid - pc CTAs the rest in order (evenly
-// when there are at least as many units as CTAs, else one each).
-int64_t cta_of_unit_host(int64_t u, int64_t n_units, int64_t pc, int64_t k, int64_t grid) {
-  const int64_t pre_units = std::min(pc * k, n_units);
-  if (u < pre_units) return u / k;  // (k > 0 here)
-  const int64_t rest = n_units - pre_units;
-  const int64_t n = grid - pc;
-  const int64_t up = u - pre_units;
-  if (rest < n) return pc + up;
-  return pc + ((up + 1) * n - 1) / rest;
-}
-
-// An upper bound of suffix_pieces_host without the walk over requests: K consecutive
-// units span at most 2 + ceil((K - 2) / m) CTAs when every CTA holding units holds at
-// least m of them (and never more than K).
-int suffix_pieces_bound(int units_per_req, int64_t n_units, int64_t pc, int64_t k,
-                        int64_t grid) {
-  const int64_t pre_units = std::min(pc * k, n_units);
-  const int64_t rest = n_units - pre_units;
-  const int64_t n = grid - pc;
-  int64_t m = INT64_MAX;
-  if (k > 0 && pre_units > 0) m = std::min(m, pre_units >= k ? k : pre_units);
-  if (rest > 0) m = std::min(m, n > 0 && rest >= n ? rest / n : int64_t{1});
-  if (m == INT64_MAX) m = 1;
-  const int64_t K = units_per_req;
-  const int64_t b = K <= 2 ? K : 2 + (K - 2 + m - 1) / m;
-  return static_cast<int>(std::min(K, b));
-}
-
-// Most CTAs that hold units of one request (the suffix slots the merge reads).
-int suffix_pieces_host(int num_reqs, int units_per_req, int64_t pc, int64_t k, int64_t grid) {
-  const int64_t n_units = static_cast<int64_t>(num_reqs) * units_per_req;
-  if (pc >= grid && pc * k < n_units) return 1 << 20;  // the units do not fit
-  int64_t most = 1;
-  for (int r = 0; r < num_reqs; ++r) {
-    const int64_t a = cta_of_unit_host(static_cast<int64_t>(r) * units_per_req, n_units, pc, k, grid);
-    const int64_t b =
-        cta_of_unit_host(static_cast<int64_t>(r) * units_per_req + units_per_req - 1, n_units, pc,
-                         k, grid);
-    most = std::max(most, b - a + 1);
-  }
-  return static_cast<int>(std::min<int64_t>(most, 1 << 20));
-}
 
 // sched_override: -1 (the cost model decides), CSP_SCHEDULE_TWO_KERNELS or
 // CSP_SCHEDULE_SINGLE (taken where the single kernel can run); ranges_override > 0
@@ -279,43 +228,30 @@ void make_plan(int num_reqs, int total_q, int max_q, int max_k, int cpl, int Hq,
   p.off_part_lse = p.off_part_o + align256(static_cast<size_t>(p.n_parts) * rows_total * D * 2);
   p.bytes = p.off_part_lse + align256(static_cast<size_t>(p.n_parts) * rows_total * 4);
 
-  // Decode-like batches (a request's rows of one KV head fit one 16-row MMA tile, at
-  // most 8 KV heads, a page of every KV head within 32 KB): one cooperative kernel.
-  // d_base * s CTAs each run a prefix range and then stream k suffix units; the other
-  // CTAs stream the rest of the suffix units from the start.  A suffix unit is
-  // unit_pages pages of one request over every KV head (about three units per SM, at
-  // most 8 units per request).  s and k come from a cost model measured on GB300 (per
-  // CTA, in us): the prefix's first tile lands at ~3.5; a prefix 64-key tile takes its
-  // bytes' time at ~31 GB/s (the per-SM copy rate of page-sized boxes) or ~1.22 per 256
-  // rows (tensor core and softmax), whichever is longer; writing a range's partial
-  // takes ~3.4; the suffix's first item lands at ~3 and a page of every KV head then
-  // takes its bytes' time at ~45 GB/s.  Both kinds of CTA should finish together.  The
-  // merge after them costs ~0.1 per slot its loop is unrolled to (8 or 16 slots: the
-  // prefix ranges and the suffix pieces of a request); on a tie the fewer prefix ranges
-  // win.  The single kernel is taken only if the same model does not expect the
-  // two-kernel schedule to be faster (a long prefix over many 256-row blocks leaves it
-  // too few SMs for one of the phases).
+  // Decode-like batches (a request's rows of one KV head fit one 16-row MMA tile):
+  // one cooperative kernel.  d_base * s CTAs each run a prefix range and then stream
+  // k suffix units; the other CTAs stream the rest of the suffix units from the
+  // start.  s and k come from a cost model measured on GB300 (per CTA, in us): the
+  // prefix's first tile lands at ~3.5; a prefix 64-key tile takes its bytes' time at
+  // ~31 GB/s (the per-SM copy rate) or ~1.22 per 256 rows (tensor core and softmax),
+  // whichever is longer; writing a range's partial takes ~3.4; the suffix's first
+  // item lands at ~5 and a suffix unit then takes its bytes' time at ~28.5 GB/s (the
+  // copies and the computing warps pace it together).  Both kinds of CTA should finish
+  // together.  The merge after them costs ~0.1 per slot its loop is unrolled to (8 up
+  // to 7 prefix ranges, 16 beyond); on a tie the fewer prefix ranges win.  The single
+  // kernel is taken only if the same model does not expect the two-kernel schedule to
+  // be faster (a long prefix over many 256-row blocks leaves it too few SMs for one
+  // of the phases).
   const int d_base = p.p_pairs * Hkv;
-  const int64_t page_box = static_cast<int64_t>(kPage) * Hkv * D * 2;
-  const int64_t q_area = (static_cast<int64_t>(max_q) * Hq * D * 2 + 1023) & ~int64_t{1023};
-  const int item_pages =
-      static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(8, 65536 / (2 * page_box))));
-  const int64_t item_bytes = 2 * page_box * item_pages + q_area;
-  const int ring_slots = static_cast<int>(
-      std::min<int64_t>(csp::kDecodeMaxRing, csp::decode_ring_bytes() / item_bytes));
-  if (cpl > 0 && static_cast<int64_t>(max_q) * p.group <= kDecodeRows && d_base <= sms &&
-      Hkv <= 8 && page_box <= 32768 && ring_slots >= 2) {
+  if (cpl > 0 && static_cast<int64_t>(max_q) * p.group <= kDecodeRows && d_base <= sms) {
     const int pre_tiles = cdiv(cpl, 64);
-    const double kRate = 31e3, kPageRate = 45e3, kUnitRate = 28.5e3;  // bytes per us per SM
+    const double kRate = 31e3, kUnitRate = 28.5e3;  // bytes per us per SM
     const double pair_rows = std::min(256.0, static_cast<double>(total_q) * p.group);
     const double tile_us = std::max(64.0 * 4.0 * D / kRate, 1.22 * pair_rows / 256.0);
-    const int pages = std::max(1, cdiv(max_len, kPage));  // suffix pages per request
-    const int64_t all_pages = static_cast<int64_t>(num_reqs) * pages;
-    int unit_pages = static_cast<int>(std::max<int64_t>(1, all_pages / (3LL * sms)));
-    unit_pages = std::max(unit_pages, cdiv(pages, 8));
-    const int K = cdiv(pages, unit_pages);
-    const int64_t units = static_cast<int64_t>(num_reqs) * K;
-    const double unit_us = unit_pages * 2.0 * page_box / kPageRate;
+    const double unit_us =
+        (std::max(1, cdiv(max_len, 64)) * 64.0 * 4.0 * D + max_q * p.group * D * 2.0) /
+        kUnitRate;
+    const int64_t units = static_cast<int64_t>(num_reqs) * Hkv;
     const int s_max = std::max(1, std::min({pre_tiles, csp::kDecodeMaxParts - 1, sms / d_base}));
     // best number of prefix units for c ranges (and the model's time for it)
     auto best_k = [&](int c, double* t_out) {
@@ -324,95 +260,67 @@ void make_plan(int num_reqs, int total_q, int max_q, int max_k, int cpl, int Hq,
       const double pre_us = 3.5 + cdiv(pre_tiles, c) * tile_us + 3.4;
       const int64_t k_lo = nc > 0 ? 0 : cdiv64(units, pc);
       double best_t = -1.0;
-      int kb = -1;
+      int kb = 0;
       for (int64_t kk = k_lo; kk <= cdiv64(units, pc); ++kk) {
         const int64_t rest = std::max<int64_t>(0, units - pc * kk);
         const int64_t per = nc > 0 ? cdiv64(rest, nc) : 0;
-        if (nc <= 0 && pc * kk < units) continue;
-        const int slots = c + suffix_pieces_bound(K, units, pc, kk, sms);
-        if (slots <= csp::kDecodeMaxParts) {
-          // a prefix CTA's first suffix item lands ~2.5 after its range is written
-          const double t =
-              std::max(pre_us + (kk > 0 ? 2.5 : 0.0) + kk * unit_us, 3.0 + per * unit_us) +
-              (slots <= 8 ? 0.8 : 1.6);
-          if (best_t < 0.0 || t < best_t) {
-            best_t = t;
-            kb = static_cast<int>(kk);
-          }
+        // a prefix CTA's first suffix item lands ~3.5 after its range is written
+        const double t =
+            std::max(pre_us + (kk > 0 ? 3.5 : 0.0) + kk * unit_us, 5.0 + per * unit_us) +
+            (c + 1 <= 8 ? 0.8 : 1.6);
+        if (best_t < 0.0 || t < best_t) {
+          best_t = t;
+          kb = static_cast<int>(kk);
         }
         if (per == 0) break;
       }
       *t_out = best_t;
       return kb;
     };
-    int s = 0;
+    int s = 1;
     double best = -1.0;
     for (int c = 1; c <= s_max; ++c) {
       double t;
-      if (best_k(c, &t) < 0) continue;
+      best_k(c, &t);
       if (best < 0.0 || t < best) {
         best = t;
         s = c;
       }
     }
     // the two-kernel schedule: its prefix kernel (p_splits ranges per block, in waves
-    // over the SMs), while the SMs it leaves free start the suffix (the warp-MMA paged
-    // kernel, ~28.5 GB/s per SM), which every SM then streams
+    // over the SMs), while the SMs it leaves free start the suffix, which every SM
+    // then streams
     const double pre2_us = cdiv64(static_cast<int64_t>(d_base) * p.p_splits, sms) *
                            (3.5 + p.p_tiles_per_split * tile_us + 3.4);
-    const int64_t free_sms =
-        std::max<int64_t>(0, sms - static_cast<int64_t>(d_base) * p.p_splits);
-    const double unit2_us =
-        (std::max(1, cdiv(max_len, 64)) * 64.0 * 4.0 * D + max_q * p.group * D * 2.0) /
-        kUnitRate;
+    const int64_t free_sms = std::max<int64_t>(0, sms - static_cast<int64_t>(d_base) * p.p_splits);
     const double two_us =
         pre2_us + 5.0 +
-        std::max(0.0, static_cast<double>(num_reqs) * Hkv * unit2_us - free_sms * pre2_us) /
-            sms;
-    if (ranges_override > 0) {
-      double t;
-      const int c = std::min(ranges_override, s_max);
-      if (best_k(c, &t) >= 0) {
-        s = c;
-        best = t;
-      }
-    }
-    p.single = s > 0 && (sched_override == CSP_SCHEDULE_SINGLE ||
-                         (sched_override < 0 && best <= two_us));
-    if (s > 0) {
-      double t_s;
-      const int k = best_k(s, &t_s);
-      p.d_splits = s;
-      p.d_prefix_ctas = d_base * s;
-      p.d_prefix_units = k;
-      p.d_grid = sms;
-      p.d_units_per_req = K;
-      p.d_unit_pages = unit_pages;
-      p.d_item_pages = item_pages;
-      p.d_page_bytes = static_cast<int>(page_box);
-      p.d_item_bytes = static_cast<int>(item_bytes);
-      p.d_ring_slots = ring_slots;
-      p.d_q_off = static_cast<int>(2 * page_box * item_pages);
-      p.d_suffix_slots = suffix_pieces_host(num_reqs, K, p.d_prefix_ctas, k, sms);
-      const int n_slots = s + p.d_suffix_slots;
-      // slots: [0, s) the prefix ranges, then the suffix pieces; an LSE slot is padded
-      // to a multiple of four rows (the merge's tensor map wants 16-byte strides)
-      p.d_lse_stride = (static_cast<int64_t>(rows_total) + 3) & ~int64_t{3};
-      // rows per merge chunk: a CTA's share, within the box limit and the shared
-      // memory the merge stages them in
-      p.d_merge_rows = static_cast<int>(std::min<int64_t>(
-          {cdiv64(static_cast<int64_t>(rows_total), sms), 252,
-           static_cast<int64_t>(kMergeSmemBytes / (static_cast<size_t>(n_slots) * D * 2))}));
-      p.d_merge_rows = std::max(p.d_merge_rows, 1);
-      p.d_off_o = kHeaderBytes;
-      p.d_off_lse = p.d_off_o + align256(static_cast<size_t>(n_slots) * rows_total * D * 2);
-      // the workspace fits this schedule at any number of ranges (the most slots)
-      const size_t lse_max = static_cast<size_t>(csp::kDecodeMaxParts) * p.d_lse_stride * 4;
-      p.bytes = std::max(p.bytes, kHeaderBytes +
-                                      align256(static_cast<size_t>(csp::kDecodeMaxParts) *
-                                               rows_total * D * 2) +
-                                      align256(lse_max));
-    }
+        std::max(0.0, static_cast<double>(units) * unit_us - free_sms * pre2_us) / sms;
+    p.single = sched_override == CSP_SCHEDULE_SINGLE ||
+               (sched_override < 0 && best <= two_us);
+    if (ranges_override > 0) s = std::min(ranges_override, s_max);
+    double t_s;
+    const int k = best_k(s, &t_s);
+    p.d_splits = s;
+    p.d_prefix_ctas = d_base * s;
+    p.d_prefix_units = k;
+    p.d_grid = sms;
+    // slots: [0, s) the prefix ranges, s the suffix; an LSE slot is padded to a
+    // multiple of four rows (the merge's tensor map wants 16-byte strides)
+    p.d_lse_stride = (static_cast<int64_t>(rows_total) + 3) & ~int64_t{3};
+    // rows per merge chunk: a CTA's share, within the box limit and the shared memory
+    // the merge stages them in
+    p.d_merge_rows = static_cast<int>(std::min<int64_t>(
+        {cdiv64(static_cast<int64_t>(rows_total), sms), 252,
+         static_cast<int64_t>(kMergeSmemBytes / (static_cast<size_t>(s + 1) * D * 2))}));
+    p.d_merge_rows = std::max(p.d_merge_rows, 1);
+    p.d_off_o = kHeaderBytes;
+    p.d_off_lse = p.d_off_o + align256(static_cast<size_t>(s + 1) * rows_total * D * 2);
+    // the workspace fits this schedule at any number of ranges (the most slots)
+    const size_t lse_max = static_cast<size_t>(s_max + 1) * p.d_lse_stride * 4;
+    p.bytes = std::max(p.bytes, kHeaderBytes +
+                                    align256(static_cast<size_t>(s_max + 1) * rows_total * D * 2) +
+                                    align256(lse_max));
   }
   *P = p;
 }
@@ -461,14 +369,13 @@ int attention_call(const void* q, const void* k_cache, const void* v_cache, int3
     return events ? cudaEventRecord(static_cast<cudaEvent_t>(events[i]), stream) : cudaSuccess;
   };
   if (P.single) {
-    CUtensorMap tm_q, tm_v, tm_kp, tm_ks, tm_vs;
+    CUtensorMap tm_q, tm_k, tm_v, tm_kp;
     const uint64_t row_b = static_cast<uint64_t>(D) * 2;
     const uint64_t ntok = static_cast<uint64_t>(num_blocks) * block_size;
     if ((st = make_map_3d(&tm_q, q, D, Hq, total_q, row_b, row_b * Hq, 64, P.group,
                           128 / P.group)) != CSP_OK ||
-        (st = make_map_kv_pages(&tm_v, v_cache, D, Hkv, ntok, 1)) != CSP_OK ||
-        (st = make_map_kv_pages(&tm_ks, k_cache, D, Hkv, ntok, Hkv)) != CSP_OK ||
-        (st = make_map_kv_pages(&tm_vs, v_cache, D, Hkv, ntok, Hkv)) != CSP_OK ||
+        (st = make_map_kv_pages(&tm_k, k_cache, D, Hkv, ntok)) != CSP_OK ||
+        (st = make_map_kv_pages(&tm_v, v_cache, D, Hkv, ntok)) != CSP_OK ||
         (st = make_map_3d(&tm_kp, k_cache, D, Hkv, ntok, row_b, row_b * Hkv, 64, 1, kPage)) !=
             CSP_OK)
       return st;
@@ -493,7 +400,7 @@ int attention_call(const void* q, const void* k_cache, const void* v_cache, int3
     // the merge's views of the slots: bf16 rows [slot][row][D] and LSEs [slot][row]
     CUtensorMap tm_po, tm_pl;
     {
-      const uint64_t n_slots = static_cast<uint64_t>(P.d_splits) + P.d_suffix_slots;
+      const uint64_t n_slots = static_cast<uint64_t>(P.d_splits) + 1;
       const uint64_t rows = static_cast<uint64_t>(total_q) * Hq;
       const cuuint64_t od[3] = {static_cast<cuuint64_t>(D), rows, n_slots};
       const cuuint64_t os[2] = {row_b, rows * row_b};
@@ -520,15 +427,9 @@ int attention_call(const void* q, const void* k_cache, const void* v_cache, int3
     da.prefix_ctas = P.d_prefix_ctas;
     da.prefix_units = P.d_prefix_units;
     da.merge_rows = P.d_merge_rows;
-    da.units_per_req = P.d_units_per_req;
-    da.unit_pages = P.d_unit_pages;
-    da.item_pages = P.d_item_pages;
-    da.page_bytes = P.d_page_bytes;
-    da.item_bytes = P.d_item_bytes;
-    da.ring_slots = P.d_ring_slots;
-    da.q_off = P.d_q_off;
-    da.suffix_slots = P.d_suffix_slots;
-    da.max_rows = max_seqlen_q * P.group;
+    // every request's suffix within one item (two 64-key tiles): two groups of four
+    // warps take alternate units
+    da.unit_groups = max_seqlen_k - cpl <= 2 * 64 ? 2 : 1;
     da.key_tiles = cdiv(cpl, 64);
     da.bar_count = reinterpret_cast<int*>(ws + kOffBarCount);
     da.bar_gen = reinterpret_cast<unsigned*>(ws + kOffBarGen);
@@ -536,8 +437,9 @@ int attention_call(const void* q, const void* k_cache, const void* v_cache, int3
     da.lse = lse;
     // phase events: [0] before the kernel, [1..3] after it
     if ((e = mark(0)) != cudaSuccess) return cuda_fail(e);
-    if ((e = csp::launch_decode(D, tm_q, tm_v, tm_kp, tm_ks, tm_vs, tm_po, tm_pl, da, P.d_grid,
-                                stream)) != cudaSuccess)
+    if ((e = csp::launch_decode(D, tm_q, tm_k, tm_v, tm_kp, tm_po, tm_pl, da, P.d_grid,
+                                stream)) !=
+        cudaSuccess)
       return cuda_fail(e);
     for (int i = 1; i < 4; ++i)
       if ((e = mark(i)) != cudaSuccess) return cuda_fail(e);
@@ -564,7 +466,7 @@ int attention_call(const void* q, const void* k_cache, const void* v_cache, int3
     if ((st = make_map_3d(&tm_k, k_cache, D, Hkv, ntok, row_b, row_b * Hkv, 64, 1, kPage)) !=
         CSP_OK)
       return st;
-    if ((st = make_map_kv_pages(&tm_v, v_cache, D, Hkv, ntok, 1)) != CSP_OK) return st;
+    if ((st = make_map_kv_pages(&tm_v, v_cache, D, Hkv, ntok)) != CSP_OK) return st;
     csp::PrefixArgs pa;
     pa.k = static_cast<const __nv_bfloat16*>(k_cache);
     pa.v = static_cast<const __nv_bfloat16*>(v_cache);
@@ -624,7 +526,7 @@ int attention_call(const void* q, const void* k_cache, const void* v_cache, int3
                           128 / P.group)) != CSP_OK ||
         (st = make_map_3d(&tm_k, k_cache, D, Hkv, ntok, row_b, row_b * Hkv, 64, 1, kPage)) !=
             CSP_OK ||
-        (st = make_map_kv_pages(&tm_v, v_cache, D, Hkv, ntok, 1)) != CSP_OK)
+        (st = make_map_kv_pages(&tm_v, v_cache, D, Hkv, ntok)) != CSP_OK)
       return st;
     e = csp::launch_paged_tc(D, tm_q, tm_k, tm_v, ga, overlap, stream);
   } else {

@@ -21,9 +21,9 @@
 //    slots plus the suffix slot, by LSE rescaling) into bf16 out and the natural-log
 //    LSE: one round trip to L2 per row, spread over every SM.
 //
-// Suffix streaming within a CTA: warp 8 produces ring items (whole pages of every KV
-// head, loaded by TMA) and warp h (< Hkv) computes KV head h of every item on
-// mma.sync (see produce_suffix and consume_suffix).
+// Suffix streaming within a CTA: warp 8 produces ring items (two 64-key tiles of a
+// unit, loaded by TMA) and warps 0-7 compute them on mma.sync (see produce_items and
+// consume_items).
 #include <type_traits>
 
 #include "merge.cuh"
@@ -33,31 +33,52 @@ namespace csp {
 namespace {
 
 constexpr int kThreads = prefix::kThreads;  // 352: eleven warps
+constexpr int kKeys = 64;                   // keys per suffix stage
 constexpr int kPage = 16;
-constexpr int kWarpProducer = 8;            // produces the suffix items
+constexpr int kTilePages = kKeys / kPage;
+constexpr int kRows = 16;                   // packed rows of a suffix unit (one M tile)
+constexpr int kStreamWarps = 8;             // warps 0-7 stream the suffix
+constexpr int kWarpScheduler = 8;           // produces the suffix items
 constexpr int kMergeBarOff = 512;           // merge barrier within the suffix barrier area
 
-static_assert(kThreads == 352, "eleven warps: 8 softmax/consumers, 2 MMA (one the producer), loader");
+static_assert(kThreads == 352, "eleven warps: 8 softmax/streaming, 2 MMA (one the scheduler), loader");
 
 template <int D>
 struct SLayout {
-  static constexpr int kRing = 221184;  // bytes for the suffix ring (216 KB)
-  // the data area serves both roles: the prefix's Q + ring + staging, or the ring
+  static constexpr int kHalves = D / 64;
+  static constexpr int kKV = kKeys * D * 2;  // one K (or V) stage: [page][half][16 keys][128 B]
+  static constexpr int kQHalf = kRows * 128;
+  static constexpr int kQ = kHalves * kQHalf;
+  static constexpr int kStage = 2 * kKV + kQ;    // K, V, then Q
+  static constexpr int kItem = 2 * kStage;       // two tiles of one unit
+  static constexpr int kRing = 221184;           // bytes of items (216 KB)
+  static constexpr int kSlots = kRing / kItem > 6 ? 6 : kRing / kItem;
+  // the data area serves both roles: the prefix's Q + ring + staging, or the items
   static constexpr int kPrefixData = prefix::Layout<D>::kData;
-  static constexpr int kData = kRing > kPrefixData ? kRing : kPrefixData;
+  static constexpr int kData = kSlots * kItem > kPrefixData ? kSlots * kItem : kPrefixData;
   static constexpr int kPrefixBars = kData;                        // prefix::kBarBytes
   static constexpr int kSuffixBars = kPrefixBars + prefix::kBarBytes;
   static constexpr int kSuffixBarBytes = 1024;
   static constexpr int kDynamic = kSuffixBars + kSuffixBarBytes + 1024;  // + align slack
+  static_assert(kSlots >= 3, "two items in flight ahead of the computed one");
+  static_assert(kStage % 1024 == 0 && (2 * kKV) % 1024 == 0, "swizzled stage alignment");
+  static_assert(2 * kSlots * 8 + kSlots * 32 + 16 <= kSuffixBarBytes, "suffix barrier area");
   static_assert(kDynamic <= 227 * 1024, "one CTA per SM");
 };
 
-// Byte offset of 16-byte chunk c (of D/8) of key `key` (< 16) in one KV head's page
-// as the page boxes leave it: [feature half][16 keys][128 B], 128-byte swizzle (the
-// chunk index XOR the row's index mod 8): conflict-free ldmatrix.
+// Byte offset of 16-byte chunk c (of D/8) of row `row` in a [halves][rows][128 B]
+// tile with the 128-byte swizzle (chunk index XOR row mod 8): conflict-free ldmatrix.
+template <int kTileRows>
+__device__ __forceinline__ uint32_t sw128(int row, int c) {
+  return static_cast<uint32_t>((c >> 3) * (kTileRows * 128) + row * 128 +
+                               (((c & 7) ^ (row & 7)) << 4));
+}
+
+// The same for a K or V stage as the page boxes leave it: [page][half][16 keys][128 B]
+// (one box per page brings both feature halves), swizzled by the row's index.
 template <int D>
 __device__ __forceinline__ uint32_t kv_off(int key, int c) {
-  const int r = (c >> 3) * 16 + key;
+  const int r = (key >> 4) * (16 * (D / 64)) + (c >> 3) * 16 + (key & 15);
   return static_cast<uint32_t>(r * 128 + (((c & 7) ^ (r & 7)) << 4));
 }
 
@@ -71,442 +92,398 @@ __device__ __forceinline__ void st_release_gpu_u32(unsigned* p, unsigned v) {
   asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
-__device__ __forceinline__ uint32_t lds_u32(uint32_t addr) {
-  uint32_t v;
-  asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
-  return v;
-}
-
-__device__ __forceinline__ uint4 lds_u128(uint32_t addr) {
-  uint4 v;
-  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "r"(addr)
-               : "memory");
-  return v;
-}
-
-__device__ __forceinline__ void sts_u16(uint32_t addr, uint16_t v) {
-  asm volatile("st.shared.b16 [%0], %1;" ::"r"(addr), "h"(v) : "memory");
-}
-
-// The transpose of an 8x8 matrix of 16-bit elements held as mma fragments: lane i
-// holds row i / 4, columns 2 (i % 4) and 2 (i % 4) + 1, before and after.
-__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
-  uint32_t y;
-  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
-  return y;
+// the streaming warps of one unit group: named barrier 1 + group, kWPU warps
+template <int kWPU>
+__device__ __forceinline__ void group_sync(int group) {
+  asm volatile("bar.sync %0, %1;" ::"r"(1 + group), "r"(kWPU * 32) : "memory");
 }
 
 // ------------------------------------------------------------------ streaming --
-// The suffix phase of a CTA is its range of suffix units: unit u is the run of
-// unit_pages suffix pages [j * unit_pages, (j + 1) * unit_pages) of request
-// r = u / units_per_req (j = u % units_per_req), over every KV head.  Consecutive
-// units of one request form a run: the CTA's piece of that request.  A run's pages go
-// through a ring of ring_slots items in shared memory, item_pages pages each:
-//  * warp 8 produces them.  It reads a run's query range and length (lanes 0-2) and the
-//    block ids of an item's pages (one per lane), one run / one item ahead, and fills a
-//    free slot: lane 2k (2k + 1) issues one TMA box with K (V) of the item's page k for
-//    every KV head (16 tokens x Hkv x D, [head][feature half][16 tokens][128 B]); the
-//    run's first item also brings its query rows ([token][Hq][D], one bulk copy).
-//  * warp h computes KV head h of every item: S^T = K Q^T and O^T += V^T P^T on
-//    mma.sync m16n8k16 (bf16 in, fp32 accumulate) with the page's 16 keys as M and the
-//    head's packed rows (query, head-in-group) as N, fed by ldmatrix; the causal limit
-//    (bottom-right alignment, §四) and an online softmax in base 2 with the row
-//    reductions over the 8 lanes holding a row; P moves from the S^T fragments to the
-//    B operand of O^T by a register transpose (movmatrix).  At the run's end the warp
-//    writes its rows' normalised partial and log2-sum-exp into the piece's slot.
+// The CTA's suffix units, two 64-key tiles of a unit at a time.  An "item" is a pair
+// of stages holding tiles t and t + 1 of one unit (the second left empty when the
+// unit has a single tile left); a unit's first item also carries its Q rows.  Items
+// go through a ring of kSlots in shared memory:
+//  * warp 8 produces them.  It walks the CTA's units (see unit_range), reads each
+//    request's query range, length and block ids (lane j the id of the item's page j,
+//    one item ahead), and fills a free slot: lane j < 16 issues one TMA box of the
+//    item's K or V (one page of one KV head, both feature halves), and the lanes copy
+//    the Q rows with 16-byte cp.async (rows past the unit's are zero-filled without a
+//    read).  A page past the request re-reads the item's first page (its keys are
+//    masked); the item's descriptor tells the consumers which unit and tiles it holds.
+//  * warps 0-7 consume them: warps 0-3 compute the item's first tile and warps 4-7 its
+//    second, warp w taking keys [16 (w % 4), 16 (w % 4) + 16): S = Q K^T and O += P V
+//    on mma.sync m16n8k16 (bf16 in, fp32 accumulate) fed by ldmatrix, masked by the
+//    request's causal limit (bottom-right alignment, §四), online softmax in base 2.
+//    V rows past the request are zeroed first (a TMA page holds whatever the cache
+//    has there).  At the unit's end the eight warps merge through the item's memory
+//    and write the normalised bf16 rows and their log2-sum-exp into the suffix slot.
 // Loads never hold up the computing warps: the producer alone waits for free slots.
 struct ItemDesc {
-  int r;        // request; < 0: no more items
-  int q0, q_len, seq_len;
-  int page0;    // the item's first suffix page (index within the request's suffix)
-  int npages;   // pages in the item (0 for a run with no key left in this CTA's units)
-  int flags;    // kFirst | kLast | kFill
-  int piece;    // the run's suffix slot, counted from slot n_splits
+  int q0, q_len, seq_len, kvh, ntiles, t0, pad0, pad1;  // ntiles < 0: no more items
 };
-constexpr int kFirst = 1;  // the run's first item (its Q rows come with it)
-constexpr int kLast = 2;   // the run's last item: the piece's partial is written after it
-constexpr int kFill = 4;   // ... and the run holds the request's last unit: the request's
-                           // suffix slots that no CTA writes get lse = -inf
 
-// Units [u_begin, u_end) of CTA b: a CTA that runs a prefix range takes the next
-// prefix_units units in CTA order after it; the remaining R units go to the other n
-// CTAs in order, evenly when R >= n (CTA c: [c R / n, (c + 1) R / n)), else one each
-// to the first R.  So the CTAs holding one request's units are consecutive and each
-// holds at least one of them.
-__device__ __forceinline__ void unit_range_of(const DecodeArgs& a, int b, int& u_begin,
-                                              int& u_end) {
-  const int64_t n_units = static_cast<int64_t>(a.num_reqs) * a.units_per_req;
+// The CTA's units: a CTA that ran a prefix range takes the next prefix_units units in
+// CTA order after it; the remaining units are split evenly over the other CTAs (CTA c
+// of those n takes units [c*R/n, (c+1)*R/n) of the R left).
+__device__ __forceinline__ void unit_range(const DecodeArgs& a, int& u_begin, int& u_end) {
+  const int n_units = a.num_reqs * a.pre.num_kv_heads;
+  const int b = static_cast<int>(blockIdx.x);
   const int64_t pre_units =
-      min(static_cast<int64_t>(a.prefix_ctas) * a.prefix_units, n_units);
+      min(static_cast<int64_t>(a.prefix_ctas) * a.prefix_units, static_cast<int64_t>(n_units));
   if (b < a.prefix_ctas) {
     u_begin = static_cast<int>(min(static_cast<int64_t>(b) * a.prefix_units, pre_units));
     u_end = static_cast<int>(min(static_cast<int64_t>(b + 1) * a.prefix_units, pre_units));
-    return;
-  }
-  const int64_t rest = n_units - pre_units;
-  const int64_t n = static_cast<int64_t>(gridDim.x) - a.prefix_ctas;
-  const int64_t c = b - a.prefix_ctas;
-  if (rest >= n) {
-    u_begin = static_cast<int>(pre_units + c * rest / n);
-    u_end = static_cast<int>(pre_units + (c + 1) * rest / n);
   } else {
-    u_begin = static_cast<int>(pre_units + min(c, rest));
-    u_end = static_cast<int>(pre_units + min(c + 1, rest));
+    const int64_t rest = n_units - pre_units;
+    const int n_ctas = static_cast<int>(gridDim.x) - a.prefix_ctas;
+    const int c = b - a.prefix_ctas;
+    u_begin = static_cast<int>(pre_units + c * rest / n_ctas);
+    u_end = static_cast<int>(pre_units + (c + 1) * rest / n_ctas);
   }
-}
-
-// The CTA whose range holds unit u (the inverse of unit_range_of).
-__device__ __forceinline__ int cta_of_unit(const DecodeArgs& a, int64_t u) {
-  const int64_t n_units = static_cast<int64_t>(a.num_reqs) * a.units_per_req;
-  const int64_t pre_units =
-      min(static_cast<int64_t>(a.prefix_ctas) * a.prefix_units, n_units);
-  if (u < pre_units) return static_cast<int>(u / a.prefix_units);
-  const int64_t rest = n_units - pre_units;
-  const int64_t n = static_cast<int64_t>(gridDim.x) - a.prefix_ctas;
-  const int64_t up = u - pre_units;
-  if (rest < n) return a.prefix_ctas + static_cast<int>(up);
-  return a.prefix_ctas + static_cast<int>(((up + 1) * n - 1) / rest);
 }
 
 template <int D>
-__device__ __forceinline__ void produce_suffix(const DecodeArgs& a, const CUtensorMap* tm_ks,
-                                               const CUtensorMap* tm_vs, uint8_t* ring,
-                                               uint64_t* st_full, uint64_t* st_empty,
-                                               ItemDesc* idesc, volatile int* abort_flag) {
+__device__ __forceinline__ void produce_items(const DecodeArgs& a, const CUtensorMap* tm_k,
+                                              const CUtensorMap* tm_v, uint8_t* ring,
+                                              uint64_t* st_full, uint64_t* st_empty,
+                                              ItemDesc* idesc, volatile int* abort_flag) {
+  using L = SLayout<D>;
+  constexpr int kS = L::kSlots;
+  constexpr int kChunks = D / 8;
+  constexpr int kBoxesPerTile = kTilePages * 2;  // pages x {K, V}, both feature halves each
+  static_assert(2 * kBoxesPerTile <= 32, "one box per lane");
   const PrefixArgs& p = a.pre;
   const int lane = threadIdx.x & 31;
-  const int K = a.units_per_req, PU = a.unit_pages, PI = a.item_pages, S = a.ring_slots;
-  const int64_t col0 = p.cpl / kPage;  // block-table column of suffix page 0
+  const int page0 = p.cpl / kPage;
+  const int hkv = p.num_kv_heads;
   int u, u_end;
-  unit_range_of(a, blockIdx.x, u, u_end);
-  // lanes 0-2: cu_seqlens_q[r], cu_seqlens_q[r + 1], seq_lens[r]
-  auto fetch_meta = [&](int r) -> int {
-    int m = 0;
-    if (lane == 0) m = __ldg(a.cu_seqlens_q + r);
-    else if (lane == 1) m = __ldg(a.cu_seqlens_q + r + 1);
-    else if (lane == 2) m = __ldg(a.seq_lens + r);
-    return m;
-  };
-  // lane k < item_pages: the block id of suffix page pg + k of request r, read before
-  // the request's length is known (an entry past its pages, within the row's stride,
-  // is read but never used)
-  auto fetch_ids = [&](int r, int pg) -> int {
-    if (lane >= PI) return 0;
-    const int64_t col = min(col0 + pg + lane, a.bt_stride - 1);
-    return __ldg(a.block_table + static_cast<int64_t>(r) * a.bt_stride + col);
-  };
+  unit_range(a, u, u_end);
+  // the unit being produced and the next one's metadata (read one unit ahead)
   int item = 0;
+  // next unit's raw metadata: lanes 0-2 hold cu_seqlens_q[r], cu_seqlens_q[r+1],
+  // seq_lens[r]; lanes 0-7 also the block ids of its first eight pages
+  auto fetch = [&](int uu, int& meta, int& id) {
+    meta = 0;
+    id = 0;
+    if (uu >= u_end) return;
+    const int r = uu / hkv;
+    const int32_t* bt = a.block_table + static_cast<int64_t>(r) * a.bt_stride;
+    if (lane == 0) meta = __ldg(a.cu_seqlens_q + r);
+    if (lane == 1) meta = __ldg(a.cu_seqlens_q + r + 1);
+    if (lane == 2) meta = __ldg(a.seq_lens + r);
+    // read before the request's length is known: entries past its pages (up to the
+    // row stride) are read but never used
+    if (lane < 2 * kTilePages) id = __ldg(bt + min(static_cast<int64_t>(page0 + lane), a.bt_stride - 1));
+  };
+  int n_meta, n_id;
+  fetch(u, n_meta, n_id);
   bool ok = true;
-  int meta = 0, ids = 0;
-  if (u < u_end) {
-    const int r = u / K;
-    meta = fetch_meta(r);
-    ids = fetch_ids(r, (u - r * K) * PU);
-  }
-  while (ok && u < u_end) {
-    const int r = u / K;
-    const int ja = u - r * K;
-    const int jb = min(K - 1, u_end - 1 - r * K);  // the run's last unit
-    const int q0 = __shfl_sync(0xffffffffu, meta, 0);
-    // (at most max_rows packed rows per KV head: the size of the slot's Q area)
-    const int q_len = min(__shfl_sync(0xffffffffu, meta, 1) - q0, a.max_rows / p.group);
-    const int seq_len = __shfl_sync(0xffffffffu, meta, 2);
-    int it_ids = ids;
-    // the next run's metadata and first block ids, one run ahead
-    const int u_next = r * K + jb + 1;
-    if (u_next < u_end) {
-      const int rn = u_next / K;
-      meta = fetch_meta(rn);
-      ids = fetch_ids(rn, (u_next - rn * K) * PU);
+  for (; ok; ++u) {
+    // ---- unit u (or the end): its metadata, and the next unit's on its way
+    int q0 = 0, q_len = 0, seq_len = 0, ids = 0;
+    const bool end = u >= u_end;
+    if (!end) {
+      q0 = __shfl_sync(0xffffffffu, n_meta, 0);
+      q_len = __shfl_sync(0xffffffffu, n_meta, 1) - q0;
+      seq_len = __shfl_sync(0xffffffffu, n_meta, 2);
+      ids = n_id;
+      fetch(u + 1, n_meta, n_id);
+      if (q_len <= 0) continue;  // no query rows: nothing to compute or write
     }
-    if (q_len > 0) {  // a request without query rows this step has nothing to compute
-      const int n_r = max(0, (seq_len - p.cpl + kPage - 1) / kPage);
-      const int p_lo = ja * PU;
-      const int npg = max(0, min((jb + 1) * PU, n_r) - p_lo);
-      const int n_items = max(1, (npg + PI - 1) / PI);
-      const int piece = static_cast<int>(blockIdx.x) - cta_of_unit(a, static_cast<int64_t>(r) * K);
-      const bool holds_last = jb == K - 1;
-      const uint32_t qbytes = static_cast<uint32_t>(q_len) * p.num_q_heads * D * 2;
-      for (int it = 0; it < n_items; ++it) {
-        const int slot = item % S;
-        if (item >= S &&
-            !(ok = warp_mbar_wait(&st_empty[slot], ((item / S) - 1) & 1, abort_flag, p.status)))
-          break;
-        const int pg0 = p_lo + it * PI;
-        const int pages = max(0, min(PI, npg - it * PI));
-        // the block ids of the run's next item, one item ahead
-        const int nxt = it + 1 < n_items ? fetch_ids(r, pg0 + PI) : 0;
-        const uint32_t qb = it == 0 ? qbytes : 0u;
-        if (lane == 0) {
-          ItemDesc& d = idesc[slot];
-          d.r = r;
-          d.q0 = q0;
-          d.q_len = q_len;
-          d.seq_len = seq_len;
-          d.page0 = pg0;
-          d.npages = pages;
-          d.flags = (it == 0 ? kFirst : 0) | (it == n_items - 1 ? kLast : 0) |
-                    (it == n_items - 1 && holds_last ? kFill : 0);
-          d.piece = piece;
-          mbar_arrive_expect_tx(&st_full[slot],
-                                static_cast<uint32_t>(pages) * 2u * a.page_bytes + qb);
-        }
-        __syncwarp();
-        uint8_t* base = ring + static_cast<size_t>(slot) * a.item_bytes;
-        const int blk = __shfl_sync(0xffffffffu, it_ids, (lane >> 1) & 31);
-        if (lane < 2 * pages) {
-          const int k = lane >> 1, kv = lane & 1;
-          tma_load_4d(base + (2 * k + kv) * a.page_bytes, kv ? tm_vs : tm_ks, &st_full[slot], 0,
-                      blk * kPage, 0, 0);
-        }
-        if (qb > 0 && lane == 31)
-          bulk_load(base + a.q_off, a.q + static_cast<int64_t>(q0) * p.num_q_heads * D, qb,
-                    &st_full[slot]);
-        ++item;
-        it_ids = nxt;
-      }
-    }
-    u = u_next;
-  }
-  // the end: one marker item that every consumer reads
-  if (ok) {
-    const int slot = item % S;
-    if (item < S ||
-        warp_mbar_wait(&st_empty[slot], ((item / S) - 1) & 1, abort_flag, p.status)) {
+    const int kvh = u - (u / hkv) * hkv;
+    const int nkeys = seq_len - p.cpl;
+    const int nt = end ? -1 : max(1, (nkeys + kKeys - 1) / kKeys);  // >= 1 all-masked tile
+    const int npages = (seq_len + kPage - 1) / kPage;
+    const int32_t* bt = a.block_table + static_cast<int64_t>(end ? 0 : u / hkv) * a.bt_stride;
+    // the end: one marker per consumer group (each group reads every unit_groups-th item)
+    for (int t0 = 0; end ? t0 < 2 * a.unit_groups : t0 < nt; t0 += 2) {
+      const int slot = item % kS;
+      if (item >= kS &&
+          !(ok = warp_mbar_wait(&st_empty[slot], ((item / kS) - 1) & 1, abort_flag, p.status)))
+        break;
+      const int tiles = end ? 0 : min(2, nt - t0);
       if (lane == 0) {
-        idesc[slot].r = -1;
-        mbar_arrive_expect_tx(&st_full[slot], 0u);
+        ItemDesc& d = idesc[slot];
+        d.q0 = q0;
+        d.q_len = q_len;
+        d.seq_len = seq_len;
+        d.kvh = kvh;
+        d.ntiles = nt;
+        d.t0 = t0;
+        mbar_arrive_expect_tx(&st_full[slot], static_cast<uint32_t>(tiles * 2 * L::kKV));
       }
-    }
-  }
-  __syncwarp();
-}
-
-// One page (16 keys) of KV head h for the warp's kNT x 8 packed rows.
-template <int D, int kNT>
-__device__ __forceinline__ void page_step(uint32_t kb, uint32_t vb, int key0,
-                                          const uint32_t (&qf)[kNT][D / 16][2],
-                                          float (&o)[D / 16][kNT][4], float (&m_run)[kNT][2],
-                                          float (&l_part)[kNT][2], const int (&lim)[kNT][2],
-                                          float scale_log2, int lane) {
-  constexpr int kMT = D / 16;
-  const int g = lane >> 2;
-  // S^T = K Q^T: two accumulators per n-tile (even / odd k-steps) halve the chain
-  float s[kNT][2][4];
-#pragma unroll
-  for (int nt = 0; nt < kNT; ++nt)
-#pragma unroll
-    for (int x = 0; x < 2; ++x) s[nt][x][0] = s[nt][x][1] = s[nt][x][2] = s[nt][x][3] = 0.f;
-  {
-    const int key = (lane & 7) + ((lane >> 3) & 1) * 8;
-#pragma unroll
-    for (int kk = 0; kk < kMT; ++kk) {
-      uint32_t ka[4];
-      ldmatrix_x4(kb + kv_off<D>(key, kk * 2 + (lane >> 4)), ka[0], ka[1], ka[2], ka[3]);
-#pragma unroll
-      for (int nt = 0; nt < kNT; ++nt) mma_bf16_16816(s[nt][kk & 1], ka, qf[nt][kk][0], qf[nt][kk][1]);
-    }
-  }
-  // masked scores (keys past a row's causal limit, or past the request), online softmax
-  // in base 2; the row's 16 keys sit on the 8 lanes of one column (xor 4, 8, 16)
-  uint32_t pb[kNT][2];
-#pragma unroll
-  for (int nt = 0; nt < kNT; ++nt) {
-    float pv[4];
-#pragma unroll
-    for (int e = 0; e < 2; ++e) {
-      const float v0 = key0 + g <= lim[nt][e] ? (s[nt][0][e] + s[nt][1][e]) * scale_log2 : -INFINITY;
-      const float v1 =
-          key0 + g + 8 <= lim[nt][e] ? (s[nt][0][2 + e] + s[nt][1][2 + e]) * scale_log2 : -INFINITY;
-      float mx = fmaxf(v0, v1);
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-      // keep the running max unless it grows by more than 2^8 (always on the row's
-      // first unmasked keys, where it is -inf): p = 2^(s - m) <= 256, and O and l need
-      // rescaling only now and then
-      if (mx > m_run[nt][e] + 8.f) {
-        const float alpha = fast_exp2(m_run[nt][e] - mx);
-        l_part[nt][e] *= alpha;
-#pragma unroll
-        for (int mt = 0; mt < kMT; ++mt) {
-          o[mt][nt][e] *= alpha;
-          o[mt][nt][2 + e] *= alpha;
+      __syncwarp();
+      // block ids of the item's pages: lane j holds page page0 + 4 t0 + j; the next
+      // item's are read now, one item ahead
+      int nxt = 0;
+      if (t0 + 2 < nt && lane < 2 * kTilePages) {
+        const int pp = page0 + (t0 + 2) * kTilePages + lane;
+        nxt = pp < npages ? __ldg(bt + pp) : 0;
+      }
+      {
+        const int h = lane / kBoxesPerTile, rem = lane % kBoxesPerTile;
+        const int q = rem >> 1, kv = rem & 1;
+        const int pq = (h * kTilePages + q) & (2 * kTilePages - 1);
+        const int id_q = __shfl_sync(0xffffffffu, ids, pq);
+        const int id_0 = __shfl_sync(0xffffffffu, ids, 0);
+        const int page = page0 + t0 * kTilePages + pq;
+        const int blk = page < npages ? id_q : id_0;
+        if (lane < tiles * kBoxesPerTile) {
+          uint8_t* dst = ring + slot * L::kItem + h * L::kStage + kv * L::kKV + q * (kPage * D * 2);
+          tma_load_4d(dst, kv ? tm_v : tm_k, &st_full[slot], 0, blk * kPage, 0, kvh);
         }
-        m_run[nt][e] = mx;
       }
-      const float mu = m_run[nt][e] == -INFINITY ? 0.f : m_run[nt][e];
-      pv[e] = fast_exp2(v0 - mu);
-      pv[2 + e] = fast_exp2(v1 - mu);
-      l_part[nt][e] += pv[e] + pv[2 + e];
+      if (t0 == 0 && !end) {
+        const uint32_t qb = smem_u32(ring + slot * L::kItem + 2 * L::kKV);
+        const int rows = q_len * p.group;
+        for (int x = lane; x < kRows * kChunks; x += 32) {
+          const int row = x / kChunks, c = x % kChunks;
+          const bool in = row < rows;
+          const int qi = row / p.group, hj = row - qi * p.group;
+          const int64_t off =
+              (static_cast<int64_t>(q0 + qi) * p.num_q_heads + kvh * p.group + hj) * D + c * 8;
+          cp_async_16_u32(qb + sw128<kRows>(row, c), in ? a.q + off : a.q, in ? 16u : 0u);
+        }
+      }
+      cp_async_mbar_arrive(&st_full[slot]);
+      ++item;
+      ids = nxt;
     }
-    // P^T (keys x rows) as two 8x8 blocks -> the B fragments of O^T += V^T P^T
-    pb[nt][0] = movmatrix_trans(pack_bf16x2(pv[0], pv[1]));
-    pb[nt][1] = movmatrix_trans(pack_bf16x2(pv[2], pv[3]));
+    if (end) break;
   }
-  // O^T += V^T P^T: m-tile mt holds features [16 mt, 16 mt + 16)
-  {
-    const int key = (lane & 7) + ((lane >> 4) & 1) * 8;
-#pragma unroll
-    for (int mt = 0; mt < kMT; ++mt) {
-      uint32_t va[4];
-      ldmatrix_x4_trans(vb + kv_off<D>(key, mt * 2 + ((lane >> 3) & 1)), va[0], va[1], va[2],
-                        va[3]);
-#pragma unroll
-      for (int nt = 0; nt < kNT; ++nt) mma_bf16_16816(o[mt][nt], va, pb[nt][0], pb[nt][1]);
-    }
-  }
+  cp_async_wait<0>();
 }
 
-// Warp h (< Hkv) computes KV head h of every item of the CTA's suffix stream, its
-// packed rows in kNT n-tiles of 8.
-template <int D, int kNT>
-__device__ __forceinline__ void consume_suffix(const DecodeArgs& a, uint8_t* ring,
-                                               uint64_t* st_full, uint64_t* st_empty,
-                                               const ItemDesc* idesc, volatile int* abort_flag) {
+// kG groups of 8 / kG streaming warps: group g takes items g, g + kG, g + 2 kG, ...
+// (kG = 2 only when every unit is a single item, so a unit never spans two groups).
+// Within a group, warp w' takes keys [w' * 16 kG, (w' + 1) * 16 kG) of the item's 128
+// (kG blocks of 16 keys in one of its two tiles).
+template <int D, int kG>
+__device__ __forceinline__ void consume_items(const DecodeArgs& a, uint8_t* ring,
+                                              uint64_t* st_full, uint64_t* st_empty,
+                                              const ItemDesc* idesc, volatile int* abort_flag) {
+  using L = SLayout<D>;
+  constexpr int kS = L::kSlots;
+  constexpr int kChunks = D / 8;          // 16-byte chunks per row
+  constexpr int kDT = D / 8;              // O n-tiles (8 features each)
+  constexpr int kORow = D + 4;            // merge scratch row (floats)
+  constexpr int kWPU = kStreamWarps / kG; // warps per unit
+  constexpr int kB = kG;                  // 16-key blocks per warp
+  static_assert(kWPU * kRows * kORow * 4 + 2 * kWPU * kRows * 4 <= L::kItem,
+                "merge scratch fits one item");
   const PrefixArgs& p = a.pre;
-  constexpr int kMT = D / 16;
-  constexpr int kHB = kPage * D * 2;  // one KV head's page inside a page box
-  const int lane = threadIdx.x & 31;
-  const int h = threadIdx.x >> 5;     // the KV head
-  const int g = lane >> 2, t = lane & 3;
-  const int S = a.ring_slots;
+  const int tid = threadIdx.x;  // 0 .. 255
+  const int lane = tid & 31;
+  const int wi = tid >> 5;      // 0 .. 7
+  const int grp = wi / kWPU;    // this warp's group
+  const int wg = wi % kWPU;     // its index within the group
+  const int half = (wg * 16 * kB) >> 6;      // which tile of the item this warp computes
+  const int kw0 = (wg * 16 * kB) & 63;       // its first key within that tile
   const uint32_t rbase = smem_u32(ring);
-  uint32_t qf[kNT][kMT][2];
-  float o[kMT][kNT][4];
-  float m_run[kNT][2], l_part[kNT][2];
-  int lim[kNT][2];  // the last key position a row sees (-1: a padding row)
-  int rows_valid = 0, q0 = 0;
-  for (int item = 0;; ++item) {
-    const int slot = item % S;
-    const uint32_t par = (item / S) & 1;
+
+  int c_nt = 0, c_seq = 0, c_qlen = 0, c_q0 = 0, c_kvh = 0, rows_valid = 0;
+  int pos[2] = {-1, -1};
+  float o[kDT][4];
+  float m_run[2], l_run[2];
+  uint32_t qa[D / 16][4];
+  for (int item = grp;; item += kG) {
+    const int slot = item % kS;
+    const uint32_t par = (item / kS) & 1;
     if (!warp_mbar_wait(&st_full[slot], par, abort_flag, p.status)) break;
-    // every lane observes the completed phase (the copied bytes are visible to it)
+    // every lane observes the completed phase (the TMA bytes are visible to it)
     mbar_test_wait(&st_full[slot], par);
     const ItemDesc d = idesc[slot];
-    if (d.r < 0) break;
-    const uint32_t ib = rbase + slot * a.item_bytes;
-    if (d.flags & kFirst) {
-      q0 = d.q0;
-      rows_valid = d.q_len * p.group;
-      // B fragments of Q^T: lane (g, t) holds row nt*8 + g, features kk*16 + 2t (+1)
-      // and kk*16 + 8 + 2t (+1), from the item's Q rows ([token][Hq][D])
+    if (d.ntiles < 0) break;
+    const uint32_t ib = rbase + slot * L::kItem;
+    const int t0 = d.t0;
+    if (t0 == 0) {
+      c_nt = d.ntiles;
+      c_seq = d.seq_len;
+      c_qlen = d.q_len;
+      c_q0 = d.q0;
+      c_kvh = d.kvh;
+      rows_valid = c_qlen * p.group;
 #pragma unroll
-      for (int nt = 0; nt < kNT; ++nt) {
-        const int n = nt * 8 + g;
-        const bool in = n < rows_valid;
-        const int qi = in ? n / p.group : 0, j = in ? n - qi * p.group : 0;
-        const uint32_t qrow =
-            ib + a.q_off + static_cast<uint32_t>((qi * p.num_q_heads + h * p.group + j) * D * 2);
-#pragma unroll
-        for (int kk = 0; kk < kMT; ++kk) {
-          qf[nt][kk][0] = in ? lds_u32(qrow + (kk * 16 + 2 * t) * 2) : 0u;
-          qf[nt][kk][1] = in ? lds_u32(qrow + (kk * 16 + 8 + 2 * t) * 2) : 0u;
-        }
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const int n2 = nt * 8 + 2 * t + e;
-          lim[nt][e] = n2 < rows_valid ? d.seq_len - d.q_len + n2 / p.group : -1;
-          m_run[nt][e] = -INFINITY;
-          l_part[nt][e] = 0.f;
-        }
+      for (int h = 0; h < 2; ++h) {
+        const int rho = (lane >> 2) + 8 * h;
+        pos[h] = rho < rows_valid ? c_seq - c_qlen + rho / p.group : -1;
+        m_run[h] = -INFINITY;
+        l_run[h] = 0.f;
       }
 #pragma unroll
-      for (int mt = 0; mt < kMT; ++mt)
+      for (int i = 0; i < kDT; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+      const uint32_t qb = ib + 2 * L::kKV;
 #pragma unroll
-        for (int nt = 0; nt < kNT; ++nt) o[mt][nt][0] = o[mt][nt][1] = o[mt][nt][2] = o[mt][nt][3] = 0.f;
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const int row = (lane & 7) + ((lane >> 3) & 1) * 8;
+        const int c = kk * 2 + (lane >> 4);
+        ldmatrix_x4(qb + sw128<kRows>(row, c), qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3]);
+      }
     }
-    for (int k = 0; k < d.npages; ++k) {
-      const uint32_t kb = ib + (2 * k) * a.page_bytes + h * kHB;
-      const uint32_t vb = kb + a.page_bytes;
-      const int key0 = p.cpl + (d.page0 + k) * kPage;
-      if (key0 + kPage > d.seq_len) {
-        // keys past the request: zero their V rows (P is 0 there, but the page may
-        // hold anything, and 0 x NaN is NaN)
-        const int nv = max(0, d.seq_len - key0);
-        for (int x = lane; x < kPage * (D / 8); x += 32) {
-          const int key = x / (D / 8), c = x % (D / 8);
-          if (key >= nv)
-            asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(vb + kv_off<D>(key, c)),
-                         "r"(0u)
+    if (t0 + half < c_nt) {
+      const uint32_t kb = ib + half * L::kStage;
+      const uint32_t vb = kb + L::kKV;
+      const int key0 = p.cpl + (t0 + half) * kKeys + kw0;
+      if (key0 + 16 * kB > c_seq) {
+        // this warp's keys past the request: zero their V rows (P is 0 there, but the
+        // page may hold anything)
+        for (int x = lane; x < 16 * kB * kChunks; x += 32) {
+          const int k = x / kChunks, c = x % kChunks;
+          if (key0 + k >= c_seq)
+            asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(
+                             vb + kv_off<D>(kw0 + k, c)), "r"(0u)
                          : "memory");
         }
         __syncwarp();
       }
-      page_step<D, kNT>(kb, vb, key0, qf, o, m_run, l_part, lim, p.scale_log2, lane);
-    }
-    if (d.flags & kLast) {
-      // ---- the piece's partial: normalised rows (bf16) and their log2-sum-exp
-      float inv[kNT][2], lse2[kNT][2];
+      // S = Q K^T over this warp's keys (two n-tiles of 8 per 16-key block)
+      float sacc[2 * kB][4];
 #pragma unroll
-      for (int nt = 0; nt < kNT; ++nt)
+      for (int i = 0; i < 2 * kB; ++i) sacc[i][0] = sacc[i][1] = sacc[i][2] = sacc[i][3] = 0.f;
 #pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          float l = l_part[nt][e];
-          l += __shfl_xor_sync(0xffffffffu, l, 4);
-          l += __shfl_xor_sync(0xffffffffu, l, 8);
-          l += __shfl_xor_sync(0xffffffffu, l, 16);
-          inv[nt][e] = l > 0.f ? 1.f / l : 0.f;
-          lse2[nt][e] = l > 0.f ? m_run[nt][e] + log2f(l) : -INFINITY;
-        }
-      // stage the rows [row][D] in this head's K page of the item (read already)
-      const uint32_t stg = ib + h * kHB;
-      __syncwarp();
+      for (int kk = 0; kk < D / 16; ++kk) {
 #pragma unroll
-      for (int mt = 0; mt < kMT; ++mt)
-#pragma unroll
-        for (int nt = 0; nt < kNT; ++nt)
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int n = nt * 8 + 2 * t + e;
-            const uint32_t at = stg + static_cast<uint32_t>((n * D + mt * 16 + g) * 2);
-            __nv_bfloat16 lo = __float2bfloat16_rn(o[mt][nt][e] * inv[nt][e]);
-            __nv_bfloat16 hi = __float2bfloat16_rn(o[mt][nt][2 + e] * inv[nt][e]);
-            sts_u16(at, *reinterpret_cast<uint16_t*>(&lo));
-            sts_u16(at + 16, *reinterpret_cast<uint16_t*>(&hi));
-          }
-      __syncwarp();
-      const int64_t rows_all = static_cast<int64_t>(p.total_q) * p.num_q_heads;
-      const int slot_idx = p.n_splits + d.piece;
-      auto grow = [&](int n) {
-        const int qi = n / p.group;
-        return static_cast<int64_t>(q0 + qi) * p.num_q_heads + h * p.group + (n - qi * p.group);
-      };
-      for (int x = lane; x < rows_valid * (D / 8); x += 32) {
-        const int n = x / (D / 8), c = x % (D / 8);
-        const uint4 v = lds_u128(stg + static_cast<uint32_t>((n * D + c * 8) * 2));
-        *reinterpret_cast<uint4*>(p.part_o + (slot_idx * rows_all + grow(n)) * D + c * 8) = v;
-      }
-      if (g == 0) {
-#pragma unroll
-        for (int nt = 0; nt < kNT; ++nt)
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int n = nt * 8 + 2 * t + e;
-            if (n < rows_valid) p.part_lse[slot_idx * p.lse_stride + grow(n)] = lse2[nt][e];
-          }
-      }
-      if (d.flags & kFill) {
-        // this CTA holds the request's last unit: the request's suffix slots of CTAs
-        // that hold none of its units (past the CTAs that do) read lse = -inf
-        const int first = cta_of_unit(a, static_cast<int64_t>(d.r) * a.units_per_req);
-        for (int sidx = 0; sidx < a.suffix_slots; ++sidx) {
-          bool filled = false;
-          if (first + sidx <= static_cast<int>(blockIdx.x)) {
-            int ub, ue;
-            unit_range_of(a, first + sidx, ub, ue);
-            filled = ub < ue;
-          }
-          if (filled) continue;
-          for (int n = lane; n < rows_valid; n += 32)
-            p.part_lse[(p.n_splits + sidx) * p.lse_stride + grow(n)] = -INFINITY;
+        for (int b = 0; b < kB; ++b) {
+          const int key = kw0 + 16 * b + (lane & 7) + (lane >> 4) * 8;
+          const int c = kk * 2 + ((lane >> 3) & 1);
+          uint32_t b0, b1, b2, b3;
+          ldmatrix_x4(kb + kv_off<D>(key, c), b0, b1, b2, b3);
+          mma_bf16_16816(sacc[2 * b], qa[kk], b0, b1);
+          mma_bf16_16816(sacc[2 * b + 1], qa[kk], b2, b3);
         }
       }
-      __syncwarp();
+      // mask (keys past the request, and the causal limit), online softmax in base 2
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        float mx = -INFINITY;
+#pragma unroll
+        for (int nt = 0; nt < 2 * kB; ++nt) {
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int kabs = key0 + nt * 8 + (lane & 3) * 2 + e;
+            float& sref = sacc[nt][2 * h + e];
+            sref = (kabs < c_seq && kabs <= pos[h]) ? sref * p.scale_log2 : -INFINITY;
+            mx = fmaxf(mx, sref);
+          }
+        }
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+        // keep the running max unless it grows by more than 2^8 (always on the row's
+        // first unmasked keys, where it is -inf): then p = 2^(s - m) <= 256 and O and
+        // l need rescaling only now and then
+        if (mx > m_run[h] + 8.f) {
+          const float alpha = fast_exp2(m_run[h] - mx);
+          l_run[h] *= alpha;
+#pragma unroll
+          for (int dt = 0; dt < kDT; ++dt) {
+            o[dt][2 * h] *= alpha;
+            o[dt][2 * h + 1] *= alpha;
+          }
+          m_run[h] = mx;
+        }
+        const float m_use = (m_run[h] == -INFINITY) ? 0.f : m_run[h];
+        float sum = 0.f;
+#pragma unroll
+        for (int nt = 0; nt < 2 * kB; ++nt) {
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            float& sref = sacc[nt][2 * h + e];
+            sref = fast_exp2(sref - m_use);
+            sum += sref;
+          }
+        }
+        l_run[h] += sum;
+      }
+      // O += P V over the same keys
+#pragma unroll
+      for (int b = 0; b < kB; ++b) {
+        uint32_t pa[4];
+        pa[0] = pack_bf16x2(sacc[2 * b][0], sacc[2 * b][1]);
+        pa[1] = pack_bf16x2(sacc[2 * b][2], sacc[2 * b][3]);
+        pa[2] = pack_bf16x2(sacc[2 * b + 1][0], sacc[2 * b + 1][1]);
+        pa[3] = pack_bf16x2(sacc[2 * b + 1][2], sacc[2 * b + 1][3]);
+#pragma unroll
+        for (int dp = 0; dp < kDT / 2; ++dp) {
+          const int key = kw0 + 16 * b + (lane & 7) + ((lane >> 3) & 1) * 8;
+          const int c = dp * 2 + (lane >> 4);
+          uint32_t b0, b1, b2, b3;
+          ldmatrix_x4_trans(vb + kv_off<D>(key, c), b0, b1, b2, b3);
+          mma_bf16_16816(o[2 * dp], pa, b0, b1);
+          mma_bf16_16816(o[2 * dp + 1], pa, b2, b3);
+        }
+      }
     }
-    // the item goes back to the producer (its copies will overwrite what this warp
+    if (t0 + 2 >= c_nt) {
+      // ---- the unit's last item: the group's warps' (max, sum, O) -> one normalised
+      // partial per row, through this item's memory (only this group reads the item)
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        l_run[h] += __shfl_xor_sync(0xffffffffu, l_run[h], 1);
+        l_run[h] += __shfl_xor_sync(0xffffffffu, l_run[h], 2);
+      }
+      group_sync<kWPU>(grp);  // every warp of the group is done reading this item's K/V
+      float* s_o = reinterpret_cast<float*>(ring + slot * L::kItem);  // [kWPU][16][kORow]
+      float* s_m = s_o + kWPU * kRows * kORow;                        // [kWPU][16]
+      float* s_l = s_m + kWPU * kRows;                                // [kWPU][16]
+      // every warp's raw (max, sum, O) of its keys; the weights come in the final pass
+      if ((lane & 3) == 0) {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          s_m[wg * kRows + (lane >> 2) + 8 * h] = m_run[h];
+          s_l[wg * kRows + (lane >> 2) + 8 * h] = l_run[h];
+        }
+      }
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int rr = (lane >> 2) + 8 * h;
+        if (rr >= rows_valid) continue;
+        float* dst = s_o + (wg * kRows + rr) * kORow;
+#pragma unroll
+        for (int dt = 0; dt < kDT; ++dt) {
+          const int dd = dt * 8 + (lane & 3) * 2;
+          *reinterpret_cast<float2*>(dst + dd) = make_float2(o[dt][2 * h], o[dt][2 * h + 1]);
+        }
+      }
+      group_sync<kWPU>(grp);
+      const int64_t slot_rows = static_cast<int64_t>(p.n_splits) * p.total_q * p.num_q_heads;
+      // warp w' finalises rows w', w' + kWPU, ...; lane c owns features [4c, 4c + 4)
+      for (int rr = wg; rr < rows_valid; rr += kWPU) {
+        float mw[kWPU];
+        float mg = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < kWPU; ++w) {
+          mw[w] = s_m[w * kRows + rr];
+          mg = fmaxf(mg, mw[w]);
+        }
+        float lsum = 0.f;
+#pragma unroll
+        for (int w = 0; w < kWPU; ++w) {
+          mw[w] = (mw[w] == -INFINITY) ? 0.f : fast_exp2(mw[w] - mg);  // warp w's weight
+          lsum += s_l[w * kRows + rr] * mw[w];
+        }
+        const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+        const int qi = rr / p.group, j = rr - qi * p.group;
+        const int64_t row = static_cast<int64_t>(c_q0 + qi) * p.num_q_heads + c_kvh * p.group + j;
+        const int64_t prow = slot_rows + row;
+        if (lane < D / 4) {
+          float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+          for (int w = 0; w < kWPU; ++w) {
+            const float4 v =
+                *reinterpret_cast<const float4*>(s_o + (w * kRows + rr) * kORow + lane * 4);
+            acc.x = fmaf(mw[w], v.x, acc.x);
+            acc.y = fmaf(mw[w], v.y, acc.y);
+            acc.z = fmaf(mw[w], v.z, acc.z);
+            acc.w = fmaf(mw[w], v.w, acc.w);
+          }
+          store_bf16x4(p.part_o + prow * D + lane * 4,
+                       make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv));
+        }
+        if (lane == 0)
+          p.part_lse[p.n_splits * p.lse_stride + row] = lsum > 0.f ? mg + log2f(lsum) : -INFINITY;
+      }
+    }
+    // the item goes back to the producer (its TMA will overwrite what this warp
     // wrote through the generic proxy)
     fence_proxy_async_smem();
     __syncwarp();
@@ -522,8 +499,7 @@ __device__ __forceinline__ void consume_suffix(const DecodeArgs& a, uint8_t* rin
 // chunk); rows past the workspace's arrive zero-filled and are not merged.  Then half
 // a warp merges each row: every lane computes the slots' weights from their LSEs and
 // sums features [i*D/16, (i+1)*D/16) of every slot, its loop unrolled to kSlots >= the
-// slot count.  An empty slot (lse -inf) gets weight 0 and its rows are not read into
-// the sum (a suffix slot that no piece wrote holds whatever an earlier call left).
+// slot count.  An empty slot (lse -inf) gets weight 0.
 template <int D, int kSlots>
 __device__ __forceinline__ void merge_rows_staged(const DecodeArgs& a, const CUtensorMap* tm_po,
                                                   const CUtensorMap* tm_pl, uint8_t* smem,
@@ -531,7 +507,7 @@ __device__ __forceinline__ void merge_rows_staged(const DecodeArgs& a, const CUt
   constexpr int kF = D / 16;
   using Vec = typename std::conditional<kF == 8, uint4, uint2>::type;
   const PrefixArgs& p = a.pre;
-  const int n = p.n_splits + a.suffix_slots;  // slots
+  const int n = p.n_splits + 1;  // slots
   const int chunk = a.merge_rows;
   const int lbox = (chunk + 6) & ~3;  // LSEs per slot in a chunk's copy
   const int64_t rows = static_cast<int64_t>(p.total_q) * p.num_q_heads;
@@ -592,7 +568,6 @@ __device__ __forceinline__ void merge_rows_staged(const DecodeArgs& a, const CUt
       for (int f = 0; f < kF; ++f) acc[f] = 0.f;
 #pragma unroll
       for (int s = 0; s < kSlots; ++s) {
-        if (l[s] == 0.f) continue;
         const uint32_t* u = reinterpret_cast<const uint32_t*>(&v[s]);
 #pragma unroll
         for (int f = 0; f < kF / 2; ++f) {
@@ -624,10 +599,9 @@ __device__ __forceinline__ void merge_rows_staged(const DecodeArgs& a, const CUt
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_cascade_kernel(const __grid_constant__ CUtensorMap tm_q,
+                          const __grid_constant__ CUtensorMap tm_k,
                           const __grid_constant__ CUtensorMap tm_v,
                           const __grid_constant__ CUtensorMap tm_kp,
-                          const __grid_constant__ CUtensorMap tm_ks,
-                          const __grid_constant__ CUtensorMap tm_vs,
                           const __grid_constant__ CUtensorMap tm_po,
                           const __grid_constant__ CUtensorMap tm_pl, const DecodeArgs a) {
   using L = SLayout<D>;
@@ -636,12 +610,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const PrefixArgs& p = a.pre;
   const int warp = threadIdx.x >> 5;
-  // generation of the grid barrier at the end (read now, off the critical path)
-  const unsigned g0 = threadIdx.x == 0 ? ld_acquire_gpu_u32(a.bar_gen) : 0u;
+  const int lane = threadIdx.x & 31;
+  // generation of the grid barrier at the end, read now with a relaxed load: nothing
+  // waits on it until the barrier (an acquire here would hold thread 0, and through the
+  // first CTA barrier every warp, for a round trip to memory).  The previous call
+  // advanced it before that kernel ended, and this CTA's arrival below (a release)
+  // orders the read before any CTA of this call can advance it.
+  unsigned g0 = 0u;
+  if (threadIdx.x == 0)
+    asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(g0) : "l"(a.bar_gen) : "memory");
   // the first TMA through each map would otherwise wait for its descriptor
-  if (threadIdx.x == 32 * kWarpProducer) {
-    prefetch_tensormap(&tm_ks);
-    prefetch_tensormap(&tm_vs);
+  if (threadIdx.x == 32 * kWarpScheduler) {
+    prefetch_tensormap(&tm_k);
     prefetch_tensormap(&tm_v);
     prefetch_tensormap(&tm_q);
     prefetch_tensormap(&tm_kp);
@@ -666,19 +646,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
   }
 
-  // ---- role 2: the suffix units, produced by warp 8 and computed by warps [0, Hkv)
-  const int S = a.ring_slots;
-  uint64_t* st_full = reinterpret_cast<uint64_t*>(smem + L::kSuffixBars);  // [S]
-  uint64_t* st_empty = st_full + kDecodeMaxRing;                           // [S]
-  ItemDesc* idesc = reinterpret_cast<ItemDesc*>(st_empty + kDecodeMaxRing); // [S]
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(idesc + kDecodeMaxRing);
+  // ---- role 2: the suffix units, produced by warp 8 and computed by warps 0-7
+  constexpr int kS = L::kSlots;
+  uint64_t* st_full = reinterpret_cast<uint64_t*>(smem + L::kSuffixBars);  // [kS]
+  uint64_t* st_empty = st_full + kS;                                        // [kS]
+  ItemDesc* idesc = reinterpret_cast<ItemDesc*>(st_empty + kS);              // [kS]
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(idesc + kS);
   uint64_t* merge_bar = reinterpret_cast<uint64_t*>(smem + L::kSuffixBars + kMergeBarOff);
   int u_begin, u_end;
-  unit_range_of(a, blockIdx.x, u_begin, u_end);
+  unit_range(a, u_begin, u_end);
   if (threadIdx.x == 0) {
-    for (int i = 0; i < S; ++i) {
-      mbar_init(&st_full[i], 1);                 // the producer's expect_tx arrival
-      mbar_init(&st_empty[i], p.num_kv_heads);  // one arrival per consumer warp
+    for (int i = 0; i < kS; ++i) {
+      mbar_init(&st_full[i], 1 + 32);  // the producer's expect_tx + its lanes' copies
+      mbar_init(&st_empty[i], kStreamWarps / a.unit_groups);  // the warps of one unit
     }
     mbar_init(merge_bar, 1);
     *abort_flag = 0;
@@ -686,13 +666,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   __syncthreads();
   if (u_begin < u_end) {  // (a prefix CTA may have none)
-    if (warp == kWarpProducer) {
-      produce_suffix<D>(a, &tm_ks, &tm_vs, smem, st_full, st_empty, idesc, abort_flag);
-    } else if (warp < p.num_kv_heads) {
-      if (a.max_rows <= 8)
-        consume_suffix<D, 1>(a, smem, st_full, st_empty, idesc, abort_flag);
+    if (warp == kWarpScheduler) {
+      produce_items<D>(a, &tm_k, &tm_v, smem, st_full, st_empty, idesc, abort_flag);
+    } else if (warp < kStreamWarps) {
+      if (a.unit_groups == 2)
+        consume_items<D, 2>(a, smem, st_full, st_empty, idesc, abort_flag);
       else
-        consume_suffix<D, 2>(a, smem, st_full, st_empty, idesc, abort_flag);
+        consume_items<D, 1>(a, smem, st_full, st_empty, idesc, abort_flag);
     }
   }
   // the bulk copies of the merge below overwrite what was written here through the
@@ -727,16 +707,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   // which are contiguous in every slot: one bulk copy per slot brings a chunk of them
   // (and their LSEs) into shared memory, then half a warp merges each row
   // (the slot loop is unrolled to a bound: 8 when it suffices)
-  if (p.n_splits + a.suffix_slots <= 8)
+  if (p.n_splits + 1 <= 8)
     merge_rows_staged<D, 8>(a, &tm_po, &tm_pl, smem, merge_bar, abort_flag);
   else
     merge_rows_staged<D, kDecodeMaxParts>(a, &tm_po, &tm_pl, smem, merge_bar, abort_flag);
 }
 
 template <int D>
-cudaError_t launch_decode_d(const CUtensorMap& tm_q, const CUtensorMap& tm_v,
-                            const CUtensorMap& tm_kp, const CUtensorMap& tm_ks,
-                            const CUtensorMap& tm_vs, const CUtensorMap& tm_po,
+cudaError_t launch_decode_d(const CUtensorMap& tm_q, const CUtensorMap& tm_k,
+                            const CUtensorMap& tm_v, const CUtensorMap& tm_kp,
+                            const CUtensorMap& tm_po,
                             const CUtensorMap& tm_pl, const DecodeArgs& a, int grid,
                             cudaStream_t stream) {
   static std::atomic<uint64_t> attr_done{0};
@@ -753,22 +733,19 @@ cudaError_t launch_decode_d(const CUtensorMap& tm_q, const CUtensorMap& tm_v,
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, decode_cascade_kernel<D>, tm_q, tm_v, tm_kp, tm_ks, tm_vs,
-                            tm_po, tm_pl, a);
+  return cudaLaunchKernelEx(&cfg, decode_cascade_kernel<D>, tm_q, tm_k, tm_v, tm_kp, tm_po,
+                            tm_pl, a);
 }
 
 }  // namespace
 
-int decode_ring_bytes() { return SLayout<128>::kRing; }
-
-cudaError_t launch_decode(int head_dim, const CUtensorMap& tm_q, const CUtensorMap& tm_v,
-                          const CUtensorMap& tm_kp, const CUtensorMap& tm_ks,
-                          const CUtensorMap& tm_vs, const CUtensorMap& tm_po,
-                          const CUtensorMap& tm_pl, const DecodeArgs& a, int grid,
-                          cudaStream_t stream) {
+cudaError_t launch_decode(int head_dim, const CUtensorMap& tm_q, const CUtensorMap& tm_k,
+                          const CUtensorMap& tm_v, const CUtensorMap& tm_kp,
+                          const CUtensorMap& tm_po, const CUtensorMap& tm_pl,
+                          const DecodeArgs& a, int grid, cudaStream_t stream) {
   if (head_dim == 64)
-    return launch_decode_d<64>(tm_q, tm_v, tm_kp, tm_ks, tm_vs, tm_po, tm_pl, a, grid, stream);
-  return launch_decode_d<128>(tm_q, tm_v, tm_kp, tm_ks, tm_vs, tm_po, tm_pl, a, grid, stream);
+    return launch_decode_d<64>(tm_q, tm_k, tm_v, tm_kp, tm_po, tm_pl, a, grid, stream);
+  return launch_decode_d<128>(tm_q, tm_k, tm_v, tm_kp, tm_po, tm_pl, a, grid, stream);
 }
 
 }  // namespace csp

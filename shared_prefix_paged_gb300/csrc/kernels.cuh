@@ -65,24 +65,18 @@ struct PagedArgs {
 };
 
 // Single-kernel cascade step for decode-like batches (decode_cascade.cu): at most 16
-// packed rows (query, head-in-group) per request and KV head, at most 8 KV heads.
-// CTAs [0, prefix_ctas) run one prefix range each (pre.n_splits ranges per (KV head,
-// 256-row block), range s = 64-key tiles [s*key_tiles/n_splits,
-// (s+1)*key_tiles/n_splits), slot s), then stream prefix_units suffix units; the
-// other CTAs share the remaining suffix units.  A suffix unit is a run of unit_pages
-// suffix pages of one request, all KV heads (request r owns units
-// [r*units_per_req, (r+1)*units_per_req)).  A CTA's consecutive units of one request
-// form one piece, whose partial goes to slot n_splits + (the CTA's index - the index
-// of the first CTA holding a unit of that request); suffix_slots bounds that index.
-// After a grid-wide barrier every CTA merges an equal share of the rows from slots
-// [0, n_splits + suffix_slots).
-// Most partial results per row one merge reads.
+// packed rows (query, head-in-group) per request and KV head.  CTAs [0, prefix_ctas)
+// run one prefix range each (pre.n_splits ranges per (KV head, 256-row block), range
+// s = 64-key tiles [s*key_tiles/n_splits, (s+1)*key_tiles/n_splits), slot s), then
+// stream prefix_units suffix units; the other CTAs share the remaining suffix units
+// (request, KV head).  Suffix partials go to slot n_splits.  After a grid-wide barrier
+// every CTA merges an equal share of the rows from slots [0, n_splits].
+// Most partial results per row (the prefix ranges + the suffix): one merge reads at
+// most 16 slots.
 constexpr int kDecodeMaxParts = 16;
-// Ring slots of the suffix stream (upper bound).
-constexpr int kDecodeMaxRing = 6;
 
 struct DecodeArgs {
-  PrefixArgs pre;            // prefix phase; part_o / part_lse hold the slots above
+  PrefixArgs pre;            // prefix phase; part_o / part_lse hold n_splits + 1 slots
   const __nv_bfloat16* q;    // [total_q][num_q_heads][D]
   const __nv_bfloat16* k;    // [num_blocks][16][num_kv_heads][D]
   const __nv_bfloat16* v;
@@ -94,16 +88,9 @@ struct DecodeArgs {
   int prefix_ctas;           // num_kv_heads * pre.pairs * pre.n_splits (<= grid)
   int prefix_units;          // suffix units each prefix CTA streams after its range
   int merge_rows;            // rows per merge chunk (the merge tensor maps' box)
+  int unit_groups;           // 2: every suffix unit is one item (<= 128 keys) and two groups
+                             // of four warps take alternate units; 1: all eight warps
   int key_tiles;             // ceil(cpl / 64)
-  int units_per_req;         // suffix units per request
-  int unit_pages;            // suffix pages per unit
-  int item_pages;            // pages per ring item (all KV heads, K and V)
-  int page_bytes;            // one page of K (or V) of every KV head: 16 * Hkv * D * 2
-  int item_bytes;            // one ring slot: item_pages pages of K and V, then the Q area
-  int ring_slots;            // <= kDecodeMaxRing
-  int q_off;                 // the Q area's offset within a ring slot
-  int suffix_slots;          // suffix pieces per request at most
-  int max_rows;              // packed rows per request and KV head at most (<= 16)
   int* bar_count;            // zero at launch; the kernel leaves it zero
   unsigned* bar_gen;         // any value; advanced by one per call
   __nv_bfloat16* out;
@@ -111,20 +98,15 @@ struct DecodeArgs {
 };
 
 // grid <= the number of co-resident CTAs (one per SM); launched cooperatively.
-// tm_po / tm_pl: the workspace slots as bf16 [n_splits + suffix_slots][rows][D] and
-// fp32 [n_splits + suffix_slots][pre.lse_stride], boxes of merge_rows rows (and of
+// tm_po / tm_pl: the workspace slots as bf16 [n_splits + 1][rows][D] and fp32
+// [n_splits + 1][pre.lse_stride], boxes of merge_rows rows (and of
 // (merge_rows + 6) & ~3 LSEs).
-// tm_ks / tm_vs: the K / V cache as pages of every KV head with both feature halves
-// (boxes {64, 16, D / 64, Hkv} of {64, tokens, D / 64, Hkv}), for the suffix; tm_v: V
-// as pages of one KV head (boxes {64, 16, D / 64, 1}) and tm_kp: K as {D, Hkv,
+// tm_k / tm_v: the K / V cache as pages of one KV head with both feature halves
+// (boxes {64, 16, D / 64, 1} of {64, tokens, D / 64, Hkv}); tm_kp: K as {D, Hkv,
 // tokens} with boxes {64, 1, 16}, for the prefix ranges.
-// Bytes of shared memory the decode schedule's suffix ring may use (ring_slots x
-// item_bytes must fit).
-int decode_ring_bytes();
-
-cudaError_t launch_decode(int head_dim, const CUtensorMap& tm_q, const CUtensorMap& tm_v,
-                          const CUtensorMap& tm_kp, const CUtensorMap& tm_ks,
-                          const CUtensorMap& tm_vs, const CUtensorMap& tm_po,
+cudaError_t launch_decode(int head_dim, const CUtensorMap& tm_q, const CUtensorMap& tm_k,
+                          const CUtensorMap& tm_v, const CUtensorMap& tm_kp,
+                          const CUtensorMap& tm_po,
                           const CUtensorMap& tm_pl, const DecodeArgs& a, int grid,
                           cudaStream_t stream);
 
