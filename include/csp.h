@@ -359,6 +359,79 @@ CSP_API int merge_states(void* out, float* out_lse, const void* prefix_out, cons
                  int32_t num_heads, int32_t head_dim, int32_t partial_dtype, void* stream);
 
 /*
+ * cascade_plan_device — the common-prefix planner as one small kernel on `stream`, for
+ * steps captured in a CUDA graph.  §十一: cascade does not fit a full CUDA graph when
+ * the use-cascade decision is taken per batch on the host and the number of kernel
+ * calls follows it; §七: FlashInfer splits a plan step from a run step so that the run
+ * can be captured.  Here the plan reads the batch where it already is (device memory)
+ * and leaves its result there for cascade_attn_device_plan, so a step is the same
+ * fixed launches whatever the batch.  The arithmetic is cascade_plan's (§八 Step 1-2,
+ * §三, and the same modes), with the same results.
+ *
+ *   block_table          device int32 [num_reqs, bt_row_stride]
+ *   seq_lens             device int32 [num_reqs]
+ *   num_computed_tokens  device int32 [num_reqs]
+ *   plan_out             device int32 [4]: [0] the prefix length for the attention call
+ *                        (common_prefix_len when cascade is taken, else 0), [1]
+ *                        use_cascade, [2] common_prefix_len, [3] status (CSP_OK, or
+ *                        CSP_ERR_INVALID_ARG for lengths cascade_plan would refuse, with
+ *                        [0..2] = 0)
+ * Asynchronous; no device-to-host copy.  Returns CSP_OK, CSP_ERR_INVALID_ARG (nothing
+ * launched) or CSP_ERR_CUDA.
+ */
+CSP_API int cascade_plan_device(const int32_t* block_table, int64_t bt_row_stride,
+                                int32_t num_reqs, const int32_t* seq_lens,
+                                const int32_t* num_computed_tokens, int32_t block_size,
+                                int32_t mode, int32_t* plan_out, void* stream);
+
+/*
+ * cascade_attn_device_plan — cascade_attn with the prefix length read from device
+ * memory (plan[0], as cascade_plan_device leaves it) when the kernel runs, so that the
+ * pair can be captured in a CUDA graph once and replayed for every batch that fits the
+ * launch plan.  The launch plan (grid, prefix key ranges, workspace partition) is made
+ * on the host for common_prefix_len_bound, a multiple of block_size at least as large
+ * as any plan[0] the launch will read (plan[0] is clamped to it); plan[0] = 0 computes
+ * the standard path.  Only the single-kernel schedule reads its prefix length from
+ * device memory: batches it does not take (more than 16 packed rows per request and
+ * KV head, more than 8 KV heads, or too many 256-row blocks) and a bound of 0 return
+ * CSP_ERR_UNSUPPORTED with nothing launched.  Size the workspace with
+ * csp_workspace_size for common_prefix_len_bound.  Other arguments, layouts and
+ * errors: as for cascade_attn.
+ */
+CSP_API int cascade_attn_device_plan(const void* q, const void* k_cache, const void* v_cache,
+                                     int32_t num_blocks, const int32_t* block_table,
+                                     int64_t bt_row_stride, const int32_t* cu_seqlens_q,
+                                     const int32_t* seqused_k, int32_t num_reqs,
+                                     int32_t total_q, int32_t max_seqlen_q,
+                                     int32_t max_seqlen_k, const int32_t* plan,
+                                     int32_t common_prefix_len_bound, int32_t block_size,
+                                     int32_t num_q_heads, int32_t num_kv_heads,
+                                     int32_t head_dim, float softmax_scale, void* out,
+                                     float* lse, void* workspace, size_t workspace_bytes,
+                                     void* stream);
+
+/*
+ * csp_apply_sinks — attention sinks (§九 "Attention Sinks": every backend takes an
+ * optional `sinks` argument).  Each query head h has one sink logit s_h (natural log,
+ * not multiplied by the softmax scale) that joins the softmax of every row of head h
+ * as one more key whose value row is zero.  Applied to a finished result of
+ * cascade_attn or paged_attn (its out and natural-log lse) as the LSE merge (§一,
+ * merge_attn_states) with an empty partial whose lse is s_h:
+ *     lse' = ln(e^lse + e^s_h),   out' = out * e^(lse - lse')
+ * so the step is exact up to one more bf16 rounding of out.  s_h = -inf leaves a row
+ * unchanged; a row with no key (lse = -inf) keeps out = 0 and gets lse' = s_h.
+ *
+ *   out     device bf16 [num_tokens, num_heads, head_dim], 16-byte aligned, in place
+ *   lse     device fp32 [num_tokens, num_heads], natural log, in place (required)
+ *   sinks   device fp32 [num_heads]
+ *   head_dim  a multiple of 8 with head_dim / 8 dividing 32 (8 ... 256)
+ * Asynchronous on `stream`; order it after the attention call that wrote out and lse.
+ * Returns CSP_OK, CSP_ERR_INVALID_ARG (nothing launched) or CSP_ERR_CUDA.
+ */
+CSP_API int csp_apply_sinks(void* out, float* lse, const float* sinks, int32_t num_tokens,
+                            int32_t num_heads, int32_t head_dim, void* stream);
+
+/*
  * csp_workspace_status — copies the workspace status word to the host (a blocking
  * copy on `stream`).  0 means no kernel reported a problem since the workspace was
  * zero-filled; CSP_ERR_TIMEOUT means a bounded wait gave up.  Writes *status_out.

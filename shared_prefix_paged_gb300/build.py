@@ -20,7 +20,7 @@ BUILD = os.path.join(HERE, "_build")
 INCLUDE = os.path.join(ROOT, "include")
 LIB_NAME = "libcsp_gb300.so"
 SOURCES = ["api.cu", "prefix_attn.cu", "paged_attn.cu", "paged_tc.cu", "decode_cascade.cu",
-           "combine.cu", "noalloc.cu"]
+           "combine.cu", "noalloc.cu", "plan_device.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

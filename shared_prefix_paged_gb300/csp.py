@@ -32,7 +32,8 @@ DTYPE_BF16, DTYPE_F32 = 0, 1
 EXPORTS = ("cascade_plan", "csp_workspace_size", "cascade_attn", "cascade_attn_timed",
            "cascade_attn_scheduled", "paged_attn", "merge_states", "csp_workspace_status",
            "csp_status_string", "csp_last_cuda_error", "csp_version", "cascade_attn_noalloc",
-           "csp_noalloc_status", "csp_cascade_schedule", "csp_validate_batch")
+           "csp_noalloc_status", "csp_cascade_schedule", "csp_validate_batch",
+           "csp_apply_sinks", "cascade_plan_device", "cascade_attn_device_plan")
 
 _lock = threading.Lock()
 _lib: Optional[ctypes.CDLL] = None
@@ -78,12 +79,16 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         lib.merge_states.argtypes = [p, p, p, p, p, p, i32, i32, i32, i32, p]
         lib.csp_workspace_status.argtypes = [p, p, p]
         lib.csp_validate_batch.argtypes = [p, i64, i32, p, p, i32, i32, i32, p]
+        lib.csp_apply_sinks.argtypes = [p, p, p, i32, i32, i32, p]
+        lib.cascade_plan_device.argtypes = [p, i64, i32, p, p, i32, i32, p, p]
+        lib.cascade_attn_device_plan.argtypes = attn + [p, i32] + tail
         lib.csp_status_string.argtypes = [ctypes.c_int]
         lib.csp_status_string.restype = ctypes.c_char_p
         for name in ("cascade_plan", "csp_workspace_size", "cascade_attn", "cascade_attn_timed",
                      "cascade_attn_scheduled", "paged_attn",
                      "merge_states", "csp_workspace_status", "csp_last_cuda_error",
-                     "csp_version", "csp_cascade_schedule", "csp_validate_batch"):
+                     "csp_version", "csp_cascade_schedule", "csp_validate_batch",
+                     "csp_apply_sinks", "cascade_plan_device", "cascade_attn_device_plan"):
             getattr(lib, name).restype = ctypes.c_int
         _lib = lib
         return lib
@@ -238,7 +243,7 @@ def alloc_workspace(nbytes: int, device):
 def _attn(fn_name, q, k_cache, v_cache, block_table, cu_seqlens_q, seqused_k, *, max_seqlen_q,
           max_seqlen_k, softmax_scale, common_prefix_len=None, out=None, lse=None,
           workspace=None, stream=None, phase_events=None, schedule=None, prefix_ranges=0,
-          validate=None):
+          validate=None, sinks=None):
     import torch
     lib = load()
     total_q, hq, d = q.shape
@@ -277,15 +282,19 @@ def _attn(fn_name, q, k_cache, v_cache, block_table, cu_seqlens_q, seqused_k, *,
         handles = (ctypes.c_void_p * 4)(*[ev.cuda_event for ev in phase_events])
         args.append(ctypes.cast(handles, ctypes.c_void_p))
     _check(getattr(lib, fn_name)(*args), fn_name)
+    if sinks is not None:
+        apply_sinks(out, lse, sinks, stream=stream)
     return out, lse
 
 
 def cascade_attn(q, k_cache, v_cache, block_table, cu_seqlens_q, seqused_k, *, max_seqlen_q,
                  max_seqlen_k, common_prefix_len, softmax_scale, out=None, lse=None,
                  workspace=None, stream=None, phase_events=None, schedule=None,
-                 prefix_ranges=0, validate=None):
+                 prefix_ranges=0, validate=None, sinks=None):
     """Cascade attention (prefix phase + suffix phase + LSE merge) on device tensors.
 
+    sinks: optional fp32 device tensor [Hq] of per-head sink logits (natural log),
+    applied to the result by csp_apply_sinks.
     validate: optional host copies (block_table, seq_lens, cu_seqlens_q) that the
     library checks (csp_validate_batch) before launching; a bad batch raises
     CspError(CSP_ERR_INVALID_ARG) and nothing runs on the device.
@@ -301,18 +310,32 @@ def cascade_attn(q, k_cache, v_cache, block_table, cu_seqlens_q, seqused_k, *, m
                  max_seqlen_q=max_seqlen_q, max_seqlen_k=max_seqlen_k,
                  softmax_scale=softmax_scale, common_prefix_len=common_prefix_len, out=out,
                  lse=lse, workspace=workspace, stream=stream, phase_events=phase_events,
-                 schedule=schedule, prefix_ranges=prefix_ranges, validate=validate)
+                 schedule=schedule, prefix_ranges=prefix_ranges, validate=validate,
+                 sinks=sinks)
 
 
 def paged_attn(q, k_cache, v_cache, block_table, cu_seqlens_q, seqused_k, *, max_seqlen_q,
                max_seqlen_k, softmax_scale, out=None, lse=None, workspace=None, stream=None,
-               validate=None):
-    """Standard (flat) paged attention on device tensors (validate: as for
+               validate=None, sinks=None):
+    """Standard (flat) paged attention on device tensors (validate, sinks: as for
     cascade_attn)."""
     return _attn("paged_attn", q, k_cache, v_cache, block_table, cu_seqlens_q, seqused_k,
                  max_seqlen_q=max_seqlen_q, max_seqlen_k=max_seqlen_k,
                  softmax_scale=softmax_scale, out=out, lse=lse, workspace=workspace,
-                 stream=stream, validate=validate)
+                 stream=stream, validate=validate, sinks=sinks)
+
+
+def apply_sinks(out, lse, sinks, *, stream=None):
+    """csp_apply_sinks: per-head sink logits (fp32 device tensor [Hq], natural log)
+    folded into a finished result (out bf16 [T, Hq, D] and lse fp32 [T, Hq], in place)."""
+    import torch
+    lib = load()
+    t, hq, d = out.shape
+    if sinks.dtype != torch.float32 or sinks.numel() != hq or not sinks.is_cuda:
+        raise ValueError("sinks: an fp32 device tensor with one logit per query head")
+    _check(lib.csp_apply_sinks(_ptr(out), _ptr(lse), _ptr(sinks.contiguous()), t, hq, d,
+                               _stream_ptr(stream, out.device)), "csp_apply_sinks")
+    return out, lse
 
 
 def merge_states(prefix_out, prefix_lse, suffix_out, suffix_lse, *, out=None, out_lse=None,

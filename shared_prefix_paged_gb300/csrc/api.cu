@@ -335,7 +335,7 @@ int attention_call(const void* q, const void* k_cache, const void* v_cache, int3
                    int32_t block_size, int32_t Hq, int32_t Hkv, int32_t D, float scale,
                    void* out, float* lse, void* workspace, size_t workspace_bytes,
                    void* stream_ptr, void* const* events = nullptr, int sched_override = -1,
-                   int ranges_override = 0) {
+                   int ranges_override = 0, const int32_t* cpl_dev = nullptr) {
   int st = check_shape(num_reqs, total_q, max_seqlen_q, max_seqlen_k, Hq, Hkv, D, block_size);
   if (st != CSP_OK) return st;
   if (cpl < 0 || cpl % block_size != 0 || cpl > max_seqlen_k) return CSP_ERR_INVALID_ARG;
@@ -354,6 +354,8 @@ int attention_call(const void* q, const void* k_cache, const void* v_cache, int3
   make_plan(num_reqs, total_q, max_seqlen_q, max_seqlen_k, cpl, Hq, Hkv, D, sms, &P,
             sched_override, ranges_override);
   if (sched_override == CSP_SCHEDULE_SINGLE && !P.single) return CSP_ERR_UNSUPPORTED;
+  // a prefix length in device memory: only the single-kernel schedule reads it there
+  if (cpl_dev != nullptr && (!P.single || cpl == 0)) return CSP_ERR_UNSUPPORTED;
   if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255) != 0 ||
       workspace_bytes < P.bytes)
     return CSP_ERR_WORKSPACE;
@@ -435,6 +437,8 @@ int attention_call(const void* q, const void* k_cache, const void* v_cache, int3
     da.bar_gen = reinterpret_cast<unsigned*>(ws + kOffBarGen);
     da.out = static_cast<__nv_bfloat16*>(out);
     da.lse = lse;
+    da.cpl_dev = cpl_dev;
+    da.max_seqlen_k = max_seqlen_k;
     // phase events: [0] before the kernel, [1..3] after it
     if ((e = mark(0)) != cudaSuccess) return cuda_fail(e);
     if ((e = csp::launch_decode(D, tm_q, tm_k, tm_v, tm_kp, tm_po, tm_pl, da, P.d_grid,
@@ -757,6 +761,51 @@ int merge_states(void* out, float* out_lse, const void* prefix_out, const float*
       static_cast<__nv_bfloat16*>(out), out_lse, prefix_out, prefix_lse, suffix_out, suffix_lse,
       num_tokens * num_heads, head_dim, partial_dtype == CSP_DTYPE_F32,
       static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? CSP_OK : cuda_fail(e);
+}
+
+int cascade_plan_device(const int32_t* block_table, int64_t bt_row_stride, int32_t num_reqs,
+                        const int32_t* seq_lens, const int32_t* num_computed_tokens,
+                        int32_t block_size, int32_t mode, int32_t* plan_out, void* stream) {
+  if (!plan_out || num_reqs < 0 || block_size <= 0 || bt_row_stride < 0)
+    return CSP_ERR_INVALID_ARG;
+  if (mode < CSP_MODE_AUTO || mode > CSP_MODE_PAGE_THRESHOLDS) return CSP_ERR_INVALID_ARG;
+  if (num_reqs > 0 && (!block_table || !seq_lens || !num_computed_tokens))
+    return CSP_ERR_INVALID_ARG;
+  cudaError_t e = csp::launch_plan_device(block_table, bt_row_stride, num_reqs, seq_lens,
+                                          num_computed_tokens, block_size, mode, plan_out,
+                                          static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? CSP_OK : cuda_fail(e);
+}
+
+int cascade_attn_device_plan(const void* q, const void* k_cache, const void* v_cache,
+                             int32_t num_blocks, const int32_t* block_table,
+                             int64_t bt_row_stride, const int32_t* cu_seqlens_q,
+                             const int32_t* seqused_k, int32_t num_reqs, int32_t total_q,
+                             int32_t max_seqlen_q, int32_t max_seqlen_k, const int32_t* plan,
+                             int32_t common_prefix_len_bound, int32_t block_size,
+                             int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                             float softmax_scale, void* out, float* lse, void* workspace,
+                             size_t workspace_bytes, void* stream) {
+  if (!plan) return CSP_ERR_INVALID_ARG;
+  return attention_call(q, k_cache, v_cache, num_blocks, block_table, bt_row_stride,
+                        cu_seqlens_q, seqused_k, num_reqs, total_q, max_seqlen_q, max_seqlen_k,
+                        common_prefix_len_bound, block_size, num_q_heads, num_kv_heads,
+                        head_dim, softmax_scale, out, lse, workspace, workspace_bytes, stream,
+                        nullptr, CSP_SCHEDULE_SINGLE, 0, plan);
+}
+
+int csp_apply_sinks(void* out, float* lse, const float* sinks, int32_t num_tokens,
+                    int32_t num_heads, int32_t head_dim, void* stream) {
+  if (num_tokens < 0 || num_heads <= 0 || head_dim <= 0 || head_dim % 8 != 0 ||
+      32 % (head_dim / 8) != 0)
+    return CSP_ERR_INVALID_ARG;
+  if (num_tokens == 0) return CSP_OK;
+  if (!out || !lse || !sinks || !aligned16(out)) return CSP_ERR_INVALID_ARG;
+  if (static_cast<int64_t>(num_tokens) * num_heads > INT32_MAX) return CSP_ERR_INVALID_ARG;
+  cudaError_t e = csp::launch_apply_sinks(static_cast<__nv_bfloat16*>(out), lse, sinks,
+                                          num_tokens * num_heads, num_heads, head_dim,
+                                          static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? CSP_OK : cuda_fail(e);
 }
 

@@ -137,6 +137,42 @@ void launch_slots_d(const MergeArgs& m, unsigned grid, cudaStream_t stream) {
     merge_slots_kernel<D, kMaxParts><<<grid, kMergeThreads, 0, stream>>>(m);
 }
 
+// Attention sinks on a finished result: the LSE merge of row (t, h) with an empty
+// partial whose LSE is sinks[h] (one more key of value zero in the row's softmax):
+//   lse' = ln(e^lse + e^s),  out' = out e^(lse - lse').
+// Each thread rescales 8 features of one row; a row's threads sit in one warp (D / 8
+// divides 32), which reads every row's LSE before any of them is rewritten.
+__global__ void __launch_bounds__(256)
+    apply_sinks_kernel(__nv_bfloat16* __restrict__ out, float* __restrict__ lse,
+                       const float* __restrict__ sinks, int rows, int heads, int head_dim) {
+  const int chunks = head_dim / 8;
+  const int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const bool valid = idx < static_cast<int64_t>(rows) * chunks;
+  const int row = valid ? static_cast<int>(idx / chunks) : 0;
+  const int c = valid ? static_cast<int>(idx % chunks) : 0;
+  const float l = valid ? lse[row] : 0.f;
+  __syncwarp();
+  if (!valid) return;
+  const float s = __ldg(sinks + row % heads);
+  const float m = fmaxf(l, s);
+  float lnew = -INFINITY, w = 0.f;
+  if (m != -INFINITY) {
+    const float a = expf(l - m), b = expf(s - m);
+    lnew = m + logf(a + b);
+    w = a / (a + b);
+  }
+  uint4* p = reinterpret_cast<uint4*>(out + static_cast<int64_t>(row) * head_dim + c * 8);
+  uint4 u = *p;
+  __nv_bfloat162* pu = reinterpret_cast<__nv_bfloat162*>(&u);
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const float2 f = __bfloat1622float2(pu[e]);
+    pu[e] = __floats2bfloat162_rn(f.x * w, f.y * w);
+  }
+  *p = u;
+  if (c == 0) lse[row] = lnew;
+}
+
 }  // namespace
 
 cudaError_t launch_merge_slots(int head_dim, const __nv_bfloat16* part_o, const float* part_lse,
@@ -169,6 +205,19 @@ cudaError_t launch_merge_states(__nv_bfloat16* out, float* out_lse, const void* 
     merge_states_kernel<true><<<grid, 256, 0, stream>>>(out, out_lse, o1, l1, o2, l2, rows, head_dim);
   else
     merge_states_kernel<false><<<grid, 256, 0, stream>>>(out, out_lse, o1, l1, o2, l2, rows, head_dim);
+  return cudaGetLastError();
+}
+
+}  // namespace csp
+
+namespace csp {
+
+cudaError_t launch_apply_sinks(__nv_bfloat16* out, float* lse, const float* sinks, int rows,
+                               int heads, int head_dim, cudaStream_t stream) {
+  const int64_t threads = static_cast<int64_t>(rows) * (head_dim / 8);
+  const int64_t grid = (threads + 255) / 256;
+  apply_sinks_kernel<<<static_cast<unsigned>(grid), 256, 0, stream>>>(out, lse, sinks, rows,
+                                                                     heads, head_dim);
   return cudaGetLastError();
 }
 

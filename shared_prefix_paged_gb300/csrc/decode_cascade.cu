@@ -597,13 +597,10 @@ __device__ __forceinline__ void merge_rows_staged(const DecodeArgs& a, const CUt
 
 // ------------------------------------------------------------------ the kernel --
 template <int D>
-__global__ void __launch_bounds__(kThreads, 1)
-    decode_cascade_kernel(const __grid_constant__ CUtensorMap tm_q,
-                          const __grid_constant__ CUtensorMap tm_k,
-                          const __grid_constant__ CUtensorMap tm_v,
-                          const __grid_constant__ CUtensorMap tm_kp,
-                          const __grid_constant__ CUtensorMap tm_po,
-                          const __grid_constant__ CUtensorMap tm_pl, const DecodeArgs a) {
+__device__ __forceinline__ void decode_body(const CUtensorMap& tm_q, const CUtensorMap& tm_k,
+                                            const CUtensorMap& tm_v, const CUtensorMap& tm_kp,
+                                            const CUtensorMap& tm_po, const CUtensorMap& tm_pl,
+                                            const DecodeArgs& a) {
   using L = SLayout<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -714,13 +711,51 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    decode_cascade_kernel(const __grid_constant__ CUtensorMap tm_q,
+                          const __grid_constant__ CUtensorMap tm_k,
+                          const __grid_constant__ CUtensorMap tm_v,
+                          const __grid_constant__ CUtensorMap tm_kp,
+                          const __grid_constant__ CUtensorMap tm_po,
+                          const __grid_constant__ CUtensorMap tm_pl, const DecodeArgs a) {
+  decode_body<D>(tm_q, tm_k, tm_v, tm_kp, tm_po, tm_pl, a);
+}
+
+// The same step with the prefix length read from device memory (*a.cpl_dev, written
+// by the device planner before this launch): the launch plan was made for an upper
+// bound of it, and everything that follows from the prefix length (the prefix's key
+// tiles, where the suffix starts, whether a request's suffix fits one item) is set
+// here from the value read.  A prefix length of 0 leaves the prefix ranges empty and
+// gives every request all its keys in the suffix phase: the standard path.
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    decode_cascade_dev_kernel(const __grid_constant__ CUtensorMap tm_q,
+                              const __grid_constant__ CUtensorMap tm_k,
+                              const __grid_constant__ CUtensorMap tm_v,
+                              const __grid_constant__ CUtensorMap tm_kp,
+                              const __grid_constant__ CUtensorMap tm_po,
+                              const __grid_constant__ CUtensorMap tm_pl, const DecodeArgs a_in) {
+  __shared__ int s_cpl;
+  if (threadIdx.x == 0) s_cpl = *a_in.cpl_dev;
+  __syncthreads();
+  DecodeArgs a = a_in;
+  const int cpl = min(max(s_cpl, 0), a_in.pre.cpl);  // (never past the bound planned for)
+  a.pre.cpl = cpl;
+  a.key_tiles = (cpl + 63) / 64;
+  a.unit_groups = a_in.max_seqlen_k - cpl <= 2 * 64 ? 2 : 1;
+  decode_body<D>(tm_q, tm_k, tm_v, tm_kp, tm_po, tm_pl, a);
+}
+
+template <int D>
 cudaError_t launch_decode_d(const CUtensorMap& tm_q, const CUtensorMap& tm_k,
                             const CUtensorMap& tm_v, const CUtensorMap& tm_kp,
                             const CUtensorMap& tm_po,
                             const CUtensorMap& tm_pl, const DecodeArgs& a, int grid,
                             cudaStream_t stream) {
-  static std::atomic<uint64_t> attr_done{0};
-  cudaError_t e = set_smem_once(decode_cascade_kernel<D>, SLayout<D>::kDynamic, attr_done);
+  static std::atomic<uint64_t> attr_done{0}, attr_done_dev{0};
+  auto kernel = a.cpl_dev ? decode_cascade_dev_kernel<D> : decode_cascade_kernel<D>;
+  cudaError_t e = set_smem_once(kernel, SLayout<D>::kDynamic,
+                                a.cpl_dev ? attr_done_dev : attr_done);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
@@ -733,8 +768,7 @@ cudaError_t launch_decode_d(const CUtensorMap& tm_q, const CUtensorMap& tm_k,
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, decode_cascade_kernel<D>, tm_q, tm_k, tm_v, tm_kp, tm_po,
-                            tm_pl, a);
+  return cudaLaunchKernelEx(&cfg, kernel, tm_q, tm_k, tm_v, tm_kp, tm_po, tm_pl, a);
 }
 
 }  // namespace

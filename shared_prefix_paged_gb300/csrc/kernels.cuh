@@ -95,6 +95,9 @@ struct DecodeArgs {
   unsigned* bar_gen;         // any value; advanced by one per call
   __nv_bfloat16* out;
   float* lse;                // natural-log LSE or nullptr
+  const int32_t* cpl_dev;    // null, or the prefix length in device memory (the launch
+                             // plan was made for pre.cpl, an upper bound of it)
+  int max_seqlen_k;          // the longest request's KV length
 };
 
 // grid <= the number of co-resident CTAs (one per SM); launched cooperatively.
@@ -137,5 +140,16 @@ cudaError_t launch_merge_slots(int head_dim, const __nv_bfloat16* part_o, const 
 cudaError_t launch_merge_states(__nv_bfloat16* out, float* out_lse, const void* o1,
                                 const float* l1, const void* o2, const float* l2, int rows,
                                 int head_dim, bool f32_partials, cudaStream_t stream);
+
+// The device planner (plan_device.cu): plan[0..3] = the prefix length to use (0 when
+// cascade is not taken), use_cascade, the common prefix length, status.
+cudaError_t launch_plan_device(const int32_t* block_table, int64_t bt_row_stride, int num_reqs,
+                               const int32_t* seq_lens, const int32_t* computed, int block_size,
+                               int mode, int32_t* plan, cudaStream_t stream);
+
+// Attention sinks applied to a finished result (rows = tokens x heads, natural-log
+// lse updated in place); head_dim / 8 divides 32.
+cudaError_t launch_apply_sinks(__nv_bfloat16* out, float* lse, const float* sinks, int rows,
+                               int heads, int head_dim, cudaStream_t stream);
 
 }  // namespace csp

@@ -146,3 +146,13 @@ def test_validate_batch_rejects_bad_tables():
     assert csp.validate_batch(np.zeros((0, 4), np.int32), [], **ok) == (csp.CSP_OK, -1)
     assert csp.validate_batch(b.block_table, b.seq_lens, block_size=16,
                               num_blocks=0)[0] == csp.CSP_ERR_INVALID_ARG
+
+
+def test_apply_sinks_argument_errors_launch_nothing():
+    lib = csp.load()
+    # head_dim not a multiple of 8, or with head_dim / 8 not dividing 32; missing lse
+    assert lib.csp_apply_sinks(None, None, None, 4, 8, 12, None) == csp.CSP_ERR_INVALID_ARG
+    assert lib.csp_apply_sinks(None, None, None, 4, 8, 24, None) == csp.CSP_ERR_INVALID_ARG
+    assert lib.csp_apply_sinks(None, None, None, 4, 0, 64, None) == csp.CSP_ERR_INVALID_ARG
+    assert lib.csp_apply_sinks(None, None, None, 4, 8, 64, None) == csp.CSP_ERR_INVALID_ARG
+    assert lib.csp_apply_sinks(None, None, None, 0, 8, 64, None) == csp.CSP_OK
