@@ -70,3 +70,68 @@ def plan(block_table, seq_lens, num_computed_tokens, block_size: int):
     ncpb = num_common_prefix_blocks(block_table, seq_lens, block_size)
     cpl = common_prefix_len(ncpb, block_size, num_computed_tokens)
     return cpl, use_cascade_thresholds(cpl, len(seq_lens))
+
+
+# -- multi-level cascade ---------------------------------------------------------------
+# "vLLM Cascade Attention：用法、场景与原理解析" §七: FlashInfer's cascade runs any
+# number of levels (num_levels), where vLLM's runs two (prefix + suffix).  Reading: the
+# levels form a prefix tree over consecutive requests; a level-d segment is a run of at
+# least two consecutive requests that share the blocks of keys [k_lo, k_hi) beyond the
+# segment of level d - 1 that holds them (level 0: the whole batch, from key 0).  Within
+# each segment the plan is §八 Step 1-2's again: the longest run of shared block ids from
+# k_lo (each row only within its used entries), capped to the segment's minimum
+# num_computed_tokens and floored to block_size; a request's suffix starts at the end of
+# the deepest segment that holds it.  Below a segment, the requests split into maximal
+# runs that share the next block; a run of one request has no further level.
+
+
+def plan_levels(block_table, seq_lens, num_computed_tokens, block_size: int,
+                max_levels: int):
+    """(segments, suffix_start): segments as (level, r_lo, r_hi, k_lo, k_hi) in the order
+    a depth-first walk emits them, and each request's suffix start (token)."""
+    n = len(seq_lens)
+    used = [_cdiv(int(seq_lens[r]), block_size) for r in range(n)]
+    start = [0] * n
+    segments = []
+
+    def shared_run(r_lo, r_hi, col):
+        """Columns from `col` on that every row of [r_lo, r_hi) uses and shares."""
+        k = col
+        while True:
+            if any(k >= used[r] for r in range(r_lo, r_hi)):
+                return k - col
+            first = int(block_table[r_lo][k])
+            if any(int(block_table[r][k]) != first for r in range(r_lo, r_hi)):
+                return k - col
+            k += 1
+
+    def walk(r_lo, r_hi, k_lo, level):
+        if level >= max_levels:
+            return
+        k_next = k_lo
+        if r_hi - r_lo >= 2:
+            nb = shared_run(r_lo, r_hi, k_lo // block_size)
+            k_hi = (k_lo // block_size + nb) * block_size
+            k_hi = min(k_hi, min(int(num_computed_tokens[r]) for r in range(r_lo, r_hi)))
+            k_hi = (k_hi // block_size) * block_size
+            if k_hi > k_lo:
+                segments.append((level, r_lo, r_hi, k_lo, k_hi))
+                for r in range(r_lo, r_hi):
+                    start[r] = k_hi
+                k_next = k_hi
+        # the runs of consecutive requests that share the block at k_next
+        col = k_next // block_size
+        r = r_lo
+        while r < r_hi:
+            e = r + 1
+            if col < used[r]:
+                while e < r_hi and col < used[e] and \
+                        int(block_table[e][col]) == int(block_table[r][col]):
+                    e += 1
+            if e - r >= 2 and not (r == r_lo and e == r_hi and k_next == k_lo):
+                walk(r, e, k_next, level + 1)
+            r = e
+
+    if n > 0:
+        walk(0, n, 0, 0)
+    return segments, start
