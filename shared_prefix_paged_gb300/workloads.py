@@ -121,6 +121,16 @@ def build_batch(name: str, seq_lens, q_lens, shared_tokens: int, *, num_q_heads:
         tail = int(seq_lens[r]) % bs
         if private[r] > 0 and tail != 0:
             last_private.append((int(ids[-1]), tail))
+    return _draw(name, seq_lens, q_lens, table, num_blocks, shared_blocks, unused, last_private,
+                 num_q_heads=num_q_heads, num_kv_heads=num_kv_heads, head_dim=head_dim,
+                 gen=gen, block_size=bs, scale=scale, k_scale=k_scale)
+
+
+def _draw(name, seq_lens, q_lens, table, num_blocks, shared_blocks, unused, last_private, *,
+          num_q_heads, num_kv_heads, head_dim, gen, block_size, scale, k_scale) -> Batch:
+    """Step 3 of the module recipe and the poisoning, for a laid-out block table."""
+    n = int(seq_lens.shape[0])
+    bs = block_size
     total_q = int(q_lens.sum())
     hq, hkv, d = num_q_heads, num_kv_heads, head_dim
     q = torch.randn((total_q, hq, d), generator=gen, dtype=torch.float32).to(torch.bfloat16)
@@ -146,6 +156,57 @@ def build_batch(name: str, seq_lens, q_lens, shared_tokens: int, *, num_q_heads:
         q_lens=q_lens.astype(np.int32), cu_seqlens_q=cu, block_table=table.astype(np.int32),
         num_blocks=num_blocks, shared_blocks=shared_blocks, q=q.contiguous(),
         k_cache=k.contiguous(), v_cache=v.contiguous())
+
+
+def build_tree_batch(name: str, chunk_lens, paths, private_lens, q_lens, *,
+                     num_q_heads: int, num_kv_heads: int, head_dim: int,
+                     gen: torch.Generator, block_size: int = BLOCK_SIZE,
+                     scale: Optional[float] = None, pad_cols: int = 2) -> Batch:
+    """A batch whose requests share chunks of KV along a tree: request r's KV is the
+    chunks ``paths[r]`` (ids into ``chunk_lens``, each a whole number of blocks, laid
+    out once and shared by every request whose path holds it), then
+    ``private_lens[r]`` tokens of its own; its last ``q_lens[r]`` positions are this
+    step's queries.  Physical ids: the chunks' blocks take the first ids of the pool's
+    permutation in chunk order, then each request's private blocks; draws and
+    poisoning as for ``build_batch``."""
+    bs = block_size
+    chunk_lens = [int(c) for c in chunk_lens]
+    assert all(c > 0 and c % bs == 0 for c in chunk_lens)
+    n = len(paths)
+    assert len(private_lens) == n and len(q_lens) == n
+    seq_lens = np.array([sum(chunk_lens[c] for c in paths[r]) + int(private_lens[r])
+                         for r in range(n)], np.int64)
+    q_lens = np.asarray(q_lens, np.int64)
+    assert np.all(q_lens >= 0) and np.all(seq_lens >= q_lens)
+    chunk_blocks = [c // bs for c in chunk_lens]
+    private = [_cdiv(int(p), bs) for p in private_lens]
+    needed = sum(chunk_blocks) + sum(private)
+    num_blocks = math.ceil(1.25 * needed) + 1
+    perm = torch.randperm(num_blocks, generator=gen).numpy().astype(np.int64)
+    starts = np.concatenate([[0], np.cumsum(chunk_blocks)]).astype(np.int64)
+    cursor = int(starts[-1])
+    used = [sum(chunk_blocks[c] for c in paths[r]) + private[r] for r in range(n)]
+    width = max(used, default=0) + pad_cols
+    unused = perm[needed:]
+    assert unused.size >= 1
+    table = np.full((n, max(width, 1)), int(unused[0]), dtype=np.int64)
+    last_private = []
+    for r in range(n):
+        col = 0
+        for c in paths[r]:
+            table[r, col:col + chunk_blocks[c]] = perm[starts[c]:starts[c + 1]]
+            col += chunk_blocks[c]
+        ids = perm[cursor:cursor + private[r]]
+        cursor += private[r]
+        table[r, col:col + private[r]] = ids
+        tail = int(private_lens[r]) % bs
+        if private[r] > 0 and tail != 0:
+            last_private.append((int(ids[-1]), tail))
+    first = {p[0] for p in paths if p}
+    shared_blocks = chunk_blocks[first.pop()] if len(first) == 1 and all(paths) else 0
+    return _draw(name, seq_lens, q_lens, table, num_blocks, shared_blocks, unused,
+                 last_private, num_q_heads=num_q_heads, num_kv_heads=num_kv_heads,
+                 head_dim=head_dim, gen=gen, block_size=bs, scale=scale, k_scale=1.0)
 
 
 def _gen(seed: int) -> torch.Generator:
@@ -199,6 +260,26 @@ def sweep_point(n: int, p: int, s: int = 128) -> Batch:
     return decode_batch(seed=1000 + 100 * i_n + i_p, n=n, p=p, s=s)
 
 
+def tree_decode(seed: int = 1005, head_dim: int = 128, chunked: bool = False) -> Batch:
+    """A three-level decode batch: 16 requests over one 1024-token system prompt; two
+    families of 8 over their own documents (512 and 768 tokens); within the first
+    family two groups of 4 over 256-token sub-documents; 40 to 200 private tokens each
+    (the last one the query).  Hq 32, Hkv 8.  chunked: request 5 prefills its last 300
+    tokens (past its private ones, into its sub-document: the planner's cap then
+    shortens its segments) and request 12 its last 64."""
+    g = _gen(seed)
+    chunks = [1024, 512, 768, 256, 256]
+    paths = [(0, 1, 3)] * 4 + [(0, 1, 4)] * 4 + [(0, 2)] * 8
+    private = torch.randint(40, 201, (16,), generator=g).tolist()
+    q = [1] * 16
+    if chunked:
+        q[5] = 300
+        q[12] = 64
+    return build_tree_batch(f"tree_decode_D{head_dim}" + ("_chunked" if chunked else ""),
+                            chunks, paths, private, q, num_q_heads=32, num_kv_heads=8,
+                            head_dim=head_dim, gen=g)
+
+
 def by_name(name: str) -> Batch:
     """The named batch shapes used by the tests and the benchmark."""
     table = {
@@ -207,5 +288,7 @@ def by_name(name: str) -> Batch:
         "chunked": chunked_prefill,
         "chunked_cap": lambda: chunked_prefill(seed=1013, shared_tokens=3072),
         "long": long_prefix,
+        "tree": tree_decode,
+        "tree_chunked": lambda: tree_decode(seed=1006, chunked=True),
     }
     return table[name]()
