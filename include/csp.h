@@ -432,6 +432,76 @@ CSP_API int csp_apply_sinks(void* out, float* lse, const float* sinks, int32_t n
                             int32_t num_heads, int32_t head_dim, void* stream);
 
 /*
+ * Multi-level cascade.  §七: FlashInfer's cascade runs any number of levels
+ * (num_levels) where vLLM's runs two.  The levels form a prefix tree over consecutive
+ * requests: a segment (level, r_lo, r_hi, k_lo, k_hi) is a run of at least two
+ * consecutive requests [r_lo, r_hi) that share the blocks of keys [k_lo, k_hi), the
+ * keys right after those of the level - 1 segment that holds them (level 0: from key
+ * 0).  Each segment is found as §八 Step 1-2 finds the common prefix, within its own
+ * requests and from k_lo: the longest run of shared block ids, capped to the
+ * segment's minimum num_computed_tokens and floored to block_size.  A request's suffix
+ * starts at the end of the deepest segment that holds it (0 when none does).  A batch
+ * of two families of requests over one system prompt (a shared document per family)
+ * is the three-level case: the system prompt at level 0, each family's document at
+ * level 1, each request's own tokens in its suffix.
+ *
+ * cascade_plan_levels — the planner (host only).  Walks the prefix tree depth first,
+ * at most max_levels deep, and writes at most max_segments segments as 7 int32 each:
+ * level, r_lo, r_hi, k_lo, k_hi and the segment's query rows tok_lo, tok_hi (its
+ * requests' query tokens, q_len_r = seq_lens[r] - num_computed_tokens[r]); writes
+ * *num_segments_out and suffix_start_out[num_reqs] (host).  Block table and lengths:
+ * host arrays as for cascade_plan.  Returns CSP_OK, CSP_ERR_INVALID_ARG (lengths
+ * cascade_plan would refuse, max_levels outside 1..8) or CSP_ERR_UNSUPPORTED (more
+ * than max_segments segments).
+ */
+CSP_API int cascade_plan_levels(const int32_t* block_table, int64_t bt_row_stride,
+                                int32_t num_reqs, const int32_t* seq_lens,
+                                const int32_t* num_computed_tokens, int32_t block_size,
+                                int32_t max_levels, int32_t max_segments,
+                                int32_t* segments_out, int32_t* num_segments_out,
+                                int32_t* suffix_start_out);
+
+/*
+ * csp_workspace_size_levels — workspace bytes cascade_attn_levels needs for these
+ * segments (host array, as cascade_plan_levels writes them) and a longest suffix of
+ * max_suffix_len keys (max over r of seqused_k[r] - suffix_start[r]).  Returns
+ * CSP_OK, CSP_ERR_INVALID_ARG, CSP_ERR_UNSUPPORTED (the shapes cascade_attn refuses;
+ * more than 24 prefix slots: the levels' largest key-range splits added up) or
+ * CSP_ERR_CUDA (no device to size the grid for).
+ */
+CSP_API int csp_workspace_size_levels(int32_t num_reqs, int32_t total_q, int32_t max_seqlen_q,
+                                      int32_t max_seqlen_k, const int32_t* segments,
+                                      int32_t num_segments, int32_t max_suffix_len,
+                                      int32_t num_q_heads, int32_t num_kv_heads,
+                                      int32_t head_dim, size_t* bytes_out);
+
+/*
+ * cascade_attn_levels — attention through a multi-level cascade: every segment's
+ * query rows over its shared keys (non-causal: the keys lie within every one of its
+ * requests' computed tokens), each request's suffix keys [suffix_start[r],
+ * seqused_k[r]) causal, and the LSE merge of all of them; the result equals the
+ * standard path's up to rounding.  segments: host int32 [num_segments][7] as
+ * cascade_plan_levels writes them (the key ranges of the segments that hold a request
+ * must follow one another from key 0 to its suffix start; two segments of one level
+ * hold no request in common; each within every one of its requests' computed tokens);
+ * suffix_start: device int32 [num_reqs]; max_suffix_len as for
+ * csp_workspace_size_levels.  Segments of one level write that level's slots of the
+ * workspace; a row no segment of a level holds has an empty slot there (lse -inf).
+ * Other arguments, layouts and errors: as for cascade_attn; segments that break the
+ * host-checkable rules above return CSP_ERR_INVALID_ARG with nothing launched.
+ */
+CSP_API int cascade_attn_levels(const void* q, const void* k_cache, const void* v_cache,
+                                int32_t num_blocks, const int32_t* block_table,
+                                int64_t bt_row_stride, const int32_t* cu_seqlens_q,
+                                const int32_t* seqused_k, int32_t num_reqs, int32_t total_q,
+                                int32_t max_seqlen_q, int32_t max_seqlen_k,
+                                const int32_t* segments, int32_t num_segments,
+                                const int32_t* suffix_start, int32_t max_suffix_len,
+                                int32_t block_size, int32_t num_q_heads, int32_t num_kv_heads,
+                                int32_t head_dim, float softmax_scale, void* out, float* lse,
+                                void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * csp_workspace_status — copies the workspace status word to the host (a blocking
  * copy on `stream`).  0 means no kernel reported a problem since the workspace was
  * zero-filled; CSP_ERR_TIMEOUT means a bounded wait gave up.  Writes *status_out.

@@ -33,7 +33,8 @@ EXPORTS = ("cascade_plan", "csp_workspace_size", "cascade_attn", "cascade_attn_t
            "cascade_attn_scheduled", "paged_attn", "merge_states", "csp_workspace_status",
            "csp_status_string", "csp_last_cuda_error", "csp_version", "cascade_attn_noalloc",
            "csp_noalloc_status", "csp_cascade_schedule", "csp_validate_batch",
-           "csp_apply_sinks", "cascade_plan_device", "cascade_attn_device_plan")
+           "csp_apply_sinks", "cascade_plan_device", "cascade_attn_device_plan",
+           "cascade_plan_levels", "csp_workspace_size_levels", "cascade_attn_levels")
 
 _lock = threading.Lock()
 _lib: Optional[ctypes.CDLL] = None
@@ -82,13 +83,19 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         lib.csp_apply_sinks.argtypes = [p, p, p, i32, i32, i32, p]
         lib.cascade_plan_device.argtypes = [p, i64, i32, p, p, i32, i32, p, p]
         lib.cascade_attn_device_plan.argtypes = attn + [p, i32] + tail
+        lib.cascade_plan_levels.argtypes = [p, i64, i32, p, p, i32, i32, i32, p, p, p]
+        lib.csp_workspace_size_levels.argtypes = [i32, i32, i32, i32, p, i32, i32, i32, i32,
+                                                  i32, p]
+        lib.cascade_attn_levels.argtypes = attn + [p, i32, p, i32] + tail
         lib.csp_status_string.argtypes = [ctypes.c_int]
         lib.csp_status_string.restype = ctypes.c_char_p
         for name in ("cascade_plan", "csp_workspace_size", "cascade_attn", "cascade_attn_timed",
                      "cascade_attn_scheduled", "paged_attn",
                      "merge_states", "csp_workspace_status", "csp_last_cuda_error",
                      "csp_version", "csp_cascade_schedule", "csp_validate_batch",
-                     "csp_apply_sinks", "cascade_plan_device", "cascade_attn_device_plan"):
+                     "csp_apply_sinks", "cascade_plan_device", "cascade_attn_device_plan",
+                     "cascade_plan_levels", "csp_workspace_size_levels",
+                     "cascade_attn_levels"):
             getattr(lib, name).restype = ctypes.c_int
         _lib = lib
         return lib
@@ -323,6 +330,72 @@ def paged_attn(q, k_cache, v_cache, block_table, cu_seqlens_q, seqused_k, *, max
                  max_seqlen_q=max_seqlen_q, max_seqlen_k=max_seqlen_k,
                  softmax_scale=softmax_scale, out=out, lse=lse, workspace=workspace,
                  stream=stream, validate=validate, sinks=sinks)
+
+
+SEG_INTS = 7  # level, r_lo, r_hi, k_lo, k_hi, tok_lo, tok_hi
+
+
+def cascade_plan_levels(block_table, seq_lens, num_computed_tokens, *, block_size=16,
+                        max_levels=3, max_segments=256):
+    """(segments int32 [S, 7], suffix_start int32 [num_reqs]) of the multi-level planner
+    for host arrays; segments rows are (level, r_lo, r_hi, k_lo, k_hi, tok_lo, tok_hi)."""
+    lib = load()
+    bt = _host_i32(block_table)
+    sl = _host_i32(seq_lens)
+    nc = _host_i32(num_computed_tokens)
+    n = int(sl.shape[0])
+    stride = int(bt.shape[1]) if bt.ndim == 2 else 0
+    segs = np.zeros((max(max_segments, 1), SEG_INTS), np.int32)
+    start = np.zeros(max(n, 1), np.int32)
+    count = ctypes.c_int32(0)
+    _check(lib.cascade_plan_levels(bt.ctypes.data if bt.size else None, stride, n,
+                                   sl.ctypes.data if n else None,
+                                   nc.ctypes.data if n else None, block_size, max_levels,
+                                   max_segments, segs.ctypes.data, ctypes.byref(count),
+                                   start.ctypes.data), "cascade_plan_levels")
+    return segs[:count.value].copy(), start[:n].copy()
+
+
+def workspace_size_levels(num_reqs, total_q, max_seqlen_q, max_seqlen_k, segments,
+                          max_suffix_len, num_q_heads, num_kv_heads, head_dim) -> int:
+    lib = load()
+    seg = _host_i32(segments).reshape(-1, SEG_INTS)
+    out = ctypes.c_size_t(0)
+    _check(lib.csp_workspace_size_levels(num_reqs, total_q, max_seqlen_q, max_seqlen_k,
+                                         seg.ctypes.data if seg.size else None, seg.shape[0],
+                                         max_suffix_len, num_q_heads, num_kv_heads, head_dim,
+                                         ctypes.byref(out)), "csp_workspace_size_levels")
+    return int(out.value)
+
+
+def cascade_attn_levels(q, k_cache, v_cache, block_table, cu_seqlens_q, seqused_k, *,
+                        max_seqlen_q, max_seqlen_k, segments, suffix_start, max_suffix_len,
+                        softmax_scale, out=None, lse=None, workspace=None, stream=None):
+    """Multi-level cascade attention on device tensors: segments as cascade_plan_levels
+    returns them (host), suffix_start an int32 device tensor [num_reqs], max_suffix_len
+    the longest suffix in keys (seqused_k - suffix_start, maximum over requests)."""
+    import torch
+    lib = load()
+    total_q, hq, d = q.shape
+    num_blocks, bs, hkv, _ = k_cache.shape
+    n = int(seqused_k.shape[0])
+    seg = _host_i32(segments).reshape(-1, SEG_INTS)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((total_q, hq), dtype=torch.float32, device=q.device)
+    if workspace is None:
+        workspace = alloc_workspace(
+            workspace_size_levels(n, total_q, max_seqlen_q, max_seqlen_k, seg,
+                                  max_suffix_len, hq, hkv, d), q.device)
+    _check(lib.cascade_attn_levels(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), num_blocks, _ptr(block_table),
+        int(block_table.stride(0)), _ptr(cu_seqlens_q), _ptr(seqused_k), n, total_q,
+        int(max_seqlen_q), int(max_seqlen_k), seg.ctypes.data if seg.size else None,
+        seg.shape[0], _ptr(suffix_start), int(max_suffix_len), bs, hq, hkv, d,
+        float(softmax_scale), _ptr(out), _ptr(lse), _ptr(workspace), workspace.numel(),
+        _stream_ptr(stream, q.device)), "cascade_attn_levels")
+    return out, lse
 
 
 def apply_sinks(out, lse, sinks, *, stream=None):

@@ -7,6 +7,7 @@
 #include <cmath>
 #include <cstring>
 #include <mutex>
+#include <vector>
 
 #include "csp.h"
 #include "kernels.cuh"
@@ -326,6 +327,164 @@ void make_plan(int num_reqs, int total_q, int max_q, int max_k, int cpl, int Hq,
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+// ------------------------------------------------------------------ multi-level --
+// A multi-level cascade (§七: FlashInfer runs any number of levels): segments of
+// consecutive requests that share keys [k_lo, k_hi), each computed by the prefix body
+// over its requests' query rows into the slots of its level, then every request's
+// suffix from its own start, then the LSE merge of every slot.
+constexpr int kMaxLevels = 8;
+constexpr int kSegInts = 7;  // level, r_lo, r_hi, k_lo, k_hi, tok_lo, tok_hi
+
+struct LevelPlan {
+  int n_levels = 0;
+  int level_splits[kMaxLevels] = {};
+  int level_base[kMaxLevels] = {};
+  int n_prefix = 0;
+  LaunchPlan suf;  // the suffix (paged) part
+  int n_parts = 0;
+  size_t off_counters = 0, off_part_o = 0, off_part_lse = 0, bytes = 0;
+};
+
+// Key ranges per segment: one per 16 key tiles (1024 keys), at most 8.
+int segment_splits(const int32_t* seg) {
+  const int tiles = cdiv(seg[4] - seg[3], 64);
+  return std::max(1, std::min(8, tiles / 16));
+}
+
+// Host checks of a segment list: fields in range, and two segments that hold a request
+// in common of different levels, the shallower one holding all of the deeper one's
+// requests and ending where (or before) its keys start; so no key of a request is
+// counted twice.
+int check_segments(int num_reqs, int total_q, int max_k, const int32_t* segs, int n_seg) {
+  if (n_seg < 0 || (n_seg > 0 && !segs)) return CSP_ERR_INVALID_ARG;
+  for (int i = 0; i < n_seg; ++i) {
+    const int32_t* s = segs + static_cast<int64_t>(i) * kSegInts;
+    if (s[0] < 0 || s[0] >= kMaxLevels || s[1] < 0 || s[1] >= s[2] || s[2] > num_reqs ||
+        s[3] < 0 || s[3] % kPage != 0 || s[4] % kPage != 0 || s[4] <= s[3] || s[4] > max_k ||
+        s[5] < 0 || s[5] > s[6] || s[6] > total_q)
+      return CSP_ERR_INVALID_ARG;
+  }
+  for (int i = 0; i < n_seg; ++i) {
+    const int32_t* a = segs + static_cast<int64_t>(i) * kSegInts;
+    for (int j = i + 1; j < n_seg; ++j) {
+      const int32_t* b = segs + static_cast<int64_t>(j) * kSegInts;
+      if (a[2] <= b[1] || b[2] <= a[1]) continue;
+      const int32_t* up = a[0] < b[0] ? a : b;
+      const int32_t* dn = a[0] < b[0] ? b : a;
+      if (a[0] == b[0] || dn[1] < up[1] || dn[2] > up[2] || dn[3] < up[4])
+        return CSP_ERR_INVALID_ARG;
+    }
+  }
+  return CSP_OK;
+}
+
+int make_level_plan(int num_reqs, int total_q, int max_q, int max_k, const int32_t* segs,
+                    int n_seg, int max_suffix_len, int Hq, int Hkv, int D, int sms,
+                    LevelPlan* out) {
+  LevelPlan L;
+  int st = check_segments(num_reqs, total_q, max_k, segs, n_seg);
+  if (st != CSP_OK) return st;
+  if (max_suffix_len < 0 || max_suffix_len > max_k) return CSP_ERR_INVALID_ARG;
+  for (int i = 0; i < n_seg; ++i) {
+    const int32_t* s = segs + static_cast<int64_t>(i) * kSegInts;
+    L.level_splits[s[0]] = std::max(L.level_splits[s[0]], segment_splits(s));
+    L.n_levels = std::max(L.n_levels, s[0] + 1);
+  }
+  for (int d = 0; d < L.n_levels; ++d) {
+    L.level_base[d] = L.n_prefix;
+    L.n_prefix += L.level_splits[d];
+  }
+  if (L.n_prefix > 24) return CSP_ERR_UNSUPPORTED;
+  // the suffix: as the two-kernel schedule's suffix kernel for suffixes of at most
+  // max_suffix_len keys, with at most 32 partials per row in all
+  make_plan(num_reqs, total_q, max_q, max_k, max_k - max_suffix_len, Hq, Hkv, D, sms, &L.suf,
+            CSP_SCHEDULE_TWO_KERNELS);
+  const int max_len = std::max(1, max_suffix_len);
+  int split_keys = L.suf.s_split_keys;
+  if (cdiv(max_len, split_keys) > 32 - L.n_prefix)
+    split_keys = cdiv(cdiv(max_len, 32 - L.n_prefix), 64) * 64;
+  L.suf.s_split_keys = split_keys;
+  L.suf.s_splits = std::max(1, cdiv(max_len, split_keys));
+  L.n_parts = L.n_prefix + L.suf.s_splits;
+  const size_t rows = static_cast<size_t>(total_q) * Hq;
+  L.off_counters = kHeaderBytes;
+  L.off_part_o = L.off_counters + align256(static_cast<size_t>(total_q) * Hkv * 4);
+  L.off_part_lse = L.off_part_o + align256(static_cast<size_t>(L.n_parts) * rows * D * 2);
+  L.bytes = L.off_part_lse + align256(static_cast<size_t>(L.n_parts) * rows * 4);
+  *out = L;
+  return CSP_OK;
+}
+
+// The planner's walk (the same steps as oracle.planner.plan_levels, in C++).
+struct LevelWalk {
+  const int32_t* bt;
+  int64_t stride;
+  const int32_t* seq_lens;
+  const int32_t* computed;
+  const int64_t* used;
+  const int32_t* tok;  // query token of request r: tok[r] .. tok[r + 1]
+  int bs, max_levels, max_segments;
+  int32_t* segs;
+  int n = 0;
+  int32_t* start;
+  bool overflow = false;
+
+  int64_t shared_run(int r_lo, int r_hi, int64_t col) const {
+    int64_t k = col;
+    for (;; ++k) {
+      for (int r = r_lo; r < r_hi; ++r)
+        if (k >= used[r]) return k - col;
+      const int32_t first = bt[static_cast<int64_t>(r_lo) * stride + k];
+      for (int r = r_lo + 1; r < r_hi; ++r)
+        if (bt[static_cast<int64_t>(r) * stride + k] != first) return k - col;
+    }
+  }
+
+  void walk(int r_lo, int r_hi, int64_t k_lo, int level) {
+    if (level >= max_levels || overflow) return;
+    int64_t k_next = k_lo;
+    if (r_hi - r_lo >= 2) {
+      const int64_t nb = shared_run(r_lo, r_hi, k_lo / bs);
+      int64_t k_hi = (k_lo / bs + nb) * bs;
+      int32_t min_c = INT32_MAX;
+      for (int r = r_lo; r < r_hi; ++r) min_c = std::min(min_c, computed[r]);
+      k_hi = std::min<int64_t>(k_hi, min_c);
+      k_hi = (k_hi / bs) * bs;
+      if (k_hi > k_lo) {
+        if (n >= max_segments) {
+          overflow = true;
+          return;
+        }
+        int32_t* s = segs + static_cast<int64_t>(n) * kSegInts;
+        s[0] = level;
+        s[1] = r_lo;
+        s[2] = r_hi;
+        s[3] = static_cast<int32_t>(k_lo);
+        s[4] = static_cast<int32_t>(k_hi);
+        s[5] = tok[r_lo];
+        s[6] = tok[r_hi];
+        ++n;
+        for (int r = r_lo; r < r_hi; ++r) start[r] = static_cast<int32_t>(k_hi);
+        k_next = k_hi;
+      }
+    }
+    // the runs of consecutive requests that share the block at k_next
+    const int64_t col = k_next / bs;
+    for (int r = r_lo; r < r_hi;) {
+      int e = r + 1;
+      if (col < used[r]) {
+        while (e < r_hi && col < used[e] &&
+               bt[static_cast<int64_t>(e) * stride + col] ==
+                   bt[static_cast<int64_t>(r) * stride + col])
+          ++e;
+      }
+      if (e - r >= 2 && !(r == r_lo && e == r_hi && k_next == k_lo)) walk(r, e, k_next, level + 1);
+      r = e;
+    }
+  }
+};
+
 
 // Shared body of cascade_attn (cpl > 0) and paged_attn (cpl == 0).
 int attention_call(const void* q, const void* k_cache, const void* v_cache, int32_t num_blocks,
@@ -793,6 +952,184 @@ int cascade_attn_device_plan(const void* q, const void* k_cache, const void* v_c
                         common_prefix_len_bound, block_size, num_q_heads, num_kv_heads,
                         head_dim, softmax_scale, out, lse, workspace, workspace_bytes, stream,
                         nullptr, CSP_SCHEDULE_SINGLE, 0, plan);
+}
+
+int cascade_plan_levels(const int32_t* block_table, int64_t bt_row_stride, int32_t num_reqs,
+                        const int32_t* seq_lens, const int32_t* num_computed_tokens,
+                        int32_t block_size, int32_t max_levels, int32_t max_segments,
+                        int32_t* segments_out, int32_t* num_segments_out,
+                        int32_t* suffix_start_out) {
+  if (!num_segments_out || num_reqs < 0 || block_size <= 0 || max_levels < 1 ||
+      max_levels > kMaxLevels || max_segments < 0 || (max_segments > 0 && !segments_out))
+    return CSP_ERR_INVALID_ARG;
+  *num_segments_out = 0;
+  if (num_reqs == 0) return CSP_OK;
+  if (!block_table || !seq_lens || !num_computed_tokens || !suffix_start_out)
+    return CSP_ERR_INVALID_ARG;
+  std::vector<int64_t> used(num_reqs);
+  std::vector<int32_t> tok(num_reqs + 1, 0);
+  for (int r = 0; r < num_reqs; ++r) {
+    if (seq_lens[r] < 0 || num_computed_tokens[r] < 0 || num_computed_tokens[r] > seq_lens[r])
+      return CSP_ERR_INVALID_ARG;
+    used[r] = cdiv64(seq_lens[r], block_size);
+    if (used[r] > bt_row_stride) return CSP_ERR_INVALID_ARG;
+    tok[r + 1] = tok[r] + (seq_lens[r] - num_computed_tokens[r]);
+    suffix_start_out[r] = 0;
+  }
+  LevelWalk w{block_table, bt_row_stride, seq_lens, num_computed_tokens, used.data(), tok.data(),
+              block_size, max_levels, max_segments, segments_out, 0, suffix_start_out};
+  w.walk(0, num_reqs, 0, 0);
+  if (w.overflow) return CSP_ERR_UNSUPPORTED;
+  *num_segments_out = w.n;
+  return CSP_OK;
+}
+
+int csp_workspace_size_levels(int32_t num_reqs, int32_t total_q, int32_t max_seqlen_q,
+                              int32_t max_seqlen_k, const int32_t* segments,
+                              int32_t num_segments, int32_t max_suffix_len, int32_t num_q_heads,
+                              int32_t num_kv_heads, int32_t head_dim, size_t* bytes_out) {
+  if (!bytes_out) return CSP_ERR_INVALID_ARG;
+  int st = check_shape(num_reqs, total_q, max_seqlen_q, max_seqlen_k, num_q_heads, num_kv_heads,
+                       head_dim, kPage);
+  if (st != CSP_OK) return st;
+  if ((st = check_segments(num_reqs, total_q, max_seqlen_k, segments, num_segments)) != CSP_OK)
+    return st;
+  if (max_suffix_len < 0 || max_suffix_len > max_seqlen_k) return CSP_ERR_INVALID_ARG;
+  int sms = 0;
+  if ((st = device_sm_count(&sms)) != CSP_OK) return st;
+  LevelPlan L;
+  if ((st = make_level_plan(num_reqs, total_q, max_seqlen_q, max_seqlen_k, segments,
+                            num_segments, max_suffix_len, num_q_heads, num_kv_heads, head_dim,
+                            sms, &L)) != CSP_OK)
+    return st;
+  *bytes_out = L.bytes;
+  return CSP_OK;
+}
+
+int cascade_attn_levels(const void* q, const void* k_cache, const void* v_cache, int32_t num_blocks,
+                        const int32_t* block_table, int64_t bt_row_stride,
+                        const int32_t* cu_seqlens_q, const int32_t* seqused_k, int32_t num_reqs,
+                        int32_t total_q, int32_t max_seqlen_q, int32_t max_seqlen_k,
+                        const int32_t* segments, int32_t num_segments,
+                        const int32_t* suffix_start, int32_t max_suffix_len, int32_t block_size,
+                        int32_t Hq, int32_t Hkv, int32_t D, float softmax_scale, void* out,
+                        float* lse, void* workspace, size_t workspace_bytes, void* stream_ptr) {
+  int st = check_shape(num_reqs, total_q, max_seqlen_q, max_seqlen_k, Hq, Hkv, D, block_size);
+  if (st != CSP_OK) return st;
+  if (!(softmax_scale > 0.f) || !std::isfinite(softmax_scale)) return CSP_ERR_INVALID_ARG;
+  if (num_blocks <= 0 || static_cast<int64_t>(num_blocks) * block_size > INT32_MAX)
+    return CSP_ERR_INVALID_ARG;
+  if (total_q == 0 || num_reqs == 0) return CSP_OK;
+  if (!q || !k_cache || !v_cache || !block_table || !cu_seqlens_q || !seqused_k || !out ||
+      !suffix_start)
+    return CSP_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out))
+    return CSP_ERR_INVALID_ARG;
+  if (bt_row_stride < cdiv(max_seqlen_k, block_size)) return CSP_ERR_INVALID_ARG;
+  int sms = 0;
+  if ((st = device_sm_count(&sms)) != CSP_OK) return st;
+  LevelPlan L;
+  if ((st = make_level_plan(num_reqs, total_q, max_seqlen_q, max_seqlen_k, segments, num_segments,
+                            max_suffix_len, Hq, Hkv, D, sms, &L)) != CSP_OK)
+    return st;
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255) != 0 ||
+      workspace_bytes < L.bytes)
+    return CSP_ERR_WORKSPACE;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  int* status = reinterpret_cast<int*>(ws);
+  int* counters = reinterpret_cast<int*>(ws + L.off_counters);
+  __nv_bfloat16* part_o = reinterpret_cast<__nv_bfloat16*>(ws + L.off_part_o);
+  float* part_lse = reinterpret_cast<float*>(ws + L.off_part_lse);
+  const int64_t rows = static_cast<int64_t>(total_q) * Hq;
+  const int group = Hq / Hkv;
+  const float scale_log2 = softmax_scale * 1.4426950408889634f;
+  const LaunchPlan& P = L.suf;
+  const bool merge_after = P.tc;
+  cudaError_t e;
+  // a row no segment of a level holds reads lse = -inf (weight 0) in that level's slots
+  if ((e = csp::launch_fill_f32(part_lse, L.n_prefix * rows, -INFINITY, stream)) != cudaSuccess)
+    return cuda_fail(e);
+  if (P.s_splits > 1 && !merge_after &&
+      (e = cudaMemsetAsync(counters, 0, static_cast<size_t>(total_q) * Hkv * sizeof(int32_t),
+                           stream)) != cudaSuccess)
+    return cuda_fail(e);
+  CUtensorMap tm_q, tm_k, tm_v;
+  const uint64_t row_b = static_cast<uint64_t>(D) * 2;
+  const uint64_t ntok = static_cast<uint64_t>(num_blocks) * block_size;
+  if ((st = make_map_3d(&tm_q, q, D, Hq, total_q, row_b, row_b * Hq, 64, group, 128 / group)) !=
+          CSP_OK ||
+      (st = make_map_3d(&tm_k, k_cache, D, Hkv, ntok, row_b, row_b * Hkv, 64, 1, kPage)) !=
+          CSP_OK ||
+      (st = make_map_kv_pages(&tm_v, v_cache, D, Hkv, ntok)) != CSP_OK)
+    return st;
+  for (int i = 0; i < num_segments; ++i) {
+    const int32_t* s = segments + static_cast<int64_t>(i) * kSegInts;
+    const int tokens = s[6] - s[5];
+    if (tokens == 0) continue;  // its requests have no query rows this step
+    const int splits = segment_splits(s);
+    const int tiles = cdiv(s[4] - s[3], 64);
+    csp::PrefixArgs pa;
+    pa.k = static_cast<const __nv_bfloat16*>(k_cache);
+    pa.v = static_cast<const __nv_bfloat16*>(v_cache);
+    pa.block_table = block_table + static_cast<int64_t>(s[1]) * bt_row_stride;
+    pa.total_q = tokens;
+    pa.num_q_heads = Hq;
+    pa.num_kv_heads = Hkv;
+    pa.group = group;
+    pa.cpl = s[4];
+    pa.pairs = cdiv(tokens * group, 256);
+    pa.n_splits = splits;
+    pa.tiles_per_split = cdiv(tiles, splits);
+    pa.scale_log2 = scale_log2;
+    pa.part_o = part_o;
+    pa.part_lse = part_lse;
+    pa.lse_stride = rows;
+    pa.status = status;
+    pa.key_lo = s[3];
+    pa.tok0 = s[5];
+    pa.slot_base = L.level_base[s[0]];
+    pa.rows_all = rows;
+    if ((e = csp::launch_prefix(D, tm_q, tm_k, tm_v, pa, stream)) != cudaSuccess)
+      return cuda_fail(e);
+  }
+  csp::PagedArgs ga;
+  ga.q = static_cast<const __nv_bfloat16*>(q);
+  ga.k = static_cast<const __nv_bfloat16*>(k_cache);
+  ga.v = static_cast<const __nv_bfloat16*>(v_cache);
+  ga.block_table = block_table;
+  ga.bt_stride = bt_row_stride;
+  ga.cu_seqlens_q = cu_seqlens_q;
+  ga.seq_lens = seqused_k;
+  ga.num_reqs = num_reqs;
+  ga.total_q = total_q;
+  ga.num_q_heads = Hq;
+  ga.num_kv_heads = Hkv;
+  ga.group = group;
+  ga.key_start = 0;
+  ga.key_start_of = suffix_start;
+  ga.split_keys = P.s_split_keys;
+  ga.n_splits = P.s_splits;
+  ga.row_tiles = P.s_row_tiles;
+  ga.scale_log2 = scale_log2;
+  ga.part_o = part_o;
+  ga.part_lse = part_lse;
+  ga.n_prefix = L.n_prefix;
+  ga.counters = merge_after ? nullptr : counters;
+  ga.out = static_cast<__nv_bfloat16*>(out);
+  ga.lse = lse;
+  ga.status = status;
+  if (P.tc) {
+    e = csp::launch_paged_tc(D, tm_q, tm_k, tm_v, ga, false, stream);
+  } else {
+    e = csp::launch_paged(D, ga, false, stream);
+  }
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (merge_after &&
+      (e = csp::launch_merge_slots(D, part_o, part_lse, L.n_parts, rows,
+                                   static_cast<__nv_bfloat16*>(out), lse, stream)) != cudaSuccess)
+    return cuda_fail(e);
+  return CSP_OK;
 }
 
 int csp_apply_sinks(void* out, float* lse, const float* sinks, int32_t num_tokens,

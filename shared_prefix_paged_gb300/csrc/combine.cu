@@ -8,6 +8,8 @@
 // stores, fp32 math.  (Inside cascade_attn the same merge runs in the attention
 // kernels themselves, see merge.cuh, or, after a tcgen05 suffix phase, in
 // merge_slots_kernel below.)
+#include <algorithm>
+
 #include "common.cuh"
 #include "kernels.cuh"
 #include "merge.cuh"
@@ -218,6 +220,28 @@ cudaError_t launch_apply_sinks(__nv_bfloat16* out, float* lse, const float* sink
   const int64_t grid = (threads + 255) / 256;
   apply_sinks_kernel<<<static_cast<unsigned>(grid), 256, 0, stream>>>(out, lse, sinks, rows,
                                                                      heads, head_dim);
+  return cudaGetLastError();
+}
+
+}  // namespace csp
+
+namespace csp {
+namespace {
+
+// n floats at p set to v (the level slots' LSEs of a multi-level cascade start at -inf:
+// a row that no segment of a level holds then has weight 0 in that level's slots).
+__global__ void __launch_bounds__(256) fill_f32_kernel(float* __restrict__ p, int64_t n, float v) {
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += stride)
+    p[i] = v;
+}
+
+}  // namespace
+
+cudaError_t launch_fill_f32(float* p, int64_t n, float v, cudaStream_t stream) {
+  if (n <= 0) return cudaSuccess;
+  const int64_t blocks = std::min<int64_t>((n + 255) / 256, 4096);
+  fill_f32_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(p, n, v);
   return cudaGetLastError();
 }
 

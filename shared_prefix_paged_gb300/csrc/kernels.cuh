@@ -32,6 +32,15 @@ struct PrefixArgs {
   float* part_lse;       // [n_parts][lse_stride], log2 domain (row t * num_q_heads + h)
   int64_t lse_stride;    // floats per LSE slot, >= total_q * num_q_heads
   int* status;           // workspace status word
+  // A segment of a multi-level cascade (cascade_attn_levels): the rows are the query
+  // tokens [tok0, tok0 + total_q) of the batch (block_table then points at the row of
+  // the segment's first request), the keys [key_lo, cpl), and range s writes slot
+  // slot_base + s of slots that hold rows_all rows each.  The defaults are the prefix
+  // phase of a two-level cascade.
+  int key_lo = 0;
+  int tok0 = 0;
+  int slot_base = 0;
+  int64_t rows_all = 0;  // 0: total_q * num_q_heads
 };
 
 // Paged attention over a key range of each request (the suffix phase with
@@ -62,6 +71,8 @@ struct PagedArgs {
   __nv_bfloat16* out;    // final output: direct mode (part_o == nullptr) or last contributor
   float* lse;            // natural-log LSE or nullptr
   int* status;           // workspace status word (bounded waits of the tcgen05 variant)
+  const int32_t* key_start_of = nullptr;  // per request (device), in place of key_start
+                                          // (the suffixes of a multi-level cascade)
 };
 
 // Single-kernel cascade step for decode-like batches (decode_cascade.cu): at most 16
@@ -146,6 +157,9 @@ cudaError_t launch_merge_states(__nv_bfloat16* out, float* out_lse, const void* 
 cudaError_t launch_plan_device(const int32_t* block_table, int64_t bt_row_stride, int num_reqs,
                                const int32_t* seq_lens, const int32_t* computed, int block_size,
                                int mode, int32_t* plan, cudaStream_t stream);
+
+// n floats at p set to v.
+cudaError_t launch_fill_f32(float* p, int64_t n, float v, cudaStream_t stream);
 
 // Attention sinks applied to a finished result (rows = tokens x heads, natural-log
 // lse updated in place); head_dim / 8 divides 32.

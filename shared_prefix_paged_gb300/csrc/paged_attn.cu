@@ -86,7 +86,8 @@ __global__ void __launch_bounds__(kThreads)
 
   // key range of this split, clipped by the causal limit of the tile's last row
   const int last_query = (row0 + rows_here - 1) / a.group;
-  const int kbeg = a.key_start + split * a.split_keys;
+  const int kbeg =
+      (a.key_start_of != nullptr ? __ldg(a.key_start_of + r) : a.key_start) + split * a.split_keys;
   int kend = min(kbeg + a.split_keys, seq);
   kend = min(kend, seq - q_len + last_query + 1);
   const int n_tiles = kend > kbeg ? (kend - kbeg + kTileKeys - 1) / kTileKeys : 0;

@@ -59,7 +59,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   // keys of this split, clipped by the causal limit of the CTA's last row
   const int last_query = (prow0 + rows_here - 1) >> gshift;
-  const int kbeg = a.key_start + split * a.split_keys;
+  const int kbeg =
+      (a.key_start_of != nullptr ? __ldg(a.key_start_of + r) : a.key_start) + split * a.split_keys;
   int kend = min(kbeg + a.split_keys, seq);
   kend = min(kend, seq - q_len + last_query + 1);
   const int ntiles = kend > kbeg ? (kend - kbeg + prefix::kKeysN - 1) / prefix::kKeysN : 0;

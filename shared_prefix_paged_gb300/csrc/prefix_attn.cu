@@ -31,7 +31,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int split = blockIdx.x % a.n_splits;
   const int pair = (blockIdx.x / a.n_splits) % a.pairs;
   const int kvh = blockIdx.x / (a.n_splits * a.pairs);
-  const int key_tiles = (a.cpl + prefix::kKeysN - 1) / prefix::kKeysN;
+  const int key_tiles = (a.cpl - a.key_lo + prefix::kKeysN - 1) / prefix::kKeysN;
   const int t_first = min(split * a.tiles_per_split, key_tiles);
   const int t_last = min(t_first + a.tiles_per_split, key_tiles);
   prefix::prefix_range<D>(&tm_q, &tm_k, &tm_v, a, prefix::prefix_geom(a, pair), kvh, split,

@@ -86,9 +86,9 @@ struct RangeGeom {
 __device__ __forceinline__ RangeGeom prefix_geom(const PrefixArgs& a, int pair) {
   RangeGeom g;
   g.bt = a.block_table;
-  g.key0 = 0;
+  g.key0 = a.key_lo;
   g.key_end = a.cpl;
-  g.tok0 = 0;
+  g.tok0 = a.tok0;
   g.prow0 = pair * 256;
   g.rows_total = a.total_q * a.group;
   g.causal_base = 0;
@@ -475,14 +475,17 @@ __device__ __forceinline__ void prefix_range(const CUtensorMap* tm_q_p,
       const int r = it / kChunks;
       const int c = it % kChunks;
       const int packed = geo.prow0 + r;
-      const int t = packed >> gshift;
-      if (t >= a.total_q) continue;
+      if ((packed >> gshift) >= a.total_q) continue;
+      const int t = a.tok0 + (packed >> gshift);
       const int64_t row = static_cast<int64_t>(t) * a.num_q_heads + kvh * a.group +
                           (packed & (a.group - 1));
-      const int64_t prow = static_cast<int64_t>(split) * a.total_q * a.num_q_heads + row;
+      const int64_t rows_all =
+          a.rows_all > 0 ? a.rows_all : static_cast<int64_t>(a.total_q) * a.num_q_heads;
+      const int64_t slot = a.slot_base + split;
+      const int64_t prow = slot * rows_all + row;
       *reinterpret_cast<uint4*>(a.part_o + prow * D + c * 8) =
           *reinterpret_cast<const uint4*>(stage + r * L::kStageRow + c * 8);
-      if (c == 0) a.part_lse[split * a.lse_stride + row] = s_lse[r];
+      if (c == 0) a.part_lse[slot * a.lse_stride + row] = s_lse[r];
     }
   }
 }
