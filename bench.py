@@ -68,6 +68,9 @@ def parse_args(argv=None):
                     help="device timing only (no e2e, flat comparison or CPU baseline)")
     ap.add_argument("--sweep", action="store_true",
                     help="N x P decode sweep: cascade vs flat at every point, one line each")
+    ap.add_argument("--levels", action="store_true",
+                    help="tree-shaped decode batches: flat vs two-level vs multi-level "
+                         "cascade, one line each")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     return ap.parse_args(argv)
 
@@ -264,6 +267,20 @@ class DeviceRun:
         self.merge_after = (self.use_cascade and not self.single and self.cpl > 0 and
                             self.suffix_kernel == "paged_tc_kernel")
 
+    def setup_levels(self, max_levels: int):
+        """The multi-level plan of the batch and its workspace."""
+        import torch
+        from shared_prefix_paged_gb300 import csp
+        b = self.b
+        self.segs, self.start = csp.cascade_plan_levels(
+            b.block_table, b.seq_lens, b.num_computed_tokens, block_size=b.block_size,
+            max_levels=max_levels)
+        self.start_dev = torch.from_numpy(self.start).to(self.dev)
+        self.max_suffix = int((b.seq_lens - self.start).max())
+        self.ws_levels = csp.alloc_workspace(csp.workspace_size_levels(
+            b.num_reqs, b.total_q, b.max_seqlen_q, b.max_seqlen_k, self.segs, self.max_suffix,
+            b.num_q_heads, b.num_kv_heads, b.head_dim), self.dev)
+
     def plan(self):
         st = self._plan_fn(*self._plan_args)
         if st != 0:
@@ -274,7 +291,12 @@ class DeviceRun:
         b = self.b
         common = dict(max_seqlen_q=b.max_seqlen_q, max_seqlen_k=b.max_seqlen_k,
                       softmax_scale=b.scale, out=self.out[i], lse=self.lse[i], workspace=self.ws)
-        if path == "cascade":
+        if path == "levels":
+            csp.cascade_attn_levels(self.q[i], self.k[i], self.v[i], self.bt, self.cu, self.sl,
+                                    segments=self.segs, suffix_start=self.start_dev,
+                                    max_suffix_len=self.max_suffix,
+                                    **dict(common, workspace=self.ws_levels))
+        elif path == "cascade":
             csp.cascade_attn(self.q[i], self.k[i], self.v[i], self.bt, self.cu, self.sl,
                              common_prefix_len=self.cpl, phase_events=events, **common)
         else:
@@ -736,6 +758,44 @@ def run_sweep(args, dist: Dist):
             torch.cuda.empty_cache()
 
 
+def run_levels(args, dist: Dist):
+    """Flat, two-level and multi-level cascade on tree-shaped decode batches (families of
+    requests over one system prompt, each family over its own document)."""
+    import torch
+    from shared_prefix_paged_gb300 import accounting, csp, workloads
+    torch.cuda.set_device(dist.local_rank)
+    device = torch.device("cuda", dist.local_rank)
+    peaks = load_peaks()
+    for fam, per, system, doc in ((8, 16, 2048, 4096), (4, 16, 1024, 8192),
+                                  (16, 8, 4096, 2048)):
+        b = workloads.tree_families(families=fam, per_family=per, system=system, doc=doc)
+        R = args.copies or default_copies(b)
+        run = DeviceRun(b, R, device)
+        run.setup_levels(max_levels=3)
+        steps = max(R, min(args.steps, 2000))
+        t = {}
+        for path in ("flat", "cascade", "levels"):
+            e, _, _, _ = time_graph_steps(run, path, steps, args.warmup, dist, False)
+            t[path] = e / steps * 1e6
+        lv = accounting.levels_min_bytes(b, run.segs, run.start)
+        line = {"levels": True, "workload": b.name, "num_reqs": b.num_reqs,
+                "segments": int(run.segs.shape[0]), "cpl": run.cpl,
+                "flat_us": round(t["flat"], 3), "cascade_us": round(t["cascade"], 3),
+                "levels_us": round(t["levels"], 3),
+                "levels_vs_cascade": round(t["cascade"] / t["levels"], 3),
+                "levels_vs_flat": round(t["flat"] / t["levels"], 3),
+                "kv_tokens": {"flat": accounting.flat_kv_tokens(b.seq_lens),
+                              "cascade": accounting.cascade_kv_tokens(b.seq_lens, run.cpl),
+                              "levels": accounting.levels_kv_tokens(b.seq_lens, run.segs,
+                                                                    run.start)},
+                "levels_hbm_frac": round(lv / (t["levels"] * 1e-6) / 1e9 / peaks["hbm_gbs"], 3),
+                "peak_source": peaks["source"]}
+        if dist.rank == 0:
+            print(json.dumps(line), flush=True)
+        del run
+        torch.cuda.empty_cache()
+
+
 def main(argv=None):
     args = parse_args(argv)
     if args.impl == "reference":
@@ -749,6 +809,9 @@ def main(argv=None):
     try:
         if args.sweep:
             run_sweep(args, dist)
+            return 0
+        if args.levels:
+            run_levels(args, dist)
             return 0
         res = run_ours(args, dist)
         if dist.rank == 0:

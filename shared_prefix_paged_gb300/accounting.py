@@ -47,3 +47,21 @@ def flat_min_bytes(batch) -> int:
     kv = flat_kv_tokens(batch.seq_lens) * kv_bytes_per_token(batch.num_kv_heads, batch.head_dim)
     rows = batch.total_q * batch.num_q_heads
     return kv + rows * batch.head_dim * 2 * 2 + rows * 4
+
+
+def levels_kv_tokens(seq_lens, segments, suffix_start) -> int:
+    """Multi-level cascade (§七, num_levels): each segment's shared keys once, then each
+    request's KV after its deepest segment.  segments: rows (level, r_lo, r_hi, k_lo,
+    k_hi, ...)."""
+    s = np.asarray(seq_lens, dtype=np.int64)
+    st = np.asarray(suffix_start, dtype=np.int64)
+    shared = sum(int(g[4]) - int(g[3]) for g in segments)
+    return shared + int((s - st).sum())
+
+
+def levels_min_bytes(batch, segments, suffix_start) -> int:
+    """Minimal HBM bytes of one multi-level call: KV once, q read, out + lse written."""
+    kv = levels_kv_tokens(batch.seq_lens, segments, suffix_start) * kv_bytes_per_token(
+        batch.num_kv_heads, batch.head_dim)
+    rows = batch.total_q * batch.num_q_heads
+    return kv + rows * batch.head_dim * 2 * 2 + rows * 4

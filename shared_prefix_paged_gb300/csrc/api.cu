@@ -341,16 +341,11 @@ struct LevelPlan {
   int level_splits[kMaxLevels] = {};
   int level_base[kMaxLevels] = {};
   int n_prefix = 0;
-  LaunchPlan suf;  // the suffix (paged) part
+  std::vector<int> seg_splits;  // key ranges of each segment
+  LaunchPlan suf;               // the suffix (paged) part
   int n_parts = 0;
   size_t off_counters = 0, off_part_o = 0, off_part_lse = 0, bytes = 0;
 };
-
-// Key ranges per segment: one per 16 key tiles (1024 keys), at most 8.
-int segment_splits(const int32_t* seg) {
-  const int tiles = cdiv(seg[4] - seg[3], 64);
-  return std::max(1, std::min(8, tiles / 16));
-}
 
 // Host checks of a segment list: fields in range, and two segments that hold a request
 // in common of different levels, the shallower one holding all of the deeper one's
@@ -386,9 +381,49 @@ int make_level_plan(int num_reqs, int total_q, int max_q, int max_k, const int32
   int st = check_segments(num_reqs, total_q, max_k, segs, n_seg);
   if (st != CSP_OK) return st;
   if (max_suffix_len < 0 || max_suffix_len > max_k) return CSP_ERR_INVALID_ARG;
+  // the suffix: as the two-kernel schedule's suffix kernel for suffixes of at most
+  // max_suffix_len keys (its split count is settled below, once the prefix slots are)
+  make_plan(num_reqs, total_q, max_q, max_k, max_k - max_suffix_len, Hq, Hkv, D, sms, &L.suf,
+            CSP_SCHEDULE_TWO_KERNELS);
+  // Key ranges per segment.  All segments run in one grid (one CTA per SM), next to the
+  // suffix kernel on the SMs they leave free, so the call takes about max(the longest
+  // CTA, (prefix + suffix SM time) / SMs); a CTA costs its tiles plus ~3 tiles of fixed
+  // cost at ~1.22 us each (the prefix kernel's cost model), the suffix its bytes at
+  // ~32 GB/s per SM.  Every segment aims at the same number of tiles per range (at
+  // most 8 ranges); the levels' largest range counts add up to at most 24 slots; on a
+  // tie the fewer ranges win.
+  const int group = Hq / Hkv;
+  const double tile_us = 1.22;
+  const double suf_sm_us =
+      static_cast<double>(num_reqs) * Hkv * (0.5 * max_suffix_len + 64.0) * 4.0 * D / 32e3;
+  L.seg_splits.assign(n_seg, 1);
+  double best = -1.0;
+  for (int tp = 1 << 20; tp >= 2; tp = tp > 256 ? 256 : tp / 2) {
+    std::vector<int> sp(n_seg, 1);
+    int lvl[kMaxLevels] = {};
+    double work = suf_sm_us, longest = 0.0;
+    for (int i = 0; i < n_seg; ++i) {
+      const int32_t* s = segs + static_cast<int64_t>(i) * kSegInts;
+      const int tiles = cdiv(s[4] - s[3], 64);
+      sp[i] = std::max(1, std::min(8, cdiv(tiles, tp)));
+      lvl[s[0]] = std::max(lvl[s[0]], sp[i]);
+      const int ctas = Hkv * cdiv((s[6] - s[5]) * group, 256) * sp[i];
+      const double cta_us = (cdiv(tiles, sp[i]) + 3) * tile_us;
+      work += ctas * cta_us;
+      if (ctas > 0) longest = std::max(longest, cta_us);
+    }
+    int slots = 0;
+    for (int d = 0; d < kMaxLevels; ++d) slots += lvl[d];
+    if (slots > 24) continue;
+    const double cost = std::max(longest, work / sms);
+    if (best < 0.0 || cost < best) {
+      best = cost;
+      L.seg_splits = sp;
+    }
+  }
   for (int i = 0; i < n_seg; ++i) {
     const int32_t* s = segs + static_cast<int64_t>(i) * kSegInts;
-    L.level_splits[s[0]] = std::max(L.level_splits[s[0]], segment_splits(s));
+    L.level_splits[s[0]] = std::max(L.level_splits[s[0]], L.seg_splits[i]);
     L.n_levels = std::max(L.n_levels, s[0] + 1);
   }
   for (int d = 0; d < L.n_levels; ++d) {
@@ -396,10 +431,7 @@ int make_level_plan(int num_reqs, int total_q, int max_q, int max_k, const int32
     L.n_prefix += L.level_splits[d];
   }
   if (L.n_prefix > 24) return CSP_ERR_UNSUPPORTED;
-  // the suffix: as the two-kernel schedule's suffix kernel for suffixes of at most
-  // max_suffix_len keys, with at most 32 partials per row in all
-  make_plan(num_reqs, total_q, max_q, max_k, max_k - max_suffix_len, Hq, Hkv, D, sms, &L.suf,
-            CSP_SCHEDULE_TWO_KERNELS);
+  // at most 32 partials per row in all
   const int max_len = std::max(1, max_suffix_len);
   int split_keys = L.suf.s_split_keys;
   if (cdiv(max_len, split_keys) > 32 - L.n_prefix)
@@ -1063,35 +1095,51 @@ int cascade_attn_levels(const void* q, const void* k_cache, const void* v_cache,
           CSP_OK ||
       (st = make_map_kv_pages(&tm_v, v_cache, D, Hkv, ntok)) != CSP_OK)
     return st;
-  for (int i = 0; i < num_segments; ++i) {
+  // every segment with query rows in one grid (a table of at most
+  // kMaxSegmentsPerLaunch segments per launch)
+  csp::PrefixArgs pa;
+  pa.k = static_cast<const __nv_bfloat16*>(k_cache);
+  pa.v = static_cast<const __nv_bfloat16*>(v_cache);
+  pa.block_table = block_table;
+  pa.num_q_heads = Hq;
+  pa.num_kv_heads = Hkv;
+  pa.group = group;
+  pa.scale_log2 = scale_log2;
+  pa.part_o = part_o;
+  pa.part_lse = part_lse;
+  pa.lse_stride = rows;
+  pa.rows_all = rows;
+  pa.status = status;
+  csp::SegmentTable table;
+  table.n = 0;
+  table.bt_stride = bt_row_stride;
+  int grid = 0;
+  bool launched = false;
+  for (int i = 0; i <= num_segments; ++i) {
+    if ((i == num_segments || table.n == csp::kMaxSegmentsPerLaunch) && table.n > 0) {
+      if ((e = csp::launch_prefix_segments(D, tm_q, tm_k, tm_v, pa, table, grid, stream)) !=
+          cudaSuccess)
+        return cuda_fail(e);
+      launched = true;
+      table.n = 0;
+      grid = 0;
+    }
+    if (i == num_segments) break;
     const int32_t* s = segments + static_cast<int64_t>(i) * kSegInts;
     const int tokens = s[6] - s[5];
     if (tokens == 0) continue;  // its requests have no query rows this step
-    const int splits = segment_splits(s);
-    const int tiles = cdiv(s[4] - s[3], 64);
-    csp::PrefixArgs pa;
-    pa.k = static_cast<const __nv_bfloat16*>(k_cache);
-    pa.v = static_cast<const __nv_bfloat16*>(v_cache);
-    pa.block_table = block_table + static_cast<int64_t>(s[1]) * bt_row_stride;
-    pa.total_q = tokens;
-    pa.num_q_heads = Hq;
-    pa.num_kv_heads = Hkv;
-    pa.group = group;
-    pa.cpl = s[4];
-    pa.pairs = cdiv(tokens * group, 256);
-    pa.n_splits = splits;
-    pa.tiles_per_split = cdiv(tiles, splits);
-    pa.scale_log2 = scale_log2;
-    pa.part_o = part_o;
-    pa.part_lse = part_lse;
-    pa.lse_stride = rows;
-    pa.status = status;
-    pa.key_lo = s[3];
-    pa.tok0 = s[5];
-    pa.slot_base = L.level_base[s[0]];
-    pa.rows_all = rows;
-    if ((e = csp::launch_prefix(D, tm_q, tm_k, tm_v, pa, stream)) != cudaSuccess)
-      return cuda_fail(e);
+    csp::SegmentDesc& sd = table.s[table.n++];
+    sd.cta0 = grid;
+    sd.bt_row = s[1];
+    sd.key_lo = s[3];
+    sd.key_hi = s[4];
+    sd.tok0 = s[5];
+    sd.tokens = tokens;
+    sd.slot_base = L.level_base[s[0]];
+    sd.splits = L.seg_splits[i];
+    sd.tiles_per_split = cdiv(cdiv(s[4] - s[3], 64), sd.splits);
+    sd.pairs = cdiv(tokens * group, 256);
+    grid += Hkv * sd.pairs * sd.splits;
   }
   csp::PagedArgs ga;
   ga.q = static_cast<const __nv_bfloat16*>(q);
@@ -1119,12 +1167,16 @@ int cascade_attn_levels(const void* q, const void* k_cache, const void* v_cache,
   ga.out = static_cast<__nv_bfloat16*>(out);
   ga.lse = lse;
   ga.status = status;
+  // concurrent with the last prefix grid (programmatic dependent launch: the suffix
+  // waits for it before it reads the prefix slots; earlier prefix grids, launched
+  // plainly, finished before it started)
   if (P.tc) {
-    e = csp::launch_paged_tc(D, tm_q, tm_k, tm_v, ga, false, stream);
+    e = csp::launch_paged_tc(D, tm_q, tm_k, tm_v, ga, launched, stream);
   } else {
-    e = csp::launch_paged(D, ga, false, stream);
+    e = csp::launch_paged(D, ga, launched, stream);
   }
   if (e != cudaSuccess) return cuda_fail(e);
+  // in stream order (no programmatic launch): every slot is complete
   if (merge_after &&
       (e = csp::launch_merge_slots(D, part_o, part_lse, L.n_parts, rows,
                                    static_cast<__nv_bfloat16*>(out), lse, stream)) != cudaSuccess)

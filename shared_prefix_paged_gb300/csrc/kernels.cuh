@@ -43,6 +43,26 @@ struct PrefixArgs {
   int64_t rows_all = 0;  // 0: total_q * num_q_heads
 };
 
+// The segments of a multi-level cascade in one grid (prefix_attn.cu): segment i owns
+// CTAs [cta0, cta0 + Hkv * pairs * splits) and runs the prefix body over its query
+// rows [tok0, tok0 + tokens) and keys [key_lo, key_hi) of block-table row bt_row,
+// writing slots slot_base .. slot_base + splits - 1.  Passed by value (kernel
+// parameter space), at most kMaxSegmentsPerLaunch segments.
+constexpr int kMaxSegmentsPerLaunch = 48;
+struct SegmentDesc {
+  int cta0;
+  int bt_row;
+  int key_lo, key_hi;
+  int tok0, tokens;
+  int slot_base;
+  int splits, tiles_per_split, pairs;
+};
+struct SegmentTable {
+  int n;
+  int64_t bt_stride;
+  SegmentDesc s[kMaxSegmentsPerLaunch];
+};
+
 // Paged attention over a key range of each request (the suffix phase with
 // key_start = cpl, §八 Step 5 Phase 2; the standard path with key_start = 0, §五).
 struct PagedArgs {
@@ -126,6 +146,13 @@ cudaError_t launch_decode(int head_dim, const CUtensorMap& tm_q, const CUtensorM
 
 cudaError_t launch_prefix(int head_dim, const CUtensorMap& tm_q, const CUtensorMap& tm_k,
                           const CUtensorMap& tm_v, const PrefixArgs& a, cudaStream_t stream);
+
+// base: the fields every segment shares (caches, block_table row 0, heads, scale,
+// slots and their strides, status); grid = the table's CTAs in all.
+cudaError_t launch_prefix_segments(int head_dim, const CUtensorMap& tm_q,
+                                   const CUtensorMap& tm_k, const CUtensorMap& tm_v,
+                                   const PrefixArgs& base, const SegmentTable& t, int grid,
+                                   cudaStream_t stream);
 
 // after_prefix: launched right behind this call's prefix kernel on the same stream
 // (programmatic dependent launch, so it runs concurrently with it).

@@ -280,6 +280,21 @@ def tree_decode(seed: int = 1005, head_dim: int = 128, chunked: bool = False) ->
                             head_dim=head_dim, gen=g)
 
 
+def tree_families(seed: int = 1011, families: int = 8, per_family: int = 16,
+                  system: int = 2048, doc: int = 4096, s: int = 128) -> Batch:
+    """Families of decode requests over one system prompt: ``families`` groups of
+    ``per_family`` requests, each group over its own ``doc``-token document after the
+    ``system``-token prompt, each request with ``s`` private tokens (the last one the
+    query).  Hq 32, Hkv 8, D 128.  Default: 128 requests, 2048 + 4096 + 128 tokens."""
+    g = _gen(seed)
+    chunks = [system] + [doc] * families
+    paths = [(0, 1 + f) for f in range(families) for _ in range(per_family)]
+    n = families * per_family
+    return build_tree_batch(f"tree_F{families}x{per_family}_sys{system}_doc{doc}_S{s}",
+                            chunks, paths, [s] * n, [1] * n, num_q_heads=32, num_kv_heads=8,
+                            head_dim=128, gen=g)
+
+
 def by_name(name: str) -> Batch:
     """The named batch shapes used by the tests and the benchmark."""
     table = {
@@ -290,5 +305,6 @@ def by_name(name: str) -> Batch:
         "long": long_prefix,
         "tree": tree_decode,
         "tree_chunked": lambda: tree_decode(seed=1006, chunked=True),
+        "families": tree_families,
     }
     return table[name]()

@@ -116,3 +116,15 @@ def test_segment_without_query_rows():
     out, lse, segs = run_levels(b, dev, 3)
     assert any(s[5] == s[6] for s in segs.tolist())
     H.compare(out, lse, ref_o, ref_l, what="segment without rows")
+
+
+@pytest.mark.parametrize("shape", [(8, 16, 2048, 4096), (4, 16, 1024, 8192), (16, 8, 4096, 2048)])
+def test_family_batches_the_benchmark_times(shape):
+    fam, per, system, doc = shape
+    b = workloads.tree_families(families=fam, per_family=per, system=system, doc=doc)
+    dev = H.to_device(b)
+    rows = H.sample_rows(b, 500, seed=1012)
+    ref_o, ref_l = H.oracle_ref(b, rows)
+    out, lse, segs = run_levels(b, dev, 3)
+    assert segs.shape[0] == 1 + fam
+    H.compare(out, lse, ref_o, ref_l, rows=rows, what=f"families {shape}")
