@@ -174,7 +174,7 @@ CSP_API int csp_workspace_size(int32_t num_reqs, int32_t total_q, int32_t max_se
                        int32_t num_kv_heads, int32_t head_dim, size_t* bytes_out);
 
 /* csp_cascade_schedule results. */
-enum { CSP_SCHEDULE_TWO_KERNELS = 0, CSP_SCHEDULE_SINGLE = 1 };
+enum { CSP_SCHEDULE_TWO_KERNELS = 0, CSP_SCHEDULE_SINGLE = 1, CSP_SCHEDULE_FUSED = 2 };
 
 /*
  * csp_cascade_schedule — which kernels cascade_attn launches for a batch of this
@@ -189,7 +189,12 @@ enum { CSP_SCHEDULE_TWO_KERNELS = 0, CSP_SCHEDULE_SINGLE = 1 };
  *                              where every request has at most 16 / (num_q_heads /
  *                              num_kv_heads) query tokens: some CTAs run ranges of the
  *                              prefix phase while the others stream the suffix
- *                              phase, then every CTA merges a share of the rows.
+ *                              phase, then every CTA merges a share of the rows;
+ *   CSP_SCHEDULE_FUSED       : one launch of one CTA per SM for any batch: the prefix
+ *                              phase's CTAs first, then suffix CTAs on tcgen05 (up to
+ *                              256 query rows of one request and KV head each); every
+ *                              CTA counts itself in the row groups it covered and a
+ *                              group's last contributor merges its rows.
  * Writes *schedule_out and, when prefix_splits_out is not NULL, the number of key
  * ranges the prefix phase is cut into (one workspace slot each).  Returns CSP_OK,
  * CSP_ERR_INVALID_ARG, CSP_ERR_UNSUPPORTED or CSP_ERR_CUDA.
@@ -236,9 +241,10 @@ CSP_API int cascade_attn(const void* q, const void* k_cache, const void* v_cache
 /*
  * cascade_attn_scheduled — cascade_attn with the schedule given by the caller instead
  * of the cost model's (for tests and tuning; results are the same up to rounding):
- *   schedule       CSP_SCHEDULE_TWO_KERNELS, or CSP_SCHEDULE_SINGLE where that kernel
- *                  can run (a request's rows of one KV head fit 16 and the prefix's
- *                  256-row blocks x KV heads fit the SMs; else CSP_ERR_UNSUPPORTED)
+ *   schedule       CSP_SCHEDULE_TWO_KERNELS, CSP_SCHEDULE_FUSED, or
+ *                  CSP_SCHEDULE_SINGLE where that kernel can run (a request's rows of
+ *                  one KV head fit 16 and the prefix's 256-row blocks x KV heads fit
+ *                  the SMs; else CSP_ERR_UNSUPPORTED)
  *   prefix_ranges  > 0: the single kernel's number of prefix key ranges (capped at 15,
  *                  the prefix's 64-key tiles and the SMs' room); 0: the cost model's
  * common_prefix_len must be > 0.  Other arguments, the workspace (csp_workspace_size

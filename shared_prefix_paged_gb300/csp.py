@@ -25,7 +25,7 @@ CSP_ERR_CUDA = -4
 CSP_ERR_TIMEOUT = -6
 
 MODE_AUTO, MODE_FORCE_CASCADE, MODE_FORCE_FLAT, MODE_PAGE_THRESHOLDS = 0, 1, 2, 3
-SCHEDULE_TWO_KERNELS, SCHEDULE_SINGLE = 0, 1
+SCHEDULE_TWO_KERNELS, SCHEDULE_SINGLE, SCHEDULE_FUSED = 0, 1, 2
 DTYPE_BF16, DTYPE_F32 = 0, 1
 
 # every symbol include/csp.h declares
@@ -219,7 +219,7 @@ def workspace_size(num_reqs, total_q, max_seqlen_q, max_seqlen_k, common_prefix_
 def cascade_schedule(num_reqs, total_q, max_seqlen_q, max_seqlen_k, common_prefix_len,
                      num_q_heads, num_kv_heads, head_dim):
     """(schedule, prefix key ranges) that cascade_attn uses for this batch shape on the
-    current device: SCHEDULE_TWO_KERNELS or SCHEDULE_SINGLE."""
+    current device: SCHEDULE_TWO_KERNELS, SCHEDULE_SINGLE or SCHEDULE_FUSED."""
     lib = load()
     sched = ctypes.c_int32(0)
     splits = ctypes.c_int32(0)
@@ -309,9 +309,9 @@ def cascade_attn(q, k_cache, v_cache, block_table, cu_seqlens_q, seqused_k, *, m
     here when None); one that is too small raises (CSP_ERR_WORKSPACE).
     phase_events: optional four torch.cuda.Event(enable_timing=True); when given, the
     call goes through cascade_attn_timed and records them between the kernels.
-    schedule: SCHEDULE_TWO_KERNELS or SCHEDULE_SINGLE to override the cost model
-    (cascade_attn_scheduled), with prefix_ranges > 0 fixing the single kernel's number
-    of prefix key ranges.
+    schedule: SCHEDULE_TWO_KERNELS, SCHEDULE_SINGLE or SCHEDULE_FUSED to override the
+    cost model (cascade_attn_scheduled), with prefix_ranges > 0 fixing the single
+    kernel's number of prefix key ranges.
     """
     return _attn("cascade_attn", q, k_cache, v_cache, block_table, cu_seqlens_q, seqused_k,
                  max_seqlen_q=max_seqlen_q, max_seqlen_k=max_seqlen_k,

@@ -26,6 +26,9 @@ constexpr int kPage = 16;
 // Workspace header: [0] status word; the grid barrier of the single-kernel decode
 // schedule: [64] its count (that kernel leaves it at zero) and [128] its generation.
 constexpr size_t kHeaderBytes = 256;
+// Batches with a tcgen05 suffix (more than 16 rows per request and KV head) take the
+// fused schedule unless the caller asks for another.
+constexpr bool kFusedByDefault = false;
 constexpr size_t kOffBarCount = 64;
 constexpr size_t kOffBarGen = 128;
 // Shared memory the decode schedule's merge stages its bf16 rows in.
@@ -154,6 +157,9 @@ struct LaunchPlan {
   bool direct = false;  // paged kernel writes the final output itself
   int n_parts = 0;      // partial results per row group
   size_t off_counters = 0, off_part_o = 0, off_part_lse = 0, bytes = 0;
+  // the fused schedule: prefix ranges and tcgen05 suffix units in one grid
+  // (paged_tc.cu), merged by each row group's last contributor
+  bool fused = false;
   // single-kernel decode schedule (decode_cascade.cu)
   bool single = false;
   int d_splits = 0, d_prefix_ctas = 0, d_prefix_units = 0, d_grid = 0, d_merge_rows = 0;
@@ -169,7 +175,8 @@ void make_plan(int num_reqs, int total_q, int max_q, int max_k, int cpl, int Hq,
   LaunchPlan p;
   p.group = Hq / Hkv;
   p.decode = static_cast<int64_t>(max_q) * p.group <= 16;
-  p.tc = !p.decode;
+  // the fused schedule runs every suffix unit on the tcgen05 body
+  p.tc = !p.decode || (cpl > 0 && sched_override == CSP_SCHEDULE_FUSED);
   const int max_len = std::max(0, max_k - cpl);
   if (cpl > 0) {
     const int rows = total_q * p.group;
@@ -323,6 +330,8 @@ void make_plan(int num_reqs, int total_q, int max_q, int max_k, int cpl, int Hq,
                                     align256(static_cast<size_t>(s_max + 1) * rows_total * D * 2) +
                                     align256(lse_max));
   }
+  p.fused = cpl > 0 && !p.single &&
+            (sched_override == CSP_SCHEDULE_FUSED || (sched_override < 0 && p.tc && kFusedByDefault));
   *P = p;
 }
 
@@ -645,14 +654,16 @@ int attention_call(const void* q, const void* k_cache, const void* v_cache, int3
   // kernel merges every row (the two phases never wait for each other); otherwise the
   // suffix kernel merges, and several suffix splits count themselves in row-group
   // counters that start at zero in every call, whatever the workspace held.
-  const bool merge_after = P.tc && cpl > 0;
-  if (P.n_parts > 0 && P.s_splits > 1 && !merge_after &&
+  // The fused schedule counts prefix ranges and suffix splits in the same counters.
+  const bool merge_after = P.tc && cpl > 0 && !P.fused;
+  if (P.n_parts > 0 && (P.s_splits > 1 || P.fused) && !merge_after &&
       (e = cudaMemsetAsync(counters, 0, static_cast<size_t>(total_q) * Hkv * sizeof(int32_t),
                            stream)) != cudaSuccess)
     return cuda_fail(e);
 
+  CUtensorMap tm_q, tm_k, tm_v;
+  csp::PrefixArgs pa;
   if (cpl > 0) {
-    CUtensorMap tm_q, tm_k, tm_v;
     const uint64_t row_b = static_cast<uint64_t>(D) * 2;
     if ((st = make_map_3d(&tm_q, q, D, Hq, total_q, row_b, row_b * Hq, 64, P.group,
                           128 / P.group)) != CSP_OK)
@@ -662,7 +673,6 @@ int attention_call(const void* q, const void* k_cache, const void* v_cache, int3
         CSP_OK)
       return st;
     if ((st = make_map_kv_pages(&tm_v, v_cache, D, Hkv, ntok)) != CSP_OK) return st;
-    csp::PrefixArgs pa;
     pa.k = static_cast<const __nv_bfloat16*>(k_cache);
     pa.v = static_cast<const __nv_bfloat16*>(v_cache);
     pa.block_table = block_table;
@@ -679,7 +689,7 @@ int attention_call(const void* q, const void* k_cache, const void* v_cache, int3
     pa.part_lse = part_lse;
     pa.lse_stride = static_cast<int64_t>(total_q) * Hq;
     pa.status = status;
-    if ((e = csp::launch_prefix(D, tm_q, tm_k, tm_v, pa, stream)) != cudaSuccess)
+    if (!P.fused && (e = csp::launch_prefix(D, tm_q, tm_k, tm_v, pa, stream)) != cudaSuccess)
       return cuda_fail(e);
   }
   if ((e = mark(1)) != cudaSuccess) return cuda_fail(e);
@@ -713,7 +723,10 @@ int attention_call(const void* q, const void* k_cache, const void* v_cache, int3
   // concurrent with the prefix kernel (programmatic dependent launch) unless phase
   // events sit between the two
   const bool overlap = cpl > 0 && events == nullptr;
-  if (P.tc) {
+  if (P.fused) {
+    ga.prefix_contributors = P.p_splits;
+    e = csp::launch_cascade_fused(D, tm_q, tm_k, tm_v, pa, ga, stream);
+  } else if (P.tc) {
     CUtensorMap tm_q, tm_k, tm_v;
     const uint64_t row_b = static_cast<uint64_t>(D) * 2;
     const uint64_t ntok = static_cast<uint64_t>(num_blocks) * block_size;
@@ -896,7 +909,8 @@ int cascade_attn_scheduled(const void* q, const void* k_cache, const void* v_cac
                            float softmax_scale, void* out, float* lse, void* workspace,
                            size_t workspace_bytes, void* stream, int32_t schedule,
                            int32_t prefix_ranges) {
-  if (schedule != CSP_SCHEDULE_TWO_KERNELS && schedule != CSP_SCHEDULE_SINGLE)
+  if (schedule != CSP_SCHEDULE_TWO_KERNELS && schedule != CSP_SCHEDULE_SINGLE &&
+      schedule != CSP_SCHEDULE_FUSED)
     return CSP_ERR_INVALID_ARG;
   if (prefix_ranges < 0 || common_prefix_len <= 0) return CSP_ERR_INVALID_ARG;
   return attention_call(q, k_cache, v_cache, num_blocks, block_table, bt_row_stride, cu_seqlens_q,
@@ -1238,7 +1252,8 @@ int csp_cascade_schedule(int32_t num_reqs, int32_t total_q, int32_t max_seqlen_q
   LaunchPlan P;
   make_plan(num_reqs, total_q, max_seqlen_q, max_seqlen_k, common_prefix_len, num_q_heads,
             num_kv_heads, head_dim, sms, &P);
-  *schedule_out = P.single ? CSP_SCHEDULE_SINGLE : CSP_SCHEDULE_TWO_KERNELS;
+  *schedule_out = P.single ? CSP_SCHEDULE_SINGLE
+                           : (P.fused ? CSP_SCHEDULE_FUSED : CSP_SCHEDULE_TWO_KERNELS);
   if (prefix_splits_out) *prefix_splits_out = P.single ? P.d_splits : P.p_splits;
   return CSP_OK;
 }

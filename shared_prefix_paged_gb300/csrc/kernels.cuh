@@ -93,6 +93,8 @@ struct PagedArgs {
   int* status;           // workspace status word (bounded waits of the tcgen05 variant)
   const int32_t* key_start_of = nullptr;  // per request (device), in place of key_start
                                           // (the suffixes of a multi-level cascade)
+  int prefix_contributors = 0;  // prefix ranges counted in the same row-group counters
+                                // (the fused launch)
 };
 
 // Single-kernel cascade step for decode-like batches (decode_cascade.cu): at most 16
@@ -167,6 +169,14 @@ cudaError_t launch_paged(int head_dim, const PagedArgs& a, bool after_prefix,
 cudaError_t launch_paged_tc(int head_dim, const CUtensorMap& tm_q, const CUtensorMap& tm_k,
                             const CUtensorMap& tm_v, const PagedArgs& a, bool after_prefix,
                             cudaStream_t stream);
+
+// The fused cascade step (paged_tc.cu): the prefix grid of `pa` and the tcgen05
+// suffix grid of `ga` in one launch, merged by each row group's last contributor
+// (ga.counters zero at the start, ga.prefix_contributors = pa.n_splits, ga.n_prefix =
+// the prefix slots).  Maps as for launch_paged_tc.
+cudaError_t launch_cascade_fused(int head_dim, const CUtensorMap& tm_q, const CUtensorMap& tm_k,
+                                 const CUtensorMap& tm_v, const PrefixArgs& pa,
+                                 const PagedArgs& ga, cudaStream_t stream);
 
 // merge_attn_states over n_parts slots of every row (rows = total_q * num_q_heads):
 // part_o [n_parts][rows][D] bf16 normalised, part_lse [n_parts][rows] log2 domain ->

@@ -33,21 +33,16 @@ using prefix::kThreads;
 template <int D>
 constexpr int kDynamic = Layout<D>::kData + prefix::kBarBytes + 1024;
 
+// One CTA of the suffix (or standard-path) grid: request row tile bx (request
+// bx / row_tiles), KV head g, key split `split`.
 template <int D>
-__global__ void __launch_bounds__(kThreads, 1)
-    paged_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
-                    const __grid_constant__ CUtensorMap tm_k,
-                    const __grid_constant__ CUtensorMap tm_v, const PagedArgs a) {
+__device__ __forceinline__ void tc_suffix_cta(const CUtensorMap* tm_q, const CUtensorMap* tm_k,
+                                              const CUtensorMap* tm_v, const PagedArgs& a,
+                                              int bx, int g, int split, uint8_t* smem,
+                                              uint64_t* bars) {
   using L = Layout<D>;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kData);
-
-  const int r = blockIdx.x / a.row_tiles;
-  const int rt = blockIdx.x % a.row_tiles;
-  const int g = blockIdx.y;
-  const int split = blockIdx.z;
+  const int r = bx / a.row_tiles;
+  const int rt = bx % a.row_tiles;
   const int q0 = __ldg(a.cu_seqlens_q + r);
   const int q_len = __ldg(a.cu_seqlens_q + r + 1) - q0;
   const int seq = __ldg(a.seq_lens + r);
@@ -91,7 +86,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   geo.prow0 = prow0;
   geo.rows_total = rows_total;
   geo.causal_base = seq - q_len;
-  prefix::prefix_range<D, true>(&tm_q, &tm_k, &tm_v, pa, geo, g, split, 0, ntiles, smem, bars);
+  prefix::prefix_range<D, true>(tm_q, tm_k, tm_v, pa, geo, g, split, 0, ntiles, smem, bars);
 
   // 256 normalised rows (bf16) and their log2-sum-exp are staged and visible
   const __nv_bfloat16* stage = reinterpret_cast<const __nv_bfloat16*>(smem);
@@ -128,7 +123,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   m.part_lse = a.part_lse;
   m.counters = a.counters;
   m.n_parts = a.n_prefix + a.n_splits;
-  m.n_count = a.n_splits;
+  m.n_count = a.n_splits + a.prefix_contributors;
   m.rows = a.total_q * a.num_q_heads;
   m.num_q_heads = a.num_q_heads;
   m.num_kv_heads = a.num_kv_heads;
@@ -143,6 +138,101 @@ __global__ void __launch_bounds__(kThreads, 1)
   count_and_merge_block<D>(m, q0 + tok_first, n_tok, g, rows_here, out_row,
                            [&](int rr) { return ((prow0 + rr) >> gshift) - tok_first; }, s_last,
                            s_w);
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    paged_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
+                    const __grid_constant__ CUtensorMap tm_k,
+                    const __grid_constant__ CUtensorMap tm_v, const PagedArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Layout<D>::kData);
+  tc_suffix_cta<D>(&tm_q, &tm_k, &tm_v, a, blockIdx.x, blockIdx.y, blockIdx.z, smem, bars);
+}
+
+// The whole cascade step in one launch (prefill-shaped batches): CTAs [0, n_pre) are
+// the prefix phase's (KV head, 256-row block, key range) CTAs, the rest the suffix
+// grid's (request row tile, KV head, key split) CTAs in the order the suffix kernel
+// numbers them.  Every CTA writes its partial slot and counts itself in the row
+// groups (token, KV head) it covered, prefix ranges and suffix splits in the same
+// counters; a group's last contributor merges every slot of its rows (merge.cuh).
+// So no phase waits for the other and no kernel follows: the prefix CTAs, numbered
+// first, start first and the suffix fills the SMs they leave free.
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    cascade_fused_kernel(const __grid_constant__ CUtensorMap tm_q,
+                         const __grid_constant__ CUtensorMap tm_k,
+                         const __grid_constant__ CUtensorMap tm_v, const PrefixArgs pa,
+                         const PagedArgs ga, int n_pre) {
+  using L = Layout<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kData);
+  const int b = static_cast<int>(blockIdx.x);
+  if (b >= n_pre) {
+    const int s = b - n_pre;
+    const int nx = ga.num_reqs * ga.row_tiles;
+    tc_suffix_cta<D>(&tm_q, &tm_k, &tm_v, ga, s % nx, (s / nx) % ga.num_kv_heads,
+                     s / (nx * ga.num_kv_heads), smem, bars);
+    return;
+  }
+  // a prefix range: its slot `split`, written by the body
+  const int split = b % pa.n_splits;
+  const int pair = (b / pa.n_splits) % pa.pairs;
+  const int kvh = b / (pa.n_splits * pa.pairs);
+  const int key_tiles = (pa.cpl + prefix::kKeysN - 1) / prefix::kKeysN;
+  const int t_first = min(split * pa.tiles_per_split, key_tiles);
+  const int t_last = min(t_first + pa.tiles_per_split, key_tiles);
+  prefix::prefix_range<D>(&tm_q, &tm_k, &tm_v, pa, prefix::prefix_geom(pa, pair), kvh, split,
+                          t_first, t_last, smem, bars);
+  // count it in the row groups of its 256 rows; the last contributor merges
+  const int gshift = __ffs(pa.group) - 1;
+  const int prow0 = pair * kRowsCta;
+  const int rows_here = min(kRowsCta, pa.total_q * pa.group - prow0);
+  if (rows_here <= 0) return;
+  MergeArgs m;
+  m.part_o = ga.part_o;
+  m.part_lse = ga.part_lse;
+  m.counters = ga.counters;
+  m.n_parts = ga.n_prefix + ga.n_splits;
+  m.n_count = ga.n_splits + ga.prefix_contributors;
+  m.rows = ga.total_q * ga.num_q_heads;
+  m.num_q_heads = ga.num_q_heads;
+  m.num_kv_heads = ga.num_kv_heads;
+  m.group = ga.group;
+  m.out = ga.out;
+  m.lse = ga.lse;
+  int* s_last = reinterpret_cast<int*>(smem + kRowsCta * L::kStageRow * 2);
+  float* s_w = reinterpret_cast<float*>(s_last + kRowsCta + 1);
+  const int tok_first = prow0 >> gshift;
+  const int n_tok = ((prow0 + rows_here - 1) >> gshift) - tok_first + 1;
+  auto out_row = [&](int rr) {
+    const int rho = prow0 + rr;
+    return static_cast<int64_t>(rho >> gshift) * pa.num_q_heads + kvh * pa.group +
+           (rho & (pa.group - 1));
+  };
+  count_and_merge_block<D>(m, tok_first, n_tok, kvh, rows_here, out_row,
+                           [&](int rr) { return ((prow0 + rr) >> gshift) - tok_first; }, s_last,
+                           s_w);
+}
+
+template <int D>
+cudaError_t launch_fused_t(const CUtensorMap& tm_q, const CUtensorMap& tm_k,
+                           const CUtensorMap& tm_v, const PrefixArgs& pa, const PagedArgs& ga,
+                           int n_pre, int n_suf, cudaStream_t stream) {
+  static std::atomic<uint64_t> attr_done{0};
+  cudaError_t e = set_smem_once(cascade_fused_kernel<D>, kDynamic<D>, attr_done);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(n_pre + n_suf);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kDynamic<D>;
+  cfg.stream = stream;
+  cfg.numAttrs = 0;
+  return cudaLaunchKernelEx(&cfg, cascade_fused_kernel<D>, tm_q, tm_k, tm_v, pa, ga, n_pre);
 }
 
 template <int D>
@@ -168,6 +258,15 @@ cudaError_t launch_tc_t(const CUtensorMap& tm_q, const CUtensorMap& tm_k,
 }
 
 }  // namespace
+
+cudaError_t launch_cascade_fused(int head_dim, const CUtensorMap& tm_q, const CUtensorMap& tm_k,
+                                 const CUtensorMap& tm_v, const PrefixArgs& pa,
+                                 const PagedArgs& ga, cudaStream_t stream) {
+  const int n_pre = pa.n_splits * pa.pairs * pa.num_kv_heads;
+  const int n_suf = ga.num_reqs * ga.row_tiles * ga.num_kv_heads * ga.n_splits;
+  if (head_dim == 64) return launch_fused_t<64>(tm_q, tm_k, tm_v, pa, ga, n_pre, n_suf, stream);
+  return launch_fused_t<128>(tm_q, tm_k, tm_v, pa, ga, n_pre, n_suf, stream);
+}
 
 cudaError_t launch_paged_tc(int head_dim, const CUtensorMap& tm_q, const CUtensorMap& tm_k,
                             const CUtensorMap& tm_v, const PagedArgs& a, bool after_prefix,
