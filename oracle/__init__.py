@@ -74,6 +74,12 @@ def _load(mutant: int = 0) -> ctypes.CDLL:
         lib.oracle_attention_sinks.argtypes = [p, p, p, i32, i32, p, i64, p, p, i32, i32, i32,
                                                i32, f64, p, p, p, i64, p, p, i32]
         lib.oracle_attention_sinks.restype = ctypes.c_int
+        lib.oracle_attention_fp8kv.argtypes = [p, p, p, i32, i32, p, i64, p, p, i32, i32, i32,
+                                               i32, f64, f64, f64, i32, i32, p, p, i64, p, p,
+                                               i32]
+        lib.oracle_attention_fp8kv.restype = ctypes.c_int
+        lib.oracle_e4m3_decode.argtypes = [p]
+        lib.oracle_e4m3_decode.restype = None
         lib.oracle_merge_states.argtypes = [p, p, p, p, i64, i32, p, p]
         lib.oracle_merge_states.restype = None
         lib.oracle_mutant_id.restype = ctypes.c_int
@@ -167,6 +173,64 @@ def attention(q, k_cache, v_cache, block_table, cu_seqlens_q, seq_lens, scale, *
                                        _ptr(out), _ptr(lse), int(n_threads))
     if st != 0:
         raise ValueError(f"oracle_attention failed with status {st} (bad block id or shape)")
+    return out, lse
+
+
+def _bytes(t) -> np.ndarray:
+    """uint8 tensor (torch, CPU) or array -> contiguous uint8 array."""
+    if isinstance(t, np.ndarray):
+        assert t.dtype == np.uint8
+        return np.ascontiguousarray(t)
+    import torch
+    assert t.dtype == torch.uint8, t.dtype
+    return t.detach().cpu().contiguous().numpy()
+
+
+def e4m3_values(*, mutant=0) -> np.ndarray:
+    """float64 [256]: the value of every E4M3 byte, from the format's definition."""
+    out = np.empty(256, np.float64)
+    _load(mutant).oracle_e4m3_decode(_ptr(out))
+    return out
+
+
+def attention_fp8kv(q, k_cache, v_cache, block_table, cu_seqlens_q, seq_lens, scale, k_scale,
+                    v_scale, *, mode=FULL, cpl=0, rows=None, n_threads=None, mutant=0):
+    """Oracle attention over an FP8 (E4M3) KV cache with per-tensor scales.
+
+    k_cache / v_cache: uint8 [num_blocks, bs, Hkv, D] of E4M3 bytes; an element's value
+    is decode(byte) * k_scale (or * v_scale).  Other arguments and the result: as for
+    attention()."""
+    lib = _load(mutant)
+    qb, kb, vb = _bits(q), _bytes(k_cache), _bytes(v_cache)
+    total_q, Hq, D = qb.shape
+    num_blocks, bs, Hkv, D2 = kb.shape
+    assert D2 == D and vb.shape == kb.shape
+    bt, cu, sl = _i32(block_table), _i32(cu_seqlens_q), _i32(seq_lens)
+    N = sl.shape[0]
+    assert bt.ndim == 2 and bt.shape[0] == N and cu.shape[0] == N + 1
+    assert int(cu[-1]) == total_q
+    if n_threads is None:
+        n_threads = os.cpu_count() or 1
+    if rows is None:
+        out = np.empty((total_q, Hq, D), np.float64)
+        lse = np.empty((total_q, Hq), np.float64)
+        rt = rh = None
+        n = total_q * Hq
+    else:
+        rows = np.ascontiguousarray(np.asarray(rows, dtype=np.int32).reshape(-1, 2))
+        rt = np.ascontiguousarray(rows[:, 0])
+        rh = np.ascontiguousarray(rows[:, 1])
+        n = rows.shape[0]
+        out = np.empty((n, D), np.float64)
+        lse = np.empty((n,), np.float64)
+    st = lib.oracle_attention_fp8kv(_ptr(qb), _ptr(kb), _ptr(vb), num_blocks, bs, _ptr(bt),
+                                    bt.shape[1], _ptr(cu), _ptr(sl), N, Hq, Hkv, D, float(scale),
+                                    float(k_scale), float(v_scale), mode, int(cpl),
+                                    _ptr(rt) if rt is not None else None,
+                                    _ptr(rh) if rh is not None else None, n, _ptr(out),
+                                    _ptr(lse), int(n_threads))
+    if st != 0:
+        raise ValueError(f"oracle_attention_fp8kv failed with status {st}")
     return out, lse
 
 

@@ -39,13 +39,22 @@
  *     out = sum_j exp(s_j - m) v_j / l,   lse = m + ln(l)
  * s_h = -inf is the standard path exactly.
  *
+ * FP8 KV cache (§六: FlashInfer's cascade wrapper refuses a KV cache stored in FP8;
+ * the page names the format, not its encoding).  Read as the OCP FP8 E4M3 format
+ * ("e4m3fn": 1 sign bit, 4 exponent bits with bias 7, 3 mantissa bits, no
+ * infinities, S.1111.111 = NaN, largest finite 448) with one scale per tensor, as
+ * KV caches store it: an element's value is decode(byte) * k_scale (or * v_scale),
+ *     decode = (-1)^S * 2^(E-7) * (1 + M/8)   for E > 0,
+ *              (-1)^S * 2^-6 * (M/8)          for E = 0,
+ * and attention runs on those values exactly as on a bf16 cache.
+ *
  * Every floating-point step is IEEE double; bf16 inputs are widened exactly.
  * Sums run in key / feature index order.  No blocking, no fusion, no reordering.
  * An empty key range gives out = 0 and lse = -inf.
  *
  * Layouts (all row-major, contiguous):
  *   q        bf16 bits [total_q, Hq, D]
- *   k, v     bf16 bits [num_blocks, block_size, Hkv, D]
+ *   k, v     bf16 bits [num_blocks, block_size, Hkv, D] (or E4M3 bytes, same shape)
  *   block_table int32 [num_reqs, bt_stride]   (only the first cdiv(seq_len, bs)
  *            entries of a row are read)
  *   cu_seqlens_q int32 [num_reqs + 1], seq_lens int32 [num_reqs]
@@ -69,8 +78,8 @@ enum { ORACLE_FULL = 0, ORACLE_PREFIX = 1, ORACLE_SUFFIX = 2 };
 
 typedef struct {
   const uint16_t* q;
-  const uint16_t* k;
-  const uint16_t* v;
+  const void* k;
+  const void* v;
   int32_t num_blocks;
   int32_t block_size;
   const int32_t* block_table;
@@ -83,7 +92,28 @@ typedef struct {
   int32_t mode;
   int32_t cpl;
   const double* sinks; /* [Hq] or NULL: no sinks (standard path only) */
+  int32_t kv_fp8;      /* 0: k, v are bf16 bits; 1: E4M3 bytes with the scales below */
+  double k_scale, v_scale;
 } oracle_problem;
+
+/* The E4M3 byte b as a double, from the format's definition (header). */
+static double e4m3_to_double(uint8_t b) {
+  const int sign = b >> 7;
+  const int e = (b >> 3) & 15;
+  const int mant = b & 7;
+  if (e == 15 && mant == 7) return NAN;
+#if ORACLE_MUTANT == 9
+  const double mag = e == 0 ? ldexp(mant / 8.0, -6) : ldexp(1.0 + mant / 8.0, e - 8); /* planted: bias 8 */
+#else
+  const double mag = e == 0 ? ldexp(mant / 8.0, -6) : ldexp(1.0 + mant / 8.0, e - 7);
+#endif
+  return sign ? -mag : mag;
+}
+
+/* oracle_e4m3_decode: the 256 codes' values (for the tests' pins). */
+void oracle_e4m3_decode(double* out256) {
+  for (int b = 0; b < 256; ++b) out256[b] = e4m3_to_double((uint8_t)b);
+}
 
 static double bf16_bits_to_double(uint16_t bits) {
   uint32_t u = (uint32_t)bits << 16;
@@ -99,9 +129,15 @@ static int request_of_token(const oracle_problem* P, int32_t t) {
   return -1;
 }
 
+/* Element d of a K or V row: bf16 widened, or an E4M3 byte decoded and scaled. */
+static double kv_elem(const oracle_problem* P, const void* row, int d, double scale) {
+  if (P->kv_fp8) return e4m3_to_double(((const uint8_t*)row)[d]) * scale;
+  return bf16_bits_to_double(((const uint16_t*)row)[d]);
+}
+
 /* Address of the D features of logical key j of request r, KV head g. */
-static const uint16_t* kv_row(const oracle_problem* P, const uint16_t* cache, int r, int32_t j,
-                              int g, int* bad) {
+static const void* kv_row(const oracle_problem* P, const void* cache, int r, int32_t j, int g,
+                          int* bad) {
 #if ORACLE_MUTANT == 5
   int32_t blk = P->block_table[(int64_t)r * P->bt_stride + j / P->block_size];
   int32_t slot = (j + 1) % P->block_size; /* planted: slot off by one inside the page */
@@ -113,7 +149,8 @@ static const uint16_t* kv_row(const oracle_problem* P, const uint16_t* cache, in
     *bad = 1;
     return NULL;
   }
-  return cache + (((int64_t)blk * P->block_size + slot) * P->Hkv + g) * (int64_t)P->D;
+  const int64_t elem = (((int64_t)blk * P->block_size + slot) * P->Hkv + g) * (int64_t)P->D;
+  return (const uint8_t*)cache + elem * (P->kv_fp8 ? 1 : 2);
 }
 
 /* One output row: query token t, query head h.  Returns 0, or -1 on a bad index. */
@@ -158,13 +195,14 @@ static int attend_row(const oracle_problem* P, int32_t t, int32_t h, double* out
   int bad = 0;
   double m = -INFINITY;
   for (int32_t j = lo; j < hi; ++j) {
-    const uint16_t* krow = kv_row(P, P->k, r, j, g, &bad);
+    const void* krow = kv_row(P, P->k, r, j, g, &bad);
     if (bad) {
       free(s);
       return -1;
     }
     double acc = 0.0;
-    for (int d = 0; d < D; ++d) acc += bf16_bits_to_double(qrow[d]) * bf16_bits_to_double(krow[d]);
+    for (int d = 0; d < D; ++d)
+      acc += bf16_bits_to_double(qrow[d]) * kv_elem(P, krow, d, P->k_scale);
 #if ORACLE_MUTANT == 1
     s[j - lo] = acc; /* planted: softmax scale dropped */
 #else
@@ -183,15 +221,15 @@ static int attend_row(const oracle_problem* P, int32_t t, int32_t h, double* out
   for (int d = 0; d < D; ++d) {
     double acc = 0.0;
     for (int32_t j = lo; j < hi; ++j) {
-      const uint16_t* vrow = kv_row(P, P->v, r, j, g, &bad);
+      const void* vrow = kv_row(P, P->v, r, j, g, &bad);
       if (bad) {
         free(s);
         return -1;
       }
 #if ORACLE_MUTANT == 6
-      acc += exp(s[j - lo] - m) * bf16_bits_to_double(vrow[(d + 1) % D]); /* planted: feature shift */
+      acc += exp(s[j - lo] - m) * kv_elem(P, vrow, (d + 1) % D, P->v_scale); /* planted: feature shift */
 #else
-      acc += exp(s[j - lo] - m) * bf16_bits_to_double(vrow[d]);
+      acc += exp(s[j - lo] - m) * kv_elem(P, vrow, d, P->v_scale);
 #endif
     }
     out[d] = acc / l;
@@ -278,7 +316,7 @@ int oracle_attention(const uint16_t* q, const uint16_t* k, const uint16_t* v, in
                      double* out, double* lse, int32_t n_threads) {
   oracle_problem P = {q,           k,        v,    num_blocks, block_size, block_table, bt_stride,
                       cu_seqlens_q, seq_lens, num_reqs, Hq,  Hkv,        D,           scale,
-                      mode,        cpl,      NULL};
+                      mode,        cpl,      NULL, 0, 1.0, 1.0};
   int64_t total_q = cu_seqlens_q[num_reqs];
   return run_rows(&P, NULL, NULL, total_q * Hq, out, lse, n_threads);
 }
@@ -292,7 +330,7 @@ int oracle_attention_sinks(const uint16_t* q, const uint16_t* k, const uint16_t*
                            int64_t n_rows, double* out, double* lse, int32_t n_threads) {
   oracle_problem P = {q,           k,        v,    num_blocks, block_size, block_table, bt_stride,
                       cu_seqlens_q, seq_lens, num_reqs, Hq,  Hkv,        D,           scale,
-                      ORACLE_FULL, 0,       sinks};
+                      ORACLE_FULL, 0,       sinks, 0, 1.0, 1.0};
   if (row_token) return run_rows(&P, row_token, row_head, n_rows, out, lse, n_threads);
   return run_rows(&P, NULL, NULL, (int64_t)cu_seqlens_q[num_reqs] * Hq, out, lse, n_threads);
 }
@@ -307,8 +345,26 @@ int oracle_attention_rows(const uint16_t* q, const uint16_t* k, const uint16_t* 
                           int32_t n_threads) {
   oracle_problem P = {q,           k,        v,    num_blocks, block_size, block_table, bt_stride,
                       cu_seqlens_q, seq_lens, num_reqs, Hq,  Hkv,        D,           scale,
-                      mode,        cpl,      NULL};
+                      mode,        cpl,      NULL, 0, 1.0, 1.0};
   return run_rows(&P, row_token, row_head, n_rows, out, lse, n_threads);
+}
+
+/*
+ * oracle_attention_fp8kv: the listed rows (row_token NULL: every row, [total_q, Hq]
+ * order) over an E4M3 KV cache with per-tensor scales, in any mode.
+ */
+int oracle_attention_fp8kv(const uint16_t* q, const uint8_t* k, const uint8_t* v,
+                           int32_t num_blocks, int32_t block_size, const int32_t* block_table,
+                           int64_t bt_stride, const int32_t* cu_seqlens_q, const int32_t* seq_lens,
+                           int32_t num_reqs, int32_t Hq, int32_t Hkv, int32_t D, double scale,
+                           double k_scale, double v_scale, int32_t mode, int32_t cpl,
+                           const int32_t* row_token, const int32_t* row_head, int64_t n_rows,
+                           double* out, double* lse, int32_t n_threads) {
+  oracle_problem P = {q,           k,        v,    num_blocks, block_size, block_table, bt_stride,
+                      cu_seqlens_q, seq_lens, num_reqs, Hq,  Hkv,        D,           scale,
+                      mode,        cpl,      NULL, 1, k_scale, v_scale};
+  if (row_token) return run_rows(&P, row_token, row_head, n_rows, out, lse, n_threads);
+  return run_rows(&P, NULL, NULL, (int64_t)cu_seqlens_q[num_reqs] * Hq, out, lse, n_threads);
 }
 
 /*

@@ -131,7 +131,7 @@ def _close(a, b, tol, what):
     fin = np.isfinite(b)
     if not np.array_equal(np.isfinite(a), fin):
         return [f"{what}: finiteness differs"]
-    if not np.array_equal(a[~fin], b[~fin]):
+    if not np.array_equal(a[~fin], b[~fin], equal_nan=True):
         return [f"{what}: non-finite values differ"]
     err = np.max(np.abs(a[fin] - b[fin]), initial=0.0)
     return [] if err <= tol else [f"{what}: max err {err:.3e} > {tol:.1e}"]
@@ -332,5 +332,50 @@ def pin_sinks(mutant=0):
     return fails
 
 
+def to_e4m3(x: torch.Tensor, scale: float) -> torch.Tensor:
+    """x / scale as E4M3 bytes (torch's float8_e4m3fn rounding: input drawing only)."""
+    return (x.float() / scale).to(torch.float8_e4m3fn).view(torch.uint8)
+
+
+def e4m3_library_values() -> np.ndarray:
+    """The 256 codes decoded by torch's float8_e4m3fn (a library routine)."""
+    codes = torch.arange(256, dtype=torch.int32).to(torch.uint8)
+    return codes.view(torch.float8_e4m3fn).to(torch.float64).numpy()
+
+
+def pin_fp8kv(mutant=0):
+    """FP8 (E4M3) KV cache: every code decodes as torch's float8_e4m3fn does; over a
+    cache whose scaled values are exact in bf16 (power-of-two scales) the FP8 oracle
+    equals the bf16 oracle on those values bit for bit; with other scales it equals
+    dense library attention over the decoded, scaled values."""
+    fails = []
+    got = oracle.e4m3_values(mutant=mutant)
+    fails += _close(got, e4m3_library_values(), 0.0, "e4m3 code table")
+    for seed, sl, ql, Hq, Hkv, D, bs, sh in CASES:
+        paged, dense = dense_problem(seed, sl, ql, Hq=Hq, Hkv=Hkv, D=D, bs=bs, shared_tokens=sh)
+        for ks, vs, exact in ((2.0 ** -4, 2.0 ** -3, True), (0.0173, 0.0291, False)):
+            kb = to_e4m3(paged["k_cache"], ks)
+            vb = to_e4m3(paged["v_cache"], vs)
+            o, l = oracle.attention_fp8kv(paged["q"], kb, vb, paged["block_table"],
+                                          paged["cu_seqlens_q"], paged["seq_lens"],
+                                          paged["scale"], ks, vs, mutant=mutant, n_threads=2)
+            kd = kb.view(torch.float8_e4m3fn).double() * ks
+            vd = vb.view(torch.float8_e4m3fn).double() * vs
+            if exact:
+                ref = dict(paged, k_cache=kd.to(torch.bfloat16), v_cache=vd.to(torch.bfloat16))
+                assert torch.equal(ref["k_cache"].double().nan_to_num(7.0), kd.nan_to_num(7.0))
+                ro, rl = _run(ref, mutant)
+                fails += _close(o, ro, 0.0, f"case{seed} fp8 vs bf16 out")
+                fails += _close(l, rl, 0.0, f"case{seed} fp8 vs bf16 lse")
+            else:
+                # the dense requests' values, through the same quantisation
+                dk = [(to_e4m3(k, ks).view(torch.float8_e4m3fn).double() * ks) for k in dense["k"]]
+                dv = [(to_e4m3(v, vs).view(torch.float8_e4m3fn).double() * vs) for v in dense["v"]]
+                ro, rl = library_reference(paged, dict(dense, k=dk, v=dv))
+                fails += _close(o, ro, 1e-10, f"case{seed} fp8 library out")
+                fails += _close(l, rl, 1e-10, f"case{seed} fp8 library lse")
+    return fails
+
+
 ALL_PINS = [pin_dense_library, pin_partials_library, pin_closed_forms, pin_merge_identity,
-            pin_page_invariance, pin_sinks]
+            pin_page_invariance, pin_sinks, pin_fp8kv]

@@ -16,7 +16,7 @@ def test_pin_passes_on_oracle(pin):
 
 # Planted faults: scale dropped, causal off by one, GQA groups interleaved, base-2 LSE,
 # slot off by one inside a page, feature index shifted, merge exponent sign flipped.
-@pytest.mark.parametrize("mutant", [1, 2, 3, 4, 5, 6, 7, 8])
+@pytest.mark.parametrize("mutant", [1, 2, 3, 4, 5, 6, 7, 8, 9])
 def test_planted_fault_is_caught(mutant):
     assert oracle._load(mutant).oracle_mutant_id() == mutant
     caught = [p.__name__ for p in pins.ALL_PINS if p(mutant=mutant)]
