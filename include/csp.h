@@ -438,6 +438,55 @@ CSP_API int csp_apply_sinks(void* out, float* lse, const float* sinks, int32_t n
                             int32_t num_heads, int32_t head_dim, void* stream);
 
 /*
+ * FP8 KV cache.  §六: FlashInfer's cascade wrapper is switched off for a KV cache
+ * stored in FP8.  These entry points take K and V caches of E4M3 bytes (OCP FP8 E4M3,
+ * "e4m3fn": bias 7, no infinities, S.1111.111 = NaN) in the usual layout
+ * [num_blocks, block_size, num_kv_heads, head_dim], each with one scale per tensor:
+ * an element's value is decode(byte) * k_scale (or * v_scale), and the result is the
+ * attention over those values.  The kernels widen the bytes to f16 (exact: every
+ * E4M3 value is an f16 value) and compute in f16 with fp32 accumulation: the queries
+ * are converted to f16 first (exact for bf16 values in f16's normal range, |q| in
+ * [2^-14, 65504]; rounded to f16's subnormal grid below it), k_scale is folded into
+ * the softmax scale and v_scale into the normalised output.  Half the KV bytes of a
+ * bf16 cache are read.
+ *
+ * csp_workspace_size_fp8kv — workspace bytes of cascade_attn_fp8kv (common_prefix_len
+ * > 0) or paged_attn_fp8kv (0): the plan's partials plus an f16 copy of q.  Errors as
+ * for csp_workspace_size.
+ */
+CSP_API int csp_workspace_size_fp8kv(int32_t num_reqs, int32_t total_q, int32_t max_seqlen_q,
+                                     int32_t max_seqlen_k, int32_t common_prefix_len,
+                                     int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                                     size_t* bytes_out);
+
+/*
+ * cascade_attn_fp8kv / paged_attn_fp8kv — cascade_attn and paged_attn over an E4M3 KV
+ * cache (k_cache, v_cache: device uint8, 16-byte aligned) with scales k_scale, v_scale
+ * (finite, > 0; else CSP_ERR_INVALID_ARG).  They run the two-kernel schedule (the
+ * prefix kernel and the paged kernels with the tiles widened in shared memory) and
+ * need csp_workspace_size_fp8kv bytes of workspace (else CSP_ERR_WORKSPACE).  Other
+ * arguments, layouts and errors: as for cascade_attn and paged_attn.
+ */
+CSP_API int cascade_attn_fp8kv(const void* q, const void* k_cache, const void* v_cache,
+                               int32_t num_blocks, const int32_t* block_table,
+                               int64_t bt_row_stride, const int32_t* cu_seqlens_q,
+                               const int32_t* seqused_k, int32_t num_reqs, int32_t total_q,
+                               int32_t max_seqlen_q, int32_t max_seqlen_k,
+                               int32_t common_prefix_len, int32_t block_size,
+                               int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                               float softmax_scale, float k_scale, float v_scale, void* out,
+                               float* lse, void* workspace, size_t workspace_bytes,
+                               void* stream);
+CSP_API int paged_attn_fp8kv(const void* q, const void* k_cache, const void* v_cache,
+                             int32_t num_blocks, const int32_t* block_table,
+                             int64_t bt_row_stride, const int32_t* cu_seqlens_q,
+                             const int32_t* seqused_k, int32_t num_reqs, int32_t total_q,
+                             int32_t max_seqlen_q, int32_t max_seqlen_k, int32_t block_size,
+                             int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                             float softmax_scale, float k_scale, float v_scale, void* out,
+                             float* lse, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * Multi-level cascade.  §七: FlashInfer's cascade runs any number of levels
  * (num_levels) where vLLM's runs two.  The levels form a prefix tree over consecutive
  * requests: a segment (level, r_lo, r_hi, k_lo, k_hi) is a run of at least two

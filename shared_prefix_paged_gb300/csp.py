@@ -34,7 +34,8 @@ EXPORTS = ("cascade_plan", "csp_workspace_size", "cascade_attn", "cascade_attn_t
            "csp_status_string", "csp_last_cuda_error", "csp_version", "cascade_attn_noalloc",
            "csp_noalloc_status", "csp_cascade_schedule", "csp_validate_batch",
            "csp_apply_sinks", "cascade_plan_device", "cascade_attn_device_plan",
-           "cascade_plan_levels", "csp_workspace_size_levels", "cascade_attn_levels")
+           "cascade_plan_levels", "csp_workspace_size_levels", "cascade_attn_levels",
+           "csp_workspace_size_fp8kv", "cascade_attn_fp8kv", "paged_attn_fp8kv")
 
 _lock = threading.Lock()
 _lib: Optional[ctypes.CDLL] = None
@@ -87,6 +88,11 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         lib.csp_workspace_size_levels.argtypes = [i32, i32, i32, i32, p, i32, i32, i32, i32,
                                                   i32, p]
         lib.cascade_attn_levels.argtypes = attn + [p, i32, p, i32] + tail
+        f32 = ctypes.c_float
+        tail8 = [i32, i32, i32, i32, f32, f32, f32, p, p, p, sz, p]
+        lib.csp_workspace_size_fp8kv.argtypes = [i32, i32, i32, i32, i32, i32, i32, i32, p]
+        lib.cascade_attn_fp8kv.argtypes = attn + [i32] + tail8
+        lib.paged_attn_fp8kv.argtypes = attn + tail8
         lib.csp_status_string.argtypes = [ctypes.c_int]
         lib.csp_status_string.restype = ctypes.c_char_p
         for name in ("cascade_plan", "csp_workspace_size", "cascade_attn", "cascade_attn_timed",
@@ -95,7 +101,8 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
                      "csp_version", "csp_cascade_schedule", "csp_validate_batch",
                      "csp_apply_sinks", "cascade_plan_device", "cascade_attn_device_plan",
                      "cascade_plan_levels", "csp_workspace_size_levels",
-                     "cascade_attn_levels"):
+                     "cascade_attn_levels", "csp_workspace_size_fp8kv", "cascade_attn_fp8kv",
+                     "paged_attn_fp8kv"):
             getattr(lib, name).restype = ctypes.c_int
         _lib = lib
         return lib
@@ -395,6 +402,49 @@ def cascade_attn_levels(q, k_cache, v_cache, block_table, cu_seqlens_q, seqused_
         seg.shape[0], _ptr(suffix_start), int(max_suffix_len), bs, hq, hkv, d,
         float(softmax_scale), _ptr(out), _ptr(lse), _ptr(workspace), workspace.numel(),
         _stream_ptr(stream, q.device)), "cascade_attn_levels")
+    return out, lse
+
+
+def workspace_size_fp8kv(num_reqs, total_q, max_seqlen_q, max_seqlen_k, common_prefix_len,
+                         num_q_heads, num_kv_heads, head_dim) -> int:
+    lib = load()
+    out = ctypes.c_size_t(0)
+    _check(lib.csp_workspace_size_fp8kv(num_reqs, total_q, max_seqlen_q, max_seqlen_k,
+                                        common_prefix_len, num_q_heads, num_kv_heads, head_dim,
+                                        ctypes.byref(out)), "csp_workspace_size_fp8kv")
+    return int(out.value)
+
+
+def attn_fp8kv(q, k_cache, v_cache, block_table, cu_seqlens_q, seqused_k, *, max_seqlen_q,
+               max_seqlen_k, softmax_scale, k_scale, v_scale, common_prefix_len=0, out=None,
+               lse=None, workspace=None, stream=None):
+    """Attention over an FP8 (E4M3) KV cache: k_cache / v_cache uint8 device tensors
+    [num_blocks, 16, Hkv, D] of E4M3 bytes, values decode(byte) * k_scale (v_scale).
+    common_prefix_len > 0: cascade_attn_fp8kv; 0: paged_attn_fp8kv (the standard path)."""
+    import torch
+    lib = load()
+    total_q, hq, d = q.shape
+    num_blocks, bs, hkv, _ = k_cache.shape
+    if k_cache.dtype != torch.uint8 or v_cache.dtype != torch.uint8:
+        raise ValueError("k_cache and v_cache: uint8 tensors of E4M3 bytes")
+    n = int(seqused_k.shape[0])
+    cpl = int(common_prefix_len)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((total_q, hq), dtype=torch.float32, device=q.device)
+    if workspace is None:
+        workspace = alloc_workspace(workspace_size_fp8kv(n, total_q, max_seqlen_q, max_seqlen_k,
+                                                         cpl, hq, hkv, d), q.device)
+    args = [_ptr(q), _ptr(k_cache), _ptr(v_cache), num_blocks, _ptr(block_table),
+            int(block_table.stride(0)), _ptr(cu_seqlens_q), _ptr(seqused_k), n, total_q,
+            int(max_seqlen_q), int(max_seqlen_k)]
+    if cpl > 0:
+        args.append(cpl)
+    args += [bs, hq, hkv, d, float(softmax_scale), float(k_scale), float(v_scale), _ptr(out),
+             _ptr(lse), _ptr(workspace), workspace.numel(), _stream_ptr(stream, q.device)]
+    name = "cascade_attn_fp8kv" if cpl > 0 else "paged_attn_fp8kv"
+    _check(getattr(lib, name)(*args), name)
     return out, lse
 
 

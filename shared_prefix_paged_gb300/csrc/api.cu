@@ -99,6 +99,23 @@ int make_map_3d(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1, ui
   return CSP_OK;
 }
 
+// An E4M3 K or V cache [blocks][16][Hkv][D] (bytes) as {D, Hkv, tokens}, boxes {D, 1, 16}
+// (one page of one KV head), no swizzle.
+int make_map_bytes_3d(CUtensorMap* map, const void* base, int D, int Hkv, uint64_t ntok) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return cuda_fail(cudaErrorNotSupported);
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(Hkv), ntok};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(D),
+                                 static_cast<cuuint64_t>(Hkv) * static_cast<cuuint64_t>(D)};
+  const cuuint32_t box[3] = {static_cast<cuuint32_t>(D), 1, kPage};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return cuda_fail(cudaErrorInvalidValue);
+  return CSP_OK;
+}
+
 // A K or V cache [blocks][16][Hkv][D] seen as 4-D {64 features, tokens, D / 64
 // feature halves, Hkv} (the halves and heads listed after the tokens), 128-byte
 // swizzle, boxes {64, 16, D / 64, 1}: one page of one KV head lands in shared memory
@@ -535,7 +552,8 @@ int attention_call(const void* q, const void* k_cache, const void* v_cache, int3
                    int32_t block_size, int32_t Hq, int32_t Hkv, int32_t D, float scale,
                    void* out, float* lse, void* workspace, size_t workspace_bytes,
                    void* stream_ptr, void* const* events = nullptr, int sched_override = -1,
-                   int ranges_override = 0, const int32_t* cpl_dev = nullptr) {
+                   int ranges_override = 0, const int32_t* cpl_dev = nullptr, bool kv_fp8 = false,
+                   float k_scale = 1.f, float v_scale = 1.f) {
   int st = check_shape(num_reqs, total_q, max_seqlen_q, max_seqlen_k, Hq, Hkv, D, block_size);
   if (st != CSP_OK) return st;
   if (cpl < 0 || cpl % block_size != 0 || cpl > max_seqlen_k) return CSP_ERR_INVALID_ARG;
@@ -548,25 +566,58 @@ int attention_call(const void* q, const void* k_cache, const void* v_cache, int3
   if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out))
     return CSP_ERR_INVALID_ARG;
   if (bt_row_stride < cdiv(max_seqlen_k, block_size)) return CSP_ERR_INVALID_ARG;
+  if (kv_fp8) {
+    // an E4M3 cache runs on the two-kernel schedule (its kernels widen the tiles)
+    if (!(k_scale > 0.f) || !std::isfinite(k_scale) || !(v_scale > 0.f) ||
+        !std::isfinite(v_scale))
+      return CSP_ERR_INVALID_ARG;
+    if (cpl_dev != nullptr || (sched_override >= 0 && sched_override != CSP_SCHEDULE_TWO_KERNELS))
+      return CSP_ERR_UNSUPPORTED;
+    sched_override = CSP_SCHEDULE_TWO_KERNELS;
+  }
   int sms = 0;
   if ((st = device_sm_count(&sms)) != CSP_OK) return st;
   LaunchPlan P;
   make_plan(num_reqs, total_q, max_seqlen_q, max_seqlen_k, cpl, Hq, Hkv, D, sms, &P,
             sched_override, ranges_override);
+  // an E4M3 cache: the f16 copy of the queries after the plan's partition
+  const size_t q16_off = align256(P.bytes);
+  const size_t need =
+      kv_fp8 ? q16_off + align256(static_cast<size_t>(total_q) * Hq * D * 2) : P.bytes;
   if (sched_override == CSP_SCHEDULE_SINGLE && !P.single) return CSP_ERR_UNSUPPORTED;
   // a prefix length in device memory: only the single-kernel schedule reads it there
   if (cpl_dev != nullptr && (!P.single || cpl == 0)) return CSP_ERR_UNSUPPORTED;
   if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255) != 0 ||
-      workspace_bytes < P.bytes)
+      workspace_bytes < need)
     return CSP_ERR_WORKSPACE;
   cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   int* status = reinterpret_cast<int*>(ws);
+  const void* q_in = q;  // the queries the kernels read
   int* counters = reinterpret_cast<int*>(ws + P.off_counters);
   __nv_bfloat16* part_o = reinterpret_cast<__nv_bfloat16*>(ws + P.off_part_o);
   float* part_lse = reinterpret_cast<float*>(ws + P.off_part_lse);
-  const float scale_log2 = scale * 1.4426950408889634f;
+  const float scale_log2 = scale * 1.4426950408889634f * (kv_fp8 ? k_scale : 1.f);
   cudaError_t e;
+  if (kv_fp8) {
+    q_in = ws + q16_off;
+    if ((e = csp::launch_bf16_to_f16(q, ws + q16_off, static_cast<int64_t>(total_q) * Hq * D,
+                                     stream)) != cudaSuccess)
+      return cuda_fail(e);
+  }
+  // the K/V maps of the tcgen05 kernels: 16-bit pages, or E4M3 pages
+  auto kv_maps = [&](CUtensorMap* tk, CUtensorMap* tv) -> int {
+    const uint64_t ntok = static_cast<uint64_t>(num_blocks) * block_size;
+    const uint64_t row_b = static_cast<uint64_t>(D) * 2;
+    int r;
+    if (kv_fp8) {
+      if ((r = make_map_bytes_3d(tk, k_cache, D, Hkv, ntok)) != CSP_OK) return r;
+      return make_map_bytes_3d(tv, v_cache, D, Hkv, ntok);
+    }
+    if ((r = make_map_3d(tk, k_cache, D, Hkv, ntok, row_b, row_b * Hkv, 64, 1, kPage)) != CSP_OK)
+      return r;
+    return make_map_kv_pages(tv, v_cache, D, Hkv, ntok);
+  };
   auto mark = [&](int i) -> cudaError_t {
     return events ? cudaEventRecord(static_cast<cudaEvent_t>(events[i]), stream) : cudaSuccess;
   };
@@ -665,14 +716,10 @@ int attention_call(const void* q, const void* k_cache, const void* v_cache, int3
   csp::PrefixArgs pa;
   if (cpl > 0) {
     const uint64_t row_b = static_cast<uint64_t>(D) * 2;
-    if ((st = make_map_3d(&tm_q, q, D, Hq, total_q, row_b, row_b * Hq, 64, P.group,
+    if ((st = make_map_3d(&tm_q, q_in, D, Hq, total_q, row_b, row_b * Hq, 64, P.group,
                           128 / P.group)) != CSP_OK)
       return st;
-    const uint64_t ntok = static_cast<uint64_t>(num_blocks) * block_size;
-    if ((st = make_map_3d(&tm_k, k_cache, D, Hkv, ntok, row_b, row_b * Hkv, 64, 1, kPage)) !=
-        CSP_OK)
-      return st;
-    if ((st = make_map_kv_pages(&tm_v, v_cache, D, Hkv, ntok)) != CSP_OK) return st;
+    if ((st = kv_maps(&tm_k, &tm_v)) != CSP_OK) return st;
     pa.k = static_cast<const __nv_bfloat16*>(k_cache);
     pa.v = static_cast<const __nv_bfloat16*>(v_cache);
     pa.block_table = block_table;
@@ -689,15 +736,19 @@ int attention_call(const void* q, const void* k_cache, const void* v_cache, int3
     pa.part_lse = part_lse;
     pa.lse_stride = static_cast<int64_t>(total_q) * Hq;
     pa.status = status;
-    if (!P.fused && (e = csp::launch_prefix(D, tm_q, tm_k, tm_v, pa, stream)) != cudaSuccess)
+    pa.v_scale = kv_fp8 ? v_scale : 1.f;
+    if (!P.fused &&
+        (e = kv_fp8 ? csp::launch_prefix_f8(D, tm_q, tm_k, tm_v, pa, stream)
+                    : csp::launch_prefix(D, tm_q, tm_k, tm_v, pa, stream)) != cudaSuccess)
       return cuda_fail(e);
   }
   if ((e = mark(1)) != cudaSuccess) return cuda_fail(e);
 
   csp::PagedArgs ga;
-  ga.q = static_cast<const __nv_bfloat16*>(q);
+  ga.q = static_cast<const __nv_bfloat16*>(q_in);
   ga.k = static_cast<const __nv_bfloat16*>(k_cache);
   ga.v = static_cast<const __nv_bfloat16*>(v_cache);
+  ga.v_scale = kv_fp8 ? v_scale : 1.f;
   ga.block_table = block_table;
   ga.bt_stride = bt_row_stride;
   ga.cu_seqlens_q = cu_seqlens_q;
@@ -729,16 +780,15 @@ int attention_call(const void* q, const void* k_cache, const void* v_cache, int3
   } else if (P.tc) {
     CUtensorMap tm_q, tm_k, tm_v;
     const uint64_t row_b = static_cast<uint64_t>(D) * 2;
-    const uint64_t ntok = static_cast<uint64_t>(num_blocks) * block_size;
-    if ((st = make_map_3d(&tm_q, q, D, Hq, total_q, row_b, row_b * Hq, 64, P.group,
+    if ((st = make_map_3d(&tm_q, q_in, D, Hq, total_q, row_b, row_b * Hq, 64, P.group,
                           128 / P.group)) != CSP_OK ||
-        (st = make_map_3d(&tm_k, k_cache, D, Hkv, ntok, row_b, row_b * Hkv, 64, 1, kPage)) !=
-            CSP_OK ||
-        (st = make_map_kv_pages(&tm_v, v_cache, D, Hkv, ntok)) != CSP_OK)
+        (st = kv_maps(&tm_k, &tm_v)) != CSP_OK)
       return st;
-    e = csp::launch_paged_tc(D, tm_q, tm_k, tm_v, ga, overlap, stream);
+    e = kv_fp8 ? csp::launch_paged_tc_f8(D, tm_q, tm_k, tm_v, ga, overlap, stream)
+               : csp::launch_paged_tc(D, tm_q, tm_k, tm_v, ga, overlap, stream);
   } else {
-    e = csp::launch_paged(D, ga, overlap, stream);
+    e = kv_fp8 ? csp::launch_paged_f8(D, ga, overlap, stream)
+               : csp::launch_paged(D, ga, overlap, stream);
   }
   if (e != cudaSuccess) return cuda_fail(e);
   if ((e = mark(2)) != cudaSuccess) return cuda_fail(e);
@@ -936,6 +986,52 @@ int cascade_attn_timed(const void* q, const void* k_cache, const void* v_cache,
                         common_prefix_len, block_size, num_q_heads, num_kv_heads, head_dim,
                         softmax_scale, out, lse, workspace, workspace_bytes, stream,
                         phase_events);
+}
+
+int csp_workspace_size_fp8kv(int32_t num_reqs, int32_t total_q, int32_t max_seqlen_q,
+                             int32_t max_seqlen_k, int32_t common_prefix_len, int32_t num_q_heads,
+                             int32_t num_kv_heads, int32_t head_dim, size_t* bytes_out) {
+  if (!bytes_out) return CSP_ERR_INVALID_ARG;
+  int st = check_shape(num_reqs, total_q, max_seqlen_q, max_seqlen_k, num_q_heads, num_kv_heads,
+                       head_dim, kPage);
+  if (st != CSP_OK) return st;
+  if (common_prefix_len < 0 || common_prefix_len % kPage != 0) return CSP_ERR_INVALID_ARG;
+  int sms = 0;
+  if ((st = device_sm_count(&sms)) != CSP_OK) return st;
+  LaunchPlan P;
+  make_plan(num_reqs, total_q, max_seqlen_q, max_seqlen_k, common_prefix_len, num_q_heads,
+            num_kv_heads, head_dim, sms, &P, CSP_SCHEDULE_TWO_KERNELS);
+  *bytes_out = align256(P.bytes) + align256(static_cast<size_t>(total_q) * num_q_heads * head_dim * 2);
+  return CSP_OK;
+}
+
+int cascade_attn_fp8kv(const void* q, const void* k_cache, const void* v_cache,
+                       int32_t num_blocks, const int32_t* block_table, int64_t bt_row_stride,
+                       const int32_t* cu_seqlens_q, const int32_t* seqused_k, int32_t num_reqs,
+                       int32_t total_q, int32_t max_seqlen_q, int32_t max_seqlen_k,
+                       int32_t common_prefix_len, int32_t block_size, int32_t num_q_heads,
+                       int32_t num_kv_heads, int32_t head_dim, float softmax_scale,
+                       float k_scale, float v_scale, void* out, float* lse, void* workspace,
+                       size_t workspace_bytes, void* stream) {
+  return attention_call(q, k_cache, v_cache, num_blocks, block_table, bt_row_stride, cu_seqlens_q,
+                        seqused_k, num_reqs, total_q, max_seqlen_q, max_seqlen_k,
+                        common_prefix_len, block_size, num_q_heads, num_kv_heads, head_dim,
+                        softmax_scale, out, lse, workspace, workspace_bytes, stream, nullptr, -1,
+                        0, nullptr, true, k_scale, v_scale);
+}
+
+int paged_attn_fp8kv(const void* q, const void* k_cache, const void* v_cache, int32_t num_blocks,
+                     const int32_t* block_table, int64_t bt_row_stride,
+                     const int32_t* cu_seqlens_q, const int32_t* seqused_k, int32_t num_reqs,
+                     int32_t total_q, int32_t max_seqlen_q, int32_t max_seqlen_k,
+                     int32_t block_size, int32_t num_q_heads, int32_t num_kv_heads,
+                     int32_t head_dim, float softmax_scale, float k_scale, float v_scale,
+                     void* out, float* lse, void* workspace, size_t workspace_bytes,
+                     void* stream) {
+  return attention_call(q, k_cache, v_cache, num_blocks, block_table, bt_row_stride, cu_seqlens_q,
+                        seqused_k, num_reqs, total_q, max_seqlen_q, max_seqlen_k, 0, block_size,
+                        num_q_heads, num_kv_heads, head_dim, softmax_scale, out, lse, workspace,
+                        workspace_bytes, stream, nullptr, -1, 0, nullptr, true, k_scale, v_scale);
 }
 
 int paged_attn(const void* q, const void* k_cache, const void* v_cache, int32_t num_blocks,

@@ -40,7 +40,7 @@ __global__ void __launch_bounds__(256)
     w2 = exp2f((b - m) * kLog2e);
   }
   const float ws = w1 + w2;
-  const float inv = ws > 0.f ? 1.f / ws : 0.f;
+  const float inv = !(ws <= 0.f) ? 1.f / ws : 0.f;  // a NaN sum propagates
   float x1[8], x2[8];
   const int64_t off = static_cast<int64_t>(row) * head_dim + c * 8;
   if constexpr (kF32) {
@@ -68,12 +68,12 @@ __global__ void __launch_bounds__(256)
 #pragma unroll
   for (int e = 0; e < 4; ++e) {
     // an empty side (lse = -inf, weight 0) contributes nothing, whatever its values
-    const float y0 = (w1 > 0.f ? w1 * x1[2 * e] : 0.f) + (w2 > 0.f ? w2 * x2[2 * e] : 0.f);
-    const float y1 = (w1 > 0.f ? w1 * x1[2 * e + 1] : 0.f) + (w2 > 0.f ? w2 * x2[2 * e + 1] : 0.f);
+    const float y0 = (w1 != 0.f ? w1 * x1[2 * e] : 0.f) + (w2 != 0.f ? w2 * x2[2 * e] : 0.f);
+    const float y1 = (w1 != 0.f ? w1 * x1[2 * e + 1] : 0.f) + (w2 != 0.f ? w2 * x2[2 * e + 1] : 0.f);
     w[e] = pack_bf16x2(y0 * inv, y1 * inv);
   }
   *reinterpret_cast<uint4*>(out + off) = make_uint4(w[0], w[1], w[2], w[3]);
-  if (c == 0 && out_lse != nullptr) out_lse[row] = ws > 0.f ? m + logf(ws) : -INFINITY;
+  if (c == 0 && out_lse != nullptr) out_lse[row] = !(ws <= 0.f) ? m + logf(ws) : -INFINITY;
 }
 
 // n slots per row (the cascade call's partials, log2 domain): one thread per 8
@@ -117,12 +117,12 @@ __global__ void __launch_bounds__(kMergeThreads)
       acc[2 * e + 1] = w != 0.f ? fmaf(w, f.y, acc[2 * e + 1]) : acc[2 * e + 1];
     }
   }
-  const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+  const float inv = !(wsum <= 0.f) ? 1.f / wsum : 0.f;  // a NaN sum propagates
   *reinterpret_cast<uint4*>(m.out + row * D + c * 8) =
       make_uint4(pack_bf16x2(acc[0] * inv, acc[1] * inv), pack_bf16x2(acc[2] * inv, acc[3] * inv),
                  pack_bf16x2(acc[4] * inv, acc[5] * inv), pack_bf16x2(acc[6] * inv, acc[7] * inv));
   if (c == 0 && m.lse != nullptr)
-    m.lse[row] = wsum > 0.f ? (mx + log2f(wsum)) * 0.69314718055994531f : -INFINITY;
+    m.lse[row] = !(wsum <= 0.f) ? (mx + log2f(wsum)) * 0.69314718055994531f : -INFINITY;
 }
 
 template <int D>
@@ -237,6 +237,33 @@ __global__ void __launch_bounds__(256) fill_f32_kernel(float* __restrict__ p, in
 }
 
 }  // namespace
+
+// bf16 -> f16, 8 values per thread (the queries of an FP8-cache call; exact for every
+// bf16 value in f16's normal range, rounded to nearest below it).
+__global__ void __launch_bounds__(256) bf16_to_f16_kernel(const uint4* __restrict__ in,
+                                                          uint4* __restrict__ out, int64_t n8) {
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * 256 + threadIdx.x; i < n8;
+       i += static_cast<int64_t>(gridDim.x) * 256) {
+    const uint4 u = __ldg(in + i);
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[e]));
+      o[e] = pack_f16x2(f.x, f.y);
+    }
+    out[i] = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+}
+
+cudaError_t launch_bf16_to_f16(const void* in, void* out, int64_t n, cudaStream_t stream) {
+  const int64_t n8 = n / 8;  // n is a multiple of 8 (rows of D features)
+  if (n8 <= 0) return cudaSuccess;
+  const int64_t blocks = std::min<int64_t>((n8 + 255) / 256, 4096);
+  bf16_to_f16_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
+      static_cast<const uint4*>(in), static_cast<uint4*>(out), n8);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_fill_f32(float* p, int64_t n, float v, cudaStream_t stream) {
   if (n <= 0) return cudaSuccess;

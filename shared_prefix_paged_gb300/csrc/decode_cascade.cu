@@ -461,7 +461,7 @@ __device__ __forceinline__ void consume_items(const DecodeArgs& a, uint8_t* ring
           mw[w] = (mw[w] == -INFINITY) ? 0.f : fast_exp2(mw[w] - mg);  // warp w's weight
           lsum += s_l[w * kRows + rr] * mw[w];
         }
-        const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+        const float inv = !(lsum <= 0.f) ? 1.f / lsum : 0.f;  // a NaN sum propagates
         const int qi = rr / p.group, j = rr - qi * p.group;
         const int64_t row = static_cast<int64_t>(c_q0 + qi) * p.num_q_heads + c_kvh * p.group + j;
         const int64_t prow = slot_rows + row;
@@ -480,7 +480,7 @@ __device__ __forceinline__ void consume_items(const DecodeArgs& a, uint8_t* ring
                        make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv));
         }
         if (lane == 0)
-          p.part_lse[p.n_splits * p.lse_stride + row] = lsum > 0.f ? mg + log2f(lsum) : -INFINITY;
+          p.part_lse[p.n_splits * p.lse_stride + row] = !(lsum <= 0.f) ? mg + log2f(lsum) : -INFINITY;
       }
     }
     // the item goes back to the producer (its TMA will overwrite what this warp
@@ -576,7 +576,7 @@ __device__ __forceinline__ void merge_rows_staged(const DecodeArgs& a, const CUt
           acc[2 * f + 1] = fmaf(l[s], x.y, acc[2 * f + 1]);
         }
       }
-      const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+      const float inv = !(wsum <= 0.f) ? 1.f / wsum : 0.f;
 #pragma unroll
       for (int f = 0; f < kF; ++f) acc[f] *= inv;
       if (in) {
@@ -587,7 +587,7 @@ __device__ __forceinline__ void merge_rows_staged(const DecodeArgs& a, const CUt
         for (int f = 0; f < kF / 2; ++f) ou[f] = pack_bf16x2(acc[2 * f], acc[2 * f + 1]);
         *reinterpret_cast<Vec*>(a.out + row * D + hl * kF) = o;
         if (hl == 0 && a.lse != nullptr)
-          a.lse[row] = wsum > 0.f ? (mx + log2f(wsum)) * 0.69314718055994531f : -INFINITY;
+          a.lse[row] = !(wsum <= 0.f) ? (mx + log2f(wsum)) * 0.69314718055994531f : -INFINITY;
       }
     }
     // the next chunk's copies overwrite what was read here

@@ -41,6 +41,9 @@ struct PrefixArgs {
   int tok0 = 0;
   int slot_base = 0;
   int64_t rows_all = 0;  // 0: total_q * num_q_heads
+  // An FP8 (E4M3) KV cache: the V scale, applied to the normalised rows (the K scale is
+  // folded into scale_log2 by the host).
+  float v_scale = 1.f;
 };
 
 // The segments of a multi-level cascade in one grid (prefix_attn.cu): segment i owns
@@ -95,6 +98,10 @@ struct PagedArgs {
                                           // (the suffixes of a multi-level cascade)
   int prefix_contributors = 0;  // prefix ranges counted in the same row-group counters
                                 // (the fused launch)
+  // An FP8 (E4M3) KV cache (the *_f8 launchers): q then points at an f16 copy of the
+  // queries, k and v at the E4M3 caches, and the V scale multiplies the normalised
+  // rows (the K scale is folded into scale_log2).
+  float v_scale = 1.f;
 };
 
 // Single-kernel cascade step for decode-like batches (decode_cascade.cu): at most 16
@@ -197,6 +204,20 @@ cudaError_t launch_plan_device(const int32_t* block_table, int64_t bt_row_stride
 
 // n floats at p set to v.
 cudaError_t launch_fill_f32(float* p, int64_t n, float v, cudaStream_t stream);
+
+// n bf16 values (a multiple of 8, 16-byte aligned) -> f16.
+cudaError_t launch_bf16_to_f16(const void* in, void* out, int64_t n, cudaStream_t stream);
+
+// The FP8 (E4M3) KV cache variants: tm_k and tm_v map the byte caches as {D, Hkv,
+// tokens} with boxes {D, 1, 16} (no swizzle); tm_q and the paged kernels' q the f16
+// queries; PrefixArgs / PagedArgs v_scale the V scale (the K scale is in scale_log2).
+cudaError_t launch_prefix_f8(int head_dim, const CUtensorMap& tm_q, const CUtensorMap& tm_k,
+                             const CUtensorMap& tm_v, const PrefixArgs& a, cudaStream_t stream);
+cudaError_t launch_paged_f8(int head_dim, const PagedArgs& a, bool after_prefix,
+                            cudaStream_t stream);
+cudaError_t launch_paged_tc_f8(int head_dim, const CUtensorMap& tm_q, const CUtensorMap& tm_k,
+                               const CUtensorMap& tm_v, const PagedArgs& a, bool after_prefix,
+                               cudaStream_t stream);
 
 // Attention sinks applied to a finished result (rows = tokens x heads, natural-log
 // lse updated in place); head_dim / 8 divides 32.

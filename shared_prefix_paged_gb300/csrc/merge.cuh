@@ -74,7 +74,7 @@ __device__ __forceinline__ void merge_row_warp(const MergeArgs& m, int64_t row, 
 #pragma unroll
   for (int s = 16; s > 0; s >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, s);
   wsum += w_own;
-  const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+  const float inv = !(wsum <= 0.f) ? 1.f / wsum : 0.f;  // a NaN sum propagates
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   if (w_own != 0.f) {
     const float wo = w_own * inv;
@@ -107,7 +107,7 @@ __device__ __forceinline__ void merge_row_warp(const MergeArgs& m, int64_t row, 
   }
   if (lane < D / 4) store_bf16x4(m.out + row * D + lane * 4, acc);
   if (lane == 0 && m.lse != nullptr)
-    m.lse[row] = wsum > 0.f ? (mx + log2f(wsum)) * 0.69314718055994531f : -INFINITY;
+    m.lse[row] = !(wsum <= 0.f) ? (mx + log2f(wsum)) * 0.69314718055994531f : -INFINITY;
 }
 
 // Called by every thread of the CTA (it contains __syncthreads) after the CTA wrote
@@ -171,11 +171,11 @@ __device__ __forceinline__ void merge_rows_block(const MergeArgs& m, int n_rows,
     const float w_own =
         (own && mx != -INFINITY && own_lse[i] != -INFINITY) ? fast_exp2(own_lse[i] - mx) : 0.f;
     wsum += w_own;
-    const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+    const float inv = !(wsum <= 0.f) ? 1.f / wsum : 0.f;  // a NaN sum propagates
     for (int p = 0; p < np; ++p) w[p] *= inv;
     w[np] = w_own * inv;
     if (m.lse != nullptr)
-      m.lse[row] = wsum > 0.f ? (mx + log2f(wsum)) * 0.69314718055994531f : -INFINITY;
+      m.lse[row] = !(wsum <= 0.f) ? (mx + log2f(wsum)) * 0.69314718055994531f : -INFINITY;
   }
   __syncthreads();
   // the rows, 16 bytes (8 features) per item, eight items per thread in flight

@@ -39,29 +39,37 @@ __device__ __forceinline__ uint32_t swz(int row, int chunk) {
   return static_cast<uint32_t>(row * (D * 2) + ((chunk ^ (row & 7)) << 4));
 }
 
-template <int D>
+template <int D, bool kF8 = false>
 struct PagedLayout {
-  // two 64-key tiles in flight (68 KB for D=128), so three CTAs fit on an SM
+  // two 64-key tiles in flight (68 KB for D=128), so three CTAs fit on an SM.  An E4M3
+  // cache keeps its two tiles in flight as bytes and widens the current one into a
+  // single f16 K/V buffer (the same 68 KB).
   static constexpr int kStages = 2;
   static constexpr int kRows = 16;
   static constexpr int kQBytes = kRows * D * 2;
   static constexpr int kKVBytes = kTileKeys * D * 2;
+  static constexpr int kBufs = kF8 ? 1 : kStages;          // 16-bit K (and V) tiles
   static constexpr int kQ = 0;
   static constexpr int kK = kQ + kQBytes;
-  static constexpr int kV = kK + kStages * kKVBytes;
-  static constexpr int kLast = kV + kStages * kKVBytes;   // int [64] row-group flags
+  static constexpr int kV = kK + kBufs * kKVBytes;
+  static constexpr int kF8Tile = kTileKeys * D;             // E4M3 K (or V) tile
+  static constexpr int kF8Base = kV + kBufs * kKVBytes;     // [stage][K, V] E4M3 tiles
+  static constexpr int kLast = kF8Base + (kF8 ? kStages * 2 * kF8Tile : 0);  // int [64] flags
   static constexpr int kEnd = kLast + 64 * 4;
   // decode merge scratch (reuses the K/V stages after the last tile): per warp 16
   // rows of D floats with a padded stride, then per-warp max and sum
   static constexpr int kORow = D + 8;
   static constexpr int kMergeBytes = 4 * 16 * kORow * 4 + 2 * 4 * 16 * 4;
-  static_assert(kMergeBytes <= 2 * kStages * kKVBytes, "merge scratch");
+  static_assert(kMergeBytes <= kLast - kK, "merge scratch");
 };
 
-template <int D>
+// kF8: an E4M3 KV cache (a.k, a.v its bytes, a.q the f16 queries): the tiles arrive
+// as bytes, are widened to f16 in shared memory (exact) and run on f16 MMAs; the V
+// scale multiplies the normalised rows.
+template <int D, bool kF8>
 __global__ void __launch_bounds__(kThreads)
     paged_attn_kernel(const PagedArgs a) {
-  using L = PagedLayout<D>;
+  using L = PagedLayout<D, kF8>;
   constexpr int kStages = L::kStages;
   constexpr int kChunks = D / 8;               // 16-byte chunks per row
   constexpr int kWarpKeys = 16;                // keys of a tile each warp handles
@@ -97,6 +105,29 @@ __global__ void __launch_bounds__(kThreads)
 
   auto load_tile = [&](int ti, int stage) {
     const int kt0 = kbeg + ti * kTileKeys;
+    if constexpr (kF8) {
+      // 16-byte chunks of E4M3 bytes (16 features each), [key][D bytes] per tile
+      constexpr int kC16 = D / 16;
+      const uint8_t* k8 = reinterpret_cast<const uint8_t*>(a.k);
+      const uint8_t* v8 = reinterpret_cast<const uint8_t*>(a.v);
+      uint8_t* sk = smem + L::kF8Base + stage * 2 * L::kF8Tile;
+      uint8_t* sv = sk + L::kF8Tile;
+#pragma unroll
+      for (int x = threadIdx.x; x < kTileKeys * kC16; x += kThreads) {
+        const int key = x / kC16, c = x % kC16;
+        const int kabs = kt0 + key;
+        const bool ok = kabs < kend;
+        int64_t off = 0;
+        if (ok) {
+          const int blk = __ldg(bt_row + kabs / kPage);
+          off = ((static_cast<int64_t>(blk) * kPage + kabs % kPage) * a.num_kv_heads + g) * D +
+                c * 16;
+        }
+        cp_async_16(sk + key * D + c * 16, k8 + off, ok ? 16u : 0u);
+        cp_async_16(sv + key * D + c * 16, v8 + off, ok ? 16u : 0u);
+      }
+      return;
+    }
     uint8_t* sk = smem + L::kK + stage * L::kKVBytes;
     uint8_t* sv = smem + L::kV + stage * L::kKVBytes;
 #pragma unroll
@@ -162,8 +193,27 @@ __global__ void __launch_bounds__(kThreads)
         ldmatrix_x4(sbase + L::kQ + swz<D>(row, c), qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3]);
       }
     }
+    if constexpr (kF8) {
+      // widen tile ti into the f16 K/V buffer (every warp finished tile ti - 1)
+      constexpr int kC16 = D / 16;
+      const uint8_t* src = smem + L::kF8Base + (ti % kStages) * 2 * L::kF8Tile;
+#pragma unroll 2
+      for (int x = threadIdx.x; x < 2 * kTileKeys * kC16; x += kThreads) {
+        const bool is_v = x >= kTileKeys * kC16;
+        const int y = is_v ? x - kTileKeys * kC16 : x;
+        const int key = y / kC16, c = y % kC16;
+        const uint4 raw =
+            *reinterpret_cast<const uint4*>(src + (is_v ? L::kF8Tile : 0) + key * D + c * 16);
+        uint4 lo, hi;
+        e4m3x16_to_f16(raw, lo, hi);
+        uint8_t* dst = smem + (is_v ? L::kV : L::kK);
+        *reinterpret_cast<uint4*>(dst + swz<D>(key, 2 * c)) = lo;
+        *reinterpret_cast<uint4*>(dst + swz<D>(key, 2 * c + 1)) = hi;
+      }
+      __syncthreads();
+    }
     {
-    const int stage = ti % kStages;
+    const int stage = kF8 ? 0 : ti % kStages;
     const uint32_t sk = sbase + L::kK + stage * L::kKVBytes;
     const uint32_t sv = sbase + L::kV + stage * L::kKVBytes;
     const int kt0 = kbeg + ti * kTileKeys;
@@ -180,8 +230,13 @@ __global__ void __launch_bounds__(kThreads)
         const int c = kk * 2 + ((lane >> 3) & 1);
         uint32_t b0, b1, b2, b3;
         ldmatrix_x4(sk + swz<D>(key, c), b0, b1, b2, b3);
-        mma_bf16_16816(sacc[2 * np], qa[kk], b0, b1);
-        mma_bf16_16816(sacc[2 * np + 1], qa[kk], b2, b3);
+        if constexpr (kF8) {
+          mma_f16_16816(sacc[2 * np], qa[kk], b0, b1);
+          mma_f16_16816(sacc[2 * np + 1], qa[kk], b2, b3);
+        } else {
+          mma_bf16_16816(sacc[2 * np], qa[kk], b0, b1);
+          mma_bf16_16816(sacc[2 * np + 1], qa[kk], b2, b3);
+        }
       }
     }
     // mask, online softmax (base 2)
@@ -225,18 +280,24 @@ __global__ void __launch_bounds__(kThreads)
 #pragma unroll
     for (int kk = 0; kk < kWarpKeys / 16; ++kk) {
       uint32_t pa[4];
-      pa[0] = pack_bf16x2(sacc[2 * kk][0], sacc[2 * kk][1]);
-      pa[1] = pack_bf16x2(sacc[2 * kk][2], sacc[2 * kk][3]);
-      pa[2] = pack_bf16x2(sacc[2 * kk + 1][0], sacc[2 * kk + 1][1]);
-      pa[3] = pack_bf16x2(sacc[2 * kk + 1][2], sacc[2 * kk + 1][3]);
+      auto pack = [](float x, float y) { return kF8 ? pack_f16x2(x, y) : pack_bf16x2(x, y); };
+      pa[0] = pack(sacc[2 * kk][0], sacc[2 * kk][1]);
+      pa[1] = pack(sacc[2 * kk][2], sacc[2 * kk][3]);
+      pa[2] = pack(sacc[2 * kk + 1][0], sacc[2 * kk + 1][1]);
+      pa[3] = pack(sacc[2 * kk + 1][2], sacc[2 * kk + 1][3]);
 #pragma unroll
       for (int dp = 0; dp < kDT / 2; ++dp) {
         const int key = kw0 + kk * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
         const int c = dp * 2 + (lane >> 4);
         uint32_t b0, b1, b2, b3;
         ldmatrix_x4_trans(sv + swz<D>(key, c), b0, b1, b2, b3);
-        mma_bf16_16816(o[2 * dp], pa, b0, b1);
-        mma_bf16_16816(o[2 * dp + 1], pa, b2, b3);
+        if constexpr (kF8) {
+          mma_f16_16816(o[2 * dp], pa, b0, b1);
+          mma_f16_16816(o[2 * dp + 1], pa, b2, b3);
+        } else {
+          mma_bf16_16816(o[2 * dp], pa, b0, b1);
+          mma_bf16_16816(o[2 * dp + 1], pa, b2, b3);
+        }
       }
     }
     }
@@ -315,8 +376,9 @@ __global__ void __launch_bounds__(kThreads)
         const float mw = s_m[w * 16 + rr];
         lsum += (mw == -INFINITY) ? 0.f : s_l[w * 16 + rr] * exp2f(mw - mg);
       }
-      const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
-      const float lse2 = lsum > 0.f ? mg + log2f(lsum) : -INFINITY;
+      float inv = !(lsum <= 0.f) ? 1.f / lsum : 0.f;  // a NaN sum propagates
+      if constexpr (kF8) inv *= a.v_scale;
+      const float lse2 = !(lsum <= 0.f) ? mg + log2f(lsum) : -INFINITY;
       const int qi = rho / a.group, j = rho % a.group;
       const int64_t orow = static_cast<int64_t>(q0 + qi) * a.num_q_heads + g * a.group + j;
       float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -355,12 +417,12 @@ __global__ void __launch_bounds__(kThreads)
   }
 }
 
-template <int D>
+template <int D, bool kF8>
 cudaError_t launch_paged_t(const PagedArgs& a, bool after_prefix, cudaStream_t stream) {
-  using L = PagedLayout<D>;
+  using L = PagedLayout<D, kF8>;
   const int smem = L::kEnd;
   static std::atomic<uint64_t> attr_done{0};
-  cudaError_t e = set_smem_once(paged_attn_kernel<D>, smem, attr_done);
+  cudaError_t e = set_smem_once(paged_attn_kernel<D, kF8>, smem, attr_done);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(a.num_reqs * a.row_tiles, a.num_kv_heads, a.n_splits);
@@ -374,15 +436,21 @@ cudaError_t launch_paged_t(const PagedArgs& a, bool after_prefix, cudaStream_t s
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = after_prefix ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, paged_attn_kernel<D>, a);
+  return cudaLaunchKernelEx(&cfg, paged_attn_kernel<D, kF8>, a);
 }
 
 }  // namespace
 
 cudaError_t launch_paged(int head_dim, const PagedArgs& a, bool after_prefix,
                          cudaStream_t stream) {
-  if (head_dim == 64) return launch_paged_t<64>(a, after_prefix, stream);
-  return launch_paged_t<128>(a, after_prefix, stream);
+  if (head_dim == 64) return launch_paged_t<64, false>(a, after_prefix, stream);
+  return launch_paged_t<128, false>(a, after_prefix, stream);
+}
+
+cudaError_t launch_paged_f8(int head_dim, const PagedArgs& a, bool after_prefix,
+                            cudaStream_t stream) {
+  if (head_dim == 64) return launch_paged_t<64, true>(a, after_prefix, stream);
+  return launch_paged_t<128, true>(a, after_prefix, stream);
 }
 
 }  // namespace csp

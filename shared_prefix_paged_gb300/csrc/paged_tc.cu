@@ -30,17 +30,18 @@ using prefix::kThreads;
 
 // Dynamic shared memory: the data area, the barrier area, and slack to align the
 // base to 1024 bytes (128-byte swizzled tiles).
-template <int D>
-constexpr int kDynamic = Layout<D>::kData + prefix::kBarBytes + 1024;
+template <int D, bool kF8 = false>
+constexpr int kDynamic = Layout<D, kF8>::kData + prefix::kBarBytes + 1024;
 
 // One CTA of the suffix (or standard-path) grid: request row tile bx (request
 // bx / row_tiles), KV head g, key split `split`.
-template <int D>
+template <int D, bool kF8 = false>
 __device__ __forceinline__ void tc_suffix_cta(const CUtensorMap* tm_q, const CUtensorMap* tm_k,
                                               const CUtensorMap* tm_v, const PagedArgs& a,
                                               int bx, int g, int split, uint8_t* smem,
                                               uint64_t* bars) {
-  using L = Layout<D>;
+  using L = Layout<D, kF8>;
+  constexpr int kNThreads = kF8 ? prefix::kThreadsF8 : kThreads;
   const int r = bx / a.row_tiles;
   const int rt = bx % a.row_tiles;
   const int q0 = __ldg(a.cu_seqlens_q + r);
@@ -78,6 +79,7 @@ __device__ __forceinline__ void tc_suffix_cta(const CUtensorMap* tm_q, const CUt
   pa.part_lse = nullptr;
   pa.lse_stride = 0;
   pa.status = a.status;
+  pa.v_scale = a.v_scale;
   prefix::RangeGeom geo;
   geo.bt = a.block_table + static_cast<int64_t>(r) * a.bt_stride;
   geo.key0 = kbeg;
@@ -86,7 +88,7 @@ __device__ __forceinline__ void tc_suffix_cta(const CUtensorMap* tm_q, const CUt
   geo.prow0 = prow0;
   geo.rows_total = rows_total;
   geo.causal_base = seq - q_len;
-  prefix::prefix_range<D, true>(tm_q, tm_k, tm_v, pa, geo, g, split, 0, ntiles, smem, bars);
+  prefix::prefix_range<D, true, kF8>(tm_q, tm_k, tm_v, pa, geo, g, split, 0, ntiles, smem, bars);
 
   // 256 normalised rows (bf16) and their log2-sum-exp are staged and visible
   const __nv_bfloat16* stage = reinterpret_cast<const __nv_bfloat16*>(smem);
@@ -100,7 +102,7 @@ __device__ __forceinline__ void tc_suffix_cta(const CUtensorMap* tm_q, const CUt
            (rho & (a.group - 1));
   };
   // the final rows (standard path, one split) or this split's partial slot
-  for (int it = threadIdx.x; it < rows_here * kChunks; it += kThreads) {
+  for (int it = threadIdx.x; it < rows_here * kChunks; it += kNThreads) {
     const int rr = it / kChunks, c = it % kChunks;
     const int64_t orow = out_row(rr);
     const uint4 v = *reinterpret_cast<const uint4*>(stage + rr * L::kStageRow + c * 8);
@@ -140,16 +142,17 @@ __device__ __forceinline__ void tc_suffix_cta(const CUtensorMap* tm_q, const CUt
                            s_w);
 }
 
-template <int D>
-__global__ void __launch_bounds__(kThreads, 1)
+template <int D, bool kF8>
+__global__ void __launch_bounds__(kF8 ? prefix::kThreadsF8 : kThreads, 1)
     paged_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                     const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const PagedArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Layout<D>::kData);
-  tc_suffix_cta<D>(&tm_q, &tm_k, &tm_v, a, blockIdx.x, blockIdx.y, blockIdx.z, smem, bars);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Layout<D, kF8>::kData);
+  tc_suffix_cta<D, kF8>(&tm_q, &tm_k, &tm_v, a, blockIdx.x, blockIdx.y, blockIdx.z, smem,
+                        bars);
 }
 
 // The whole cascade step in one launch (prefill-shaped batches): CTAs [0, n_pre) are
@@ -235,17 +238,17 @@ cudaError_t launch_fused_t(const CUtensorMap& tm_q, const CUtensorMap& tm_k,
   return cudaLaunchKernelEx(&cfg, cascade_fused_kernel<D>, tm_q, tm_k, tm_v, pa, ga, n_pre);
 }
 
-template <int D>
+template <int D, bool kF8>
 cudaError_t launch_tc_t(const CUtensorMap& tm_q, const CUtensorMap& tm_k,
                         const CUtensorMap& tm_v, const PagedArgs& a, bool after_prefix,
                         cudaStream_t stream) {
   static std::atomic<uint64_t> attr_done{0};
-  cudaError_t e = set_smem_once(paged_tc_kernel<D>, kDynamic<D>, attr_done);
+  cudaError_t e = set_smem_once(paged_tc_kernel<D, kF8>, kDynamic<D, kF8>, attr_done);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(a.num_reqs * a.row_tiles, a.num_kv_heads, a.n_splits);
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = kDynamic<D>;
+  cfg.blockDim = dim3(kF8 ? prefix::kThreadsF8 : kThreads);
+  cfg.dynamicSmemBytes = kDynamic<D, kF8>;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   // behind this call's prefix kernel: start on the SMs it leaves free; the merge
@@ -254,7 +257,7 @@ cudaError_t launch_tc_t(const CUtensorMap& tm_q, const CUtensorMap& tm_k,
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = after_prefix ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, paged_tc_kernel<D>, tm_q, tm_k, tm_v, a);
+  return cudaLaunchKernelEx(&cfg, paged_tc_kernel<D, kF8>, tm_q, tm_k, tm_v, a);
 }
 
 }  // namespace
@@ -271,8 +274,15 @@ cudaError_t launch_cascade_fused(int head_dim, const CUtensorMap& tm_q, const CU
 cudaError_t launch_paged_tc(int head_dim, const CUtensorMap& tm_q, const CUtensorMap& tm_k,
                             const CUtensorMap& tm_v, const PagedArgs& a, bool after_prefix,
                             cudaStream_t stream) {
-  if (head_dim == 64) return launch_tc_t<64>(tm_q, tm_k, tm_v, a, after_prefix, stream);
-  return launch_tc_t<128>(tm_q, tm_k, tm_v, a, after_prefix, stream);
+  if (head_dim == 64) return launch_tc_t<64, false>(tm_q, tm_k, tm_v, a, after_prefix, stream);
+  return launch_tc_t<128, false>(tm_q, tm_k, tm_v, a, after_prefix, stream);
+}
+
+cudaError_t launch_paged_tc_f8(int head_dim, const CUtensorMap& tm_q, const CUtensorMap& tm_k,
+                               const CUtensorMap& tm_v, const PagedArgs& a, bool after_prefix,
+                               cudaStream_t stream) {
+  if (head_dim == 64) return launch_tc_t<64, true>(tm_q, tm_k, tm_v, a, after_prefix, stream);
+  return launch_tc_t<128, true>(tm_q, tm_k, tm_v, a, after_prefix, stream);
 }
 
 }  // namespace csp

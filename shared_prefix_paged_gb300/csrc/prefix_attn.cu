@@ -13,18 +13,20 @@ using prefix::kThreads;
 
 // Dynamic shared memory: the data area, the barrier area, and slack to align the
 // base to 1024 bytes (128-byte swizzled TMA tiles).
-template <int D>
-constexpr int kDynamic = Layout<D>::kData + prefix::kBarBytes + 1024;
+template <int D, bool kF8 = false>
+constexpr int kDynamic = Layout<D, kF8>::kData + prefix::kBarBytes + 1024;
 
-template <int D>
-__global__ void __launch_bounds__(kThreads, 1)
+// kF8: an E4M3 KV cache (tm_k and tm_v its byte maps, tm_q the f16 queries), with two
+// more warps that widen each tile.
+template <int D, bool kF8>
+__global__ void __launch_bounds__(kF8 ? prefix::kThreadsF8 : kThreads, 1)
     prefix_attn_kernel(const __grid_constant__ CUtensorMap tm_q,
                        const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, const PrefixArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Layout<D>::kData);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Layout<D, kF8>::kData);
   // the suffix kernel (launched as a programmatic dependent) may start now; it reads
   // this grid's partials only after waiting for the grid to complete
   grid_launch_dependents();
@@ -34,8 +36,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int key_tiles = (a.cpl - a.key_lo + prefix::kKeysN - 1) / prefix::kKeysN;
   const int t_first = min(split * a.tiles_per_split, key_tiles);
   const int t_last = min(t_first + a.tiles_per_split, key_tiles);
-  prefix::prefix_range<D>(&tm_q, &tm_k, &tm_v, a, prefix::prefix_geom(a, pair), kvh, split,
-                          t_first, t_last, smem, bars);
+  prefix::prefix_range<D, false, kF8>(&tm_q, &tm_k, &tm_v, a, prefix::prefix_geom(a, pair),
+                                      kvh, split, t_first, t_last, smem, bars);
 }
 
 // Every segment of a multi-level cascade in one grid: a CTA finds its segment in the
@@ -78,33 +80,33 @@ __global__ void __launch_bounds__(kThreads, 1)
                           t_first, t_last, smem, bars);
 }
 
-template <int D>
+template <int D, bool kF8>
 cudaLaunchConfig_t prefix_config(const PrefixArgs& a, cudaStream_t stream,
                                  cudaLaunchAttribute* attr) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(a.n_splits * a.pairs * a.num_kv_heads);
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = kDynamic<D>;
+  cfg.blockDim = dim3(kF8 ? prefix::kThreadsF8 : kThreads);
+  cfg.dynamicSmemBytes = kDynamic<D, kF8>;
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 0;
   return cfg;
 }
 
-template <int D>
+template <int D, bool kF8>
 cudaError_t prepare() {
   static std::atomic<uint64_t> attr_done{0};
-  return set_smem_once(prefix_attn_kernel<D>, kDynamic<D>, attr_done);
+  return set_smem_once(prefix_attn_kernel<D, kF8>, kDynamic<D, kF8>, attr_done);
 }
 
-template <int D>
+template <int D, bool kF8>
 cudaError_t launch_prefix_d(const CUtensorMap& tm_q, const CUtensorMap& tm_k,
                             const CUtensorMap& tm_v, const PrefixArgs& a, cudaStream_t stream) {
-  cudaError_t e = prepare<D>();
+  cudaError_t e = prepare<D, kF8>();
   if (e != cudaSuccess) return e;
   cudaLaunchAttribute attr[1];
-  cudaLaunchConfig_t cfg = prefix_config<D>(a, stream, attr);
-  return cudaLaunchKernelEx(&cfg, prefix_attn_kernel<D>, tm_q, tm_k, tm_v, a);
+  cudaLaunchConfig_t cfg = prefix_config<D, kF8>(a, stream, attr);
+  return cudaLaunchKernelEx(&cfg, prefix_attn_kernel<D, kF8>, tm_q, tm_k, tm_v, a);
 }
 
 template <int D>
@@ -135,8 +137,14 @@ cudaError_t launch_prefix_segments(int head_dim, const CUtensorMap& tm_q,
 
 cudaError_t launch_prefix(int head_dim, const CUtensorMap& tm_q, const CUtensorMap& tm_k,
                           const CUtensorMap& tm_v, const PrefixArgs& a, cudaStream_t stream) {
-  if (head_dim == 64) return launch_prefix_d<64>(tm_q, tm_k, tm_v, a, stream);
-  return launch_prefix_d<128>(tm_q, tm_k, tm_v, a, stream);
+  if (head_dim == 64) return launch_prefix_d<64, false>(tm_q, tm_k, tm_v, a, stream);
+  return launch_prefix_d<128, false>(tm_q, tm_k, tm_v, a, stream);
+}
+
+cudaError_t launch_prefix_f8(int head_dim, const CUtensorMap& tm_q, const CUtensorMap& tm_k,
+                             const CUtensorMap& tm_v, const PrefixArgs& a, cudaStream_t stream) {
+  if (head_dim == 64) return launch_prefix_d<64, true>(tm_q, tm_k, tm_v, a, stream);
+  return launch_prefix_d<128, true>(tm_q, tm_k, tm_v, a, stream);
 }
 
 }  // namespace csp

@@ -42,11 +42,17 @@ constexpr int kPage = 16;      // tokens per KV page
 constexpr int kPagesPerTile = kKeysN / kPage;
 constexpr int kStages = 4;
 constexpr int kThreads = 352;  // 2 softmax warpgroups, two MMA issuers, the K/V loader
+// An FP8 (E4M3) KV cache: the loader warp and one more warp widen each tile to f16
+// (exact: E4M3 is a subset of f16) for MMAs with f16 operands.
+constexpr int kThreadsF8 = 384;
+constexpr int kWarpConv = 11;
+constexpr int kF8Stages = 4;   // E4M3 tiles in flight (the f16 ring is then 2 deep)
 constexpr int kWarpMma = 8;
 constexpr int kWarpTma = 9;    // Q by TMA, then the MMA issuer of M tile 1
 constexpr int kWarpLoad = 10;  // K and V by TMA
-template <int D>
+template <int D, bool kF8 = false>
 struct Layout {
+  static constexpr int kStagesL = kF8 ? 2 : kStages;    // 16-bit K/V tiles in the ring
   static constexpr int kHalves = D / 64;
   static constexpr int kQHalf = kRowsM * 128;           // 128 rows x 64 bf16
   static constexpr int kKVHalf = kKeysN * 128;          // 64 keys x 64 bf16
@@ -55,8 +61,12 @@ struct Layout {
   static constexpr int kVPage = kPage * D * 2;          // one page of V: both halves
   static constexpr int kQ = 0;                          // [2 M tiles][halves]
   static constexpr int kK0 = kQ + 2 * kQTile;
-  static constexpr int kV0 = kK0 + kStages * kKVBytes;
-  static constexpr int kRing = kV0 + kStages * kKVBytes;
+  static constexpr int kV0 = kK0 + kStagesL * kKVBytes;
+  // E4M3 tiles as loaded: K [64 keys][D bytes], then V the same, per stage
+  static constexpr int kF8Tile = kKeysN * D;
+  static constexpr int kF8Stage = 2 * kF8Tile;
+  static constexpr int kF8Ring = kV0 + kStagesL * kKVBytes;
+  static constexpr int kRing = kF8Ring + (kF8 ? kF8Stages * kF8Stage : 0);
   // after the main loop, [0, kRing) stages the CTA's 256 normalised rows:
   // [row][D + 8] bf16 (the padding spreads the rows one warp writes over all banks)
   static constexpr int kStageRow = D + 8;
@@ -65,7 +75,8 @@ struct Layout {
   static constexpr int kData = kLse + kRowsCta * 4;     // end of the data area
 };
 
-// Bytes of the caller's barrier area: 15 mbarriers, the TMEM slot and the abort flag.
+// Bytes of the caller's barrier area: up to 25 mbarriers, the TMEM slot and the abort
+// flag.
 constexpr int kBarBytes = 256;
 
 // Where one CTA's rows and keys come from.  The prefix phase: the rows are every
@@ -123,25 +134,36 @@ __device__ __forceinline__ bool wg_bar_any(int id, bool pred) {
 // tm_k: the K cache as {D, Hkv, tokens} with boxes {64, 1, 16} (one page, one half);
 // tm_v: the V cache as {64, tokens, D / 64, Hkv} with boxes {64, 16, D / 64, 1} (one
 // page, both halves); both with the 128-byte swizzle.
-template <int D, bool kCausal = false>
+template <int D, bool kCausal = false, bool kF8 = false>
 __device__ __forceinline__ void prefix_range(const CUtensorMap* tm_q_p,
                                              const CUtensorMap* tm_k_p,
                                              const CUtensorMap* tm_v_p, const PrefixArgs& a,
                                              const RangeGeom& geo, int kvh, int split,
                                              int t_first, int t_last, uint8_t* smem,
                                              uint64_t* bars) {
-  using L = Layout<D>;
+  using L = Layout<D, kF8>;
+  constexpr int kS = L::kStagesL;
+  constexpr int kNThreads = kF8 ? kThreadsF8 : kThreads;
   const CUtensorMap& tm_q = *tm_q_p;
   const CUtensorMap& tm_k = *tm_k_p;
   const CUtensorMap& tm_v = *tm_v_p;
   uint64_t* bar_q = bars + 0;
-  uint64_t* kv_full = bars + 1;   // [kStages]
-  uint64_t* kv_empty = bars + 1 + kStages;  // [kStages]
-  uint64_t* s_full = bars + 1 + 2 * kStages;    // [2 tiles][2 buffers]
-  uint64_t* p_full = bars + 5 + 2 * kStages;    // [2 tiles][2 buffers]
-  uint64_t* o_last = bars + 11 + 2 * kStages;   // [2 tiles] the last PV (9, 10 unused)
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 13 + 2 * kStages);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 14 + 2 * kStages);
+  uint64_t* kv_full = bars + 1;   // [kS]
+  uint64_t* kv_empty = bars + 1 + kS;  // [kS]
+  uint64_t* s_full = bars + 1 + 2 * kS;    // [2 tiles][2 buffers]
+  uint64_t* p_full = bars + 5 + 2 * kS;    // [2 tiles][2 buffers]
+  uint64_t* o_last = bars + 11 + 2 * kS;   // [2 tiles] the last PV (9, 10 unused)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 13 + 2 * kS);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 14 + 2 * kS);
+  uint64_t* f8_full = bars + 15 + 2 * kS;   // [kF8Stages] E4M3 tiles landed (kF8)
+  uint64_t* f8_empty = bars + 19 + 2 * kS;  // [kF8Stages] E4M3 tiles widened (kF8)
+  uint64_t* tail_in = bars + 15 + 2 * kS;   // bf16: the last tile landed (see the loader)
+  // A range that ends inside a page (a request's last page) leaves slots past its end
+  // in that page: whatever the cache holds there (NaN included) would reach O through
+  // P = 0 times V in the MMA, so those V rows are zeroed before the PV reads them.
+  const bool ragged_end = kCausal && (geo.key_end % kPage) != 0;
+  static_assert((kF8 ? 23 + 2 * kS : 15 + 2 * kS) * 8 <= kBarBytes, "barrier area");
+  static_assert(!kF8 || kWarpConv * 32 + 32 == kThreadsF8, "the converter warp is the last");
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -159,9 +181,19 @@ __device__ __forceinline__ void prefix_range(const CUtensorMap* tm_q_p,
 
   if (threadIdx.x == 0) {
     mbar_init(bar_q, 1);
-    for (int s = 0; s < kStages; ++s) {
-      mbar_init(&kv_full[s], 1);  // the loader's expect_tx; the TMA bytes complete it
+    for (int s = 0; s < kS; ++s) {
+      // bf16: the loader's expect_tx, the TMA bytes complete it; E4M3: every thread
+      // of the two converter warps
+      mbar_init(&kv_full[s], kF8 ? 64 : 1);
       mbar_init(&kv_empty[s], has_m1 ? 2 : 1);  // one commit per M tile's issuer
+    }
+    if constexpr (kF8) {
+      for (int s = 0; s < kF8Stages; ++s) {
+        mbar_init(&f8_full[s], 1);    // the loader's expect_tx
+        mbar_init(&f8_empty[s], 64);  // every converter thread
+      }
+    } else {
+      mbar_init(tail_in, 1);
     }
     for (int b = 0; b < 4; ++b) {
       mbar_init(&s_full[b], 1);
@@ -201,12 +233,13 @@ __device__ __forceinline__ void prefix_range(const CUtensorMap* tm_q_p,
   // commit per issuer).
   if ((warp == kWarpMma || (warp == kWarpTma && has_m1)) && lane == 0 && ntiles > 0) {
     const int m = warp == kWarpMma ? 0 : 1;
-    constexpr uint32_t kIdS = umma_idesc_bf16(128, kKeysN, 0, 0);
-    constexpr uint32_t kIdO = umma_idesc_bf16(128, D, 0, 1);
+    constexpr uint32_t kIdS =
+        kF8 ? umma_idesc_f16(128, kKeysN, 0, 0) : umma_idesc_bf16(128, kKeysN, 0, 0);
+    constexpr uint32_t kIdO = kF8 ? umma_idesc_f16(128, D, 0, 1) : umma_idesc_bf16(128, D, 0, 1);
     const uint32_t q_addr = smem_u32(smem + L::kQ + m * L::kQTile);
     const uint32_t tm = tmem + m * 256;
     auto issue_s = [&](int i) {
-      const uint32_t k_addr = smem_u32(smem + L::kK0 + (i % kStages) * L::kKVBytes);
+      const uint32_t k_addr = smem_u32(smem + L::kK0 + (i % kS) * L::kKVBytes);
       const uint32_t d = tm + (i & 1) * kKeysN;
 #pragma unroll
       for (int k = 0; k < D / 16; ++k) {
@@ -224,7 +257,7 @@ __device__ __forceinline__ void prefix_range(const CUtensorMap* tm_q_p,
     while (ok && next_pv < ntiles) {
       bool progressed = false;
       if (next_s < ntiles && next_s <= next_pv + 1 &&
-          mbar_test_wait(&kv_full[next_s % kStages], (next_s / kStages) & 1)) {
+          mbar_test_wait(&kv_full[next_s % kS], (next_s / kS) & 1)) {
         tc_fence_after();
         issue_s(next_s);
         ++next_s;
@@ -234,7 +267,7 @@ __device__ __forceinline__ void prefix_range(const CUtensorMap* tm_q_p,
           mbar_test_wait(&p_full[m * 2 + (next_pv & 1)], (next_pv >> 1) & 1)) {
         tc_fence_after();
         const int i = next_pv;
-        const uint32_t v_addr = smem_u32(smem + L::kV0 + (i % kStages) * L::kKVBytes);
+        const uint32_t v_addr = smem_u32(smem + L::kV0 + (i % kS) * L::kKVBytes);
         const uint32_t p_tmem = tm + (i & 1) * kKeysN;
 #pragma unroll
         for (int kk = 0; kk < kKeysN / 16; ++kk)  // 16 keys = one page of V
@@ -242,7 +275,7 @@ __device__ __forceinline__ void prefix_range(const CUtensorMap* tm_q_p,
                            umma_desc_sw128(v_addr + kk * L::kVPage, kPage * 128, 1024), kIdO,
                            (i > 0 || kk > 0) ? 1u : 0u);
         if (i == ntiles - 1) umma_commit(&o_last[m]);
-        umma_commit(&kv_empty[i % kStages]);
+        umma_commit(&kv_empty[i % kS]);
         ++next_pv;
         progressed = true;
       }
@@ -268,7 +301,7 @@ __device__ __forceinline__ void prefix_range(const CUtensorMap* tm_q_p,
   // read a window ahead.  A page wholly past the range is loaded from an out-of-range
   // token coordinate: TMA fills it with zeros (no NaN from a page the cache never
   // wrote can reach O).
-  if (warp == kWarpLoad && ntiles > 0) {
+  if (!kF8 && warp == kWarpLoad && ntiles > 0) {
     constexpr int kIdTiles = 32 / kPagesPerTile;
     constexpr int kKBoxes = kPagesPerTile * L::kHalves;
     const int npages = (geo.key_end - geo.key0 + kPage - 1) / kPage;
@@ -282,15 +315,18 @@ __device__ __forceinline__ void prefix_range(const CUtensorMap* tm_q_p,
     int ids_nxt = ntiles > kIdTiles ? load_ids(kIdTiles) : -1;
     int issued = 0;
     for (int j = 0; j < ntiles; ++j) {
-      const int st = j % kStages;
-      if (j >= kStages &&
-          !warp_mbar_wait(&kv_empty[st], ((j / kStages) - 1) & 1, abort_flag, a.status))
+      const int st = j % kS;
+      if (j >= kS && !warp_mbar_wait(&kv_empty[st], ((j / kS) - 1) & 1, abort_flag, a.status))
         break;
       if (j > 0 && j % kIdTiles == 0) {
         ids_cur = ids_nxt;
         ids_nxt = j + kIdTiles < ntiles ? load_ids(j + kIdTiles) : -1;
       }
-      if (lane == 0) mbar_arrive_expect_tx(&kv_full[st], 2 * L::kKVBytes);
+      // a ragged last tile lands on tail_in; the warp zeroes its slots past the range
+      // and then releases the stage (below)
+      const bool fix = ragged_end && j == ntiles - 1;
+      uint64_t* land = fix ? tail_in : &kv_full[st];
+      if (lane == 0) mbar_arrive_expect_tx(land, 2 * L::kKVBytes);
       __syncwarp();
       // lanes [0, kKBoxes): K page lane / halves, half lane % halves; then one lane per
       // page of V
@@ -301,24 +337,156 @@ __device__ __forceinline__ void prefix_range(const CUtensorMap* tm_q_p,
       if (is_k) {
         const int h = lane % L::kHalves;
         tma_load_3d(smem + L::kK0 + st * L::kKVBytes + h * L::kKVHalf + q * (kPage * 128),
-                    &tm_k, &kv_full[st], h * 64, kvh, tok);
+                    &tm_k, land, h * 64, kvh, tok);
       } else if (lane < kKBoxes + kPagesPerTile) {
-        tma_load_4d(smem + L::kV0 + st * L::kKVBytes + q * L::kVPage, &tm_v, &kv_full[st], 0,
-                    tok, 0, kvh);
+        tma_load_4d(smem + L::kV0 + st * L::kKVBytes + q * L::kVPage, &tm_v, land, 0, tok, 0,
+                    kvh);
+      }
+      if (fix) {
+        // V rows of keys [key_end, the end of its page) of this tile: zero, made
+        // visible to the tensor core's proxy, then the stage is released
+        if (!warp_mbar_wait(tail_in, 0, abort_flag, a.status)) {
+          if (lane == 0) {
+            const long long c0 = clock64();
+            while (!mbar_try_wait(tail_in, 0) && clock64() - c0 < kWaitLimitCycles) {
+            }
+          }
+          __syncwarp();
+          break;
+        }
+        const int kt = geo.key_end - (geo.key0 + tile_of(j) * kKeysN);  // first key to clear
+        const int page = kt / kPage, r0 = kt % kPage;
+        const int n16 = (kPage - r0) * L::kHalves * 8;                  // 16-byte pieces
+        for (int x = lane; x < n16; x += 32) {
+          const int r = r0 + x / (L::kHalves * 8);
+          const int h = (x / 8) % L::kHalves;
+          *reinterpret_cast<uint4*>(smem + L::kV0 + st * L::kKVBytes + page * L::kVPage +
+                                    h * (kPage * 128) + r * 128 + (x % 8) * 16) =
+              make_uint4(0u, 0u, 0u, 0u);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&kv_full[st]);
+        issued = j;  // its copies have landed
+        break;
       }
       issued = j + 1;
     }
     // after a failure the last tiles' copies may still be landing: they must land
     // before this CTA's shared memory is reused or released (a bounded wait each)
     if (lane == 0) {
-      for (int j = issued > kStages ? issued - kStages : 0; j < issued; ++j) {
+      for (int j = issued > kS ? issued - kS : 0; j < issued; ++j) {
         const long long c0 = clock64();
-        while (!mbar_try_wait(&kv_full[j % kStages], (j / kStages) & 1) &&
+        while (!mbar_try_wait(&kv_full[j % kS], (j / kS) & 1) &&
                clock64() - c0 < kWaitLimitCycles) {
         }
       }
     }
     __syncwarp();
+  }
+  // ------------------------------------------ E4M3 loader (TMA) and widening --
+  // The loader brings tile j's E4M3 pages (K [16 keys][D bytes] per page, then V) into
+  // stage j % kF8Stages once the converters are done with tile j - kF8Stages; the two
+  // converter warps widen tile j into f16 ring stage j % 2 (the 128-byte swizzled
+  // layout TMA writes for 16-bit tiles) once PV(j - 2) of every M tile is done, make
+  // the writes visible to the tensor core's proxy and arrive on kv_full.
+  if constexpr (kF8) {
+    // widen this warp's half (part 0: the loader, 1: warp kWarpConv) of tile j
+    auto widen = [&](int j, int part) -> bool {
+      const int f = j % kF8Stages, st = j % kS;
+      if (!warp_mbar_wait(&f8_full[f], (j / kF8Stages) & 1, abort_flag, a.status)) return false;
+      if (j >= kS && !warp_mbar_wait(&kv_empty[st], ((j / kS) - 1) & 1, abort_flag, a.status))
+        return false;
+      constexpr int kC16 = D / 16;  // 16-byte E4M3 chunks per key
+      constexpr int kTileChunks = kKeysN * kC16;
+      const uint8_t* src = smem + L::kF8Ring + f * L::kF8Stage;
+#pragma unroll 4
+      for (int x = part * 32 + lane; x < 2 * kTileChunks; x += 64) {
+        const bool is_v = x >= kTileChunks;
+        const int y = is_v ? x - kTileChunks : x;
+        const int key = y / kC16, c16 = y % kC16;
+        const uint4 raw =
+            *reinterpret_cast<const uint4*>(src + (is_v ? L::kF8Tile : 0) + key * D + c16 * 16);
+        uint4 lo, hi;
+        e4m3x16_to_f16(raw, lo, hi);
+        if (is_v && geo.key0 + tile_of(j) * kKeysN + key >= geo.key_end) {
+          // a slot past the range (a ragged last page): zero, not the cache's bytes
+          lo = make_uint4(0u, 0u, 0u, 0u);
+          hi = lo;
+        }
+        // features [16 c16, 16 c16 + 16): half c16 / 4, 16-byte chunks 2 (c16 % 4) + {0, 1}
+        const int h = c16 >> 2, c8 = (c16 & 3) * 2;
+        const int row = is_v ? L::kV0 + st * L::kKVBytes + (key / kPage) * L::kVPage +
+                                   h * (kPage * 128) + (key % kPage) * 128
+                             : L::kK0 + st * L::kKVBytes + h * L::kKVHalf + key * 128;
+        const int sw = (row >> 7) & 7;
+        *reinterpret_cast<uint4*>(smem + row + ((c8 ^ sw) << 4)) = lo;
+        *reinterpret_cast<uint4*>(smem + row + (((c8 + 1) ^ sw) << 4)) = hi;
+      }
+      fence_proxy_async_smem();
+      mbar_arrive(&kv_full[st]);
+      mbar_arrive(&f8_empty[f]);
+      return true;
+    };
+    if (warp == kWarpLoad && ntiles > 0) {
+      // step t: load tile t, then widen tile t - (kF8Stages - 1); the load of tile t
+      // waits for the widening of tile t - kF8Stages, which this warp did a step
+      // earlier and warp kWarpConv does on its own
+      constexpr int kLag = kF8Stages - 1;
+      constexpr int kIdTiles = 32 / kPagesPerTile;
+      const int npages = (geo.key_end - geo.key0 + kPage - 1) / kPage;
+      const int32_t* bt_pages = geo.bt + geo.key0 / kPage;
+      auto load_ids = [&](int i_base) {
+        const int i = i_base + lane / kPagesPerTile;
+        const int page = tile_of(i) * kPagesPerTile + (lane & (kPagesPerTile - 1));
+        return i < ntiles && page < npages ? __ldg(bt_pages + page) : -1;
+      };
+      int ids_cur = load_ids(0);
+      int ids_nxt = ntiles > kIdTiles ? load_ids(kIdTiles) : -1;
+      int issued = 0;
+      bool ok = true;
+      for (int t = 0; ok && t < ntiles + kLag; ++t) {
+        if (t < ntiles) {
+          const int f = t % kF8Stages;
+          if (t >= kF8Stages &&
+              !warp_mbar_wait(&f8_empty[f], ((t / kF8Stages) - 1) & 1, abort_flag, a.status))
+            break;
+          if (t > 0 && t % kIdTiles == 0) {
+            ids_cur = ids_nxt;
+            ids_nxt = t + kIdTiles < ntiles ? load_ids(t + kIdTiles) : -1;
+          }
+          if (lane == 0) mbar_arrive_expect_tx(&f8_full[f], L::kF8Stage);
+          __syncwarp();
+          // lanes [0, 4): K pages, [4, 8): V pages; one box of 16 keys x D bytes each
+          const int q = lane & (kPagesPerTile - 1);
+          const int blk =
+              __shfl_sync(0xffffffffu, ids_cur, ((t % kIdTiles) * kPagesPerTile + q) & 31);
+          const int tok = blk >= 0 ? blk * kPage : -kPage;  // -16: a box of zeros
+          if (lane < 2 * kPagesPerTile) {
+            const bool is_v = lane >= kPagesPerTile;
+            tma_load_3d(smem + L::kF8Ring + f * L::kF8Stage + (is_v ? L::kF8Tile : 0) +
+                            q * (kPage * D),
+                        is_v ? &tm_v : &tm_k, &f8_full[f], 0, kvh, tok);
+          }
+          issued = t + 1;
+        }
+        if (t >= kLag) ok = widen(t - kLag, 0);
+      }
+      // after a failure the last tiles' copies may still be landing (a bounded wait each)
+      if (lane == 0) {
+        for (int j = issued > kF8Stages ? issued - kF8Stages : 0; j < issued; ++j) {
+          const long long c0 = clock64();
+          while (!mbar_try_wait(&f8_full[j % kF8Stages], (j / kF8Stages) & 1) &&
+                 clock64() - c0 < kWaitLimitCycles) {
+          }
+        }
+      }
+      __syncwarp();
+    }
+    if (warp == kWarpConv && ntiles > 0) {
+      for (int j = 0; j < ntiles; ++j)
+        if (!widen(j, 1)) break;
+    }
   }
   if (warp >= 8) __syncwarp();
 
@@ -379,8 +547,7 @@ __device__ __forceinline__ void prefix_range(const CUtensorMap* tm_q_p,
         // once every M tile's PV(i-1) is done; its phase is unambiguous: the stage's
         // previous tile (i-1-kStages) was freed before tile i-1 was loaded into it,
         // and its next tile's PV cannot complete before this thread writes P(i).
-        warp_mbar_wait(&kv_empty[(i - 1) % kStages], ((i - 1) / kStages) & 1, abort_flag,
-                       a.status);
+        warp_mbar_wait(&kv_empty[(i - 1) % kS], ((i - 1) / kS) & 1, abort_flag, a.status);
         tc_fence_after();
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
@@ -401,7 +568,7 @@ __device__ __forceinline__ void prefix_range(const CUtensorMap* tm_q_p,
         const float p0 = fast_exp2(fmaf(sv[2 * j], a.scale_log2, neg_m));
         const float p1 = fast_exp2(fmaf(sv[2 * j + 1], a.scale_log2, neg_m));
         sum4[j & 3] += p0 + p1;
-        pw[j] = pack_bf16x2(p0, p1);
+        pw[j] = kF8 ? pack_f16x2(p0, p1) : pack_bf16x2(p0, p1);
       }
       l_run += (sum4[0] + sum4[1]) + (sum4[2] + sum4[3]);
       tmem_st32_u(t_lane + (i & 1) * kKeysN, pw);
@@ -435,8 +602,10 @@ __device__ __forceinline__ void prefix_range(const CUtensorMap* tm_q_p,
   __nv_bfloat16* stage = reinterpret_cast<__nv_bfloat16*>(smem);
   if (softmax_warp) {
     tc_fence_after();
-    // a row that saw no key (l = 0) stages zeros
-    const float inv_l = (have && l_run > 0.f) ? 1.f / l_run : 0.f;
+    // a row that saw no key (l = 0) stages zeros; an E4M3 cache's V scale is applied
+    // here, to the normalised rows
+    float inv_l = (have && !(l_run <= 0.f)) ? 1.f / l_run : 0.f;  // NaN propagates
+    if constexpr (kF8) inv_l *= a.v_scale;
     __nv_bfloat16* dst = stage + (wg * kRowsM + row) * L::kStageRow;
 #pragma unroll
     for (int c = 0; c < D / 32; ++c) {
@@ -459,7 +628,7 @@ __device__ __forceinline__ void prefix_range(const CUtensorMap* tm_q_p,
   float* s_lse = reinterpret_cast<float*>(smem + L::kLse);
   if (warp < 8)
     s_lse[wg * kRowsM + row] =
-        (softmax_warp && have && l_run > 0.f) ? m_run + log2f(l_run) : -INFINITY;
+        (softmax_warp && have && !(l_run <= 0.f)) ? m_run + log2f(l_run) : -INFINITY;
   tc_fence_before();
   __syncthreads();
   if (warp == kWarpMma) {
@@ -471,7 +640,7 @@ __device__ __forceinline__ void prefix_range(const CUtensorMap* tm_q_p,
   {
     constexpr int kChunks = D / 8;
     const int gshift = __ffs(a.group) - 1;  // group is a power of two
-    for (int it = threadIdx.x; it < kRowsCta * kChunks; it += kThreads) {
+    for (int it = threadIdx.x; it < kRowsCta * kChunks; it += kNThreads) {
       const int r = it / kChunks;
       const int c = it % kChunks;
       const int packed = geo.prow0 + r;

@@ -209,6 +209,16 @@ def build_tree_batch(name: str, chunk_lens, paths, private_lens, q_lens, *,
                  head_dim=head_dim, gen=gen, block_size=bs, scale=scale, k_scale=1.0)
 
 
+def to_fp8(b: Batch, k_scale: float = 2.0 ** -6, v_scale: float = 2.0 ** -6):
+    """The batch's K and V caches as E4M3 bytes (uint8, same shape) for per-tensor scales
+    k_scale, v_scale: byte = E4M3(x / scale), by torch's float8_e4m3fn rounding (an
+    input draw, not the method).  Poisoned values stay unusable: NaN stays NaN and the
+    +-1000 tail slots saturate to NaN.  Returns (k_bytes, v_bytes)."""
+    k8 = (b.k_cache.float() / k_scale).to(torch.float8_e4m3fn).view(torch.uint8)
+    v8 = (b.v_cache.float() / v_scale).to(torch.float8_e4m3fn).view(torch.uint8)
+    return k8.contiguous(), v8.contiguous()
+
+
 def _gen(seed: int) -> torch.Generator:
     return torch.Generator().manual_seed(seed)
 

@@ -156,3 +156,26 @@ def test_apply_sinks_argument_errors_launch_nothing():
     assert lib.csp_apply_sinks(None, None, None, 4, 0, 64, None) == csp.CSP_ERR_INVALID_ARG
     assert lib.csp_apply_sinks(None, None, None, 4, 8, 64, None) == csp.CSP_ERR_INVALID_ARG
     assert lib.csp_apply_sinks(None, None, None, 0, 8, 64, None) == csp.CSP_OK
+
+
+def test_fp8kv_argument_errors_launch_nothing():
+    lib = csp.load()
+    buf = (ctypes.c_uint8 * 4096)()
+    base = (ctypes.addressof(buf) + 255) // 256 * 256
+    p = ctypes.c_void_p(base)
+    # shapes: group 3 is unsupported, head_dim 96 too
+    out = ctypes.c_size_t(0)
+    assert lib.csp_workspace_size_fp8kv(4, 4, 1, 64, 0, 24, 8, 128, ctypes.byref(out)) == \
+        csp.CSP_ERR_UNSUPPORTED
+    assert lib.csp_workspace_size_fp8kv(4, 4, 1, 64, 0, 8, 2, 96, ctypes.byref(out)) == \
+        csp.CSP_ERR_UNSUPPORTED
+    assert lib.csp_workspace_size_fp8kv(4, 4, 1, 64, 8, 8, 2, 64, ctypes.byref(out)) == \
+        csp.CSP_ERR_INVALID_ARG                       # prefix not a multiple of 16
+    # scales must be finite and positive: refused before any device work
+    args = [p, p, p, 8, p, 4, p, p, 1, 1, 1, 16, 16, 16, 8, 2, 64, 0.125]
+    for ks, vs in ((0.0, 1.0), (1.0, -1.0), (float("inf"), 1.0), (1.0, float("nan"))):
+        assert lib.cascade_attn_fp8kv(*args, ks, vs, p, None, p, 4096, None) == \
+            csp.CSP_ERR_INVALID_ARG
+    args_flat = args[:12] + args[13:]
+    assert lib.paged_attn_fp8kv(*args_flat, 0.0, 1.0, p, None, p, 4096, None) == \
+        csp.CSP_ERR_INVALID_ARG
