@@ -45,23 +45,26 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
+// Two E4M3 bytes (the low 16 bits of w, lower element in the lower byte) -> two f16
+// values (lower element in the lower half).  Exact: every E4M3 value, NaN included, is
+// an f16 value.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t w) {
+  uint32_t r;
+  asm("{\n\t.reg .b16 lo, hi;\n\t"
+      "mov.b32 {lo, hi}, %1;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, lo;\n\t}"
+      : "=r"(r)
+      : "r"(w));
+  return r;
+}
+
 // Sixteen E4M3 bytes (element e in byte e) -> sixteen f16 values, elements 0-7 in
-// `lo` and 8-15 in `hi`, two per 32-bit word, lower element in the lower half.  Exact:
-// every E4M3 value (NaN included) is an f16 value.
+// `lo` and 8-15 in `hi`, two per 32-bit word, lower element in the lower half.
 __device__ __forceinline__ void e4m3x16_to_f16(uint4 raw, uint4& lo, uint4& hi) {
-  const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
-  uint32_t o[8];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const __half2_raw a = __nv_cvt_fp8x2_to_halfraw2(
-        static_cast<__nv_fp8x2_storage_t>(w[i] & 0xFFFFu), __NV_E4M3);
-    const __half2_raw b = __nv_cvt_fp8x2_to_halfraw2(
-        static_cast<__nv_fp8x2_storage_t>(w[i] >> 16), __NV_E4M3);
-    o[2 * i] = static_cast<uint32_t>(a.x) | (static_cast<uint32_t>(a.y) << 16);
-    o[2 * i + 1] = static_cast<uint32_t>(b.x) | (static_cast<uint32_t>(b.y) << 16);
-  }
-  lo = make_uint4(o[0], o[1], o[2], o[3]);
-  hi = make_uint4(o[4], o[5], o[6], o[7]);
+  lo = make_uint4(e4m3x2_to_f16x2(raw.x), e4m3x2_to_f16x2(raw.x >> 16), e4m3x2_to_f16x2(raw.y),
+                  e4m3x2_to_f16x2(raw.y >> 16));
+  hi = make_uint4(e4m3x2_to_f16x2(raw.z), e4m3x2_to_f16x2(raw.z >> 16), e4m3x2_to_f16x2(raw.w),
+                  e4m3x2_to_f16x2(raw.w >> 16));
 }
 
 // ---------------------------------------------------------------- mbarrier --

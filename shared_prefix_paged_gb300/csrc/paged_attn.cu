@@ -42,9 +42,9 @@ __device__ __forceinline__ uint32_t swz(int row, int chunk) {
 template <int D, bool kF8 = false>
 struct PagedLayout {
   // two 64-key tiles in flight (68 KB for D=128), so three CTAs fit on an SM.  An E4M3
-  // cache keeps its two tiles in flight as bytes and widens the current one into a
-  // single f16 K/V buffer (the same 68 KB).
-  static constexpr int kStages = 2;
+  // cache keeps four tiles in flight as bytes (the same bytes in flight per SM with two
+  // CTAs) and widens the current one into a single f16 K/V buffer (100 KB).
+  static constexpr int kStages = kF8 ? 4 : 2;
   static constexpr int kRows = 16;
   static constexpr int kQBytes = kRows * D * 2;
   static constexpr int kKVBytes = kTileKeys * D * 2;
@@ -194,21 +194,24 @@ __global__ void __launch_bounds__(kThreads)
       }
     }
     if constexpr (kF8) {
-      // widen tile ti into the f16 K/V buffer (every warp finished tile ti - 1)
+      // widen tile ti into the f16 K/V buffer (every warp finished tile ti - 1): this
+      // thread's column c (16 features) of keys key0 + kStep i; the swizzle term
+      // key & 7 is the same for every i
       constexpr int kC16 = D / 16;
-      const uint8_t* src = smem + L::kF8Base + (ti % kStages) * 2 * L::kF8Tile;
-#pragma unroll 2
-      for (int x = threadIdx.x; x < 2 * kTileKeys * kC16; x += kThreads) {
-        const bool is_v = x >= kTileKeys * kC16;
-        const int y = is_v ? x - kTileKeys * kC16 : x;
-        const int key = y / kC16, c = y % kC16;
-        const uint4 raw =
-            *reinterpret_cast<const uint4*>(src + (is_v ? L::kF8Tile : 0) + key * D + c * 16);
+      constexpr int kStep = kThreads / kC16;
+      const int c = threadIdx.x % kC16, key0 = threadIdx.x / kC16;
+      const uint8_t* src = smem + L::kF8Base + (ti % kStages) * 2 * L::kF8Tile + key0 * D + c * 16;
+      const uint32_t lo_off = swz<D>(key0, 2 * c), hi_off = swz<D>(key0, 2 * c + 1);
+#pragma unroll
+      for (int i = 0; i < kTileKeys / kStep; ++i) {
         uint4 lo, hi;
-        e4m3x16_to_f16(raw, lo, hi);
-        uint8_t* dst = smem + (is_v ? L::kV : L::kK);
-        *reinterpret_cast<uint4*>(dst + swz<D>(key, 2 * c)) = lo;
-        *reinterpret_cast<uint4*>(dst + swz<D>(key, 2 * c + 1)) = hi;
+        e4m3x16_to_f16(*reinterpret_cast<const uint4*>(src + i * kStep * D), lo, hi);
+        *reinterpret_cast<uint4*>(smem + L::kK + i * kStep * D * 2 + lo_off) = lo;
+        *reinterpret_cast<uint4*>(smem + L::kK + i * kStep * D * 2 + hi_off) = hi;
+        e4m3x16_to_f16(*reinterpret_cast<const uint4*>(src + L::kF8Tile + i * kStep * D), lo,
+                       hi);
+        *reinterpret_cast<uint4*>(smem + L::kV + i * kStep * D * 2 + lo_off) = lo;
+        *reinterpret_cast<uint4*>(smem + L::kV + i * kStep * D * 2 + hi_off) = hi;
       }
       __syncthreads();
     }

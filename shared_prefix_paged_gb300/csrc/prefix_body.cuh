@@ -46,7 +46,7 @@ constexpr int kThreads = 352;  // 2 softmax warpgroups, two MMA issuers, the K/V
 // (exact: E4M3 is a subset of f16) for MMAs with f16 operands.
 constexpr int kThreadsF8 = 384;
 constexpr int kWarpConv = 11;
-constexpr int kF8Stages = 4;   // E4M3 tiles in flight (the f16 ring is then 2 deep)
+constexpr int kF8Stages = 6;   // E4M3 tiles in flight (the f16 ring is then 2 deep)
 constexpr int kWarpMma = 8;
 constexpr int kWarpTma = 9;    // Q by TMA, then the MMA issuer of M tile 1
 constexpr int kWarpLoad = 10;  // K and V by TMA
@@ -155,14 +155,15 @@ __device__ __forceinline__ void prefix_range(const CUtensorMap* tm_q_p,
   uint64_t* o_last = bars + 11 + 2 * kS;   // [2 tiles] the last PV (9, 10 unused)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 13 + 2 * kS);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 14 + 2 * kS);
-  uint64_t* f8_full = bars + 15 + 2 * kS;   // [kF8Stages] E4M3 tiles landed (kF8)
-  uint64_t* f8_empty = bars + 19 + 2 * kS;  // [kF8Stages] E4M3 tiles widened (kF8)
+  uint64_t* f8_full = bars + 15 + 2 * kS;               // [kF8Stages] E4M3 tiles landed
+  uint64_t* f8_empty = bars + 15 + 2 * kS + kF8Stages;  // [kF8Stages] E4M3 tiles widened
   uint64_t* tail_in = bars + 15 + 2 * kS;   // bf16: the last tile landed (see the loader)
   // A range that ends inside a page (a request's last page) leaves slots past its end
   // in that page: whatever the cache holds there (NaN included) would reach O through
   // P = 0 times V in the MMA, so those V rows are zeroed before the PV reads them.
   const bool ragged_end = kCausal && (geo.key_end % kPage) != 0;
-  static_assert((kF8 ? 23 + 2 * kS : 15 + 2 * kS) * 8 <= kBarBytes, "barrier area");
+  static_assert((kF8 ? 15 + 2 * kS + 2 * kF8Stages : 16 + 2 * kS) * 8 <= kBarBytes,
+                "barrier area");
   static_assert(!kF8 || kWarpConv * 32 + 32 == kThreadsF8, "the converter warp is the last");
 
   const int warp = threadIdx.x >> 5;
@@ -367,7 +368,9 @@ __device__ __forceinline__ void prefix_range(const CUtensorMap* tm_q_p,
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(&kv_full[st]);
-        issued = j;  // its copies have landed
+        // its phase of kv_full is complete: the wait below must count it, or it would
+        // wait on the stage's previous (already passed) phase
+        issued = j + 1;
         break;
       }
       issued = j + 1;
@@ -397,31 +400,48 @@ __device__ __forceinline__ void prefix_range(const CUtensorMap* tm_q_p,
       if (!warp_mbar_wait(&f8_full[f], (j / kF8Stages) & 1, abort_flag, a.status)) return false;
       if (j >= kS && !warp_mbar_wait(&kv_empty[st], ((j / kS) - 1) & 1, abort_flag, a.status))
         return false;
-      constexpr int kC16 = D / 16;  // 16-byte E4M3 chunks per key
-      constexpr int kTileChunks = kKeysN * kC16;
-      const uint8_t* src = smem + L::kF8Ring + f * L::kF8Stage;
-#pragma unroll 4
-      for (int x = part * 32 + lane; x < 2 * kTileChunks; x += 64) {
-        const bool is_v = x >= kTileChunks;
-        const int y = is_v ? x - kTileChunks : x;
-        const int key = y / kC16, c16 = y % kC16;
-        const uint4 raw =
-            *reinterpret_cast<const uint4*>(src + (is_v ? L::kF8Tile : 0) + key * D + c16 * 16);
+      // This thread's chunks: column c16 (16 features) of keys key0 + (64 / kC16) i
+      // (the 64 threads of the two warps cover 64 / kC16 keys per step); within a
+      // 128-byte row the swizzle term is key & 7, the same for every i.
+      constexpr int kC16 = D / 16;           // 16-byte E4M3 chunks per key
+      constexpr int kStep = 64 / kC16;       // keys per step
+      const int t64 = part * 32 + lane;
+      const int c16 = t64 % kC16, key0 = t64 / kC16;
+      const int h = c16 >> 2, c8 = (c16 & 3) * 2;
+      const int sw = key0 & 7;
+      const int lo_off = (c8 ^ sw) << 4, hi_off = ((c8 + 1) ^ sw) << 4;
+      const uint8_t* src = smem + L::kF8Ring + f * L::kF8Stage + key0 * D + c16 * 16;
+      uint8_t* dk = smem + L::kK0 + st * L::kKVBytes + h * L::kKVHalf + key0 * 128;
+      uint8_t* dv = smem + L::kV0 + st * L::kKVBytes + h * (kPage * 128) + key0 * 128;
+#pragma unroll
+      for (int i = 0; i < kKeysN / kStep; ++i) {
         uint4 lo, hi;
-        e4m3x16_to_f16(raw, lo, hi);
-        if (is_v && geo.key0 + tile_of(j) * kKeysN + key >= geo.key_end) {
-          // a slot past the range (a ragged last page): zero, not the cache's bytes
-          lo = make_uint4(0u, 0u, 0u, 0u);
-          hi = lo;
+        e4m3x16_to_f16(*reinterpret_cast<const uint4*>(src + i * kStep * D), lo, hi);
+        *reinterpret_cast<uint4*>(dk + i * kStep * 128 + lo_off) = lo;
+        *reinterpret_cast<uint4*>(dk + i * kStep * 128 + hi_off) = hi;
+      }
+#pragma unroll
+      for (int i = 0; i < kKeysN / kStep; ++i) {
+        const int key = key0 + i * kStep;  // V rows: [page][half][16 keys][128 B]
+        uint4 lo, hi;
+        e4m3x16_to_f16(*reinterpret_cast<const uint4*>(src + L::kF8Tile + i * kStep * D), lo,
+                       hi);
+        uint8_t* row = dv + (key / kPage) * L::kVPage + (key % kPage - key0) * 128;
+        *reinterpret_cast<uint4*>(row + lo_off) = lo;
+        *reinterpret_cast<uint4*>(row + hi_off) = hi;
+      }
+      if (kCausal && j == ntiles - 1 && ragged_end) {
+        // slots past the range in its last page: zero, not the cache's bytes (after this
+        // thread's own writes above; the same thread wrote these rows)
+#pragma unroll
+        for (int i = 0; i < kKeysN / kStep; ++i) {
+          const int key = key0 + i * kStep;
+          if (geo.key0 + tile_of(j) * kKeysN + key >= geo.key_end) {
+            uint8_t* row = dv + (key / kPage) * L::kVPage + (key % kPage - key0) * 128;
+            *reinterpret_cast<uint4*>(row + lo_off) = make_uint4(0u, 0u, 0u, 0u);
+            *reinterpret_cast<uint4*>(row + hi_off) = make_uint4(0u, 0u, 0u, 0u);
+          }
         }
-        // features [16 c16, 16 c16 + 16): half c16 / 4, 16-byte chunks 2 (c16 % 4) + {0, 1}
-        const int h = c16 >> 2, c8 = (c16 & 3) * 2;
-        const int row = is_v ? L::kV0 + st * L::kKVBytes + (key / kPage) * L::kVPage +
-                                   h * (kPage * 128) + (key % kPage) * 128
-                             : L::kK0 + st * L::kKVBytes + h * L::kKVHalf + key * 128;
-        const int sw = (row >> 7) & 7;
-        *reinterpret_cast<uint4*>(smem + row + ((c8 ^ sw) << 4)) = lo;
-        *reinterpret_cast<uint4*>(smem + row + (((c8 + 1) ^ sw) << 4)) = hi;
       }
       fence_proxy_async_smem();
       mbar_arrive(&kv_full[st]);
