@@ -68,6 +68,9 @@ def parse_args(argv=None):
                     help="device timing only (no e2e, flat comparison or CPU baseline)")
     ap.add_argument("--sweep", action="store_true",
                     help="N x P decode sweep: cascade vs flat at every point, one line each")
+    ap.add_argument("--fp8", action="store_true",
+                    help="FP8 (E4M3) KV cache: bf16 vs FP8 cascade and flat, one line per "
+                         "workload")
     ap.add_argument("--levels", action="store_true",
                     help="tree-shaped decode batches: flat vs two-level vs multi-level "
                          "cascade, one line each")
@@ -796,6 +799,80 @@ def run_levels(args, dist: Dist):
         torch.cuda.empty_cache()
 
 
+def run_fp8(args, dist: Dist):
+    """bf16 and FP8 (E4M3, per-tensor scales) KV caches on the same batches: cascade and
+    the standard path, microseconds per call and minimal bytes / time."""
+    import torch
+    from shared_prefix_paged_gb300 import accounting, csp
+    torch.cuda.set_device(dist.local_rank)
+    device = torch.device("cuda", dist.local_rank)
+    peaks = load_peaks()
+    for name in ("decode", "chunked"):
+        b = make_batch(name, dist.rank)
+        R = args.copies or default_copies(b)
+        run = DeviceRun(b, R, device)
+        # scales that map the largest used magnitude just inside E4M3's range (the +-1000
+        # poison of unused slots aside); the bytes are drawn on the device
+        def amax(t):
+            x = t.float().abs()
+            return float(x[torch.isfinite(x) & (x < 999.0)].max())
+        ks, vs = amax(run.k[0]) / 440.0, amax(run.v[0]) / 440.0
+        k8 = [(run.k[i].float() / ks).to(torch.float8_e4m3fn).view(torch.uint8)
+              for i in range(R)]
+        v8 = [(run.v[i].float() / vs).to(torch.float8_e4m3fn).view(torch.uint8)
+              for i in range(R)]
+        ws8 = csp.alloc_workspace(csp.workspace_size_fp8kv(
+            b.num_reqs, b.total_q, b.max_seqlen_q, b.max_seqlen_k, run.cpl, b.num_q_heads,
+            b.num_kv_heads, b.head_dim), device)
+        steps = max(R, min(args.steps, 2000))
+        t = {}
+        for path in ("cascade", "flat"):
+            e, _, _, _ = time_graph_steps(run, path, steps, args.warmup, dist, False)
+            t["bf16_" + path] = e / steps * 1e6
+
+        class Fp8Run:
+            """DeviceRun's graph interface over the E4M3 caches."""
+            def __init__(self, cpl):
+                self.R, self.dev, self.cpl = R, device, cpl
+
+            def graph(self, path, n, events=None):
+                def step(i):
+                    csp.attn_fp8kv(run.q[i], k8[i], v8[i], run.bt, run.cu, run.sl,
+                                   max_seqlen_q=b.max_seqlen_q, max_seqlen_k=b.max_seqlen_k,
+                                   softmax_scale=b.scale, k_scale=ks, v_scale=vs,
+                                   common_prefix_len=self.cpl, out=run.out[i], lse=run.lse[i],
+                                   workspace=ws8)
+                s = torch.cuda.Stream(device)
+                s.wait_stream(torch.cuda.current_stream(device))
+                with torch.cuda.stream(s):
+                    for i in range(n):
+                        step(i % R)
+                torch.cuda.current_stream(device).wait_stream(s)
+                torch.cuda.synchronize(device)
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g):
+                    for i in range(n):
+                        step(i % R)
+                return g
+
+        for path, cpl in (("cascade", run.cpl), ("flat", 0)):
+            e, _, _, _ = time_graph_steps(Fp8Run(cpl), path, steps, args.warmup, dist, False)
+            t["fp8_" + path] = e / steps * 1e6
+        kv8 = accounting.cascade_min_bytes(b, run.cpl) - accounting.cascade_kv_tokens(
+            b.seq_lens, run.cpl) * accounting.kv_bytes_per_token(b.num_kv_heads, b.head_dim) // 2
+        line = {"fp8": True, "workload": b.name, "cpl": run.cpl,
+                "k_scale": ks, "v_scale": vs,
+                **{k + "_us": round(v, 3) for k, v in t.items()},
+                "fp8_cascade_min_bytes": kv8,
+                "fp8_cascade_hbm_frac": round(kv8 / (t["fp8_cascade"] * 1e-6) / 1e9 /
+                                              peaks["hbm_gbs"], 3),
+                "peak_source": peaks["source"]}
+        if dist.rank == 0:
+            print(json.dumps(line), flush=True)
+        del run
+        torch.cuda.empty_cache()
+
+
 def main(argv=None):
     args = parse_args(argv)
     if args.impl == "reference":
@@ -812,6 +889,9 @@ def main(argv=None):
             return 0
         if args.levels:
             run_levels(args, dist)
+            return 0
+        if args.fp8:
+            run_fp8(args, dist)
             return 0
         res = run_ours(args, dist)
         if dist.rank == 0:
