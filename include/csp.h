@@ -89,8 +89,9 @@ typedef enum {
 
 /* cascade_plan modes. */
 enum {
-  CSP_MODE_AUTO = 0,            /* GB300 rule: cascade when it cuts the streamed KV
-                                   tokens by >= 1.8x (fitted to a measured sweep)     */
+  CSP_MODE_AUTO = 0,            /* GB300 rule: cascade when the standard path would
+                                   stream >= 8192 KV tokens and cascade cuts them by
+                                   >= 1.8x (fitted to a measured sweep)               */
   CSP_MODE_FORCE_CASCADE = 1,   /* use cascade whenever common_prefix_len > 0          */
   CSP_MODE_FORCE_FLAT = 2,      /* never use cascade                                   */
   CSP_MODE_PAGE_THRESHOLDS = 3  /* the pages' rule only: prefix >= 256 and batch >= 8  */

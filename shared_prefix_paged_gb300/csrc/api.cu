@@ -38,6 +38,8 @@ int merge_lse_box(int rows) { return (rows + 3 + 3) & ~3; }
 // Most packed rows (query, head-in-group) per request and KV head that the decode
 // schedule takes: one warp-level MMA tile.
 constexpr int kDecodeRows = 16;
+// CSP_MODE_AUTO takes cascade only when the standard path streams this many KV tokens
+constexpr int64_t kAutoMinFlatTokens = 8192;
 constexpr int kMaxSplits = 32;  // suffix splits; with the prefix's slots at most 32 partials per row
 
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
@@ -230,6 +232,9 @@ void make_plan(int num_reqs, int total_q, int max_q, int max_k, int cpl, int Hq,
   const int64_t units = static_cast<int64_t>(num_reqs) * p.s_row_tiles * Hkv;
   const int max_s = std::min(kMaxSplits, 32 - p.p_slots);
   int s = units > 0 ? static_cast<int>(std::min<int64_t>(cdiv64(2LL * sms, units), max_s)) : 1;
+  // the warp-MMA kernel merges up to 8 splits of a row tile inside a thread-block cluster
+  // (no counters, no global partials): take at most 8
+  if (!p.tc) s = std::min(s, 8);
   if (p.tc) {
     // one CTA per SM: waves x (a split's tiles + ~5 tiles of fixed cost: the first
     // tile's latency, the output and the merge)
@@ -707,7 +712,10 @@ int attention_call(const void* q, const void* k_cache, const void* v_cache, int3
   // counters that start at zero in every call, whatever the workspace held.
   // The fused schedule counts prefix ranges and suffix splits in the same counters.
   const bool merge_after = P.tc && cpl > 0 && !P.fused;
-  if (P.n_parts > 0 && (P.s_splits > 1 || P.fused) && !merge_after &&
+  // the warp-MMA kernel with 2..8 key splits merges them inside a thread-block cluster
+  // (distributed shared memory): no counters
+  const bool cluster = !P.tc && !P.fused && P.s_splits >= 2 && P.s_splits <= 8;
+  if (P.n_parts > 0 && (P.s_splits > 1 || P.fused) && !merge_after && !cluster &&
       (e = cudaMemsetAsync(counters, 0, static_cast<size_t>(total_q) * Hkv * sizeof(int32_t),
                            stream)) != cudaSuccess)
     return cuda_fail(e);
@@ -770,7 +778,8 @@ int attention_call(const void* q, const void* k_cache, const void* v_cache, int3
   ga.out = static_cast<__nv_bfloat16*>(out);
   ga.lse = lse;
   ga.status = status;
-  if (merge_after) ga.counters = nullptr;
+  ga.cluster_splits = cluster;
+  if (merge_after || cluster) ga.counters = nullptr;
   // concurrent with the prefix kernel (programmatic dependent launch) unless phase
   // events sit between the two
   const bool overlap = cpl > 0 && events == nullptr;
@@ -865,10 +874,12 @@ int cascade_plan(const int32_t* block_table, int64_t bt_row_stride, int32_t num_
       break;
     default: {
       // GB300 rule, fitted to a cascade-vs-flat sweep of N in {4..256} x P in
-      // {128..16384} (S = 128) on one GB300: cascade when it cuts the KV tokens the
-      // standard path streams by at least 1.8x (the prefix read once instead of N
-      // times).  On that grid it was never more than 2% slower than the better path;
-      // the pages' thresholds (prefix >= 256, batch >= 8) lost up to 2.2x at N = 4.
+      // {128..16384} (S = 128, Hkv 8, D 128) on one GB300: cascade when the standard
+      // path would stream at least 8192 KV tokens (below that both calls are latency-
+      // bound and the flat one, a single launch, is the faster) and cascade cuts those
+      // tokens by at least 1.8x (the prefix read once instead of N times).  On that
+      // grid it picked the faster path at every point; the pages' thresholds (prefix
+      // >= 256, batch >= 8) lost up to 2.1x at N = 4.
       int64_t flat_tokens = 0, casc_tokens = cpl;
       for (int r = 0; r < num_reqs; ++r) {
         flat_tokens += seq_lens[r];
@@ -878,7 +889,8 @@ int cascade_plan(const int32_t* block_table, int64_t bt_row_stride, int32_t num_
       (void)num_kv_heads;
       (void)head_dim;
       (void)num_sms;
-      use = cpl > 0 && casc_tokens > 0 && 5 * flat_tokens >= 9 * casc_tokens;
+      use = cpl > 0 && casc_tokens > 0 && flat_tokens >= kAutoMinFlatTokens &&
+            5 * flat_tokens >= 9 * casc_tokens;
       break;
     }
   }
@@ -1188,11 +1200,12 @@ int cascade_attn_levels(const void* q, const void* k_cache, const void* v_cache,
   const float scale_log2 = softmax_scale * 1.4426950408889634f;
   const LaunchPlan& P = L.suf;
   const bool merge_after = P.tc;
+  const bool cluster = !P.tc && P.s_splits >= 2 && P.s_splits <= 8;  // as in attention_call
   cudaError_t e;
   // a row no segment of a level holds reads lse = -inf (weight 0) in that level's slots
   if ((e = csp::launch_fill_f32(part_lse, L.n_prefix * rows, -INFINITY, stream)) != cudaSuccess)
     return cuda_fail(e);
-  if (P.s_splits > 1 && !merge_after &&
+  if (P.s_splits > 1 && !merge_after && !cluster &&
       (e = cudaMemsetAsync(counters, 0, static_cast<size_t>(total_q) * Hkv * sizeof(int32_t),
                            stream)) != cudaSuccess)
     return cuda_fail(e);
@@ -1273,7 +1286,8 @@ int cascade_attn_levels(const void* q, const void* k_cache, const void* v_cache,
   ga.part_o = part_o;
   ga.part_lse = part_lse;
   ga.n_prefix = L.n_prefix;
-  ga.counters = merge_after ? nullptr : counters;
+  ga.counters = (merge_after || cluster) ? nullptr : counters;
+  ga.cluster_splits = cluster;
   ga.out = static_cast<__nv_bfloat16*>(out);
   ga.lse = lse;
   ga.status = status;

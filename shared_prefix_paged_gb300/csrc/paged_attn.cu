@@ -60,7 +60,11 @@ struct PagedLayout {
   // rows of D floats with a padded stride, then per-warp max and sum
   static constexpr int kORow = D + 8;
   static constexpr int kMergeBytes = 4 * 16 * kORow * 4 + 2 * 4 * 16 * 4;
-  static_assert(kMergeBytes <= kLast - kK, "merge scratch");
+  // the cluster merge's exchange area after it: each row's normalised O (fp32) and
+  // log2-sum-exp, read by the other CTAs of the cluster
+  static constexpr int kXO = kK + kMergeBytes;
+  static constexpr int kXL = kXO + 16 * D * 4;
+  static_assert(kXL + 16 * 4 <= kLast, "merge scratch and exchange area");
 };
 
 // kF8: an E4M3 KV cache (a.k, a.v its bytes, a.q the f16 queries): the tiles arrive
@@ -331,8 +335,10 @@ __global__ void __launch_bounds__(kThreads)
   m.out = a.out;
   m.lse = a.lse;
   // one suffix split: this CTA merges its rows itself, in registers, with the prefix
-  // slots; several splits: write a partial and let the last split merge
+  // slots; several splits: write a partial and let the last split merge, or (a cluster
+  // of the splits) leave it in shared memory for the cluster merge below
   const bool merge_in_place = partial && a.n_splits == 1;
+  const bool in_cluster = a.cluster_splits;
 
   {
     // merge the four warps' (m, l, O) of the same 16 rows through shared memory
@@ -396,7 +402,11 @@ __global__ void __launch_bounds__(kThreads)
         }
         acc = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
       }
-      if (merge_in_place) {
+      if (in_cluster) {
+        float* xo = reinterpret_cast<float*>(smem + L::kXO);
+        if (lane < D / 4) *reinterpret_cast<float4*>(xo + rr * D + lane * 4) = acc;
+        if (lane == 0) reinterpret_cast<float*>(smem + L::kXL)[rr] = lse2;
+      } else if (merge_in_place) {
         merge_row_warp<D>(m, orow, lane, true, acc, lse2);
       } else if (partial) {
         const int64_t prow = static_cast<int64_t>(a.n_prefix + split) * a.total_q *
@@ -408,6 +418,57 @@ __global__ void __launch_bounds__(kThreads)
         if (lane == 0 && a.lse != nullptr) a.lse[orow] = lse2 * kLn2;
       }
     }
+  }
+
+  if (in_cluster) {
+    // The cluster is this row tile's key splits (cluster rank = split).  After the
+    // barrier every CTA's rows are in its exchange area; CTA `rank` merges rows rank,
+    // rank + n_splits, ... : the prefix slots (global memory, after the prefix grid)
+    // and every split's partial (distributed shared memory), one warp per row.
+    cluster_barrier();
+    const int ns = a.n_splits;
+    const int rank = static_cast<int>(cluster_rank());
+    const int np = a.n_prefix;
+    if (np > 0) grid_dependency_wait();
+    const uint32_t xo0 = smem_u32(smem + L::kXO), xl0 = smem_u32(smem + L::kXL);
+    for (int rr = rank + ns * warp; rr < rows_here; rr += ns * 4) {
+      const int rho = row0 + rr;
+      const int qi = rho / a.group, j = rho % a.group;
+      const int64_t orow = static_cast<int64_t>(q0 + qi) * a.num_q_heads + g * a.group + j;
+      // lane p: the log2-sum-exp of partial p (prefix slots first, then the splits)
+      float lp = -INFINITY;
+      if (lane < np)
+        lp = __ldcg(a.part_lse + static_cast<int64_t>(lane) * m.rows + orow);
+      else if (lane < np + ns)
+        lp = ld_cluster_f32(cluster_map(xl0 + rr * 4, lane - np));
+      float mx = lp;
+#pragma unroll
+      for (int sft = 16; sft > 0; sft >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, sft));
+      const float w = (mx == -INFINITY || lp == -INFINITY) ? 0.f : fast_exp2(lp - mx);
+      float wsum = w;
+#pragma unroll
+      for (int sft = 16; sft > 0; sft >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, sft);
+      const float inv = !(wsum <= 0.f) ? 1.f / wsum : 0.f;  // a NaN sum propagates
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int p = 0; p < np + ns; ++p) {
+        const float wp = __shfl_sync(0xffffffffu, w, p) * inv;
+        if (wp == 0.f || lane >= D / 4) continue;  // an empty partial is never read
+        const float4 v =
+            p < np ? load_bf16x4_cg(a.part_o + (static_cast<int64_t>(p) * m.rows + orow) * D +
+                                    lane * 4)
+                   : ld_cluster_f32x4(cluster_map(xo0 + (rr * D + lane * 4) * 4, p - np));
+        acc.x = fmaf(wp, v.x, acc.x);
+        acc.y = fmaf(wp, v.y, acc.y);
+        acc.z = fmaf(wp, v.z, acc.z);
+        acc.w = fmaf(wp, v.w, acc.w);
+      }
+      if (lane < D / 4) store_bf16x4(a.out + orow * D + lane * 4, acc);
+      if (lane == 0 && a.lse != nullptr)
+        a.lse[orow] = !(wsum <= 0.f) ? (mx + log2f(wsum)) * kLn2 : -INFINITY;
+    }
+    // no CTA leaves while another may still read its exchange area
+    cluster_barrier();
+    return;
   }
 
   if (partial && !merge_in_place) {
@@ -432,13 +493,24 @@ cudaError_t launch_paged_t(const PagedArgs& a, bool after_prefix, cudaStream_t s
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
+  int n = 0;
   // Right after the prefix kernel of the same call: start while it runs; the merge
   // with the prefix slots waits for the prefix grid (griddepcontrol.wait).
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  if (after_prefix) {
+    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+  }
+  if (a.cluster_splits) {  // a row tile's splits: one cluster
+    attr[n].id = cudaLaunchAttributeClusterDimension;
+    attr[n].val.clusterDim.x = 1;
+    attr[n].val.clusterDim.y = 1;
+    attr[n].val.clusterDim.z = static_cast<unsigned>(a.n_splits);
+    ++n;
+  }
   cfg.attrs = attr;
-  cfg.numAttrs = after_prefix ? 1 : 0;
+  cfg.numAttrs = n;
   return cudaLaunchKernelEx(&cfg, paged_attn_kernel<D, kF8>, a);
 }
 

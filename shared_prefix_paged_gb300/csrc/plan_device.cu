@@ -96,11 +96,11 @@ __global__ void __launch_bounds__(kPlanThreads)
       use = cpl >= 256 && num_reqs >= 8;
       break;
     default: {
-      // the GB300 rule of cascade_plan: cascade when it cuts the streamed KV tokens by
-      // at least 1.8x
+      // the GB300 rule of cascade_plan: cascade when the standard path would stream at
+      // least 8192 KV tokens and cascade cuts them by at least 1.8x
       const long long flat = static_cast<long long>(s_flat);
       const long long casc = cpl + flat - static_cast<long long>(num_reqs) * cpl;
-      use = cpl > 0 && casc > 0 && 5 * flat >= 9 * casc;
+      use = cpl > 0 && casc > 0 && flat >= 8192 && 5 * flat >= 9 * casc;
       break;
     }
   }

@@ -73,7 +73,12 @@ def test_planner_modes_and_errors():
     args = (b.block_table, b.seq_lens, b.num_computed_tokens)
     assert csp.cascade_plan(*args, mode=csp.MODE_FORCE_FLAT) == (512, False)
     assert csp.cascade_plan(*args, mode=csp.MODE_FORCE_CASCADE) == (512, True)
-    assert csp.cascade_plan(*args, mode=csp.MODE_AUTO) == (512, True)
+    # the GB300 rule leaves a batch whose standard path streams under 8192 KV tokens
+    # (8 x 544 here) to that path: both calls are latency-bound there
+    assert csp.cascade_plan(*args, mode=csp.MODE_AUTO) == (512, False)
+    big = workloads.decode_batch(n=16, p=512, s=32)    # 16 x 544 = 8704 tokens, 3.5x fewer
+    bargs = (big.block_table, big.seq_lens, big.num_computed_tokens)
+    assert csp.cascade_plan(*bargs, mode=csp.MODE_AUTO) == (512, True)
     # the GB300 rule keeps cascade for a small batch over a long prefix (the pages'
     # thresholds refuse N < 8) and refuses it where it would save too few bytes
     small = workloads.decode_batch(n=4, p=4096, s=32)
