@@ -181,11 +181,10 @@ enum { CSP_SCHEDULE_TWO_KERNELS = 0, CSP_SCHEDULE_SINGLE = 1, CSP_SCHEDULE_FUSED
  * csp_cascade_schedule — which kernels cascade_attn launches for a batch of this
  * shape on the current device.  Host integers, the same as the attention call will
  * get (common_prefix_len > 0).
- *   CSP_SCHEDULE_TWO_KERNELS : a prefix-phase kernel, then a paged kernel for the
- *                              suffix phase (any batch); where a request and KV head
- *                              have at most 16 query rows (query tokens x heads in
- *                              the group) the paged kernel's CTAs also merge, for
- *                              more rows a third kernel merges every row after both;
+ *   CSP_SCHEDULE_TWO_KERNELS : a prefix-phase kernel, and beside it (on the SMs it
+ *                              leaves free) a paged kernel for the suffix phase that
+ *                              writes its partial results; a third kernel merges
+ *                              every row once both are done (any batch);
  *   CSP_SCHEDULE_SINGLE      : one cooperative kernel of one CTA per SM, for batches
  *                              where every request has at most 16 / (num_q_heads /
  *                              num_kv_heads) query tokens: some CTAs run ranges of the
@@ -246,8 +245,11 @@ CSP_API int cascade_attn(const void* q, const void* k_cache, const void* v_cache
  *                  CSP_SCHEDULE_SINGLE where that kernel can run (a request's rows of
  *                  one KV head fit 16 and the prefix's 256-row blocks x KV heads fit
  *                  the SMs; else CSP_ERR_UNSUPPORTED)
- *   prefix_ranges  > 0: the single kernel's number of prefix key ranges (capped at 15,
- *                  the prefix's 64-key tiles and the SMs' room); 0: the cost model's
+ *   prefix_ranges  > 0: the number of prefix key ranges of the single kernel (capped at
+ *                  15, the prefix's 64-key tiles and the SMs' room) or of the
+ *                  two-kernel schedule when a request and KV head have at most 16
+ *                  query rows (capped at 16 and the prefix's 64-key tiles); 0: the
+ *                  cost model's
  * common_prefix_len must be > 0.  Other arguments, the workspace (csp_workspace_size
  * covers every schedule and number of ranges) and the errors are cascade_attn's;
  * CSP_ERR_INVALID_ARG for an unknown schedule or a negative prefix_ranges.

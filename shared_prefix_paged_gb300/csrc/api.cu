@@ -179,6 +179,9 @@ struct LaunchPlan {
   // the fused schedule: prefix ranges and tcgen05 suffix units in one grid
   // (paged_tc.cu), merged by each row group's last contributor
   bool fused = false;
+  // the two-kernel schedule with the warp-MMA suffix writing its partials and a merge
+  // kernel after both phases (as after a tcgen05 suffix)
+  bool split_merge = false;
   // single-kernel decode schedule (decode_cascade.cu)
   bool single = false;
   int d_splits = 0, d_prefix_ctas = 0, d_prefix_units = 0, d_grid = 0, d_merge_rows = 0;
@@ -351,6 +354,54 @@ void make_plan(int num_reqs, int total_q, int max_q, int max_k, int cpl, int Hq,
     p.bytes = std::max(p.bytes, kHeaderBytes +
                                     align256(static_cast<size_t>(s_max + 1) * rows_total * D * 2) +
                                     align256(lse_max));
+  }
+  // The two-kernel schedule for decode-shaped rows: the prefix kernel on some SMs, the
+  // warp-MMA suffix kernel writing its partials on the rest (neither waits for the
+  // other), then the slot merge kernel.  The number of prefix key ranges comes from a
+  // cost model fitted to a sweep of N in {16..256} x P in {1024..16384} (S = 128, Hq
+  // 32, Hkv 8, D 128) on one GB300: a prefix CTA costs ~4 us plus its 64-key tiles at
+  // the longer of the copy time (~20 GB/s per SM while the suffix streams too) and
+  // ~1 us per 256 rows; the suffix streams at ~20 GB/s per SM on the SMs the prefix
+  // leaves free and then on all; the merge costs ~0.2 ns per row and slot.  Against an
+  // in-place merge (the suffix waiting for the whole prefix grid) it was 20-27% faster
+  // at N >= 128.  The workspace fits up to 16 ranges (a caller's override).
+  if (cpl > 0 && !p.tc) {
+    const int key_tiles = cdiv(cpl, 64);
+    const int r_max = std::min(16, key_tiles);
+    // the workspace fits this schedule at any number of ranges up to 16 (a caller's
+    // override), whichever schedule the cost model picks
+    const size_t rows_total = static_cast<size_t>(total_q) * Hq;
+    const size_t fit = static_cast<size_t>(r_max + p.s_splits);
+    const size_t off_o = p.off_counters + align256(static_cast<size_t>(total_q) * Hkv * 4);
+    const size_t off_lse = off_o + align256(fit * rows_total * D * 2);
+    p.bytes = std::max(p.bytes, off_lse + align256(fit * rows_total * 4));
+    if (!p.single && sched_override != CSP_SCHEDULE_FUSED) {
+      p.split_merge = true;
+      const int base = p.p_pairs * Hkv;
+      const double t_tile =
+          std::max(64.0 * 4.0 * D / 1024.0 / 20.0,
+                   std::min(256.0, static_cast<double>(total_q) * p.group) / 256.0);
+      const double suf_kb =
+          static_cast<double>(num_reqs) * Hkv * (0.5 * max_len + 64.0) * 4.0 * D / 1024.0;
+      double best = -1.0;
+      for (int r = 1; r <= r_max; ++r) {
+        const int64_t ctas = static_cast<int64_t>(base) * r;
+        const double t_pre = 4.0 + cdiv(key_tiles, r) * t_tile;
+        const double t =
+            std::max(cdiv64(ctas, sms) * t_pre, (ctas * t_pre + suf_kb / 20.0) / sms) +
+            0.2e-3 * static_cast<double>(rows_total) * (r + 1) * D / 128.0;
+        if (best < 0.0 || t < best) {
+          best = t;
+          p.p_splits = r;
+        }
+      }
+      if (ranges_override > 0) p.p_splits = std::min(ranges_override, r_max);
+      p.p_tiles_per_split = cdiv(key_tiles, p.p_splits);
+      p.p_slots = p.p_splits;
+      p.n_parts = p.p_slots + p.s_splits;
+      p.off_part_o = off_o;
+      p.off_part_lse = off_lse;
+    }
   }
   p.fused = cpl > 0 && !p.single &&
             (sched_override == CSP_SCHEDULE_FUSED || (sched_override < 0 && p.tc && kFusedByDefault));
@@ -711,10 +762,11 @@ int attention_call(const void* q, const void* k_cache, const void* v_cache, int3
   // suffix kernel merges, and several suffix splits count themselves in row-group
   // counters that start at zero in every call, whatever the workspace held.
   // The fused schedule counts prefix ranges and suffix splits in the same counters.
-  const bool merge_after = P.tc && cpl > 0 && !P.fused;
+  const bool merge_after = (P.tc || P.split_merge) && cpl > 0 && !P.fused;
   // the warp-MMA kernel with 2..8 key splits merges them inside a thread-block cluster
   // (distributed shared memory): no counters
-  const bool cluster = !P.tc && !P.fused && P.s_splits >= 2 && P.s_splits <= 8;
+  const bool cluster =
+      !P.tc && !P.fused && !P.split_merge && P.s_splits >= 2 && P.s_splits <= 8;
   if (P.n_parts > 0 && (P.s_splits > 1 || P.fused) && !merge_after && !cluster &&
       (e = cudaMemsetAsync(counters, 0, static_cast<size_t>(total_q) * Hkv * sizeof(int32_t),
                            stream)) != cudaSuccess)
@@ -779,6 +831,7 @@ int attention_call(const void* q, const void* k_cache, const void* v_cache, int3
   ga.lse = lse;
   ga.status = status;
   ga.cluster_splits = cluster;
+  ga.partials_only = merge_after;
   if (merge_after || cluster) ga.counters = nullptr;
   // concurrent with the prefix kernel (programmatic dependent launch) unless phase
   // events sit between the two

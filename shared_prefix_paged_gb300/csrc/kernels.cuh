@@ -101,6 +101,8 @@ struct PagedArgs {
   // The warp-MMA kernel with 2..8 key splits: the splits of a row tile run as one
   // thread-block cluster and merge through distributed shared memory (no counters).
   bool cluster_splits = false;
+  // write every split's partial slot and merge nothing (a merge kernel follows)
+  bool partials_only = false;
   // An FP8 (E4M3) KV cache (the *_f8 launchers): q then points at an f16 copy of the
   // queries, k and v at the E4M3 caches, and the V scale multiplies the normalised
   // rows (the K scale is folded into scale_log2).

@@ -337,7 +337,7 @@ __global__ void __launch_bounds__(kThreads)
   // one suffix split: this CTA merges its rows itself, in registers, with the prefix
   // slots; several splits: write a partial and let the last split merge, or (a cluster
   // of the splits) leave it in shared memory for the cluster merge below
-  const bool merge_in_place = partial && a.n_splits == 1;
+  const bool merge_in_place = partial && a.n_splits == 1 && !a.partials_only;
   const bool in_cluster = a.cluster_splits;
 
   {
@@ -471,7 +471,7 @@ __global__ void __launch_bounds__(kThreads)
     return;
   }
 
-  if (partial && !merge_in_place) {
+  if (partial && !merge_in_place && a.counters != nullptr) {
     // several splits: count in the row groups; the last split merges every slot
     const int tok_first = row0 / a.group;
     const int n_tok = (row0 + rows_here - 1) / a.group - tok_first + 1;
