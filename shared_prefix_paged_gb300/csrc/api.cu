@@ -182,6 +182,9 @@ struct LaunchPlan {
   // the two-kernel schedule with the warp-MMA suffix writing its partials and a merge
   // kernel after both phases (as after a tcgen05 suffix)
   bool split_merge = false;
+  // the cost models' estimates (us): the single kernel at its best number of ranges,
+  // the two-kernel schedule's split-merge at its best number of ranges
+  double est_single_us = 0.0, est_split_us = 0.0;
   // single-kernel decode schedule (decode_cascade.cu)
   bool single = false;
   int d_splits = 0, d_prefix_ctas = 0, d_prefix_units = 0, d_grid = 0, d_merge_rows = 0;
@@ -275,6 +278,40 @@ void make_plan(int num_reqs, int total_q, int max_q, int max_k, int cpl, int Hq,
   // kernel is taken only if the same model does not expect the two-kernel schedule to
   // be faster (a long prefix over many 256-row blocks leaves it too few SMs for one
   // of the phases).
+  // The two-kernel schedule for decode-shaped rows: the prefix kernel on some SMs, the
+  // warp-MMA suffix kernel writing its partials on the rest (neither waits for the
+  // other), then the slot merge kernel.  Its number of prefix key ranges and its time
+  // come from a cost model fitted to a sweep of N in {16..256} x P in {1024..16384}
+  // (S = 128, Hq 32, Hkv 8, D 128, 1-12 ranges) on one GB300: ~4 us of fixed cost, a
+  // prefix CTA ~4 us plus its 64-key tiles at the longer of the copy time (~40 GB/s per
+  // SM) and ~1 us per 256 rows, the suffix at ~20 GB/s per SM on the SMs the prefix
+  // leaves free and then on all, the merge ~0.05 ns per row and slot.  On that grid its
+  // pick was the best measured range count at 13 of 15 points and within 5% at the
+  // others.  Against an in-place merge (the suffix waiting for the whole prefix grid)
+  // this schedule was 20-27% faster at N >= 128.
+  int split_r = 1;
+  if (cpl > 0 && !p.tc) {
+    const int key_tiles = cdiv(cpl, 64);
+    const int r_max = std::min(16, key_tiles);
+    const int base = p.p_pairs * Hkv;
+    const double rows_all = static_cast<double>(total_q) * Hq;
+    const double t_tile = std::max(64.0 * 4.0 * D / 1024.0 / 40.0,
+                                   std::min(256.0, static_cast<double>(total_q) * p.group) / 256.0);
+    const double suf_kb =
+        static_cast<double>(num_reqs) * Hkv * (0.5 * max_len + 64.0) * 4.0 * D / 1024.0;
+    double best = -1.0;
+    for (int r = 1; r <= r_max; ++r) {
+      const int64_t ctas = static_cast<int64_t>(base) * r;
+      const double t_pre = 4.0 + cdiv(key_tiles, r) * t_tile;
+      const double t = 4.0 + std::max(cdiv64(ctas, sms) * t_pre, (ctas * t_pre + suf_kb / 20.0) / sms) +
+                       0.05e-3 * rows_all * (r + 1) * D / 128.0;
+      if (best < 0.0 || t < best) {
+        best = t;
+        split_r = r;
+      }
+    }
+    p.est_split_us = best;
+  }
   const int d_base = p.p_pairs * Hkv;
   if (cpl > 0 && static_cast<int64_t>(max_q) * p.group <= kDecodeRows && d_base <= sms) {
     const int pre_tiles = cdiv(cpl, 64);
@@ -329,8 +366,14 @@ void make_plan(int num_reqs, int total_q, int max_q, int max_k, int cpl, int Hq,
     const double two_us =
         pre2_us + 5.0 +
         std::max(0.0, static_cast<double>(units) * unit_us - free_sms * pre2_us) / sms;
+    p.est_single_us = best;
+    // the single kernel when the model expects it to beat both two-kernel variants
+    // (the one with an in-place merge, and, within the split-merge model's fitting
+    // range of at least 64 query rows per KV head, the split-merge one)
+    const bool split_fitted = static_cast<int64_t>(total_q) * p.group >= 64;
     p.single = sched_override == CSP_SCHEDULE_SINGLE ||
-               (sched_override < 0 && best <= two_us);
+               (sched_override < 0 && best <= two_us &&
+                (!split_fitted || best <= p.est_split_us));
     if (ranges_override > 0) s = std::min(ranges_override, s_max);
     double t_s;
     const int k = best_k(s, &t_s);
@@ -359,12 +402,13 @@ void make_plan(int num_reqs, int total_q, int max_q, int max_k, int cpl, int Hq,
   // warp-MMA suffix kernel writing its partials on the rest (neither waits for the
   // other), then the slot merge kernel.  The number of prefix key ranges comes from a
   // cost model fitted to a sweep of N in {16..256} x P in {1024..16384} (S = 128, Hq
-  // 32, Hkv 8, D 128) on one GB300: a prefix CTA costs ~4 us plus its 64-key tiles at
-  // the longer of the copy time (~20 GB/s per SM while the suffix streams too) and
-  // ~1 us per 256 rows; the suffix streams at ~20 GB/s per SM on the SMs the prefix
-  // leaves free and then on all; the merge costs ~0.2 ns per row and slot.  Against an
-  // in-place merge (the suffix waiting for the whole prefix grid) it was 20-27% faster
-  // at N >= 128.  The workspace fits up to 16 ranges (a caller's override).
+  // 32, Hkv 8, D 128, 1-12 ranges) on one GB300: a prefix CTA costs ~4 us plus its
+  // 64-key tiles at the longer of the copy time (~40 GB/s per SM) and ~1 us per 256
+  // rows; the suffix streams at ~20 GB/s per SM on the SMs the prefix leaves free and
+  // then on all; the merge costs ~0.05 ns per row and slot.  On that grid its pick was
+  // the best measured range count at 13 of 15 points and within 5% at the others.
+  // Against an in-place merge (the suffix waiting for the whole prefix grid) this
+  // schedule was 20-27% faster at N >= 128.  The workspace fits up to 16 ranges.
   if (cpl > 0 && !p.tc) {
     const int key_tiles = cdiv(cpl, 64);
     const int r_max = std::min(16, key_tiles);
@@ -377,24 +421,7 @@ void make_plan(int num_reqs, int total_q, int max_q, int max_k, int cpl, int Hq,
     p.bytes = std::max(p.bytes, off_lse + align256(fit * rows_total * 4));
     if (!p.single && sched_override != CSP_SCHEDULE_FUSED) {
       p.split_merge = true;
-      const int base = p.p_pairs * Hkv;
-      const double t_tile =
-          std::max(64.0 * 4.0 * D / 1024.0 / 20.0,
-                   std::min(256.0, static_cast<double>(total_q) * p.group) / 256.0);
-      const double suf_kb =
-          static_cast<double>(num_reqs) * Hkv * (0.5 * max_len + 64.0) * 4.0 * D / 1024.0;
-      double best = -1.0;
-      for (int r = 1; r <= r_max; ++r) {
-        const int64_t ctas = static_cast<int64_t>(base) * r;
-        const double t_pre = 4.0 + cdiv(key_tiles, r) * t_tile;
-        const double t =
-            std::max(cdiv64(ctas, sms) * t_pre, (ctas * t_pre + suf_kb / 20.0) / sms) +
-            0.2e-3 * static_cast<double>(rows_total) * (r + 1) * D / 128.0;
-        if (best < 0.0 || t < best) {
-          best = t;
-          p.p_splits = r;
-        }
-      }
+      p.p_splits = split_r;
       if (ranges_override > 0) p.p_splits = std::min(ranges_override, r_max);
       p.p_tiles_per_split = cdiv(key_tiles, p.p_splits);
       p.p_slots = p.p_splits;
