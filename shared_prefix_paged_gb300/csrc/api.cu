@@ -282,29 +282,32 @@ void make_plan(int num_reqs, int total_q, int max_q, int max_k, int cpl, int Hq,
   // warp-MMA suffix kernel writing its partials on the rest (neither waits for the
   // other), then the slot merge kernel.  Its number of prefix key ranges and its time
   // come from a cost model fitted to a sweep of N in {16..256} x P in {1024..16384}
-  // (S = 128, Hq 32, Hkv 8, D 128, 1-12 ranges) on one GB300: ~4 us of fixed cost, a
-  // prefix CTA ~4 us plus its 64-key tiles at the longer of the copy time (~40 GB/s per
-  // SM) and ~1 us per 256 rows, the suffix at ~20 GB/s per SM on the SMs the prefix
-  // leaves free and then on all, the merge ~0.05 ns per row and slot.  On that grid its
-  // pick was the best measured range count at 13 of 15 points and within 5% at the
-  // others.  Against an in-place merge (the suffix waiting for the whole prefix grid)
-  // this schedule was 20-27% faster at N >= 128.
+  // (S = 128, Hq 32, Hkv 8, D 128, 1-12 ranges) and the long-prefix batch (N = 256,
+  // P = 16384, S up to 1024, Hq 64) on one GB300: ~6 us of fixed cost; a prefix CTA
+  // ~3 us plus its 64-key tiles at the longer of the copy time (~40 GB/s per SM) and
+  // ~0.9 us per 256 rows; a suffix unit (request, KV head) ~1 us plus its bytes at
+  // ~40 GB/s per SM, on the SMs the prefix leaves free and then on all; the merge
+  // ~0.1 ns per row and slot.  On those 16 shapes its pick was the best measured range
+  // count at 14 and within 5% at the other two.  Against an in-place merge (the suffix
+  // waiting for the whole prefix grid) this schedule was 20-27% faster at N >= 128.
   int split_r = 1;
   if (cpl > 0 && !p.tc) {
     const int key_tiles = cdiv(cpl, 64);
     const int r_max = std::min(16, key_tiles);
     const int base = p.p_pairs * Hkv;
     const double rows_all = static_cast<double>(total_q) * Hq;
-    const double t_tile = std::max(64.0 * 4.0 * D / 1024.0 / 40.0,
-                                   std::min(256.0, static_cast<double>(total_q) * p.group) / 256.0);
-    const double suf_kb =
-        static_cast<double>(num_reqs) * Hkv * (0.5 * max_len + 64.0) * 4.0 * D / 1024.0;
+    const double t_tile =
+        std::max(64.0 * 4.0 * D / 1024.0 / 40.0,
+                 0.9 * std::min(256.0, static_cast<double>(total_q) * p.group) / 256.0);
+    const double suf_sm_us = static_cast<double>(num_reqs) * Hkv *
+                             (1.0 + (0.5 * max_len + 64.0) * 4.0 * D / 1024.0 / 40.0);
     double best = -1.0;
     for (int r = 1; r <= r_max; ++r) {
       const int64_t ctas = static_cast<int64_t>(base) * r;
-      const double t_pre = 4.0 + cdiv(key_tiles, r) * t_tile;
-      const double t = 4.0 + std::max(cdiv64(ctas, sms) * t_pre, (ctas * t_pre + suf_kb / 20.0) / sms) +
-                       0.05e-3 * rows_all * (r + 1) * D / 128.0;
+      const double t_pre = 3.0 + cdiv(key_tiles, r) * t_tile;
+      const double t = 6.0 +
+                       std::max(cdiv64(ctas, sms) * t_pre, (ctas * t_pre + suf_sm_us) / sms) +
+                       0.1e-3 * rows_all * (r + 1) * D / 128.0;
       if (best < 0.0 || t < best) {
         best = t;
         split_r = r;
