@@ -266,9 +266,8 @@ class DeviceRun:
         self.suffix_kernel = ("paged_tc_kernel"
                               if b.max_seqlen_q * (b.num_q_heads // b.num_kv_heads) > 16
                               else "paged_attn_kernel")
-        # after a prefix phase the tcgen05 suffix leaves the merge to a third kernel
-        self.merge_after = (self.use_cascade and not self.single and self.cpl > 0 and
-                            self.suffix_kernel == "paged_tc_kernel")
+        # the two-kernel schedule's suffix (either kernel) leaves the merge to a third one
+        self.merge_after = self.use_cascade and not self.single and self.cpl > 0
 
     def setup_levels(self, max_levels: int):
         """The multi-level plan of the batch and its workspace."""
