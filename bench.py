@@ -402,12 +402,48 @@ def phase_times(run: DeviceRun, rounds: int = 16, batches: int = 3):
 
 
 def e2e_steps(run: DeviceRun, steps: int):
-    """Public-API steps from pinned host memory: one H2D copy of the step's inputs (q,
-    block table, cu_seqlens, seq_lens packed in one pinned buffer), the host planner
-    (csp.Planner), the attention call (csp.PreparedCall), one D2H copy of out and lse
-    (adjacent in one device buffer), then the host waits for the result.  Returns the
-    rate, the bytes copied each way per step, the step count and the average time of
-    each part (host: perf_counter; device: CUDA events on the stream)."""
+    """End-to-end steps through the C ABI with host buffers: `cascade_step_host` (one
+    call per step) copies the step's q, block table, cu_seqlens and seq_lens from
+    pinned host memory to the device, plans on the host, runs the attention call,
+    copies out and lse back to pinned host memory and waits.  The KV caches stay
+    resident (R copies, rotated as in the device timing).  Returns the rate, the bytes
+    copied each way per step and the step count."""
+    import torch
+    from shared_prefix_paged_gb300 import csp
+    b = run.b
+    dev = run.dev
+    pin = lambda t: t.contiguous().pin_memory()
+    q_h = pin(b.q)
+    bt_h = pin(torch.from_numpy(np.ascontiguousarray(b.block_table)))
+    cu_h = pin(torch.from_numpy(b.cu_seqlens_q))
+    sl_h = pin(torch.from_numpy(b.seq_lens))
+    nc_h = pin(torch.from_numpy(b.num_computed_tokens))
+    out_h = torch.empty(b.q.shape, dtype=torch.bfloat16).pin_memory()
+    lse_h = torch.empty((b.total_q, b.num_q_heads), dtype=torch.float32).pin_memory()
+    need = max(csp.step_scratch_size(b.cu_seqlens_q, b.seq_lens, b.block_table.shape[1], c,
+                                     b.num_q_heads, b.num_kv_heads, b.head_dim)
+               for c in (0, run.cpl))
+    scratch = csp.alloc_workspace(need, dev)
+    calls = [csp.HostStep(q_h, bt_h, cu_h, sl_h, nc_h, run.k[i], run.v[i],
+                          softmax_scale=b.scale, out=out_h, lse=lse_h, scratch=scratch)
+             for i in range(run.R)]
+    h2d = sum(t.numel() * t.element_size() for t in (q_h, bt_h, cu_h, sl_h))
+    d2h = out_h.numel() * 2 + lse_h.numel() * 4
+    for i in range(5):
+        calls[i % run.R]()
+    t0 = time.perf_counter()
+    for s in range(steps):
+        calls[s % run.R]()
+    el = time.perf_counter() - t0
+    return b.total_q * steps / el, h2d, d2h, steps
+
+
+def e2e_breakdown(run: DeviceRun, steps: int):
+    """The same step's parts issued one by one from Python, for a breakdown: one H2D
+    copy of the step's inputs (packed in one pinned buffer), the host planner
+    (csp.Planner), the attention call (csp.PreparedCall), one D2H copy of out and lse,
+    then the host waits; host parts by perf_counter, device parts by CUDA events on the
+    stream.  Returns the average time of each part."""
     import torch
     from shared_prefix_paged_gb300 import csp
     b = run.b
@@ -489,7 +525,7 @@ def e2e_steps(run: DeviceRun, steps: int):
                  "device_plan_to_kernel_end_us": round(dev_ms[1] * 1e3, 2),
                  "device_d2h_us": round(dev_ms[2] * 1e3, 2),
                  "step_us": round(el / steps * 1e6, 2)}
-    return b.total_q * steps / el, h2d, d2h, steps, breakdown
+    return breakdown
 
 
 def cpu_oracle_rate(b, seconds: float, rng_seed=0):
@@ -665,13 +701,16 @@ def run_ours(args, dist: Dist):
                           "kv_bytes": int(accounting.flat_kv_tokens(b.seq_lens) *
                                           accounting.kv_bytes_per_token(b.num_kv_heads,
                                                                         b.head_dim))}
-        e_qps, h2d, d2h, e_steps, bd = e2e_steps(run, min(K, 3000))
+        e_qps, h2d, d2h, e_steps = e2e_steps(run, min(K, 3000))
+        bd = e2e_breakdown(run, min(K, 500))
         e_total, _ = aggregate(dist, e_qps, 1.0)
         result["e2e"] = {"value": round(e_total, 1), "unit": UNIT, "h2d_bytes_per_step": h2d,
-                         "d2h_bytes_per_step": d2h, "steps": e_steps, "breakdown": bd,
-                         "note": "one pinned H2D copy of q + block table + cu_seqlens + "
-                                 "seq_lens, host planner, the attention call, one D2H copy "
-                                 "of out + lse, host waits each step; KV cache resident"}
+                         "d2h_bytes_per_step": d2h, "steps": e_steps,
+                         "call": "cascade_step_host (C ABI, host buffers): H2D of q, block "
+                                 "table, cu_seqlens, seq_lens from pinned memory, host "
+                                 "planner, attention call, D2H of out + lse, host waits; "
+                                 "KV cache resident",
+                         "breakdown_python_parts": bd}
         if dist.rank == 0 and dist.world == 1:
             rate, threads, rows = cpu_oracle_rate(b, args.cpu_seconds)
             result["cpu_baseline"] = {"value": round(rate, 3), "unit": UNIT, "cores": threads,

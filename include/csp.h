@@ -560,6 +560,48 @@ CSP_API int cascade_attn_levels(const void* q, const void* k_cache, const void* 
                                 void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * cascade_step_host — one whole step from host buffers: copies the step's q, block
+ * table, cu_seqlens_q and seq_lens to the device, plans on the host (cascade_plan with
+ * `mode`; the standard path when it declines cascade), runs the attention call, copies
+ * out and lse back and waits for them (a stream synchronisation), so out and lse hold
+ * the result when it returns.  For a user whose batch lives in host memory; pinned
+ * (page-locked) host buffers let the copies run asynchronously.
+ *
+ *   q                    host bf16 [total_q, num_q_heads, head_dim]
+ *   block_table          host int32 [num_reqs, bt_row_stride]
+ *   cu_seqlens_q         host int32 [num_reqs + 1]
+ *   seq_lens             host int32 [num_reqs]
+ *   num_computed_tokens  host int32 [num_reqs] (the planner's cap)
+ *   k_cache, v_cache     device, as for cascade_attn (resident, as in serving)
+ *   out, lse             host bf16 [total_q, num_q_heads, head_dim], fp32 [total_q,
+ *                        num_q_heads] (natural log), written
+ *   device_scratch       device, 256-byte aligned, csp_step_scratch_size bytes for the
+ *                        prefix length the planner returns (0 and that length cover both
+ *                        paths), zero-filled before its first use: it holds the
+ *                        attention call's workspace at its start, then the step's device
+ *                        copies
+ *   common_prefix_len_out  the prefix length used (0: the standard path), or NULL
+ * Returns CSP_OK, the planner's or cascade_attn's errors (nothing launched on an
+ * argument error), CSP_ERR_WORKSPACE, or CSP_ERR_CUDA.
+ *
+ * csp_step_scratch_size — device_scratch bytes for such a step with a given prefix
+ * length (host arrays as above).
+ */
+CSP_API int csp_step_scratch_size(int32_t num_reqs, int32_t total_q, const int32_t* cu_seqlens_q,
+                                  const int32_t* seq_lens, int64_t bt_row_stride,
+                                  int32_t common_prefix_len, int32_t num_q_heads,
+                                  int32_t num_kv_heads, int32_t head_dim, size_t* bytes_out);
+CSP_API int cascade_step_host(const void* q, const int32_t* block_table, int64_t bt_row_stride,
+                              const int32_t* cu_seqlens_q, const int32_t* seq_lens,
+                              const int32_t* num_computed_tokens, int32_t num_reqs,
+                              int32_t total_q, const void* k_cache, const void* v_cache,
+                              int32_t num_blocks, int32_t block_size, int32_t num_q_heads,
+                              int32_t num_kv_heads, int32_t head_dim, float softmax_scale,
+                              int32_t mode, void* out, float* lse, void* device_scratch,
+                              size_t scratch_bytes, void* stream,
+                              int32_t* common_prefix_len_out);
+
+/*
  * csp_workspace_status — copies the workspace status word to the host (a blocking
  * copy on `stream`).  0 means no kernel reported a problem since the workspace was
  * zero-filled; CSP_ERR_TIMEOUT means a bounded wait gave up.  Writes *status_out.

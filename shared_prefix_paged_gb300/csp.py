@@ -35,7 +35,8 @@ EXPORTS = ("cascade_plan", "csp_workspace_size", "cascade_attn", "cascade_attn_t
            "csp_noalloc_status", "csp_cascade_schedule", "csp_validate_batch",
            "csp_apply_sinks", "cascade_plan_device", "cascade_attn_device_plan",
            "cascade_plan_levels", "csp_workspace_size_levels", "cascade_attn_levels",
-           "csp_workspace_size_fp8kv", "cascade_attn_fp8kv", "paged_attn_fp8kv")
+           "csp_workspace_size_fp8kv", "cascade_attn_fp8kv", "paged_attn_fp8kv",
+           "csp_step_scratch_size", "cascade_step_host")
 
 _lock = threading.Lock()
 _lib: Optional[ctypes.CDLL] = None
@@ -93,6 +94,9 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         lib.csp_workspace_size_fp8kv.argtypes = [i32, i32, i32, i32, i32, i32, i32, i32, p]
         lib.cascade_attn_fp8kv.argtypes = attn + [i32] + tail8
         lib.paged_attn_fp8kv.argtypes = attn + tail8
+        lib.csp_step_scratch_size.argtypes = [i32, i32, p, p, i64, i32, i32, i32, i32, p]
+        lib.cascade_step_host.argtypes = [p, p, i64, p, p, p, i32, i32, p, p, i32, i32, i32,
+                                          i32, i32, f32, i32, p, p, p, sz, p, p]
         lib.csp_status_string.argtypes = [ctypes.c_int]
         lib.csp_status_string.restype = ctypes.c_char_p
         for name in ("cascade_plan", "csp_workspace_size", "cascade_attn", "cascade_attn_timed",
@@ -102,7 +106,7 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
                      "csp_apply_sinks", "cascade_plan_device", "cascade_attn_device_plan",
                      "cascade_plan_levels", "csp_workspace_size_levels",
                      "cascade_attn_levels", "csp_workspace_size_fp8kv", "cascade_attn_fp8kv",
-                     "paged_attn_fp8kv"):
+                     "paged_attn_fp8kv", "csp_step_scratch_size", "cascade_step_host"):
             getattr(lib, name).restype = ctypes.c_int
         _lib = lib
         return lib
@@ -446,6 +450,47 @@ def attn_fp8kv(q, k_cache, v_cache, block_table, cu_seqlens_q, seqused_k, *, max
     name = "cascade_attn_fp8kv" if cpl > 0 else "paged_attn_fp8kv"
     _check(getattr(lib, name)(*args), name)
     return out, lse
+
+
+class HostStep:
+    """cascade_step_host on fixed host arrays (numpy, ideally in pinned memory) and device
+    caches: arguments marshalled once; each call copies the step's inputs in, plans,
+    runs the attention call, copies out / lse back into the given host arrays and
+    waits.  Returns the prefix length used (0: the standard path)."""
+
+    def __init__(self, q, block_table, cu_seqlens_q, seq_lens, num_computed_tokens, k_cache,
+                 v_cache, *, softmax_scale, out, lse, scratch, mode=MODE_AUTO, stream=None):
+        lib = load()
+        self._keep = (q, block_table, cu_seqlens_q, seq_lens, num_computed_tokens, out, lse)
+        num_blocks, bs, hkv, d = k_cache.shape
+        total_q, hq, _ = q.shape
+        n = int(seq_lens.shape[0])
+        self._cpl = ctypes.c_int32(0)
+        ptr = lambda a: ctypes.c_void_p(a.ctypes.data if hasattr(a, "ctypes") else a.data_ptr())
+        self._fn = lib.cascade_step_host
+        self._args = (ptr(q), ptr(block_table), int(block_table.shape[1]), ptr(cu_seqlens_q),
+                      ptr(seq_lens), ptr(num_computed_tokens), n, total_q, _ptr(k_cache),
+                      _ptr(v_cache), num_blocks, bs, hq, hkv, d, float(softmax_scale), mode,
+                      ptr(out), ptr(lse), _ptr(scratch), scratch.numel(),
+                      _stream_ptr(stream, k_cache.device), ctypes.byref(self._cpl))
+
+    def __call__(self) -> int:
+        _check(self._fn(*self._args), "cascade_step_host")
+        return int(self._cpl.value)
+
+
+def step_scratch_size(cu_seqlens_q, seq_lens, bt_row_stride, common_prefix_len, num_q_heads,
+                      num_kv_heads, head_dim) -> int:
+    lib = load()
+    cu = _host_i32(cu_seqlens_q)
+    sl = _host_i32(seq_lens)
+    n = int(sl.shape[0])
+    out = ctypes.c_size_t(0)
+    _check(lib.csp_step_scratch_size(n, int(cu[-1]) if n else 0, cu.ctypes.data,
+                                     sl.ctypes.data if n else None, int(bt_row_stride),
+                                     int(common_prefix_len), num_q_heads, num_kv_heads,
+                                     head_dim, ctypes.byref(out)), "csp_step_scratch_size")
+    return int(out.value)
 
 
 def apply_sinks(out, lse, sinks, *, stream=None):

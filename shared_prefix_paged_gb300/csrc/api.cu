@@ -1391,6 +1391,122 @@ int cascade_attn_levels(const void* q, const void* k_cache, const void* v_cache,
   return CSP_OK;
 }
 
+// ---------------------------------------------------------------- host step --
+// One step from host buffers: the layout of the device scratch (256-byte aligned
+// pieces): the attention call's workspace first (its header — the status word and the
+// single kernel's barrier — stays at the scratch's start whatever the batch), then q,
+// block table, cu_seqlens_q, seq_lens, out and lse.  Fills the sizes and maxima for the
+// batch; returns CSP_OK or an argument error.
+struct StepLayout {
+  int32_t max_q = 0, max_k = 0;
+  size_t off_q = 0, off_bt = 0, off_cu = 0, off_sl = 0, off_out = 0, off_lse = 0, off_ws = 0;
+  size_t q_bytes = 0, bt_bytes = 0, out_bytes = 0, lse_bytes = 0, ws_bytes = 0, total = 0;
+};
+
+int step_layout(int32_t num_reqs, int32_t total_q, const int32_t* cu_seqlens_q,
+                const int32_t* seq_lens, int64_t bt_row_stride, int32_t cpl, int32_t Hq,
+                int32_t Hkv, int32_t D, StepLayout* L) {
+  if (num_reqs < 0 || total_q < 0 || bt_row_stride < 0) return CSP_ERR_INVALID_ARG;
+  if (num_reqs > 0 && (!cu_seqlens_q || !seq_lens)) return CSP_ERR_INVALID_ARG;
+  StepLayout l;
+  if (num_reqs > 0 && (cu_seqlens_q[0] != 0 || cu_seqlens_q[num_reqs] != total_q))
+    return CSP_ERR_INVALID_ARG;
+  for (int r = 0; r < num_reqs; ++r) {
+    const int32_t ql = cu_seqlens_q[r + 1] - cu_seqlens_q[r];
+    if (ql < 0 || seq_lens[r] < ql) return CSP_ERR_INVALID_ARG;
+    l.max_q = std::max(l.max_q, ql);
+    l.max_k = std::max(l.max_k, seq_lens[r]);
+  }
+  int st = csp_workspace_size(num_reqs, total_q, l.max_q, l.max_k, cpl, Hq, Hkv, D, &l.ws_bytes);
+  if (st != CSP_OK) return st;
+  l.q_bytes = static_cast<size_t>(total_q) * Hq * D * 2;
+  l.bt_bytes = static_cast<size_t>(num_reqs) * bt_row_stride * 4;
+  l.out_bytes = l.q_bytes;
+  l.lse_bytes = static_cast<size_t>(total_q) * Hq * 4;
+  l.off_ws = 0;
+  l.off_q = align256(l.ws_bytes);
+  l.off_bt = l.off_q + align256(l.q_bytes);
+  l.off_cu = l.off_bt + align256(l.bt_bytes);
+  l.off_sl = l.off_cu + align256(static_cast<size_t>(num_reqs + 1) * 4);
+  l.off_out = l.off_sl + align256(static_cast<size_t>(num_reqs) * 4);
+  l.off_lse = l.off_out + align256(l.out_bytes);
+  l.total = l.off_lse + align256(l.lse_bytes);
+  *L = l;
+  return CSP_OK;
+}
+
+int csp_step_scratch_size(int32_t num_reqs, int32_t total_q, const int32_t* cu_seqlens_q,
+                          const int32_t* seq_lens, int64_t bt_row_stride,
+                          int32_t common_prefix_len, int32_t num_q_heads, int32_t num_kv_heads,
+                          int32_t head_dim, size_t* bytes_out) {
+  if (!bytes_out) return CSP_ERR_INVALID_ARG;
+  StepLayout L;
+  const int st = step_layout(num_reqs, total_q, cu_seqlens_q, seq_lens, bt_row_stride,
+                             common_prefix_len, num_q_heads, num_kv_heads, head_dim, &L);
+  if (st != CSP_OK) return st;
+  *bytes_out = L.total;
+  return CSP_OK;
+}
+
+int cascade_step_host(const void* q, const int32_t* block_table, int64_t bt_row_stride,
+                      const int32_t* cu_seqlens_q, const int32_t* seq_lens,
+                      const int32_t* num_computed_tokens, int32_t num_reqs, int32_t total_q,
+                      const void* k_cache, const void* v_cache, int32_t num_blocks,
+                      int32_t block_size, int32_t num_q_heads, int32_t num_kv_heads,
+                      int32_t head_dim, float softmax_scale, int32_t mode, void* out, float* lse,
+                      void* device_scratch, size_t scratch_bytes, void* stream_ptr,
+                      int32_t* common_prefix_len_out) {
+  if (total_q == 0 || num_reqs == 0) {
+    if (common_prefix_len_out) *common_prefix_len_out = 0;
+    return CSP_OK;
+  }
+  if (!q || !block_table || !cu_seqlens_q || !seq_lens || !num_computed_tokens || !out ||
+      !lse)
+    return CSP_ERR_INVALID_ARG;
+  int32_t cpl = 0, use = 0;
+  int st = cascade_plan(block_table, bt_row_stride, num_reqs, seq_lens, num_computed_tokens,
+                        block_size, num_q_heads, num_kv_heads, head_dim, 0, mode, &cpl, &use);
+  if (st != CSP_OK) return st;
+  if (!use) cpl = 0;
+  StepLayout L;
+  if ((st = step_layout(num_reqs, total_q, cu_seqlens_q, seq_lens, bt_row_stride, cpl,
+                        num_q_heads, num_kv_heads, head_dim, &L)) != CSP_OK)
+    return st;
+  if (!device_scratch || (reinterpret_cast<uintptr_t>(device_scratch) & 255) != 0 ||
+      scratch_bytes < L.total)
+    return CSP_ERR_WORKSPACE;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+  uint8_t* d = static_cast<uint8_t*>(device_scratch);
+  cudaError_t e;
+  // the step's inputs in: four copies (from pinned host memory they run asynchronously)
+  if ((e = cudaMemcpyAsync(d + L.off_q, q, L.q_bytes, cudaMemcpyHostToDevice, stream)) !=
+          cudaSuccess ||
+      (e = cudaMemcpyAsync(d + L.off_bt, block_table, L.bt_bytes, cudaMemcpyHostToDevice,
+                           stream)) != cudaSuccess ||
+      (e = cudaMemcpyAsync(d + L.off_cu, cu_seqlens_q, static_cast<size_t>(num_reqs + 1) * 4,
+                           cudaMemcpyHostToDevice, stream)) != cudaSuccess ||
+      (e = cudaMemcpyAsync(d + L.off_sl, seq_lens, static_cast<size_t>(num_reqs) * 4,
+                           cudaMemcpyHostToDevice, stream)) != cudaSuccess)
+    return cuda_fail(e);
+  st = attention_call(d + L.off_q, k_cache, v_cache, num_blocks,
+                      reinterpret_cast<const int32_t*>(d + L.off_bt), bt_row_stride,
+                      reinterpret_cast<const int32_t*>(d + L.off_cu),
+                      reinterpret_cast<const int32_t*>(d + L.off_sl), num_reqs, total_q, L.max_q,
+                      L.max_k, cpl, block_size, num_q_heads, num_kv_heads, head_dim,
+                      softmax_scale, d + L.off_out, reinterpret_cast<float*>(d + L.off_lse),
+                      d + L.off_ws, L.ws_bytes, stream);
+  if (st != CSP_OK) return st;
+  // the result out, and the host waits for it
+  if ((e = cudaMemcpyAsync(out, d + L.off_out, L.out_bytes, cudaMemcpyDeviceToHost, stream)) !=
+          cudaSuccess ||
+      (e = cudaMemcpyAsync(lse, d + L.off_lse, L.lse_bytes, cudaMemcpyDeviceToHost, stream)) !=
+          cudaSuccess ||
+      (e = cudaStreamSynchronize(stream)) != cudaSuccess)
+    return cuda_fail(e);
+  if (common_prefix_len_out) *common_prefix_len_out = cpl;
+  return CSP_OK;
+}
+
 int csp_apply_sinks(void* out, float* lse, const float* sinks, int32_t num_tokens,
                     int32_t num_heads, int32_t head_dim, void* stream) {
   if (num_tokens < 0 || num_heads <= 0 || head_dim <= 0 || head_dim % 8 != 0 ||

@@ -184,3 +184,25 @@ def test_fp8kv_argument_errors_launch_nothing():
     args_flat = args[:12] + args[13:]
     assert lib.paged_attn_fp8kv(*args_flat, 0.0, 1.0, p, None, p, 4096, None) == \
         csp.CSP_ERR_INVALID_ARG
+
+
+def test_step_scratch_size_checks_the_batch():
+    b = workloads.tiny_decode()
+    lib = csp.load()
+    out = ctypes.c_size_t(0)
+    cu = np.ascontiguousarray(b.cu_seqlens_q, np.int32)
+    sl = np.ascontiguousarray(b.seq_lens, np.int32)
+    w = b.block_table.shape[1]
+    good = lib.csp_step_scratch_size(b.num_reqs, b.total_q, cu.ctypes.data, sl.ctypes.data, w,
+                                     0, 8, 2, 64, ctypes.byref(out))
+    # a valid batch passes the host checks; without a GPU the device query then fails
+    assert good in (csp.CSP_OK, csp.CSP_ERR_CUDA)
+    bad = cu.copy()
+    bad[-1] += 1                                    # total_q disagrees with cu_seqlens_q
+    assert lib.csp_step_scratch_size(b.num_reqs, b.total_q, bad.ctypes.data, sl.ctypes.data, w,
+                                     0, 8, 2, 64, ctypes.byref(out)) == csp.CSP_ERR_INVALID_ARG
+    short = sl.copy()
+    short[0] = 0                                    # fewer keys than queries
+    assert lib.csp_step_scratch_size(b.num_reqs, b.total_q, cu.ctypes.data, short.ctypes.data,
+                                     w, 0, 8, 2, 64, ctypes.byref(out)) == \
+        csp.CSP_ERR_INVALID_ARG
