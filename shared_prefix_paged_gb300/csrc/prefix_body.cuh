@@ -578,19 +578,22 @@ __device__ __forceinline__ void prefix_range(const CUtensorMap* tm_q_p,
           tmem_st32(tO + c * 32, o);
         }
       }
-      // p = 2^(s * scale * log2(e) - m): one FFMA and one ex2 per score
+      // p = 2^(s * scale * log2(e) - m): one ex2 per score, the scaling and the row sum
+      // as paired fp32 instructions (two scores each)
       uint32_t pw[kKeysN / 2];
-      float sum4[4] = {0.f, 0.f, 0.f, 0.f};
+      float2 sum2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
       // a row whose keys so far are all masked keeps m_run = -inf: its p are 0
       const float neg_m = (kCausal && m_run == -INFINITY) ? 0.f : -m_run;
+      const float2 sc2 = make_float2(a.scale_log2, a.scale_log2);
+      const float2 nm2 = make_float2(neg_m, neg_m);
 #pragma unroll
       for (int j = 0; j < kKeysN / 2; ++j) {
-        const float p0 = fast_exp2(fmaf(sv[2 * j], a.scale_log2, neg_m));
-        const float p1 = fast_exp2(fmaf(sv[2 * j + 1], a.scale_log2, neg_m));
-        sum4[j & 3] += p0 + p1;
-        pw[j] = kF8 ? pack_f16x2(p0, p1) : pack_bf16x2(p0, p1);
+        const float2 x = fma_f32x2(make_float2(sv[2 * j], sv[2 * j + 1]), sc2, nm2);
+        const float2 pp = make_float2(fast_exp2(x.x), fast_exp2(x.y));
+        sum2[j & 1] = add_f32x2(sum2[j & 1], pp);
+        pw[j] = kF8 ? pack_f16x2(pp.x, pp.y) : pack_bf16x2(pp.x, pp.y);
       }
-      l_run += (sum4[0] + sum4[1]) + (sum4[2] + sum4[3]);
+      l_run += (sum2[0].x + sum2[1].x) + (sum2[0].y + sum2[1].y);
       tmem_st32_u(t_lane + (i & 1) * kKeysN, pw);
       tmem_wait_st();
       tc_fence_before();
