@@ -353,6 +353,14 @@ __device__ __forceinline__ float2 fma_f32x2(float2 a, float2 b, float2 c) {
   return *reinterpret_cast<const float2*>(&r);
 }
 
+__device__ __forceinline__ float2 mul_f32x2(float2 a, float2 b) {
+  uint64_t r;
+  asm("mul.rn.f32x2 %0, %1, %2;"
+      : "=l"(r)
+      : "l"(*reinterpret_cast<const uint64_t*>(&a)), "l"(*reinterpret_cast<const uint64_t*>(&b)));
+  return *reinterpret_cast<const float2*>(&r);
+}
+
 __device__ __forceinline__ float2 add_f32x2(float2 a, float2 b) {
   uint64_t r;
   asm("add.rn.f32x2 %0, %1, %2;"

@@ -356,13 +356,16 @@ __device__ __forceinline__ void consume_items(const DecodeArgs& a, uint8_t* ring
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         float mx = -INFINITY;
+        const float2 sc2 = make_float2(p.scale_log2, p.scale_log2);
 #pragma unroll
         for (int nt = 0; nt < 2 * kB; ++nt) {
+          // the two scores of a pair scaled in one paired instruction, then masked
+          const float2 s2 = mul_f32x2(make_float2(sacc[nt][2 * h], sacc[nt][2 * h + 1]), sc2);
 #pragma unroll
           for (int e = 0; e < 2; ++e) {
             const int kabs = key0 + nt * 8 + (lane & 3) * 2 + e;
             float& sref = sacc[nt][2 * h + e];
-            sref = (kabs < c_seq && kabs <= pos[h]) ? sref * p.scale_log2 : -INFINITY;
+            sref = (kabs < c_seq && kabs <= pos[h]) ? (e ? s2.y : s2.x) : -INFINITY;
             mx = fmaxf(mx, sref);
           }
         }
@@ -382,17 +385,16 @@ __device__ __forceinline__ void consume_items(const DecodeArgs& a, uint8_t* ring
           m_run[h] = mx;
         }
         const float m_use = (m_run[h] == -INFINITY) ? 0.f : m_run[h];
-        float sum = 0.f;
+        float2 sum2 = make_float2(0.f, 0.f);
+        const float2 nm2 = make_float2(-m_use, -m_use);
 #pragma unroll
         for (int nt = 0; nt < 2 * kB; ++nt) {
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            float& sref = sacc[nt][2 * h + e];
-            sref = fast_exp2(sref - m_use);
-            sum += sref;
-          }
+          const float2 x = add_f32x2(make_float2(sacc[nt][2 * h], sacc[nt][2 * h + 1]), nm2);
+          sacc[nt][2 * h] = fast_exp2(x.x);
+          sacc[nt][2 * h + 1] = fast_exp2(x.y);
+          sum2 = add_f32x2(sum2, make_float2(sacc[nt][2 * h], sacc[nt][2 * h + 1]));
         }
-        l_run[h] += sum;
+        l_run[h] += sum2.x + sum2.y;
       }
       // O += P V over the same keys
 #pragma unroll

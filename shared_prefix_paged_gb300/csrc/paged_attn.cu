@@ -250,13 +250,16 @@ __global__ void __launch_bounds__(kThreads)
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       float mx = -INFINITY;
+      const float2 sc2 = make_float2(a.scale_log2, a.scale_log2);
 #pragma unroll
       for (int nt = 0; nt < kNT; ++nt) {
+        // the two scores of a pair scaled in one paired instruction, then masked
+        const float2 s2 = mul_f32x2(make_float2(sacc[nt][2 * h], sacc[nt][2 * h + 1]), sc2);
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
           const int kabs = kt0 + kw0 + nt * 8 + (lane & 3) * 2 + e;
           float& sref = sacc[nt][2 * h + e];
-          sref = (kabs < kend && kabs <= pos[h]) ? sref * a.scale_log2 : -INFINITY;
+          sref = (kabs < kend && kabs <= pos[h]) ? (e ? s2.y : s2.x) : -INFINITY;
           mx = fmaxf(mx, sref);
         }
       }
@@ -265,22 +268,23 @@ __global__ void __launch_bounds__(kThreads)
       const float m_new = fmaxf(m_run[h], mx);
       const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
       const float alpha = exp2f(m_run[h] - m_use);
-      float sum = 0.f;
+      float2 sum2 = make_float2(0.f, 0.f);
+      const float2 nm2 = make_float2(-m_use, -m_use);
 #pragma unroll
       for (int nt = 0; nt < kNT; ++nt) {
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          float& sref = sacc[nt][2 * h + e];
-          sref = exp2f(sref - m_use);
-          sum += sref;
-        }
+        const float2 x = add_f32x2(make_float2(sacc[nt][2 * h], sacc[nt][2 * h + 1]), nm2);
+        sacc[nt][2 * h] = exp2f(x.x);
+        sacc[nt][2 * h + 1] = exp2f(x.y);
+        sum2 = add_f32x2(sum2, make_float2(sacc[nt][2 * h], sacc[nt][2 * h + 1]));
       }
-      l_run[h] = l_run[h] * alpha + sum;
+      l_run[h] = l_run[h] * alpha + (sum2.x + sum2.y);
       m_run[h] = m_new;
+      const float2 al2 = make_float2(alpha, alpha);
 #pragma unroll
       for (int dt = 0; dt < kDT; ++dt) {
-        o[dt][2 * h] *= alpha;
-        o[dt][2 * h + 1] *= alpha;
+        const float2 r = mul_f32x2(make_float2(o[dt][2 * h], o[dt][2 * h + 1]), al2);
+        o[dt][2 * h] = r.x;
+        o[dt][2 * h + 1] = r.y;
       }
     }
     // O += P V
