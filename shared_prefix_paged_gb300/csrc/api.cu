@@ -1282,8 +1282,10 @@ int cascade_attn_levels(const void* q, const void* k_cache, const void* v_cache,
   const int group = Hq / Hkv;
   const float scale_log2 = softmax_scale * 1.4426950408889634f;
   const LaunchPlan& P = L.suf;
-  const bool merge_after = P.tc;
-  const bool cluster = !P.tc && P.s_splits >= 2 && P.s_splits <= 8;  // as in attention_call
+  // as in the two-kernel schedule: the suffix writes its partials beside the segment
+  // grid (neither waits for the other) and the slot merge follows
+  const bool merge_after = true;
+  const bool cluster = false;
   cudaError_t e;
   // a row no segment of a level holds reads lse = -inf (weight 0) in that level's slots
   if ((e = csp::launch_fill_f32(part_lse, L.n_prefix * rows, -INFINITY, stream)) != cudaSuccess)
@@ -1371,6 +1373,7 @@ int cascade_attn_levels(const void* q, const void* k_cache, const void* v_cache,
   ga.n_prefix = L.n_prefix;
   ga.counters = (merge_after || cluster) ? nullptr : counters;
   ga.cluster_splits = cluster;
+  ga.partials_only = merge_after;
   ga.out = static_cast<__nv_bfloat16*>(out);
   ga.lse = lse;
   ga.status = status;
