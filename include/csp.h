@@ -161,13 +161,14 @@ CSP_API int csp_validate_batch(const int32_t* block_table, int64_t bt_row_stride
  * csp_workspace_size — bytes of device workspace that cascade_attn (with this
  * common_prefix_len) or paged_attn (common_prefix_len = 0) needs for this batch
  * shape on the current device.  All arguments are host integers, the same as the
- * attention call will get.  The workspace holds a status word, the counters and the
- * call counter of the single-kernel schedule, one word per (query token, KV head) and
+ * attention call will get.  The workspace holds a status word, the grid barrier's
+ * arrival count of the single-kernel schedule, one word per (query token, KV head) and
  * the split partial results; it must be 256-byte aligned and zero-filled before its
  * first use, and is not to be modified between calls except for zeroing it all again
- * (each call leaves its counters at zero or clears them itself, so one workspace may
- * serve batches of different shapes).  After a call reported CSP_ERR_TIMEOUT, zero
- * the workspace again before reusing it.
+ * (each call leaves its merge counters at zero and the arrival count at a multiple of
+ * the device's SM count, so one workspace may serve batches of different shapes on
+ * one device).  After a call reported CSP_ERR_TIMEOUT, zero the workspace again
+ * before reusing it.
  * Returns CSP_OK and writes *bytes_out, or CSP_ERR_INVALID_ARG / CSP_ERR_CUDA.
  */
 CSP_API int csp_workspace_size(int32_t num_reqs, int32_t total_q, int32_t max_seqlen_q,

@@ -23,14 +23,14 @@ int cuda_fail(cudaError_t e) {
 }
 
 constexpr int kPage = 16;
-// Workspace header: [0] status word; the grid barrier of the single-kernel decode
-// schedule: [64] its count (that kernel leaves it at zero) and [128] its generation.
+// Workspace header: [0] status word; [64] the 64-bit arrival count of the single-kernel
+// decode schedule's grid barrier (each call adds its grid, the SM count, so the count
+// stays a multiple of it between calls).
 constexpr size_t kHeaderBytes = 256;
 // Batches with a tcgen05 suffix (more than 16 rows per request and KV head) take the
 // fused schedule unless the caller asks for another.
 constexpr bool kFusedByDefault = false;
 constexpr size_t kOffBarCount = 64;
-constexpr size_t kOffBarGen = 128;
 // Shared memory the decode schedule's merge stages its bf16 rows in.
 constexpr size_t kMergeSmemBytes = 192 * 1024;
 // LSE box of a merge chunk: the chunk's rows, rounded out to 16-byte boundaries.
@@ -770,8 +770,7 @@ int attention_call(const void* q, const void* k_cache, const void* v_cache, int3
     // warps take alternate units
     da.unit_groups = max_seqlen_k - cpl <= 2 * 64 ? 2 : 1;
     da.key_tiles = cdiv(cpl, 64);
-    da.bar_count = reinterpret_cast<int*>(ws + kOffBarCount);
-    da.bar_gen = reinterpret_cast<unsigned*>(ws + kOffBarGen);
+    da.bar_count = reinterpret_cast<unsigned long long*>(ws + kOffBarCount);
     da.out = static_cast<__nv_bfloat16*>(out);
     da.lse = lse;
     da.cpl_dev = cpl_dev;

@@ -58,11 +58,14 @@ struct SLayout {
   static constexpr int kData = kSlots * kItem > kPrefixData ? kSlots * kItem : kPrefixData;
   static constexpr int kPrefixBars = kData;                        // prefix::kBarBytes
   static constexpr int kSuffixBars = kPrefixBars + prefix::kBarBytes;
-  static constexpr int kSuffixBarBytes = 1024;
+  static constexpr int kSuffixBarBytes = 2048;  // barriers, descriptors; then the exchange
+  static constexpr int kXchOff = 1024;           // consumers' row maxima and sums (1 KB)
   static constexpr int kDynamic = kSuffixBars + kSuffixBarBytes + 1024;  // + align slack
   static_assert(kSlots >= 3, "two items in flight ahead of the computed one");
   static_assert(kStage % 1024 == 0 && (2 * kKV) % 1024 == 0, "swizzled stage alignment");
-  static_assert(2 * kSlots * 8 + kSlots * 32 + 16 <= kSuffixBarBytes, "suffix barrier area");
+  static_assert(2 * kSlots * 8 + kSlots * 32 + 16 <= kMergeBarOff, "suffix barrier area");
+  static_assert(kMergeBarOff + 8 <= kXchOff && kXchOff + 2 * 8 * 16 * 4 <= kSuffixBarBytes,
+                "exchange area: [groups][2][warps per group][16] floats");
   static_assert(kDynamic <= 227 * 1024, "one CTA per SM");
 };
 
@@ -82,14 +85,18 @@ __device__ __forceinline__ uint32_t kv_off(int key, int c) {
   return static_cast<uint32_t>(r * 128 + (((c & 7) ^ (r & 7)) << 4));
 }
 
-__device__ __forceinline__ unsigned ld_acquire_gpu_u32(const unsigned* p) {
-  unsigned v;
-  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+__device__ __forceinline__ unsigned long long ld_acquire_gpu_u64(const unsigned long long* p) {
+  unsigned long long v;
+  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
   return v;
 }
 
-__device__ __forceinline__ void st_release_gpu_u32(unsigned* p, unsigned v) {
-  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+__device__ __forceinline__ unsigned long long atom_add_acq_rel_gpu_u64(unsigned long long* p,
+                                                                        unsigned long long v) {
+  unsigned long long old;
+  asm volatile("atom.add.acq_rel.gpu.global.u64 %0, [%1], %2;" : "=l"(old) : "l"(p), "l"(v)
+               : "memory");
+  return old;
 }
 
 // the streaming warps of one unit group: named barrier 1 + group, kWPU warps
@@ -107,16 +114,19 @@ __device__ __forceinline__ void group_sync(int group) {
 //    request's query range, length and block ids (lane j the id of the item's page j,
 //    one item ahead), and fills a free slot: lane j < 16 issues one TMA box of the
 //    item's K or V (one page of one KV head, both feature halves), and the lanes copy
-//    the Q rows with 16-byte cp.async (rows past the unit's are zero-filled without a
-//    read).  A page past the request re-reads the item's first page (its keys are
-//    masked); the item's descriptor tells the consumers which unit and tiles it holds.
-//  * warps 0-7 consume them: warps 0-3 compute the item's first tile and warps 4-7 its
-//    second, warp w taking keys [16 (w % 4), 16 (w % 4) + 16): S = Q K^T and O += P V
-//    on mma.sync m16n8k16 (bf16 in, fp32 accumulate) fed by ldmatrix, masked by the
+//    the unit's Q rows with 16-byte cp.async.  A page past the request re-reads the
+//    item's first page (its keys are masked); the item's descriptor tells the consumers
+//    which unit and tiles it holds.
+//  * warps 0-7 consume them, in groups (see consume_items): S = Q K^T and O += P V on
+//    mma.sync m16n8k16 (bf16 in, fp32 accumulate) fed by ldmatrix, masked by the
 //    request's causal limit (bottom-right alignment, §四), online softmax in base 2.
-//    V rows past the request are zeroed first (a TMA page holds whatever the cache
-//    has there).  At the unit's end the eight warps merge through the item's memory
-//    and write the normalised bf16 rows and their log2-sum-exp into the suffix slot.
+//    Each warp of a group scores its own block of the item's keys, and accumulates
+//    O for its own slice of the features over all of them: the group exchanges its
+//    rows' maxima and P through shared memory, so the item goes back to the producer
+//    as soon as P V is done and no O is merged across warps.  V rows past the request
+//    are zeroed first (a TMA page holds whatever the cache has there).  At the unit's
+//    end the group sums its rows' l and every warp writes its normalised slice of
+//    the bf16 rows (and warp 0 their log2-sum-exp) into the suffix slot.
 // Loads never hold up the computing warps: the producer alone waits for free slots.
 struct ItemDesc {
   int q0, q_len, seq_len, kvh, ntiles, t0, pad0, pad1;  // ntiles < 0: no more items
@@ -234,15 +244,16 @@ __device__ __forceinline__ void produce_items(const DecodeArgs& a, const CUtenso
         }
       }
       if (t0 == 0 && !end) {
+        // only the unit's rows: the consumers mask every score of the rows past them
+        // (by selection, so whatever those rows hold never reaches a result)
         const uint32_t qb = smem_u32(ring + slot * L::kItem + 2 * L::kKV);
         const int rows = q_len * p.group;
-        for (int x = lane; x < kRows * kChunks; x += 32) {
+        for (int x = lane; x < rows * kChunks; x += 32) {
           const int row = x / kChunks, c = x % kChunks;
-          const bool in = row < rows;
           const int qi = row / p.group, hj = row - qi * p.group;
           const int64_t off =
               (static_cast<int64_t>(q0 + qi) * p.num_q_heads + kvh * p.group + hj) * D + c * 8;
-          cp_async_16_u32(qb + sw128<kRows>(row, c), in ? a.q + off : a.q, in ? 16u : 0u);
+          cp_async_16_u32(qb + sw128<kRows>(row, c), a.q + off, 16u);
         }
       }
       cp_async_mbar_arrive(&st_full[slot]);
@@ -254,37 +265,56 @@ __device__ __forceinline__ void produce_items(const DecodeArgs& a, const CUtenso
   cp_async_wait<0>();
 }
 
-// kG groups of 8 / kG streaming warps: group g takes items g, g + kG, g + 2 kG, ...
-// (kG = 2 only when every unit is a single item, so a unit never spans two groups).
-// Within a group, warp w' takes keys [w' * 16 kG, (w' + 1) * 16 kG) of the item's 128
-// (kG blocks of 16 keys in one of its two tiles).
+// kG groups of kWPU = 8 / kG streaming warps: group g takes items g, g + kG, g + 2 kG,
+// ... (kG = 2 only when every unit is a single item, so a unit never spans two groups).
+// Warp w' of a group:
+//  * scores keys [16 kB w', 16 kB (w' + 1)) of the item's 128 (kB = kG blocks of 16
+//    keys, in tile 16 kB w' / 64), masks and scales them, and posts its rows' maxima;
+//  * after a group barrier, takes the group's maxima (so the running max, and every
+//    rescaling of O and l, is the same in all the group's warps), forms P = 2^(S - m)
+//    and stores it as bf16 over the K rows it alone read (16-key block b of the item
+//    lands on the first 512 bytes of that block's K page, [16 rows][2 x 16 B] with the
+//    chunk index XOR bit 2 of the row: conflict-free stores and ldmatrix);
+//  * after a second group barrier, accumulates O for features [w' D / kWPU,
+//    (w' + 1) D / kWPU) over all the item's keys, P fed by ldmatrix from those blocks
+//    and V by ldmatrix.trans, and gives the item back;
+//  * at the unit's end, sums its rows' l with the group's (a third barrier) and
+//    writes its normalised features of the unit's rows.
 template <int D, int kG>
 __device__ __forceinline__ void consume_items(const DecodeArgs& a, uint8_t* ring,
                                               uint64_t* st_full, uint64_t* st_empty,
-                                              const ItemDesc* idesc, volatile int* abort_flag) {
+                                              const ItemDesc* idesc, float* xch,
+                                              volatile int* abort_flag) {
   using L = SLayout<D>;
   constexpr int kS = L::kSlots;
-  constexpr int kChunks = D / 8;          // 16-byte chunks per row
-  constexpr int kDT = D / 8;              // O n-tiles (8 features each)
-  constexpr int kORow = D + 4;            // merge scratch row (floats)
-  constexpr int kWPU = kStreamWarps / kG; // warps per unit
-  constexpr int kB = kG;                  // 16-key blocks per warp
-  static_assert(kWPU * kRows * kORow * 4 + 2 * kWPU * kRows * 4 <= L::kItem,
-                "merge scratch fits one item");
+  constexpr int kChunks = D / 8;           // 16-byte chunks per row
+  constexpr int kWPU = kStreamWarps / kG;  // warps per unit
+  constexpr int kB = kG;                   // 16-key blocks per warp
+  constexpr int kNT = D / kWPU / 8;        // n-tiles (8 features each) of a warp's O slice
+  constexpr int kPageBytes = kPage * D * 2;
+  static_assert(kNT >= 1 && kNT <= 4 && (kNT == 1 || kNT % 2 == 0), "O slice of 8, 16 or 32");
+  static_assert(kPageBytes >= kB * 512, "a P block fits its K page");
   const PrefixArgs& p = a.pre;
   const int tid = threadIdx.x;  // 0 .. 255
   const int lane = tid & 31;
   const int wi = tid >> 5;      // 0 .. 7
   const int grp = wi / kWPU;    // this warp's group
   const int wg = wi % kWPU;     // its index within the group
-  const int half = (wg * 16 * kB) >> 6;      // which tile of the item this warp computes
+  const int half = (wg * 16 * kB) >> 6;      // which tile of the item this warp scores
   const int kw0 = (wg * 16 * kB) & 63;       // its first key within that tile
+  const int g = lane >> 2;                   // rows g and g + 8 of the fragments
   const uint32_t rbase = smem_u32(ring);
+  float* xm = xch + grp * (2 * kWPU * kRows);  // [kWPU][16] row maxima
+  float* xl = xm + kWPU * kRows;               // [kWPU][16] row sums
+  // P block `ks` (16 keys) of an item: the first 512 bytes of its K page
+  auto p_block = [&](uint32_t ib, int ks) -> uint32_t {
+    return ib + (ks >> 2) * L::kStage + (ks & 3) * kPageBytes;
+  };
 
   int c_nt = 0, c_seq = 0, c_qlen = 0, c_q0 = 0, c_kvh = 0, rows_valid = 0;
   int pos[2] = {-1, -1};
-  float o[kDT][4];
-  float m_run[2], l_run[2];
+  float o[kNT][4];
+  float m_run[2], l_run[2];  // the group's running max; this lane's share of the sum
   uint32_t qa[D / 16][4];
   for (int item = grp;; item += kG) {
     const int slot = item % kS;
@@ -305,13 +335,13 @@ __device__ __forceinline__ void consume_items(const DecodeArgs& a, uint8_t* ring
       rows_valid = c_qlen * p.group;
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
-        const int rho = (lane >> 2) + 8 * h;
+        const int rho = g + 8 * h;
         pos[h] = rho < rows_valid ? c_seq - c_qlen + rho / p.group : -1;
         m_run[h] = -INFINITY;
         l_run[h] = 0.f;
       }
 #pragma unroll
-      for (int i = 0; i < kDT; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+      for (int i = 0; i < kNT; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
       const uint32_t qb = ib + 2 * L::kKV;
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
@@ -320,13 +350,20 @@ __device__ __forceinline__ void consume_items(const DecodeArgs& a, uint8_t* ring
         ldmatrix_x4(qb + sw128<kRows>(row, c), qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3]);
       }
     }
-    if (t0 + half < c_nt) {
+    const int tiles = min(2, c_nt - t0);  // tiles this item holds
+    const bool mine = half < tiles;       // this warp has keys in it
+    // ---- S = Q K^T over this warp's keys (two n-tiles of 8 per 16-key block), masked
+    // (keys past the request, and the causal limit) and scaled to base 2
+    float sacc[2 * kB][4];
+    float mx[2] = {-INFINITY, -INFINITY};
+    if (mine) {
       const uint32_t kb = ib + half * L::kStage;
       const uint32_t vb = kb + L::kKV;
       const int key0 = p.cpl + (t0 + half) * kKeys + kw0;
       if (key0 + 16 * kB > c_seq) {
         // this warp's keys past the request: zero their V rows (P is 0 there, but the
-        // page may hold anything)
+        // page may hold anything); every warp of the group reads them after the
+        // barriers below
         for (int x = lane; x < 16 * kB * kChunks; x += 32) {
           const int k = x / kChunks, c = x % kChunks;
           if (key0 + k >= c_seq)
@@ -334,10 +371,7 @@ __device__ __forceinline__ void consume_items(const DecodeArgs& a, uint8_t* ring
                              vb + kv_off<D>(kw0 + k, c)), "r"(0u)
                          : "memory");
         }
-        __syncwarp();
       }
-      // S = Q K^T over this warp's keys (two n-tiles of 8 per 16-key block)
-      float sacc[2 * kB][4];
 #pragma unroll
       for (int i = 0; i < 2 * kB; ++i) sacc[i][0] = sacc[i][1] = sacc[i][2] = sacc[i][3] = 0.f;
 #pragma unroll
@@ -352,11 +386,9 @@ __device__ __forceinline__ void consume_items(const DecodeArgs& a, uint8_t* ring
           mma_bf16_16816(sacc[2 * b + 1], qa[kk], b2, b3);
         }
       }
-      // mask (keys past the request, and the causal limit), online softmax in base 2
+      const float2 sc2 = make_float2(p.scale_log2, p.scale_log2);
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
-        float mx = -INFINITY;
-        const float2 sc2 = make_float2(p.scale_log2, p.scale_log2);
 #pragma unroll
         for (int nt = 0; nt < 2 * kB; ++nt) {
           // the two scores of a pair scaled in one paired instruction, then masked
@@ -366,130 +398,137 @@ __device__ __forceinline__ void consume_items(const DecodeArgs& a, uint8_t* ring
             const int kabs = key0 + nt * 8 + (lane & 3) * 2 + e;
             float& sref = sacc[nt][2 * h + e];
             sref = (kabs < c_seq && kabs <= pos[h]) ? (e ? s2.y : s2.x) : -INFINITY;
-            mx = fmaxf(mx, sref);
+            mx[h] = fmaxf(mx[h], sref);
           }
         }
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-        // keep the running max unless it grows by more than 2^8 (always on the row's
-        // first unmasked keys, where it is -inf): then p = 2^(s - m) <= 256 and O and
-        // l need rescaling only now and then
-        if (mx > m_run[h] + 8.f) {
-          const float alpha = fast_exp2(m_run[h] - mx);
-          l_run[h] *= alpha;
+        mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 1));
+        mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 2));
+      }
+    }
+    if ((lane & 3) == 0) {
+      xm[wg * kRows + g] = mx[0];
+      xm[wg * kRows + g + 8] = mx[1];
+    }
+    group_sync<kWPU>(grp);
+    // ---- the group's maxima; keep the running max unless it grows by more than 2^8
+    // (always on the row's first unmasked keys, where it is -inf): then p = 2^(s - m)
+    // <= 256 and O and l need rescaling only now and then
 #pragma unroll
-          for (int dt = 0; dt < kDT; ++dt) {
-            o[dt][2 * h] *= alpha;
-            o[dt][2 * h + 1] *= alpha;
-          }
-          m_run[h] = mx;
+    for (int h = 0; h < 2; ++h) {
+      float mg = -INFINITY;
+#pragma unroll
+      for (int w = 0; w < kWPU; ++w) mg = fmaxf(mg, xm[w * kRows + g + 8 * h]);
+      if (mg > m_run[h] + 8.f) {
+        const float alpha = fast_exp2(m_run[h] - mg);
+        l_run[h] *= alpha;
+#pragma unroll
+        for (int nt = 0; nt < kNT; ++nt) {
+          o[nt][2 * h] *= alpha;
+          o[nt][2 * h + 1] *= alpha;
         }
+        m_run[h] = mg;
+      }
+    }
+    if (mine) {
+      // ---- P = 2^(S - m) as bf16 over this warp's K rows (read by it alone)
+      float2 sum2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
         const float m_use = (m_run[h] == -INFINITY) ? 0.f : m_run[h];
-        float2 sum2 = make_float2(0.f, 0.f);
         const float2 nm2 = make_float2(-m_use, -m_use);
 #pragma unroll
         for (int nt = 0; nt < 2 * kB; ++nt) {
           const float2 x = add_f32x2(make_float2(sacc[nt][2 * h], sacc[nt][2 * h + 1]), nm2);
           sacc[nt][2 * h] = fast_exp2(x.x);
           sacc[nt][2 * h + 1] = fast_exp2(x.y);
-          sum2 = add_f32x2(sum2, make_float2(sacc[nt][2 * h], sacc[nt][2 * h + 1]));
+          sum2[h] = add_f32x2(sum2[h], make_float2(sacc[nt][2 * h], sacc[nt][2 * h + 1]));
         }
-        l_run[h] += sum2.x + sum2.y;
+        l_run[h] += sum2[h].x + sum2[h].y;
       }
-      // O += P V over the same keys
 #pragma unroll
       for (int b = 0; b < kB; ++b) {
-        uint32_t pa[4];
-        pa[0] = pack_bf16x2(sacc[2 * b][0], sacc[2 * b][1]);
-        pa[1] = pack_bf16x2(sacc[2 * b][2], sacc[2 * b][3]);
-        pa[2] = pack_bf16x2(sacc[2 * b + 1][0], sacc[2 * b + 1][1]);
-        pa[3] = pack_bf16x2(sacc[2 * b + 1][2], sacc[2 * b + 1][3]);
+        const uint32_t pb = p_block(ib, wg * kB + b);
 #pragma unroll
-        for (int dp = 0; dp < kDT / 2; ++dp) {
-          const int key = kw0 + 16 * b + (lane & 7) + ((lane >> 3) & 1) * 8;
-          const int c = dp * 2 + (lane >> 4);
-          uint32_t b0, b1, b2, b3;
-          ldmatrix_x4_trans(vb + kv_off<D>(key, c), b0, b1, b2, b3);
-          mma_bf16_16816(o[2 * dp], pa, b0, b1);
-          mma_bf16_16816(o[2 * dp + 1], pa, b2, b3);
+        for (int j = 0; j < 2; ++j) {
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int row = g + 8 * h;
+            const uint32_t addr =
+                pb + row * 32 + ((j ^ ((row >> 2) & 1)) << 4) + (lane & 3) * 4;
+            asm volatile("st.shared.u32 [%0], %1;" ::"r"(addr),
+                         "r"(pack_bf16x2(sacc[2 * b + j][2 * h], sacc[2 * b + j][2 * h + 1]))
+                         : "memory");
+          }
         }
       }
     }
+    group_sync<kWPU>(grp);
+    // ---- O (this warp's features) += P V over the item's keys
+    {
+      const int prow = (lane & 7) + ((lane >> 3) & 1) * 8;
+      const uint32_t p_off = prow * 32 + (((lane >> 4) ^ ((prow >> 2) & 1)) << 4);
+      const int vkey = (lane & 7) + ((lane >> 3) & 1) * 8;
+      for (int ks = 0; ks < 4 * tiles; ++ks) {
+        uint32_t pa[4];
+        ldmatrix_x4(p_block(ib, ks) + p_off, pa[0], pa[1], pa[2], pa[3]);
+        const uint32_t vb = ib + (ks >> 2) * L::kStage + L::kKV;
+        const int key = (ks & 3) * 16 + vkey;
+        if constexpr (kNT == 1) {
+          uint32_t b0, b1;
+          asm volatile("ldmatrix.sync.aligned.m8n8.x2.trans.shared.b16 {%0,%1}, [%2];"
+                       : "=r"(b0), "=r"(b1)
+                       : "r"(vb + kv_off<D>(key, wg)));
+          mma_bf16_16816(o[0], pa, b0, b1);
+        } else {
+#pragma unroll
+          for (int dp = 0; dp < kNT / 2; ++dp) {
+            const int c = wg * kNT + dp * 2 + (lane >> 4);
+            uint32_t b0, b1, b2, b3;
+            ldmatrix_x4_trans(vb + kv_off<D>(key, c), b0, b1, b2, b3);
+            mma_bf16_16816(o[2 * dp], pa, b0, b1);
+            mma_bf16_16816(o[2 * dp + 1], pa, b2, b3);
+          }
+        }
+      }
+    }
+    // the item goes back to the producer (its TMA will overwrite what this warp wrote
+    // there through the generic proxy: P, zeroed V rows)
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&st_empty[slot]);
     if (t0 + 2 >= c_nt) {
-      // ---- the unit's last item: the group's warps' (max, sum, O) -> one normalised
-      // partial per row, through this item's memory (only this group reads the item)
+      // ---- the unit's end: the group's row sums, then this warp's normalised features
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         l_run[h] += __shfl_xor_sync(0xffffffffu, l_run[h], 1);
         l_run[h] += __shfl_xor_sync(0xffffffffu, l_run[h], 2);
       }
-      group_sync<kWPU>(grp);  // every warp of the group is done reading this item's K/V
-      float* s_o = reinterpret_cast<float*>(ring + slot * L::kItem);  // [kWPU][16][kORow]
-      float* s_m = s_o + kWPU * kRows * kORow;                        // [kWPU][16]
-      float* s_l = s_m + kWPU * kRows;                                // [kWPU][16]
-      // every warp's raw (max, sum, O) of its keys; the weights come in the final pass
       if ((lane & 3) == 0) {
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          s_m[wg * kRows + (lane >> 2) + 8 * h] = m_run[h];
-          s_l[wg * kRows + (lane >> 2) + 8 * h] = l_run[h];
-        }
-      }
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int rr = (lane >> 2) + 8 * h;
-        if (rr >= rows_valid) continue;
-        float* dst = s_o + (wg * kRows + rr) * kORow;
-#pragma unroll
-        for (int dt = 0; dt < kDT; ++dt) {
-          const int dd = dt * 8 + (lane & 3) * 2;
-          *reinterpret_cast<float2*>(dst + dd) = make_float2(o[dt][2 * h], o[dt][2 * h + 1]);
-        }
+        xl[wg * kRows + g] = l_run[0];
+        xl[wg * kRows + g + 8] = l_run[1];
       }
       group_sync<kWPU>(grp);
       const int64_t slot_rows = static_cast<int64_t>(p.n_splits) * p.total_q * p.num_q_heads;
-      // warp w' finalises rows w', w' + kWPU, ...; lane c owns features [4c, 4c + 4)
-      for (int rr = wg; rr < rows_valid; rr += kWPU) {
-        float mw[kWPU];
-        float mg = -INFINITY;
 #pragma unroll
-        for (int w = 0; w < kWPU; ++w) {
-          mw[w] = s_m[w * kRows + rr];
-          mg = fmaxf(mg, mw[w]);
-        }
+      for (int h = 0; h < 2; ++h) {
+        const int rr = g + 8 * h;
+        if (rr >= rows_valid) continue;
         float lsum = 0.f;
 #pragma unroll
-        for (int w = 0; w < kWPU; ++w) {
-          mw[w] = (mw[w] == -INFINITY) ? 0.f : fast_exp2(mw[w] - mg);  // warp w's weight
-          lsum += s_l[w * kRows + rr] * mw[w];
-        }
+        for (int w = 0; w < kWPU; ++w) lsum += xl[w * kRows + rr];
         const float inv = !(lsum <= 0.f) ? 1.f / lsum : 0.f;  // a NaN sum propagates
         const int qi = rr / p.group, j = rr - qi * p.group;
         const int64_t row = static_cast<int64_t>(c_q0 + qi) * p.num_q_heads + c_kvh * p.group + j;
-        const int64_t prow = slot_rows + row;
-        if (lane < D / 4) {
-          float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        __nv_bfloat16* dst = p.part_o + (slot_rows + row) * D + wg * kNT * 8 + (lane & 3) * 2;
 #pragma unroll
-          for (int w = 0; w < kWPU; ++w) {
-            const float4 v =
-                *reinterpret_cast<const float4*>(s_o + (w * kRows + rr) * kORow + lane * 4);
-            acc.x = fmaf(mw[w], v.x, acc.x);
-            acc.y = fmaf(mw[w], v.y, acc.y);
-            acc.z = fmaf(mw[w], v.z, acc.z);
-            acc.w = fmaf(mw[w], v.w, acc.w);
-          }
-          store_bf16x4(p.part_o + prow * D + lane * 4,
-                       make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv));
-        }
-        if (lane == 0)
-          p.part_lse[p.n_splits * p.lse_stride + row] = !(lsum <= 0.f) ? mg + log2f(lsum) : -INFINITY;
+        for (int nt = 0; nt < kNT; ++nt)
+          *reinterpret_cast<uint32_t*>(dst + nt * 8) =
+              pack_bf16x2(o[nt][2 * h] * inv, o[nt][2 * h + 1] * inv);
+        if (wg == 0 && (lane & 3) == 0)
+          p.part_lse[p.n_splits * p.lse_stride + row] =
+              !(lsum <= 0.f) ? m_run[h] + log2f(lsum) : -INFINITY;
       }
     }
-    // the item goes back to the producer (its TMA will overwrite what this warp
-    // wrote through the generic proxy)
-    fence_proxy_async_smem();
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&st_empty[slot]);
   }
 }
 
@@ -610,14 +649,6 @@ __device__ __forceinline__ void decode_body(const CUtensorMap& tm_q, const CUten
   const PrefixArgs& p = a.pre;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  // generation of the grid barrier at the end, read now with a relaxed load: nothing
-  // waits on it until the barrier (an acquire here would hold thread 0, and through the
-  // first CTA barrier every warp, for a round trip to memory).  The previous call
-  // advanced it before that kernel ended, and this CTA's arrival below (a release)
-  // orders the read before any CTA of this call can advance it.
-  unsigned g0 = 0u;
-  if (threadIdx.x == 0)
-    asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(g0) : "l"(a.bar_gen) : "memory");
   // the first TMA through each map would otherwise wait for its descriptor
   if (threadIdx.x == 32 * kWarpScheduler) {
     prefetch_tensormap(&tm_k);
@@ -652,6 +683,7 @@ __device__ __forceinline__ void decode_body(const CUtensorMap& tm_q, const CUten
   ItemDesc* idesc = reinterpret_cast<ItemDesc*>(st_empty + kS);              // [kS]
   volatile int* abort_flag = reinterpret_cast<volatile int*>(idesc + kS);
   uint64_t* merge_bar = reinterpret_cast<uint64_t*>(smem + L::kSuffixBars + kMergeBarOff);
+  float* xch = reinterpret_cast<float*>(smem + L::kSuffixBars + L::kXchOff);
   int u_begin, u_end;
   unit_range(a, u_begin, u_end);
   if (threadIdx.x == 0) {
@@ -669,30 +701,31 @@ __device__ __forceinline__ void decode_body(const CUtensorMap& tm_q, const CUten
       produce_items<D>(a, &tm_k, &tm_v, smem, st_full, st_empty, idesc, abort_flag);
     } else if (warp < kStreamWarps) {
       if (a.unit_groups == 2)
-        consume_items<D, 2>(a, smem, st_full, st_empty, idesc, abort_flag);
+        consume_items<D, 2>(a, smem, st_full, st_empty, idesc, xch, abort_flag);
       else
-        consume_items<D, 1>(a, smem, st_full, st_empty, idesc, abort_flag);
+        consume_items<D, 1>(a, smem, st_full, st_empty, idesc, xch, abort_flag);
     }
   }
   // the bulk copies of the merge below overwrite what was written here through the
   // generic proxy
   fence_proxy_async_smem();
 
-  // ---- grid-wide barrier: every partial of the call is written.  The arrival is one
-  // acquire-release add (the CTA barrier before it makes every thread's partial
-  // stores part of what it releases); the last CTA zeroes the count and advances the
-  // generation, which the others read at their start (no CTA can advance it before
-  // every CTA has arrived).
+  // ---- grid-wide barrier: every partial of the call is written.  Arrivals go to one
+  // 64-bit count that is never reset: every call adds its grid size G (the SM count,
+  // the same on every call), so call n moves it from n G to (n + 1) G and a CTA whose
+  // arrival returned c waits for the next multiple of G above c.  The arrival is an
+  // acquire-release add (the CTA barrier before it makes every thread's partial stores
+  // part of what it releases); the last CTA's add itself completes the count, so no
+  // store follows it on the critical path.
   __syncthreads();
   if (threadIdx.x == 0) {
-    const int old = atomic_add_acq_rel_gpu(a.bar_count, 1);
-    if (old == static_cast<int>(gridDim.x) - 1) {
-      *a.bar_count = 0;
-      st_release_gpu_u32(a.bar_gen, g0 + 1u);
-    } else {
+    const unsigned long long g = gridDim.x;
+    const unsigned long long old = atom_add_acq_rel_gpu_u64(a.bar_count, 1ull);
+    const unsigned long long target = old - old % g + g;
+    if (old + 1ull != target) {
       const long long c0 = clock64();
       unsigned spins = 0;
-      while (ld_acquire_gpu_u32(a.bar_gen) == g0) {
+      while (ld_acquire_gpu_u64(a.bar_count) < target) {
         if ((++spins & 255u) == 0 && clock64() - c0 > kWaitLimitCycles) {
           if (p.status) atomicCAS(p.status, 0, kErrTimeout);
           break;

@@ -136,8 +136,8 @@ struct DecodeArgs {
   int unit_groups;           // 2: every suffix unit is one item (<= 128 keys) and two groups
                              // of four warps take alternate units; 1: all eight warps
   int key_tiles;             // ceil(cpl / 64)
-  int* bar_count;            // zero at launch; the kernel leaves it zero
-  unsigned* bar_gen;         // any value; advanced by one per call
+  unsigned long long* bar_count;  // grid-barrier arrivals: a multiple of the grid at launch
+                                  // (zero at first); each call adds the grid size
   __nv_bfloat16* out;
   float* lse;                // natural-log LSE or nullptr
   const int32_t* cpl_dev;    // null, or the prefix length in device memory (the launch
