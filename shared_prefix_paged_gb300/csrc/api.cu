@@ -267,17 +267,20 @@ void make_plan(int num_reqs, int total_q, int max_q, int max_k, int cpl, int Hq,
   // Decode-like batches (a request's rows of one KV head fit one 16-row MMA tile):
   // one cooperative kernel.  d_base * s CTAs each run a prefix range and then stream
   // k suffix units; the other CTAs stream the rest of the suffix units from the
-  // start.  s and k come from a cost model measured on GB300 (per CTA, in us): the
-  // prefix's first tile lands at ~3.5; a prefix 64-key tile takes its bytes' time at
-  // ~31 GB/s (the per-SM copy rate) or ~1.22 per 256 rows (tensor core and softmax),
-  // whichever is longer; writing a range's partial takes ~3.4; the suffix's first
-  // item lands at ~5 and a suffix unit then takes its bytes' time at ~28.5 GB/s (the
-  // copies and the computing warps pace it together).  Both kinds of CTA should finish
-  // together.  The merge after them costs ~0.1 per slot its loop is unrolled to (8 up
-  // to 7 prefix ranges, 16 beyond); on a tie the fewer prefix ranges win.  The single
-  // kernel is taken only if the same model does not expect the two-kernel schedule to
-  // be faster (a long prefix over many 256-row blocks leaves it too few SMs for one
-  // of the phases).
+  // start.  s and k come from a cost model fitted to a sweep on one GB300 of N in
+  // {16..256} x P in {1024..16384} (S = 128, Hq 32, Hkv 8, D 128) over 2-12 ranges
+  // (99 points; rms error 2%, worst 6%), per CTA in us: a prefix range costs ~8.3 of
+  // fixed work (its first tiles landing, writing its partial) plus its 64-key tiles,
+  // each at its bytes' time at ~45 GB/s or ~0.87 per 256 rows (tensor core and
+  // softmax), whichever is longer; a suffix unit takes its bytes' time at ~40 GB/s
+  // (the copies and the computing warps pace it together), the first landing at ~5.9
+  // (~1.8 after a range on a prefix CTA).  Both kinds of CTA should finish together.
+  // The grid barrier and the merge after them cost ~0.9 plus ~0.08 per KB of slots a
+  // CTA merges; on a tie the fewer prefix ranges win.  On that grid the pick was
+  // within 2% of the best measured range count at every point.  The single kernel is
+  // taken only if it is not expected to be slower than the two-kernel schedule (a
+  // long prefix over many 256-row blocks leaves it too few SMs for one of the
+  // phases).
   // The two-kernel schedule for decode-shaped rows: the prefix kernel on some SMs, the
   // warp-MMA suffix kernel writing its partials on the rest (neither waits for the
   // other), then the slot merge kernel.  Its number of prefix key ranges and its time
@@ -318,9 +321,9 @@ void make_plan(int num_reqs, int total_q, int max_q, int max_k, int cpl, int Hq,
   const int d_base = p.p_pairs * Hkv;
   if (cpl > 0 && static_cast<int64_t>(max_q) * p.group <= kDecodeRows && d_base <= sms) {
     const int pre_tiles = cdiv(cpl, 64);
-    const double kRate = 31e3, kUnitRate = 28.5e3;  // bytes per us per SM
+    const double kRate = 44.8e3, kUnitRate = 39.9e3;  // bytes per us per SM
     const double pair_rows = std::min(256.0, static_cast<double>(total_q) * p.group);
-    const double tile_us = std::max(64.0 * 4.0 * D / kRate, 1.22 * pair_rows / 256.0);
+    const double tile_us = std::max(64.0 * 4.0 * D / kRate, 0.87 * pair_rows / 256.0);
     const double unit_us =
         (std::max(1, cdiv(max_len, 64)) * 64.0 * 4.0 * D + max_q * p.group * D * 2.0) /
         kUnitRate;
@@ -330,17 +333,20 @@ void make_plan(int num_reqs, int total_q, int max_q, int max_k, int cpl, int Hq,
     auto best_k = [&](int c, double* t_out) {
       const int64_t pc = static_cast<int64_t>(d_base) * c;  // prefix CTAs
       const int64_t nc = sms - pc;                            // suffix-only CTAs
-      const double pre_us = 3.5 + cdiv(pre_tiles, c) * tile_us + 3.4;
+      const double pre_us = 8.3 + cdiv(pre_tiles, c) * tile_us;
+      // the grid barrier and the merge: KB of slots per CTA
+      const double merge_us =
+          0.9 + 0.082e-3 * static_cast<double>(total_q) * Hq * (c + 1) * D * 2.0 / sms;
       const int64_t k_lo = nc > 0 ? 0 : cdiv64(units, pc);
       double best_t = -1.0;
       int kb = 0;
       for (int64_t kk = k_lo; kk <= cdiv64(units, pc); ++kk) {
         const int64_t rest = std::max<int64_t>(0, units - pc * kk);
         const int64_t per = nc > 0 ? cdiv64(rest, nc) : 0;
-        // a prefix CTA's first suffix item lands ~3.5 after its range is written
+        // a prefix CTA's first suffix item lands ~1.8 after its range is written
         const double t =
-            std::max(pre_us + (kk > 0 ? 3.5 : 0.0) + kk * unit_us, 5.0 + per * unit_us) +
-            (c + 1 <= 8 ? 0.8 : 1.6);
+            std::max(pre_us + (kk > 0 ? 1.8 : 0.0) + kk * unit_us, 5.9 + per * unit_us) +
+            merge_us;
         if (best_t < 0.0 || t < best_t) {
           best_t = t;
           kb = static_cast<int>(kk);
@@ -362,13 +368,16 @@ void make_plan(int num_reqs, int total_q, int max_q, int max_k, int cpl, int Hq,
     }
     // the two-kernel schedule: its prefix kernel (p_splits ranges per block, in waves
     // over the SMs), while the SMs it leaves free start the suffix, which every SM
-    // then streams
+    // then streams (its own rates: a prefix tile at ~31 GB/s or ~1.22 us per 256
+    // rows, a suffix unit at ~28.5 GB/s per SM)
+    const double tile2_us = std::max(64.0 * 4.0 * D / 31e3, 1.22 * pair_rows / 256.0);
+    const double unit2_us = unit_us * kUnitRate / 28.5e3;
     const double pre2_us = cdiv64(static_cast<int64_t>(d_base) * p.p_splits, sms) *
-                           (3.5 + p.p_tiles_per_split * tile_us + 3.4);
+                           (3.5 + p.p_tiles_per_split * tile2_us + 3.4);
     const int64_t free_sms = std::max<int64_t>(0, sms - static_cast<int64_t>(d_base) * p.p_splits);
     const double two_us =
         pre2_us + 5.0 +
-        std::max(0.0, static_cast<double>(units) * unit_us - free_sms * pre2_us) / sms;
+        std::max(0.0, static_cast<double>(units) * unit2_us - free_sms * pre2_us) / sms;
     p.est_single_us = best;
     // the single kernel when the model expects it to beat both two-kernel variants
     // (the one with an in-place merge, and, within the split-merge model's fitting
