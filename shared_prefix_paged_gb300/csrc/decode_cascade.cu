@@ -738,9 +738,12 @@ __device__ __forceinline__ void decode_body(const CUtensorMap& tm_q, const CUten
   // ---- merge_attn_states: CTA b takes rows [b R / G, (b + 1) R / G) of the R rows,
   // which are contiguous in every slot: one bulk copy per slot brings a chunk of them
   // (and their LSEs) into shared memory, then half a warp merges each row
-  // (the slot loop is unrolled to a bound: 8 when it suffices)
+  // (the slot loop is unrolled to a bound: 8, 12 or 16 slots; every slot past the
+  // call's costs each row a load and its FMAs)
   if (p.n_splits + 1 <= 8)
     merge_rows_staged<D, 8>(a, &tm_po, &tm_pl, smem, merge_bar, abort_flag);
+  else if (p.n_splits + 1 <= 12)
+    merge_rows_staged<D, 12>(a, &tm_po, &tm_pl, smem, merge_bar, abort_flag);
   else
     merge_rows_staged<D, kDecodeMaxParts>(a, &tm_po, &tm_pl, smem, merge_bar, abort_flag);
 }
