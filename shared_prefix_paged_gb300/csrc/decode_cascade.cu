@@ -63,7 +63,7 @@ struct SLayout {
   static constexpr int kDynamic = kSuffixBars + kSuffixBarBytes + 1024;  // + align slack
   static_assert(kSlots >= 3, "two items in flight ahead of the computed one");
   static_assert(kStage % 1024 == 0 && (2 * kKV) % 1024 == 0, "swizzled stage alignment");
-  static_assert(2 * kSlots * 8 + kSlots * 32 + 16 <= kMergeBarOff, "suffix barrier area");
+  static_assert(4 * kSlots * 8 + kSlots * 32 + 16 <= kMergeBarOff, "suffix barrier area");
   static_assert(kMergeBarOff + 8 <= kXchOff && kXchOff + 2 * 8 * 16 * 4 <= kSuffixBarBytes,
                 "exchange area: [groups][2][warps per group][16] floats");
   static_assert(kDynamic <= 227 * 1024, "one CTA per SM");
@@ -103,6 +103,22 @@ __device__ __forceinline__ unsigned long long atom_add_acq_rel_gpu_u64(unsigned 
 template <int kWPU>
 __device__ __forceinline__ void group_sync(int group) {
   asm volatile("bar.sync %0, %1;" ::"r"(1 + group), "r"(kWPU * 32) : "memory");
+}
+
+// Items and their slot barriers.  Item i sits in ring slot i % kS and is computed by
+// group i % groups; each (group, slot) pair has its own full and empty barrier, so that
+// the items one barrier sees are exactly every L-th item (L = lcm(groups, kS)) and a
+// waiter never skips one of its phases (with shared barriers a group that skips the
+// other group's phase of a slot could take that phase's completion for its own).
+template <int kG, int kS>
+__device__ __forceinline__ int item_barrier(int i) {
+  const unsigned u = static_cast<unsigned>(i);
+  return static_cast<int>((u % kG) * kS + u % kS);
+}
+template <int kG, int kS>
+__device__ __forceinline__ uint32_t item_parity(int i) {
+  constexpr unsigned kPeriod = (kG == 2 && (kS & 1)) ? 2 * kS : kS;  // lcm(kG, kS)
+  return (static_cast<unsigned>(i) / kPeriod) & 1u;
 }
 
 // ------------------------------------------------------------------ streaming --
@@ -152,7 +168,7 @@ __device__ __forceinline__ void unit_range(const DecodeArgs& a, int& u_begin, in
   }
 }
 
-template <int D>
+template <int D, int kG>
 __device__ __forceinline__ void produce_items(const DecodeArgs& a, const CUtensorMap* tm_k,
                                               const CUtensorMap* tm_v, uint8_t* ring,
                                               uint64_t* st_full, uint64_t* st_empty,
@@ -206,10 +222,14 @@ __device__ __forceinline__ void produce_items(const DecodeArgs& a, const CUtenso
     const int npages = (seq_len + kPage - 1) / kPage;
     const int32_t* bt = a.block_table + static_cast<int64_t>(end ? 0 : u / hkv) * a.bt_stride;
     // the end: one marker per consumer group (each group reads every unit_groups-th item)
-    for (int t0 = 0; end ? t0 < 2 * a.unit_groups : t0 < nt; t0 += 2) {
+    for (int t0 = 0; end ? t0 < 2 * kG : t0 < nt; t0 += 2) {
       const int slot = item % kS;
+      const int fb = item_barrier<kG, kS>(item);
+      // the slot's previous item must have been given back
       if (item >= kS &&
-          !(ok = warp_mbar_wait(&st_empty[slot], ((item / kS) - 1) & 1, abort_flag, p.status)))
+          !(ok = warp_mbar_wait(&st_empty[item_barrier<kG, kS>(item - kS)],
+                                item_parity<kG, kS>(item - kS), abort_flag,
+                                p.status)))
         break;
       const int tiles = end ? 0 : min(2, nt - t0);
       if (lane == 0) {
@@ -220,7 +240,7 @@ __device__ __forceinline__ void produce_items(const DecodeArgs& a, const CUtenso
         d.kvh = kvh;
         d.ntiles = nt;
         d.t0 = t0;
-        mbar_arrive_expect_tx(&st_full[slot], static_cast<uint32_t>(tiles * 2 * L::kKV));
+        mbar_arrive_expect_tx(&st_full[fb], static_cast<uint32_t>(tiles * 2 * L::kKV));
       }
       __syncwarp();
       // block ids of the item's pages: lane j holds page page0 + 4 t0 + j; the next
@@ -240,7 +260,7 @@ __device__ __forceinline__ void produce_items(const DecodeArgs& a, const CUtenso
         const int blk = page < npages ? id_q : id_0;
         if (lane < tiles * kBoxesPerTile) {
           uint8_t* dst = ring + slot * L::kItem + h * L::kStage + kv * L::kKV + q * (kPage * D * 2);
-          tma_load_4d(dst, kv ? tm_v : tm_k, &st_full[slot], 0, blk * kPage, 0, kvh);
+          tma_load_4d(dst, kv ? tm_v : tm_k, &st_full[fb], 0, blk * kPage, 0, kvh);
         }
       }
       if (t0 == 0 && !end) {
@@ -256,7 +276,7 @@ __device__ __forceinline__ void produce_items(const DecodeArgs& a, const CUtenso
           cp_async_16_u32(qb + sw128<kRows>(row, c), a.q + off, 16u);
         }
       }
-      cp_async_mbar_arrive(&st_full[slot]);
+      cp_async_mbar_arrive(&st_full[fb]);
       ++item;
       ids = nxt;
     }
@@ -318,10 +338,11 @@ __device__ __forceinline__ void consume_items(const DecodeArgs& a, uint8_t* ring
   uint32_t qa[D / 16][4];
   for (int item = grp;; item += kG) {
     const int slot = item % kS;
-    const uint32_t par = (item / kS) & 1;
-    if (!warp_mbar_wait(&st_full[slot], par, abort_flag, p.status)) break;
+    const int fb = item_barrier<kG, kS>(item);
+    const uint32_t par = item_parity<kG, kS>(item);
+    if (!warp_mbar_wait(&st_full[fb], par, abort_flag, p.status)) break;
     // every lane observes the completed phase (the TMA bytes are visible to it)
-    mbar_test_wait(&st_full[slot], par);
+    mbar_test_wait(&st_full[fb], par);
     const ItemDesc d = idesc[slot];
     if (d.ntiles < 0) break;
     const uint32_t ib = rbase + slot * L::kItem;
@@ -495,7 +516,7 @@ __device__ __forceinline__ void consume_items(const DecodeArgs& a, uint8_t* ring
     // there through the generic proxy: P, zeroed V rows)
     fence_proxy_async_smem();
     __syncwarp();
-    if (lane == 0) mbar_arrive(&st_empty[slot]);
+    if (lane == 0) mbar_arrive(&st_empty[fb]);
     if (t0 + 2 >= c_nt) {
       // ---- the unit's end: the group's row sums, then this warp's normalised features
 #pragma unroll
@@ -678,16 +699,16 @@ __device__ __forceinline__ void decode_body(const CUtensorMap& tm_q, const CUten
 
   // ---- role 2: the suffix units, produced by warp 8 and computed by warps 0-7
   constexpr int kS = L::kSlots;
-  uint64_t* st_full = reinterpret_cast<uint64_t*>(smem + L::kSuffixBars);  // [kS]
-  uint64_t* st_empty = st_full + kS;                                        // [kS]
-  ItemDesc* idesc = reinterpret_cast<ItemDesc*>(st_empty + kS);              // [kS]
+  uint64_t* st_full = reinterpret_cast<uint64_t*>(smem + L::kSuffixBars);  // [2][kS]
+  uint64_t* st_empty = st_full + 2 * kS;                                    // [2][kS]
+  ItemDesc* idesc = reinterpret_cast<ItemDesc*>(st_empty + 2 * kS);          // [kS]
   volatile int* abort_flag = reinterpret_cast<volatile int*>(idesc + kS);
   uint64_t* merge_bar = reinterpret_cast<uint64_t*>(smem + L::kSuffixBars + kMergeBarOff);
   float* xch = reinterpret_cast<float*>(smem + L::kSuffixBars + L::kXchOff);
   int u_begin, u_end;
   unit_range(a, u_begin, u_end);
   if (threadIdx.x == 0) {
-    for (int i = 0; i < kS; ++i) {
+    for (int i = 0; i < 2 * kS; ++i) {  // per (group, slot)
       mbar_init(&st_full[i], 1 + 32);  // the producer's expect_tx + its lanes' copies
       mbar_init(&st_empty[i], kStreamWarps / a.unit_groups);  // the warps of one unit
     }
@@ -698,7 +719,10 @@ __device__ __forceinline__ void decode_body(const CUtensorMap& tm_q, const CUten
   __syncthreads();
   if (u_begin < u_end) {  // (a prefix CTA may have none)
     if (warp == kWarpScheduler) {
-      produce_items<D>(a, &tm_k, &tm_v, smem, st_full, st_empty, idesc, abort_flag);
+      if (a.unit_groups == 2)
+        produce_items<D, 2>(a, &tm_k, &tm_v, smem, st_full, st_empty, idesc, abort_flag);
+      else
+        produce_items<D, 1>(a, &tm_k, &tm_v, smem, st_full, st_empty, idesc, abort_flag);
     } else if (warp < kStreamWarps) {
       if (a.unit_groups == 2)
         consume_items<D, 2>(a, smem, st_full, st_empty, idesc, xch, abort_flag);
